@@ -1,0 +1,167 @@
+"""Pins of the oracle's Philox4x32-10 and stochastic rounding.
+
+Philox: the all-zero known answer of the published generator (6627e8d5 e169c58d bc57ac4c
+9b00dbd8) and agreement with an independent implementation, Triton's `tl.philox`, executed by
+Triton's CPU interpreter in a child process (a library routine; it is never used by the product).
+
+Stochastic rounding ("4-bit computation from the start of Inkling 2 Small's pretraining",
+lhc.media, backward-pass paragraphs: chooses the higher or lower representable value by distance
+so that the value is preserved on average):
+  - the result is always one of the two neighbours;
+  - exactly representable values never move;
+  - at a quarter of the way up, the up-fraction over 2^22 words is 1/4 within 5 sigma, and the
+    nearest-even cast fails that same test (control);
+  - the mean of many SR draws of random values reproduces the values (unbiasedness).
+"""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+KAT_ZERO = [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+
+
+def test_philox_known_answer_zero(orc):
+    out = orc.philox4x32_10([0, 0, 0, 0], [0, 0])
+    assert [int(x) for x in out] == KAT_ZERO
+
+
+_TRITON_CHILD = r"""
+import os, sys, json
+os.environ["TRITON_INTERPRET"] = "1"
+import numpy as np, torch, triton, triton.language as tl
+
+@triton.jit
+def kern(out_ptr, c0_ptr, c1_ptr, c2_ptr, c3_ptr, seed, N: tl.constexpr):
+    o = tl.arange(0, N)
+    c0 = tl.load(c0_ptr + o); c1 = tl.load(c1_ptr + o); c2 = tl.load(c2_ptr + o); c3 = tl.load(c3_ptr + o)
+    a, b, c, d = tl.philox(seed, c0, c1, c2, c3)
+    tl.store(out_ptr + o * 4 + 0, a.to(tl.int32, bitcast=True))
+    tl.store(out_ptr + o * 4 + 1, b.to(tl.int32, bitcast=True))
+    tl.store(out_ptr + o * 4 + 2, c.to(tl.int32, bitcast=True))
+    tl.store(out_ptr + o * 4 + 3, d.to(tl.int32, bitcast=True))
+
+cases = json.loads(sys.stdin.read())
+res = []
+for seed, ctrs in cases:
+    ctrs = np.array(ctrs, dtype=np.uint32)
+    N = len(ctrs)
+    cols = [torch.from_numpy(ctrs[:, i].view(np.int32).copy()) for i in range(4)]
+    out = torch.zeros(N * 4, dtype=torch.int32)
+    kern[(1,)](out, *cols, seed, N=N)
+    res.append(out.numpy().view(np.uint32).reshape(N, 4).tolist())
+print(json.dumps(res))
+"""
+
+
+def test_philox_against_triton_interpreter(orc):
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(11)
+    cases = []
+    for seed in [0, 1, 0xDEADBEEF, (1 << 63) + 12345, 0xFFFFFFFFFFFFFFFF]:
+        ctrs = rng.integers(0, 1 << 32, size=(16, 4), dtype=np.uint64).astype(np.uint32)
+        ctrs[0] = 0
+        ctrs[1] = 0xFFFFFFFF
+        cases.append([int(seed), ctrs.tolist()])
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    p = subprocess.run([sys.executable, "-c", _TRITON_CHILD], input=json.dumps(cases),
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    res = json.loads(p.stdout.strip().splitlines()[-1])
+    for (seed, ctrs), got in zip(cases, res):
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        for ctr, words in zip(ctrs, got):
+            assert [int(x) for x in orc.philox4x32_10(ctr, key)] == words
+
+
+def test_sr_word_keying(orc):
+    seed, sid = 0x0123456789ABCDEF, 7
+    idx = np.array([0, 1, 2, 3, 4, 5, (1 << 32) * 4 + 6, (1 << 40) + 3], np.uint64)
+    for i in idx:
+        i = int(i)
+        j = i >> 2
+        words = orc.philox4x32_10([j & 0xFFFFFFFF, j >> 32, sid, 0],
+                                  [seed & 0xFFFFFFFF, seed >> 32])
+        assert orc.sr_words(seed, sid, i, 1)[0] == words[i & 3]
+
+
+def _e4m3_neighbours(orc, v):
+    codes = np.arange(0x7F, dtype=np.uint8)
+    grid = orc.e4m3_value(codes).astype(np.float64)
+    a = np.abs(v.astype(np.float64))
+    lo_idx = np.searchsorted(grid, a, side="right") - 1
+    lo_idx = np.minimum(lo_idx, 126)
+    hi_idx = np.minimum(lo_idx + 1, 126)
+    return lo_idx, hi_idx, grid
+
+
+def test_sr_lands_on_a_neighbour(orc):
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(200000) * np.exp2(rng.integers(-12, 9, 200000))).astype(np.float32)
+    v = np.clip(v, -448, 448).astype(np.float32)
+    r = rng.integers(0, 1 << 32, size=v.size, dtype=np.uint64).astype(np.uint32)
+    got = orc.e4m3_sr(v, r)
+    lo, hi, _ = _e4m3_neighbours(orc, v)
+    mag = got & 0x7F
+    assert np.all((mag == lo) | (mag == hi))
+    assert np.array_equal(got >> 7, np.signbit(v).astype(np.uint8))
+
+
+def test_sr_exact_values_never_move(orc):
+    vals = orc.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    v = np.concatenate([vals, -vals]).astype(np.float32)
+    for r in [0, 1, 0x7FFFFFFF, 0xFFFFFFFF]:
+        got = orc.e4m3_sr(v, np.full(v.size, r, np.uint32))
+        assert np.array_equal(got, orc.e4m3_rne_sat(v))
+
+
+@pytest.mark.parametrize("lo_code", [0x01, 0x12, 0x38, 0x5B, 0x7C])
+def test_sr_quarter_way_up_fraction(orc, lo_code):
+    lo = float(orc.e4m3_value([lo_code])[0])
+    hi = float(orc.e4m3_value([lo_code + 1])[0])
+    v = np.float32(lo + 0.25 * (hi - lo))
+    assert float(v) == lo + 0.25 * (hi - lo)
+    n = 1 << 22
+    words = orc.sr_words(seed=12345, stream_id=0, idx_base=0, n=n)
+    got = orc.e4m3_sr(np.full(n, v, np.float32), words)
+    up = np.mean(got == lo_code + 1)
+    sigma = np.sqrt(0.25 * 0.75 / n)
+    assert abs(up - 0.25) < 5 * sigma
+    # control: nearest-even never rounds a quarter-way value up
+    rne = orc.e4m3_rne_sat(np.full(8, v, np.float32))
+    assert np.all(rne == lo_code)
+
+
+def test_sr_unbiased_on_random_values(orc):
+    rng = np.random.default_rng(5)
+    n_vals, draws = 512, 4096
+    v = (rng.random(n_vals) * 400 + 0.01).astype(np.float32)
+    acc = np.zeros(n_vals, np.float64)
+    sq = np.zeros(n_vals, np.float64)
+    for d in range(draws):
+        w = orc.sr_words(seed=d, stream_id=3, idx_base=0, n=n_vals)
+        q = orc.e4m3_value(orc.e4m3_sr(v, w)).astype(np.float64)
+        acc += q
+        sq += q * q
+    mean = acc / draws
+    lo, hi, grid = _e4m3_neighbours(orc, v)
+    ulp = grid[hi] - grid[lo]
+    p = (v - grid[lo]) / np.where(ulp > 0, ulp, 1)
+    sd = ulp * np.sqrt(np.maximum(p * (1 - p), 1e-12) / draws)
+    z = (mean - v) / np.maximum(sd, 1e-30)
+    z = z[ulp > 0]
+    assert np.abs(z.mean()) * np.sqrt(z.size) < 5
+    assert np.max(np.abs(z)) < 6
+
+
+def test_philox_words_uniform(orc):
+    w = orc.sr_words(seed=99, stream_id=1, idx_base=0, n=1 << 20)
+    hist = np.bincount(w >> 24, minlength=256).astype(np.float64)
+    expected = w.size / 256
+    chi2 = ((hist - expected) ** 2 / expected).sum()
+    # 255 degrees of freedom: mean 255, sd 22.6; 6 sd bound
+    assert chi2 < 255 + 6 * 22.6
