@@ -1,0 +1,237 @@
+/*
+ * moe4.h -- C ABI of libmoe4.so: the 4-bit MoE expert-layer numerics on B300 (sm_103a).
+ *
+ * The method (described in prose on the pages cited below) quantises the forward operands of the
+ * expert layers to NVFP4, picking each block's scale by Four Over Six, multiplies them in a
+ * block-scaled grouped expert GEMM, requantises the transposed forward operands to MXFP8 with
+ * stochastic rounding for the backward GEMMs, and encodes expert outputs for the return path
+ * with a Hadamard transform before quantisation.
+ *
+ * Pages:
+ *   [DEBUT] "Inkling 2 Small's Native 4-Bit Training: Debut and Doubts" (agihunt.info),
+ *           "Confirmed": NVFP4 forward of the expert layers with dedicated kernels, MXFP8
+ *           backward with requantisation and stochastic rounding, Four Over Six, per-expert
+ *           scales.
+ *   [LHC]   "4-bit computation from the start of Inkling 2 Small's pretraining" (lhc.media):
+ *           fewer-bits paragraph (4-bit values, one scale per sixteen, 4.5 bits/value);
+ *           backward-pass paragraphs (dequantise, transpose at higher precision, requantise to
+ *           MXFP8 with stochastic rounding); communication paragraph (NVFP4 dispatch, Hadamard
+ *           transform before the return path is quantised); the paragraph on in-house kernels
+ *           that fuse the transform and quantisation into the matrix multiplication.
+ *   [4WEEK] "Thinking Machines: Nvidia FP4 Up to 6x Faster, Runs Gain 8%" (fourweekmba.com):
+ *           model-card update (48 layers, 8 of 384 experts per token), "What Thinking Machines
+ *           Changed" (NVFP4 expert forward with a dedicated kernel, MXFP8 backward).
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless a comment says
+ *     "host".  The library never allocates device memory and never frees what it is given.
+ *     Calls that need scratch take (ws, ws_bytes); moe4_workspace_size() gives the size.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
+ *     only enqueues work on it and returns; nothing is synchronised unless a comment says so.
+ *   - bf16 values are passed as their uint16_t bit patterns; E2M1, E4M3 and E8M0 values as raw
+ *     bytes.  Matrices are row-major with their contraction / blocking dimension contiguous.
+ *   - NVFP4 tensor [R, C]: codes uint8 [R, C/2] (element 2j in the low nibble, 2j+1 in the high
+ *     nibble), sf uint8 E4M3 [R, C/16] ("canonical" layout), and one float per-tensor decode
+ *     scale g_dec (per matrix; per expert for weights).
+ *   - MXFP8 tensor [R, C]: q uint8 E4M3 [R, C], e8 uint8 E8M0 [R, C/32] (canonical layout).
+ *   - Return value: MOE4_OK, or a negative status; on error nothing has been enqueued.
+ *     Argument checks cover null pointers, sizes, divisibility and 16-byte alignment of every
+ *     vector-accessed buffer.  NaN and infinite inputs are not checked and give unspecified
+ *     codes.
+ */
+#ifndef MOE4_H
+#define MOE4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+#define MOE4_OK               0
+#define MOE4_ERR_ARG        (-1) /* null pointer, bad size, misaligned buffer, bad flag */
+#define MOE4_ERR_UNSUPPORTED (-2) /* a valid request this build does not implement */
+#define MOE4_ERR_CUDA       (-3) /* a CUDA call or kernel launch failed */
+#define MOE4_ERR_TIMEOUT    (-4) /* a device-side wait gave up (reported by moe4_get_status) */
+#define MOE4_ERR_WORKSPACE  (-5) /* ws is NULL or smaller than moe4_workspace_size() */
+
+/* ------------------------------------------------------------------ flags */
+#define MOE4_FOUR_OVER_SIX  0x00001u /* NVFP4: per block choose scale amax->6 or amax->4 */
+#define MOE4_AMAX_GIVEN     0x00002u /* NVFP4: use amax_in instead of computing the amax */
+#define MOE4_SR             0x00004u /* MXFP8: stochastic rounding (else nearest-even) */
+#define MOE4_ROWWISE        0x00010u /* MXFP8 quantise: blocks along the rows' contiguous dim */
+#define MOE4_COLWISE        0x00020u /* MXFP8 quantise: the transpose, blocks along rows */
+#define MOE4_OUT_F32        0x00100u /* output binary32 */
+#define MOE4_OUT_BF16       0x00200u /* output bf16 */
+#define MOE4_GROUP_M        0x01000u /* grouped GEMM: groups are row ranges of A and D */
+#define MOE4_GROUP_K        0x02000u /* grouped GEMM: groups are ranges of the contraction */
+#define MOE4_ACCUMULATE     0x04000u /* grouped GEMM: D += result (binary32 output only) */
+#define MOE4_SF_MMA_LAYOUT  0x10000u /* scale factors are in the tensor-core tile layout */
+
+/* ------------------------------------------------------------------ library */
+int moe4_version(void);                      /* e.g. 100 for 0.1.0 */
+const char *moe4_status_string(int status);  /* static string, never NULL */
+
+/* Operation ids for moe4_workspace_size(). */
+#define MOE4_OP_NVFP4_QUANTIZE   1 /* a = nmat */
+#define MOE4_OP_HADAMARD_QUANT   2 /* no arguments */
+#define MOE4_OP_PERMUTE_PLAN     3 /* a = tokens, b = top_k, c = experts */
+#define MOE4_OP_GEMM_NVFP4       4 /* a = rows of A, b = N (rows of B per group), c = K, with E via moe4_workspace_size_gemm */
+size_t moe4_workspace_size(int op, int64_t a, int64_t b, int64_t c);
+/* Scratch for the grouped GEMMs when their scale factors come in the canonical layout:
+ * kind 0 = NVFP4 (16-blocks), 1 = MXFP8 (32-blocks); a_rows x K for A, E x b_rows x K for B. */
+size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, int64_t b_rows, int64_t K);
+
+/* Synchronise `stream`, then read and clear the device status word that kernels set when a
+ * bounded wait gives up.  Returns MOE4_OK or MOE4_ERR_TIMEOUT (or MOE4_ERR_CUDA). */
+int moe4_get_status(void *stream);
+
+/* ------------------------------------------------------------------ NVFP4 [LHC fewer bits; DEBUT]
+ * nvfp4_quantize: x bf16 [nmat, rows, ld] (the first `cols` of each row are used; ld >= cols,
+ * ld % 8 == 0).  For each matrix m: amax_m = max|x| (or amax_in[m] with MOE4_AMAX_GIVEN);
+ * g_enc = 2688/amax_m (1 if amax is 0, FLT_MAX on overflow), g_dec[m] = 1/g_enc; y = x * g_enc;
+ * per 16-block along cols, candidate scales E4M3(blockamax/6) and, with MOE4_FOUR_OVER_SIX,
+ * E4M3(blockamax/4); codes E2M1(y * (1/scale)) (nearest-even, saturating); the 4-candidate is
+ * kept iff its pairwise-tree sum of squared errors in the y domain is strictly smaller.
+ * Outputs: codes [nmat, rows, cols/2], sf [nmat, rows, cols/16] (canonical, or the tensor-core
+ * tile layout of moe4_sf_to_mma_layout with MOE4_SF_MMA_LAYOUT, which needs rows % 128 == 0 and
+ * cols % 64 == 0), g_dec [nmat].  cols % 16 == 0.
+ * ws: moe4_workspace_size(MOE4_OP_NVFP4_QUANTIZE, nmat) bytes unless MOE4_AMAX_GIVEN.
+ * Bit-exact with the oracle: every binary32 step is one correctly rounded operation. */
+int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                   uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
+                   uint32_t flags, void *ws, size_t ws_bytes, void *stream);
+
+/* nvfp4_dequantize: x_hat = (e2m1(q) * e4m3(sf)) * g_dec[m]; out [nmat, rows, cols] as bf16
+ * (MOE4_OUT_BF16, nearest-even) or binary32 (MOE4_OUT_F32).  Canonical sf only. */
+int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t nmat,
+                     int64_t rows, int64_t cols, void *out, uint32_t flags, void *stream);
+
+/* ------------------------------------------------------------------ MXFP8 [LHC backward pass]
+ * mxfp8_requant_transpose_sr: for each matrix m of NVFP4 [rows, cols]: dequantise to binary32,
+ * transpose, and quantise each 32-block along the new contiguous dimension (rows) to MXFP8:
+ * scale exponent e = smallest integer with blockamax <= 448 * 2^e, clamped to [-127, 127], stored
+ * as e + 127; elements v = x_hat * 2^-e rounded to E4M3 stochastically (MOE4_SR) or to
+ * nearest-even.  Stochastic rounding of the element with linear index idx in the output
+ * [nmat, cols, rows] uses word idx % 4 of Philox4x32-10(counter = (lo(idx/4), hi(idx/4),
+ * stream_id, 0), key = (lo(seed), hi(seed))) and rounds the magnitude up iff
+ * word < floor(frac * 2^32), frac being its distance above the E4M3 value below, in units of
+ * the gap.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
+ * rows % 32 == 0, cols % 32 == 0.  Canonical input sf only. */
+int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const float *g_dec,
+                               int64_t nmat, int64_t rows, int64_t cols, uint8_t *q_t,
+                               uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,
+                               void *stream);
+
+/* mxfp8_quantize: bf16 x [rows, cols] to MXFP8 with the same scale and rounding rules.
+ * MOE4_ROWWISE: q [rows, cols], e8 [rows, cols/32] (cols % 32 == 0); random index = the
+ * element's index in q.  MOE4_COLWISE: q [cols, rows], e8 [cols, rows/32] (rows % 32 == 0,
+ * cols % 32 == 0); random index = the element's index in that transposed output.  Exactly one
+ * of the two flags.  Nearest-even unless MOE4_SR. */
+int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, uint8_t *e8,
+                   uint64_t seed, uint32_t stream_id, uint32_t flags, void *stream);
+
+/* ------------------------------------------------------------------ Hadamard codec [LHC comms]
+ * hadamard_quant: x bf16 [rows, cols], cols % 128 == 0.  Each contiguous 128-chunk of a row is
+ * rotated by the Sylvester-ordered Hadamard matrix (butterflies of span 1, 2, ..., 64, then
+ * times RN(1/sqrt(128))) in binary32, and the rotated tensor is NVFP4-quantised as above (its
+ * own amax; Four Over Six per flags).  ws: moe4_workspace_size(MOE4_OP_HADAMARD_QUANT).
+ * hadamard_dequant: NVFP4 dequantise, the same rotation (it is its own inverse), bf16 out. */
+int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *sf,
+                   float *g_dec, uint32_t flags, void *ws, size_t ws_bytes, void *stream);
+int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t rows,
+                     int64_t cols, uint16_t *out_bf16, uint32_t flags, void *stream);
+
+/* ------------------------------------------------------------------ grouped GEMMs
+ * grouped_expert_gemm_nvfp4 [DEBUT; 4WEEK: NVFP4 expert forward with a dedicated kernel]:
+ * A: NVFP4 [rows_total, K] (a_codes, a_sf, a_g_dec[1]); B: E expert matrices NVFP4 [N, K]
+ * (b_codes [E, N, K/2], b_sf, b_g_dec[E]).  group_offs: device int32 [E+1], non-decreasing,
+ * offs[0] = 0, offs[E] = rows_total, every entry a multiple of 128.  For each expert e and row
+ * i in [offs[e], offs[e+1]):  D[i, n] = a_g_dec * b_g_dec[e] * sum_k deq(A)[i,k] * deq(B_e)[n,k]
+ * accumulated in binary32 by the tensor cores.  D [rows_total, N]: binary32 (MOE4_OUT_F32) or
+ * bf16 (MOE4_OUT_BF16).  N % 256 == 0, K % 256 == 0.  Scale factors are canonical unless
+ * MOE4_SF_MMA_LAYOUT; canonical ones are converted into ws
+ * (moe4_workspace_size_gemm(0, rows_total, E, N, K) bytes). */
+int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                              const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                              const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t N,
+                              int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* grouped_gemm_mxfp8 [DEBUT, 4WEEK: MXFP8 backward]: D = A * B^T per group, both operands MXFP8
+ * with their contraction dimension contiguous.
+ * MOE4_GROUP_M (dgrad): A [M, K] (q, e8), B [E, N, K]; rows offs[e]..offs[e+1] of A and D use
+ *   B[e]; D [M, N]; offs[E] = M.
+ * MOE4_GROUP_K (wgrad): A [M, Ktot], B [N, Ktot]; D [E, M, N] with
+ *   D[e] = A[:, offs[e]:offs[e+1]] * B[:, offs[e]:offs[e+1]]^T; offs[E] = Ktot = K; an empty
+ *   group writes zeros (or leaves D[e] untouched with MOE4_ACCUMULATE).
+ * offs entries are multiples of 128; M % 128 == 0, N % 256 == 0, K % 128 == 0.  Output
+ * binary32 or bf16; MOE4_ACCUMULATE adds into a binary32 D.  Canonical scale factors are
+ * converted into ws (moe4_workspace_size_gemm(1, ...)). */
+int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
+                       const uint8_t *b_e8, const int32_t *group_offs, int64_t E, int64_t M,
+                       int64_t N, int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/* moe4_sf_to_mma_layout: rearrange canonical scale factors sf [nmat, rows, nblk] into the
+ * tensor-core tile layout: for each 128-row tile and each group of 4 consecutive blocks, 512
+ * bytes where row r = 32*j + i of the tile puts its 4 bytes at offset 16*i + 4*j.  rows % 128
+ * == 0, nblk % 4 == 0.  A pure permutation (bit-exact). */
+int moe4_sf_to_mma_layout(const uint8_t *sf, int64_t nmat, int64_t rows, int64_t nblk,
+                          uint8_t *out, void *stream);
+
+/* ------------------------------------------------------------------ routing and dispatch
+ * [4WEEK model card: 8 of 384 experts per token; LHC: inputs dispatched in NVFP4]
+ * moe4_route_topk: logits f32 [T, E] -> idx int32 [T, k] (descending logit, ties to the lower
+ * expert index) and w f32 [T, k] = softmax over the k chosen logits.  1 <= k <= 32, E <= 4096. */
+int moe4_route_topk(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *idx, float *w,
+                    void *stream);
+
+/* moe4_permute_plan: from idx [T, k] build offs int32 [E+1] (each expert's rows, stable in
+ * (token, slot), zero-padded to a multiple of 128), row_of int32 [T, k] (dispatched row of each
+ * (token, slot)) and src_of int32 [rows_cap] (source token of each dispatched row, -1 for
+ * padding).  rows_cap >= T*k + 127*E.  ws: moe4_workspace_size(MOE4_OP_PERMUTE_PLAN, T, k, E). */
+int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64_t E, int32_t *offs,
+                      int32_t *row_of, int32_t *src_of, int64_t rows_cap, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* moe4_permute_nvfp4: gather NVFP4 rows: out row r = input row src_of[r], or zeros (codes 0,
+ * scale 0) when src_of[r] < 0; r < rows_total.  codes [T, cols/2], sf [T, cols/16] canonical;
+ * cols % 32 == 0. */
+int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64_t T, int64_t cols,
+                       const int32_t *src_of, int64_t rows_total, uint8_t *out_codes,
+                       uint8_t *out_sf, void *stream);
+
+/* moe4_swiglu: gu f32 [rows, 2f] -> h bf16 [rows, f], h = g/(1+exp(-g)) * u with g the first f
+ * columns and u the last f (binary32, then nearest-even to bf16).  f % 4 == 0. */
+int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h, void *stream);
+
+/* moe4_combine: y bf16 [T, d], y[t] = sum over slots j in order of w[t,j] * yhat[row_of[t,j]]:
+ * one binary32 product and one binary32 add per slot from 0, then nearest-even to bf16.
+ * yhat bf16 [rows, d]; d % 8 == 0. */
+int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const float *w, int64_t T,
+                 int64_t k, int64_t d, uint16_t *y, void *stream);
+
+/* moe4_sgd_update: FP32 master weights [LHC: master weights in FP32] w32 <- w32 - lr * dw (one
+ * product, one difference) and w_bf16 <- bf16(w32) (nearest-even); n % 4 == 0. */
+int moe4_sgd_update(float *w32, const float *dw, int64_t n, float lr, uint16_t *w_bf16,
+                    void *stream);
+
+/* ------------------------------------------------------------------ conversions (for checks)
+ * moe4_convert: the device's own conversions of binary32 in[n]: kind 0 = E2M1 code (one byte
+ * per value, nearest-even, saturating, sign kept), 1 = E4M3 code (nearest-even, saturating),
+ * 2 = bf16 bits (two bytes per value), 3 = E4M3 code by stochastic rounding with word
+ * moe4_sr_word(seed=0, stream_id=0, idx=i) of value i.  n % 4 == 0. */
+int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream);
+
+/* moe4_sr_words: the stochastic-rounding words of indices idx_base .. idx_base+n-1 (n % 4 == 0,
+ * idx_base % 4 == 0), uint32 out[n]. */
+int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint32_t *out,
+                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE4_H */

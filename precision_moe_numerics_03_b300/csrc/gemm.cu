@@ -1,0 +1,631 @@
+// gemm.cu -- block-scaled grouped expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// Method: the forward pass of the expert layers runs in NVFP4 with a dedicated kernel, the
+// backward pass in MXFP8 ("Inkling 2 Small's Native 4-Bit Training: Debut and Doubts",
+// agihunt.info, "Confirmed"; "Thinking Machines: Nvidia FP4 Up to 6x Faster, Runs Gain 8%",
+// fourweekmba.com, "What Thinking Machines Changed").
+//
+// One persistent CTA per SM, 8 warps:
+//   warp 0 (one lane)  TMA producer: A tile 128 rows x 128 bytes, B tile 256 rows x 128 bytes
+//                      (128-byte swizzle), and the two tiles' scale factors (1-D bulk copies of
+//                      the tensor-core scale layout), into a 4-stage shared-memory ring;
+//   warp 1 (one lane)  MMA issuer: per stage, tcgen05.cp of the scale factors into tensor memory,
+//                      then four tcgen05.mma (kind::mxf4nvf4 with 4 UE4M3 scales per 64 values, or
+//                      kind::mxf8f6f4 E4M3 with one UE8M0 scale per 32), accumulating a 128x256
+//                      binary32 tile in tensor memory; tcgen05.commit frees the stage;
+//   warp 2             allocates / frees the 512 tensor-memory columns;
+//   warps 4..7         epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..),
+//                      times the per-tensor scales, to binary32 or bf16 in global memory.
+// Every mbarrier wait is bounded (about two seconds of SM clock); a wait that gives up sets the
+// library status word, stops the CTA's loops, drains its own copies and MMAs, and frees tensor
+// memory before the CTA exits.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace moe4 {
+
+__device__ unsigned int g_status = 0;
+
+namespace gemm {
+
+constexpr int BM = 128;         // rows of A per tile (MMA M)
+constexpr int BN = 256;         // rows of B per tile (MMA N)
+constexpr int BKB = 128;        // bytes of contraction per stage (one 128-byte swizzle row)
+constexpr int STAGES = 4;
+constexpr int THREADS = 256;
+constexpr int A_TILE = BM * BKB;
+constexpr int B_TILE = BN * BKB;
+constexpr int TMEM_COLS = 512;
+constexpr int ACC_COLS = BN;    // binary32 accumulator: one column per output column
+constexpr long long kWaitCycles = 1ll << 32;
+
+template <int KIND>
+struct Cfg;
+template <>
+struct Cfg<0> {                       // NVFP4
+    static constexpr int ELEMS = 256;  // contraction elements per stage
+    static constexpr int ATOMS = 4;    // 512-byte scale atoms per 128-row tile per stage
+    static constexpr int ELEMS_PER_ATOM = 64;
+};
+template <>
+struct Cfg<1> {                       // MXFP8
+    static constexpr int ELEMS = 128;
+    static constexpr int ATOMS = 1;
+    static constexpr int ELEMS_PER_ATOM = 128;
+};
+
+template <int KIND>
+struct Layout {
+    static constexpr int SFA = Cfg<KIND>::ATOMS * 512;
+    static constexpr int SFB = 2 * Cfg<KIND>::ATOMS * 512;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_TILE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_TILE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB;
+    static constexpr int NBAR = 2 * STAGES + 3;  // full, empty, tmem_full, tmem_empty, drain
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
+    static constexpr int TX = A_TILE + B_TILE + SFA + SFB;
+    // tensor-memory columns: accumulator [0, 256), then per stage SFA and SFB
+    static constexpr int SF_COLS_A = Cfg<KIND>::ATOMS * 4;
+    static constexpr int SF_COLS_B = Cfg<KIND>::ATOMS * 8;
+    static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
+    static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+};
+
+struct Args {
+    const uint8_t *sfa;     // tensor-core scale layout of A
+    const uint8_t *sfb;     // tensor-core scale layout of B
+    const float *a_g_dec;   // NVFP4 only
+    const float *b_g_dec;   // NVFP4 only, [E]
+    const int32_t *offs;    // [E+1]
+    int E;
+    int group_k;            // 0: groups are row ranges of A/D; 1: ranges of the contraction
+    int64_t M, N, K;        // D is [M, N] per group (group_k: [E, M, N]); K = contraction length
+    void *d;
+    int out_bf16;
+    int accumulate;
+    int64_t num_tiles;
+    int n_tiles_n, n_tiles_m;
+    int64_t sfa_tile_stride;  // atoms between consecutive 128-row tiles of A's scale layout
+    int64_t sfb_tile_stride;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: false when the CTA is aborting or the wait ran out (which starts the abort).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicOr(&g_status, 1u);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+template <int KIND>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+    if constexpr (KIND == 0) {
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.u32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}" ::"r"(d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.u32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}" ::"r"(d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    }
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets (16-byte units),
+// the fixed version bit 46, and the swizzle mode in bits 61..63 (2 = 128-byte, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+
+// Instruction descriptor of the block-scaled kinds: B scale id [4,6), A format [7,10), B format
+// [10,13), K-major A and B (bits 15, 16 clear), N>>3 [17,23), scale type bit 23 (0 UE4M3,
+// 1 UE8M0), M>>4 [24,29), A scale id [29,31).
+template <int KIND>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+    const uint32_t fmt = KIND == 0 ? 1u : 0u;       // E2M1 for mxf4nvf4, E4M3 for mxf8f6f4
+    const uint32_t scale_type = KIND == 0 ? 0u : 1u;
+    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (scale_type << 23) |
+           ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+struct Tile {
+    int64_t m0, n0;     // first row of A / D, first row of B (N index)
+    int64_t b_row;      // first row of B in the B tensor (expert offset folded in)
+    int64_t k_begin;    // contraction start (elements)
+    int n_stages;
+    int e;
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
+    Tile tl;
+    if (!p.group_k) {
+        const int64_t mt = t / p.n_tiles_n, nt = t - mt * p.n_tiles_n;
+        tl.m0 = mt * BM;
+        tl.n0 = nt * BN;
+        int lo = 0, hi = p.E;  // largest e with offs[e] <= m0
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.offs + mid) <= tl.m0) lo = mid; else hi = mid;
+        }
+        tl.e = lo;
+        tl.b_row = (int64_t)lo * p.N + tl.n0;
+        tl.k_begin = 0;
+        tl.n_stages = (int)(p.K / Cfg<KIND>::ELEMS);
+    } else {
+        const int64_t per_e = (int64_t)p.n_tiles_m * p.n_tiles_n;
+        const int64_t e = t / per_e, rem = t - e * per_e;
+        const int64_t mt = rem / p.n_tiles_n, nt = rem - mt * p.n_tiles_n;
+        tl.e = (int)e;
+        tl.m0 = mt * BM;
+        tl.n0 = nt * BN;
+        tl.b_row = tl.n0;
+        const int32_t k0 = __ldg(p.offs + e), k1 = __ldg(p.offs + e + 1);
+        tl.k_begin = k0;
+        tl.n_stages = (k1 - k0) / Cfg<KIND>::ELEMS;
+    }
+    return tl;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
+    using L = Layout<KIND>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *full = bars, *empty = bars + STAGES;
+    uint64_t *tmem_full = bars + 2 * STAGES, *tmem_empty = tmem_full + 1, *drain = tmem_full + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    const int warp = warp_id(), lane = lane_id();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_parity[STAGES];
+        bool issued[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_parity[s] = 0;
+        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND>(p, t);
+            for (int ks = 0; ks < tl.n_stages; ++ks) {
+                if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag)) break;
+                uint64_t *fb = full + stage;
+                mbar_expect_tx(fb, L::TX);
+                const int64_t kel = tl.k_begin + (int64_t)ks * Cfg<KIND>::ELEMS;   // contraction element
+                const int xbytes = (int)(KIND == 0 ? kel / 2 : kel);
+                tma_load_2d(smem + L::OFF_A + stage * A_TILE, &tmA, fb, xbytes, (int)tl.m0);
+                tma_load_2d(smem + L::OFF_B + stage * B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
+                const int64_t atom = kel / Cfg<KIND>::ELEMS_PER_ATOM;
+                const uint8_t *sa = p.sfa + ((tl.m0 / BM) * p.sfa_tile_stride + atom) * 512;
+                bulk_load(smem + L::OFF_SFA + stage * L::SFA, sa, L::SFA, fb);
+                for (int rt = 0; rt < 2; ++rt) {
+                    const uint8_t *sb = p.sfb + ((tl.b_row / BM + rt) * p.sfb_tile_stride + atom) * 512;
+                    bulk_load(smem + L::OFF_SFB + stage * L::SFB + rt * L::SFA, sb, L::SFA, fb);
+                }
+                issued[stage] = true;
+                issued_parity[stage] = phase;
+                if (++stage == STAGES) stage = 0, phase ^= 1u;
+            }
+        }
+        if (*abort_flag) {  // let this CTA's own copies land before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s]) {
+                    const uint32_t a = smem_u32(full + s);
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(a, issued_parity[s]) && clock64() - t0 < kWaitCycles) {
+                    }
+                }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        const uint32_t a_base = smem_u32(smem + L::OFF_A), b_base = smem_u32(smem + L::OFF_B);
+        const uint32_t sfa_base = smem_u32(smem + L::OFF_SFA), sfb_base = smem_u32(smem + L::OFF_SFB);
+        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND>(p, t);
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag)) break;
+            tc_fence_after();
+            if (tl.n_stages == 0) {
+                mbar_arrive(tmem_full);
+            } else {
+                for (int ks = 0; ks < tl.n_stages; ++ks) {
+                    if (!mbar_wait(full + stage, phase, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t sf_col = tmem + ACC_COLS + stage * L::SF_COLS;
+                    // scale factors: atom i of A -> columns sf_col + 4i; atom i of B row tile rt ->
+                    // sf_col + SF_COLS_A + 8i + 4rt
+#pragma unroll
+                    for (int i = 0; i < Cfg<KIND>::ATOMS; ++i) {
+                        tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_base + stage * L::SFA + i * 512, 0, 128, 0));
+#pragma unroll
+                        for (int rt = 0; rt < 2; ++rt)
+                            tc_cp_sf(sf_col + L::SF_COLS_A + 8 * i + 4 * rt,
+                                     smem_desc(sfb_base + stage * L::SFB + rt * L::SFA + i * 512, 0, 128, 0));
+                    }
+                    const uint32_t a_addr = a_base + stage * A_TILE, b_addr = b_base + stage * B_TILE;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024, 2);
+                        const uint64_t bd = smem_desc(b_addr + 32 * k, 16, 1024, 2);
+                        uint32_t sfa_t, sfb_t, idesc;
+                        if constexpr (KIND == 0) {
+                            sfa_t = sf_col + 4 * k;
+                            sfb_t = sf_col + L::SF_COLS_A + 8 * k;
+                            idesc = make_idesc<0>(0);
+                        } else {
+                            sfa_t = sf_col;
+                            sfb_t = sf_col + L::SF_COLS_A;
+                            idesc = make_idesc<1>((uint32_t)k);
+                        }
+                        tc_mma<KIND>(tmem, ad, bd, idesc, sfa_t, sfb_t, (ks > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty + stage);
+                    if (++stage == STAGES) stage = 0, phase ^= 1u;
+                }
+                tc_commit(tmem_full);
+            }
+            acc_phase ^= 1u;
+        }
+        // all of this thread's MMAs and copies complete before tensor memory is freed
+        tc_commit(drain);
+        const uint32_t a = smem_u32(drain);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(a, 0) && clock64() - t0 < kWaitCycles) {
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND>(p, t);
+            if (!mbar_wait(tmem_full, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            float alpha = 1.0f;
+            if constexpr (KIND == 0) alpha = __fmul_rn(__ldg(p.a_g_dec), __ldg(p.b_g_dec + tl.e));
+            const int64_t row = tl.m0 + q * 32 + lane;
+            const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                if (tl.n_stages > 0) {
+                    tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0;
+                }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
+                if (p.out_bf16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.d) + dbase + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            w[i] = (uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i]) |
+                                   ((uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i + 1]) << 16);
+                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else if (p.accumulate) {
+                    if (tl.n_stages == 0) continue;
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4 o = dst[j];
+                        o.x = __fadd_rn(o.x, v[4 * j]);
+                        o.y = __fadd_rn(o.y, v[4 * j + 1]);
+                        o.z = __fadd_rn(o.z, v[4 * j + 2]);
+                        o.w = __fadd_rn(o.w, v[4 * j + 3]);
+                        dst[j] = o;
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+            acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D byte tensor [rows, inner_bytes] with a box of box_rows x 128 bytes, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int64_t rows, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)BKB, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Args &a, cudaStream_t st) {
+    using L = Layout<KIND>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
+            cudaSuccess)
+            return MOE4_ERR_CUDA;
+        attr_set = true;
+    }
+    if (a.num_tiles == 0) return MOE4_OK;
+    const int64_t grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
+    grouped_gemm_kernel<KIND><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, a);
+    return launch_status();
+}
+
+}  // namespace gemm
+}  // namespace moe4
+
+using namespace moe4;
+using namespace moe4::gemm;
+
+extern "C" int moe4_get_status(void *stream) {
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE4_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return MOE4_ERR_CUDA;
+    return v ? MOE4_ERR_TIMEOUT : MOE4_OK;
+}
+
+// Canonical scales -> tensor-core layout into ws when the caller did not pass that layout.
+static int stage_scales(const uint8_t *a_sf, int64_t a_rows, const uint8_t *b_sf, int64_t b_rows, int64_t K, int blk,
+                        uint32_t flags, void *ws, size_t ws_bytes, const uint8_t **sfa, const uint8_t **sfb,
+                        cudaStream_t st) {
+    if (flags & MOE4_SF_MMA_LAYOUT) {
+        *sfa = a_sf;
+        *sfb = b_sf;
+        return MOE4_OK;
+    }
+    const size_t na = (size_t)(a_rows * (K / blk)), nb = (size_t)(b_rows * (K / blk));
+    const size_t need = (na + 255) / 256 * 256 + (nb + 255) / 256 * 256;
+    if (!ws || ws_bytes < need || !aligned16(ws)) return MOE4_ERR_WORKSPACE;
+    uint8_t *wa = static_cast<uint8_t *>(ws);
+    uint8_t *wb = wa + (na + 255) / 256 * 256;
+    int rc = moe4_sf_to_mma_layout(a_sf, 1, a_rows, K / blk, wa, st);
+    if (rc == MOE4_OK) rc = moe4_sf_to_mma_layout(b_sf, 1, b_rows, K / blk, wb, st);
+    *sfa = wa;
+    *sfb = wb;
+    return rc;
+}
+
+extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                                         const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                                         const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t N,
+                                         int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
+                                         void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && rows_total >= 0 && rows_total % BM == 0 && N > 0 && N % BN == 0 && K > 0 &&
+                   K % 256 == 0);
+    MOE4_CHECK_ARG(a_codes && a_sf && a_g_dec && b_codes && b_sf && b_g_dec && group_offs && d);
+    MOE4_CHECK_ARG(aligned16(a_codes) && aligned16(b_codes) && aligned16(a_sf) && aligned16(b_sf) && aligned16(d));
+    MOE4_CHECK_ARG((flags & ~(MOE4_OUT_F32 | MOE4_OUT_BF16 | MOE4_SF_MMA_LAYOUT)) == 0);
+    const bool bf16 = (flags & MOE4_OUT_BF16) != 0;
+    MOE4_CHECK_ARG(bf16 != ((flags & MOE4_OUT_F32) != 0));
+    MOE4_CHECK_ARG(rows_total < (int64_t(1) << 31) && E * N < (int64_t(1) << 31));
+    if (rows_total == 0) return MOE4_OK;
+    cudaStream_t st = as_stream(stream);
+    const uint8_t *sfa, *sfb;
+    int rc = stage_scales(a_sf, rows_total, b_sf, E * N, K, 16, flags, ws, ws_bytes, &sfa, &sfb, st);
+    if (rc != MOE4_OK) return rc;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, a_codes, K / 2, rows_total, BM) || !make_map(&tb, b_codes, K / 2, E * N, BN))
+        return MOE4_ERR_CUDA;
+    Args a{};
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.a_g_dec = a_g_dec;
+    a.b_g_dec = b_g_dec;
+    a.offs = group_offs;
+    a.E = (int)E;
+    a.group_k = 0;
+    a.M = rows_total;
+    a.N = N;
+    a.K = K;
+    a.d = d;
+    a.out_bf16 = bf16;
+    a.accumulate = 0;
+    a.n_tiles_n = (int)(N / BN);
+    a.n_tiles_m = (int)(rows_total / BM);
+    a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
+    a.sfa_tile_stride = K / 64;
+    a.sfb_tile_stride = K / 64;
+    return launch<0>(ta, tb, a, st);
+}
+
+extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b, const uint8_t *b_e8,
+                                  const int32_t *group_offs, int64_t E, int64_t M, int64_t N, int64_t K, void *d,
+                                  uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && M >= 0 && M % BM == 0 && N > 0 && N % BN == 0 && K >= 0 && K % 128 == 0);
+    MOE4_CHECK_ARG(a && a_e8 && b && b_e8 && group_offs && d);
+    MOE4_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(a_e8) && aligned16(b_e8) && aligned16(d));
+    MOE4_CHECK_ARG((flags & ~(MOE4_OUT_F32 | MOE4_OUT_BF16 | MOE4_SF_MMA_LAYOUT | MOE4_GROUP_M | MOE4_GROUP_K |
+                              MOE4_ACCUMULATE)) == 0);
+    const bool bf16 = (flags & MOE4_OUT_BF16) != 0;
+    MOE4_CHECK_ARG(bf16 != ((flags & MOE4_OUT_F32) != 0));
+    const bool gk = (flags & MOE4_GROUP_K) != 0;
+    MOE4_CHECK_ARG(gk != ((flags & MOE4_GROUP_M) != 0));
+    MOE4_CHECK_ARG(!((flags & MOE4_ACCUMULATE) && bf16));
+    MOE4_CHECK_ARG(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    cudaStream_t st = as_stream(stream);
+    Args g{};
+    const uint8_t *sfa, *sfb;
+    CUtensorMap ta, tb;
+    if (!gk) {
+        if (M == 0 || K == 0) return MOE4_OK;
+        int rc = stage_scales(a_e8, M, b_e8, E * N, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
+        if (rc != MOE4_OK) return rc;
+        if (!make_map(&ta, a, K, M, BM) || !make_map(&tb, b, K, E * N, BN)) return MOE4_ERR_CUDA;
+        g.n_tiles_m = (int)(M / BM);
+        g.n_tiles_n = (int)(N / BN);
+        g.num_tiles = (int64_t)g.n_tiles_m * g.n_tiles_n;
+    } else {
+        if (M == 0) return MOE4_OK;
+        if (K == 0) {  // every group empty
+            if (flags & MOE4_ACCUMULATE) return MOE4_OK;
+            return cudaMemsetAsync(d, 0, (size_t)(E * M * N) * (bf16 ? 2 : 4), st) == cudaSuccess ? MOE4_OK
+                                                                                              : MOE4_ERR_CUDA;
+        }
+        int rc = stage_scales(a_e8, M, b_e8, N, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
+        if (rc != MOE4_OK) return rc;
+        if (!make_map(&ta, a, K, M, BM) || !make_map(&tb, b, K, N, BN)) return MOE4_ERR_CUDA;
+        g.n_tiles_m = (int)(M / BM);
+        g.n_tiles_n = (int)(N / BN);
+        g.num_tiles = E * g.n_tiles_m * g.n_tiles_n;
+    }
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.offs = group_offs;
+    g.E = (int)E;
+    g.group_k = gk;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.d = d;
+    g.out_bf16 = bf16;
+    g.accumulate = (flags & MOE4_ACCUMULATE) != 0;
+    g.sfa_tile_stride = K / 128;
+    g.sfb_tile_stride = K / 128;
+    return launch<1>(ta, tb, g, st);
+}

@@ -1,0 +1,473 @@
+// quant.cu -- NVFP4 quantisation with Four Over Six, NVFP4 dequantisation, and the Hadamard(128)
+// return-path codec.
+//
+// Method: "4-bit computation from the start of Inkling 2 Small's pretraining" (lhc.media):
+// 4-bit values with a scale shared by sixteen values (fewer-bits paragraph); a Hadamard
+// transform spreads out extreme values before the return path is quantised (communication
+// paragraph).  "Inkling 2 Small's Native 4-Bit Training: Debut and Doubts" (agihunt.info,
+// "Confirmed"): Four Over Six chooses between two scaling factors; per-expert scales.
+//
+// HBM-bound kernels: 16-byte vector loads, one thread per 16-value block (two 16-byte loads, one
+// 8-byte code store, one scale byte), grid-stride loops sized to the SM count.
+#include "common.cuh"
+
+#include <cfloat>
+
+namespace moe4 {
+
+int num_sms() {
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0, n = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached = n > 0 ? n : 148;
+    }
+    return cached;
+}
+
+// ------------------------------------------------------------------ amax pass
+// Per matrix: max |x| over bf16 values, as binary32 bits (non-negative floats order as unsigned
+// integers), folded into amax_bits[m] with one atomicMax per block.
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                        int64_t cols, int64_t ld, int64_t mat_stride,
+                                                        unsigned int *__restrict__ amax_bits) {
+    const int m = blockIdx.y;
+    const uint16_t *xm = x + (int64_t)m * mat_stride;
+    const int64_t vec_per_row = cols / 8;
+    const int64_t nvec = rows * vec_per_row;
+    uint32_t best = 0;  // two packed bf16 magnitudes
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = (ld == cols) ? 0 : v / vec_per_row;
+        const int64_t c = (ld == cols) ? v * 8 : (v - r * vec_per_row) * 8;
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(xm + r * ld + c));
+        best = __vmaxu2(best, q.x & 0x7FFF7FFFu);
+        best = __vmaxu2(best, q.y & 0x7FFF7FFFu);
+        best = __vmaxu2(best, q.z & 0x7FFF7FFFu);
+        best = __vmaxu2(best, q.w & 0x7FFF7FFFu);
+    }
+    uint32_t mag = max(best & 0xFFFFu, best >> 16) << 16;
+    mag = __reduce_max_sync(0xFFFFFFFFu, mag);
+    __shared__ uint32_t part[8];
+    if (lane_id() == 0) part[warp_id()] = mag;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b = max(b, part[i]);
+        if (b) atomicMax(amax_bits + m, b);
+    }
+}
+
+// ------------------------------------------------------------------ NVFP4 block quantiser
+struct GlobalScale {
+    float enc, dec;
+};
+
+__device__ __forceinline__ GlobalScale global_scale(float amax) {
+    float enc = 1.0f;
+    if (amax != 0.0f) {
+        enc = __fdiv_rn(2688.0f, amax);
+        if (isinf(enc)) enc = FLT_MAX;
+    }
+    return {enc, __fdiv_rn(1.0f, enc)};
+}
+
+// One candidate scale (a/m) for a block of 16 scaled values y: codes (two words, nibble i =
+// element i), scale code, and the pairwise-tree sum of squared errors.
+__device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, float m, uint32_t &w0,
+                                                 uint32_t &w1, uint32_t &scode) {
+    const float t = __fdiv_rn(a, m);
+    scode = e4m3_rn(t);
+    const float sfv = e4m3_to_f32(scode);
+    float d[16];
+    if (sfv == 0.0f) {
+        w0 = w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w0 |= (__float_as_uint(y[i]) >> 31) << (4 * i + 3);
+            w1 |= (__float_as_uint(y[i + 8]) >> 31) << (4 * i + 3);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) d[i] = y[i];
+    } else {
+        const float rcp = __fdiv_rn(1.0f, sfv);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(y[i], rcp);
+        w0 = e2m1x8_rn(v);
+        w1 = e2m1x8_rn(v + 8);
+        float e[16];
+        e2m1x8_to_f32(w0, e);
+        e2m1x8_to_f32(w1, e + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) d[i] = __fsub_rn(y[i], __fmul_rn(e[i], sfv));
+    }
+    float s[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(d[i], d[i]);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < off; ++i) s[i] = __fadd_rn(s[i], s[i + off]);
+    return s[0];
+}
+
+__device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, uint32_t &w0,
+                                            uint32_t &w1, uint32_t &scode) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(y[i]));
+    const float err6 = nvfp4_candidate(y, a, 6.0f, w0, w1, scode);
+    if (four_over_six) {
+        uint32_t u0, u1, s4;
+        const float err4 = nvfp4_candidate(y, a, 4.0f, u0, u1, s4);
+        if (err4 < err6) {
+            w0 = u0;
+            w1 = u1;
+            scode = s4;
+        }
+    }
+}
+
+// Offset of the scale byte of (row, blk) in the tensor-core tile layout of a matrix with
+// `rows` rows and `nblk` blocks per row.
+__device__ __forceinline__ int64_t sf_mma_offset(int64_t row, int64_t blk, int64_t nblk) {
+    const int64_t rt = row >> 7, i = row & 31, j = (row >> 5) & 3;
+    const int64_t kg = blk >> 2, kb = blk & 3;
+    return (rt * (nblk >> 2) + kg) * 512 + i * 16 + j * 4 + kb;
+}
+
+// One thread per 16-value block.  amax per matrix from amax_in (given) or amax_bits (pass 1).
+// The block index b runs over all matrices; with contiguous rows (ld == cols) the input, code and
+// canonical-scale offsets are b*16, b*8 and b, and the matrix index only moves forward in the
+// grid-stride loop, so no division is needed on that path.
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(
+    const uint16_t *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+    int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
+    bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
+    float *__restrict__ g_dec) {
+    const int64_t nblk = cols / 16;
+    const int64_t per_mat = rows * nblk;
+    const int64_t total = nmat * per_mat;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gtid < nmat) {
+        const float am = amax_in ? amax_in[gtid] : __uint_as_float(amax_bits[gtid]);
+        g_dec[gtid] = global_scale(am).dec;
+    }
+    const bool contiguous = (ld == cols);
+    int64_t m = -1, mat_begin = 0, mat_end = 0;
+    float g_enc = 1.0f;
+    for (int64_t b = gtid; b < total; b += (int64_t)gridDim.x * blockDim.x) {
+        if (b >= mat_end) {
+            m = b / per_mat;
+            mat_begin = m * per_mat;
+            mat_end = mat_begin + per_mat;
+            const float am = amax_in ? amax_in[m] : __uint_as_float(amax_bits[m]);
+            g_enc = global_scale(am).enc;
+        }
+        const int64_t rem = b - mat_begin;
+        int64_t row = 0, blk = 0;
+        if (!contiguous || sf_mma) {
+            row = (int64_t)((uint32_t)rem / (uint32_t)nblk);
+            blk = rem - row * nblk;
+        }
+        const uint16_t *srcp = contiguous ? x + b * 16 : x + m * mat_stride + row * ld + blk * 16;
+        const uint4 *src = reinterpret_cast<const uint4 *>(srcp);
+        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y[2 * i] = __fmul_rn(bf16_lo(wv[i]), g_enc);
+            y[2 * i + 1] = __fmul_rn(bf16_hi(wv[i]), g_enc);
+        }
+        uint32_t w0, w1, scode;
+        nvfp4_block(y, four_over_six, w0, w1, scode);
+        *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
+        if (sf_mma)
+            sf[mat_begin + sf_mma_offset(row, blk, nblk)] = (uint8_t)scode;
+        else
+            sf[b] = (uint8_t)scode;
+    }
+}
+
+// ------------------------------------------------------------------ dequantise
+__global__ void __launch_bounds__(256) nvfp4_dequant_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
+    int64_t nmat, int64_t rows, int64_t cols, bool out_bf16, void *__restrict__ out) {
+    const int64_t nblk = cols / 16;
+    const int64_t per_mat = rows * nblk;
+    const int64_t total = nmat * per_mat;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = b / per_mat;
+        const uint2 w = *reinterpret_cast<const uint2 *>(codes + b * 8);
+        const float sfv = e4m3_to_f32(sf[b]);
+        const float gd = g_dec[m];
+        float e[16], o[16];
+        e2m1x8_to_f32(w.x, e);
+        e2m1x8_to_f32(w.y, e + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(__fmul_rn(e[i], sfv), gd);
+        if (out_bf16) {
+            uint32_t p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                p[i] = (uint32_t)f32_to_bf16_bits(o[2 * i]) | ((uint32_t)f32_to_bf16_bits(o[2 * i + 1]) << 16);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + b * 16);
+            dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+            dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + b * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ Hadamard(128)
+// A warp holds one 128-chunk, lane l elements 4l..4l+3.  Butterfly span h pairs element i (bit h
+// clear) with i+h: the lower one becomes u[i] + u[i+h], the upper one u[i] - u[i+h].  Spans 1 and
+// 2 are inside a lane, spans 4..64 pair lane l with lane l ^ (h/4).
+__device__ __forceinline__ void fwht128_warp(float u[4]) {
+    float a0 = __fadd_rn(u[0], u[1]), a1 = __fsub_rn(u[0], u[1]);
+    float a2 = __fadd_rn(u[2], u[3]), a3 = __fsub_rn(u[2], u[3]);
+    u[0] = __fadd_rn(a0, a2);
+    u[2] = __fsub_rn(a0, a2);
+    u[1] = __fadd_rn(a1, a3);
+    u[3] = __fsub_rn(a1, a3);
+    const int lane = lane_id();
+#pragma unroll
+    for (int lm = 1; lm < 32; lm <<= 1) {
+        const bool upper = (lane & lm) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float p = __shfl_xor_sync(0xFFFFFFFFu, u[j], lm);
+            u[j] = upper ? __fsub_rn(p, u[j]) : __fadd_rn(u[j], p);
+        }
+    }
+    const float c = __uint_as_float(0x3DB504F3u);  // nearest binary32 to 1/sqrt(128)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) u[j] = __fmul_rn(u[j], c);
+}
+
+__device__ __forceinline__ void load_chunk_bf16(const uint16_t *p, float u[4]) {
+    const uint2 q = *reinterpret_cast<const uint2 *>(p);
+    u[0] = bf16_lo(q.x);
+    u[1] = bf16_hi(q.x);
+    u[2] = bf16_lo(q.y);
+    u[3] = bf16_hi(q.y);
+}
+
+__global__ void __launch_bounds__(256) hadamard_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                            int64_t cols, unsigned int *__restrict__ amax_bits) {
+    const int64_t chunks = rows * (cols / 128);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    float best = 0.0f;
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
+        float u[4];
+        load_chunk_bf16(x + ch * 128 + lane_id() * 4, u);
+        fwht128_warp(u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) best = fmaxf(best, fabsf(u[j]));
+    }
+    uint32_t b = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(best));
+    __shared__ uint32_t part[8];
+    if (lane_id() == 0) part[warp_id()] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, part[i]);
+        if (m) atomicMax(amax_bits, m);
+    }
+}
+
+// Four values of a 16-block held by four consecutive lanes (lane%4 = quarter q): one candidate.
+__device__ __forceinline__ float quarter_candidate(const float y[4], float a, float m, uint32_t &bits16,
+                                                   uint32_t &scode) {
+    const float t = __fdiv_rn(a, m);
+    scode = e4m3_rn(t);
+    const float sfv = e4m3_to_f32(scode);
+    float d[4];
+    if (sfv == 0.0f) {
+        bits16 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            bits16 |= (__float_as_uint(y[i]) >> 31) << (4 * i + 3);
+            d[i] = y[i];
+        }
+    } else {
+        const float rcp = __fdiv_rn(1.0f, sfv);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = __fmul_rn(y[i], rcp);
+            v[i + 4] = 0.0f;
+        }
+        bits16 = e2m1x8_rn(v) & 0xFFFFu;
+        float e[8];
+        e2m1x8_to_f32(bits16, e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] = __fsub_rn(y[i], __fmul_rn(e[i], sfv));
+    }
+    // the block's pairwise tree: offsets 8 and 4 cross lanes (quarters q^2, q^1), 2 and 1 inside
+    float s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = __fmul_rn(d[i], d[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = __fadd_rn(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 2));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = __fadd_rn(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 1));
+    s[0] = __fadd_rn(s[0], s[2]);
+    s[1] = __fadd_rn(s[1], s[3]);
+    s[0] = __fadd_rn(s[0], s[1]);
+    // the quarter-0 lane holds the block's sum; broadcast it to the other three
+    return __shfl_sync(0xFFFFFFFFu, s[0], lane_id() & ~3);
+}
+
+__global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                             int64_t cols, const unsigned int *__restrict__ amax_bits,
+                                                             bool four_over_six, uint8_t *__restrict__ codes,
+                                                             uint8_t *__restrict__ sf, float *__restrict__ g_dec) {
+    const GlobalScale gs = global_scale(__uint_as_float(*amax_bits));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_dec = gs.dec;
+    const int64_t chunks = rows * (cols / 128);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = lane_id();
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
+        float u[4];
+        load_chunk_bf16(x + ch * 128 + lane * 4, u);
+        fwht128_warp(u);
+        float y[4];
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            y[j] = __fmul_rn(u[j], gs.enc);
+            a = fmaxf(a, fabsf(y[j]));
+        }
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        uint32_t bits, scode;
+        const float err6 = quarter_candidate(y, a, 6.0f, bits, scode);
+        if (four_over_six) {
+            uint32_t b4, s4;
+            const float err4 = quarter_candidate(y, a, 4.0f, b4, s4);
+            if (err4 < err6) {
+                bits = b4;
+                scode = s4;
+            }
+        }
+        *reinterpret_cast<uint16_t *>(codes + ch * 64 + lane * 2) = (uint16_t)bits;
+        if ((lane & 3) == 0) sf[ch * 8 + (lane >> 2)] = (uint8_t)scode;
+    }
+}
+
+__global__ void __launch_bounds__(256) hadamard_dequant_kernel(const uint8_t *__restrict__ codes,
+                                                               const uint8_t *__restrict__ sf,
+                                                               const float *__restrict__ g_dec, int64_t rows,
+                                                               int64_t cols, uint16_t *__restrict__ out) {
+    const int64_t chunks = rows * (cols / 128);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = lane_id();
+    const float gd = *g_dec;
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
+        const uint32_t bits = *reinterpret_cast<const uint16_t *>(codes + ch * 64 + lane * 2);
+        const float sfv = e4m3_to_f32(sf[ch * 8 + (lane >> 2)]);
+        float e[8], u[4];
+        e2m1x8_to_f32(bits, e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) u[j] = __fmul_rn(__fmul_rn(e[j], sfv), gd);
+        fwht128_warp(u);
+        const uint32_t lo = (uint32_t)f32_to_bf16_bits(u[0]) | ((uint32_t)f32_to_bf16_bits(u[1]) << 16);
+        const uint32_t hi = (uint32_t)f32_to_bf16_bits(u[2]) | ((uint32_t)f32_to_bf16_bits(u[3]) << 16);
+        *reinterpret_cast<uint2 *>(out + ch * 128 + lane * 4) = make_uint2(lo, hi);
+    }
+}
+
+static int grid_for(int64_t work_items, int threads, int per_sm) {
+    const int64_t need = (work_items + threads - 1) / threads;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+}  // namespace moe4
+
+using namespace moe4;
+
+extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                              uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
+                              uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0 && ld >= cols && ld % 8 == 0);
+    MOE4_CHECK_ARG(codes && sf && g_dec);
+    MOE4_CHECK_ARG(rows == 0 || (x && aligned16(x) && aligned16(codes)));
+    MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_AMAX_GIVEN | MOE4_SF_MMA_LAYOUT)) == 0);
+    const bool given = (flags & MOE4_AMAX_GIVEN) != 0;
+    const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    MOE4_CHECK_ARG(!given || amax_in);
+    MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
+    MOE4_CHECK_ARG(rows * (cols / 16) < (int64_t(1) << 32));
+    cudaStream_t st = as_stream(stream);
+    unsigned int *amax_bits = nullptr;
+    if (!given) {
+        if (!ws || ws_bytes < (size_t)nmat * sizeof(unsigned int)) return MOE4_ERR_WORKSPACE;
+        amax_bits = static_cast<unsigned int *>(ws);
+        if (cudaMemsetAsync(amax_bits, 0, (size_t)nmat * sizeof(unsigned int), st) != cudaSuccess)
+            return MOE4_ERR_CUDA;
+        if (rows > 0) {
+            const int64_t nvec = rows * (cols / 8);
+            int gx = grid_for(nvec, 256, 8 * 1);
+            const int64_t per_mat_cap = ((int64_t)num_sms() * 8 + nmat - 1) / nmat;
+            if (gx > per_mat_cap) gx = (int)per_mat_cap;
+            if (gx < 1) gx = 1;
+            amax_bf16_kernel<<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
+        }
+    }
+    const int64_t total = nmat * rows * (cols / 16);
+    const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
+    nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, given ? amax_in : nullptr,
+                                             amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf,
+                                             g_dec);
+    return launch_status();
+}
+
+extern "C" int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t nmat,
+                                int64_t rows, int64_t cols, void *out, uint32_t flags, void *stream) {
+    MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0);
+    MOE4_CHECK_ARG(codes && sf && g_dec && out && aligned16(out) && aligned16(codes));
+    const bool bf16 = (flags & MOE4_OUT_BF16) != 0;
+    MOE4_CHECK_ARG(bf16 != ((flags & MOE4_OUT_F32) != 0));
+    const int64_t total = nmat * rows * (cols / 16);
+    if (total == 0) return MOE4_OK;
+    nvfp4_dequant_kernel<<<grid_for(total, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, nmat, rows,
+                                                                                  cols, bf16, out);
+    return launch_status();
+}
+
+extern "C" int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *sf,
+                              float *g_dec, uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0);
+    MOE4_CHECK_ARG(codes && sf && g_dec && (rows == 0 || (x && aligned16(x))));
+    MOE4_CHECK_ARG((flags & ~MOE4_FOUR_OVER_SIX) == 0);
+    if (!ws || ws_bytes < sizeof(unsigned int)) return MOE4_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    unsigned int *amax_bits = static_cast<unsigned int *>(ws);
+    if (cudaMemsetAsync(amax_bits, 0, sizeof(unsigned int), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    const int64_t chunks = rows * (cols / 128);
+    const int grid = grid_for(chunks * 32 > 1 ? chunks * 32 : 1, 256, 8);
+    if (chunks > 0) hadamard_amax_kernel<<<grid, 256, 0, st>>>(x, rows, cols, amax_bits);
+    hadamard_quant_kernel<<<grid, 256, 0, st>>>(x, rows, cols, amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0,
+                                                codes, sf, g_dec);
+    return launch_status();
+}
+
+extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t rows,
+                                int64_t cols, uint16_t *out_bf16, uint32_t flags, void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0 && flags == 0);
+    MOE4_CHECK_ARG(codes && sf && g_dec && out_bf16 && aligned16(out_bf16));
+    const int64_t chunks = rows * (cols / 128);
+    if (chunks == 0) return MOE4_OK;
+    hadamard_dequant_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, rows,
+                                                                                            cols, out_bf16);
+    return launch_status();
+}

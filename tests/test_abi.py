@@ -1,0 +1,92 @@
+"""The C-ABI library: it loads without a GPU, exports every entry point that include/moe4.h
+declares, and rejects bad arguments on the host before any CUDA call (sizes, flags, alignment,
+missing workspace).  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_moe_numerics_03_b300 import build, moe4
+    build.build()
+    return moe4.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ["nvfp4_quantize", "mxfp8_requant_transpose_sr", "grouped_expert_gemm_nvfp4",
+                     "grouped_gemm_mxfp8", "hadamard_quant", "hadamard_dequant"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from precision_moe_numerics_03_b300 import moe4
+    names = _declared()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe4.exported_symbols()) == names
+
+
+def test_host_side_queries(lib):
+    assert lib.moe4_version() >= 100
+    assert lib.moe4_status_string(0) == b"ok"
+    assert b"argument" in lib.moe4_status_string(-1)
+    assert lib.moe4_workspace_size(1, 384, 0, 0) == 384 * 4
+    assert lib.moe4_workspace_size(2, 0, 0, 0) == 4
+    assert lib.moe4_workspace_size(3, 16384, 8, 384) == (128 * 384 + 384) * 4
+    assert lib.moe4_workspace_size_gemm(0, 256, 1, 256, 512) == 256 * 32 * 2
+
+
+FAKE = 1 << 20          # a 16-byte aligned address that is never dereferenced
+MISALIGNED = FAKE + 4
+
+
+@pytest.mark.parametrize("case", [
+    # (entry point, arguments) -- each must fail its host-side checks
+    ("nvfp4_quantize", (FAKE, 1, 16, 15, 16, FAKE, FAKE, FAKE, None, 1, FAKE, 64, None)),   # cols % 16
+    ("nvfp4_quantize", (FAKE, 1, 16, 16, 8, FAKE, FAKE, FAKE, None, 1, FAKE, 64, None)),    # ld < cols
+    ("nvfp4_quantize", (MISALIGNED, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, FAKE, 64, None)),
+    ("nvfp4_quantize", (FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1 << 30, FAKE, 64, None)),  # bad flag
+    ("nvfp4_quantize", (FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 2, FAKE, 64, None)),   # AMAX_GIVEN, no amax
+    ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 48, 64, FAKE, FAKE, 0, 0, 4, None)),  # rows % 32
+    ("mxfp8_quantize", (FAKE, 32, 64, FAKE, FAKE, 0, 0, 0x30, None)),                        # both layouts
+    ("hadamard_quant", (FAKE, 4, 64, FAKE, FAKE, FAKE, 1, FAKE, 4, None)),                   # cols % 128
+    ("grouped_expert_gemm_nvfp4", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 100, 256, 256, FAKE, 0x100,
+                                   None, 0, None)),                                          # rows % 128
+    ("grouped_expert_gemm_nvfp4", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE, 0x300,
+                                   None, 0, None)),                                          # two outputs
+    ("grouped_gemm_mxfp8", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 128, FAKE, 0x100 | 0x1000 | 0x2000,
+                            None, 0, None)),                                                 # both groupings
+    ("grouped_gemm_mxfp8", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 128, FAKE, 0x200 | 0x2000 | 0x4000,
+                            None, 0, None)),                                                 # bf16 accumulate
+    ("moe4_route_topk", (FAKE, 4, 8, 40, FAKE, FAKE, None)),                                 # k > 32
+    ("moe4_permute_plan", (FAKE, 4, 2, 8, FAKE, FAKE, FAKE, 10, FAKE, 1 << 20, None)),       # rows_cap too small
+    ("moe4_swiglu", (FAKE, 4, 6, FAKE, None)),                                               # f % 4
+    ("moe4_combine", (FAKE, FAKE, FAKE, 4, 2, 12, FAKE, None)),                              # d % 8
+    ("moe4_sgd_update", (FAKE, FAKE, 6, 0.1, FAKE, None)),                                   # n % 4
+    ("moe4_sf_to_mma_layout", (FAKE, 1, 100, 4, FAKE, None)),                                # rows % 128
+    ("moe4_convert", (7, FAKE, 4, FAKE, None)),                                              # bad kind
+])
+def test_argument_checks_fail_on_host(lib, case):
+    name, args = case
+    assert getattr(lib, name)(*args) == -1
+
+
+def test_missing_workspace_is_reported(lib):
+    # nvfp4_quantize without AMAX_GIVEN and without ws -> MOE4_ERR_WORKSPACE, before any launch
+    assert lib.nvfp4_quantize(FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, None, 0, None) == -5
+    assert lib.hadamard_quant(FAKE, 4, 128, FAKE, FAKE, FAKE, 1, None, 0, None) == -5

@@ -1,0 +1,176 @@
+"""GPU parity of the block-scaled grouped GEMMs against the oracle's float64 GEMM of the operands
+the oracle quantised itself.
+
+Tolerance (binary32 output): relative Frobenius error <= 1e-5 and, element by element,
+|D - D_ref| <= 2^-16 * sum_k |a_k * b_k|.  bf16 output: within one bf16 ulp of RN_bf16(D_ref).
+The NVFP4 GEMM is the expert forward ("Inkling 2 Small's Native 4-Bit Training: Debut and Doubts",
+"Confirmed": NVFP4 forward of the expert layers with dedicated kernels); the MXFP8 GEMMs are the
+backward dgrad (rows grouped by expert) and wgrad (contraction grouped by expert).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_moe_numerics_03_b300 import inputs, moe4
+from gpu_helpers import DEV, empty_u8, nvfp4_quantize, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 1e-5
+ELEM = 2.0 ** -16
+
+
+def check_f32(D, Dref, S, what=""):
+    D = D.astype(np.float64)
+    err = np.abs(D - Dref)
+    nref = np.linalg.norm(Dref)
+    rel = np.linalg.norm(D - Dref) / (nref if nref > 0 else 1.0)
+    bad = err > ELEM * S
+    assert rel <= REL_FRO and not bad.any(), (
+        "%s rel_fro=%.3e, %d of %d elements over 2^-16*S, worst err/S=%.3e, D[0,:4]=%s ref=%s" %
+        (what, rel, int(bad.sum()), bad.size, float(np.max(err / np.maximum(S, 1e-300))),
+         D.reshape(-1)[:4], Dref.reshape(-1)[:4]))
+
+
+def check_bf16(Dbits, Dref):
+    got = Dbits.astype(np.int64)
+    want = oracle.f32_to_bf16(Dref.astype(np.float32)).astype(np.int64)
+    # compare as ordered integers (sign-magnitude bf16 -> monotone key)
+    def key(b):
+        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+    assert np.max(np.abs(key(got) - key(want))) <= 1
+
+
+def _bf16(rng, shape, std=1.0, t=False):
+    x = rng.standard_t(3, shape) / np.sqrt(3) if t else rng.standard_normal(shape)
+    return inputs.to_bf16_bits((x * std).astype(np.float32))
+
+
+def _offs(sizes):
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+
+
+def _nvfp4_case(rows_sizes, N, K, seed, out_bf16=False, sf_mma=False):
+    rng = np.random.default_rng(seed)
+    E = len(rows_sizes)
+    offs = _offs(rows_sizes)
+    R = int(offs[-1])
+    a_bits = _bf16(rng, (R, K), t=True)
+    b_bits = _bf16(rng, (E * N, K), 0.02)
+    # device path
+    ac, asf, ag = nvfp4_quantize(to_dev(a_bits), 1, R, K)
+    bc, bsf, bg = nvfp4_quantize(to_dev(b_bits), E, N, K)
+    flags = moe4.OUT_BF16 if out_bf16 else moe4.OUT_F32
+    if sf_mma:
+        asf2, bsf2 = torch.empty_like(asf), torch.empty_like(bsf)
+        moe4.moe4_sf_to_mma_layout(asf, 1, R, K // 16, asf2)
+        moe4.moe4_sf_to_mma_layout(bsf, E, N, K // 16, bsf2)
+        asf, bsf = asf2, bsf2
+        flags |= moe4.SF_MMA_LAYOUT
+    D = torch.empty((R, N), dtype=torch.int16 if out_bf16 else torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, R, E, N, K))
+    moe4.grouped_expert_gemm_nvfp4(ac, asf, ag, bc, bsf, bg, to_dev(offs), E, R, N, K, D, flags, ws)
+    assert moe4.moe4_get_status() == moe4.OK
+    # oracle path
+    rac, ras, rag = oracle.nvfp4_quantize(oracle.bf16_to_f32(a_bits))
+    rbc, rbs, rbg = oracle.nvfp4_quantize(oracle.bf16_to_f32(b_bits).reshape(E, N, K))
+    Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rac, ras, rag),
+                                    oracle.nvfp4_dequantize(rbc, rbs, rbg), offs)
+    return D, Dref, S
+
+
+def test_nvfp4_single_expert_workload():
+    # X 256x512 (N(0,1) with 1% outliers x20) times W (512x256 stored K-major as 256x512)
+    rng = inputs.host_rng(1, 0)
+    x = inputs.to_bf16_bits(inputs.host_outliers(rng, inputs.host_normal(rng, (256, 512))))
+    w = inputs.to_bf16_bits(inputs.host_normal(inputs.host_rng(1, 1), (256, 512), 0.02))
+    ac, asf, ag = nvfp4_quantize(to_dev(x), 1, 256, 512)
+    bc, bsf, bg = nvfp4_quantize(to_dev(w), 1, 256, 512)
+    offs = to_dev(np.array([0, 256], np.int32))
+    D = torch.empty((256, 256), dtype=torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, 256, 1, 256, 512))
+    moe4.grouped_expert_gemm_nvfp4(ac, asf, ag, bc, bsf, bg, offs, 1, 256, 256, 512, D, moe4.OUT_F32, ws)
+    assert moe4.moe4_get_status() == moe4.OK
+    rac, ras, rag = oracle.nvfp4_quantize(oracle.bf16_to_f32(x))
+    rbc, rbs, rbg = oracle.nvfp4_quantize(oracle.bf16_to_f32(w))
+    Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rac, ras, rag),
+                                    oracle.nvfp4_dequantize(rbc, rbs, rbg)[None], np.array([0, 256]))
+    check_f32(to_np(D), Dref, S, "single expert")
+
+
+@pytest.mark.parametrize("sf_mma", [False, True])
+def test_nvfp4_grouped_with_empty_groups(sf_mma):
+    D, Dref, S = _nvfp4_case([128, 0, 256, 384, 128, 0], N=512, K=768, seed=5, sf_mma=sf_mma)
+    check_f32(to_np(D), Dref, S, "grouped")
+
+
+def test_nvfp4_bf16_output():
+    D, Dref, S = _nvfp4_case([256, 128], N=256, K=512, seed=6, out_bf16=True)
+    check_bf16(to_np(D, np.uint16), Dref)
+
+
+def test_nvfp4_small_moe_shapes():
+    # 8 experts, d_model 2048, gate/up width 2048 (2 x 1024): groups of a top-2 routing, padded
+    rng = np.random.default_rng(12)
+    counts = rng.multinomial(8192, np.ones(8) / 8)
+    sizes = (counts + 127) // 128 * 128
+    D, Dref, S = _nvfp4_case(list(sizes), N=2048, K=2048, seed=13)
+    check_f32(to_np(D), Dref, S, "small moe")
+
+
+def _mxfp8_rowwise(x_bits, rows, cols):
+    q = empty_u8(rows, cols)
+    e8 = empty_u8(rows, cols // 32)
+    moe4.mxfp8_quantize(to_dev(x_bits), rows, cols, q, e8, 0, 0, moe4.ROWWISE)
+    return q, e8
+
+
+def test_mxfp8_dgrad_group_m():
+    rng = np.random.default_rng(21)
+    sizes = [256, 0, 128, 384]
+    E, N, K = len(sizes), 512, 640
+    offs = _offs(sizes)
+    M = int(offs[-1])
+    a_bits = _bf16(rng, (M, K))
+    b_bits = _bf16(rng, (E * N, K), 0.02)
+    aq, ae = _mxfp8_rowwise(a_bits, M, K)
+    bq, be = _mxfp8_rowwise(b_bits, E * N, K)
+    D = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, E, N, K))
+    moe4.grouped_gemm_mxfp8(aq, ae, bq, be, to_dev(offs), E, M, N, K, D, moe4.OUT_F32 | moe4.GROUP_M, ws)
+    assert moe4.moe4_get_status() == moe4.OK
+    ra = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(oracle.bf16_to_f32(a_bits), colwise=False))
+    rb = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(oracle.bf16_to_f32(b_bits), colwise=False))
+    Dref, S = oracle.grouped_gemm_m(ra, rb.reshape(E, N, K), offs)
+    check_f32(to_np(D), Dref, S, "mxfp8 dgrad")
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_mxfp8_wgrad_group_k(accumulate):
+    rng = np.random.default_rng(22)
+    sizes = [128, 256, 0, 384]
+    E, M, N = len(sizes), 256, 512
+    offs = _offs(sizes)
+    Kt = int(offs[-1])
+    a_bits = _bf16(rng, (M, Kt))
+    b_bits = _bf16(rng, (N, Kt))
+    aq, ae = _mxfp8_rowwise(a_bits, M, Kt)
+    bq, be = _mxfp8_rowwise(b_bits, N, Kt)
+    init = rng.standard_normal((E, M, N)).astype(np.float32)
+    D = to_dev(init) if accumulate else torch.full((E, M, N), np.nan, dtype=torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, Kt))
+    flags = moe4.OUT_F32 | moe4.GROUP_K | (moe4.ACCUMULATE if accumulate else 0)
+    moe4.grouped_gemm_mxfp8(aq, ae, bq, be, to_dev(offs), E, M, N, Kt, D, flags, ws)
+    assert moe4.moe4_get_status() == moe4.OK
+    ra = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(oracle.bf16_to_f32(a_bits), colwise=False))
+    rb = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(oracle.bf16_to_f32(b_bits), colwise=False))
+    Dref, S = oracle.grouped_gemm_k(ra, rb, offs)
+    got = to_np(D)
+    if accumulate:
+        # D = RN(init + product): widen the bound by the rounding of that one addition
+        Dref = Dref + init
+        S = S + np.abs(init) * 2.0 ** -7
+    check_f32(got, Dref, S, "mxfp8 wgrad")
+    if not accumulate:
+        assert np.all(got[2] == 0)

@@ -1,0 +1,109 @@
+"""GPU parity of the MoE steps around the expert GEMMs: top-k routing (indices bit-exact, weights
+to 1e-6 relative), the dispatch plan and the NVFP4 row gather (bit-exact), SwiGLU (within one bf16
+ulp: it calls expf), the weighted combine and the SGD update of FP32 master weights (bit-exact).
+
+Shapes: the small grouped MoE (8 experts, top-2) and the Inkling-shaped layer (384 experts, top-8,
+N(0,1) logits plus a per-expert N(0,1) bias, 16384 tokens)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_moe_numerics_03_b300 import inputs, moe4
+from gpu_helpers import DEV, empty_u8, first_mismatch, nvfp4_quantize, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _logits(T, E, bias, seed):
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    if bias:
+        lg = (lg + rng.standard_normal(E).astype(np.float32)).astype(np.float32)
+    return lg
+
+
+def _route_gpu(lg, k):
+    T, E = lg.shape
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    moe4.moe4_route_topk(to_dev(lg), T, E, k, idx, w)
+    torch.cuda.synchronize()
+    return idx, w
+
+
+@pytest.mark.parametrize("T,E,k,bias", [(4096, 8, 2, False), (16384, 384, 8, True), (33, 40, 32, False)])
+def test_route_topk(T, E, k, bias):
+    lg = _logits(T, E, bias, T + E)
+    lg[0, :] = 0.25                          # a fully tied row: lowest expert indices win
+    idx, w = _route_gpu(lg, k)
+    ridx, rw = oracle.route_topk(lg, k)
+    assert first_mismatch(to_np(idx), ridx) is None
+    assert np.allclose(to_np(w), rw, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("T,E,k,bias", [(4096, 8, 2, False), (16384, 384, 8, True), (5, 3, 2, False)])
+def test_permute_plan_and_gather(T, E, k, bias):
+    lg = _logits(T, E, bias, 7 * T + E)
+    ridx, _ = oracle.route_topk(lg, k)     # a seeded host input to both sides
+    rows_cap = T * k + 127 * E
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    src_of = torch.empty(rows_cap, dtype=torch.int32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E))
+    moe4.moe4_permute_plan(to_dev(ridx), T, k, E, offs, row_of, src_of, rows_cap, ws)
+    torch.cuda.synchronize()
+    roffs, rrow = oracle.permute_plan(ridx, E)
+    assert first_mismatch(to_np(offs), roffs) is None
+    assert first_mismatch(to_np(row_of), rrow) is None
+    Rp = int(roffs[-1])
+    rsrc = np.full(rows_cap, -1, np.int32)
+    rsrc[rrow.reshape(-1)] = np.repeat(np.arange(T, dtype=np.int32), k)
+    assert first_mismatch(to_np(src_of), rsrc) is None
+    # gather the NVFP4 rows of a token tensor
+    cols = 256
+    x = inputs.to_bf16_bits(np.random.default_rng(1).standard_normal((T, cols)).astype(np.float32))
+    c, s, g = nvfp4_quantize(to_dev(x), 1, T, cols)
+    oc, osf = empty_u8(Rp, cols // 2), empty_u8(Rp, cols // 16)
+    moe4.moe4_permute_nvfp4(c, s, T, cols, src_of, Rp, oc, osf)
+    torch.cuda.synchronize()
+    rc, rs, _ = oracle.nvfp4_quantize(oracle.bf16_to_f32(x))
+    assert first_mismatch(to_np(oc), oracle.permute_rows(rc, rrow, Rp)) is None
+    assert first_mismatch(to_np(osf), oracle.permute_rows(rs, rrow, Rp)) is None
+
+
+def test_swiglu_within_one_bf16_ulp():
+    rows, f = 640, 1024
+    gu = (np.random.default_rng(2).standard_normal((rows, 2 * f)) * 4).astype(np.float32)
+    h = torch.empty((rows, f), dtype=torch.int16, device=DEV)
+    moe4.moe4_swiglu(to_dev(gu), rows, f, h)
+    torch.cuda.synchronize()
+    got = to_np(h, np.uint16).astype(np.int32)
+    want = oracle.f32_to_bf16(oracle.swiglu(gu)).astype(np.int32)
+    # bf16 bit patterns of same-sign values differ by the number of ulps between them
+    assert np.max(np.abs(got - want)) <= 1
+
+
+def test_combine_bit_exact():
+    T, k, d, R = 1000, 8, 512, 9000
+    rng = np.random.default_rng(3)
+    yh = inputs.to_bf16_bits(rng.standard_normal((R, d)).astype(np.float32))
+    row_of = rng.permutation(R)[:T * k].reshape(T, k).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    y = torch.empty((T, d), dtype=torch.int16, device=DEV)
+    moe4.moe4_combine(to_dev(yh), to_dev(row_of), to_dev(w), T, k, d, y)
+    torch.cuda.synchronize()
+    assert first_mismatch(to_np(y, np.uint16), oracle.combine(yh, row_of, w)) is None
+
+
+def test_sgd_update_bit_exact():
+    n = 1 << 16
+    rng = np.random.default_rng(4)
+    w32 = rng.standard_normal(n).astype(np.float32) * np.float32(0.02)
+    dw = rng.standard_normal(n).astype(np.float32)
+    wt = to_dev(w32)
+    wb = torch.empty(n, dtype=torch.int16, device=DEV)
+    moe4.moe4_sgd_update(wt, to_dev(dw), n, 1e-3, wb)
+    torch.cuda.synchronize()
+    rw, rb = oracle.sgd_update(w32, dw, 1e-3)
+    assert first_mismatch(to_np(wt), rw) is None and first_mismatch(to_np(wb, np.uint16), rb) is None

@@ -1,0 +1,233 @@
+"""GPU parity of the NVFP4 quantiser (Four Over Six), the dequantiser, the Hadamard codec and the
+device's own conversions, against the oracle, bit for bit.
+
+Inputs follow the seeded recipe of precision_moe_numerics_03_b300.inputs: the single-expert
+workload (X 256x512 N(0,1) with 1% outliers x20, W 512x256 N(0, 0.02)), ragged shapes, batched
+per-expert matrices, degenerate tensors, and the backward-requant workload's full-size X
+[32768, 4096] Student-t(3) and W [384, 2048, 4096] N(0, 0.02) with sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_moe_numerics_03_b300 import inputs, moe4
+from gpu_helpers import DEV, empty_u8, first_mismatch, nvfp4_quantize, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    moe4.load()
+
+
+def _check_quant(x_bits_np, nmat, rows, cols, fos=True, amax=None):
+    x32 = oracle.bf16_to_f32(x_bits_np).reshape(nmat, rows, cols)
+    c, s, g = nvfp4_quantize(to_dev(x_bits_np.reshape(nmat * rows, cols)), nmat, rows, cols,
+                             moe4.FOUR_OVER_SIX if fos else 0, amax=amax)
+    rc, rs, rg = oracle.nvfp4_quantize(x32, four_over_six=fos, amax=amax)
+    msg = first_mismatch(to_np(c), rc) or first_mismatch(to_np(s), rs) or first_mismatch(to_np(g), rg)
+    assert msg is None, msg
+    return c, s, g
+
+
+def _single_expert():
+    rng = inputs.host_rng(1, 0)
+    x = inputs.host_outliers(rng, inputs.host_normal(rng, (256, 512)))
+    w = inputs.host_normal(inputs.host_rng(1, 1), (256, 512), 0.02)
+    return inputs.to_bf16_bits(x), inputs.to_bf16_bits(w)
+
+
+@pytest.mark.parametrize("fos", [True, False])
+def test_single_expert_operands(fos):
+    x, w = _single_expert()
+    _check_quant(x, 1, 256, 512, fos)
+    _check_quant(w, 1, 256, 512, fos)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 16), (1, 3, 48), (1, 300, 144), (3, 37, 256), (5, 128, 64)])
+def test_ragged_and_batched(shape):
+    nmat, rows, cols = shape
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = rng.standard_t(3, (nmat, rows, cols)).astype(np.float32)
+    x *= np.exp2(rng.integers(-8, 8, (nmat, 1, 1))).astype(np.float32)  # per-matrix scale
+    _check_quant(inputs.to_bf16_bits(x), nmat, rows, cols)
+
+
+def test_amax_given_and_strided_rows():
+    rng = np.random.default_rng(3)
+    rows, cols, ld = 64, 96, 128
+    full = inputs.to_bf16_bits(rng.standard_normal((rows, ld)).astype(np.float32))
+    x = full[:, :cols]
+    amax = np.float32(7.25)
+    c, s, g = nvfp4_quantize(to_dev(full), 1, rows, cols, amax=amax, ld=ld)
+    rc, rs, rg = oracle.nvfp4_quantize(oracle.bf16_to_f32(np.ascontiguousarray(x)), amax=amax)
+    assert first_mismatch(to_np(c)[0], rc) is None and first_mismatch(to_np(s)[0], rs) is None
+    assert to_np(g)[0] == rg
+
+
+def test_degenerate_tensors():
+    z = np.zeros((4, 32), np.uint16)
+    _check_quant(z, 1, 4, 32)                                   # amax 0: g_dec = 1, all codes 0
+    neg = inputs.to_bf16_bits(-np.zeros((2, 32), np.float32))
+    _check_quant(neg, 1, 2, 32)                                 # -0 keeps its sign
+    tiny = inputs.to_bf16_bits(np.full((2, 32), 1e-39, np.float32))
+    _check_quant(tiny, 1, 2, 32)                                # g_enc overflows to FLT_MAX
+    big = inputs.to_bf16_bits(np.array([[3e38] + [1.0] * 15], np.float32))
+    _check_quant(big, 1, 1, 16)
+    # no rows: only g_dec is written (1.0)
+    c, s, g = nvfp4_quantize(torch.empty((0, 32), dtype=torch.int16, device=DEV), 2, 0, 32)
+    assert list(to_np(g)) == [1.0, 1.0]
+
+
+def test_sf_mma_layout_is_a_permutation():
+    rng = np.random.default_rng(4)
+    nmat, rows, cols = 2, 256, 512
+    x = inputs.to_bf16_bits(rng.standard_normal((nmat * rows, cols)).astype(np.float32))
+    xd = to_dev(x)
+    c0, s0, g0 = nvfp4_quantize(xd, nmat, rows, cols)
+    c1, s1, g1 = nvfp4_quantize(xd, nmat, rows, cols, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    out = empty_u8(nmat, rows, cols // 16)
+    moe4.moe4_sf_to_mma_layout(s0, nmat, rows, cols // 16, out)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, c1) and torch.equal(g0, g1) and torch.equal(out, s1)
+    # the layout itself, recomputed on the host for every byte
+    s0n, s1n = to_np(s0), to_np(s1).reshape(nmat, -1)
+    nblk = cols // 16
+    for m in range(nmat):
+        for r in range(0, rows, 37):
+            for b in range(nblk):
+                off = ((r // 128) * (nblk // 4) + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+                assert s1n[m, off] == s0n[m, r, b]
+
+
+@pytest.mark.parametrize("bf16_out", [True, False])
+def test_dequantize(bf16_out):
+    x, _ = _single_expert()
+    c, s, g = nvfp4_quantize(to_dev(x), 1, 256, 512)
+    out = torch.empty((1, 256, 512), dtype=torch.int16 if bf16_out else torch.float32, device=DEV)
+    moe4.nvfp4_dequantize(c, s, g, 1, 256, 512, out, moe4.OUT_BF16 if bf16_out else moe4.OUT_F32)
+    torch.cuda.synchronize()
+    ref = oracle.nvfp4_dequantize(*oracle.nvfp4_quantize(oracle.bf16_to_f32(x)))
+    if bf16_out:
+        assert first_mismatch(to_np(out, np.uint16)[0], oracle.f32_to_bf16(ref)) is None
+    else:
+        assert first_mismatch(to_np(out)[0], ref) is None
+
+
+def test_requant_stream_x_full_size_sampled_rows():
+    rows, cols = 32768, 4096
+    g = inputs.device_generator(4, 0, DEV)
+    x = inputs.device_student_t((rows, cols), g, DEV)
+    xb = x.view(torch.int16)
+    c, s, gd = nvfp4_quantize(xb, 1, rows, cols)
+    host = to_np(xb, np.uint16)
+    amax = np.abs(oracle.bf16_to_f32(host)).max()
+    sample = np.random.default_rng(0).choice(rows, 64, replace=False)
+    sample = np.concatenate([sample, [0, rows - 1]])
+    rc, rs, rg = oracle.nvfp4_quantize(oracle.bf16_to_f32(host[sample]), amax=amax)
+    assert to_np(gd)[0] == rg
+    assert first_mismatch(to_np(c)[0][sample], rc) is None
+    assert first_mismatch(to_np(s)[0][sample], rs) is None
+
+
+def test_requant_stream_w_full_size_sampled_experts():
+    E, rows, cols = 384, 2048, 4096
+    g = inputs.device_generator(4, 1, DEV)
+    w = inputs.device_normal((E * rows, cols), 0.02, g, DEV).view(torch.int16)
+    c, s, gd = nvfp4_quantize(w, E, rows, cols)
+    cn, sn, gn = to_np(c), to_np(s), to_np(gd)
+    for e in [0, 191, 383]:
+        host = to_np(w[e * rows:(e + 1) * rows], np.uint16)
+        x32 = oracle.bf16_to_f32(host)
+        amax = np.abs(x32).max()
+        pick = np.random.default_rng(e).choice(rows, 16, replace=False)
+        rc, rs, rg = oracle.nvfp4_quantize(x32[pick], amax=amax)
+        assert gn[e] == rg
+        assert first_mismatch(cn[e][pick], rc) is None and first_mismatch(sn[e][pick], rs) is None
+
+
+@pytest.mark.parametrize("shape", [(4, 128), (37, 256), (256, 512)])
+def test_hadamard_codec(shape):
+    rows, cols = shape
+    rng = np.random.default_rng(rows)
+    x = rng.standard_t(3, (rows, cols)).astype(np.float32)
+    x[rng.random(x.shape) < 0.003] *= 50
+    xb = inputs.to_bf16_bits(x)
+    codes = empty_u8(rows, cols // 2)
+    sf = empty_u8(rows, cols // 16)
+    gd = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT))
+    moe4.hadamard_quant(to_dev(xb), rows, cols, codes, sf, gd, moe4.FOUR_OVER_SIX, ws)
+    out = torch.empty((rows, cols), dtype=torch.int16, device=DEV)
+    moe4.hadamard_dequant(codes, sf, gd, rows, cols, out)
+    torch.cuda.synchronize()
+    rc, rs, rg = oracle.hadamard_quant(oracle.bf16_to_f32(xb))
+    assert first_mismatch(to_np(codes), rc) is None
+    assert first_mismatch(to_np(sf), rs) is None
+    assert to_np(gd)[0] == rg
+    ref = oracle.hadamard_dequant(rc, rs, rg)
+    assert first_mismatch(to_np(out, np.uint16), ref) is None
+
+
+def _device_patterns(start, count):
+    bits = torch.arange(start, start + count, dtype=torch.int64, device=DEV)
+    return (bits - (bits >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32).view(torch.float32)
+
+
+@pytest.mark.parametrize("sign", [0, 1])
+def test_device_e2m1_conversion_exhaustive_binades(sign):
+    lo = (sign << 31) | (123 << 23)
+    step = 1 << 24
+    for start in range(lo, lo + (8 << 23), step):
+        v = _device_patterns(start, step)
+        out = torch.empty(step, dtype=torch.uint8, device=DEV)
+        moe4.moe4_convert(0, v, step, out)
+        torch.cuda.synchronize()
+        assert first_mismatch(to_np(out), oracle.e2m1_range(start, step)) is None
+
+
+def test_device_e4m3_conversion_exhaustive_binades():
+    step = 1 << 24
+    for sign in (0, 1):
+        lo, hi = (sign << 31) | (115 << 23), (sign << 31) | (136 << 23)
+        for start in range(lo, hi, step):
+            n = min(step, hi - start)
+            v = _device_patterns(start, n)
+            out = torch.empty(n, dtype=torch.uint8, device=DEV)
+            moe4.moe4_convert(1, v, n, out)
+            torch.cuda.synchronize()
+            assert first_mismatch(to_np(out), oracle.e4m3_range(start, n)) is None
+
+
+def test_device_conversions_strided_all_patterns():
+    bits = np.arange(0, 1 << 32, 4099, dtype=np.uint64).astype(np.uint32)
+    v = bits.view(np.float32)
+    v = v[np.isfinite(v)]
+    v = v[: v.size // 4 * 4]
+    vd = to_dev(v)
+    for kind, ref in [(0, oracle.e2m1_rne_sat(v)), (1, oracle.e4m3_rne_sat(v))]:
+        out = torch.empty(v.size, dtype=torch.uint8, device=DEV)
+        moe4.moe4_convert(kind, vd, v.size, out)
+        torch.cuda.synchronize()
+        assert first_mismatch(to_np(out), ref) is None, kind
+    out = torch.empty(v.size, dtype=torch.int16, device=DEV)
+    moe4.moe4_convert(2, vd, v.size, out)
+    torch.cuda.synchronize()
+    assert first_mismatch(to_np(out, np.uint16), oracle.f32_to_bf16(v)) is None
+
+
+def test_device_stochastic_rounding_and_words():
+    rng = np.random.default_rng(9)
+    n = 1 << 20
+    v = (rng.standard_normal(n) * np.exp2(rng.integers(-14, 8, n))).astype(np.float32)
+    v = np.clip(v, -448, 448).astype(np.float32)
+    out = torch.empty(n, dtype=torch.uint8, device=DEV)
+    moe4.moe4_convert(3, to_dev(v), n, out)
+    words = torch.empty(n, dtype=torch.int32, device=DEV)
+    moe4.moe4_sr_words(0x0123456789ABCDEF, 5, 1 << 33, n, words)
+    torch.cuda.synchronize()
+    ref_words0 = oracle.sr_words(0, 0, 0, n)
+    assert first_mismatch(to_np(out), oracle.e4m3_sr(v, ref_words0)) is None
+    assert first_mismatch(to_np(words, np.uint32), oracle.sr_words(0x0123456789ABCDEF, 5, 1 << 33, n)) is None

@@ -1,0 +1,111 @@
+"""GPU parity of the MXFP8 requantise-transpose with stochastic rounding and of the MXFP8
+quantiser of bf16 tensors, against the oracle, bit for bit ("4-bit computation from the start of
+Inkling 2 Small's pretraining", lhc.media, backward-pass paragraphs).
+
+Cases: several tiles with ragged edges (rows not a multiple of 128, columns not a multiple of 64),
+batched matrices with one global random index, SR and nearest-even, several seeds and stream ids;
+the backward-requant workload's full-size X [32768, 4096] (sampled output rows recomputed by the
+oracle with the same global indices) and the SR unbiasedness check over seeds 0..15.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_moe_numerics_03_b300 import inputs, moe4
+from gpu_helpers import DEV, empty_u8, first_mismatch, nvfp4_quantize, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _requant_gpu(c, s, g, nmat, rows, cols, seed, sid, sr):
+    q = empty_u8(nmat, cols, rows)
+    e8 = empty_u8(nmat, cols, rows // 32)
+    moe4.mxfp8_requant_transpose_sr(c, s, g, nmat, rows, cols, q, e8, seed, sid, moe4.SR if sr else 0)
+    torch.cuda.synchronize()
+    return q, e8
+
+
+@pytest.mark.parametrize("shape", [(1, 32, 32), (1, 96, 96), (2, 160, 192), (3, 256, 512)])
+@pytest.mark.parametrize("sr,seed,sid", [(True, 0, 0), (True, 12345, 7), (False, 0, 0)])
+def test_requant_small(shape, sr, seed, sid):
+    nmat, rows, cols = shape
+    rng = np.random.default_rng(rows + cols + nmat)
+    x = inputs.to_bf16_bits(rng.standard_t(3, (nmat * rows, cols)).astype(np.float32))
+    c, s, g = nvfp4_quantize(to_dev(x), nmat, rows, cols)
+    q, e8 = _requant_gpu(c, s, g, nmat, rows, cols, seed, sid, sr)
+    oc, os_, og = oracle.nvfp4_quantize(oracle.bf16_to_f32(x).reshape(nmat, rows, cols))
+    rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=sr, seed=seed, stream_id=sid)
+    assert first_mismatch(to_np(e8), re8) is None
+    assert first_mismatch(to_np(q), rq) is None
+
+
+def test_requant_single_expert_operands():
+    rng = inputs.host_rng(1, 0)
+    x = inputs.to_bf16_bits(inputs.host_outliers(rng, inputs.host_normal(rng, (256, 512))))
+    w = inputs.to_bf16_bits(inputs.host_normal(inputs.host_rng(1, 1), (256, 512), 0.02))
+    for t, sid in ((x, 0), (w, 1)):
+        c, s, g = nvfp4_quantize(to_dev(t), 1, 256, 512)
+        q, e8 = _requant_gpu(c, s, g, 1, 256, 512, 0, sid, True)
+        oc, os_, og = oracle.nvfp4_quantize(oracle.bf16_to_f32(t))
+        rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=True, seed=0, stream_id=sid)
+        assert first_mismatch(to_np(q), rq) is None and first_mismatch(to_np(e8), re8) is None
+
+
+def test_requant_full_size_x_sampled_output_rows():
+    rows, cols = 32768, 4096
+    x = inputs.device_student_t((rows, cols), inputs.device_generator(4, 0, DEV), DEV).view(torch.int16)
+    c, s, g = nvfp4_quantize(x, 1, rows, cols)
+    seed, sid = 3, 2
+    q, e8 = _requant_gpu(c, s, g, 1, rows, cols, seed, sid, True)
+    qn, e8n = to_np(q)[0], to_np(e8)[0]
+    x32 = oracle.bf16_to_f32(to_np(x, np.uint16))
+    amax = np.abs(x32).max()
+    for c0 in [0, 1024, 4064]:                 # 32 output rows starting at c0
+        # the oracle quantises the 32 input columns itself (16-blocks never straddle the slice)
+        codes, scl, gd = oracle.nvfp4_quantize(np.ascontiguousarray(x32[:, c0:c0 + 32]), amax=amax)
+        xh = oracle.nvfp4_dequantize(codes, scl, gd)               # [rows, 32]
+        rq, re8 = oracle.mxfp8_quantize_rows(np.ascontiguousarray(xh.T), sr=True, seed=seed, stream_id=sid,
+                                             idx_base=c0 * rows)
+        assert first_mismatch(qn[c0:c0 + 32], rq) is None
+        assert first_mismatch(e8n[c0:c0 + 32], re8) is None
+
+
+def test_sr_unbiased_over_seeds_on_device():
+    rows, cols = 1024, 512
+    x = inputs.to_bf16_bits(np.random.default_rng(8).standard_t(3, (rows, cols)).astype(np.float32))
+    c, s, g = nvfp4_quantize(to_dev(x), 1, rows, cols)
+    xh = oracle.nvfp4_dequantize(*oracle.nvfp4_quantize(oracle.bf16_to_f32(x))).T.astype(np.float64)
+    acc = np.zeros_like(xh)
+    for seed in range(16):
+        q, e8 = _requant_gpu(c, s, g, 1, rows, cols, seed, 0, True)
+        acc += oracle.mxfp8_dequantize(to_np(q)[0], to_np(e8)[0])
+    mean = acc / 16
+    _, er = oracle.mxfp8_requant_transpose(*oracle.nvfp4_quantize(oracle.bf16_to_f32(x)), sr=False)
+    scale = np.repeat(np.exp2(er.astype(np.float64) - 127), 32, axis=1)
+    grid = oracle.e4m3_value(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    v = np.abs(xh) / scale
+    lo = np.clip(np.searchsorted(grid, v, side="right") - 1, 0, 125)
+    ulp = (grid[lo + 1] - grid[lo]) * scale
+    p = np.clip((np.abs(xh) - grid[lo] * scale) / ulp, 0, 1)
+    sd = ulp * np.sqrt(p * (1 - p) / 16)
+    live = sd > 0
+    z = ((mean - xh)[live] / sd[live]).sum() / np.sqrt(live.sum())
+    assert abs(z) < 5, z
+
+
+@pytest.mark.parametrize("layout", ["row", "col"])
+@pytest.mark.parametrize("sr", [False, True])
+def test_mxfp8_quantize(layout, sr):
+    rows, cols = 320, 192
+    rng = np.random.default_rng(11)
+    x = inputs.to_bf16_bits((rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-6, 6, (rows, 1))))
+                            .astype(np.float32))
+    shape_q = (rows, cols) if layout == "row" else (cols, rows)
+    q = empty_u8(*shape_q)
+    e8 = empty_u8(shape_q[0], shape_q[1] // 32)
+    flags = (moe4.ROWWISE if layout == "row" else moe4.COLWISE) | (moe4.SR if sr else 0)
+    moe4.mxfp8_quantize(to_dev(x), rows, cols, q, e8, 77, 4, flags)
+    torch.cuda.synchronize()
+    rq, re8 = oracle.mxfp8_quantize(oracle.bf16_to_f32(x), colwise=(layout == "col"), sr=sr, seed=77, stream_id=4)
+    assert first_mismatch(to_np(q), rq) is None and first_mismatch(to_np(e8), re8) is None
