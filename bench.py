@@ -1,0 +1,597 @@
+#!/usr/bin/env python
+"""Benchmark of the 4-bit MoE expert-layer step on B300.
+
+One step = one pass of the whole hot path over one batch of the Inkling-shaped layer (16384
+tokens, d_model 4096, SwiGLU width 2048, 384 experts, top-8 of N(0,1) logits plus a per-expert
+N(0,1) bias, Student-t(3) activations, N(0, 0.02) expert weights held as FP32 masters):
+
+  forward   top-k routing and dispatch plan; NVFP4 (Four Over Six) quantisation of X, of every
+            expert's gate/up and down weights (per-expert scales) and of H; NVFP4 row gather;
+            grouped NVFP4 GEMMs (gate/up, then down) with SwiGLU between them; Hadamard(128) NVFP4
+            return-path encode + decode; weighted combine;
+  backward  combine gradient; MXFP8 quantisation of dY and dGU (row-wise and transposed);
+            dequantise -> transpose -> MXFP8 requantisation with Philox stochastic rounding of
+            W_down, H, W_gate/up and X; grouped MXFP8 dgrad (row-grouped) and wgrad
+            (contraction-grouped) GEMMs for both projections; SwiGLU backward; SGD on the FP32
+            master weights (which writes the bf16 copies the next step quantises).
+
+`value` is expert-GEMM TFLOP/s of the whole step: the algorithmic FLOPs of the six expert GEMMs
+(routed rows only) divided by the device time of the step.  The JSON line also carries per-kernel
+times, the requantisation GB/s, the roofline of the dominant kernel, clocks, the end-to-end
+number through the C ABI with host buffers, and the CPU oracle's rate on a bounded sample.
+
+`--impl reference` times the oracle (the plain CPU definition of the method) on a bounded sample
+of the same workload: one expert with one 128-row tile of routed tokens, through every step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+T_TOK, D_MODEL, D_FF, N_EXP, TOP_K = 16384, 4096, 2048, 384, 8
+WORKLOAD = "inkling-moe-layer-step: T=16384 d=4096 f=2048 E=384 top8, NVFP4 fwd + MXFP8 bwd + SGD"
+SMALL = dict(T=4096, d=2048, f=1024, E=8, k=2)
+METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
+LR = 1e-3
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"], src="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------------------------
+# the device step
+# ---------------------------------------------------------------------------------------------
+class LayerStep:
+    """All device buffers of one layer step and the sequence of library calls."""
+
+    def __init__(self, T, d, f, E, k, device, seed_workload=5):
+        import torch
+        from precision_moe_numerics_03_b300 import inputs, moe4
+        self.torch, self.m = torch, moe4
+        self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
+        self.dev = device
+        dev = device
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.rows_cap = (T * k + 127 * E + 127) // 128 * 128
+        R = self.rows_cap
+        g = lambda s: inputs.device_generator(seed_workload, s, dev)
+        # inputs of a step
+        self.X = inputs.device_student_t((T, d), g(0), dev).view(torch.int16)
+        lg = torch.randn((T, E), generator=g(1), device=dev)
+        bias = torch.randn((E,), generator=g(2), device=dev)
+        self.logits = (lg + bias).contiguous()
+        self.dy = inputs.device_normal((T, d), 1.0, g(3), dev).view(torch.int16)
+        # FP32 master weights and their bf16 copies
+        self.W32_gu = torch.randn((E, 2 * f, d), generator=g(4), device=dev).mul_(0.02)
+        self.W32_d = torch.randn((E, d, f), generator=g(5), device=dev).mul_(0.02)
+        self.Wb_gu = self.W32_gu.to(torch.bfloat16).view(torch.int16)
+        self.Wb_d = self.W32_d.to(torch.bfloat16).view(torch.int16)
+        # routing
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.src_of = torch.empty(R, dtype=torch.int32, device=dev)
+        self.plan_ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E), dev)
+        self.qws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, E), dev)
+        self.hws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT), dev)
+        # forward tensors
+        self.Xq_c, self.Xq_s = torch.empty((T, d // 2), **u8), torch.empty((T, d // 16), **u8)
+        self.Xq_g = torch.empty(1, dtype=torch.float32, device=dev)
+        self.Xp_c, self.Xp_s = torch.empty((R, d // 2), **u8), torch.empty((R, d // 16), **u8)
+        self.Wgu_c, self.Wgu_s = torch.empty((E, 2 * f, d // 2), **u8), torch.empty((E, 2 * f, d // 16), **u8)
+        self.Wgu_g = torch.empty(E, dtype=torch.float32, device=dev)
+        self.Wd_c, self.Wd_s = torch.empty((E, d, f // 2), **u8), torch.empty((E, d, f // 16), **u8)
+        self.Wd_g = torch.empty(E, dtype=torch.float32, device=dev)
+        self.GU = torch.empty((R, 2 * f), dtype=torch.float32, device=dev)
+        self.H = torch.empty((R, f), dtype=torch.int16, device=dev)
+        self.Hq_c, self.Hq_s = torch.empty((R, f // 2), **u8), torch.empty((R, f // 16), **u8)
+        self.Hq_g = torch.empty(1, dtype=torch.float32, device=dev)
+        self.Y = torch.empty((R, d), dtype=torch.int16, device=dev)
+        self.Yc_c, self.Yc_s = torch.empty((R, d // 2), **u8), torch.empty((R, d // 16), **u8)
+        self.Yc_g = torch.empty(1, dtype=torch.float32, device=dev)
+        self.Yhat = torch.empty((R, d), dtype=torch.int16, device=dev)
+        self.y = torch.empty((T, d), dtype=torch.int16, device=dev)
+        # backward tensors
+        self.dYp = torch.empty((R, d), dtype=torch.int16, device=dev)
+        self.dYr_q, self.dYr_e = torch.empty((R, d), **u8), torch.empty((R, d // 32), **u8)
+        self.dYc_q, self.dYc_e = torch.empty(d * R, **u8), torch.empty(d * R // 32, **u8)
+        self.WdT_q, self.WdT_e = torch.empty((E, f, d), **u8), torch.empty((E, f, d // 32), **u8)
+        self.HqT_q, self.HqT_e = torch.empty(f * R, **u8), torch.empty(f * R // 32, **u8)
+        self.dH = torch.empty((R, f), dtype=torch.float32, device=dev)
+        self.dWd = torch.empty((E, d, f), dtype=torch.float32, device=dev)
+        self.dGU = torch.empty((R, 2 * f), dtype=torch.int16, device=dev)
+        self.dGUr_q, self.dGUr_e = torch.empty((R, 2 * f), **u8), torch.empty((R, 2 * f // 32), **u8)
+        self.dGUc_q, self.dGUc_e = torch.empty(2 * f * R, **u8), torch.empty(2 * f * R // 32, **u8)
+        self.WguT_q, self.WguT_e = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
+        self.XpT_q, self.XpT_e = torch.empty(d * R, **u8), torch.empty(d * R // 32, **u8)
+        self.dXp = torch.empty((R, d), dtype=torch.int16, device=dev)
+        self.dWgu = torch.empty((E, 2 * f, d), dtype=torch.float32, device=dev)
+        # scratch for the GEMMs' scale-layout change (largest call)
+        wsz = max(moe4.moe4_workspace_size_gemm(1, R, E, f, d), moe4.moe4_workspace_size_gemm(1, R, E, d, 2 * f),
+                  moe4.moe4_workspace_size_gemm(1, d, 1, f, R), moe4.moe4_workspace_size_gemm(1, 2 * f, 1, d, R))
+        self.gws = moe4.workspace(wsz, dev)
+        self.Rp = None
+        self.launches = 0
+        self.step_index = 0
+
+    # algorithmic FLOPs of the six expert GEMMs (routed rows only)
+    def gemm_flops(self):
+        rows = self.T * self.k
+        fwd = 2 * rows * (2 * self.f) * self.d + 2 * rows * self.d * self.f
+        return fwd, 2 * fwd
+
+    def run(self, timer=None):
+        m, torch = self.m, self.torch
+        T, d, f, E, k = self.T, self.d, self.f, self.E, self.k
+        FOS, MMA = m.FOUR_OVER_SIX, m.SF_MMA_LAYOUT
+        tm = timer if timer is not None else _NullTimer()
+        n = 0
+        seed = 1000 + self.step_index
+        self.step_index += 1
+        # ---------------- forward
+        with tm("route"):
+            m.moe4_route_topk(self.logits, T, E, k, self.idx, self.w)
+            m.moe4_permute_plan(self.idx, T, k, E, self.offs, self.row_of, self.src_of, self.rows_cap, self.plan_ws)
+        n += 4
+        Rp = int(self.offs[E].item())          # host needs the padded row count (one 4-byte read)
+        self.Rp = Rp
+        with tm("quant_x"):
+            m.nvfp4_quantize(self.X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
+            m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
+        n += 3
+        with tm("quant_w"):
+            m.nvfp4_quantize(self.Wb_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, None, FOS | MMA, self.qws)
+            m.nvfp4_quantize(self.Wb_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, None, FOS | MMA, self.qws)
+        n += 4
+        with tm("gemm_nvfp4"):
+            m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
+                                        E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
+        n += 1
+        with tm("swiglu_quant_h"):
+            m.moe4_swiglu(self.GU[:Rp], Rp, f, self.H[:Rp])
+            m.nvfp4_quantize(self.H[:Rp], 1, Rp, f, f, self.Hq_c, self.Hq_s, self.Hq_g, None, FOS | MMA, self.qws)
+        n += 3
+        with tm("gemm_nvfp4"):
+            m.grouped_expert_gemm_nvfp4(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s, self.Wd_g, self.offs,
+                                        E, Rp, d, f, self.Y, m.OUT_BF16 | MMA)
+        n += 1
+        with tm("hadamard"):
+            m.hadamard_quant(self.Y[:Rp], Rp, d, self.Yc_c, self.Yc_s, self.Yc_g, FOS, self.hws)
+            m.hadamard_dequant(self.Yc_c, self.Yc_s, self.Yc_g, Rp, d, self.Yhat[:Rp])
+        n += 3
+        with tm("combine"):
+            m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, self.y)
+        n += 1
+        # ---------------- backward
+        with tm("mxfp8_quant"):
+            m.moe4_combine_backward(self.dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYp[:Rp])
+            m.mxfp8_quantize(self.dYp[:Rp], Rp, d, self.dYr_q, self.dYr_e, 0, 0, m.ROWWISE)
+            m.mxfp8_quantize(self.dYp[:Rp], Rp, d, self.dYc_q, self.dYc_e, 0, 0, m.COLWISE)
+        n += 3
+        with tm("requant"):
+            m.mxfp8_requant_transpose_sr(self.Wd_c, self.Wd_s, self.Wd_g, E, d, f, self.WdT_q, self.WdT_e, seed, 1,
+                                         m.SR | MMA)
+            m.mxfp8_requant_transpose_sr(self.Hq_c, self.Hq_s, self.Hq_g, 1, Rp, f, self.HqT_q, self.HqT_e, seed, 2,
+                                         m.SR | MMA)
+        n += 2
+        with tm("gemm_mxfp8"):
+            m.grouped_gemm_mxfp8(self.dYr_q, self.dYr_e, self.WdT_q, self.WdT_e, self.offs, E, Rp, f, d, self.dH,
+                                 m.OUT_F32 | m.GROUP_M, self.gws)
+            m.grouped_gemm_mxfp8(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp, self.dWd,
+                                 m.OUT_F32 | m.GROUP_K, self.gws)
+        n += 6
+        with tm("swiglu_bwd"):
+            m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
+        n += 1
+        with tm("mxfp8_quant"):
+            m.mxfp8_quantize(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, 0, 0, m.ROWWISE)
+            m.mxfp8_quantize(self.dGU[:Rp], Rp, 2 * f, self.dGUc_q, self.dGUc_e, 0, 0, m.COLWISE)
+        n += 2
+        with tm("requant"):
+            m.mxfp8_requant_transpose_sr(self.Wgu_c, self.Wgu_s, self.Wgu_g, E, 2 * f, d, self.WguT_q, self.WguT_e,
+                                         seed, 3, m.SR | MMA)
+            m.mxfp8_requant_transpose_sr(self.Xp_c, self.Xp_s, self.Xq_g, 1, Rp, d, self.XpT_q, self.XpT_e, seed, 4,
+                                         m.SR | MMA)
+        n += 2
+        with tm("gemm_mxfp8"):
+            m.grouped_gemm_mxfp8(self.dGUr_q, self.dGUr_e, self.WguT_q, self.WguT_e, self.offs, E, Rp, d, 2 * f,
+                                 self.dXp, m.OUT_BF16 | m.GROUP_M, self.gws)
+            m.grouped_gemm_mxfp8(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d, Rp,
+                                 self.dWgu, m.OUT_F32 | m.GROUP_K, self.gws)
+        n += 6
+        with tm("sgd"):
+            m.moe4_sgd_update(self.W32_gu, self.dWgu, self.W32_gu.numel(), LR, self.Wb_gu)
+            m.moe4_sgd_update(self.W32_d, self.dWd, self.W32_d.numel(), LR, self.Wb_d)
+        n += 2
+        self.launches += n
+        return n
+
+    # algorithmic HBM bytes of the kernel groups (per step), for the roofline
+    def group_bytes(self):
+        T, d, f, E, k = self.T, self.d, self.f, self.E, self.k
+        rows = T * k
+        offs = self.offs.cpu().numpy()
+        live = int(np.count_nonzero(np.diff(offs)))
+        nv = 0.5625       # NVFP4 bytes per value (codes + E4M3 scale per 16)
+        mx = 1.03125      # MXFP8 bytes per value (E4M3 + E8M0 per 32)
+        w_gu, w_d = E * 2 * f * d, E * d * f
+        b = {}
+        b["quant_w"] = (w_gu + w_d) * (2 + 2 + nv)                       # amax pass, quant pass, output
+        b["quant_x"] = T * d * (2 + 2 + nv) + rows * d * nv * 2          # + gather read/write
+        b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
+                           rows * f * nv + live * d * f * nv + rows * d * 2)
+        b["requant"] = (w_gu + w_d + rows * (f + d)) * (nv + mx)
+        b["mxfp8_quant"] = rows * d * (2 + 2 + 2 * mx) + T * d * 2 + rows * 2 * f * (2 * 2 + 2 * mx)
+        b["gemm_mxfp8"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +           # dgrad down
+                           rows * d * mx + rows * f * mx + E * d * f * 4 +              # wgrad down
+                           rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2 +   # dgrad gate/up
+                           rows * 2 * f * mx + rows * d * mx + E * 2 * f * d * 4)       # wgrad gate/up
+        b["sgd"] = (w_gu + w_d) * (4 + 4 + 4 + 2)
+        b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 * 2 + rows * f * (2 + nv)
+        b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
+        b["hadamard"] = rows * d * (2 + 2 + nv + nv + 2)
+        b["combine"] = rows * d * 2 + T * d * 2
+        b["route"] = T * E * 4 + rows * 4 * 4
+        return b
+
+
+class _NullTimer:
+    def __call__(self, name):
+        return self
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+class EventTimer:
+    """CUDA events on the launching stream around each named group of calls."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.records = []
+
+    def __call__(self, name):
+        self._name = name
+        return self
+
+    def __enter__(self):
+        s = self.torch.cuda.Event(enable_timing=True)
+        s.record()
+        self._start = s
+        return self
+
+    def __exit__(self, *a):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.records.append((self._name, self._start, e))
+        return False
+
+    def totals(self):
+        out = {}
+        for name, s, e in self.records:
+            out[name] = out.get(name, 0.0) + s.elapsed_time(e)
+        return out
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------------------------
+def oracle_sample_step(d=D_MODEL, f=D_FF, rows=128, seed=0):
+    """One expert, one 128-row tile of routed tokens, every step of the method on the oracle.
+    Returns (expert-GEMM FLOPs, seconds)."""
+    import oracle
+    from precision_moe_numerics_03_b300 import inputs
+    rng = inputs.host_rng(5, 100 + seed)
+    x = inputs.to_bf16_bits(inputs.host_student_t(rng, (rows, d)))
+    w_gu = rng.standard_normal((2 * f, d), dtype=np.float32) * np.float32(0.02)
+    w_d = rng.standard_normal((d, f), dtype=np.float32) * np.float32(0.02)
+    dy = inputs.to_bf16_bits(inputs.host_normal(rng, (rows, d)))
+    t0 = time.perf_counter()
+    o = oracle
+    wb_gu, wb_d = o.bf16_to_f32(o.f32_to_bf16(w_gu)), o.bf16_to_f32(o.f32_to_bf16(w_d))
+    xq = o.nvfp4_quantize(o.bf16_to_f32(x))
+    gq = o.nvfp4_quantize(wb_gu)
+    dq = o.nvfp4_quantize(wb_d)
+    offs = np.array([0, rows])
+    xh, gh, dh_ = o.nvfp4_dequantize(*xq), o.nvfp4_dequantize(*gq), o.nvfp4_dequantize(*dq)
+    gu, _ = o.grouped_gemm_m(xh, gh[None], offs)
+    h = o.swiglu(gu)
+    hq = o.nvfp4_quantize(o.bf16_to_f32(o.f32_to_bf16(h)))
+    y, _ = o.grouped_gemm_m(o.nvfp4_dequantize(*hq), dh_[None], offs)
+    yc = o.hadamard_quant(o.bf16_to_f32(o.f32_to_bf16(y.astype(np.float32))))
+    o.hadamard_dequant(*yc)
+    dyf = o.bf16_to_f32(dy)
+    dyr = o.mxfp8_dequantize(*o.mxfp8_quantize(dyf, colwise=False))
+    dyc = o.mxfp8_dequantize(*o.mxfp8_quantize(dyf, colwise=True))
+    wdT = o.mxfp8_dequantize(*o.mxfp8_requant_transpose(*dq, sr=True, seed=seed, stream_id=1))
+    hT = o.mxfp8_dequantize(*o.mxfp8_requant_transpose(*hq, sr=True, seed=seed, stream_id=2))
+    dH, _ = o.grouped_gemm_m(dyr, wdT[None], offs)
+    dWd, _ = o.grouped_gemm_k(dyc, hT, offs)
+    dgu = o.bf16_to_f32(o.f32_to_bf16(o.swiglu_backward(gu.astype(np.float32), dH.astype(np.float32))))
+    dgur = o.mxfp8_dequantize(*o.mxfp8_quantize(dgu, colwise=False))
+    dguc = o.mxfp8_dequantize(*o.mxfp8_quantize(dgu, colwise=True))
+    wguT = o.mxfp8_dequantize(*o.mxfp8_requant_transpose(*gq, sr=True, seed=seed, stream_id=3))
+    xT = o.mxfp8_dequantize(*o.mxfp8_requant_transpose(*xq, sr=True, seed=seed, stream_id=4))
+    o.grouped_gemm_m(dgur, wguT[None], offs)
+    dWgu, _ = o.grouped_gemm_k(dguc, xT, offs)
+    o.sgd_update(w_gu, dWgu[0].astype(np.float32), LR)
+    o.sgd_update(w_d, dWd[0].astype(np.float32), LR)
+    secs = time.perf_counter() - t0
+    fwd = 2 * rows * 2 * f * d + 2 * rows * d * f
+    return 3 * fwd, secs
+
+
+def cpu_cores_used():
+    import torch
+    return max(1, torch.get_num_threads())
+
+
+# ---------------------------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    flops, secs = 0, 0.0
+    for i in range(args.warmup):
+        oracle_sample_step(seed=i)
+    for i in range(args.steps):
+        fl, s = oracle_sample_step(seed=100 + i)
+        flops += fl
+        secs += s
+    value = flops / secs / 1e12
+    sample = "one expert (gate/up 4096x4096, down 4096x2048 weights) and one 128-row tile of routed tokens per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 GEMM / f32 quantisers",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--small", action="store_true", help="the small 8-expert shapes (a quick check, not a bench line)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+    from precision_moe_numerics_03_b300 import moe4
+    moe4.load()
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    if args.small:
+        step = LayerStep(SMALL["T"], SMALL["d"], SMALL["f"], SMALL["E"], SMALL["k"], dev)
+    else:
+        step = LayerStep(T_TOK, D_MODEL, D_FF, N_EXP, TOP_K, dev)
+    torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    if moe4.moe4_get_status() != moe4.OK:
+        raise RuntimeError("a device wait timed out during warm-up")
+
+    # ------------------------------------------------ timed region (device)
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    timer = EventTimer(torch)
+    launches = 0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        launches += step.run(timer)
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if moe4.moe4_get_status() != moe4.OK:
+        raise RuntimeError("a device wait timed out in the timed region")
+    if dist is not None:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms = elapsed_ms / args.steps
+    fwd_flops, bwd_flops = step.gemm_flops()
+    step_flops = fwd_flops + bwd_flops
+    value = world * step_flops * args.steps / (elapsed_ms / 1e3) / 1e12
+
+    # per-kernel-group times (ms per step) and the roofline of the dominant group
+    peaks = load_peaks()
+    per = {k: v / args.steps for k, v in timer.totals().items()}
+    gbytes = step.group_bytes()
+    comps = {}
+    for name, t in sorted(per.items(), key=lambda kv: -kv[1]):
+        entry = {"ms": round(t, 4), "share": round(t / ms, 4)}
+        if name in gbytes:
+            entry["GB/s"] = round(gbytes[name] / (t / 1e3) / 1e9, 1)
+        comps[name] = entry
+    comps["gemm_nvfp4"]["TFLOP/s"] = round(fwd_flops / (per["gemm_nvfp4"] / 1e3) / 1e12, 1)
+    comps["gemm_mxfp8"]["TFLOP/s"] = round(bwd_flops / (per["gemm_mxfp8"] / 1e3) / 1e12, 1)
+    fp4_peak = peaks["bf16_sus"] * 6.0     # nominal FP4 / BF16 ratio (13.5 / 2.25)
+    fp8_peak = peaks["bf16_sus"] * 2.0
+    dom = max(per, key=per.get)
+    t_dom = per[dom]
+    flops_dom = {"gemm_nvfp4": (fwd_flops, fp4_peak), "gemm_mxfp8": (bwd_flops, fp8_peak)}.get(dom)
+    if flops_dom is not None and flops_dom[0] / flops_dom[1] / 1e12 > gbytes[dom] / peaks["hbm"] / 1e9:
+        ach = flops_dom[0] / (t_dom / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": flops_dom[1], "unit": "TFLOP/s",
+                "frac": ach / flops_dom[1], "traffic": None, "kernel": dom}
+    else:
+        ach = gbytes[dom] / (t_dom / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
+                "traffic": None, "kernel": dom}
+    roof["peak_source"] = peaks["src"]
+    req_t = per.get("requant", 0.0)
+    requant_gbs = gbytes["requant"] / (req_t / 1e3) / 1e9 if req_t else None
+
+    # ------------------------------------------------ end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hX = torch.empty(step.X.shape, dtype=step.X.dtype, pin_memory=True)
+        hX.copy_(step.X)
+        hL = torch.empty(step.logits.shape, dtype=step.logits.dtype, pin_memory=True)
+        hL.copy_(step.logits)
+        hD = torch.empty(step.dy.shape, dtype=step.dy.dtype, pin_memory=True)
+        hD.copy_(step.dy)
+        hY = torch.empty(step.y.shape, dtype=step.y.dtype, pin_memory=True)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step.X.copy_(hX, non_blocking=True)
+            step.logits.copy_(hL, non_blocking=True)
+            step.dy.copy_(hD, non_blocking=True)
+            step.run()
+            hY.copy_(step.y, non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        if dist is not None:
+            tt = torch.tensor([e2e_s], dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        h2d = hX.numel() * 2 + hL.numel() * 4 + hD.numel() * 2
+        d2h = hY.numel() * 2 + 4
+        e2e = {"value": world * step_flops * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s / args.steps * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, secs = oracle_sample_step(seed=0)
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": "one expert (gate/up 4096x4096, down 4096x2048 weights) and one 128-row tile of routed "
+                         "tokens through every step", "seconds": round(secs, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4/mxfp8 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": WORKLOAD if not args.small else "small-moe-step", "tokens": step.T,
+                       "d_model": step.d, "d_ff": step.f, "experts": step.E, "top_k": step.k,
+                       "rows_padded": step.Rp, "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (126 MB): no flush needed"},
+            "requant_GBps": requant_gbs, "requant_frac_hbm": requant_gbs / peaks["hbm"] if requant_gbs else None,
+            "nvfp4_gemm_TFLOPs": comps["gemm_nvfp4"]["TFLOP/s"],
+            "nvfp4_gemm_frac_fp4_peak": comps["gemm_nvfp4"]["TFLOP/s"] / fp4_peak,
+            "components": comps,
+            "roofline": roof,
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -78,7 +78,6 @@ const char *moe4_status_string(int status);  /* static string, never NULL */
 #define MOE4_OP_NVFP4_QUANTIZE   1 /* a = nmat */
 #define MOE4_OP_HADAMARD_QUANT   2 /* no arguments */
 #define MOE4_OP_PERMUTE_PLAN     3 /* a = tokens, b = top_k, c = experts */
-#define MOE4_OP_GEMM_NVFP4       4 /* a = rows of A, b = N (rows of B per group), c = K, with E via moe4_workspace_size_gemm */
 size_t moe4_workspace_size(int op, int64_t a, int64_t b, int64_t c);
 /* Scratch for the grouped GEMMs when their scale factors come in the canonical layout:
  * kind 0 = NVFP4 (16-blocks), 1 = MXFP8 (32-blocks); a_rows x K for A, E x b_rows x K for B. */
@@ -119,7 +118,8 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec
  * stream_id, 0), key = (lo(seed), hi(seed))) and rounds the magnitude up iff
  * word < floor(frac * 2^32), frac being its distance above the E4M3 value below, in units of
  * the gap.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
- * rows % 32 == 0, cols % 32 == 0.  Canonical input sf only. */
+ * rows % 32 == 0, cols % 32 == 0.  Input scales canonical, or in the tensor-core tile layout with
+ * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0). */
 int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const float *g_dec,
                                int64_t nmat, int64_t rows, int64_t cols, uint8_t *q_t,
                                uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,
@@ -199,14 +199,29 @@ int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64_t E, int32
 
 /* moe4_permute_nvfp4: gather NVFP4 rows: out row r = input row src_of[r], or zeros (codes 0,
  * scale 0) when src_of[r] < 0; r < rows_total.  codes [T, cols/2], sf [T, cols/16] canonical;
- * cols % 32 == 0. */
+ * cols % 32 == 0.  With MOE4_SF_MMA_LAYOUT the output scales are written in the tensor-core tile
+ * layout (rows_total % 128 == 0, cols % 64 == 0). */
 int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64_t T, int64_t cols,
                        const int32_t *src_of, int64_t rows_total, uint8_t *out_codes,
-                       uint8_t *out_sf, void *stream);
+                       uint8_t *out_sf, uint32_t flags, void *stream);
 
 /* moe4_swiglu: gu f32 [rows, 2f] -> h bf16 [rows, f], h = g/(1+exp(-g)) * u with g the first f
  * columns and u the last f (binary32, then nearest-even to bf16).  f % 4 == 0. */
 int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h, void *stream);
+
+/* moe4_swiglu_backward: gu f32 [rows, 2f] (the forward's gate | up), dh f32 [rows, f] ->
+ * dgu bf16 [rows, 2f]: dg = dh * u * s * (1 + g * (1 - s)), du = dh * g * s with
+ * s = 1/(1+exp(-g)), binary32 then nearest-even to bf16.  f % 4 == 0. */
+int moe4_swiglu_backward(const float *gu, const float *dh, int64_t rows, int64_t f, uint16_t *dgu,
+                         void *stream);
+
+/* moe4_combine_backward: the gradient of the combine with respect to the returned rows:
+ * dyhat[row_of[t,j]] = bf16(w[t,j] * dy[t]) (one binary32 product per value), and zero rows for
+ * padding (src_of < 0).  dy bf16 [T, d], dyhat bf16 [rows_total, d]; d % 8 == 0, k <= 32.  The
+ * Hadamard return-path codec is passed straight through. */
+int moe4_combine_backward(const uint16_t *dy, const int32_t *row_of, const float *w,
+                          const int32_t *src_of, int64_t T, int64_t k, int64_t d,
+                          int64_t rows_total, uint16_t *dyhat, void *stream);
 
 /* moe4_combine: y bf16 [T, d], y[t] = sum over slots j in order of w[t,j] * yhat[row_of[t,j]]:
  * one binary32 product and one binary32 add per slot from 0, then nearest-even to bf16.

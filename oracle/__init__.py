@@ -408,6 +408,29 @@ def swiglu(gu: np.ndarray) -> np.ndarray:
     return (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
 
 
+def swiglu_backward(gu: np.ndarray, dh: np.ndarray) -> np.ndarray:
+    """Gradient of h = silu(g) * u: dg = dh * u * s * (1 + g * (1 - s)), du = dh * g * s with
+    s = 1/(1+exp(-g)); float64, returned as binary32 [rows, 2f] (gate | up)."""
+    gu = np.asarray(gu, np.float64)
+    dh = np.asarray(dh, np.float64)
+    f = gu.shape[1] // 2
+    g, u = gu[:, :f], gu[:, f:]
+    s = 1.0 / (1.0 + np.exp(-g))
+    dg = dh * u * s * (1.0 + g * (1.0 - s))
+    du = dh * g * s
+    return np.concatenate([dg, du], axis=1).astype(np.float32)
+
+
+def combine_backward(dy_bf16: np.ndarray, row_of: np.ndarray, w: np.ndarray, rows_total: int) -> np.ndarray:
+    """dyhat[row_of[t, j]] = bf16(w[t, j] * dy[t]), one binary32 product per value; other rows 0."""
+    dy = bf16_to_f32(dy_bf16)
+    T, k = row_of.shape
+    out = np.zeros((rows_total, dy.shape[1]), np.uint16)
+    for j in range(k):
+        out[row_of[:, j]] = f32_to_bf16((w[:, j:j + 1].astype(np.float32) * dy).astype(np.float32))
+    return out
+
+
 def combine(yhat_bf16: np.ndarray, row_of: np.ndarray, w: np.ndarray) -> np.ndarray:
     """y[t] = sum over slots j in order of w[t, j] * yhat[row_of[t, j]]: one binary32 product and
     one binary32 add per slot, accumulator starting at 0; returned as bf16."""

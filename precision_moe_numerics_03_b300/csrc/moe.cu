@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(256) permute_nvfp4_kernel(const uint8_t *__res
                                                             const uint8_t *__restrict__ sf, int64_t cols,
                                                             const int32_t *__restrict__ src_of, int64_t rows_total,
                                                             uint8_t *__restrict__ out_codes,
-                                                            uint8_t *__restrict__ out_sf) {
+                                                            uint8_t *__restrict__ out_sf, bool sf_mma) {
     const int lane = lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t cbytes = cols / 2, sbytes = cols / 16;
@@ -157,7 +157,14 @@ __global__ void __launch_bounds__(256) permute_nvfp4_kernel(const uint8_t *__res
         uint4 *dc = reinterpret_cast<uint4 *>(out_codes + r * cbytes);
         const uint4 *sc = reinterpret_cast<const uint4 *>(codes + (int64_t)(src < 0 ? 0 : src) * cbytes);
         for (int64_t i = lane; i < cbytes / 16; i += 32) dc[i] = src < 0 ? make_uint4(0, 0, 0, 0) : __ldg(sc + i);
-        if (sbytes % 8 == 0) {
+        if (sf_mma) {
+            // 4 consecutive blocks of a row are one 32-bit word in both layouts
+            const uint32_t *ss = reinterpret_cast<const uint32_t *>(sf + (int64_t)(src < 0 ? 0 : src) * sbytes);
+            for (int64_t kg = lane; kg < sbytes / 4; kg += 32) {
+                const int64_t off = ((r >> 7) * (sbytes / 4) + kg) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+                *reinterpret_cast<uint32_t *>(out_sf + off) = src < 0 ? 0u : __ldg(ss + kg);
+            }
+        } else if (sbytes % 8 == 0) {
             uint2 *ds = reinterpret_cast<uint2 *>(out_sf + r * sbytes);
             const uint2 *ss = reinterpret_cast<const uint2 *>(sf + (int64_t)(src < 0 ? 0 : src) * sbytes);
             for (int64_t i = lane; i < sbytes / 8; i += 32) ds[i] = src < 0 ? make_uint2(0, 0) : __ldg(ss + i);
@@ -185,6 +192,69 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ g
             out[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(silu, us[i])) << (16 * (i & 1));
         }
         *reinterpret_cast<uint2 *>(h + r * f + c) = make_uint2(out[0], out[1]);
+    }
+}
+
+// ------------------------------------------------------------------ SwiGLU backward
+// h = silu(g) * u:  du = dh * silu(g),  dg = dh * u * s * (1 + g * (1 - s)) with s = 1/(1+exp(-g)).
+__global__ void __launch_bounds__(256) swiglu_bwd_kernel(const float *__restrict__ gu, const float *__restrict__ dh,
+                                                         int64_t rows, int64_t f, uint16_t *__restrict__ dgu) {
+    const int64_t quads = rows * f / 4;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = (q * 4) / f;
+        const int64_t c = q * 4 - r * f;
+        const float4 g = __ldg(reinterpret_cast<const float4 *>(gu + r * 2 * f + c));
+        const float4 u = __ldg(reinterpret_cast<const float4 *>(gu + r * 2 * f + f + c));
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(dh + r * f + c));
+        const float gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w}, ds[4] = {d.x, d.y, d.z, d.w};
+        uint32_t og[2] = {0, 0}, ou[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
+            const float silu = __fmul_rn(gs[i], sg);
+            const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
+            const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
+            const float duv = __fmul_rn(ds[i], silu);
+            og[i >> 1] |= (uint32_t)f32_to_bf16_bits(dgv) << (16 * (i & 1));
+            ou[i >> 1] |= (uint32_t)f32_to_bf16_bits(duv) << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint2 *>(dgu + r * 2 * f + c) = make_uint2(og[0], og[1]);
+        *reinterpret_cast<uint2 *>(dgu + r * 2 * f + f + c) = make_uint2(ou[0], ou[1]);
+    }
+}
+
+// ------------------------------------------------------------------ combine backward
+// dyhat[r] = w[t, j] * dy[t] for the dispatched row r of (t, j); padding rows are zero.  One warp
+// per dispatched row; the slot j is found among the k rows of token t.
+__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t *__restrict__ dy, const int32_t *__restrict__ row_of,
+                                                          const float *__restrict__ w, const int32_t *__restrict__ src_of,
+                                                          int k, int64_t d, int64_t rows_total,
+                                                          uint16_t *__restrict__ dyhat) {
+    const int lane = lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); r < rows_total; r += warps) {
+        const int32_t t = src_of[r];
+        float wj = 0.0f;
+        if (t >= 0) {
+            for (int j = 0; j < k; ++j)
+                if (row_of[(int64_t)t * k + j] == r) wj = w[(int64_t)t * k + j];
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(dyhat + r * d);
+        const uint4 *src = reinterpret_cast<const uint4 *>(dy + (int64_t)(t < 0 ? 0 : t) * d);
+        for (int64_t i = lane; i < d / 8; i += 32) {
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (t >= 0) {
+                const uint4 q = __ldg(src + i);
+                const uint32_t qs[4] = {q.x, q.y, q.z, q.w};
+                uint32_t os[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    os[h] = (uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_lo(qs[h]))) |
+                            ((uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_hi(qs[h]))) << 16);
+                o = make_uint4(os[0], os[1], os[2], os[3]);
+            }
+            dst[i] = o;
+        }
     }
 }
 
@@ -280,13 +350,16 @@ extern "C" int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64
 
 extern "C" int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64_t T, int64_t cols,
                                   const int32_t *src_of, int64_t rows_total, uint8_t *out_codes, uint8_t *out_sf,
-                                  void *stream) {
+                                  uint32_t flags, void *stream) {
     MOE4_CHECK_ARG(T >= 0 && cols > 0 && cols % 32 == 0 && rows_total >= 0);
     MOE4_CHECK_ARG(src_of && out_codes && out_sf && (T == 0 || (codes && sf)));
     MOE4_CHECK_ARG(aligned16(codes) && aligned16(out_codes) && aligned16(sf) && aligned16(out_sf));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    MOE4_CHECK_ARG(!sf_mma || (rows_total % 128 == 0 && cols % 64 == 0));
     if (rows_total == 0) return MOE4_OK;
     permute_nvfp4_kernel<<<grid_cap(rows_total * 32, 256, 16), 256, 0, as_stream(stream)>>>(
-        codes, sf, cols, src_of, rows_total, out_codes, out_sf);
+        codes, sf, cols, src_of, rows_total, out_codes, out_sf, sf_mma);
     return launch_status();
 }
 
@@ -294,6 +367,26 @@ extern "C" int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h
     MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0 && gu && h && aligned16(gu) && (reinterpret_cast<uintptr_t>(h) & 7u) == 0);
     if (rows == 0) return MOE4_OK;
     swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, rows, f, h);
+    return launch_status();
+}
+
+extern "C" int moe4_swiglu_backward(const float *gu, const float *dh, int64_t rows, int64_t f, uint16_t *dgu,
+                                    void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0 && gu && dh && dgu && aligned16(gu) && aligned16(dh) &&
+                   (reinterpret_cast<uintptr_t>(dgu) & 7u) == 0);
+    if (rows == 0) return MOE4_OK;
+    swiglu_bwd_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, dh, rows, f, dgu);
+    return launch_status();
+}
+
+extern "C" int moe4_combine_backward(const uint16_t *dy, const int32_t *row_of, const float *w, const int32_t *src_of,
+                                     int64_t T, int64_t k, int64_t d, int64_t rows_total, uint16_t *dyhat,
+                                     void *stream) {
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 8 == 0 && rows_total >= 0);
+    MOE4_CHECK_ARG(src_of && dyhat && aligned16(dyhat) && (T == 0 || (dy && row_of && w && aligned16(dy))));
+    if (rows_total == 0) return MOE4_OK;
+    combine_bwd_kernel<<<grid_cap(rows_total * 32, 256, 16), 256, 0, as_stream(stream)>>>(dy, row_of, w, src_of,
+                                                                                           (int)k, d, rows_total, dyhat);
     return launch_status();
 }
 

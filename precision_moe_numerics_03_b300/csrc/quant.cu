@@ -399,8 +399,8 @@ extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int
                               uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
                               uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0 && ld >= cols && ld % 8 == 0);
-    MOE4_CHECK_ARG(codes && sf && g_dec);
-    MOE4_CHECK_ARG(rows == 0 || (x && aligned16(x) && aligned16(codes)));
+    MOE4_CHECK_ARG(g_dec);
+    MOE4_CHECK_ARG(rows == 0 || (x && codes && sf && aligned16(x) && aligned16(codes)));
     MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_AMAX_GIVEN | MOE4_SF_MMA_LAYOUT)) == 0);
     const bool given = (flags & MOE4_AMAX_GIVEN) != 0;
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;

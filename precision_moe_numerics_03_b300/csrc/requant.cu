@@ -25,7 +25,7 @@ template <SrcKind kind>
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
-    uint8_t *__restrict__ e8_t, uint64_t seed, uint32_t stream_id, bool sr) {
+    uint8_t *__restrict__ e8_t, uint64_t seed, uint32_t stream_id, bool sr, bool sf_mma) {
     __shared__ __align__(16) float tile[kTileC][kPitch];
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
     const int64_t n_ct = (C + kTileC - 1) / kTileC;
@@ -46,7 +46,12 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
         if (r < R && c < C) {
             if constexpr (kind == SrcKind::Nvfp4) {
                 const uint4 w = __ldg(reinterpret_cast<const uint4 *>(codes + ((m * R + r) * C + c) / 2));
-                const uint16_t s2 = __ldg(reinterpret_cast<const uint16_t *>(sf + ((m * R + r) * C + c) / 16));
+                // the scales of blocks c/16 and c/16 + 1 (c/16 even): adjacent bytes in both layouts
+                const int64_t nblk = C / 16, b = c / 16;
+                const int64_t soff = sf_mma ? m * R * nblk + ((r >> 7) * (nblk >> 2) + (b >> 2)) * 512 + (r & 31) * 16 +
+                                                  ((r >> 5) & 3) * 4 + (b & 3)
+                                            : (m * R + r) * nblk + b;
+                const uint16_t s2 = __ldg(reinterpret_cast<const uint16_t *>(sf + soff));
                 const float gd = g_dec[m];
                 const float sa = e4m3_to_f32(s2 & 0xFFu), sb = e4m3_to_f32(s2 >> 8);
                 e2m1x8_to_f32(w.x, v);
@@ -158,12 +163,14 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && rows % 32 == 0 && cols % 32 == 0);
     MOE4_CHECK_ARG(codes && sf && g_dec && q_t && e8_t);
     MOE4_CHECK_ARG(aligned16(codes) && aligned4(q_t) && (reinterpret_cast<uintptr_t>(sf) & 1u) == 0);
-    MOE4_CHECK_ARG((flags & ~MOE4_SR) == 0);
+    MOE4_CHECK_ARG((flags & ~(MOE4_SR | MOE4_SF_MMA_LAYOUT)) == 0);
+    const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
     const int64_t tiles = nmat * ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
     if (tiles == 0) return MOE4_OK;
     MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
     requant_transpose_kernel<SrcKind::Nvfp4><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
-        codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, (flags & MOE4_SR) != 0);
+        codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, (flags & MOE4_SR) != 0, sf_mma);
     return launch_status();
 }
 
@@ -189,7 +196,7 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
         if (tiles == 0) return MOE4_OK;
         requant_transpose_kernel<SrcKind::Bf16><<<(unsigned)tiles, 256, 0, st>>>(
-            nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, sr);
+            nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, sr, false);
     }
     return launch_status();
 }

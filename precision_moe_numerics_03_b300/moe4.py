@@ -57,7 +57,9 @@ _SIGNATURES = {
     "moe4_sf_to_mma_layout": (_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_route_topk": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "moe4_permute_plan": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
-    "moe4_permute_nvfp4": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
+    "moe4_permute_nvfp4": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _u32, _vp]),
+    "moe4_swiglu_backward": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
+    "moe4_combine_backward": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_sgd_update": (_int, [_vp, _vp, _i64, _f32, _vp, _vp]),
@@ -200,8 +202,17 @@ def moe4_permute_plan(idx, T, k, E, offs, row_of, src_of, rows_cap, ws, stream=N
           _ws_bytes(ws), _s(stream))
 
 
-def moe4_permute_nvfp4(codes, sf, T, cols, src_of, rows_total, out_codes, out_sf, stream=None):
+def moe4_permute_nvfp4(codes, sf, T, cols, src_of, rows_total, out_codes, out_sf, flags=0, stream=None):
     _call("moe4_permute_nvfp4", _p(codes), _p(sf), T, cols, _p(src_of), rows_total, _p(out_codes), _p(out_sf),
+          flags, _s(stream))
+
+
+def moe4_swiglu_backward(gu, dh, rows, f, dgu, stream=None):
+    _call("moe4_swiglu_backward", _p(gu), _p(dh), rows, f, _p(dgu), _s(stream))
+
+
+def moe4_combine_backward(dy, row_of, w, src_of, T, k, d, rows_total, dyhat, stream=None):
+    _call("moe4_combine_backward", _p(dy), _p(row_of), _p(w), _p(src_of), T, k, d, rows_total, _p(dyhat),
           _s(stream))
 
 

@@ -33,13 +33,12 @@ def check_f32(D, Dref, S, what=""):
          D.reshape(-1)[:4], Dref.reshape(-1)[:4]))
 
 
-def check_bf16(Dbits, Dref):
-    got = Dbits.astype(np.int64)
-    want = oracle.f32_to_bf16(Dref.astype(np.float32)).astype(np.int64)
-    # compare as ordered integers (sign-magnitude bf16 -> monotone key)
-    def key(b):
-        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
-    assert np.max(np.abs(key(got) - key(want))) <= 1
+def check_bf16(Dbits, Dref, S):
+    """bf16 output: one bf16 rounding (at most one ulp, 2^-8 relative) on top of the binary32
+    accumulation bound; near cancellation the accumulation term dominates."""
+    got = oracle.bf16_to_f32(Dbits).astype(np.float64)
+    bad = np.abs(got - Dref) > 2.0 ** -8 * np.abs(Dref) + ELEM * S
+    assert not bad.any(), "%d of %d bf16 outputs outside one ulp + 2^-16*S" % (int(bad.sum()), bad.size)
 
 
 def _bf16(rng, shape, std=1.0, t=False):
@@ -107,7 +106,7 @@ def test_nvfp4_grouped_with_empty_groups(sf_mma):
 
 def test_nvfp4_bf16_output():
     D, Dref, S = _nvfp4_case([256, 128], N=256, K=512, seed=6, out_bf16=True)
-    check_bf16(to_np(D, np.uint16), Dref)
+    check_bf16(to_np(D, np.uint16), Dref, S)
 
 
 def test_nvfp4_small_moe_shapes():

@@ -65,7 +65,7 @@ def test_permute_plan_and_gather(T, E, k, bias):
     x = inputs.to_bf16_bits(np.random.default_rng(1).standard_normal((T, cols)).astype(np.float32))
     c, s, g = nvfp4_quantize(to_dev(x), 1, T, cols)
     oc, osf = empty_u8(Rp, cols // 2), empty_u8(Rp, cols // 16)
-    moe4.moe4_permute_nvfp4(c, s, T, cols, src_of, Rp, oc, osf)
+    moe4.moe4_permute_nvfp4(c, s, T, cols, src_of, Rp, oc, osf, 0)
     torch.cuda.synchronize()
     rc, rs, _ = oracle.nvfp4_quantize(oracle.bf16_to_f32(x))
     assert first_mismatch(to_np(oc), oracle.permute_rows(rc, rrow, Rp)) is None
@@ -107,3 +107,60 @@ def test_sgd_update_bit_exact():
     torch.cuda.synchronize()
     rw, rb = oracle.sgd_update(w32, dw, 1e-3)
     assert first_mismatch(to_np(wt), rw) is None and first_mismatch(to_np(wb, np.uint16), rb) is None
+
+
+def test_swiglu_backward_within_one_bf16_ulp():
+    rows, f = 512, 1024
+    rng = np.random.default_rng(5)
+    gu = (rng.standard_normal((rows, 2 * f)) * 3).astype(np.float32)
+    dh = rng.standard_normal((rows, f)).astype(np.float32)
+    dgu = torch.empty((rows, 2 * f), dtype=torch.int16, device=DEV)
+    moe4.moe4_swiglu_backward(to_dev(gu), to_dev(dh), rows, f, dgu)
+    torch.cuda.synchronize()
+    got = to_np(dgu, np.uint16).astype(np.int64)
+    want = oracle.f32_to_bf16(oracle.swiglu_backward(gu, dh)).astype(np.int64)
+
+    def key(b):
+        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+    assert np.max(np.abs(key(got) - key(want))) <= 1
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (300, 16, 4)])
+def test_combine_backward_bit_exact(T, E, k):
+    lg = _logits(T, E, True, 3 * T + E)
+    ridx, rw = oracle.route_topk(lg, k)
+    roffs, rrow = oracle.permute_plan(ridx, E)
+    Rp = int(roffs[-1])
+    rows_cap = T * k + 127 * E
+    rsrc = np.full(rows_cap, -1, np.int32)
+    rsrc[rrow.reshape(-1)] = np.repeat(np.arange(T, dtype=np.int32), k)
+    d = 256
+    dy = inputs.to_bf16_bits(np.random.default_rng(T).standard_normal((T, d)).astype(np.float32))
+    out = torch.full((Rp, d), 0x7FC0, dtype=torch.int16, device=DEV)
+    moe4.moe4_combine_backward(to_dev(dy), to_dev(rrow), to_dev(rw), to_dev(rsrc), T, k, d, Rp, out)
+    torch.cuda.synchronize()
+    assert first_mismatch(to_np(out, np.uint16), oracle.combine_backward(dy, rrow, rw, Rp)) is None
+
+
+def test_permute_with_tensor_core_scale_layout():
+    T, E, k, cols = 2000, 8, 2, 512
+    lg = _logits(T, E, False, 99)
+    ridx, _ = oracle.route_topk(lg, k)
+    roffs, rrow = oracle.permute_plan(ridx, E)
+    Rp = int(roffs[-1])
+    rsrc = np.full(Rp, -1, np.int32)
+    rsrc[rrow.reshape(-1)] = np.repeat(np.arange(T, dtype=np.int32), k)
+    x = inputs.to_bf16_bits(np.random.default_rng(2).standard_normal((T, cols)).astype(np.float32))
+    c, s, g = nvfp4_quantize(to_dev(x), 1, T, cols)
+    oc, osf = empty_u8(Rp, cols // 2), empty_u8(Rp, cols // 16)
+    moe4.moe4_permute_nvfp4(c, s, T, cols, to_dev(rsrc), Rp, oc, osf, moe4.SF_MMA_LAYOUT)
+    torch.cuda.synchronize()
+    rc, rs, _ = oracle.nvfp4_quantize(oracle.bf16_to_f32(x))
+    want_s = oracle.permute_rows(rs, rrow, Rp)
+    got = to_np(osf).reshape(-1)
+    nblk = cols // 16
+    r = np.arange(Rp)[:, None]
+    b = np.arange(nblk)[None, :]
+    off = ((r // 128) * (nblk // 4) + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+    assert first_mismatch(got[off], want_s) is None
+    assert first_mismatch(to_np(oc), oracle.permute_rows(rc, rrow, Rp)) is None

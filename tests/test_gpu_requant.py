@@ -109,3 +109,21 @@ def test_mxfp8_quantize(layout, sr):
     torch.cuda.synchronize()
     rq, re8 = oracle.mxfp8_quantize(oracle.bf16_to_f32(x), colwise=(layout == "col"), sr=sr, seed=77, stream_id=4)
     assert first_mismatch(to_np(q), rq) is None and first_mismatch(to_np(e8), re8) is None
+
+
+def test_requant_reads_tensor_core_scale_layout():
+    nmat, rows, cols = 2, 256, 512
+    rng = np.random.default_rng(31)
+    x = inputs.to_bf16_bits(rng.standard_t(3, (nmat * rows, cols)).astype(np.float32))
+    xd = to_dev(x)
+    c, s, g = nvfp4_quantize(xd, nmat, rows, cols)
+    c2, s2, g2 = nvfp4_quantize(xd, nmat, rows, cols, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    q1, e1 = _requant_gpu(c, s, g, nmat, rows, cols, 5, 1, True)
+    q2 = empty_u8(nmat, cols, rows)
+    e2 = empty_u8(nmat, cols, rows // 32)
+    moe4.mxfp8_requant_transpose_sr(c2, s2, g2, nmat, rows, cols, q2, e2, 5, 1, moe4.SR | moe4.SF_MMA_LAYOUT)
+    torch.cuda.synchronize()
+    oc, os_, og = oracle.nvfp4_quantize(oracle.bf16_to_f32(x).reshape(nmat, rows, cols))
+    rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=True, seed=5, stream_id=1)
+    assert first_mismatch(to_np(q2), rq) is None and first_mismatch(to_np(e2), re8) is None
+    assert torch.equal(q1, q2) and torch.equal(e1, e2)
