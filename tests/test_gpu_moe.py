@@ -1,6 +1,6 @@
 """GPU parity of the MoE steps around the expert GEMMs: top-k routing (indices bit-exact, weights
-to 1e-6 relative), the dispatch plan and the NVFP4 row gather (bit-exact), SwiGLU (within one bf16
-ulp: it calls expf), the weighted combine and the SGD update of FP32 master weights (bit-exact).
+to 1e-6 relative), the dispatch plan and the NVFP4 row gather (bit-exact), SwiGLU and its backward (within
+one bf16 rounding: they call expf), the weighted combine and the SGD update of FP32 master weights (bit-exact).
 
 Shapes: the small grouped MoE (8 experts, top-2) and the Inkling-shaped layer (384 experts, top-8,
 N(0,1) logits plus a per-expert N(0,1) bias, 16384 tokens)."""
@@ -109,7 +109,7 @@ def test_sgd_update_bit_exact():
     assert first_mismatch(to_np(wt), rw) is None and first_mismatch(to_np(wb, np.uint16), rb) is None
 
 
-def test_swiglu_backward_within_one_bf16_ulp():
+def test_swiglu_backward_within_bf16_rounding():
     rows, f = 512, 1024
     rng = np.random.default_rng(5)
     gu = (rng.standard_normal((rows, 2 * f)) * 3).astype(np.float32)
@@ -117,12 +117,15 @@ def test_swiglu_backward_within_one_bf16_ulp():
     dgu = torch.empty((rows, 2 * f), dtype=torch.int16, device=DEV)
     moe4.moe4_swiglu_backward(to_dev(gu), to_dev(dh), rows, f, dgu)
     torch.cuda.synchronize()
-    got = to_np(dgu, np.uint16).astype(np.int64)
-    want = oracle.f32_to_bf16(oracle.swiglu_backward(gu, dh)).astype(np.int64)
-
-    def key(b):
-        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
-    assert np.max(np.abs(key(got) - key(want))) <= 1
+    got = oracle.bf16_to_f32(to_np(dgu, np.uint16)).astype(np.float64)
+    ref = oracle.swiglu_backward(gu, dh).astype(np.float64)
+    # one bf16 rounding (2^-8 relative) plus a few binary32 ulps of the terms' size: near the zero
+    # of silu' (g ~ -1.28) the factor 1 + g(1 - s) cancels in binary32
+    g, u, d = gu[:, :f].astype(np.float64), gu[:, f:].astype(np.float64), dh.astype(np.float64)
+    mag = np.abs(d) * (np.abs(u) * (1 + np.abs(g)) + np.abs(g))
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -20 * np.concatenate([mag, mag], axis=1)
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), int(bad.sum())
 
 
 @pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (300, 16, 4)])
