@@ -427,6 +427,84 @@ def run_reference(args, rank, world):
     return 0
 
 
+def profile_case(name):
+    """One kernel on a case larger than L2 but a few GB at most: 2 untimed + 3 launches."""
+    import torch
+    from precision_moe_numerics_03_b300 import inputs, moe4
+    moe4.load()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    g = lambda s: inputs.device_generator(7, s, dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    E, d, f = 16, 4096, 2048            # 16 experts of the Inkling shape: 268 M gate/up weights
+    calls = []
+    if name in ("requant", "quant_w", "sgd"):
+        w = inputs.device_normal((E * 2 * f, d), 0.02, g(0), dev).view(torch.int16)
+        c, s_ = torch.empty((E, 2 * f, d // 2), **u8), torch.empty((E, 2 * f, d // 16), **u8)
+        gd = torch.empty(E, dtype=torch.float32, device=dev)
+        ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, E), dev)
+        quant = lambda: moe4.nvfp4_quantize(w, E, 2 * f, d, d, c, s_, gd, None,
+                                            moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT, ws)
+        quant()
+        if name == "quant_w":
+            calls.append(quant)
+        elif name == "requant":
+            q, e8 = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
+            calls.append(lambda: moe4.mxfp8_requant_transpose_sr(c, s_, gd, E, 2 * f, d, q, e8, 1, 3,
+                                                                 moe4.SR | moe4.SF_MMA_LAYOUT))
+        else:
+            w32 = torch.randn((E * 2 * f * d,), generator=g(1), device=dev)
+            dw = torch.randn((E * 2 * f * d,), generator=g(2), device=dev)
+            calls.append(lambda: moe4.moe4_sgd_update(w32, dw, w32.numel(), LR, w.view(-1)))
+    elif name == "gemm_nvfp4":
+        rows = 128 * 64
+        x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
+        w = inputs.device_normal((E * 2 * f, d), 0.02, g(0), dev).view(torch.int16)
+        ac, as_ = torch.empty((rows, d // 2), **u8), torch.empty((rows, d // 16), **u8)
+        ag = torch.empty(1, dtype=torch.float32, device=dev)
+        bc, bs = torch.empty((E, 2 * f, d // 2), **u8), torch.empty((E, 2 * f, d // 16), **u8)
+        bg = torch.empty(E, dtype=torch.float32, device=dev)
+        ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, E), dev)
+        flags = moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT
+        moe4.nvfp4_quantize(x, 1, rows, d, d, ac, as_, ag, None, flags, ws)
+        moe4.nvfp4_quantize(w, E, 2 * f, d, d, bc, bs, bg, None, flags, ws)
+        offs = torch.arange(0, rows + 1, rows // E, dtype=torch.int32, device=dev)
+        out = torch.empty((rows, 2 * f), dtype=torch.float32, device=dev)
+        calls.append(lambda: moe4.grouped_expert_gemm_nvfp4(ac, as_, ag, bc, bs, bg, offs, E, rows, 2 * f, d, out,
+                                                            moe4.OUT_F32 | moe4.SF_MMA_LAYOUT))
+    else:
+        rows = 128 * 64
+        offs = torch.arange(0, rows + 1, rows // E, dtype=torch.int32, device=dev)
+        if name == "gemm_mxfp8_wgrad":
+            M, N = 2 * f, d
+            a = torch.randint(0, 120, (M, rows), generator=g(4), device=dev, dtype=torch.int32).to(torch.uint8)
+            b = torch.randint(0, 120, (N, rows), generator=g(5), device=dev, dtype=torch.int32).to(torch.uint8)
+            ae = torch.full((M, rows // 32), 120, **u8)
+            be = torch.full((N, rows // 32), 120, **u8)
+            out = torch.empty((E, M, N), dtype=torch.float32, device=dev)
+            ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, rows), dev)
+            calls.append(lambda: moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, M, N, rows, out,
+                                                         moe4.OUT_F32 | moe4.GROUP_K, ws))
+        else:
+            N, K = d, 2 * f
+            a = torch.randint(0, 120, (rows, K), generator=g(4), device=dev, dtype=torch.int32).to(torch.uint8)
+            b = torch.randint(0, 120, (E * N, K), generator=g(5), device=dev, dtype=torch.int32).to(torch.uint8)
+            ae = torch.full((rows, K // 32), 120, **u8)
+            be = torch.full((E * N, K // 32), 120, **u8)
+            out = torch.empty((rows, N), dtype=torch.int16, device=dev)
+            ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, rows, E, N, K), dev)
+            calls.append(lambda: moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, rows, N, K, out,
+                                                         moe4.OUT_BF16 | moe4.GROUP_M, ws))
+    for _ in range(5):
+        for c_ in calls:
+            c_()
+    torch.cuda.synchronize()
+    if moe4.moe4_get_status() != moe4.OK:
+        raise RuntimeError("a device wait timed out")
+    print("profile case %s done" % name)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -436,7 +514,12 @@ def main():
     ap.add_argument("--small", action="store_true", help="the small 8-expert shapes (a quick check, not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_dgrad", "sgd"],
+                    help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
+    if args.profile_case:
+        return profile_case(args.profile_case)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
