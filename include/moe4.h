@@ -103,6 +103,23 @@ int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, 
                    uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
                    uint32_t flags, void *ws, size_t ws_bytes, void *stream);
 
+/* nvfp4_quantize_noalloc: the same quantisation as nvfp4_quantize (amax computed here, flags
+ * MOE4_FOUR_OVER_SIX and MOE4_SF_MMA_LAYOUT only), for callers that cannot allocate device
+ * memory: a host runtime that plans all of its device memory when it starts and allows no
+ * allocation afterwards, or code loaded into a process whose memory pool it cannot reach, has
+ * no way to provide the `ws` buffer that nvfp4_quantize needs.  The pages describe no such
+ * entry point; it is an interface convenience of this library.
+ *   - Scratch: the per-matrix amax lives in a fixed array of 4096 uint32 (16 KiB) that every GPU
+ *     which loads the library holds until the process exits.  nmat > 4096 returns MOE4_ERR_ARG.
+ *   - Allocation: none.  The call makes no cudaMalloc or cudaFree and no allocating library call.
+ *   - First call on a device: it looks up the array's device address (cudaGetSymbolAddress) and
+ *     caches it per device; make that first call before any stream capture.
+ *   - Every call uses the same array and clears the part it needs first; calls whose work
+ *     overlaps on the GPU (on different streams, or on different host threads) race on it. */
+int nvfp4_quantize_noalloc(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols,
+                           int64_t ld, uint8_t *codes, uint8_t *sf, float *g_dec, uint32_t flags,
+                           void *stream);
+
 /* nvfp4_dequantize: x_hat = (e2m1(q) * e4m3(sf)) * g_dec[m]; out [nmat, rows, cols] as bf16
  * (MOE4_OUT_BF16, nearest-even) or binary32 (MOE4_OUT_F32).  Canonical sf only. */
 int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t nmat,

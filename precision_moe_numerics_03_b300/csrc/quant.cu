@@ -12,6 +12,7 @@
 #include "common.cuh"
 
 #include <cfloat>
+#include <mutex>
 
 namespace moe4 {
 
@@ -469,5 +470,60 @@ extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const f
     if (chunks == 0) return MOE4_OK;
     hadamard_dequant_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, rows,
                                                                                             cols, out_bf16);
+    return launch_status();
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+// nvfp4_quantize needs scratch for the per-matrix amax of its first pass.  This variant keeps
+// that scratch in a fixed array in device memory that belongs to the library, for callers that
+// cannot allocate device memory themselves (see include/moe4.h).  The array's device address is
+// looked up once per device (host code only sees a host-side stand-in for the symbol).
+namespace moe4 {
+constexpr int64_t kNoAllocMaxMats = 4096;
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) unsigned int g_noalloc_amax[kNoAllocMaxMats];
+
+static unsigned int *noalloc_amax_address() {
+    static std::mutex mu;
+    static unsigned int *addr[kNoAllocMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+}  // namespace moe4
+
+extern "C" int nvfp4_quantize_noalloc(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                                      uint8_t *codes, uint8_t *sf, float *g_dec, uint32_t flags, void *stream) {
+    MOE4_CHECK_ARG(nmat >= 1 && nmat <= kNoAllocMaxMats);
+    MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 16 == 0 && ld >= cols && ld % 8 == 0);
+    MOE4_CHECK_ARG(g_dec);
+    MOE4_CHECK_ARG(rows == 0 || (x && codes && sf && aligned16(x) && aligned16(codes)));
+    MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_SF_MMA_LAYOUT)) == 0);
+    const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
+    MOE4_CHECK_ARG(rows * (cols / 16) < (int64_t(1) << 32));
+    unsigned int *amax_bits = noalloc_amax_address();
+    if (!amax_bits) return MOE4_ERR_CUDA;
+    cudaStream_t st = as_stream(stream);
+    // the array keeps the previous call's maxima: clear the part this call folds into
+    if (cudaMemsetAsync(amax_bits, 0, (size_t)nmat * sizeof(unsigned int), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (rows > 0) {
+        const int64_t nvec = rows * (cols / 8);
+        int gx = grid_for(nvec, 256, 8);
+        const int64_t per_mat_cap = ((int64_t)num_sms() * 8 + nmat - 1) / nmat;
+        if (gx > per_mat_cap) gx = (int)per_mat_cap;
+        if (gx < 1) gx = 1;
+        amax_bf16_kernel<<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
+    }
+    const int64_t total = nmat * rows * (cols / 16);
+    const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
+    nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, nullptr, amax_bits,
+                                             (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf, g_dec);
     return launch_status();
 }

@@ -46,6 +46,7 @@ _SIGNATURES = {
     "moe4_workspace_size_gemm": (_sz, [_int, _i64, _i64, _i64, _i64]),
     "moe4_get_status": (_int, [_vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
+    "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
     "mxfp8_requant_transpose_sr": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
     "mxfp8_quantize": (_int, [_vp, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
@@ -150,6 +151,12 @@ def nvfp4_quantize(x, nmat, rows, cols, ld, codes, sf, g_dec, amax_in=None, flag
                    stream=None):
     _call("nvfp4_quantize", _p(x), nmat, rows, cols, ld, _p(codes), _p(sf), _p(g_dec), _p(amax_in), flags,
           _p(ws), _ws_bytes(ws), _s(stream))
+
+
+def nvfp4_quantize_noalloc(x, nmat, rows, cols, ld, codes, sf, g_dec, flags=FOUR_OVER_SIX, stream=None):
+    """nvfp4_quantize without a caller-provided workspace: its scratch is a fixed array owned by
+    the library (at most 4096 matrices per call; overlapping calls race on it)."""
+    _call("nvfp4_quantize_noalloc", _p(x), nmat, rows, cols, ld, _p(codes), _p(sf), _p(g_dec), flags, _s(stream))
 
 
 def nvfp4_dequantize(codes, sf, g_dec, nmat, rows, cols, out, flags=OUT_BF16, stream=None):
