@@ -84,6 +84,10 @@ class LayerStep:
         self.W32_d = torch.randn((E, d, f), generator=g(5), device=dev).mul_(0.02)
         self.Wb_gu = self.W32_gu.to(torch.bfloat16).view(torch.int16)
         self.Wb_d = self.W32_d.to(torch.bfloat16).view(torch.int16)
+        # per-expert amax of the bf16 copies: written by the fused wgrad + SGD epilogue of each step
+        # and read by the next step's weight quantisation (here seeded for the first step)
+        self.amax_gu = self.Wb_gu.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
+        self.amax_d = self.Wb_d.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
         # routing
         self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
         self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
@@ -117,14 +121,12 @@ class LayerStep:
         self.WdT_q, self.WdT_e = torch.empty((E, f, d), **u8), torch.empty((E, f, d // 32), **u8)
         self.HqT_q, self.HqT_e = torch.empty(f * R, **u8), torch.empty(f * R // 32, **u8)
         self.dH = torch.empty((R, f), dtype=torch.float32, device=dev)
-        self.dWd = torch.empty((E, d, f), dtype=torch.float32, device=dev)
         self.dGU = torch.empty((R, 2 * f), dtype=torch.int16, device=dev)
         self.dGUr_q, self.dGUr_e = torch.empty((R, 2 * f), **u8), torch.empty((R, 2 * f // 32), **u8)
         self.dGUc_q, self.dGUc_e = torch.empty(2 * f * R, **u8), torch.empty(2 * f * R // 32, **u8)
         self.WguT_q, self.WguT_e = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
         self.XpT_q, self.XpT_e = torch.empty(d * R, **u8), torch.empty(d * R // 32, **u8)
         self.dXp = torch.empty((R, d), dtype=torch.int16, device=dev)
-        self.dWgu = torch.empty((E, 2 * f, d), dtype=torch.float32, device=dev)
         # scratch for the GEMMs' scale-layout change (largest call)
         wsz = max(moe4.moe4_workspace_size_gemm(1, R, E, f, d), moe4.moe4_workspace_size_gemm(1, R, E, d, 2 * f),
                   moe4.moe4_workspace_size_gemm(1, d, 1, f, R), moe4.moe4_workspace_size_gemm(1, 2 * f, 1, d, R))
@@ -159,9 +161,11 @@ class LayerStep:
             m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
         n += 3
         with tm("quant_w"):
-            m.nvfp4_quantize(self.Wb_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, None, FOS | MMA, self.qws)
-            m.nvfp4_quantize(self.Wb_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, None, FOS | MMA, self.qws)
-        n += 4
+            GIVEN = m.AMAX_GIVEN
+            m.nvfp4_quantize(self.Wb_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.amax_gu,
+                             FOS | MMA | GIVEN)
+            m.nvfp4_quantize(self.Wb_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, self.amax_d, FOS | MMA | GIVEN)
+        n += 2
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
                                         E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
@@ -193,12 +197,14 @@ class LayerStep:
             m.mxfp8_requant_transpose_sr(self.Hq_c, self.Hq_s, self.Hq_g, 1, Rp, f, self.HqT_q, self.HqT_e, seed, 2,
                                          m.SR | MMA)
         n += 2
-        with tm("gemm_mxfp8"):
+        with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dYr_q, self.dYr_e, self.WdT_q, self.WdT_e, self.offs, E, Rp, f, d, self.dH,
                                  m.OUT_F32 | m.GROUP_M, self.gws)
-            m.grouped_gemm_mxfp8(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp, self.dWd,
-                                 m.OUT_F32 | m.GROUP_K, self.gws)
-        n += 6
+        n += 3
+        with tm("gemm_mxfp8_wgrad_sgd"):
+            m.grouped_gemm_mxfp8_wgrad_sgd(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp,
+                                           self.W32_d, self.Wb_d, LR, self.amax_d, 0, self.gws)
+        n += 3
         with tm("swiglu_bwd"):
             m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
         n += 1
@@ -212,16 +218,14 @@ class LayerStep:
             m.mxfp8_requant_transpose_sr(self.Xp_c, self.Xp_s, self.Xq_g, 1, Rp, d, self.XpT_q, self.XpT_e, seed, 4,
                                          m.SR | MMA)
         n += 2
-        with tm("gemm_mxfp8"):
+        with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dGUr_q, self.dGUr_e, self.WguT_q, self.WguT_e, self.offs, E, Rp, d, 2 * f,
                                  self.dXp, m.OUT_BF16 | m.GROUP_M, self.gws)
-            m.grouped_gemm_mxfp8(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d, Rp,
-                                 self.dWgu, m.OUT_F32 | m.GROUP_K, self.gws)
-        n += 6
-        with tm("sgd"):
-            m.moe4_sgd_update(self.W32_gu, self.dWgu, self.W32_gu.numel(), LR, self.Wb_gu)
-            m.moe4_sgd_update(self.W32_d, self.dWd, self.W32_d.numel(), LR, self.Wb_d)
-        n += 2
+        n += 3
+        with tm("gemm_mxfp8_wgrad_sgd"):
+            m.grouped_gemm_mxfp8_wgrad_sgd(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d,
+                                           Rp, self.W32_gu, self.Wb_gu, LR, self.amax_gu, 0, self.gws)
+        n += 3
         self.launches += n
         return n
 
@@ -235,17 +239,17 @@ class LayerStep:
         mx = 1.03125      # MXFP8 bytes per value (E4M3 + E8M0 per 32)
         w_gu, w_d = E * 2 * f * d, E * d * f
         b = {}
-        b["quant_w"] = (w_gu + w_d) * (2 + 2 + nv)                       # amax pass, quant pass, output
+        b["quant_w"] = (w_gu + w_d) * (2 + nv)                           # amax comes from the SGD epilogue
         b["quant_x"] = T * d * (2 + 2 + nv) + rows * d * nv * 2          # + gather read/write
         b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
                            rows * f * nv + live * d * f * nv + rows * d * 2)
         b["requant"] = (w_gu + w_d + rows * (f + d)) * (nv + mx)
         b["mxfp8_quant"] = rows * d * (2 + 2 + 2 * mx) + T * d * 2 + rows * 2 * f * (2 * 2 + 2 * mx)
-        b["gemm_mxfp8"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +           # dgrad down
-                           rows * d * mx + rows * f * mx + E * d * f * 4 +              # wgrad down
-                           rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2 +   # dgrad gate/up
-                           rows * 2 * f * mx + rows * d * mx + E * 2 * f * d * 4)       # wgrad gate/up
-        b["sgd"] = (w_gu + w_d) * (4 + 4 + 4 + 2)
+        b["gemm_mxfp8_dgrad"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +          # down
+                                 rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2)   # gate/up
+        # wgrad operands + the SGD epilogue: read W32, write W32 and the bf16 copy
+        b["gemm_mxfp8_wgrad_sgd"] = (rows * d * mx + rows * f * mx + rows * 2 * f * mx + rows * d * mx +
+                                     (w_gu + w_d) * (4 + 4 + 2))
         b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 * 2 + rows * f * (2 + nv)
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
         b["hadamard"] = rows * d * (2 + 2 + nv + nv + 2)
@@ -475,16 +479,22 @@ def profile_case(name):
     else:
         rows = 128 * 64
         offs = torch.arange(0, rows + 1, rows // E, dtype=torch.int32, device=dev)
-        if name == "gemm_mxfp8_wgrad":
+        if name in ("gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd"):
             M, N = 2 * f, d
             a = torch.randint(0, 120, (M, rows), generator=g(4), device=dev, dtype=torch.int32).to(torch.uint8)
             b = torch.randint(0, 120, (N, rows), generator=g(5), device=dev, dtype=torch.int32).to(torch.uint8)
             ae = torch.full((M, rows // 32), 120, **u8)
             be = torch.full((N, rows // 32), 120, **u8)
-            out = torch.empty((E, M, N), dtype=torch.float32, device=dev)
+            out = torch.randn((E, M, N), generator=g(6), device=dev).mul_(0.02)
             ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, rows), dev)
-            calls.append(lambda: moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, M, N, rows, out,
-                                                         moe4.OUT_F32 | moe4.GROUP_K, ws))
+            if name == "gemm_mxfp8_wgrad":
+                calls.append(lambda: moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, M, N, rows, out,
+                                                             moe4.OUT_F32 | moe4.GROUP_K, ws))
+            else:
+                wb = out.to(torch.bfloat16).view(torch.int16)
+                amax = torch.empty(E, dtype=torch.float32, device=dev)
+                calls.append(lambda: moe4.grouped_gemm_mxfp8_wgrad_sgd(a, ae, b, be, offs, E, M, N, rows, out, wb,
+                                                                       LR, amax, 0, ws))
         else:
             N, K = d, 2 * f
             a = torch.randint(0, 120, (rows, K), generator=g(4), device=dev, dtype=torch.int32).to(torch.uint8)
@@ -515,7 +525,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", default=None,
-                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_dgrad", "sgd"],
+                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
+                             "gemm_mxfp8_dgrad", "sgd"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
     if args.profile_case:
@@ -594,12 +605,14 @@ def main():
             entry["GB/s"] = round(gbytes[name] / (t / 1e3) / 1e9, 1)
         comps[name] = entry
     comps["gemm_nvfp4"]["TFLOP/s"] = round(fwd_flops / (per["gemm_nvfp4"] / 1e3) / 1e12, 1)
-    comps["gemm_mxfp8"]["TFLOP/s"] = round(bwd_flops / (per["gemm_mxfp8"] / 1e3) / 1e12, 1)
+    comps["gemm_mxfp8_dgrad"]["TFLOP/s"] = round(fwd_flops / (per["gemm_mxfp8_dgrad"] / 1e3) / 1e12, 1)
+    comps["gemm_mxfp8_wgrad_sgd"]["TFLOP/s"] = round(fwd_flops / (per["gemm_mxfp8_wgrad_sgd"] / 1e3) / 1e12, 1)
     fp4_peak = peaks["bf16_sus"] * 6.0     # nominal FP4 / BF16 ratio (13.5 / 2.25)
     fp8_peak = peaks["bf16_sus"] * 2.0
     dom = max(per, key=per.get)
     t_dom = per[dom]
-    flops_dom = {"gemm_nvfp4": (fwd_flops, fp4_peak), "gemm_mxfp8": (bwd_flops, fp8_peak)}.get(dom)
+    flops_dom = {"gemm_nvfp4": (fwd_flops, fp4_peak), "gemm_mxfp8_dgrad": (fwd_flops, fp8_peak),
+                 "gemm_mxfp8_wgrad_sgd": (fwd_flops, fp8_peak)}.get(dom)
     if flops_dom is not None and flops_dom[0] / flops_dom[1] / 1e12 > gbytes[dom] / peaks["hbm"] / 1e9:
         ach = flops_dom[0] / (t_dom / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": flops_dom[1], "unit": "TFLOP/s",

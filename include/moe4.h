@@ -192,6 +192,24 @@ int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
                        int64_t N, int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
                        void *stream);
 
+/* grouped_gemm_mxfp8_wgrad_sgd: the contraction-grouped MXFP8 weight-gradient GEMM fused with
+ * the FP32 master-weight update [LHC precisions: master weights in FP32; kernels paragraph:
+ * fusing work into the final stage of the matrix multiplication].  For each expert e:
+ * dW = A[:, offs[e]:offs[e+1]] * B[:, offs[e]:offs[e+1]]^T accumulated in binary32 (never
+ * written to memory), then w32[e] <- w32[e] - lr * dW (one product, one difference, as
+ * moe4_sgd_update), w_bf16[e] <- bf16(w32[e]) (nearest-even), and amax_out[e] = max |w_bf16[e]|
+ * (binary32; exactly the amax the next nvfp4_quantize of w_bf16 would compute, so that call can
+ * take MOE4_AMAX_GIVEN).  Bit-identical to grouped_gemm_mxfp8(MOE4_GROUP_K | MOE4_OUT_F32)
+ * followed by moe4_sgd_update.  A [M, K], B [N, K], w32 / w_bf16 [E, M, N]; M % 128 == 0,
+ * N % 256 == 0, K % 128 == 0; offs as for grouped_gemm_mxfp8 (offs[E] = K).  Experts with no rows
+ * keep their weights (and still report their amax).  flags: MOE4_SF_MMA_LAYOUT or 0 (canonical
+ * scales are converted into ws, moe4_workspace_size_gemm(1, M, 1, N, K) bytes). */
+int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
+                                 const uint8_t *b_e8, const int32_t *group_offs, int64_t E,
+                                 int64_t M, int64_t N, int64_t K, float *w32, uint16_t *w_bf16,
+                                 float lr, float *amax_out, uint32_t flags, void *ws,
+                                 size_t ws_bytes, void *stream);
+
 /* moe4_sf_to_mma_layout: rearrange canonical scale factors sf [nmat, rows, nblk] into the
  * tensor-core tile layout: for each 128-row tile and each group of 4 consecutive blocks, 512
  * bytes where row r = 32*j + i of the tile puts its 4 bytes at offset 16*i + 4*j.  rows % 128

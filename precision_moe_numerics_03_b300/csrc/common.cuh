@@ -37,8 +37,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 
 // ------------------------------------------------------------------ FP4 / FP8 conversions
 // Eight binary32 values -> eight E2M1 codes packed into a 32-bit word (element i in nibble i),
-// nearest-even with saturation at +-6.  The sign bit of every code is then forced to the sign of
-// its input, so a small negative value is -0 (code 0x8) whatever the hardware does with -0.
+// nearest-even with saturation at +-6.  The conversion keeps the sign of a result that rounds to
+// zero (a small negative value gives -0, code 0x8), which the exhaustive conversion test checks.
 __device__ __forceinline__ uint32_t e2m1x8_rn(const float v[8]) {
     uint32_t out;
     asm("{\n"
@@ -51,10 +51,7 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float v[8]) {
         "}"
         : "=r"(out)
         : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-    uint32_t signs = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) signs |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
-    return out | signs;
+    return out;
 }
 
 // Eight E2M1 codes (nibble i = element i) -> eight exact binary32 values.
@@ -111,14 +108,15 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
                                                  uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0;
-        const uint32_t n2 = hi0 ^ c3 ^ k1;
+        // one 32x32 -> 64-bit multiply per product gives both halves
+        const uint64_t p0 = (uint64_t)c0 * 0xD2511F53u;
+        const uint64_t p1 = (uint64_t)c2 * 0xCD9E8D57u;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
         c0 = n0;
-        c1 = lo1;
         c2 = n2;
-        c3 = lo0;
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
@@ -147,24 +145,69 @@ __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint3
 
 // Stochastic rounding of v (|v| <= 448) to an E4M3 code with random word r: the magnitude goes
 // up to the next E4M3 value iff r < floor(frac * 2^32), frac = distance above the value below in
-// units of the gap.  E4M3 normal range: the gap is 2^20 units of v's last bit, so the threshold
-// is v's low 20 mantissa bits shifted up by 12; subnormal range (below 2^-6): gap 2^-9.
+// units of the gap.  E4M3 normal range (|v| >= 2^-6): the value below keeps v's top 3 mantissa
+// bits, so its code is ((bits >> 20) & 0x7FF) - 960 (exponent rebias 127 -> 7, 3 mantissa
+// bits), the next value is code + 1, and the threshold is v's low 20 mantissa bits moved to the
+// top (bits << 12).  Subnormal range (|v| < 2^-6): the gap is 2^-9 and the code floor(|v|*512).
+__device__ __forceinline__ uint32_t e4m3_sr_normal(uint32_t bits, uint32_t r) {
+    return (((bits >> 20) & 0x7FFu) - 960u + (r < (bits << 12) ? 1u : 0u)) | ((bits >> 24) & 0x80u);
+}
+__device__ __forceinline__ bool e4m3_is_normal(uint32_t bits) { return (bits & 0x7FFFFFFFu) >= 0x3C800000u; }
+__device__ __forceinline__ uint32_t e4m3_sr_small(uint32_t bits, uint32_t r) {
+    const float s = __fmul_rn(__uint_as_float(bits & 0x7FFFFFFFu), 512.0f);
+    const uint32_t fl = __float2uint_rz(s);
+    const uint32_t thr = __float2uint_rz(__fmul_rn(__fsub_rn(s, __uint2float_rz(fl)), 4294967296.0f));
+    return (fl + (r < thr ? 1u : 0u)) | ((bits >> 24) & 0x80u);
+}
 __device__ __forceinline__ uint32_t e4m3_sr(float v, uint32_t r) {
-    const uint32_t sign = (__float_as_uint(v) >> 31) << 7;
-    const float a = fabsf(v);
-    const uint32_t ab = __float_as_uint(a);
-    float chosen;
-    if (ab >= 0x3C800000u) {  // a >= 2^-6
-        const uint32_t thr = (ab & 0xFFFFFu) << 12;
-        const uint32_t lo = ab & 0xFFF00000u;
-        chosen = __uint_as_float(r < thr ? lo + 0x100000u : lo);
-    } else {
-        const float s = __fmul_rn(a, 512.0f);
-        const float fl = floorf(s);
-        const uint32_t thr = __float2uint_rz(__fmul_rn(__fsub_rn(s, fl), 4294967296.0f));
-        chosen = __fmul_rn(r < thr ? __fadd_rn(fl, 1.0f) : fl, 0.001953125f);  // * 2^-9, exact
-    }
-    return e4m3_rn(chosen) | sign;
+    const uint32_t bits = __float_as_uint(v);
+    return e4m3_is_normal(bits) ? e4m3_sr_normal(bits, r) : e4m3_sr_small(bits, r);
+}
+// ------------------------------------------------------------------ packed binary32 pairs
+// mul/add/sub.rn.f32x2: two IEEE round-to-nearest operations in one instruction.  The compiler may
+// fuse a packed multiply and a following packed add or subtract into one multiply-add (observed:
+// one rounding instead of two), so these are used only where a product feeds no add or subtract;
+// bit-exact multiply-then-add chains use __fmul_rn / __fadd_rn, which are never fused.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// Two E2M1 codes (a byte) -> f16x2, and two E4M3 codes (16 bits) -> f16x2: both exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte_in_low8) {
+    uint32_t h;
+    asm("{\n"
+        ".reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "}"
+        : "=r"(h)
+        : "r"(byte_in_low8));
+    return h;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_codes) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)two_codes));
+    return h;
 }
 
 // ------------------------------------------------------------------ misc

@@ -5,7 +5,7 @@
 // agihunt.info, "Confirmed"; "Thinking Machines: Nvidia FP4 Up to 6x Faster, Runs Gain 8%",
 // fourweekmba.com, "What Thinking Machines Changed").
 //
-// One persistent CTA per SM, 8 warps:
+// One persistent CTA per SM, 12 warps:
 //   warp 0 (one lane)  TMA producer: A tile 128 rows x 128 bytes, B tile 256 rows x 128 bytes
 //                      (128-byte swizzle), and the two tiles' scale factors (1-D bulk copies of
 //                      the tensor-core scale layout), into a 4-stage shared-memory ring;
@@ -14,8 +14,11 @@
 //                      kind::mxf8f6f4 E4M3 with one UE8M0 scale per 32), accumulating a 128x256
 //                      binary32 tile in tensor memory; tcgen05.commit frees the stage;
 //   warp 2             allocates / frees the 512 tensor-memory columns;
-//   warps 4..7         epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..),
-//                      times the per-tensor scales, to binary32 or bf16 in global memory.
+//   warps 4..11        epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4).. and
+//                      half (w-4)/4 of the columns), times the per-tensor scales, to binary32 or
+//                      bf16 in global memory, added into binary32, or (the fused weight-gradient
+//                      mode) applied as an SGD step to FP32 master weights with their bf16 copy
+//                      and per-expert amax written on the way.
 // Every mbarrier wait is bounded (about two seconds of SM clock); a wait that gives up sets the
 // library status word, stops the CTA's loops, drains its own copies and MMAs, and frees tensor
 // memory before the CTA exits.
@@ -34,7 +37,8 @@ constexpr int BM = 128;         // rows of A per tile (MMA M)
 constexpr int BN = 256;         // rows of B per tile (MMA N)
 constexpr int BKB = 128;        // bytes of contraction per stage (one 128-byte swizzle row)
 constexpr int STAGES = 4;
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;    // warps 0..3: producer, MMA, TMEM, spare; 4..11: epilogue
+constexpr int EPI_THREADS = 256;
 constexpr int A_TILE = BM * BKB;
 constexpr int B_TILE = BN * BKB;
 constexpr int TMEM_COLS = 512;
@@ -77,6 +81,8 @@ struct Layout {
     static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
 };
 
+enum Out : int { F32 = 0, BF16 = 1, ACC_F32 = 2, SGD = 3 };
+
 struct Args {
     const uint8_t *sfa;     // tensor-core scale layout of A
     const uint8_t *sfb;     // tensor-core scale layout of B
@@ -87,8 +93,10 @@ struct Args {
     int group_k;            // 0: groups are row ranges of A/D; 1: ranges of the contraction
     int64_t M, N, K;        // D is [M, N] per group (group_k: [E, M, N]); K = contraction length
     void *d;
-    int out_bf16;
-    int accumulate;
+    int mode;               // Out::*
+    uint16_t *w_bf16;       // Out::Sgd: the bf16 copy of the updated weights
+    float lr;               // Out::Sgd
+    unsigned int *amax;     // Out::Sgd: per-expert max |bf16 copy| as binary32 bits
     int64_t num_tiles;
     int n_tiles_n, n_tiles_m;
     int64_t sfa_tile_stride;  // atoms between consecutive 128-row tiles of A's scale layout
@@ -197,6 +205,17 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: start address, leading / stride byte offsets (16-byte units),
 // the fixed version bit 46, and the swizzle mode in bits 61..63 (2 = 128-byte, 0 = none).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(empty + s, 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_empty, EPI_THREADS);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -386,54 +405,115 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue
+        // warp w reads TMEM lanes 32*(w%4).. (its rows) and half (w-4)/4 of the tile's columns
         const int q = warp & 3;
+        const int half = (warp - 4) >> 2;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND>(p, t);
             if (!mbar_wait(tmem_full, acc_phase, abort_flag)) break;
             tc_fence_after();
+            const bool live = tl.n_stages > 0;
             float alpha = 1.0f;
             if constexpr (KIND == 0) alpha = __fmul_rn(__ldg(p.a_g_dec), __ldg(p.b_g_dec + tl.e));
             const int64_t row = tl.m0 + q * 32 + lane;
-            const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0;
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                if (tl.n_stages > 0) {
-                    tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-                } else {
+            const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0 + half * (BN / 2);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (BN / 2));
+            if (p.mode == SGD) {
+                // W32 <- W32 - lr * dW; bf16 copy; running max |bf16| for the next quantisation.
+                // 16-column sub-chunks, loads issued three sub-chunks ahead of the one processed.
+                constexpr int SUB = 16, NSUB = (BN / 2) / SUB, DIST = 3;
+                float *w = static_cast<float *>(p.d) + dbase;
+                uint16_t *wb = p.w_bf16 + dbase;
+                const float lr = p.lr;
+                uint32_t amax2 = 0;
+                float4 buf[DIST + 1][SUB / 4];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0;
+                for (int k = 0; k < DIST; ++k)
+#pragma unroll
+                    for (int j = 0; j < SUB / 4; ++j) buf[k][j] = reinterpret_cast<const float4 *>(w + k * SUB)[j];
+#pragma unroll
+                for (int k = 0; k < NSUB; ++k) {
+                    if (k + DIST < NSUB) {
+#pragma unroll
+                        for (int j = 0; j < SUB / 4; ++j)
+                            buf[(k + DIST) % (DIST + 1)][j] = reinterpret_cast<const float4 *>(w + (k + DIST) * SUB)[j];
+                    }
+                    uint32_t r[16];
+                    if (live) {
+                        tc_ld16(tbase + (uint32_t)(k * SUB), r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = 0;
+                    }
+                    float4 *cur = buf[k % (DIST + 1)];
+                    uint32_t pk[SUB / 2];
+#pragma unroll
+                    for (int j = 0; j < SUB / 4; ++j) {
+                        float4 o = cur[j];
+                        o.x = __fsub_rn(o.x, __fmul_rn(lr, __uint_as_float(r[4 * j])));
+                        o.y = __fsub_rn(o.y, __fmul_rn(lr, __uint_as_float(r[4 * j + 1])));
+                        o.z = __fsub_rn(o.z, __fmul_rn(lr, __uint_as_float(r[4 * j + 2])));
+                        o.w = __fsub_rn(o.w, __fmul_rn(lr, __uint_as_float(r[4 * j + 3])));
+                        cur[j] = o;
+                        pk[2 * j] = (uint32_t)f32_to_bf16_bits(o.x) | ((uint32_t)f32_to_bf16_bits(o.y) << 16);
+                        pk[2 * j + 1] = (uint32_t)f32_to_bf16_bits(o.z) | ((uint32_t)f32_to_bf16_bits(o.w) << 16);
+                        amax2 = __vmaxu2(amax2, pk[2 * j] & 0x7FFF7FFFu);
+                        amax2 = __vmaxu2(amax2, pk[2 * j + 1] & 0x7FFF7FFFu);
+                    }
+                    if (live) {
+                        float4 *wo = reinterpret_cast<float4 *>(w + k * SUB);
+#pragma unroll
+                        for (int j = 0; j < SUB / 4; ++j) wo[j] = cur[j];
+                        uint4 *bo = reinterpret_cast<uint4 *>(wb + k * SUB);
+                        bo[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        bo[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
                 }
-                float v[32];
+                uint32_t m = max(amax2 & 0xFFFFu, amax2 >> 16) << 16;
+                m = __reduce_max_sync(0xFFFFFFFFu, m);
+                if (lane == 0 && m) atomicMax(p.amax + tl.e, m);
+            } else {
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t r[32];
+                    if (live) {
+                        tc_ld32(tbase + (uint32_t)(c * 32), r);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
-                if (p.out_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.d) + dbase + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            w[i] = (uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i]) |
-                                   ((uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i + 1]) << 16);
-                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int i = 0; i < 32; ++i) r[i] = 0;
                     }
-                } else if (p.accumulate) {
-                    if (tl.n_stages == 0) continue;
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float4 o = dst[j];
-                        o.x = __fadd_rn(o.x, v[4 * j]);
-                        o.y = __fadd_rn(o.y, v[4 * j + 1]);
-                        o.z = __fadd_rn(o.z, v[4 * j + 2]);
-                        o.w = __fadd_rn(o.w, v[4 * j + 3]);
-                        dst[j] = o;
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
+                    if (p.mode == BF16) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.d) + dbase + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                w[i] = (uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i]) |
+                                       ((uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i + 1]) << 16);
+                            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else if (p.mode == ACC_F32) {
+                        if (!live) continue;
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float4 o = dst[j];
+                            o.x = __fadd_rn(o.x, v[4 * j]);
+                            o.y = __fadd_rn(o.y, v[4 * j + 1]);
+                            o.z = __fadd_rn(o.z, v[4 * j + 2]);
+                            o.w = __fadd_rn(o.w, v[4 * j + 3]);
+                            dst[j] = o;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) + dbase + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
             }
             tc_fence_before();
@@ -564,8 +644,7 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     a.N = N;
     a.K = K;
     a.d = d;
-    a.out_bf16 = bf16;
-    a.accumulate = 0;
+    a.mode = bf16 ? BF16 : F32;
     a.n_tiles_n = (int)(N / BN);
     a.n_tiles_m = (int)(rows_total / BM);
     a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
@@ -623,8 +702,51 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     g.N = N;
     g.K = K;
     g.d = d;
-    g.out_bf16 = bf16;
-    g.accumulate = (flags & MOE4_ACCUMULATE) != 0;
+    g.mode = bf16 ? BF16 : ((flags & MOE4_ACCUMULATE) ? ACC_F32 : F32);
+    g.sfa_tile_stride = K / 128;
+    g.sfb_tile_stride = K / 128;
+    return launch<1>(ta, tb, g, st);
+}
+
+extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
+                                            const uint8_t *b_e8, const int32_t *group_offs, int64_t E, int64_t M,
+                                            int64_t N, int64_t K, float *w32, uint16_t *w_bf16, float lr,
+                                            float *amax_out, uint32_t flags, void *ws, size_t ws_bytes,
+                                            void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && M >= 0 && M % BM == 0 && N > 0 && N % BN == 0 && K >= 0 && K % 128 == 0);
+    MOE4_CHECK_ARG(a && a_e8 && b && b_e8 && group_offs && w32 && w_bf16 && amax_out);
+    MOE4_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(a_e8) && aligned16(b_e8) && aligned16(w32) &&
+                   aligned16(w_bf16) && aligned4(amax_out));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    MOE4_CHECK_ARG(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(amax_out, 0, (size_t)E * sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (M == 0) return MOE4_OK;
+    Args g{};
+    const uint8_t *sfa = a_e8, *sfb = b_e8;
+    CUtensorMap ta, tb;
+    const int64_t Kmap = K > 0 ? K : 128;  // an empty contraction still runs the epilogue (dW = 0)
+    if (K > 0) {
+        int rc = stage_scales(a_e8, M, b_e8, N, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
+        if (rc != MOE4_OK) return rc;
+    }
+    if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BN)) return MOE4_ERR_CUDA;
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.offs = group_offs;
+    g.E = (int)E;
+    g.group_k = 1;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.d = w32;
+    g.mode = SGD;
+    g.w_bf16 = w_bf16;
+    g.lr = lr;
+    g.amax = reinterpret_cast<unsigned int *>(amax_out);
+    g.n_tiles_m = (int)(M / BM);
+    g.n_tiles_n = (int)(N / BN);
+    g.num_tiles = E * g.n_tiles_m * g.n_tiles_n;
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
     return launch<1>(ta, tb, g, st);

@@ -75,9 +75,11 @@ __device__ __forceinline__ GlobalScale global_scale(float amax) {
 }
 
 // One candidate scale (a/m) for a block of 16 scaled values y: codes (two words, nibble i =
-// element i), scale code, and the pairwise-tree sum of squared errors.
-__device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, float m, uint32_t &w0,
-                                                 uint32_t &w1, uint32_t &scode) {
+// element i), scale code, and the pairwise-tree sum of squared errors.  Every binary32 step is a
+// round-to-nearest intrinsic that is never fused into a multiply-add (a fused d*d + s would round
+// once and change near-tie choices); the products e2m1 * e4m3 are exact in f16x2.
+__device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, float m, uint32_t &w0, uint32_t &w1,
+                                                 uint32_t &scode) {
     const float t = __fdiv_rn(a, m);
     scode = e4m3_rn(t);
     const float sfv = e4m3_to_f32(scode);
@@ -98,11 +100,15 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, flo
         for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(y[i], rcp);
         w0 = e2m1x8_rn(v);
         w1 = e2m1x8_rn(v + 8);
-        float e[16];
-        e2m1x8_to_f32(w0, e);
-        e2m1x8_to_f32(w1, e + 8);
+        uint32_t sfh2 = e4m3x2_to_h2(scode | (scode << 8));
+        const __half2 sfh = *reinterpret_cast<const __half2 *>(&sfh2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) d[i] = __fsub_rn(y[i], __fmul_rn(e[i], sfv));
+        for (int i = 0; i < 8; ++i) {
+            uint32_t h = e2m1x2_to_h2((i < 4 ? w0 : w1) >> (8 * (i & 3)));
+            const float2 f = __half22float2(__hmul2(*reinterpret_cast<const __half2 *>(&h), sfh));
+            d[2 * i] = __fsub_rn(y[2 * i], f.x);
+            d[2 * i + 1] = __fsub_rn(y[2 * i + 1], f.y);
+        }
     }
     float s[16];
 #pragma unroll
@@ -114,8 +120,8 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, flo
     return s[0];
 }
 
-__device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, uint32_t &w0,
-                                            uint32_t &w1, uint32_t &scode) {
+__device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, uint32_t &w0, uint32_t &w1,
+                                            uint32_t &scode) {
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(y[i]));

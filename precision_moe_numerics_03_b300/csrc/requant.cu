@@ -21,11 +21,42 @@ constexpr int kPitch = kTileR + 4;
 
 enum class SrcKind { Nvfp4, Bf16 };
 
-template <SrcKind kind>
+// Output of one warp iteration: the 128 values of output row c (input column c) in this tile.
+// Lane l owns values 4l..4l+3; lanes 8b..8b+7 form 32-block b (amax by three shuffles).
+template <bool kSR>
+__device__ __forceinline__ void emit_row(const float4 x4, int64_t m, int64_t c, int64_t r0, int64_t R, int64_t C,
+                                         uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t, uint64_t seed,
+                                         uint32_t stream_id) {
+    const int lane = lane_id();
+    float a = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+    const int e = mx_scale_exponent(a);
+    const float s = pow2_neg(e);
+    float v0, v1, v2, v3;
+    f2_unpack(f2_mul(f2_pack(x4.x, x4.y), f2_pack(s, s)), v0, v1);
+    f2_unpack(f2_mul(f2_pack(x4.z, x4.w), f2_pack(s, s)), v2, v3);
+    const int64_t r = r0 + lane * 4;
+    const int64_t idx = (m * C + c) * R + r;
+    uint32_t packed;
+    if constexpr (kSR) {
+        const Philox4 w = sr_words4((uint64_t)idx >> 2, stream_id, seed);
+        packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
+    } else {
+        packed = e4m3x4_rn(v0, v1, v2, v3);
+    }
+    if (r < R) {
+        *reinterpret_cast<uint32_t *>(q_t + idx) = packed;
+        if ((lane & 7) == 0) e8_t[(m * C + c) * (R / 32) + (r >> 5)] = (uint8_t)(e + 127);
+    }
+}
+
+template <SrcKind kind, bool kSR>
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
-    uint8_t *__restrict__ e8_t, uint64_t seed, uint32_t stream_id, bool sr, bool sf_mma) {
+    uint8_t *__restrict__ e8_t, uint64_t seed, uint32_t stream_id, bool sf_mma) {
     __shared__ __align__(16) float tile[kTileC][kPitch];
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
     const int64_t n_ct = (C + kTileC - 1) / kTileC;
@@ -51,15 +82,22 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
                 const int64_t soff = sf_mma ? m * R * nblk + ((r >> 7) * (nblk >> 2) + (b >> 2)) * 512 + (r & 31) * 16 +
                                                   ((r >> 5) & 3) * 4 + (b & 3)
                                             : (m * R + r) * nblk + b;
-                const uint16_t s2 = __ldg(reinterpret_cast<const uint16_t *>(sf + soff));
-                const float gd = g_dec[m];
-                const float sa = e4m3_to_f32(s2 & 0xFFu), sb = e4m3_to_f32(s2 >> 8);
-                e2m1x8_to_f32(w.x, v);
-                e2m1x8_to_f32(w.y, v + 8);
-                e2m1x8_to_f32(w.z, v + 16);
-                e2m1x8_to_f32(w.w, v + 24);
+                const uint32_t sf2 = e4m3x2_to_h2(__ldg(reinterpret_cast<const uint16_t *>(sf + soff)));
+                const uint32_t sfa2 = __byte_perm(sf2, 0, 0x1010), sfb2 = __byte_perm(sf2, 0, 0x3232);
+                const uint64_t g2 = f2_pack(g_dec[m], g_dec[m]);
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], i < 16 ? sa : sb), gd);
+                for (int q = 0; q < 4; ++q) {
+                    const __half2 sfh = *reinterpret_cast<const __half2 *>(q < 2 ? &sfa2 : &sfb2);
+#pragma unroll
+                    for (int b2 = 0; b2 < 4; ++b2) {
+                        // e2m1 * e4m3 has at most 6 significant bits: exact in f16, then exact in f32
+                        uint32_t h = e2m1x2_to_h2(words[q] >> (8 * b2));
+                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&h), sfh);
+                        const float2 f = __half22float2(es);
+                        f2_unpack(f2_mul(f2_pack(f.x, f.y), g2), v[8 * q + 2 * b2], v[8 * q + 2 * b2 + 1]);
+                    }
+                }
             } else {
                 const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (m * R + r) * C + c);
 #pragma unroll
@@ -82,35 +120,15 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
     }
     __syncthreads();
 
-    // phase 2: one output row segment (128 values) per warp iteration
+    // phase 2: two output row segments (128 values each) per warp iteration
     const int lane = lane_id();
-    const int64_t nblk_out = R / 32;
-    for (int cl = warp_id(); cl < kTileC; cl += 8) {
-        const int64_t c = c0 + cl;
-        if (c >= C) break;
-        const float4 x4 = *reinterpret_cast<const float4 *>(&tile[cl][lane * 4]);
-        float a = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        const int e = mx_scale_exponent(a);
-        const float s = pow2_neg(e);
-        const float v0 = __fmul_rn(x4.x, s), v1 = __fmul_rn(x4.y, s);
-        const float v2 = __fmul_rn(x4.z, s), v3 = __fmul_rn(x4.w, s);
-        const int64_t r = r0 + lane * 4;
-        const int64_t idx = (m * C + c) * R + r;
-        uint32_t packed;
-        if (sr) {
-            const Philox4 w = sr_words4((uint64_t)idx >> 2, stream_id, seed);
-            packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) |
-                     (e4m3_sr(v3, w.w) << 24);
-        } else {
-            packed = e4m3x4_rn(v0, v1, v2, v3);
-        }
-        if (r < R) {
-            *reinterpret_cast<uint32_t *>(q_t + idx) = packed;
-            if ((lane & 7) == 0) e8_t[(m * C + c) * nblk_out + (r >> 5)] = (uint8_t)(e + 127);
-        }
+#pragma unroll 1
+    for (int cl = warp_id(); cl < kTileC; cl += 16) {
+        const int64_t ca = c0 + cl, cb = c0 + cl + 8;
+        const float4 xa = *reinterpret_cast<const float4 *>(&tile[cl][lane * 4]);
+        const float4 xb = *reinterpret_cast<const float4 *>(&tile[cl + 8][lane * 4]);
+        if (ca < C) emit_row<kSR>(xa, m, ca, r0, R, C, q_t, e8_t, seed, stream_id);
+        if (cb < C) emit_row<kSR>(xb, m, cb, r0, R, C, q_t, e8_t, seed, stream_id);
     }
 }
 
@@ -134,7 +152,6 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        if (!live) continue;
         const int e = mx_scale_exponent(a);
         const float s = pow2_neg(e);
         const float v0 = __fmul_rn(x4[0], s), v1 = __fmul_rn(x4[1], s);
@@ -142,11 +159,11 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
         uint32_t packed;
         if (sr) {
             const Philox4 w = sr_words4((uint64_t)gidx, stream_id, seed);
-            packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) |
-                     (e4m3_sr(v3, w.w) << 24);
+            packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
         } else {
             packed = e4m3x4_rn(v0, v1, v2, v3);
         }
+        if (!live) continue;
         *reinterpret_cast<uint32_t *>(q + gidx * 4) = packed;
         if ((gidx & 7) == 0) e8[gidx >> 3] = (uint8_t)(e + 127);
     }
@@ -169,8 +186,12 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     const int64_t tiles = nmat * ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
     if (tiles == 0) return MOE4_OK;
     MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-    requant_transpose_kernel<SrcKind::Nvfp4><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
-        codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, (flags & MOE4_SR) != 0, sf_mma);
+    if (flags & MOE4_SR)
+        requant_transpose_kernel<SrcKind::Nvfp4, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, sf_mma);
+    else
+        requant_transpose_kernel<SrcKind::Nvfp4, false><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, sf_mma);
     return launch_status();
 }
 
@@ -195,8 +216,12 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned4(q));
         const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
         if (tiles == 0) return MOE4_OK;
-        requant_transpose_kernel<SrcKind::Bf16><<<(unsigned)tiles, 256, 0, st>>>(
-            nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, sr, false);
+        if (sr)
+            requant_transpose_kernel<SrcKind::Bf16, true><<<(unsigned)tiles, 256, 0, st>>>(
+                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, false);
+        else
+            requant_transpose_kernel<SrcKind::Bf16, false><<<(unsigned)tiles, 256, 0, st>>>(
+                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, false);
     }
     return launch_status();
 }

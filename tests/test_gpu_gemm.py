@@ -74,6 +74,11 @@ def _nvfp4_case(rows_sizes, N, K, seed, out_bf16=False, sf_mma=False):
     # oracle path
     rac, ras, rag = oracle.nvfp4_quantize(oracle.bf16_to_f32(a_bits))
     rbc, rbs, rbg = oracle.nvfp4_quantize(oracle.bf16_to_f32(b_bits).reshape(E, N, K))
+    if not sf_mma:  # the operands themselves must already agree bit for bit
+        for got, want, name in ((ac, rac, "A codes"), (asf, ras, "A scales"), (ag, rag, "A g_dec"),
+                                (bc, rbc, "B codes"), (bsf, rbs, "B scales"), (bg, rbg, "B g_dec")):
+            g_np = to_np(got).reshape(np.shape(want))
+            assert np.array_equal(g_np, want), "%s differ in %d places" % (name, int(np.sum(g_np != want)))
     Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rac, ras, rag),
                                     oracle.nvfp4_dequantize(rbc, rbs, rbg), offs)
     return D, Dref, S
@@ -173,3 +178,35 @@ def test_mxfp8_wgrad_group_k(accumulate):
     check_f32(got, Dref, S, "mxfp8 wgrad")
     if not accumulate:
         assert np.all(got[2] == 0)
+
+
+def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd():
+    """The fused weight-gradient + SGD epilogue is bit-identical to the unfused pair, and its
+    per-expert amax equals max |bf16 copy|."""
+    rng = np.random.default_rng(23)
+    sizes = [128, 256, 0, 384]
+    E, M, N = len(sizes), 256, 512
+    offs = _offs(sizes)
+    Kt = int(offs[-1])
+    aq, ae = _mxfp8_rowwise(_bf16(rng, (M, Kt)), M, Kt)
+    bq, be = _mxfp8_rowwise(_bf16(rng, (N, Kt)), N, Kt)
+    w0 = (rng.standard_normal((E, M, N)) * 0.02).astype(np.float32)
+    lr = 1e-2
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, Kt))
+    # unfused: dW to memory, then SGD
+    dW = torch.empty((E, M, N), dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8(aq, ae, bq, be, to_dev(offs), E, M, N, Kt, dW, moe4.OUT_F32 | moe4.GROUP_K, ws)
+    w_ref = to_dev(w0)
+    wb_ref = torch.empty((E, M, N), dtype=torch.int16, device=DEV)
+    moe4.moe4_sgd_update(w_ref, dW, w_ref.numel(), lr, wb_ref)
+    # fused
+    w_f = to_dev(w0)
+    wb_f = to_dev(oracle.f32_to_bf16(w0))          # the bf16 copy that goes with w0
+    amax = torch.full((E,), -1.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8_wgrad_sgd(aq, ae, bq, be, to_dev(offs), E, M, N, Kt, w_f, wb_f, lr, amax, 0, ws)
+    assert moe4.moe4_get_status() == moe4.OK
+    torch.cuda.synchronize()
+    assert torch.equal(w_f, w_ref)
+    assert torch.equal(wb_f, wb_ref)
+    want = np.abs(oracle.bf16_to_f32(to_np(wb_ref, np.uint16))).reshape(E, -1).max(axis=1)
+    assert np.array_equal(to_np(amax), want.astype(np.float32))

@@ -231,3 +231,13 @@ def test_device_stochastic_rounding_and_words():
     ref_words0 = oracle.sr_words(0, 0, 0, n)
     assert first_mismatch(to_np(out), oracle.e4m3_sr(v, ref_words0)) is None
     assert first_mismatch(to_np(words, np.uint32), oracle.sr_words(0x0123456789ABCDEF, 5, 1 << 33, n)) is None
+
+
+def test_full_tensor_parity_small_moe_operands():
+    """Every block of the small-MoE GEMM operands: activations [8704, 2048] Student-t(3) and
+    8 experts' weights [8, 2048, 2048] N(0, 0.02)."""
+    rng = np.random.default_rng(13)
+    a = inputs.to_bf16_bits((rng.standard_t(3, (8704, 2048)) / np.sqrt(3)).astype(np.float32))
+    b = inputs.to_bf16_bits((rng.standard_normal((8 * 2048, 2048)) * 0.02).astype(np.float32))
+    _check_quant(a, 1, 8704, 2048)
+    _check_quant(b, 8, 2048, 2048)
