@@ -60,16 +60,24 @@ struct Cfg<1> {                       // MXFP8
     static constexpr int ELEMS_PER_ATOM = 128;
 };
 
-template <int KIND>
+// Epilogue staging of the fused SGD mode, per epilogue warp: two 32x32 binary32 tiles (128-byte
+// swizzle) and two 32x32 bf16 tiles (64-byte swizzle), plus two mbarriers.
+constexpr int EPI_W_TILE = 32 * 32 * 4;
+constexpr int EPI_B_TILE = 32 * 32 * 2;
+constexpr int EPI_WARP_BYTES = 2 * EPI_W_TILE + 2 * EPI_B_TILE;
+constexpr int EPI_SGD_BYTES = 8 * EPI_WARP_BYTES;
+
+template <int KIND, int NST, int EPI>
 struct Layout {
     static constexpr int SFA = Cfg<KIND>::ATOMS * 512;
     static constexpr int SFB = 2 * Cfg<KIND>::ATOMS * 512;
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_TILE;
-    static constexpr int OFF_SFA = OFF_B + STAGES * B_TILE;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB;
-    static constexpr int NBAR = 2 * STAGES + 3;  // full, empty, tmem_full, tmem_empty, drain
+    static constexpr int OFF_B = OFF_A + NST * A_TILE;
+    static constexpr int OFF_SFA = OFF_B + NST * B_TILE;
+    static constexpr int OFF_SFB = OFF_SFA + NST * SFA;
+    static constexpr int OFF_EPI = (OFF_SFB + NST * SFB + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_EPI + EPI;
+    static constexpr int NBAR = 2 * NST + 3 + 16;  // full, empty, tmem_full, tmem_empty, drain, epilogue
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
@@ -78,7 +86,8 @@ struct Layout {
     static constexpr int SF_COLS_A = Cfg<KIND>::ATOMS * 4;
     static constexpr int SF_COLS_B = Cfg<KIND>::ATOMS * 8;
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static_assert(ACC_COLS + NST * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static_assert(SMEM <= 232448, "shared memory overflow");
 };
 
 enum Out : int { F32 = 0, BF16 = 1, ACC_F32 = 2, SGD = 3 };
@@ -154,6 +163,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -273,27 +292,32 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
     return tl;
 }
 
-template <int KIND>
+template <int KIND, bool kSgd>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
-    using L = Layout<KIND>;
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWb, const Args p) {
+    // the fused SGD mode trades two operand stages for the epilogue's staging buffers
+    constexpr int NST = kSgd ? 2 : STAGES;
+    using L = Layout<KIND, NST, kSgd ? EPI_SGD_BYTES : 0>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
-    uint64_t *full = bars, *empty = bars + STAGES;
-    uint64_t *tmem_full = bars + 2 * STAGES, *tmem_empty = tmem_full + 1, *drain = tmem_full + 2;
+    uint64_t *full = bars, *empty = bars + NST;
+    uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 1, *drain = tmem_full + 2;
+    uint64_t *epi_bar = tmem_full + 3;  // fused SGD: two per epilogue warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
     const int warp = warp_id(), lane = lane_id();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, EPI_THREADS);
         mbar_init(drain, 1);
+        for (int i = 0; i < 16; ++i) mbar_init(epi_bar + i, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -312,9 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------------------- producer
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t issued_parity[STAGES];
-        bool issued[STAGES];
-        for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_parity[s] = 0;
+        uint32_t issued_parity[NST];
+        bool issued[NST];
+        for (int s = 0; s < NST; ++s) issued[s] = false, issued_parity[s] = 0;
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND>(p, t);
             for (int ks = 0; ks < tl.n_stages; ++ks) {
@@ -334,11 +358,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 issued[stage] = true;
                 issued_parity[stage] = phase;
-                if (++stage == STAGES) stage = 0, phase ^= 1u;
+                if (++stage == NST) stage = 0, phase ^= 1u;
             }
         }
         if (*abort_flag) {  // let this CTA's own copies land before the CTA can exit
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < NST; ++s)
                 if (issued[s]) {
                     const uint32_t a = smem_u32(full + s);
                     const long long t0 = clock64();
@@ -391,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tc_mma<KIND>(tmem, ad, bd, idesc, sfa_t, sfb_t, (ks > 0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty + stage);
-                    if (++stage == STAGES) stage = 0, phase ^= 1u;
+                    if (++stage == NST) stage = 0, phase ^= 1u;
                 }
                 tc_commit(tmem_full);
             }
@@ -409,6 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - 4) >> 2;
         uint32_t acc_phase = 0;
+        uint32_t epi_phase = 0;  // fused SGD: parity of this warp's two staging barriers
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND>(p, t);
             if (!mbar_wait(tmem_full, acc_phase, abort_flag)) break;
@@ -419,55 +444,81 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t row = tl.m0 + q * 32 + lane;
             const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0 + half * (BN / 2);
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (BN / 2));
-            if (p.mode == SGD) {
-                // W32 <- W32 - lr * dW; bf16 copy; running max |bf16| for the next quantisation.
-                // 16-column sub-chunks, loads issued three sub-chunks ahead of the one processed.
-                constexpr int SUB = 16, NSUB = (BN / 2) / SUB, DIST = 3;
-                float *w = static_cast<float *>(p.d) + dbase;
-                uint16_t *wb = p.w_bf16 + dbase;
+            if constexpr (kSgd) {
+                // W32 <- W32 - lr * dW, bf16 copy, running max |bf16|.  This warp owns rows
+                // 32q..32q+31 and columns half*128 .. +127 of the tile, in four 32-column chunks:
+                // TMA brings the 32x32 binary32 chunk into shared memory (128-byte swizzle: lane l's
+                // 16-byte piece j sits at piece j ^ (l & 7) of its 128-byte row), the lane updates its
+                // row in place and writes the bf16 row (64-byte swizzle: piece j at j ^ ((l >> 1) & 3)),
+                // and TMA stores both.  The next chunk's load overlaps the current chunk's math.
+                const int wi = warp - 4;
+                uint8_t *wb_smem = smem + L::OFF_EPI + wi * EPI_WARP_BYTES;
+                uint64_t *eb = epi_bar + 2 * wi;
+                const int y0 = (int)((int64_t)tl.e * p.M + tl.m0 + q * 32);
+                const int x0 = (int)(tl.n0 + half * (BN / 2));
                 const float lr = p.lr;
                 uint32_t amax2 = 0;
-                float4 buf[DIST + 1][SUB / 4];
-#pragma unroll
-                for (int k = 0; k < DIST; ++k)
-#pragma unroll
-                    for (int j = 0; j < SUB / 4; ++j) buf[k][j] = reinterpret_cast<const float4 *>(w + k * SUB)[j];
-#pragma unroll
-                for (int k = 0; k < NSUB; ++k) {
-                    if (k + DIST < NSUB) {
-#pragma unroll
-                        for (int j = 0; j < SUB / 4; ++j)
-                            buf[(k + DIST) % (DIST + 1)][j] = reinterpret_cast<const float4 *>(w + (k + DIST) * SUB)[j];
+                bool ok = true;
+                if (lane == 0) {  // chunk 0 (buffer 0); earlier stores from these buffers must be read out
+                    bulk_wait_read_all();
+                    mbar_expect_tx(eb, EPI_W_TILE);
+                    tma_load_2d(wb_smem, &tmW, eb, x0, y0);
+                }
+                __syncwarp();
+#pragma unroll 1
+                for (int c = 0; c < 4 && ok; ++c) {
+                    const int b = c & 1;
+                    if (lane == 0 && c + 1 < 4) {
+                        bulk_wait_read_all();
+                        mbar_expect_tx(eb + (b ^ 1), EPI_W_TILE);
+                        tma_load_2d(wb_smem + (b ^ 1) * EPI_W_TILE, &tmW, eb + (b ^ 1), x0 + 32 * (c + 1), y0);
                     }
-                    uint32_t r[16];
+                    __syncwarp();
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(eb + b, (epi_phase >> b) & 1u, abort_flag));
+                    epi_phase ^= 1u << b;
+                    if (!ok) break;
+                    uint32_t r[32];
                     if (live) {
-                        tc_ld16(tbase + (uint32_t)(k * SUB), r);
+                        tc_ld32(tbase + (uint32_t)(c * 32), r);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = 0;
+                        for (int i = 0; i < 32; ++i) r[i] = 0;
                     }
-                    float4 *cur = buf[k % (DIST + 1)];
-                    uint32_t pk[SUB / 2];
+                    uint8_t *wrow = wb_smem + b * EPI_W_TILE + lane * 128;
+                    uint8_t *brow = wb_smem + 2 * EPI_W_TILE + b * EPI_B_TILE + lane * 64;
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < SUB / 4; ++j) {
-                        float4 o = cur[j];
+                    for (int j = 0; j < 8; ++j) {
+                        float4 *slot = reinterpret_cast<float4 *>(wrow + ((j ^ (lane & 7)) << 4));
+                        float4 o = *slot;
                         o.x = __fsub_rn(o.x, __fmul_rn(lr, __uint_as_float(r[4 * j])));
                         o.y = __fsub_rn(o.y, __fmul_rn(lr, __uint_as_float(r[4 * j + 1])));
                         o.z = __fsub_rn(o.z, __fmul_rn(lr, __uint_as_float(r[4 * j + 2])));
                         o.w = __fsub_rn(o.w, __fmul_rn(lr, __uint_as_float(r[4 * j + 3])));
-                        cur[j] = o;
+                        *slot = o;
                         pk[2 * j] = (uint32_t)f32_to_bf16_bits(o.x) | ((uint32_t)f32_to_bf16_bits(o.y) << 16);
                         pk[2 * j + 1] = (uint32_t)f32_to_bf16_bits(o.z) | ((uint32_t)f32_to_bf16_bits(o.w) << 16);
                         amax2 = __vmaxu2(amax2, pk[2 * j] & 0x7FFF7FFFu);
                         amax2 = __vmaxu2(amax2, pk[2 * j + 1] & 0x7FFF7FFFu);
                     }
-                    if (live) {
-                        float4 *wo = reinterpret_cast<float4 *>(w + k * SUB);
 #pragma unroll
-                        for (int j = 0; j < SUB / 4; ++j) wo[j] = cur[j];
-                        uint4 *bo = reinterpret_cast<uint4 *>(wb + k * SUB);
-                        bo[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        bo[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && live) {
+                        tma_store_2d(&tmW, wb_smem + b * EPI_W_TILE, x0 + 32 * c, y0);
+                        tma_store_2d(&tmWb, wb_smem + 2 * EPI_W_TILE + b * EPI_B_TILE, x0 + 32 * c, y0);
+                        bulk_commit();
+                    }
+                }
+                if (!ok && lane == 0) {  // let this warp's own loads land before the CTA can exit
+                    for (int bb = 0; bb < 2; ++bb) {
+                        const uint32_t aa = smem_u32(eb + bb);
+                        const long long t0 = clock64();
+                        while (!mbar_try_wait(aa, (epi_phase >> bb) & 1u) && clock64() - t0 < kWaitCycles) {
+                        }
                     }
                 }
                 uint32_t m = max(amax2 & 0xFFFFu, amax2 >> 16) << 16;
@@ -520,6 +571,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
         }
+        if constexpr (kSgd) {
+            if (lane == 0) bulk_wait_all();  // this warp's stores are complete before the CTA exits
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -547,32 +601,39 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D byte tensor [rows, inner_bytes] with a box of box_rows x 128 bytes, 128-byte swizzle.
-static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int64_t rows, int box_rows) {
+// 2-D tensor [rows, inner] of `elem`-byte elements; box of box_rows x box_inner elements.
+static bool make_map_t(CUtensorMap *m, CUtensorMapDataType type, int elem, const void *base, int64_t inner,
+                       int64_t rows, int box_inner, int box_rows, CUtensorMapSwizzle swz) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)inner_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)BKB, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(inner * elem)};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND>
-static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Args &a, cudaStream_t st) {
-    using L = Layout<KIND>;
+// Operand tile: [rows, inner_bytes] bytes, box box_rows x 128 bytes, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int64_t rows, int box_rows) {
+    return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner_bytes, rows, BKB, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int KIND, bool kSgd>
+static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tw, const CUtensorMap &twb,
+                  const Args &a, cudaStream_t st) {
+    using L = Layout<KIND, kSgd ? 2 : STAGES, kSgd ? EPI_SGD_BYTES : 0>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, kSgd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::SMEM) != cudaSuccess)
             return MOE4_ERR_CUDA;
         attr_set = true;
     }
     if (a.num_tiles == 0) return MOE4_OK;
     const int64_t grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
-    grouped_gemm_kernel<KIND><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, a);
+    grouped_gemm_kernel<KIND, kSgd><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, tw, twb, a);
     return launch_status();
 }
 
@@ -650,7 +711,7 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
     a.sfa_tile_stride = K / 64;
     a.sfb_tile_stride = K / 64;
-    return launch<0>(ta, tb, a, st);
+    return launch<0, false>(ta, tb, ta, tb, a, st);
 }
 
 extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b, const uint8_t *b_e8,
@@ -705,7 +766,7 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     g.mode = bf16 ? BF16 : ((flags & MOE4_ACCUMULATE) ? ACC_F32 : F32);
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
-    return launch<1>(ta, tb, g, st);
+    return launch<1, false>(ta, tb, ta, tb, g, st);
 }
 
 extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
@@ -718,7 +779,7 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     MOE4_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(a_e8) && aligned16(b_e8) && aligned16(w32) &&
                    aligned16(w_bf16) && aligned4(amax_out));
     MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
-    MOE4_CHECK_ARG(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    MOE4_CHECK_ARG(E * M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(amax_out, 0, (size_t)E * sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
     if (M == 0) return MOE4_OK;
@@ -749,5 +810,9 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     g.num_tiles = E * g.n_tiles_m * g.n_tiles_n;
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
-    return launch<1>(ta, tb, g, st);
+    CUtensorMap tw, twb;  // the master weights and their bf16 copy as [E*M, N], 32x32 boxes
+    if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MOE4_ERR_CUDA;
+    return launch<1, true>(ta, tb, tw, twb, g, st);
 }
