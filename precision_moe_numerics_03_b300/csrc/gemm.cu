@@ -66,6 +66,16 @@ constexpr int EPI_W_TILE = 32 * 32 * 4;
 constexpr int EPI_B_TILE = 32 * 32 * 2;
 constexpr int EPI_WARP_BYTES = 2 * EPI_W_TILE + 2 * EPI_B_TILE;
 constexpr int EPI_SGD_BYTES = 8 * EPI_WARP_BYTES;
+// Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
+// TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
+// master-weight update.  Operand stages shrink to make room for the staging buffers.
+enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2 };
+constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE;
+template <int EM>
+struct EpiCfg {
+    static constexpr int NST = EM == EPI_SGD ? 2 : (EM == EPI_TMA ? 3 : STAGES);
+    static constexpr int BYTES = EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : 0);
+};
 
 template <int KIND, int NST, int EPI>
 struct Layout {
@@ -292,13 +302,14 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
     return tl;
 }
 
-template <int KIND, bool kSgd>
+template <int KIND, int EM>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWb, const Args p) {
-    // the fused SGD mode trades two operand stages for the epilogue's staging buffers
-    constexpr int NST = kSgd ? 2 : STAGES;
-    using L = Layout<KIND, NST, kSgd ? EPI_SGD_BYTES : 0>;
+    // tmW: the output D (EPI_TMA) or the master weights (EPI_SGD); tmWb: their bf16 copy (EPI_SGD)
+    constexpr bool kSgd = EM == EPI_SGD;
+    constexpr int NST = EpiCfg<EM>::NST;
+    using L = Layout<KIND, NST, EpiCfg<EM>::BYTES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -524,6 +535,53 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t m = max(amax2 & 0xFFFFu, amax2 >> 16) << 16;
                 m = __reduce_max_sync(0xFFFFFFFFu, m);
                 if (lane == 0 && m) atomicMax(p.amax + tl.e, m);
+            } else if constexpr (EM == EPI_TMA) {
+                // each 32-column chunk: registers -> swizzled 32x32 staging tile -> TMA bulk store
+                // (binary32 rows of 128 bytes with the 128-byte swizzle, bf16 rows of 64 bytes with
+                // the 64-byte swizzle; piece j of row l sits at j ^ (l & 7) or j ^ ((l >> 1) & 3))
+                uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE;
+                const int y0 = (int)((p.group_k ? (int64_t)tl.e * p.M : 0) + tl.m0 + q * 32);
+                const int x0 = (int)(tl.n0 + half * (BN / 2));
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t r[32];
+                    if (live) {
+                        tc_ld32(tbase + (uint32_t)(c * 32), r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = 0;
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
+                    if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile out
+                    __syncwarp();
+                    if (p.mode == BF16) {
+                        uint8_t *row = stage + lane * 64;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                w[i] = (uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i]) |
+                                       ((uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i + 1]) << 16);
+                            *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        uint8_t *row = stage + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(row + ((j ^ (lane & 7)) << 4)) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmW, stage, x0 + 32 * c, y0);
+                        bulk_commit();
+                    }
+                }
             } else {
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t r[32];
@@ -571,7 +629,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
         }
-        if constexpr (kSgd) {
+        if constexpr (EM != EPI_REG) {
             if (lane == 0) bulk_wait_all();  // this warp's stores are complete before the CTA exits
         }
     }
@@ -620,21 +678,28 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int6
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int KIND, bool kSgd>
+template <int KIND, int EM>
 static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tw, const CUtensorMap &twb,
                   const Args &a, cudaStream_t st) {
-    using L = Layout<KIND, kSgd ? 2 : STAGES, kSgd ? EPI_SGD_BYTES : 0>;
+    using L = Layout<KIND, EpiCfg<EM>::NST, EpiCfg<EM>::BYTES>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, kSgd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, EM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::SMEM) != cudaSuccess)
             return MOE4_ERR_CUDA;
         attr_set = true;
     }
     if (a.num_tiles == 0) return MOE4_OK;
     const int64_t grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
-    grouped_gemm_kernel<KIND, kSgd><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, tw, twb, a);
+    grouped_gemm_kernel<KIND, EM><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, tw, twb, a);
     return launch_status();
+}
+
+// The output D as [rows, N] for the TMA-store epilogue: 32x32 boxes, binary32 (128-byte swizzle)
+// or bf16 (64-byte swizzle).
+static bool make_out_map(CUtensorMap *m, void *d, bool bf16, int64_t rows, int64_t N) {
+    return bf16 ? make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, d, N, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+                : make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace gemm
@@ -711,7 +776,9 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
     a.sfa_tile_stride = K / 64;
     a.sfb_tile_stride = K / 64;
-    return launch<0, false>(ta, tb, ta, tb, a, st);
+    CUtensorMap td;
+    if (!make_out_map(&td, d, bf16, rows_total, N)) return MOE4_ERR_CUDA;
+    return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
 }
 
 extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b, const uint8_t *b_e8,
@@ -766,7 +833,10 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     g.mode = bf16 ? BF16 : ((flags & MOE4_ACCUMULATE) ? ACC_F32 : F32);
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
-    return launch<1, false>(ta, tb, ta, tb, g, st);
+    if (g.mode == ACC_F32) return launch<1, EPI_REG>(ta, tb, ta, tb, g, st);
+    CUtensorMap td;
+    if (!make_out_map(&td, d, bf16, gk ? E * M : M, N)) return MOE4_ERR_CUDA;
+    return launch<1, EPI_TMA>(ta, tb, td, td, g, st);
 }
 
 extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
@@ -814,5 +884,5 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE4_ERR_CUDA;
-    return launch<1, true>(ta, tb, tw, twb, g, st);
+    return launch<1, EPI_SGD>(ta, tb, tw, twb, g, st);
 }
