@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
                                                   _f32p]),
             "orc_hadamard_dequant": (ctypes.c_int, [_u8p, _u8p, ctypes.c_float, _i64, _i64,
                                                     _u16p]),
+            "orc_hadamard_quant_mx": (ctypes.c_int, [_f32p, _i64, _i64, _u8p, _u8p]),
+            "orc_hadamard_dequant_mx": (ctypes.c_int, [_u8p, _u8p, _i64, _i64, _u16p]),
             "orc_e2m1_rne_sat_range": (None, [ctypes.c_uint32, _u64, _u8p]),
             "orc_e4m3_rne_sat_range": (None, [ctypes.c_uint32, _u64, _u8p]),
             "orc_bf16_rne_array": (None, [_f32p, _i64, _u16p]),
@@ -347,6 +349,28 @@ def hadamard_dequant(codes, sf, g_dec) -> np.ndarray:
     out = np.empty((R, half * 2), np.uint16)
     if lib().orc_hadamard_dequant(_p(codes, _u8p), _p(sf, _u8p), float(g_dec), R, half * 2,
                                   _p(out, _u16p)) != 0:
+        raise ValueError("hadamard: cols must be a multiple of 128")
+    return out
+
+
+def hadamard_quant_mx(x: np.ndarray):
+    """The 8.25-bit return-path codec: Hadamard(128) rotation, then MXFP8 (E4M3, E8M0 per 32,
+    nearest-even).  Returns q [R, C] and e8 [R, C/32]."""
+    x = np.ascontiguousarray(x, np.float32)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    e8 = np.empty((R, C // 32), np.uint8)
+    if lib().orc_hadamard_quant_mx(_p(x, _f32p), R, C, _p(q, _u8p), _p(e8, _u8p)) != 0:
+        raise ValueError("hadamard: cols must be a multiple of 128")
+    return q, e8
+
+
+def hadamard_dequant_mx(q, e8) -> np.ndarray:
+    q = np.ascontiguousarray(q, np.uint8)
+    e8 = np.ascontiguousarray(e8, np.uint8)
+    R, C = q.shape
+    out = np.empty((R, C), np.uint16)
+    if lib().orc_hadamard_dequant_mx(_p(q, _u8p), _p(e8, _u8p), R, C, _p(out, _u16p)) != 0:
         raise ValueError("hadamard: cols must be a multiple of 128")
     return out
 

@@ -469,6 +469,39 @@ int orc_hadamard_dequant(const uint8_t *codes, const uint8_t *sf, float g_dec, i
 }
 
 /* ============================================================================================
+ * The 8.25-bit return-path codec [LHC, communication paragraph: after the Hadamard transform the
+ * return path is quantised with per-block scales, cutting its payload from sixteen to 8.25 bits
+ * per value].  The pages name the element format "S2F6" without defining it.  Reading: 8.25 bits
+ * is an 8-bit element plus one 8-bit scale per 32 values, i.e. the MXFP8 layout used elsewhere in
+ * the recipe: E4M3 elements, E8M0 scales by the ceiling rule, nearest-even rounding (the return
+ * path belongs to the forward pass, for which the pages mention no stochastic rounding).
+ * ========================================================================================== */
+int orc_hadamard_quant_mx(const float *x, int64_t rows, int64_t cols, uint8_t *q, uint8_t *e8)
+{
+    if (cols % 128 != 0) return -1;
+    float *rot = (float *)malloc(sizeof(float) * (size_t)(rows * cols));
+    if (!rot) return -2;
+    orc_hadamard_rotate(x, rows, cols, rot);
+    int rc = orc_mxfp8_quantize_rows(rot, rows, cols, 0, 0, 0, 0, q, e8);
+    free(rot);
+    return rc;
+}
+
+int orc_hadamard_dequant_mx(const uint8_t *q, const uint8_t *e8, int64_t rows, int64_t cols, uint16_t *out_bf16)
+{
+    if (cols % 128 != 0) return -1;
+    float *xh = (float *)malloc(sizeof(float) * (size_t)(rows * cols));
+    float *rot = (float *)malloc(sizeof(float) * (size_t)(rows * cols));
+    if (!xh || !rot) { free(xh); free(rot); return -2; }
+    orc_mxfp8_dequantize_rows(q, e8, rows, cols, xh);
+    orc_hadamard_rotate(xh, rows, cols, rot);
+    for (int64_t i = 0; i < rows * cols; ++i) out_bf16[i] = (uint16_t)orc_bf16_rne(rot[i]);
+    free(xh);
+    free(rot);
+    return 0;
+}
+
+/* ============================================================================================
  * Array helpers for the cast tests: convert the binary32 bit patterns start .. start+count-1.
  * ========================================================================================== */
 void orc_e2m1_rne_sat_range(uint32_t start, uint64_t count, uint8_t *out)

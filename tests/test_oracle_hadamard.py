@@ -85,3 +85,39 @@ def test_codec_definition_and_round_trip(orc):
     # blocks a spike only coarsens its own block, and the rotation spreads it over eight)
     err_h = np.linalg.norm(back - x) / np.linalg.norm(x)
     assert err_h < 0.1
+
+
+def test_mx_codec_is_8_25_bits_per_value(orc):
+    # the pages' return-path payload: sixteen -> 8.25 bits per value
+    x = np.random.default_rng(3).standard_normal((64, 512)).astype(np.float32)
+    q, e8 = orc.hadamard_quant_mx(x)
+    assert (q.nbytes + e8.nbytes) * 8 / x.size == 8.25
+    assert 16 / ((q.nbytes + e8.nbytes) * 8 / x.size) == 16 / 8.25
+
+
+def test_mx_codec_definition_and_round_trip(orc):
+    rng = np.random.default_rng(4)
+    x = rng.standard_t(3, (128, 256)).astype(np.float32)
+    x[rng.random(x.shape) < 0.003] *= 100
+    q, e8 = orc.hadamard_quant_mx(x)
+    q2, e82 = orc.mxfp8_quantize_rows(orc.hadamard_rotate(x), sr=False)
+    assert np.array_equal(q, q2) and np.array_equal(e8, e82)
+    back = orc.bf16_to_f32(orc.hadamard_dequant_mx(q, e8))
+    want = orc.bf16_to_f32(orc.f32_to_bf16(orc.hadamard_rotate(orc.mxfp8_dequantize(q, e8))))
+    assert np.array_equal(back, want)
+    # 8-bit elements: the round trip is far tighter than the 4-bit codec's
+    err_mx = np.linalg.norm(back - x) / np.linalg.norm(x)
+    cq, sq, gq = orc.hadamard_quant(x)
+    err_fp4 = np.linalg.norm(orc.bf16_to_f32(orc.hadamard_dequant(cq, sq, gq)) - x) / np.linalg.norm(x)
+    assert err_mx < 0.05 and err_mx < err_fp4 / 2
+
+
+def test_mx_codec_spreads_a_spike(orc):
+    # a lone spike forces a large scale on its 32-block without the rotation; rotated, every value
+    # of its 128-chunk is the same size and the chunk's other values keep their precision
+    x = np.full((1, 128), 0.01, np.float32)
+    x[0, 5] = 1000.0
+    q, e8 = orc.hadamard_quant_mx(x)
+    assert len(set(e8[0].tolist())) == 1          # four equal block scales after rotation
+    qp, e8p = orc.mxfp8_quantize_rows(x, sr=False)
+    assert e8p[0, 0] > e8p[0, 1]                 # without it, the spike's block scale stands out
