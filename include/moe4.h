@@ -69,6 +69,7 @@ extern "C" {
 #define MOE4_GROUP_K        0x02000u /* grouped GEMM: groups are ranges of the contraction */
 #define MOE4_ACCUMULATE     0x04000u /* grouped GEMM: D += result (binary32 output only) */
 #define MOE4_SF_MMA_LAYOUT  0x10000u /* scale factors are in the tensor-core tile layout */
+#define MOE4_MXFP8          0x20000u /* Hadamard codec: the 8.25-bit MXFP8 variant */
 
 /* ------------------------------------------------------------------ library */
 int moe4_version(void);                      /* e.g. 100 for 0.1.0 */
@@ -155,7 +156,12 @@ int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, ui
  * rotated by the Sylvester-ordered Hadamard matrix (butterflies of span 1, 2, ..., 64, then
  * times RN(1/sqrt(128))) in binary32, and the rotated tensor is NVFP4-quantised as above (its
  * own amax; Four Over Six per flags).  ws: moe4_workspace_size(MOE4_OP_HADAMARD_QUANT).
- * hadamard_dequant: NVFP4 dequantise, the same rotation (it is its own inverse), bf16 out. */
+ * hadamard_dequant: NVFP4 dequantise, the same rotation (it is its own inverse), bf16 out.
+ * With MOE4_MXFP8 (the only flag then), the 8.25-bit variant [LHC communication: the return path
+ * falls from sixteen to 8.25 bits per value]: after the rotation each 32-block is quantised to
+ * MXFP8 (E4M3 elements, E8M0 scale by the ceiling rule, nearest-even) in one pass; `codes` is
+ * E4M3 [rows, cols], `sf` is E8M0 [rows, cols/32], g_dec and ws are not used (may be NULL).
+ * hadamard_dequant with MOE4_MXFP8 reads that layout. */
 int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *sf,
                    float *g_dec, uint32_t flags, void *ws, size_t ws_bytes, void *stream);
 int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t rows,

@@ -214,6 +214,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_codes) {
     return h;
 }
 
+__device__ __forceinline__ float2 h2_bits_to_f2(uint32_t h) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

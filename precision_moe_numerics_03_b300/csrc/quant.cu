@@ -392,6 +392,51 @@ __global__ void __launch_bounds__(256) hadamard_dequant_kernel(const uint8_t *__
     }
 }
 
+// The 8.25-bit return-path codec: Hadamard(128), then MXFP8 (E4M3 elements, one E8M0 scale per 32
+// by the ceiling rule, nearest-even).  One pass: the scales are per 32-block.  A warp holds one
+// 128-chunk (lane l: elements 4l..4l+3); lanes 8b..8b+7 form 32-block b.
+__global__ void __launch_bounds__(256) hadamard_quant_mx_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                int64_t cols, uint8_t *__restrict__ q,
+                                                                uint8_t *__restrict__ e8) {
+    const int64_t chunks = rows * (cols / 128);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = lane_id();
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
+        float u[4];
+        load_chunk_bf16(x + ch * 128 + lane * 4, u);
+        fwht128_warp(u);
+        float a = fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3])));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+        const int e = mx_scale_exponent(a);
+        const float s = pow2_neg(e);
+        *reinterpret_cast<uint32_t *>(q + ch * 128 + lane * 4) =
+            e4m3x4_rn(__fmul_rn(u[0], s), __fmul_rn(u[1], s), __fmul_rn(u[2], s), __fmul_rn(u[3], s));
+        if ((lane & 7) == 0) e8[ch * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+    }
+}
+
+__global__ void __launch_bounds__(256) hadamard_dequant_mx_kernel(const uint8_t *__restrict__ q,
+                                                                  const uint8_t *__restrict__ e8, int64_t rows,
+                                                                  int64_t cols, uint16_t *__restrict__ out) {
+    const int64_t chunks = rows * (cols / 128);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = lane_id();
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
+        const uint32_t codes = *reinterpret_cast<const uint32_t *>(q + ch * 128 + lane * 4);
+        const uint32_t b = e8[ch * 4 + (lane >> 3)];
+        const float scale = __uint_as_float(b ? (b << 23) : 0x00400000u);  // 2^(b-127), exact
+        const float2 lo = h2_bits_to_f2(e4m3x2_to_h2(codes & 0xFFFFu));  // E4M3 -> f16 is exact
+        const float2 hi = h2_bits_to_f2(e4m3x2_to_h2(codes >> 16));
+        float u[4] = {__fmul_rn(lo.x, scale), __fmul_rn(lo.y, scale), __fmul_rn(hi.x, scale), __fmul_rn(hi.y, scale)};
+        fwht128_warp(u);
+        const uint32_t w0 = (uint32_t)f32_to_bf16_bits(u[0]) | ((uint32_t)f32_to_bf16_bits(u[1]) << 16);
+        const uint32_t w1 = (uint32_t)f32_to_bf16_bits(u[2]) | ((uint32_t)f32_to_bf16_bits(u[3]) << 16);
+        *reinterpret_cast<uint2 *>(out + ch * 128 + lane * 4) = make_uint2(w0, w1);
+    }
+}
+
 static int grid_for(int64_t work_items, int threads, int per_sm) {
     const int64_t need = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms() * per_sm;
@@ -454,6 +499,14 @@ extern "C" int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const f
 extern "C" int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *sf,
                               float *g_dec, uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
     MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0);
+    if (flags & MOE4_MXFP8) {  // the 8.25-bit codec: codes = E4M3 [rows, cols], sf = E8M0 [rows, cols/32]
+        MOE4_CHECK_ARG(flags == MOE4_MXFP8 && codes && sf && (rows == 0 || (x && aligned16(x))) && aligned4(codes));
+        const int64_t chunks = rows * (cols / 128);
+        if (chunks == 0) return MOE4_OK;
+        hadamard_quant_mx_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(x, rows, cols, codes,
+                                                                                                 sf);
+        return launch_status();
+    }
     MOE4_CHECK_ARG(codes && sf && g_dec && (rows == 0 || (x && aligned16(x))));
     MOE4_CHECK_ARG((flags & ~MOE4_FOUR_OVER_SIX) == 0);
     if (!ws || ws_bytes < sizeof(unsigned int)) return MOE4_ERR_WORKSPACE;
@@ -470,7 +523,15 @@ extern "C" int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uin
 
 extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t rows,
                                 int64_t cols, uint16_t *out_bf16, uint32_t flags, void *stream) {
-    MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0 && flags == 0);
+    MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0 && (flags == 0 || flags == MOE4_MXFP8));
+    if (flags == MOE4_MXFP8) {
+        MOE4_CHECK_ARG(codes && sf && out_bf16 && aligned16(out_bf16) && aligned4(codes));
+        const int64_t chunks = rows * (cols / 128);
+        if (chunks == 0) return MOE4_OK;
+        hadamard_dequant_mx_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, rows,
+                                                                                                   cols, out_bf16);
+        return launch_status();
+    }
     MOE4_CHECK_ARG(codes && sf && g_dec && out_bf16 && aligned16(out_bf16));
     const int64_t chunks = rows * (cols / 128);
     if (chunks == 0) return MOE4_OK;

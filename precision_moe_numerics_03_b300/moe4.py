@@ -26,6 +26,7 @@ GROUP_M = 0x01000
 GROUP_K = 0x02000
 ACCUMULATE = 0x04000
 SF_MMA_LAYOUT = 0x10000
+MXFP8 = 0x20000
 
 OP_NVFP4_QUANTIZE = 1
 OP_HADAMARD_QUANT = 2

@@ -171,6 +171,96 @@ def test_hadamard_codec(shape):
     assert first_mismatch(to_np(out, np.uint16), ref) is None
 
 
+def _mx_codec(x_dev, rows, cols):
+    q = empty_u8(rows, cols)
+    e8 = empty_u8(rows, cols // 32)
+    moe4.hadamard_quant(x_dev, rows, cols, q, e8, None, moe4.MXFP8)
+    out = torch.empty((rows, cols), dtype=torch.int16, device=DEV)
+    moe4.hadamard_dequant(q, e8, None, rows, cols, out, moe4.MXFP8)
+    torch.cuda.synchronize()
+    return q, e8, out
+
+
+@pytest.mark.parametrize("shape", [(4, 128), (37, 256), (256, 512), (3, 4096)])
+def test_hadamard_mx_codec(shape):
+    """The 8.25-bit variant (rotation, then MXFP8 per 32) against the oracle, bit for bit; row 0
+    is all zero and row 1 tiny (scales in the subnormal range)."""
+    rows, cols = shape
+    rng = np.random.default_rng(100 + rows)
+    x = rng.standard_t(3, (rows, cols)).astype(np.float32)
+    x[rng.random(x.shape) < 0.003] *= 50
+    x[0] = 0.0
+    x[1] *= 1e-36
+    xb = inputs.to_bf16_bits(x)
+    q, e8, out = _mx_codec(to_dev(xb), rows, cols)
+    rq, re = oracle.hadamard_quant_mx(oracle.bf16_to_f32(xb))
+    assert first_mismatch(to_np(q), rq) is None
+    assert first_mismatch(to_np(e8), re) is None
+    assert first_mismatch(to_np(out, np.uint16), oracle.hadamard_dequant_mx(rq, re)) is None
+
+
+def test_hadamard_mx_dequant_arbitrary_codes():
+    """Decoder alone on codes the encoder would not emit: every non-NaN E4M3 byte, scales from
+    2^-127 (E8M0 byte 0) up to 2^13."""
+    rows, cols = 64, 1024
+    rng = np.random.default_rng(7)
+    finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    q = rng.choice(finite, (rows, cols))
+    e8 = rng.integers(0, 141, (rows, cols // 32)).astype(np.uint8)
+    e8[0] = 0
+    out = torch.empty((rows, cols), dtype=torch.int16, device=DEV)
+    moe4.hadamard_dequant(to_dev(q), to_dev(e8), None, rows, cols, out, moe4.MXFP8)
+    torch.cuda.synchronize()
+    assert first_mismatch(to_np(out, np.uint16), oracle.hadamard_dequant_mx(q, e8)) is None
+
+
+def _codec_full_size_input():
+    rows, cols = 131072, 4096  # the return-path tensor of 16384 tokens x top-8 at d = 4096
+    g = inputs.device_generator(5, 0, DEV)
+    return rows, cols, inputs.device_student_t((rows, cols), g, DEV).view(torch.int16)
+
+
+def test_hadamard_codecs_full_size_sampled_rows():
+    rows, cols, xb = _codec_full_size_input()
+    host = to_np(xb, np.uint16)
+    sample = np.concatenate([np.random.default_rng(5).choice(rows, 48, replace=False), [0, rows - 1]])
+    xs = oracle.bf16_to_f32(host[sample])
+
+    q, e8, out = _mx_codec(xb, rows, cols)
+    rq, re = oracle.hadamard_quant_mx(xs)
+    assert first_mismatch(to_np(q[sample]), rq) is None
+    assert first_mismatch(to_np(e8[sample]), re) is None
+    assert first_mismatch(to_np(out[sample], np.uint16), oracle.hadamard_dequant_mx(rq, re)) is None
+    del q, e8
+
+    codes = empty_u8(rows, cols // 2)
+    sf = empty_u8(rows, cols // 16)
+    gd = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT))
+    moe4.hadamard_quant(xb, rows, cols, codes, sf, gd, moe4.FOUR_OVER_SIX, ws)
+    moe4.hadamard_dequant(codes, sf, gd, rows, cols, out)
+    torch.cuda.synchronize()
+    amax = 0.0
+    for r0 in range(0, rows, 8192):  # the rotated tensor's amax sets the per-tensor scale
+        amax = max(amax, float(np.abs(oracle.hadamard_rotate(oracle.bf16_to_f32(host[r0:r0 + 8192]))).max()))
+    rc, rs, rg = oracle.nvfp4_quantize(oracle.hadamard_rotate(xs), amax=amax)
+    assert to_np(gd)[0] == rg
+    assert first_mismatch(to_np(codes[sample]), rc) is None
+    assert first_mismatch(to_np(sf[sample]), rs) is None
+    assert first_mismatch(to_np(out[sample], np.uint16), oracle.hadamard_dequant(rc, rs, rg)) is None
+
+
+def test_hadamard_mx_codec_empty_and_bad_flags():
+    q = empty_u8(1, 128)
+    e8 = empty_u8(1, 4)
+    moe4.hadamard_quant(None, 0, 128, q, e8, None, moe4.MXFP8)
+    x = torch.zeros((1, 128), dtype=torch.int16, device=DEV)
+    with pytest.raises(RuntimeError):
+        moe4.hadamard_quant(x, 1, 128, q, e8, None, moe4.MXFP8 | moe4.FOUR_OVER_SIX)
+    with pytest.raises(RuntimeError):
+        moe4.hadamard_quant(x, 1, 96, q, e8, None, moe4.MXFP8)
+
+
 def _device_patterns(start, count):
     bits = torch.arange(start, start + count, dtype=torch.int64, device=DEV)
     return (bits - (bits >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32).view(torch.float32)
