@@ -258,6 +258,69 @@ class LayerStep:
         return b
 
 
+def measure_next_rows(step, reps=3):
+    """Rows beyond the layer step, timed after it on the same routed batch (not part of `value`):
+    the MXFP8 forward kept for the final layers (bf16 -> MXFP8 nearest-even quantisation of X, of
+    both expert weights and of H, the MXFP8 row gather, the rows-grouped MXFP8 GEMMs for gate/up and
+    down with SwiGLU between them), and the 8.25-bit Hadamard + MXFP8 return-path codec."""
+    torch, m = step.torch, step.m
+    T, d, f, E, k, Rp, dev = step.T, step.d, step.f, step.E, step.k, step.Rp, step.dev
+    u8 = dict(dtype=torch.uint8, device=dev)
+    Xq, Xe = torch.empty((T, d), **u8), torch.empty((T, d // 32), **u8)
+    Xpq, Xpe = torch.empty((Rp, d), **u8), torch.empty((Rp, d // 32), **u8)
+    Gq, Ge = torch.empty((E, 2 * f, d), **u8), torch.empty((E, 2 * f, d // 32), **u8)
+    Dq, De = torch.empty((E, d, f), **u8), torch.empty((E, d, f // 32), **u8)
+    Hq, He = torch.empty((Rp, f), **u8), torch.empty((Rp, f // 32), **u8)
+    Cq, Ce = torch.empty((Rp, d), **u8), torch.empty((Rp, d // 32), **u8)
+    ws = m.workspace(max(m.moe4_workspace_size_gemm(1, Rp, E, 2 * f, d), m.moe4_workspace_size_gemm(1, Rp, E, d, f)),
+                     dev)
+    R, GM = m.ROWWISE, m.GROUP_M
+
+    def fwd(tm):
+        with tm("mx_quant"):
+            m.mxfp8_quantize(step.X, T, d, Xq, Xe, 0, 0, R)
+            m.moe4_permute_nvfp4(Xq, Xe, T, d, step.src_of, Rp, Xpq, Xpe, m.MXFP8)
+            m.mxfp8_quantize(step.Wb_gu, E * 2 * f, d, Gq, Ge, 0, 0, R)
+            m.mxfp8_quantize(step.Wb_d, E * d, f, Dq, De, 0, 0, R)
+        with tm("gemm_mxfp8_fwd"):
+            m.grouped_gemm_mxfp8(Xpq, Xpe, Gq, Ge, step.offs, E, Rp, 2 * f, d, step.GU, m.OUT_F32 | GM, ws)
+        with tm("mx_quant"):
+            m.moe4_swiglu(step.GU[:Rp], Rp, f, step.H[:Rp])
+            m.mxfp8_quantize(step.H[:Rp], Rp, f, Hq, He, 0, 0, R)
+        with tm("gemm_mxfp8_fwd"):
+            m.grouped_gemm_mxfp8(Hq, He, Dq, De, step.offs, E, Rp, d, f, step.Y, m.OUT_BF16 | GM, ws)
+        with tm("codec_mx"):
+            m.hadamard_quant(step.Y[:Rp], Rp, d, Cq, Ce, None, m.MXFP8)
+            m.hadamard_dequant(Cq, Ce, None, Rp, d, step.Yhat[:Rp], m.MXFP8)
+
+    for _ in range(2):
+        fwd(_NullTimer())
+    torch.cuda.synchronize()
+    timer = EventTimer(torch)
+    for _ in range(reps):
+        fwd(timer)
+    torch.cuda.synchronize()
+    if m.moe4_get_status() != m.OK:
+        raise RuntimeError("a device wait timed out in the MXFP8 forward")
+    per = {n: t / reps for n, t in timer.totals().items()}
+    fwd_flops = step.gemm_flops()[0]
+    rows = T * k
+    codec_bytes = rows * d * (2 + 1.03125 + 1.03125 + 2)
+    return {
+        "mxfp8_forward": {
+            "gemm_ms": round(per["gemm_mxfp8_fwd"], 4),
+            "gemm_TFLOP/s": round(fwd_flops / (per["gemm_mxfp8_fwd"] / 1e3) / 1e12, 1),
+            "quant_swiglu_ms": round(per["mx_quant"], 4),
+            "note": "bf16 -> MXFP8 (nearest-even) of X, W_gu, W_d and H + gather + SwiGLU; same routed batch",
+        },
+        "hadamard_mxfp8_codec": {
+            "ms": round(per["codec_mx"], 4),
+            "GB/s": round(codec_bytes / (per["codec_mx"] / 1e3) / 1e9, 1),
+            "bits_per_value": 8.25,
+        },
+    }
+
+
 class _NullTimer:
     def __call__(self, name):
         return self
@@ -524,6 +587,7 @@ def main():
     ap.add_argument("--small", action="store_true", help="the small 8-expert shapes (a quick check, not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
                              "gemm_mxfp8_dgrad", "sgd"],
@@ -656,6 +720,15 @@ def main():
         e2e = {"value": world * step_flops * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s / args.steps * 1e3}
 
+    nxt = None
+    if not args.no_next:
+        nxt = measure_next_rows(step)
+        mf = nxt["mxfp8_forward"]
+        mf["nvfp4_gemm_ms"] = round(per["gemm_nvfp4"], 4)
+        mf["nvfp4_gemm_speedup"] = round(mf["gemm_ms"] / per["gemm_nvfp4"], 3)
+        mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["swiglu_quant_h"], 4)
+        nxt["hadamard_mxfp8_codec"]["nvfp4_codec_ms"] = round(per["hadamard"], 4)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, secs = oracle_sample_step(seed=0)
@@ -681,6 +754,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches,
             "cpu_baseline": cpu,
+            "next_rows": nxt,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

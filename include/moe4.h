@@ -241,7 +241,9 @@ int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64_t E, int32
 /* moe4_permute_nvfp4: gather NVFP4 rows: out row r = input row src_of[r], or zeros (codes 0,
  * scale 0) when src_of[r] < 0; r < rows_total.  codes [T, cols/2], sf [T, cols/16] canonical;
  * cols % 32 == 0.  With MOE4_SF_MMA_LAYOUT the output scales are written in the tensor-core tile
- * layout (rows_total % 128 == 0, cols % 64 == 0). */
+ * layout (rows_total % 128 == 0, cols % 64 == 0).  With MOE4_MXFP8 (alone) the rows are MXFP8
+ * instead: codes [T, cols] E4M3, sf [T, cols/32] E8M0, padding rows all-zero bytes — the
+ * dispatch of the MXFP8 forward pass of the final layers [DEBUT] confirmed list, [4WEEK]. */
 int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64_t T, int64_t cols,
                        const int32_t *src_of, int64_t rows_total, uint8_t *out_codes,
                        uint8_t *out_sf, uint32_t flags, void *stream);

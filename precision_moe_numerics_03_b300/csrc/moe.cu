@@ -144,14 +144,15 @@ __global__ void __launch_bounds__(32) plan_assign_kernel(const int32_t *__restri
 
 // ------------------------------------------------------------------ NVFP4 row gather
 // One warp per dispatched row: codes in 16-byte pieces, scales in 8-byte pieces (or bytes).
-__global__ void __launch_bounds__(256) permute_nvfp4_kernel(const uint8_t *__restrict__ codes,
-                                                            const uint8_t *__restrict__ sf, int64_t cols,
-                                                            const int32_t *__restrict__ src_of, int64_t rows_total,
-                                                            uint8_t *__restrict__ out_codes,
-                                                            uint8_t *__restrict__ out_sf, bool sf_mma) {
+// One warp per dispatched row.  A row is cbytes of codes (NVFP4: cols/2, MXFP8: cols) and sbytes
+// of scales (NVFP4: cols/16, MXFP8: cols/32).
+__global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t *__restrict__ codes,
+                                                           const uint8_t *__restrict__ sf, int64_t cbytes,
+                                                           int64_t sbytes, const int32_t *__restrict__ src_of,
+                                                           int64_t rows_total, uint8_t *__restrict__ out_codes,
+                                                           uint8_t *__restrict__ out_sf, bool sf_mma) {
     const int lane = lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t cbytes = cols / 2, sbytes = cols / 16;
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); r < rows_total; r += warps) {
         const int32_t src = src_of[r];
         uint4 *dc = reinterpret_cast<uint4 *>(out_codes + r * cbytes);
@@ -354,12 +355,13 @@ extern "C" int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64
     MOE4_CHECK_ARG(T >= 0 && cols > 0 && cols % 32 == 0 && rows_total >= 0);
     MOE4_CHECK_ARG(src_of && out_codes && out_sf && (T == 0 || (codes && sf)));
     MOE4_CHECK_ARG(aligned16(codes) && aligned16(out_codes) && aligned16(sf) && aligned16(out_sf));
-    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    MOE4_CHECK_ARG(flags == 0 || flags == MOE4_SF_MMA_LAYOUT || flags == MOE4_MXFP8);
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    const bool mx = (flags & MOE4_MXFP8) != 0;
     MOE4_CHECK_ARG(!sf_mma || (rows_total % 128 == 0 && cols % 64 == 0));
     if (rows_total == 0) return MOE4_OK;
-    permute_nvfp4_kernel<<<grid_cap(rows_total * 32, 256, 16), 256, 0, as_stream(stream)>>>(
-        codes, sf, cols, src_of, rows_total, out_codes, out_sf, sf_mma);
+    permute_rows_kernel<<<grid_cap(rows_total * 32, 256, 16), 256, 0, as_stream(stream)>>>(
+        codes, sf, mx ? cols : cols / 2, mx ? cols / 32 : cols / 16, src_of, rows_total, out_codes, out_sf, sf_mma);
     return launch_status();
 }
 
