@@ -44,6 +44,10 @@ WORKLOAD = "inkling-moe-layer-step: T=16384 d=4096 f=2048 E=384 top8, NVFP4 fwd 
 SMALL = dict(T=4096, d=2048, f=1024, E=8, k=2)
 METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
+# DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
+# case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
+TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2696.8 / 2753.6}
+GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 4, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
 
 
 def load_peaks():
@@ -685,6 +689,11 @@ def main():
         ach = gbytes[dom] / (t_dom / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
                 "traffic": None, "kernel": dom}
+    nl = GROUP_LAUNCHES.get(dom, 1)
+    roof["launches_per_step"] = nl
+    if dom in TRAFFIC_RATIO:
+        roof["traffic"] = TRAFFIC_RATIO[dom] * gbytes[dom] / nl
+        roof["traffic_note"] = "DRAM bytes per launch: ncu ratio on a 16-expert capture x algorithmic bytes"
     roof["peak_source"] = peaks["src"]
     req_t = per.get("requant", 0.0)
     requant_gbs = gbytes["requant"] / (req_t / 1e3) / 1e9 if req_t else None
