@@ -6,7 +6,7 @@
 namespace moe4 {
 
 __global__ void __launch_bounds__(256) convert_kernel(int kind, const float *__restrict__ in, int64_t n,
-                                                      void *__restrict__ out) {
+                                                      void *__restrict__ out, const PhiloxKeys keys) {
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n / 4; q += (int64_t)gridDim.x * blockDim.x) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(in) + q);
         if (kind == 0) {
@@ -23,17 +23,16 @@ __global__ void __launch_bounds__(256) convert_kernel(int kind, const float *__r
             const uint32_t hi = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
             reinterpret_cast<uint2 *>(out)[q] = make_uint2(lo, hi);
         } else {
-            const Philox4 w = sr_words4((uint64_t)q, 0u, 0ull);
-            reinterpret_cast<uint32_t *>(out)[q] =
-                e4m3_sr(v.x, w.x) | (e4m3_sr(v.y, w.y) << 8) | (e4m3_sr(v.z, w.z) << 16) | (e4m3_sr(v.w, w.w) << 24);
+            // the kernels' four-at-a-time rounding (integer fast path, per-element path otherwise)
+            reinterpret_cast<uint32_t *>(out)[q] = e4m3x4_sr(v.x, v.y, v.z, v.w, sr_words4((uint64_t)q, 0u, keys));
         }
     }
 }
 
-__global__ void __launch_bounds__(256) sr_words_kernel(uint64_t seed, uint32_t stream_id, uint64_t j0, int64_t nq,
+__global__ void __launch_bounds__(256) sr_words_kernel(const PhiloxKeys keys, uint32_t stream_id, uint64_t j0, int64_t nq,
                                                        uint4 *__restrict__ out) {
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nq; q += (int64_t)gridDim.x * blockDim.x) {
-        const Philox4 w = sr_words4(j0 + (uint64_t)q, stream_id, seed);
+        const Philox4 w = sr_words4(j0 + (uint64_t)q, stream_id, keys);
         out[q] = make_uint4(w.x, w.y, w.z, w.w);
     }
 }
@@ -97,7 +96,7 @@ extern "C" int moe4_convert(int kind, const float *in, int64_t n, void *out, voi
     if (n == 0) return MOE4_OK;
     int64_t grid = (n / 4 + 255) / 256;
     if (grid > (int64_t)num_sms() * 16) grid = (int64_t)num_sms() * 16;
-    convert_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(kind, in, n, out);
+    convert_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(kind, in, n, out, philox_keys(0));
     return launch_status();
 }
 
@@ -107,7 +106,7 @@ extern "C" int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_bas
     if (n == 0) return MOE4_OK;
     int64_t grid = (n / 4 + 255) / 256;
     if (grid > (int64_t)num_sms() * 16) grid = (int64_t)num_sms() * 16;
-    sr_words_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(seed, stream_id, idx_base / 4, n / 4,
+    sr_words_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(philox_keys(seed), stream_id, idx_base / 4, n / 4,
                                                                    reinterpret_cast<uint4 *>(out));
     return launch_status();
 }

@@ -104,30 +104,45 @@ struct Philox4 {
     uint32_t x, y, z, w;
 };
 
+// The ten round keys of one (k0, k1) = (lo(seed), hi(seed)): round i uses k0 + i*0x9E3779B9 and
+// k1 + i*0xBB67AE85.  Computed on the host and passed by value as a kernel parameter, so each key
+// is read from the constant bank as an operand of the round's three-input XOR.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+static inline PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        k.k0[i] = a;
+        k.k1[i] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
+    }
+    return k;
+}
+
 __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 uint32_t k0, uint32_t k1) {
+                                                 const PhiloxKeys K) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         // high and low halves as two multiplies (measured cheaper on this GPU than one 64-bit
         // product: ~96 versus ~122 issue slots per call)
         const uint32_t hi0 = __umulhi(c0, 0xD2511F53u), lo0 = c0 * 0xD2511F53u;
         const uint32_t hi1 = __umulhi(c2, 0xCD9E8D57u), lo1 = c2 * 0xCD9E8D57u;
-        const uint32_t n0 = hi1 ^ c1 ^ k0;
-        const uint32_t n2 = hi0 ^ c3 ^ k1;
+        const uint32_t n0 = hi1 ^ c1 ^ K.k0[r];
+        const uint32_t n2 = hi0 ^ c3 ^ K.k1[r];
         c1 = lo1;
         c3 = lo0;
         c0 = n0;
         c2 = n2;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
     }
     return {c0, c1, c2, c3};
 }
 
 // The four stochastic-rounding words of output indices 4j .. 4j+3.
-__device__ __forceinline__ Philox4 sr_words4(uint64_t j, uint32_t stream_id, uint64_t seed) {
-    return philox4x32_10((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+__device__ __forceinline__ Philox4 sr_words4(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
+    return philox4x32_10((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, K);
 }
 
 // ------------------------------------------------------------------ MXFP8 scale and rounding
@@ -166,6 +181,27 @@ __device__ __forceinline__ uint32_t e4m3_sr(float v, uint32_t r) {
     if (e4m3_is_normal(bits)) return e4m3_sr_normal(bits, r);
     if ((bits & 0x7FFFFFFFu) == 0u) return (bits >> 24) & 0x80u;
     return e4m3_sr_small(bits, r);
+}
+// Four values at once (byte i = element i).  When each is zero or has |v| >= 2^-6 (the usual
+// case) the decision is made by integer addition: adding (~r) >> 12 = 2^20 - 1 - (r >> 12) to the
+// binary32 bits carries into bit 20 exactly when (r >> 12) < low20, i.e. when r < low20 * 2^12,
+// the rule above; masking the low 20 bits then leaves the chosen E4M3 value (|v| <= 448 keeps the
+// carry below the sign bit and the result finite), which the nearest-even conversion returns
+// unchanged.  Any other lane takes the per-element path.
+__device__ __forceinline__ uint32_t e4m3x4_sr(float v0, float v1, float v2, float v3, const Philox4 w) {
+    const uint32_t b0 = __float_as_uint(v0), b1 = __float_as_uint(v1);
+    const uint32_t b2 = __float_as_uint(v2), b3 = __float_as_uint(v3);
+    // 2*bits - 2 (mod 2^32) drops the sign and sends +-0 to the top: >= 2*0x3C800000 - 2 iff the
+    // value is zero or at least 2^-6 in magnitude
+    const uint32_t t = min(min(b0 * 2u - 2u, b1 * 2u - 2u), min(b2 * 2u - 2u, b3 * 2u - 2u));
+    if (t >= 0x78FFFFFEu) {
+        const float m0 = __uint_as_float((b0 + (~w.x >> 12)) & 0xFFF00000u);
+        const float m1 = __uint_as_float((b1 + (~w.y >> 12)) & 0xFFF00000u);
+        const float m2 = __uint_as_float((b2 + (~w.z >> 12)) & 0xFFF00000u);
+        const float m3 = __uint_as_float((b3 + (~w.w >> 12)) & 0xFFF00000u);
+        return e4m3x4_rn(m0, m1, m2, m3);
+    }
+    return e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
 }
 // ------------------------------------------------------------------ packed binary32 pairs
 // mul/add/sub.rn.f32x2: two IEEE round-to-nearest operations in one instruction.  The compiler may

@@ -25,8 +25,8 @@ enum class SrcKind { Nvfp4, Bf16 };
 // Lane l owns values 4l..4l+3; lanes 8b..8b+7 form 32-block b (amax by three shuffles).
 template <bool kSR>
 __device__ __forceinline__ void emit_row(const float4 x4, int64_t m, int64_t c, int64_t r0, int64_t R, int64_t C,
-                                         uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t, uint64_t seed,
-                                         uint32_t stream_id) {
+                                         uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
+                                         const PhiloxKeys keys, uint32_t stream_id) {
     const int lane = lane_id();
     float a = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
@@ -41,8 +41,7 @@ __device__ __forceinline__ void emit_row(const float4 x4, int64_t m, int64_t c, 
     const int64_t idx = (m * C + c) * R + r;
     uint32_t packed;
     if constexpr (kSR) {
-        const Philox4 w = sr_words4((uint64_t)idx >> 2, stream_id, seed);
-        packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
+        packed = e4m3x4_sr(v0, v1, v2, v3, sr_words4((uint64_t)idx >> 2, stream_id, keys));
     } else {
         packed = e4m3x4_rn(v0, v1, v2, v3);
     }
@@ -56,7 +55,7 @@ template <SrcKind kind, bool kSR>
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
-    uint8_t *__restrict__ e8_t, uint64_t seed, uint32_t stream_id, bool sf_mma) {
+    uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma) {
     __shared__ __align__(16) float tile[kTileC][kPitch];
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
     const int64_t n_ct = (C + kTileC - 1) / kTileC;
@@ -127,15 +126,15 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
         const int64_t ca = c0 + cl, cb = c0 + cl + 8;
         const float4 xa = *reinterpret_cast<const float4 *>(&tile[cl][lane * 4]);
         const float4 xb = *reinterpret_cast<const float4 *>(&tile[cl + 8][lane * 4]);
-        if (ca < C) emit_row<kSR>(xa, m, ca, r0, R, C, q_t, e8_t, seed, stream_id);
-        if (cb < C) emit_row<kSR>(xb, m, cb, r0, R, C, q_t, e8_t, seed, stream_id);
+        if (ca < C) emit_row<kSR>(xa, m, ca, r0, R, C, q_t, e8_t, keys, stream_id);
+        if (cb < C) emit_row<kSR>(xb, m, cb, r0, R, C, q_t, e8_t, keys, stream_id);
     }
 }
 
 // Row-wise MXFP8 of bf16 x [R, C]: 8 lanes per 32-block along C, 4 values per lane.
 __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__restrict__ x, int64_t R, int64_t C,
                                                             uint8_t *__restrict__ q, uint8_t *__restrict__ e8,
-                                                            uint64_t seed, uint32_t stream_id, bool sr) {
+                                                            const PhiloxKeys keys, uint32_t stream_id, bool sr) {
     const int64_t groups = R * C / 4;  // one group of 4 values per thread
     for (int64_t gidx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gidx - (threadIdx.x & 31) < groups;
          gidx += (int64_t)gridDim.x * blockDim.x) {
@@ -158,8 +157,7 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
         const float v2 = __fmul_rn(x4[2], s), v3 = __fmul_rn(x4[3], s);
         uint32_t packed;
         if (sr) {
-            const Philox4 w = sr_words4((uint64_t)gidx, stream_id, seed);
-            packed = e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
+            packed = e4m3x4_sr(v0, v1, v2, v3, sr_words4((uint64_t)gidx, stream_id, keys));
         } else {
             packed = e4m3x4_rn(v0, v1, v2, v3);
         }
@@ -188,10 +186,10 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
     if (flags & MOE4_SR)
         requant_transpose_kernel<SrcKind::Nvfp4, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
-            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, sf_mma);
+            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
     else
         requant_transpose_kernel<SrcKind::Nvfp4, false><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
-            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, seed, stream_id, sf_mma);
+            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
     return launch_status();
 }
 
@@ -211,17 +209,17 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         int64_t grid = (groups + 255) / 256;
         const int64_t cap = (int64_t)num_sms() * 8;
         if (grid > cap) grid = cap;
-        mxfp8_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(x, rows, cols, q, e8, seed, stream_id, sr);
+        mxfp8_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(x, rows, cols, q, e8, philox_keys(seed), stream_id, sr);
     } else {
         MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned4(q));
         const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
         if (tiles == 0) return MOE4_OK;
         if (sr)
             requant_transpose_kernel<SrcKind::Bf16, true><<<(unsigned)tiles, 256, 0, st>>>(
-                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, false);
+                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
         else
             requant_transpose_kernel<SrcKind::Bf16, false><<<(unsigned)tiles, 256, 0, st>>>(
-                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, seed, stream_id, false);
+                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
     }
     return launch_status();
 }

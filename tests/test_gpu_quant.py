@@ -313,6 +313,15 @@ def test_device_stochastic_rounding_and_words():
     n = 1 << 20
     v = (rng.standard_normal(n) * np.exp2(rng.integers(-14, 8, n))).astype(np.float32)
     v = np.clip(v, -448, 448).astype(np.float32)
+    # edges of the four-at-a-time fast path: signed zeros, 2^-6 and its neighbours, 448, values
+    # just under the top of a binade (carry into the exponent); the first groups of four are pure
+    # edge cases, later ones mix one tiny value into normal ones
+    edges = np.array([0.0, -0.0, 2.0 ** -6, -2.0 ** -6, np.nextafter(np.float32(2.0 ** -6), np.float32(0)),
+                      -np.nextafter(np.float32(2.0 ** -6), np.float32(0)), 448.0, -448.0, 447.9, 415.9,
+                      np.nextafter(np.float32(1.0), np.float32(0)), 1.0, 1e-30, -3e-3, 2.0 ** -9, 0.0],
+                     np.float32)
+    v[:edges.size] = edges
+    v[1024:1024 + 4 * 64:4] = edges[np.arange(64) % edges.size]
     out = torch.empty(n, dtype=torch.uint8, device=DEV)
     moe4.moe4_convert(3, to_dev(v), n, out)
     words = torch.empty(n, dtype=torch.int32, device=DEV)
