@@ -234,208 +234,207 @@ __global__ void __launch_bounds__(256) nvfp4_dequant_kernel(
 }
 
 // ------------------------------------------------------------------ Hadamard(128)
-// A warp holds one 128-chunk, lane l elements 4l..4l+3.  Butterfly span h pairs element i (bit h
-// clear) with i+h: the lower one becomes u[i] + u[i+h], the upper one u[i] - u[i+h].  Spans 1 and
-// 2 are inside a lane, spans 4..64 pair lane l with lane l ^ (h/4).
-__device__ __forceinline__ void fwht128_warp(float u[4]) {
-    float a0 = __fadd_rn(u[0], u[1]), a1 = __fsub_rn(u[0], u[1]);
-    float a2 = __fadd_rn(u[2], u[3]), a3 = __fsub_rn(u[2], u[3]);
-    u[0] = __fadd_rn(a0, a2);
-    u[2] = __fsub_rn(a0, a2);
-    u[1] = __fadd_rn(a1, a3);
-    u[3] = __fsub_rn(a1, a3);
+// One thread per 16 consecutive values (an NVFP4 block): 8 consecutive lanes hold one 128-chunk,
+// lane l its sub-block l % 8, so a warp covers four chunks.  Butterfly span h pairs element i (bit
+// h clear) with i+h: the lower one becomes u[i] + u[i+h], the upper one u[i] - u[i+h], each one
+// binary32 rounding, spans in the order 1, 2, ..., 64.  Spans 1..8 are inside a thread; spans
+// 16, 32, 64 pair lane l with lane l ^ 1, ^2, ^4, where fma(+-1, own, partner) rounds the exact
+// sum or difference once, as the add or subtract would.
+__device__ __forceinline__ void fwht128_sub16(float u[16]) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if ((i & h) == 0) {
+                const float a = u[i], b = u[i + h];
+                u[i] = __fadd_rn(a, b);
+                u[i + h] = __fsub_rn(a, b);
+            }
     const int lane = lane_id();
 #pragma unroll
-    for (int lm = 1; lm < 32; lm <<= 1) {
-        const bool upper = (lane & lm) != 0;
+    for (int lm = 1; lm < 8; lm <<= 1) {
+        const float sgn = (lane & lm) ? -1.0f : 1.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float p = __shfl_xor_sync(0xFFFFFFFFu, u[j], lm);
-            u[j] = upper ? __fsub_rn(p, u[j]) : __fadd_rn(u[j], p);
-        }
+        for (int i = 0; i < 16; ++i) u[i] = __fmaf_rn(sgn, u[i], __shfl_xor_sync(0xFFFFFFFFu, u[i], lm));
     }
     const float c = __uint_as_float(0x3DB504F3u);  // nearest binary32 to 1/sqrt(128)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) u[j] = __fmul_rn(u[j], c);
+    for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], c);
 }
 
-__device__ __forceinline__ void load_chunk_bf16(const uint16_t *p, float u[4]) {
-    const uint2 q = *reinterpret_cast<const uint2 *>(p);
-    u[0] = bf16_lo(q.x);
-    u[1] = bf16_hi(q.x);
-    u[2] = bf16_lo(q.y);
-    u[3] = bf16_hi(q.y);
-}
-
-__global__ void __launch_bounds__(256) hadamard_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                            int64_t cols, unsigned int *__restrict__ amax_bits) {
-    const int64_t chunks = rows * (cols / 128);
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    float best = 0.0f;
-    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
-        float u[4];
-        load_chunk_bf16(x + ch * 128 + lane_id() * 4, u);
-        fwht128_warp(u);
+__device__ __forceinline__ void load16_bf16(const uint16_t *p, float u[16]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(p);
+    const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) best = fmaxf(best, fabsf(u[j]));
+    for (int i = 0; i < 8; ++i) {
+        u[2 * i] = bf16_lo(w[i]);
+        u[2 * i + 1] = bf16_hi(w[i]);
     }
-    uint32_t b = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(best));
+}
+
+__device__ __forceinline__ void store16_bf16(uint16_t *p, const float u[16]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = (uint32_t)f32_to_bf16_bits(u[2 * i]) | ((uint32_t)f32_to_bf16_bits(u[2 * i + 1]) << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(p);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// The grid-stride loops run over warp-sized groups of sub-blocks so that every lane of a warp
+// takes part in the shuffles; lanes past the end compute on zeros and store nothing.  `nsub` (the
+// number of 16-value sub-blocks) is a multiple of 8, so a chunk is always whole.
+#define MOE4_SUB16_LOOP(nsub)                                                                             \
+    for (int64_t b0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) & ~int64_t(31); b0 < (nsub);      \
+         b0 += (int64_t)gridDim.x * blockDim.x)
+
+__global__ void __launch_bounds__(256) hadamard_amax_kernel(const uint16_t *__restrict__ x, int64_t nsub,
+                                                            unsigned int *__restrict__ amax_bits) {
+    float best = 0.0f;
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        float u[16];
+        if (b < nsub) {
+            load16_bf16(x + b * 16, u);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = 0.0f;
+        }
+        fwht128_sub16(u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) best = fmaxf(best, fabsf(u[i]));
+    }
+    uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(best));
     __shared__ uint32_t part[8];
-    if (lane_id() == 0) part[warp_id()] = b;
+    if (lane_id() == 0) part[warp_id()] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t m = 0;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, part[i]);
-        if (m) atomicMax(amax_bits, m);
+        uint32_t v = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) v = max(v, part[i]);
+        if (v) atomicMax(amax_bits, v);
     }
 }
 
-// Four values of a 16-block held by four consecutive lanes (lane%4 = quarter q): one candidate.
-__device__ __forceinline__ float quarter_candidate(const float y[4], float a, float m, uint32_t &bits16,
-                                                   uint32_t &scode) {
-    const float t = __fdiv_rn(a, m);
-    scode = e4m3_rn(t);
-    const float sfv = e4m3_to_f32(scode);
-    float d[4];
-    if (sfv == 0.0f) {
-        bits16 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            bits16 |= (__float_as_uint(y[i]) >> 31) << (4 * i + 3);
-            d[i] = y[i];
-        }
-    } else {
-        const float rcp = __fdiv_rn(1.0f, sfv);
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[i] = __fmul_rn(y[i], rcp);
-            v[i + 4] = 0.0f;
-        }
-        bits16 = e2m1x8_rn(v) & 0xFFFFu;
-        float e[8];
-        e2m1x8_to_f32(bits16, e);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d[i] = __fsub_rn(y[i], __fmul_rn(e[i], sfv));
-    }
-    // the block's pairwise tree: offsets 8 and 4 cross lanes (quarters q^2, q^1), 2 and 1 inside
-    float s[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = __fmul_rn(d[i], d[i]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = __fadd_rn(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 2));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = __fadd_rn(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 1));
-    s[0] = __fadd_rn(s[0], s[2]);
-    s[1] = __fadd_rn(s[1], s[3]);
-    s[0] = __fadd_rn(s[0], s[1]);
-    // the quarter-0 lane holds the block's sum; broadcast it to the other three
-    return __shfl_sync(0xFFFFFFFFu, s[0], lane_id() & ~3);
-}
-
-__global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                             int64_t cols, const unsigned int *__restrict__ amax_bits,
+// Rotate, scale by the tensor's g_enc, and quantise each 16-block with the block quantiser.
+__global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__restrict__ x, int64_t nsub,
+                                                             const unsigned int *__restrict__ amax_bits,
                                                              bool four_over_six, uint8_t *__restrict__ codes,
                                                              uint8_t *__restrict__ sf, float *__restrict__ g_dec) {
     const GlobalScale gs = global_scale(__uint_as_float(*amax_bits));
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_dec = gs.dec;
-    const int64_t chunks = rows * (cols / 128);
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int lane = lane_id();
-    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
-        float u[4];
-        load_chunk_bf16(x + ch * 128 + lane * 4, u);
-        fwht128_warp(u);
-        float y[4];
-        float a = 0.0f;
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        const bool live = b < nsub;
+        float u[16];
+        if (live) {
+            load16_bf16(x + b * 16, u);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            y[j] = __fmul_rn(u[j], gs.enc);
-            a = fmaxf(a, fabsf(y[j]));
+            for (int i = 0; i < 16; ++i) u[i] = 0.0f;
         }
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        uint32_t bits, scode;
-        const float err6 = quarter_candidate(y, a, 6.0f, bits, scode);
-        if (four_over_six) {
-            uint32_t b4, s4;
-            const float err4 = quarter_candidate(y, a, 4.0f, b4, s4);
-            if (err4 < err6) {
-                bits = b4;
-                scode = s4;
-            }
+        fwht128_sub16(u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], gs.enc);
+        uint32_t w0, w1, scode;
+        nvfp4_block(u, four_over_six, w0, w1, scode);
+        if (live) {
+            *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
+            sf[b] = (uint8_t)scode;
         }
-        *reinterpret_cast<uint16_t *>(codes + ch * 64 + lane * 2) = (uint16_t)bits;
-        if ((lane & 3) == 0) sf[ch * 8 + (lane >> 2)] = (uint8_t)scode;
     }
 }
 
 __global__ void __launch_bounds__(256) hadamard_dequant_kernel(const uint8_t *__restrict__ codes,
                                                                const uint8_t *__restrict__ sf,
-                                                               const float *__restrict__ g_dec, int64_t rows,
-                                                               int64_t cols, uint16_t *__restrict__ out) {
-    const int64_t chunks = rows * (cols / 128);
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int lane = lane_id();
+                                                               const float *__restrict__ g_dec, int64_t nsub,
+                                                               uint16_t *__restrict__ out) {
     const float gd = *g_dec;
-    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
-        const uint32_t bits = *reinterpret_cast<const uint16_t *>(codes + ch * 64 + lane * 2);
-        const float sfv = e4m3_to_f32(sf[ch * 8 + (lane >> 2)]);
-        float e[8], u[4];
-        e2m1x8_to_f32(bits, e);
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        const bool live = b < nsub;
+        float u[16];
+        if (live) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(codes + b * 8);
+            const float sfv = e4m3_to_f32(sf[b]);
+            float e[16];
+            e2m1x8_to_f32(w.x, e);
+            e2m1x8_to_f32(w.y, e + 8);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) u[j] = __fmul_rn(__fmul_rn(e[j], sfv), gd);
-        fwht128_warp(u);
-        const uint32_t lo = (uint32_t)f32_to_bf16_bits(u[0]) | ((uint32_t)f32_to_bf16_bits(u[1]) << 16);
-        const uint32_t hi = (uint32_t)f32_to_bf16_bits(u[2]) | ((uint32_t)f32_to_bf16_bits(u[3]) << 16);
-        *reinterpret_cast<uint2 *>(out + ch * 128 + lane * 4) = make_uint2(lo, hi);
+            for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(__fmul_rn(e[i], sfv), gd);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = 0.0f;
+        }
+        fwht128_sub16(u);
+        if (live) store16_bf16(out + b * 16, u);
     }
 }
 
 // The 8.25-bit return-path codec: Hadamard(128), then MXFP8 (E4M3 elements, one E8M0 scale per 32
-// by the ceiling rule, nearest-even).  One pass: the scales are per 32-block.  A warp holds one
-// 128-chunk (lane l: elements 4l..4l+3); lanes 8b..8b+7 form 32-block b.
-__global__ void __launch_bounds__(256) hadamard_quant_mx_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                                int64_t cols, uint8_t *__restrict__ q,
-                                                                uint8_t *__restrict__ e8) {
-    const int64_t chunks = rows * (cols / 128);
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int lane = lane_id();
-    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
-        float u[4];
-        load_chunk_bf16(x + ch * 128 + lane * 4, u);
-        fwht128_warp(u);
-        float a = fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3])));
+// by the ceiling rule, nearest-even).  One pass: the scales are per 32-block, which is the
+// sub-block pair of lanes 2k and 2k+1 (block amax by one shuffle).
+__global__ void __launch_bounds__(256) hadamard_quant_mx_kernel(const uint16_t *__restrict__ x, int64_t nsub,
+                                                                uint8_t *__restrict__ q, uint8_t *__restrict__ e8) {
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        const bool live = b < nsub;
+        float u[16];
+        if (live) {
+            load16_bf16(x + b * 16, u);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = 0.0f;
+        }
+        fwht128_sub16(u);
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(u[i]));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
         const int e = mx_scale_exponent(a);
         const float s = pow2_neg(e);
-        *reinterpret_cast<uint32_t *>(q + ch * 128 + lane * 4) =
-            e4m3x4_rn(__fmul_rn(u[0], s), __fmul_rn(u[1], s), __fmul_rn(u[2], s), __fmul_rn(u[3], s));
-        if ((lane & 7) == 0) e8[ch * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = e4m3x4_rn(__fmul_rn(u[4 * j], s), __fmul_rn(u[4 * j + 1], s), __fmul_rn(u[4 * j + 2], s),
+                             __fmul_rn(u[4 * j + 3], s));
+        if (live) {
+            *reinterpret_cast<uint4 *>(q + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            if ((b & 1) == 0) e8[b >> 1] = (uint8_t)(e + 127);
+        }
     }
 }
 
 __global__ void __launch_bounds__(256) hadamard_dequant_mx_kernel(const uint8_t *__restrict__ q,
-                                                                  const uint8_t *__restrict__ e8, int64_t rows,
-                                                                  int64_t cols, uint16_t *__restrict__ out) {
-    const int64_t chunks = rows * (cols / 128);
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int lane = lane_id();
-    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp_id(); ch < chunks; ch += warps) {
-        const uint32_t codes = *reinterpret_cast<const uint32_t *>(q + ch * 128 + lane * 4);
-        const uint32_t b = e8[ch * 4 + (lane >> 3)];
-        const float scale = __uint_as_float(b ? (b << 23) : 0x00400000u);  // 2^(b-127), exact
-        const float2 lo = h2_bits_to_f2(e4m3x2_to_h2(codes & 0xFFFFu));  // E4M3 -> f16 is exact
-        const float2 hi = h2_bits_to_f2(e4m3x2_to_h2(codes >> 16));
-        float u[4] = {__fmul_rn(lo.x, scale), __fmul_rn(lo.y, scale), __fmul_rn(hi.x, scale), __fmul_rn(hi.y, scale)};
-        fwht128_warp(u);
-        const uint32_t w0 = (uint32_t)f32_to_bf16_bits(u[0]) | ((uint32_t)f32_to_bf16_bits(u[1]) << 16);
-        const uint32_t w1 = (uint32_t)f32_to_bf16_bits(u[2]) | ((uint32_t)f32_to_bf16_bits(u[3]) << 16);
-        *reinterpret_cast<uint2 *>(out + ch * 128 + lane * 4) = make_uint2(w0, w1);
+                                                                  const uint8_t *__restrict__ e8, int64_t nsub,
+                                                                  uint16_t *__restrict__ out) {
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        const bool live = b < nsub;
+        float u[16];
+        if (live) {
+            const uint4 codes = *reinterpret_cast<const uint4 *>(q + b * 16);
+            const uint32_t eb = e8[b >> 1];
+            const float scale = __uint_as_float(eb ? (eb << 23) : 0x00400000u);  // 2^(eb-127), exact
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 lo = h2_bits_to_f2(e4m3x2_to_h2(cw[j] & 0xFFFFu));  // E4M3 -> f16 is exact
+                const float2 hi = h2_bits_to_f2(e4m3x2_to_h2(cw[j] >> 16));
+                u[4 * j] = __fmul_rn(lo.x, scale);
+                u[4 * j + 1] = __fmul_rn(lo.y, scale);
+                u[4 * j + 2] = __fmul_rn(hi.x, scale);
+                u[4 * j + 3] = __fmul_rn(hi.y, scale);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = 0.0f;
+        }
+        fwht128_sub16(u);
+        if (live) store16_bf16(out + b * 16, u);
     }
 }
+#undef MOE4_SUB16_LOOP
 
 static int grid_for(int64_t work_items, int threads, int per_sm) {
     const int64_t need = (work_items + threads - 1) / threads;
@@ -500,24 +499,23 @@ extern "C" int hadamard_quant(const uint16_t *x, int64_t rows, int64_t cols, uin
                               float *g_dec, uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
     MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0);
     if (flags & MOE4_MXFP8) {  // the 8.25-bit codec: codes = E4M3 [rows, cols], sf = E8M0 [rows, cols/32]
-        MOE4_CHECK_ARG(flags == MOE4_MXFP8 && codes && sf && (rows == 0 || (x && aligned16(x))) && aligned4(codes));
-        const int64_t chunks = rows * (cols / 128);
-        if (chunks == 0) return MOE4_OK;
-        hadamard_quant_mx_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(x, rows, cols, codes,
-                                                                                                 sf);
+        MOE4_CHECK_ARG(flags == MOE4_MXFP8 && codes && sf && (rows == 0 || (x && aligned16(x))) && aligned16(codes));
+        const int64_t nsub = rows * (cols / 16);
+        if (nsub == 0) return MOE4_OK;
+        hadamard_quant_mx_kernel<<<grid_for(nsub, 256, 8), 256, 0, as_stream(stream)>>>(x, nsub, codes, sf);
         return launch_status();
     }
-    MOE4_CHECK_ARG(codes && sf && g_dec && (rows == 0 || (x && aligned16(x))));
+    MOE4_CHECK_ARG(codes && sf && g_dec && aligned16(codes) && (rows == 0 || (x && aligned16(x))));
     MOE4_CHECK_ARG((flags & ~MOE4_FOUR_OVER_SIX) == 0);
     if (!ws || ws_bytes < sizeof(unsigned int)) return MOE4_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
     unsigned int *amax_bits = static_cast<unsigned int *>(ws);
     if (cudaMemsetAsync(amax_bits, 0, sizeof(unsigned int), st) != cudaSuccess) return MOE4_ERR_CUDA;
-    const int64_t chunks = rows * (cols / 128);
-    const int grid = grid_for(chunks * 32 > 1 ? chunks * 32 : 1, 256, 8);
-    if (chunks > 0) hadamard_amax_kernel<<<grid, 256, 0, st>>>(x, rows, cols, amax_bits);
-    hadamard_quant_kernel<<<grid, 256, 0, st>>>(x, rows, cols, amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0,
-                                                codes, sf, g_dec);
+    const int64_t nsub = rows * (cols / 16);
+    const int grid = grid_for(nsub > 1 ? nsub : 1, 256, 8);
+    if (nsub > 0) hadamard_amax_kernel<<<grid, 256, 0, st>>>(x, nsub, amax_bits);
+    hadamard_quant_kernel<<<grid, 256, 0, st>>>(x, nsub, amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0, codes, sf,
+                                                g_dec);
     return launch_status();
 }
 
@@ -525,18 +523,16 @@ extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const f
                                 int64_t cols, uint16_t *out_bf16, uint32_t flags, void *stream) {
     MOE4_CHECK_ARG(rows >= 0 && cols > 0 && cols % 128 == 0 && (flags == 0 || flags == MOE4_MXFP8));
     if (flags == MOE4_MXFP8) {
-        MOE4_CHECK_ARG(codes && sf && out_bf16 && aligned16(out_bf16) && aligned4(codes));
-        const int64_t chunks = rows * (cols / 128);
-        if (chunks == 0) return MOE4_OK;
-        hadamard_dequant_mx_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, rows,
-                                                                                                   cols, out_bf16);
+        MOE4_CHECK_ARG(codes && sf && out_bf16 && aligned16(out_bf16) && aligned16(codes));
+        const int64_t nsub = rows * (cols / 16);
+        if (nsub == 0) return MOE4_OK;
+        hadamard_dequant_mx_kernel<<<grid_for(nsub, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, nsub, out_bf16);
         return launch_status();
     }
-    MOE4_CHECK_ARG(codes && sf && g_dec && out_bf16 && aligned16(out_bf16));
-    const int64_t chunks = rows * (cols / 128);
-    if (chunks == 0) return MOE4_OK;
-    hadamard_dequant_kernel<<<grid_for(chunks * 32, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, rows,
-                                                                                            cols, out_bf16);
+    MOE4_CHECK_ARG(codes && sf && g_dec && out_bf16 && aligned16(out_bf16) && aligned16(codes));
+    const int64_t nsub = rows * (cols / 16);
+    if (nsub == 0) return MOE4_OK;
+    hadamard_dequant_kernel<<<grid_for(nsub, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, nsub, out_bf16);
     return launch_status();
 }
 
