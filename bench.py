@@ -192,9 +192,8 @@ class LayerStep:
         # ---------------- backward
         with tm("mxfp8_quant"):
             m.moe4_combine_backward(self.dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYp[:Rp])
-            m.mxfp8_quantize(self.dYp[:Rp], Rp, d, self.dYr_q, self.dYr_e, 0, 0, m.ROWWISE)
-            m.mxfp8_quantize(self.dYp[:Rp], Rp, d, self.dYc_q, self.dYc_e, 0, 0, m.COLWISE)
-        n += 3
+            m.mxfp8_quantize_rowcol(self.dYp[:Rp], Rp, d, self.dYr_q, self.dYr_e, self.dYc_q, self.dYc_e)
+        n += 2
         with tm("requant"):
             m.mxfp8_requant_transpose_sr(self.Wd_c, self.Wd_s, self.Wd_g, E, d, f, self.WdT_q, self.WdT_e, seed, 1,
                                          m.SR | MMA)
@@ -213,9 +212,8 @@ class LayerStep:
             m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
         n += 1
         with tm("mxfp8_quant"):
-            m.mxfp8_quantize(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, 0, 0, m.ROWWISE)
-            m.mxfp8_quantize(self.dGU[:Rp], Rp, 2 * f, self.dGUc_q, self.dGUc_e, 0, 0, m.COLWISE)
-        n += 2
+            m.mxfp8_quantize_rowcol(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, self.dGUc_q, self.dGUc_e)
+        n += 1
         with tm("requant"):
             m.mxfp8_requant_transpose_sr(self.Wgu_c, self.Wgu_s, self.Wgu_g, E, 2 * f, d, self.WguT_q, self.WguT_e,
                                          seed, 3, m.SR | MMA)
@@ -248,7 +246,8 @@ class LayerStep:
         b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
                            rows * f * nv + live * d * f * nv + rows * d * 2)
         b["requant"] = (w_gu + w_d + rows * (f + d)) * (nv + mx)
-        b["mxfp8_quant"] = rows * d * (2 + 2 + 2 * mx) + T * d * 2 + rows * 2 * f * (2 * 2 + 2 * mx)
+        # combine backward (read dy, write dYp) + one read of dYp and dGU for both MXFP8 layouts
+        b["mxfp8_quant"] = rows * d * (2 + 2 + 2 * mx) + T * d * 2 + rows * 2 * f * (2 + 2 * mx)
         b["gemm_mxfp8_dgrad"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +          # down
                                  rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2)   # gate/up
         # wgrad operands + the SGD epilogue: read W32, write W32 and the bf16 copy
@@ -527,6 +526,20 @@ def profile_case(name):
             w32 = torch.randn((E * 2 * f * d,), generator=g(1), device=dev)
             dw = torch.randn((E * 2 * f * d,), generator=g(2), device=dev)
             calls.append(lambda: moe4.moe4_sgd_update(w32, dw, w32.numel(), LR, w.view(-1)))
+    elif name in ("mxfp8_rowcol", "hadamard"):
+        rows = 32768                     # a quarter of the routed rows at d_model 4096: 268 MB of bf16
+        x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
+        if name == "mxfp8_rowcol":
+            qr, er = torch.empty((rows, d), **u8), torch.empty((rows, d // 32), **u8)
+            qc, ec = torch.empty((d, rows), **u8), torch.empty((d, rows // 32), **u8)
+            calls.append(lambda: moe4.mxfp8_quantize_rowcol(x, rows, d, qr, er, qc, ec))
+        else:
+            c, s_ = torch.empty((rows, d // 2), **u8), torch.empty((rows, d // 16), **u8)
+            gd = torch.empty(1, dtype=torch.float32, device=dev)
+            ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT), dev)
+            out = torch.empty((rows, d), dtype=torch.int16, device=dev)
+            calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws))
+            calls.append(lambda: moe4.hadamard_dequant(c, s_, gd, rows, d, out))
     elif name == "gemm_nvfp4":
         rows = 128 * 64
         x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
@@ -594,7 +607,7 @@ def main():
     ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
-                             "gemm_mxfp8_dgrad", "sgd"],
+                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
     if args.profile_case:

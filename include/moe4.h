@@ -151,6 +151,15 @@ int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const fl
 int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, uint8_t *e8,
                    uint64_t seed, uint32_t stream_id, uint32_t flags, void *stream);
 
+/* mxfp8_quantize_rowcol: both layouts of mxfp8_quantize from one read of x, nearest-even (the
+ * backward's dY and dGU feed the rows-grouped dgrad row-wise and the contraction-grouped wgrad
+ * transposed [DEBUT] confirmed list).  q_row [rows, cols], e8_row [rows, cols/32]; q_col
+ * [cols, rows], e8_col [cols, rows/32]; the bytes equal those of the two single-layout calls.
+ * rows % 32 == 0, cols % 32 == 0; x and q_row 16-byte aligned; flags must be 0. */
+int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q_row,
+                          uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
+                          void *stream);
+
 /* ------------------------------------------------------------------ Hadamard codec [LHC comms]
  * hadamard_quant: x bf16 [rows, cols], cols % 128 == 0.  Each contiguous 128-chunk of a row is
  * rotated by the Sylvester-ordered Hadamard matrix (butterflies of span 1, 2, ..., 64, then

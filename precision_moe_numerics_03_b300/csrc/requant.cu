@@ -51,11 +51,32 @@ __device__ __forceinline__ void emit_row(const float4 x4, int64_t m, int64_t c, 
     }
 }
 
-template <SrcKind kind, bool kSR>
+// The row-wise MXFP8 of the 32 values a thread holds in phase 1 (one block along the row),
+// nearest-even: written to q_r [R, C] and e8_r [R, C/32] when the kernel also emits that layout.
+__device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int64_t c, int64_t C,
+                                               uint8_t *__restrict__ q_r, uint8_t *__restrict__ e8_r) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+    const int e = mx_scale_exponent(a);
+    const float s = pow2_neg(e);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[j] = e4m3x4_rn(__fmul_rn(v[4 * j], s), __fmul_rn(v[4 * j + 1], s), __fmul_rn(v[4 * j + 2], s),
+                         __fmul_rn(v[4 * j + 3], s));
+    uint4 *dst = reinterpret_cast<uint4 *>(q_r + r * C + c);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    e8_r[r * (C / 32) + c / 32] = (uint8_t)(e + 127);
+}
+
+template <SrcKind kind, bool kSR, bool kRow = false>
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
-    uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma) {
+    uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
+    uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr) {
     __shared__ __align__(16) float tile[kTileC][kPitch];
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
     const int64_t n_ct = (C + kTileC - 1) / kTileC;
@@ -109,6 +130,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
                         v[8 * q + 2 * i + 1] = bf16_hi(ws[i]);
                     }
                 }
+                if constexpr (kRow) emit_rowwise32(v, r, c, C, q_r, e8_r);
             }
         } else {
 #pragma unroll
@@ -214,6 +236,7 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned4(q));
         const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
         if (tiles == 0) return MOE4_OK;
+        MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
         if (sr)
             requant_transpose_kernel<SrcKind::Bf16, true><<<(unsigned)tiles, 256, 0, st>>>(
                 nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
@@ -221,5 +244,19 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
             requant_transpose_kernel<SrcKind::Bf16, false><<<(unsigned)tiles, 256, 0, st>>>(
                 nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
     }
+    return launch_status();
+}
+
+extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q_row,
+                                     uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
+                                     void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 32 == 0 && flags == 0);
+    MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || x));
+    MOE4_CHECK_ARG(aligned16(x) && aligned16(q_row) && aligned4(q_col));
+    const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
+    if (tiles == 0) return MOE4_OK;
+    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
+    requant_transpose_kernel<SrcKind::Bf16, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+        nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row);
     return launch_status();
 }

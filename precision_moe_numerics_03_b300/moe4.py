@@ -51,6 +51,7 @@ _SIGNATURES = {
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
     "mxfp8_requant_transpose_sr": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
     "mxfp8_quantize": (_int, [_vp, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
+    "mxfp8_quantize_rowcol": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "hadamard_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "hadamard_dequant": (_int, [_vp, _vp, _vp, _i64, _i64, _vp, _u32, _vp]),
     "grouped_expert_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32,
@@ -174,6 +175,11 @@ def mxfp8_requant_transpose_sr(codes, sf, g_dec, nmat, rows, cols, q_t, e8_t, se
 
 def mxfp8_quantize(x, rows, cols, q, e8, seed=0, stream_id=0, flags=ROWWISE, stream=None):
     _call("mxfp8_quantize", _p(x), rows, cols, _p(q), _p(e8), seed, stream_id, flags, _s(stream))
+
+
+def mxfp8_quantize_rowcol(x, rows, cols, q_row, e8_row, q_col, e8_col, flags=0, stream=None):
+    _call("mxfp8_quantize_rowcol", _p(x), rows, cols, _p(q_row), _p(e8_row), _p(q_col), _p(e8_col), flags,
+          _s(stream))
 
 
 def hadamard_quant(x, rows, cols, codes, sf, g_dec, flags=FOUR_OVER_SIX, ws=None, stream=None):

@@ -64,6 +64,9 @@ MISALIGNED = FAKE + 4
     ("nvfp4_quantize", (FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 2, FAKE, 64, None)),   # AMAX_GIVEN, no amax
     ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 48, 64, FAKE, FAKE, 0, 0, 4, None)),  # rows % 32
     ("mxfp8_quantize", (FAKE, 32, 64, FAKE, FAKE, 0, 0, 0x30, None)),                        # both layouts
+    ("mxfp8_quantize_rowcol", (FAKE, 48, 64, FAKE, FAKE, FAKE, FAKE, 0, None)),                # rows % 32
+    ("mxfp8_quantize_rowcol", (FAKE, 32, 64, FAKE, FAKE, FAKE, FAKE, 0x4, None)),              # no SR
+    ("mxfp8_quantize_rowcol", (FAKE, 32, 64, MISALIGNED, FAKE, FAKE, FAKE, 0, None)),          # q_row align
     ("hadamard_quant", (FAKE, 4, 64, FAKE, FAKE, FAKE, 1, FAKE, 4, None)),                   # cols % 128
     ("grouped_expert_gemm_nvfp4", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 100, 256, 256, FAKE, 0x100,
                                    None, 0, None)),                                          # rows % 128

@@ -111,6 +111,35 @@ def test_mxfp8_quantize(layout, sr):
     assert first_mismatch(to_np(q), rq) is None and first_mismatch(to_np(e8), re8) is None
 
 
+@pytest.mark.parametrize("shape", [(320, 192), (96, 96), (160512 // 4, 4096)])
+def test_mxfp8_quantize_rowcol(shape):
+    """Both layouts from one read equal the oracle's row-wise and transposed MXFP8 (nearest-even);
+    the last case is a quarter of the backward's dY at the 384-expert layer, checked on sampled rows
+    and columns."""
+    rows, cols = shape
+    rng = np.random.default_rng(rows)
+    x = inputs.to_bf16_bits((rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-6, 6, (rows, 1))))
+                            .astype(np.float32))
+    x[:32] = 0  # an all-zero block in both layouts
+    qr, er = empty_u8(rows, cols), empty_u8(rows, cols // 32)
+    qc, ec = empty_u8(cols, rows), empty_u8(cols, rows // 32)
+    moe4.mxfp8_quantize_rowcol(to_dev(x), rows, cols, qr, er, qc, ec)
+    torch.cuda.synchronize()
+    xf = oracle.bf16_to_f32(x)
+    if rows * cols <= 1 << 20:
+        rq, re8 = oracle.mxfp8_quantize(xf, colwise=False)
+        assert first_mismatch(to_np(qr), rq) is None and first_mismatch(to_np(er), re8) is None
+        rq, re8 = oracle.mxfp8_quantize(xf, colwise=True)
+        assert first_mismatch(to_np(qc), rq) is None and first_mismatch(to_np(ec), re8) is None
+        return
+    pick = np.random.default_rng(1).choice(rows, 64, replace=False)
+    rq, re8 = oracle.mxfp8_quantize(xf[pick], colwise=False)
+    assert first_mismatch(to_np(qr)[pick], rq) is None and first_mismatch(to_np(er)[pick], re8) is None
+    pickc = np.random.default_rng(2).choice(cols, 16, replace=False)
+    rq, re8 = oracle.mxfp8_quantize(np.ascontiguousarray(xf[:, pickc]), colwise=True)
+    assert first_mismatch(to_np(qc)[pickc], rq) is None and first_mismatch(to_np(ec)[pickc], re8) is None
+
+
 def test_requant_reads_tensor_core_scale_layout():
     nmat, rows, cols = 2, 256, 512
     rng = np.random.default_rng(31)
