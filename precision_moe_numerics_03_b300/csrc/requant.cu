@@ -17,37 +17,41 @@ namespace moe4 {
 
 constexpr int kTileR = 128;
 constexpr int kTileC = 64;
-constexpr int kPitch = kTileR + 4;
 
 enum class SrcKind { Nvfp4, Bf16 };
 
-// Output of one warp iteration: the 128 values of output row c (input column c) in this tile.
-// Lane l owns values 4l..4l+3; lanes 8b..8b+7 form 32-block b (amax by three shuffles).
+// Output of half a warp: 128 values of output row c (input column c) of this tile.  Lane
+// sub = lane % 16 owns values 8*sub .. 8*sub + 7; lanes 4b .. 4b+3 of the half form 32-block b
+// (amax by two shuffles).  Every lane takes part in the shuffles; `live` only guards the stores.
 template <bool kSR>
-__device__ __forceinline__ void emit_row(const float4 x4, int64_t m, int64_t c, int64_t r0, int64_t R, int64_t C,
-                                         uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
-                                         const PhiloxKeys keys, uint32_t stream_id) {
-    const int lane = lane_id();
-    float a = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
+__device__ __forceinline__ void emit8(const float x[8], bool live, int64_t m, int64_t c, int64_t r0, int64_t R,
+                                      int64_t C, uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
+                                      const PhiloxKeys keys, uint32_t stream_id) {
+    const int sub = lane_id() & 15;
+    float a = fmaxf(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))),
+                    fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
     const int e = mx_scale_exponent(a);
     const float s = pow2_neg(e);
-    float v0, v1, v2, v3;
-    f2_unpack(f2_mul(f2_pack(x4.x, x4.y), f2_pack(s, s)), v0, v1);
-    f2_unpack(f2_mul(f2_pack(x4.z, x4.w), f2_pack(s, s)), v2, v3);
-    const int64_t r = r0 + lane * 4;
+    const uint64_t s2 = f2_pack(s, s);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), s2), v[2 * i], v[2 * i + 1]);
+    const int64_t r = r0 + sub * 8;
     const int64_t idx = (m * C + c) * R + r;
-    uint32_t packed;
+    uint32_t lo, hi;
     if constexpr (kSR) {
-        packed = e4m3x4_sr(v0, v1, v2, v3, sr_words4((uint64_t)idx >> 2, stream_id, keys));
+        const uint64_t j = (uint64_t)idx >> 2;
+        lo = e4m3x4_sr(v[0], v[1], v[2], v[3], sr_words4(j, stream_id, keys));
+        hi = e4m3x4_sr(v[4], v[5], v[6], v[7], sr_words4(j + 1, stream_id, keys));
     } else {
-        packed = e4m3x4_rn(v0, v1, v2, v3);
+        lo = e4m3x4_rn(v[0], v[1], v[2], v[3]);
+        hi = e4m3x4_rn(v[4], v[5], v[6], v[7]);
     }
-    if (r < R) {
-        *reinterpret_cast<uint32_t *>(q_t + idx) = packed;
-        if ((lane & 7) == 0) e8_t[(m * C + c) * (R / 32) + (r >> 5)] = (uint8_t)(e + 127);
+    if (live && r < R) {
+        *reinterpret_cast<uint2 *>(q_t + idx) = make_uint2(lo, hi);
+        if ((sub & 3) == 0) e8_t[(m * C + c) * (R / 32) + (r >> 5)] = (uint8_t)(e + 127);
     }
 }
 
@@ -71,13 +75,19 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
     e8_r[r * (C / 32) + c / 32] = (uint8_t)(e + 127);
 }
 
+// Shared tile: 64 input columns x 128 input rows of 16-bit values, transposed (row = input
+// column).  An NVFP4 source stores e2m1 * e4m3 as f16 (at most 6 significant bits: exact) and the
+// binary32 product with g_dec is formed when the value is read back, the same single rounding;
+// a bf16 source stores its bits.
+constexpr int kPitch16 = kTileR + 8;
+
 template <SrcKind kind, bool kSR, bool kRow = false>
-__global__ void __launch_bounds__(256) requant_transpose_kernel(
+__global__ void __launch_bounds__(256, 4) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
     uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
     uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr) {
-    __shared__ __align__(16) float tile[kTileC][kPitch];
+    __shared__ __align__(16) uint16_t tile[kTileC][kPitch16];
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
     const int64_t n_ct = (C + kTileC - 1) / kTileC;
     const int64_t t = blockIdx.x;
@@ -87,13 +97,13 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const int64_t m = rest / n_ct;
     const int64_t r0 = rt * kTileR, c0 = ct * kTileC;
 
-    // phase 1: load, dequantise, transpose into shared memory
+    // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
     {
         const int rl = threadIdx.x & (kTileR - 1);
         const int half = threadIdx.x >> 7;
         const int64_t r = r0 + rl;
         const int64_t c = c0 + half * 32;
-        float v[32];
+        uint32_t h[16];  // 32 16-bit values, element 2i in the low half of h[i]
         if (r < R && c < C) {
             if constexpr (kind == SrcKind::Nvfp4) {
                 const uint4 w = __ldg(reinterpret_cast<const uint4 *>(codes + ((m * R + r) * C + c) / 2));
@@ -104,18 +114,15 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
                                             : (m * R + r) * nblk + b;
                 const uint32_t sf2 = e4m3x2_to_h2(__ldg(reinterpret_cast<const uint16_t *>(sf + soff)));
                 const uint32_t sfa2 = __byte_perm(sf2, 0, 0x1010), sfb2 = __byte_perm(sf2, 0, 0x3232);
-                const uint64_t g2 = f2_pack(g_dec[m], g_dec[m]);
                 const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const __half2 sfh = *reinterpret_cast<const __half2 *>(q < 2 ? &sfa2 : &sfb2);
 #pragma unroll
                     for (int b2 = 0; b2 < 4; ++b2) {
-                        // e2m1 * e4m3 has at most 6 significant bits: exact in f16, then exact in f32
-                        uint32_t h = e2m1x2_to_h2(words[q] >> (8 * b2));
-                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&h), sfh);
-                        const float2 f = __half22float2(es);
-                        f2_unpack(f2_mul(f2_pack(f.x, f.y), g2), v[8 * q + 2 * b2], v[8 * q + 2 * b2 + 1]);
+                        uint32_t e2 = e2m1x2_to_h2(words[q] >> (8 * b2));
+                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2), sfh);
+                        h[4 * q + b2] = *reinterpret_cast<const uint32_t *>(&es);
                     }
                 }
             } else {
@@ -123,33 +130,55 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint4 w = __ldg(src + q);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        v[8 * q + 2 * i] = bf16_lo(ws[i]);
-                        v[8 * q + 2 * i + 1] = bf16_hi(ws[i]);
-                    }
+                    h[4 * q] = w.x;
+                    h[4 * q + 1] = w.y;
+                    h[4 * q + 2] = w.z;
+                    h[4 * q + 3] = w.w;
                 }
-                if constexpr (kRow) emit_rowwise32(v, r, c, C, q_r, e8_r);
+                if constexpr (kRow) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[2 * i] = bf16_lo(h[i]);
+                        v[2 * i + 1] = bf16_hi(h[i]);
+                    }
+                    emit_rowwise32(v, r, c, C, q_r, e8_r);
+                }
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            for (int i = 0; i < 16; ++i) h[i] = 0u;
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tile[half * 32 + i][rl] = v[i];
+        for (int i = 0; i < 16; ++i) {
+            tile[half * 32 + 2 * i][rl] = (uint16_t)(h[i] & 0xFFFFu);
+            tile[half * 32 + 2 * i + 1][rl] = (uint16_t)(h[i] >> 16);
+        }
     }
     __syncthreads();
 
-    // phase 2: two output row segments (128 values each) per warp iteration
+    // phase 2: each warp emits two output rows per iteration (lanes 0-15 and 16-31)
+    const float g = (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
     const int lane = lane_id();
+    const int sub = lane & 15;
 #pragma unroll 1
-    for (int cl = warp_id(); cl < kTileC; cl += 16) {
-        const int64_t ca = c0 + cl, cb = c0 + cl + 8;
-        const float4 xa = *reinterpret_cast<const float4 *>(&tile[cl][lane * 4]);
-        const float4 xb = *reinterpret_cast<const float4 *>(&tile[cl + 8][lane * 4]);
-        if (ca < C) emit_row<kSR>(xa, m, ca, r0, R, C, q_t, e8_t, keys, stream_id);
-        if (cb < C) emit_row<kSR>(xb, m, cb, r0, R, C, q_t, e8_t, keys, stream_id);
+    for (int i = 0; i < kTileC / 16; ++i) {
+        const int cl = warp_id() + 16 * i + 8 * (lane >> 4);
+        const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cl][sub * 8]);
+        const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (kind == SrcKind::Nvfp4) {
+                const float2 f = h2_bits_to_f2(pw[k]);
+                f2_unpack(f2_mul(f2_pack(f.x, f.y), f2_pack(g, g)), x[2 * k], x[2 * k + 1]);
+            } else {
+                x[2 * k] = bf16_lo(pw[k]);
+                x[2 * k + 1] = bf16_hi(pw[k]);
+            }
+        }
+        const int64_t c = c0 + cl;
+        emit8<kSR>(x, c < C, m, c, r0, R, C, q_t, e8_t, keys, stream_id);
     }
 }
 
@@ -199,7 +228,7 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
                                           void *stream) {
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && rows % 32 == 0 && cols % 32 == 0);
     MOE4_CHECK_ARG(codes && sf && g_dec && q_t && e8_t);
-    MOE4_CHECK_ARG(aligned16(codes) && aligned4(q_t) && (reinterpret_cast<uintptr_t>(sf) & 1u) == 0);
+    MOE4_CHECK_ARG(aligned16(codes) && aligned16(q_t) && (reinterpret_cast<uintptr_t>(sf) & 1u) == 0);
     MOE4_CHECK_ARG((flags & ~(MOE4_SR | MOE4_SF_MMA_LAYOUT)) == 0);
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
     MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
@@ -233,7 +262,7 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         if (grid > cap) grid = cap;
         mxfp8_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(x, rows, cols, q, e8, philox_keys(seed), stream_id, sr);
     } else {
-        MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned4(q));
+        MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned16(q));
         const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
         if (tiles == 0) return MOE4_OK;
         MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
@@ -252,7 +281,7 @@ extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t co
                                      void *stream) {
     MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 32 == 0 && flags == 0);
     MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || x));
-    MOE4_CHECK_ARG(aligned16(x) && aligned16(q_row) && aligned4(q_col));
+    MOE4_CHECK_ARG(aligned16(x) && aligned16(q_row) && aligned16(q_col));
     const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
     if (tiles == 0) return MOE4_OK;
     MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
