@@ -155,7 +155,7 @@ int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, ui
  * backward's dY and dGU feed the rows-grouped dgrad row-wise and the contraction-grouped wgrad
  * transposed [DEBUT] confirmed list).  q_row [rows, cols], e8_row [rows, cols/32]; q_col
  * [cols, rows], e8_col [cols, rows/32]; the bytes equal those of the two single-layout calls.
- * rows % 32 == 0, cols % 32 == 0; x and q_row 16-byte aligned; flags must be 0. */
+ * rows % 32 == 0, cols % 32 == 0; x, q_row and q_col 16-byte aligned; flags must be 0. */
 int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q_row,
                           uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
                           void *stream);

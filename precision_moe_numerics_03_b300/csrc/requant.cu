@@ -82,7 +82,7 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
 constexpr int kPitch16 = kTileR + 8;
 
 template <SrcKind kind, bool kSR, bool kRow = false>
-__global__ void __launch_bounds__(256, 4) requant_transpose_kernel(
+__global__ void __launch_bounds__(256, kSR ? 4 : 5) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
     uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
