@@ -60,12 +60,20 @@ struct Cfg<1> {                       // MXFP8
     static constexpr int ELEMS_PER_ATOM = 128;
 };
 
-// Epilogue staging of the fused SGD mode, per epilogue warp: two 32x32 binary32 tiles (128-byte
-// swizzle) and two 32x32 bf16 tiles (64-byte swizzle), plus two mbarriers.
-constexpr int EPI_W_TILE = 32 * 32 * 4;
-constexpr int EPI_B_TILE = 32 * 32 * 2;
-constexpr int EPI_WARP_BYTES = 2 * EPI_W_TILE + 2 * EPI_B_TILE;
+// Epilogue staging of the fused SGD mode, per epilogue warp: a ring of SGD_NB buffers, each a
+// 32x16 binary32 chunk (64-byte rows, 64-byte swizzle) and a 32x16 bf16 chunk (32-byte rows,
+// 32-byte swizzle), with one mbarrier per buffer.  Master-weight loads run SGD_LA chunks ahead of
+// the chunk being updated, so each warp keeps several loads in flight.
+constexpr int SGD_CW = 16;                    // columns per chunk
+constexpr int SGD_W_CHUNK = 32 * SGD_CW * 4;  // 2 KB
+constexpr int SGD_B_CHUNK = 32 * SGD_CW * 2;  // 1 KB
+constexpr int SGD_NB = 3;                     // ring buffers per warp
+constexpr int SGD_LA = 1;                     // load lookahead, chunks
+static_assert(SGD_LA <= SGD_NB - 2, "a refilled buffer's store must be allowed to still be pending");
+constexpr int EPI_WARP_BYTES = SGD_NB * (SGD_W_CHUNK + SGD_B_CHUNK);
 constexpr int EPI_SGD_BYTES = 8 * EPI_WARP_BYTES;
+// TMA-store epilogue: one 32x32 binary32 tile per epilogue warp
+constexpr int EPI_W_TILE = 32 * 32 * 4;
 // Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
 // TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
@@ -73,7 +81,7 @@ enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2 };
 constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE;
 template <int EM>
 struct EpiCfg {
-    static constexpr int NST = EM == EPI_SGD ? 2 : (EM == EPI_TMA ? 3 : STAGES);
+    static constexpr int NST = EM == EPI_SGD ? 3 : (EM == EPI_TMA ? 3 : STAGES);
     static constexpr int BYTES = EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : 0);
 };
 
@@ -87,7 +95,7 @@ struct Layout {
     static constexpr int OFF_SFB = OFF_SFA + NST * SFA;
     static constexpr int OFF_EPI = (OFF_SFB + NST * SFB + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI;
-    static constexpr int NBAR = 2 * NST + 3 + 16;  // full, empty, tmem_full, tmem_empty, drain, epilogue
+    static constexpr int NBAR = 2 * NST + 3 + 8 * SGD_NB;  // full, empty, tmem_full, tmem_empty, drain, epilogue
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
@@ -181,6 +189,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars, *empty = bars + NST;
     uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 1, *drain = tmem_full + 2;
-    uint64_t *epi_bar = tmem_full + 3;  // fused SGD: two per epilogue warp
+    uint64_t *epi_bar = tmem_full + 3;  // fused SGD: SGD_NB per epilogue warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, EPI_THREADS);
         mbar_init(drain, 1);
-        for (int i = 0; i < 16; ++i) mbar_init(epi_bar + i, 1);
+        for (int i = 0; i < 8 * SGD_NB; ++i) mbar_init(epi_bar + i, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - 4) >> 2;
         uint32_t acc_phase = 0;
-        uint32_t epi_phase = 0;  // fused SGD: parity of this warp's two staging barriers
+        uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND>(p, t);
             if (!mbar_wait(tmem_full, acc_phase, abort_flag)) break;
@@ -457,50 +466,75 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (BN / 2));
             if constexpr (kSgd) {
                 // W32 <- W32 - lr * dW, bf16 copy, running max |bf16|.  This warp owns rows
-                // 32q..32q+31 and columns half*128 .. +127 of the tile, in four 32-column chunks:
-                // TMA brings the 32x32 binary32 chunk into shared memory (128-byte swizzle: lane l's
-                // 16-byte piece j sits at piece j ^ (l & 7) of its 128-byte row), the lane updates its
-                // row in place and writes the bf16 row (64-byte swizzle: piece j at j ^ ((l >> 1) & 3)),
-                // and TMA stores both.  The next chunk's load overlaps the current chunk's math.
+                // 32q..32q+31 and columns half*128 .. +127 of the tile, in NCH 16-column chunks.
+                // Chunks form one stream over this CTA's tiles: chunk u (tile u / NCH of the CTA,
+                // column chunk u % NCH) uses ring buffer u % SGD_NB, whose barrier completes for
+                // the (u / SGD_NB)-th time.  TMA brings the 32x16 binary32 chunk into shared memory
+                // (64-byte swizzle: lane l's 16-byte piece j sits at piece j ^ ((l >> 1) & 3) of
+                // its 64-byte row), the lane updates its row in place and writes the bf16 row
+                // (32-byte swizzle: piece j at j ^ ((l >> 2) & 1)), and TMA stores both.  The load
+                // of chunk u + SGD_LA is issued before chunk u is processed; it may belong to the
+                // CTA's next tile, whose master weights do not depend on that tile's accumulator.
+                constexpr int NCH = (BN / 2) / SGD_CW;
                 const int wi = warp - 4;
-                uint8_t *wb_smem = smem + L::OFF_EPI + wi * EPI_WARP_BYTES;
-                uint64_t *eb = epi_bar + 2 * wi;
+                uint8_t *wring = smem + L::OFF_EPI + wi * EPI_WARP_BYTES;
+                uint8_t *bring = wring + SGD_NB * SGD_W_CHUNK;
+                uint64_t *eb = epi_bar + SGD_NB * wi;
                 const int y0 = (int)((int64_t)tl.e * p.M + tl.m0 + q * 32);
                 const int x0 = (int)(tl.n0 + half * (BN / 2));
+                const int64_t tn = t + gridDim.x;
+                const bool has_next = tn < p.num_tiles;
+                int ny0 = 0, nx0 = 0;
+                if (has_next) {
+                    const Tile tn_l = decode_tile<KIND>(p, tn);
+                    ny0 = (int)((int64_t)tn_l.e * p.M + tn_l.m0 + q * 32);
+                    nx0 = (int)(tn_l.n0 + half * (BN / 2));
+                }
+                const uint32_t u0 = sgd_tile * NCH;  // this tile's first chunk in the stream
+                // last chunk that may be issued: the end of this tile, or of the next one
+                const uint32_t u_end = u0 + (has_next ? 2 * NCH : NCH);
+                auto issue = [&](uint32_t u) {  // lane 0
+                    const bool nxt = u >= u0 + NCH;
+                    const int c = (int)(u % NCH);
+                    const int buf = (int)(u % SGD_NB);
+                    bulk_wait_read_1();  // the store of chunk u - SGD_NB, from this buffer, has read it
+                    mbar_expect_tx(eb + buf, SGD_W_CHUNK);
+                    tma_load_2d(wring + buf * SGD_W_CHUNK, &tmW, eb + buf, (nxt ? nx0 : x0) + SGD_CW * c,
+                                nxt ? ny0 : y0);
+                };
+                while (sgd_issued < u0 + SGD_LA && sgd_issued < u_end) {  // the stream's first chunks
+                    if (lane == 0) issue(sgd_issued);
+                    ++sgd_issued;
+                }
+                __syncwarp();
                 const float lr = p.lr;
                 uint32_t amax2 = 0;
                 bool ok = true;
-                if (lane == 0) {  // chunk 0 (buffer 0); earlier stores from these buffers must be read out
-                    bulk_wait_read_all();
-                    mbar_expect_tx(eb, EPI_W_TILE);
-                    tma_load_2d(wb_smem, &tmW, eb, x0, y0);
-                }
-                __syncwarp();
 #pragma unroll 1
-                for (int c = 0; c < 4 && ok; ++c) {
-                    const int b = c & 1;
-                    if (lane == 0 && c + 1 < 4) {
-                        bulk_wait_read_all();
-                        mbar_expect_tx(eb + (b ^ 1), EPI_W_TILE);
-                        tma_load_2d(wb_smem + (b ^ 1) * EPI_W_TILE, &tmW, eb + (b ^ 1), x0 + 32 * (c + 1), y0);
+                for (int c = 0; c < NCH; ++c) {
+                    const uint32_t u = u0 + c;
+                    if (sgd_issued == u + SGD_LA && sgd_issued < u_end) {
+                        if (lane == 0) issue(sgd_issued);
+                        ++sgd_issued;
                     }
                     __syncwarp();
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(eb + b, (epi_phase >> b) & 1u, abort_flag));
-                    epi_phase ^= 1u << b;
+                    const int buf = (int)(u % SGD_NB);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(eb + buf, (u / SGD_NB) & 1u, abort_flag));
                     if (!ok) break;
-                    uint32_t r[32];
+                    ++sgd_done;
+                    uint32_t r[16];
                     if (live) {
-                        tc_ld32(tbase + (uint32_t)(c * 32), r);
+                        tc_ld16(tbase + (uint32_t)(c * SGD_CW), r);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = 0;
+                        for (int i = 0; i < 16; ++i) r[i] = 0;
                     }
-                    uint8_t *wrow = wb_smem + b * EPI_W_TILE + lane * 128;
-                    uint8_t *brow = wb_smem + 2 * EPI_W_TILE + b * EPI_B_TILE + lane * 64;
-                    uint32_t pk[16];
+                    uint8_t *wrow = wring + buf * SGD_W_CHUNK + lane * 64;
+                    uint8_t *brow = bring + buf * SGD_B_CHUNK + lane * 32;
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float4 *slot = reinterpret_cast<float4 *>(wrow + ((j ^ (lane & 7)) << 4));
+                    for (int j = 0; j < 4; ++j) {
+                        float4 *slot = reinterpret_cast<float4 *>(wrow + ((j ^ ((lane >> 1) & 3)) << 4));
                         float4 o = *slot;
                         o.x = __fsub_rn(o.x, __fmul_rn(lr, __uint_as_float(r[4 * j])));
                         o.y = __fsub_rn(o.y, __fmul_rn(lr, __uint_as_float(r[4 * j + 1])));
@@ -513,28 +547,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                         amax2 = __vmaxu2(amax2, pk[2 * j + 1] & 0x7FFF7FFFu);
                     }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 2) & 1)) << 4)) =
                             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0 && live) {
-                        tma_store_2d(&tmW, wb_smem + b * EPI_W_TILE, x0 + 32 * c, y0);
-                        tma_store_2d(&tmWb, wb_smem + 2 * EPI_W_TILE + b * EPI_B_TILE, x0 + 32 * c, y0);
-                        bulk_commit();
-                    }
-                }
-                if (!ok && lane == 0) {  // let this warp's own loads land before the CTA can exit
-                    for (int bb = 0; bb < 2; ++bb) {
-                        const uint32_t aa = smem_u32(eb + bb);
-                        const long long t0 = clock64();
-                        while (!mbar_try_wait(aa, (epi_phase >> bb) & 1u) && clock64() - t0 < kWaitCycles) {
+                    if (lane == 0) {
+                        if (live) {
+                            tma_store_2d(&tmW, wring + buf * SGD_W_CHUNK, x0 + SGD_CW * c, y0);
+                            tma_store_2d(&tmWb, bring + buf * SGD_B_CHUNK, x0 + SGD_CW * c, y0);
                         }
+                        bulk_commit();  // one group per chunk, empty or not, so group counts match chunks
                     }
                 }
+                ++sgd_tile;
                 uint32_t m = max(amax2 & 0xFFFFu, amax2 >> 16) << 16;
                 m = __reduce_max_sync(0xFFFFFFFFu, m);
                 if (lane == 0 && m) atomicMax(p.amax + tl.e, m);
+                if (!ok) break;
             } else if constexpr (EM == EPI_TMA) {
                 // each 32-column chunk: registers -> swizzled 32x32 staging tile -> TMA bulk store
                 // (binary32 rows of 128 bytes with the 128-byte swizzle, bf16 rows of 64 bytes with
@@ -628,6 +658,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
+        }
+        if constexpr (kSgd) {
+            // master-weight loads the loop did not consume (it stopped early): let them land
+            if (lane == 0) {
+                for (uint32_t u = sgd_done; u < sgd_issued; ++u) {
+                    const uint32_t aa = smem_u32(epi_bar + SGD_NB * (warp - 4) + u % SGD_NB);
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(aa, (u / SGD_NB) & 1u) && clock64() - t0 < kWaitCycles) {
+                    }
+                }
+            }
         }
         if constexpr (EM != EPI_REG) {
             if (lane == 0) bulk_wait_all();  // this warp's stores are complete before the CTA exits
@@ -880,9 +921,9 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     g.num_tiles = E * g.n_tiles_m * g.n_tiles_n;
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
-    CUtensorMap tw, twb;  // the master weights and their bf16 copy as [E*M, N], 32x32 boxes
-    if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    CUtensorMap tw, twb;  // the master weights and their bf16 copy as [E*M, N], 16-column x 32-row boxes
+    if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return MOE4_ERR_CUDA;
     return launch<1, EPI_SGD>(ta, tb, tw, twb, g, st);
 }

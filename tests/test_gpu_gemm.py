@@ -180,12 +180,14 @@ def test_mxfp8_wgrad_group_k(accumulate):
         assert np.all(got[2] == 0)
 
 
-def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd():
+@pytest.mark.parametrize("sizes,M,N", [([128, 256, 0, 384], 256, 512),
+                                         ([128, 128, 0, 512, 256, 128, 384, 128], 1024, 2048)])
+def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd(sizes, M, N):
     """The fused weight-gradient + SGD epilogue is bit-identical to the unfused pair, and its
-    per-expert amax equals max |bf16 copy|."""
+    per-expert amax equals max |bf16 copy|.  The second case has 512 output tiles, several per
+    CTA, so each CTA's epilogue also prefetches the master weights of its next tile."""
     rng = np.random.default_rng(23)
-    sizes = [128, 256, 0, 384]
-    E, M, N = len(sizes), 256, 512
+    E = len(sizes)
     offs = _offs(sizes)
     Kt = int(offs[-1])
     aq, ae = _mxfp8_rowwise(_bf16(rng, (M, Kt)), M, Kt)
