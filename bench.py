@@ -296,12 +296,27 @@ def measure_next_rows(step, reps=3):
             m.hadamard_quant(step.Y[:Rp], Rp, d, Cq, Ce, None, m.MXFP8)
             m.hadamard_dequant(Cq, Ce, None, Rp, d, step.Yhat[:Rp], m.MXFP8)
 
+    MMA = m.SF_MMA_LAYOUT
+
+    def down_codec(tm):
+        # the down projection with the return-path codec fused into its final stage, beside the
+        # unfused pair (bf16 product to memory, then the codec); NVFP4 operands of the step
+        with tm("down_unfused"):
+            m.grouped_expert_gemm_nvfp4(step.Hq_c, step.Hq_s, step.Hq_g, step.Wd_c, step.Wd_s, step.Wd_g, step.offs,
+                                        E, Rp, d, f, step.Y, m.OUT_BF16 | MMA)
+            m.hadamard_quant(step.Y[:Rp], Rp, d, Cq, Ce, None, m.MXFP8)
+        with tm("down_fused"):
+            m.grouped_expert_gemm_nvfp4_hadamard_mx(step.Hq_c, step.Hq_s, step.Hq_g, step.Wd_c, step.Wd_s,
+                                                    step.Wd_g, step.offs, E, Rp, d, f, Cq, Ce, MMA)
+
     for _ in range(2):
         fwd(_NullTimer())
+        down_codec(_NullTimer())
     torch.cuda.synchronize()
     timer = EventTimer(torch)
     for _ in range(reps):
         fwd(timer)
+        down_codec(timer)
     torch.cuda.synchronize()
     if m.moe4_get_status() != m.OK:
         raise RuntimeError("a device wait timed out in the MXFP8 forward")
@@ -315,6 +330,11 @@ def measure_next_rows(step, reps=3):
             "gemm_TFLOP/s": round(fwd_flops / (per["gemm_mxfp8_fwd"] / 1e3) / 1e12, 1),
             "quant_swiglu_ms": round(per["mx_quant"], 4),
             "note": "bf16 -> MXFP8 (nearest-even) of X, W_gu, W_d and H + gather + SwiGLU; same routed batch",
+        },
+        "fused_down_gemm_codec": {
+            "fused_ms": round(per["down_fused"], 4),
+            "unfused_ms": round(per["down_unfused"], 4),
+            "note": "down GEMM with the 8.25-bit Hadamard + MXFP8 codec in its epilogue vs bf16 GEMM then codec",
         },
         "hadamard_mxfp8_codec": {
             "ms": round(per["codec_mx"], 4),

@@ -192,6 +192,20 @@ int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const
                               int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
                               void *stream);
 
+/* grouped_expert_gemm_nvfp4_hadamard_mx: the expert GEMM above with the return-path codec fused
+ * into its last stage [LHC kernels paragraph: the transform and the quantisation run in the final
+ * stage of the matrix multiplication; communication paragraph: 8.25 bits per value].  The product
+ * is rounded to bf16 as with MOE4_OUT_BF16, then each 128-column chunk of a row is rotated and
+ * quantised exactly as hadamard_quant with MOE4_MXFP8 does: q [rows_total, N] E4M3 codes and
+ * e8 [rows_total, N/32] E8M0 scales, byte for byte the result of those two calls in sequence,
+ * without the bf16 tensor in memory.  Same argument rules as grouped_expert_gemm_nvfp4 (q 16-byte
+ * aligned); flags: MOE4_SF_MMA_LAYOUT or 0. */
+int grouped_expert_gemm_nvfp4_hadamard_mx(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                                          const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                                          const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t N,
+                                          int64_t K, uint8_t *q, uint8_t *e8, uint32_t flags, void *ws,
+                                          size_t ws_bytes, void *stream);
+
 /* grouped_gemm_mxfp8 [DEBUT, 4WEEK: MXFP8 backward]: D = A * B^T per group, both operands MXFP8
  * with their contraction dimension contiguous.
  * MOE4_GROUP_M (dgrad): A [M, K] (q, e8), B [E, N, K]; rows offs[e]..offs[e+1] of A and D use

@@ -77,12 +77,18 @@ constexpr int EPI_W_TILE = 32 * 32 * 4;
 // Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
 // TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
-enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2 };
+enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3 };
+// Fused return-path codec (NVFP4 GEMM): each epilogue warp stages its 32 rows x 128 columns of
+// bf16 product (rows padded to 272 bytes: conflict-free 16-byte stores and loads).
+constexpr int HMX_PITCH = 128 * 2 + 16;
+constexpr int HMX_WARP_BYTES = 32 * HMX_PITCH;
+constexpr int EPI_HMX_BYTES = 8 * HMX_WARP_BYTES;
 constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE;
 template <int EM>
 struct EpiCfg {
-    static constexpr int NST = EM == EPI_SGD ? 3 : (EM == EPI_TMA ? 3 : STAGES);
-    static constexpr int BYTES = EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : 0);
+    static constexpr int NST = EM == EPI_SGD ? 3 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
+    static constexpr int BYTES =
+        EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
 };
 
 template <int KIND, int NST, int EPI>
@@ -124,6 +130,7 @@ struct Args {
     uint16_t *w_bf16;       // Out::Sgd: the bf16 copy of the updated weights
     float lr;               // Out::Sgd
     unsigned int *amax;     // Out::Sgd: per-expert max |bf16 copy| as binary32 bits
+    uint8_t *e8;            // fused codec: E8M0 scales [M, N/32] (d holds the E4M3 codes [M, N])
     int64_t num_tiles;
     int n_tiles_n, n_tiles_m;
     int64_t sfa_tile_stride;  // atoms between consecutive 128-row tiles of A's scale layout
@@ -565,6 +572,68 @@ __global__ void __launch_bounds__(THREADS, 1)
                 m = __reduce_max_sync(0xFFFFFFFFu, m);
                 if (lane == 0 && m) atomicMax(p.amax + tl.e, m);
                 if (!ok) break;
+            } else if constexpr (EM == EPI_HMX) {
+                // The 8.25-bit return-path codec of the bf16 product, fused: this warp's 32 rows x
+                // 128 columns (one 128-chunk per row) go accumulator -> binary32 * alpha -> bf16 ->
+                // staging (row = lane), then come back 16 values per lane, 8 lanes per row-chunk,
+                // through the Hadamard(128) butterflies and the MXFP8 quantiser (E4M3, one E8M0
+                // scale per 32 by the ceiling rule, nearest-even), straight to global memory.
+                uint8_t *stg = smem + L::OFF_EPI + (warp - 4) * HMX_WARP_BYTES;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    if (live) {
+                        tc_ld32(tbase + (uint32_t)(c * 32), r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = 0;
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = (uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i]), alpha)) |
+                               ((uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i + 1]), alpha)) << 16);
+                    uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * HMX_PITCH + c * 64);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                }
+                // the staged rows are all this warp needs: hand the accumulator back now, so the
+                // next tile's MMAs overlap the transform and quantisation below
+                tc_fence_before();
+                mbar_arrive(tmem_empty);
+                __syncwarp();
+                const int sub = lane & 7;
+                uint8_t *q_out = static_cast<uint8_t *>(p.d);
+#pragma unroll 1
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = 4 * it + (lane >> 3);
+                    const uint4 *src = reinterpret_cast<const uint4 *>(stg + rr * HMX_PITCH + sub * 32);
+                    const uint4 a0 = src[0], a1 = src[1];
+                    const uint32_t hw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    float u[16];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        u[2 * i] = bf16_lo(hw[i]);
+                        u[2 * i + 1] = bf16_hi(hw[i]);
+                    }
+                    fwht128_sub16(u);
+                    float am = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(u[i]));
+                    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+                    const int e = mx_scale_exponent(am);
+                    const float sc = pow2_neg(e);
+                    uint32_t cw[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        cw[j] = e4m3x4_rn(__fmul_rn(u[4 * j], sc), __fmul_rn(u[4 * j + 1], sc),
+                                          __fmul_rn(u[4 * j + 2], sc), __fmul_rn(u[4 * j + 3], sc));
+                    const int64_t grow = tl.m0 + q * 32 + rr;
+                    const int64_t col = tl.n0 + half * (BN / 2) + sub * 16;
+                    *reinterpret_cast<uint4 *>(q_out + grow * p.N + col) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    if ((sub & 1) == 0) p.e8[grow * (p.N / 32) + col / 32] = (uint8_t)(e + 127);
+                }
+                __syncwarp();  // the staging rows are rewritten by this warp's next tile
             } else if constexpr (EM == EPI_TMA) {
                 // each 32-column chunk: registers -> swizzled 32x32 staging tile -> TMA bulk store
                 // (binary32 rows of 128 bytes with the 128-byte swizzle, bf16 rows of 64 bytes with
@@ -655,8 +724,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(tmem_empty);
+            if constexpr (EM != EPI_HMX) {
+                tc_fence_before();
+                mbar_arrive(tmem_empty);
+            }
             acc_phase ^= 1u;
         }
         if constexpr (kSgd) {
@@ -820,6 +891,48 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     CUtensorMap td;
     if (!make_out_map(&td, d, bf16, rows_total, N)) return MOE4_ERR_CUDA;
     return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
+}
+
+extern "C" int grouped_expert_gemm_nvfp4_hadamard_mx(const uint8_t *a_codes, const uint8_t *a_sf,
+                                                     const float *a_g_dec, const uint8_t *b_codes,
+                                                     const uint8_t *b_sf, const float *b_g_dec,
+                                                     const int32_t *group_offs, int64_t E, int64_t rows_total,
+                                                     int64_t N, int64_t K, uint8_t *q, uint8_t *e8, uint32_t flags,
+                                                     void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && rows_total >= 0 && rows_total % BM == 0 && N > 0 && N % BN == 0 && K > 0 &&
+                   K % 256 == 0);
+    MOE4_CHECK_ARG(a_codes && a_sf && a_g_dec && b_codes && b_sf && b_g_dec && group_offs && q && e8);
+    MOE4_CHECK_ARG(aligned16(a_codes) && aligned16(b_codes) && aligned16(a_sf) && aligned16(b_sf) && aligned16(q));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    MOE4_CHECK_ARG(rows_total < (int64_t(1) << 31) && E * N < (int64_t(1) << 31));
+    if (rows_total == 0) return MOE4_OK;
+    cudaStream_t st = as_stream(stream);
+    const uint8_t *sfa, *sfb;
+    int rc = stage_scales(a_sf, rows_total, b_sf, E * N, K, 16, flags, ws, ws_bytes, &sfa, &sfb, st);
+    if (rc != MOE4_OK) return rc;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, a_codes, K / 2, rows_total, BM) || !make_map(&tb, b_codes, K / 2, E * N, BN))
+        return MOE4_ERR_CUDA;
+    Args a{};
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.a_g_dec = a_g_dec;
+    a.b_g_dec = b_g_dec;
+    a.offs = group_offs;
+    a.E = (int)E;
+    a.group_k = 0;
+    a.M = rows_total;
+    a.N = N;
+    a.K = K;
+    a.d = q;
+    a.e8 = e8;
+    a.mode = BF16;
+    a.n_tiles_n = (int)(N / BN);
+    a.n_tiles_m = (int)(rows_total / BM);
+    a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
+    a.sfa_tile_stride = K / 64;
+    a.sfb_tile_stride = K / 64;
+    return launch<0, EPI_HMX>(ta, tb, ta, tb, a, st);
 }
 
 extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b, const uint8_t *b_e8,

@@ -234,33 +234,7 @@ __global__ void __launch_bounds__(256) nvfp4_dequant_kernel(
 }
 
 // ------------------------------------------------------------------ Hadamard(128)
-// One thread per 16 consecutive values (an NVFP4 block): 8 consecutive lanes hold one 128-chunk,
-// lane l its sub-block l % 8, so a warp covers four chunks.  Butterfly span h pairs element i (bit
-// h clear) with i+h: the lower one becomes u[i] + u[i+h], the upper one u[i] - u[i+h], each one
-// binary32 rounding, spans in the order 1, 2, ..., 64.  Spans 1..8 are inside a thread; spans
-// 16, 32, 64 pair lane l with lane l ^ 1, ^2, ^4, where fma(+-1, own, partner) rounds the exact
-// sum or difference once, as the add or subtract would.
-__device__ __forceinline__ void fwht128_sub16(float u[16]) {
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if ((i & h) == 0) {
-                const float a = u[i], b = u[i + h];
-                u[i] = __fadd_rn(a, b);
-                u[i + h] = __fsub_rn(a, b);
-            }
-    const int lane = lane_id();
-#pragma unroll
-    for (int lm = 1; lm < 8; lm <<= 1) {
-        const float sgn = (lane & lm) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __fmaf_rn(sgn, u[i], __shfl_xor_sync(0xFFFFFFFFu, u[i], lm));
-    }
-    const float c = __uint_as_float(0x3DB504F3u);  // nearest binary32 to 1/sqrt(128)
-#pragma unroll
-    for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], c);
-}
+// The Hadamard(128) butterflies on 16 values per thread: fwht128_sub16 (common.cuh).
 
 __device__ __forceinline__ void load16_bf16(const uint16_t *p, float u[16]) {
     const uint4 *src = reinterpret_cast<const uint4 *>(p);

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "hadamard_dequant": (_int, [_vp, _vp, _vp, _i64, _i64, _vp, _u32, _vp]),
     "grouped_expert_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32,
                                          _vp, _sz, _vp]),
+    "grouped_expert_gemm_nvfp4_hadamard_mx": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                      _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32, _vp, _sz, _vp]),
     "grouped_gemm_mxfp8_wgrad_sgd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _f32, _vp,
                                             _u32, _vp, _sz, _vp]),
@@ -196,6 +198,12 @@ def grouped_expert_gemm_nvfp4(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, gr
                               flags=OUT_F32, ws=None, stream=None):
     _call("grouped_expert_gemm_nvfp4", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf), _p(b_g_dec),
           _p(group_offs), E, rows_total, N, K, _p(d), flags, _p(ws), _ws_bytes(ws), _s(stream))
+
+
+def grouped_expert_gemm_nvfp4_hadamard_mx(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, group_offs, E, rows_total,
+                                          N, K, q, e8, flags=0, ws=None, stream=None):
+    _call("grouped_expert_gemm_nvfp4_hadamard_mx", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf),
+          _p(b_g_dec), _p(group_offs), E, rows_total, N, K, _p(q), _p(e8), flags, _p(ws), _ws_bytes(ws), _s(stream))
 
 
 def grouped_gemm_mxfp8(a, a_e8, b, b_e8, group_offs, E, M, N, K, d, flags=OUT_F32 | GROUP_M, ws=None,

@@ -68,6 +68,12 @@ MISALIGNED = FAKE + 4
     ("mxfp8_quantize_rowcol", (FAKE, 32, 64, FAKE, FAKE, FAKE, FAKE, 0x4, None)),              # no SR
     ("mxfp8_quantize_rowcol", (FAKE, 32, 64, MISALIGNED, FAKE, FAKE, FAKE, 0, None)),          # q_row align
     ("hadamard_quant", (FAKE, 4, 64, FAKE, FAKE, FAKE, 1, FAKE, 4, None)),                   # cols % 128
+    ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 200, 256, FAKE,
+                                               FAKE, 0, None, 0, None)),                      # N % 256
+    ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256,
+                                               MISALIGNED, FAKE, 0, None, 0, None)),          # q alignment
+    ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE,
+                                               FAKE, 0x100, None, 0, None)),                  # output flag
     ("grouped_expert_gemm_nvfp4", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 100, 256, 256, FAKE, 0x100,
                                    None, 0, None)),                                          # rows % 128
     ("grouped_expert_gemm_nvfp4", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE, 0x300,
