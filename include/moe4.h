@@ -281,6 +281,15 @@ int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h, void *str
 int moe4_swiglu_backward(const float *gu, const float *dh, int64_t rows, int64_t f, uint16_t *dgu,
                          void *stream);
 
+/* moe4_swiglu_backward_mxfp8: the SwiGLU gradient fused with its MXFP8 quantisation, for the
+ * backward GEMMs [LHC backward pass: MXFP8 operands; the weight gradient's SwiGLU step].  The
+ * bf16 dgu of moe4_swiglu_backward (same arithmetic, same bits) is never written: its row-wise
+ * MXFP8 q_row [rows, 2f], e8_row [rows, 2f/32] and its transposed MXFP8 q_col [2f, rows],
+ * e8_col [2f, rows/32] are, byte for byte as mxfp8_quantize_rowcol of that dgu would give them
+ * (nearest-even).  rows % 32 == 0, f % 32 == 0; gu, dh, q_row, q_col 16-byte aligned; flags 0. */
+int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int64_t rows, int64_t f, uint8_t *q_row,
+                               uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags, void *stream);
+
 /* moe4_combine_backward: the gradient of the combine with respect to the returned rows:
  * dyhat[row_of[t,j]] = bf16(w[t,j] * dy[t]) (one binary32 product per value), and zero rows for
  * padding (src_of < 0).  dy bf16 [T, d], dyhat bf16 [rows_total, d]; d % 8 == 0, k <= 32.  The

@@ -18,7 +18,11 @@ namespace moe4 {
 constexpr int kTileR = 128;
 constexpr int kTileC = 64;
 
-enum class SrcKind { Nvfp4, Bf16 };
+// Nvfp4: dequantised NVFP4 codes.  Bf16: a bf16 tensor.  SwigluBwd: the SwiGLU gradient
+// dGU [R, 2f] (gate columns, then up columns) formed from the binary32 GU and dH and rounded to
+// bf16 exactly as moe4_swiglu_backward does; its tiles pair 32 gate columns with the same 32 up
+// columns, so each GU and dH value is read once.
+enum class SrcKind { Nvfp4, Bf16, SwigluBwd };
 
 // Output of half a warp: 128 values of output row c (input column c) of this tile.  Lane
 // sub = lane % 16 owns values 8*sub .. 8*sub + 7; lanes 4b .. 4b+3 of the half form 32-block b
@@ -82,27 +86,32 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
 constexpr int kPitch16 = kTileR + 8;
 
 template <SrcKind kind, bool kSR, bool kRow = false>
-__global__ void __launch_bounds__(256, kSR ? 4 : 5) requant_transpose_kernel(
+__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 : 5) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
     uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
-    uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr) {
+    uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr, const float *__restrict__ gu = nullptr,
+    const float *__restrict__ dh = nullptr) {
+    constexpr bool kSwb = kind == SrcKind::SwigluBwd;
     __shared__ __align__(16) uint16_t tile[kTileC][kPitch16];
+    const int64_t f = C / 2;  // SwigluBwd: C = 2f
     const int64_t n_rt = (R + kTileR - 1) / kTileR;
-    const int64_t n_ct = (C + kTileC - 1) / kTileC;
+    const int64_t n_ct = kSwb ? f / 32 : (C + kTileC - 1) / kTileC;
     const int64_t t = blockIdx.x;
     const int64_t rt = t % n_rt;
     const int64_t rest = t / n_rt;
     const int64_t ct = rest % n_ct;
     const int64_t m = rest / n_ct;
-    const int64_t r0 = rt * kTileR, c0 = ct * kTileC;
+    const int64_t r0 = rt * kTileR, c0 = ct * (kSwb ? 32 : kTileC);
+    // output column of transposed tile row cl
+    auto out_col = [&](int cl) -> int64_t { return kSwb ? (cl < 32 ? c0 + cl : f + c0 + (cl - 32)) : c0 + cl; };
 
     // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
     {
         const int rl = threadIdx.x & (kTileR - 1);
         const int half = threadIdx.x >> 7;
         const int64_t r = r0 + rl;
-        const int64_t c = c0 + half * 32;
+        const int64_t c = out_col(half * 32);
         uint32_t h[16];  // 32 16-bit values, element 2i in the low half of h[i]
         if (r < R && c < C) {
             if constexpr (kind == SrcKind::Nvfp4) {
@@ -123,6 +132,29 @@ __global__ void __launch_bounds__(256, kSR ? 4 : 5) requant_transpose_kernel(
                         uint32_t e2 = e2m1x2_to_h2(words[q] >> (8 * b2));
                         const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2), sfh);
                         h[4 * q + b2] = *reinterpret_cast<const uint32_t *>(&es);
+                    }
+                }
+            } else if constexpr (kSwb) {
+                // 16 gate/up column pairs per thread (one s per pair): dg = (dh * u) * s * (1 + g *
+                // (1 - s)) and du = dh * (g * s), s = 1 / (1 + exp(-g)), each step one binary32
+                // rounding, then bf16; dg to tile rows half*16 + i, du to rows 32 + half*16 + i
+                const int64_t j0 = c0 + half * 16;
+                const float4 *gp = reinterpret_cast<const float4 *>(gu + r * 2 * f + j0);
+                const float4 *upp = reinterpret_cast<const float4 *>(gu + r * 2 * f + f + j0);
+                const float4 *dp = reinterpret_cast<const float4 *>(dh + r * f + j0);
+#pragma unroll 2
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 g4 = __ldg(gp + k4), u4 = __ldg(upp + k4), d4 = __ldg(dp + k4);
+                    const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, us[4] = {u4.x, u4.y, u4.z, u4.w};
+                    const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
+                        const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
+                        const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
+                        const float duv = __fmul_rn(ds[i], __fmul_rn(gs[i], sg));
+                        tile[half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(dgv);
+                        tile[32 + half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(duv);
                     }
                 }
             } else {
@@ -148,14 +180,36 @@ __global__ void __launch_bounds__(256, kSR ? 4 : 5) requant_transpose_kernel(
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[i] = 0u;
-        }
+            if constexpr (kSwb) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            tile[half * 32 + 2 * i][rl] = (uint16_t)(h[i] & 0xFFFFu);
-            tile[half * 32 + 2 * i + 1][rl] = (uint16_t)(h[i] >> 16);
+                for (int i = 0; i < 16; ++i) {
+                    tile[half * 16 + i][rl] = 0;
+                    tile[32 + half * 16 + i][rl] = 0;
+                }
+            }
+        }
+        if constexpr (!kSwb) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                tile[half * 32 + 2 * i][rl] = (uint16_t)(h[i] & 0xFFFFu);
+                tile[half * 32 + 2 * i + 1][rl] = (uint16_t)(h[i] >> 16);
+            }
         }
     }
     __syncthreads();
+    if constexpr (kSwb && kRow) {
+        // the row-wise MXFP8 block of row r: gate columns (half 0) or up columns (half 1), read
+        // back from one column of the transposed tile
+        const int rl = threadIdx.x & (kTileR - 1);
+        const int half = threadIdx.x >> 7;
+        const int64_t r = r0 + rl;
+        if (r < R) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)tile[half * 32 + i][rl] << 16);
+            emit_rowwise32(v, r, out_col(half * 32), C, q_r, e8_r);
+        }
+    }
 
     // phase 2: each warp emits two output rows per iteration (lanes 0-15 and 16-31)
     const float g = (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
@@ -177,7 +231,7 @@ __global__ void __launch_bounds__(256, kSR ? 4 : 5) requant_transpose_kernel(
                 x[2 * k + 1] = bf16_hi(pw[k]);
             }
         }
-        const int64_t c = c0 + cl;
+        const int64_t c = out_col(cl);
         emit8<kSR>(x, c < C, m, c, r0, R, C, q_t, e8_t, keys, stream_id);
     }
 }
@@ -287,5 +341,20 @@ extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t co
     MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
     requant_transpose_kernel<SrcKind::Bf16, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row);
+    return launch_status();
+}
+
+extern "C" int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int64_t rows, int64_t f, uint8_t *q_row,
+                                          uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
+                                          void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && f > 0 && f % 32 == 0 && flags == 0);
+    MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || (gu && dh)));
+    MOE4_CHECK_ARG(aligned16(gu) && aligned16(dh) && aligned16(q_row) && aligned16(q_col));
+    const int64_t tiles = ((rows + kTileR - 1) / kTileR) * (f / 32);
+    if (tiles == 0) return MOE4_OK;
+    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
+    requant_transpose_kernel<SrcKind::SwigluBwd, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+        nullptr, nullptr, nullptr, nullptr, 1, rows, 2 * f, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, gu,
+        dh);
     return launch_status();
 }

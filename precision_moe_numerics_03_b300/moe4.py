@@ -66,6 +66,7 @@ _SIGNATURES = {
     "moe4_permute_plan": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "moe4_permute_nvfp4": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _u32, _vp]),
     "moe4_swiglu_backward": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
+    "moe4_swiglu_backward_mxfp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "moe4_combine_backward": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
@@ -239,6 +240,11 @@ def moe4_permute_nvfp4(codes, sf, T, cols, src_of, rows_total, out_codes, out_sf
 
 def moe4_swiglu_backward(gu, dh, rows, f, dgu, stream=None):
     _call("moe4_swiglu_backward", _p(gu), _p(dh), rows, f, _p(dgu), _s(stream))
+
+
+def moe4_swiglu_backward_mxfp8(gu, dh, rows, f, q_row, e8_row, q_col, e8_col, flags=0, stream=None):
+    _call("moe4_swiglu_backward_mxfp8", _p(gu), _p(dh), rows, f, _p(q_row), _p(e8_row), _p(q_col), _p(e8_col), flags,
+          _s(stream))
 
 
 def moe4_combine_backward(dy, row_of, w, src_of, T, k, d, rows_total, dyhat, stream=None):

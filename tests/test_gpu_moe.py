@@ -128,6 +128,53 @@ def test_swiglu_backward_within_bf16_rounding():
     assert not bad.any(), int(bad.sum())
 
 
+def _swiglu_bwd_mxfp8_both(gu, dh, rows, f):
+    """Fused SwiGLU backward + MXFP8 (both layouts), and the unfused pair, on device tensors."""
+    out = [empty_u8(rows, 2 * f), empty_u8(rows, 2 * f // 32), empty_u8(2 * f, rows), empty_u8(2 * f, rows // 32)]
+    moe4.moe4_swiglu_backward_mxfp8(gu, dh, rows, f, *out)
+    dgu = torch.empty((rows, 2 * f), dtype=torch.int16, device=DEV)
+    moe4.moe4_swiglu_backward(gu, dh, rows, f, dgu)
+    ref = [empty_u8(rows, 2 * f), empty_u8(rows, 2 * f // 32), empty_u8(2 * f, rows), empty_u8(2 * f, rows // 32)]
+    moe4.mxfp8_quantize_rowcol(dgu, rows, 2 * f, *ref)
+    torch.cuda.synchronize()
+    return out, ref
+
+
+@pytest.mark.parametrize("rows,f", [(96, 64), (512, 1024), (160512, 2048)])
+def test_swiglu_backward_mxfp8_equals_unfused(rows, f):
+    """Fused SwiGLU gradient + MXFP8 equals the SwiGLU gradient in bf16 followed by the row and
+    transposed MXFP8 quantiser, byte for byte; the last case is the 384-expert layer's dGU."""
+    gen = inputs.device_generator(9, rows, DEV)
+    gu = inputs.device_normal((rows, 2 * f), 3.0, gen, DEV, dtype=torch.float32)
+    dh = inputs.device_normal((rows, f), 1.0, gen, DEV, dtype=torch.float32)
+    out, ref = _swiglu_bwd_mxfp8_both(gu, dh, rows, f)
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
+
+
+def test_swiglu_backward_mxfp8_against_oracle():
+    """Dequantised row-wise output against the oracle's float64 SwiGLU gradient: the SwiGLU bound
+    of the unfused test (one bf16 rounding, binary32 cancellation near the zero of silu') plus one
+    E4M3 rounding of the bf16 value (2^-4 relative, or half the subnormal step of its block)."""
+    rows, f = 256, 512
+    rng = np.random.default_rng(15)
+    gu = (rng.standard_normal((rows, 2 * f)) * 3).astype(np.float32)
+    dh = rng.standard_normal((rows, f)).astype(np.float32)
+    out, _ = _swiglu_bwd_mxfp8_both(to_dev(gu), to_dev(dh), rows, f)
+    got = oracle.mxfp8_dequantize(to_np(out[0]), to_np(out[1])).astype(np.float64)
+    ref = oracle.swiglu_backward(gu, dh).astype(np.float64)
+    g, u, d = gu[:, :f].astype(np.float64), gu[:, f:].astype(np.float64), dh.astype(np.float64)
+    mag = np.abs(d) * (np.abs(u) * (1 + np.abs(g)) + np.abs(g))
+    tol = 2.0 ** -8 * np.abs(ref) + 2.0 ** -20 * np.concatenate([mag, mag], axis=1)
+    blk_amax = (np.abs(ref) + tol).reshape(rows, 2 * f // 32, 32).max(axis=2)
+    half_sub = np.repeat(2 * blk_amax / (448.0 * 1024), 32, axis=1)
+    bound = tol + 2.0 ** -4 * (np.abs(ref) + tol) + half_sub
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), int(bad.sum())
+    rq, re8 = oracle.mxfp8_quantize(oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))), colwise=True)
+    assert np.mean(to_np(out[2]) == rq) >= 0.9  # the transposed layout: structure (same blocks)
+
+
 @pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (300, 16, 4)])
 def test_combine_backward_bit_exact(T, E, k):
     lg = _logits(T, E, True, 3 * T + E)
