@@ -34,15 +34,13 @@ __device__ unsigned int g_status = 0;
 namespace gemm {
 
 constexpr int BM = 128;         // rows of A per tile (MMA M)
-constexpr int BN = 256;         // rows of B per tile (MMA N)
+constexpr int BN = 256;         // rows of B per tile (MMA N); the fused SGD mode uses 128
 constexpr int BKB = 128;        // bytes of contraction per stage (one 128-byte swizzle row)
 constexpr int STAGES = 4;
 constexpr int THREADS = 384;    // warps 0..3: producer, MMA, TMEM, spare; 4..11: epilogue
 constexpr int EPI_THREADS = 256;
 constexpr int A_TILE = BM * BKB;
-constexpr int B_TILE = BN * BKB;
 constexpr int TMEM_COLS = 512;
-constexpr int ACC_COLS = BN;    // binary32 accumulator: one column per output column
 constexpr long long kWaitCycles = 1ll << 32;
 
 template <int KIND>
@@ -86,31 +84,39 @@ constexpr int EPI_HMX_BYTES = 8 * HMX_WARP_BYTES;
 constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE;
 template <int EM>
 struct EpiCfg {
-    static constexpr int NST = EM == EPI_SGD ? 3 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
+    // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
+    // tile's MMAs overlap the previous tile's master-weight traffic
+    static constexpr int BNT = EM == EPI_SGD ? 128 : BN;
+    static constexpr int NST = EM == EPI_SGD ? 4 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
     static constexpr int BYTES =
         EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
 };
 
-template <int KIND, int NST, int EPI>
+template <int KIND, int NST, int EPI, int BNT>
 struct Layout {
+    static constexpr int RT = BNT / 128;  // 128-row tiles of B per tile
+    static constexpr int B_TILE = BNT * BKB;
     static constexpr int SFA = Cfg<KIND>::ATOMS * 512;
-    static constexpr int SFB = 2 * Cfg<KIND>::ATOMS * 512;
+    static constexpr int SFB = RT * Cfg<KIND>::ATOMS * 512;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NST * A_TILE;
     static constexpr int OFF_SFA = OFF_B + NST * B_TILE;
     static constexpr int OFF_SFB = OFF_SFA + NST * SFA;
     static constexpr int OFF_EPI = (OFF_SFB + NST * SFB + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI;
-    static constexpr int NBAR = 2 * NST + 3 + 8 * SGD_NB;  // full, empty, tmem_full, tmem_empty, drain, epilogue
+    // full, empty, tmem_full[2], tmem_empty[2], drain, epilogue
+    static constexpr int NBAR = 2 * NST + 5 + 8 * SGD_NB;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
     static constexpr int TX = A_TILE + B_TILE + SFA + SFB;
-    // tensor-memory columns: accumulator [0, 256), then per stage SFA and SFB
+    // tensor-memory columns: NACC accumulators of BNT columns, then per stage SFA and SFB
     static constexpr int SF_COLS_A = Cfg<KIND>::ATOMS * 4;
-    static constexpr int SF_COLS_B = Cfg<KIND>::ATOMS * 8;
+    static constexpr int SF_COLS_B = Cfg<KIND>::ATOMS * 4 * RT;
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static_assert(ACC_COLS + NST * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static constexpr int NACC = 2 * BNT + NST * SF_COLS <= TMEM_COLS ? 2 : 1;
+    static constexpr int SF_BASE = NACC * BNT;
+    static_assert(SF_BASE + NST * SF_COLS <= TMEM_COLS, "tensor memory overflow");
     static_assert(SMEM <= 232448, "shared memory overflow");
 };
 
@@ -271,11 +277,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Instruction descriptor of the block-scaled kinds: B scale id [4,6), A format [7,10), B format
 // [10,13), K-major A and B (bits 15, 16 clear), N>>3 [17,23), scale type bit 23 (0 UE4M3,
 // 1 UE8M0), M>>4 [24,29), A scale id [29,31).
-template <int KIND>
+template <int KIND, int BNT>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
     const uint32_t fmt = KIND == 0 ? 1u : 0u;       // E2M1 for mxf4nvf4, E4M3 for mxf8f6f4
     const uint32_t scale_type = KIND == 0 ? 0u : 1u;
-    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (scale_type << 23) |
+    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BNT >> 3) << 17) | (scale_type << 23) |
            ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
@@ -287,13 +293,13 @@ struct Tile {
     int e;
 };
 
-template <int KIND>
+template <int KIND, int BNT>
 __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
     Tile tl;
     if (!p.group_k) {
         const int64_t mt = t / p.n_tiles_n, nt = t - mt * p.n_tiles_n;
         tl.m0 = mt * BM;
-        tl.n0 = nt * BN;
+        tl.n0 = nt * BNT;
         int lo = 0, hi = p.E;  // largest e with offs[e] <= m0
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -309,7 +315,7 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
         const int64_t mt = rem / p.n_tiles_n, nt = rem - mt * p.n_tiles_n;
         tl.e = (int)e;
         tl.m0 = mt * BM;
-        tl.n0 = nt * BN;
+        tl.n0 = nt * BNT;
         tl.b_row = tl.n0;
         const int32_t k0 = __ldg(p.offs + e), k1 = __ldg(p.offs + e + 1);
         tl.k_begin = k0;
@@ -325,13 +331,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // tmW: the output D (EPI_TMA) or the master weights (EPI_SGD); tmWb: their bf16 copy (EPI_SGD)
     constexpr bool kSgd = EM == EPI_SGD;
     constexpr int NST = EpiCfg<EM>::NST;
-    using L = Layout<KIND, NST, EpiCfg<EM>::BYTES>;
+    constexpr int BNT = EpiCfg<EM>::BNT;
+    using L = Layout<KIND, NST, EpiCfg<EM>::BYTES, BNT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars, *empty = bars + NST;
-    uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 1, *drain = tmem_full + 2;
-    uint64_t *epi_bar = tmem_full + 3;  // fused SGD: SGD_NB per epilogue warp
+    // per accumulator buffer: tmem_full (MMA done) and tmem_empty (epilogue has read it)
+    uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 2, *drain = tmem_full + 4;
+    uint64_t *epi_bar = tmem_full + 5;  // fused SGD: SGD_NB per epilogue warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -341,8 +349,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, EPI_THREADS);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tmem_full + i, 1);
+            mbar_init(tmem_empty + i, EPI_THREADS);
+        }
         mbar_init(drain, 1);
         for (int i = 0; i < 8 * SGD_NB; ++i) mbar_init(epi_bar + i, 1);
         *abort_flag = 0;
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool issued[NST];
         for (int s = 0; s < NST; ++s) issued[s] = false, issued_parity[s] = 0;
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND>(p, t);
+            const Tile tl = decode_tile<KIND, BNT>(p, t);
             for (int ks = 0; ks < tl.n_stages; ++ks) {
                 if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag)) break;
                 uint64_t *fb = full + stage;
@@ -375,11 +385,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t kel = tl.k_begin + (int64_t)ks * Cfg<KIND>::ELEMS;   // contraction element
                 const int xbytes = (int)(KIND == 0 ? kel / 2 : kel);
                 tma_load_2d(smem + L::OFF_A + stage * A_TILE, &tmA, fb, xbytes, (int)tl.m0);
-                tma_load_2d(smem + L::OFF_B + stage * B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
+                tma_load_2d(smem + L::OFF_B + stage * L::B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
                 const int64_t atom = kel / Cfg<KIND>::ELEMS_PER_ATOM;
                 const uint8_t *sa = p.sfa + ((tl.m0 / BM) * p.sfa_tile_stride + atom) * 512;
                 bulk_load(smem + L::OFF_SFA + stage * L::SFA, sa, L::SFA, fb);
-                for (int rt = 0; rt < 2; ++rt) {
+                for (int rt = 0; rt < L::RT; ++rt) {
                     const uint8_t *sb = p.sfb + ((tl.b_row / BM + rt) * p.sfb_tile_stride + atom) * 512;
                     bulk_load(smem + L::OFF_SFB + stage * L::SFB + rt * L::SFA, sb, L::SFA, fb);
                 }
@@ -400,31 +410,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
+        uint32_t phase = 0;
+        uint32_t acc_ph[2] = {0u, 0u};
+        int acc = 0;  // accumulator buffer of this tile
         const uint32_t a_base = smem_u32(smem + L::OFF_A), b_base = smem_u32(smem + L::OFF_B);
         const uint32_t sfa_base = smem_u32(smem + L::OFF_SFA), sfb_base = smem_u32(smem + L::OFF_SFB);
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND>(p, t);
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag)) break;
+            const Tile tl = decode_tile<KIND, BNT>(p, t);
+            if (!mbar_wait(tmem_empty + acc, acc_ph[acc] ^ 1u, abort_flag)) break;
             tc_fence_after();
+            const uint32_t tmem_d = tmem + (uint32_t)(acc * BNT);
             if (tl.n_stages == 0) {
-                mbar_arrive(tmem_full);
+                mbar_arrive(tmem_full + acc);
             } else {
                 for (int ks = 0; ks < tl.n_stages; ++ks) {
                     if (!mbar_wait(full + stage, phase, abort_flag)) break;
                     tc_fence_after();
-                    const uint32_t sf_col = tmem + ACC_COLS + stage * L::SF_COLS;
+                    const uint32_t sf_col = tmem + L::SF_BASE + stage * L::SF_COLS;
                     // scale factors: atom i of A -> columns sf_col + 4i; atom i of B row tile rt ->
-                    // sf_col + SF_COLS_A + 8i + 4rt
+                    // sf_col + SF_COLS_A + 4*RT*i + 4rt
 #pragma unroll
                     for (int i = 0; i < Cfg<KIND>::ATOMS; ++i) {
                         tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_base + stage * L::SFA + i * 512, 0, 128, 0));
 #pragma unroll
-                        for (int rt = 0; rt < 2; ++rt)
-                            tc_cp_sf(sf_col + L::SF_COLS_A + 8 * i + 4 * rt,
+                        for (int rt = 0; rt < L::RT; ++rt)
+                            tc_cp_sf(sf_col + L::SF_COLS_A + 4 * L::RT * i + 4 * rt,
                                      smem_desc(sfb_base + stage * L::SFB + rt * L::SFA + i * 512, 0, 128, 0));
                     }
-                    const uint32_t a_addr = a_base + stage * A_TILE, b_addr = b_base + stage * B_TILE;
+                    const uint32_t a_addr = a_base + stage * A_TILE, b_addr = b_base + stage * L::B_TILE;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024, 2);
@@ -432,21 +445,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint32_t sfa_t, sfb_t, idesc;
                         if constexpr (KIND == 0) {
                             sfa_t = sf_col + 4 * k;
-                            sfb_t = sf_col + L::SF_COLS_A + 8 * k;
-                            idesc = make_idesc<0>(0);
+                            sfb_t = sf_col + L::SF_COLS_A + 4 * L::RT * k;
+                            idesc = make_idesc<0, BNT>(0);
                         } else {
                             sfa_t = sf_col;
                             sfb_t = sf_col + L::SF_COLS_A;
-                            idesc = make_idesc<1>((uint32_t)k);
+                            idesc = make_idesc<1, BNT>((uint32_t)k);
                         }
-                        tc_mma<KIND>(tmem, ad, bd, idesc, sfa_t, sfb_t, (ks > 0 || k > 0) ? 1u : 0u);
+                        tc_mma<KIND>(tmem_d, ad, bd, idesc, sfa_t, sfb_t, (ks > 0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty + stage);
                     if (++stage == NST) stage = 0, phase ^= 1u;
                 }
-                tc_commit(tmem_full);
+                tc_commit(tmem_full + acc);
             }
-            acc_phase ^= 1u;
+            acc_ph[acc] ^= 1u;
+            if (L::NACC == 2) acc ^= 1;
         }
         // all of this thread's MMAs and copies complete before tensor memory is freed
         tc_commit(drain);
@@ -459,18 +473,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         // warp w reads TMEM lanes 32*(w%4).. (its rows) and half (w-4)/4 of the tile's columns
         const int q = warp & 3;
         const int half = (warp - 4) >> 2;
-        uint32_t acc_phase = 0;
+        uint32_t acc_ph[2] = {0u, 0u};
+        int acc = 0;
         uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND>(p, t);
-            if (!mbar_wait(tmem_full, acc_phase, abort_flag)) break;
+            const Tile tl = decode_tile<KIND, BNT>(p, t);
+            if (!mbar_wait(tmem_full + acc, acc_ph[acc], abort_flag)) break;
             tc_fence_after();
             const bool live = tl.n_stages > 0;
             float alpha = 1.0f;
             if constexpr (KIND == 0) alpha = __fmul_rn(__ldg(p.a_g_dec), __ldg(p.b_g_dec + tl.e));
             const int64_t row = tl.m0 + q * 32 + lane;
-            const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0 + half * (BN / 2);
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (BN / 2));
+            const int64_t dbase = (p.group_k ? (int64_t)tl.e * p.M * p.N : 0) + row * p.N + tl.n0 + half * (BNT / 2);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNT + half * (BNT / 2));
             if constexpr (kSgd) {
                 // W32 <- W32 - lr * dW, bf16 copy, running max |bf16|.  This warp owns rows
                 // 32q..32q+31 and columns half*128 .. +127 of the tile, in NCH 16-column chunks.
@@ -482,20 +497,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // (32-byte swizzle: piece j at j ^ ((l >> 2) & 1)), and TMA stores both.  The load
                 // of chunk u + SGD_LA is issued before chunk u is processed; it may belong to the
                 // CTA's next tile, whose master weights do not depend on that tile's accumulator.
-                constexpr int NCH = (BN / 2) / SGD_CW;
+                constexpr int NCH = (BNT / 2) / SGD_CW;
                 const int wi = warp - 4;
                 uint8_t *wring = smem + L::OFF_EPI + wi * EPI_WARP_BYTES;
                 uint8_t *bring = wring + SGD_NB * SGD_W_CHUNK;
                 uint64_t *eb = epi_bar + SGD_NB * wi;
                 const int y0 = (int)((int64_t)tl.e * p.M + tl.m0 + q * 32);
-                const int x0 = (int)(tl.n0 + half * (BN / 2));
+                const int x0 = (int)(tl.n0 + half * (BNT / 2));
                 const int64_t tn = t + gridDim.x;
                 const bool has_next = tn < p.num_tiles;
                 int ny0 = 0, nx0 = 0;
                 if (has_next) {
-                    const Tile tn_l = decode_tile<KIND>(p, tn);
+                    const Tile tn_l = decode_tile<KIND, BNT>(p, tn);
                     ny0 = (int)((int64_t)tn_l.e * p.M + tn_l.m0 + q * 32);
-                    nx0 = (int)(tn_l.n0 + half * (BN / 2));
+                    nx0 = (int)(tn_l.n0 + half * (BNT / 2));
                 }
                 const uint32_t u0 = sgd_tile * NCH;  // this tile's first chunk in the stream
                 // last chunk that may be issued: the end of this tile, or of the next one
@@ -600,7 +615,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // the staged rows are all this warp needs: hand the accumulator back now, so the
                 // next tile's MMAs overlap the transform and quantisation below
                 tc_fence_before();
-                mbar_arrive(tmem_empty);
+                mbar_arrive(tmem_empty + acc);
                 __syncwarp();
                 const int sub = lane & 7;
                 uint8_t *q_out = static_cast<uint8_t *>(p.d);
@@ -629,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         cw[j] = e4m3x4_rn(__fmul_rn(u[4 * j], sc), __fmul_rn(u[4 * j + 1], sc),
                                           __fmul_rn(u[4 * j + 2], sc), __fmul_rn(u[4 * j + 3], sc));
                     const int64_t grow = tl.m0 + q * 32 + rr;
-                    const int64_t col = tl.n0 + half * (BN / 2) + sub * 16;
+                    const int64_t col = tl.n0 + half * (BNT / 2) + sub * 16;
                     *reinterpret_cast<uint4 *>(q_out + grow * p.N + col) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                     if ((sub & 1) == 0) p.e8[grow * (p.N / 32) + col / 32] = (uint8_t)(e + 127);
                 }
@@ -640,8 +655,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // the 64-byte swizzle; piece j of row l sits at j ^ (l & 7) or j ^ ((l >> 1) & 3))
                 uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE;
                 const int y0 = (int)((p.group_k ? (int64_t)tl.e * p.M : 0) + tl.m0 + q * 32);
-                const int x0 = (int)(tl.n0 + half * (BN / 2));
-                for (int c = 0; c < BN / 64; ++c) {
+                const int x0 = (int)(tl.n0 + half * (BNT / 2));
+                for (int c = 0; c < BNT / 64; ++c) {
                     uint32_t r[32];
                     if (live) {
                         tc_ld32(tbase + (uint32_t)(c * 32), r);
@@ -682,7 +697,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             } else {
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = 0; c < BNT / 64; ++c) {
                     uint32_t r[32];
                     if (live) {
                         tc_ld32(tbase + (uint32_t)(c * 32), r);
@@ -726,9 +741,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if constexpr (EM != EPI_HMX) {
                 tc_fence_before();
-                mbar_arrive(tmem_empty);
+                mbar_arrive(tmem_empty + acc);
             }
-            acc_phase ^= 1u;
+            acc_ph[acc] ^= 1u;
+            if (L::NACC == 2) acc ^= 1;
         }
         if constexpr (kSgd) {
             // master-weight loads the loop did not consume (it stopped early): let them land
@@ -793,7 +809,7 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int6
 template <int KIND, int EM>
 static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tw, const CUtensorMap &twb,
                   const Args &a, cudaStream_t st) {
-    using L = Layout<KIND, EpiCfg<EM>::NST, EpiCfg<EM>::BYTES>;
+    using L = Layout<KIND, EpiCfg<EM>::NST, EpiCfg<EM>::BYTES, EpiCfg<EM>::BNT>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, EM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1015,7 +1031,8 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
         int rc = stage_scales(a_e8, M, b_e8, N, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
         if (rc != MOE4_OK) return rc;
     }
-    if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BN)) return MOE4_ERR_CUDA;
+    constexpr int BNS = EpiCfg<EPI_SGD>::BNT;
+    if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BNS)) return MOE4_ERR_CUDA;
     g.sfa = sfa;
     g.sfb = sfb;
     g.offs = group_offs;
@@ -1030,7 +1047,7 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     g.lr = lr;
     g.amax = reinterpret_cast<unsigned int *>(amax_out);
     g.n_tiles_m = (int)(M / BM);
-    g.n_tiles_n = (int)(N / BN);
+    g.n_tiles_n = (int)(N / BNS);
     g.num_tiles = E * g.n_tiles_m * g.n_tiles_n;
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
