@@ -78,11 +78,24 @@ __device__ __forceinline__ GlobalScale global_scale(float amax) {
 // element i), scale code, and the pairwise-tree sum of squared errors.  Every binary32 step is a
 // round-to-nearest intrinsic that is never fused into a multiply-add (a fused d*d + s would round
 // once and change near-tie choices); the products e2m1 * e4m3 are exact in f16x2.
-__device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, float m, uint32_t &w0, uint32_t &w1,
-                                                 uint32_t &scode) {
-    const float t = __fdiv_rn(a, m);
-    scode = e4m3_rn(t);
-    const float sfv = e4m3_to_f32(scode);
+// tab[code] = (E4M3 value of a scale code, RN(1/value)) for codes 0..127, built per CTA by
+// fill_scale_tab with the same conversion and division, so a lookup replaces both.
+__device__ __forceinline__ void fill_scale_tab(float2 *tab) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const float v = e4m3_to_f32((uint32_t)i);
+        tab[i] = make_float2(v, v == 0.0f ? 0.0f : __fdiv_rn(1.0f, v));
+    }
+    __syncthreads();
+}
+
+template <int M>  // the candidate's target for the block amax: 6 or 4
+__device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, const float2 *tab, uint32_t &w0,
+                                                 uint32_t &w1, uint32_t &scode) {
+    // a/4 is a power-of-two scaling: the product by 0.25 rounds the same real number
+    const float t = M == 4 ? __fmul_rn(a, 0.25f) : __fdiv_rn(a, (float)M);
+    scode = e4m3_rn(t);  // t >= 0 (or NaN): codes 0..0x7F
+    const float2 sv = tab[scode];
+    const float sfv = sv.x;
     float d[16];
     if (sfv == 0.0f) {
         w0 = w1 = 0;
@@ -94,7 +107,7 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, flo
 #pragma unroll
         for (int i = 0; i < 16; ++i) d[i] = y[i];
     } else {
-        const float rcp = __fdiv_rn(1.0f, sfv);
+        const float rcp = sv.y;
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(y[i], rcp);
@@ -120,15 +133,15 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, flo
     return s[0];
 }
 
-__device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, uint32_t &w0, uint32_t &w1,
-                                            uint32_t &scode) {
+__device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, const float2 *tab, uint32_t &w0,
+                                            uint32_t &w1, uint32_t &scode) {
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(y[i]));
-    const float err6 = nvfp4_candidate(y, a, 6.0f, w0, w1, scode);
+    const float err6 = nvfp4_candidate<6>(y, a, tab, w0, w1, scode);
     if (four_over_six) {
         uint32_t u0, u1, s4;
-        const float err4 = nvfp4_candidate(y, a, 4.0f, u0, u1, s4);
+        const float err4 = nvfp4_candidate<4>(y, a, tab, u0, u1, s4);
         if (err4 < err6) {
             w0 = u0;
             w1 = u1;
@@ -154,6 +167,8 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
     float *__restrict__ g_dec) {
+    __shared__ float2 tab[128];
+    fill_scale_tab(tab);
     const int64_t nblk = cols / 16;
     const int64_t per_mat = rows * nblk;
     const int64_t total = nmat * per_mat;
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
             y[2 * i + 1] = __fmul_rn(bf16_hi(wv[i]), g_enc);
         }
         uint32_t w0, w1, scode;
-        nvfp4_block(y, four_over_six, w0, w1, scode);
+        nvfp4_block(y, four_over_six, tab, w0, w1, scode);
         *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
         if (sf_mma)
             sf[mat_begin + sf_mma_offset(row, blk, nblk)] = (uint8_t)scode;
@@ -295,6 +310,8 @@ __global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__r
                                                              const unsigned int *__restrict__ amax_bits,
                                                              bool four_over_six, uint8_t *__restrict__ codes,
                                                              uint8_t *__restrict__ sf, float *__restrict__ g_dec) {
+    __shared__ float2 tab[128];
+    fill_scale_tab(tab);
     const GlobalScale gs = global_scale(__uint_as_float(*amax_bits));
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_dec = gs.dec;
     MOE4_SUB16_LOOP(nsub) {
@@ -311,7 +328,7 @@ __global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__r
 #pragma unroll
         for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], gs.enc);
         uint32_t w0, w1, scode;
-        nvfp4_block(u, four_over_six, w0, w1, scode);
+        nvfp4_block(u, four_over_six, tab, w0, w1, scode);
         if (live) {
             *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
             sf[b] = (uint8_t)scode;
