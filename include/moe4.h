@@ -81,7 +81,9 @@ const char *moe4_status_string(int status);  /* static string, never NULL */
 #define MOE4_OP_PERMUTE_PLAN     3 /* a = tokens, b = top_k, c = experts */
 size_t moe4_workspace_size(int op, int64_t a, int64_t b, int64_t c);
 /* Scratch for the grouped GEMMs when their scale factors come in the canonical layout:
- * kind 0 = NVFP4 (16-blocks), 1 = MXFP8 (32-blocks); a_rows x K for A, E x b_rows x K for B. */
+ * kind 0 = NVFP4 (16-blocks), 1 = MXFP8 (32-blocks); a_rows x K for A, E x b_rows x K for B.
+ * Kind 1 adds 16 KiB that grouped_gemm_mxfp8_wgrad_sgd uses for its tile schedule (an order of
+ * the experts by group size); with less, that kernel runs its tiles in expert order. */
 size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, int64_t b_rows, int64_t K);
 
 /* Synchronise `stream`, then read and clear the device status word that kernels set when a

@@ -88,7 +88,9 @@ extern "C" size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, 
     const int64_t blk = kind == 0 ? 16 : 32;
     const size_t a = (size_t)(a_rows * (K / blk));
     const size_t b = (size_t)(E * b_rows * (K / blk));
-    return ((a + 255) / 256 * 256) + ((b + 255) / 256 * 256);
+    // MXFP8: room for the contraction-grouped kernels' expert order (up to 4096 experts)
+    const size_t order = kind == 1 ? 4096 * sizeof(int32_t) : 0;
+    return ((a + 255) / 256 * 256) + ((b + 255) / 256 * 256) + order;
 }
 
 extern "C" int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream) {

@@ -137,6 +137,7 @@ struct Args {
     float lr;               // Out::Sgd
     unsigned int *amax;     // Out::Sgd: per-expert max |bf16 copy| as binary32 bits
     uint8_t *e8;            // fused codec: E8M0 scales [M, N/32] (d holds the E4M3 codes [M, N])
+    const int32_t *order;   // contraction-grouped: experts by decreasing group size, or null
     int64_t num_tiles;
     int n_tiles_n, n_tiles_m;
     int64_t sfa_tile_stride;  // atoms between consecutive 128-row tiles of A's scale layout
@@ -310,8 +311,20 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
         tl.k_begin = 0;
         tl.n_stages = (int)(p.K / Cfg<KIND>::ELEMS);
     } else {
+        // With an expert order, tiles are listed expert by expert in decreasing group size and
+        // slot t = c + G*i (CTA c of G, its i-th tile) takes the list's next entry from the front
+        // when c + i is even and from the back otherwise: at any time half the CTAs work on long
+        // contractions (operand-bound) and half on short ones (master-weight-bound), and each CTA
+        // alternates.  For even G this maps slots onto list positions one to one.
         const int64_t per_e = (int64_t)p.n_tiles_m * p.n_tiles_n;
-        const int64_t e = t / per_e, rem = t - e * per_e;
+        int64_t l = t;
+        if (p.order != nullptr && (gridDim.x & 1u) == 0) {
+            const int64_t G = gridDim.x, c = t % G, i = t / G;
+            const int64_t fi = i * (G / 2) + c / 2;
+            l = ((c + i) & 1) == 0 ? fi : p.num_tiles - 1 - fi;
+        }
+        const int64_t r = l / per_e, rem = l - r * per_e;
+        const int64_t e = p.order != nullptr ? (int64_t)__ldg(p.order + r) : r;
         const int64_t mt = rem / p.n_tiles_n, nt = rem - mt * p.n_tiles_n;
         tl.e = (int)e;
         tl.m0 = mt * BM;
@@ -845,6 +858,20 @@ extern "C" int moe4_get_status(void *stream) {
 }
 
 // Canonical scales -> tensor-core layout into ws when the caller did not pass that layout.
+// order[rank] = expert, ranks by decreasing group size (ties: lower expert first).  One CTA.
+__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t *__restrict__ offs, int E,
+                                                            int32_t *__restrict__ order) {
+    __shared__ int32_t sz[4096];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sz[e] = __ldg(offs + e + 1) - __ldg(offs + e);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int ke = sz[e];
+        int rank = 0;
+        for (int j = 0; j < E; ++j) rank += (sz[j] > ke) || (sz[j] == ke && j < e);
+        order[rank] = e;
+    }
+}
+
 static int stage_scales(const uint8_t *a_sf, int64_t a_rows, const uint8_t *b_sf, int64_t b_rows, int64_t K, int blk,
                         uint32_t flags, void *ws, size_t ws_bytes, const uint8_t **sfa, const uint8_t **sfb,
                         cudaStream_t st) {
@@ -1033,6 +1060,18 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     }
     constexpr int BNS = EpiCfg<EPI_SGD>::BNT;
     if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BNS)) return MOE4_ERR_CUDA;
+    // the expert order for the tile schedule, after the staged scales in the workspace (without
+    // room for it the tiles run in expert order)
+    size_t used = 0;
+    if (K > 0 && !(flags & MOE4_SF_MMA_LAYOUT)) {
+        const size_t na = (size_t)(M * (K / 32)), nb = (size_t)(N * (K / 32));
+        used = (na + 255) / 256 * 256 + (nb + 255) / 256 * 256;
+    }
+    if (E <= 4096 && ws && aligned16(ws) && ws_bytes >= used + (size_t)E * sizeof(int32_t)) {
+        int32_t *order = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + used);
+        expert_order_kernel<<<1, 1024, 0, st>>>(group_offs, (int)E, order);
+        g.order = order;
+    }
     g.sfa = sfa;
     g.sfb = sfb;
     g.offs = group_offs;
