@@ -297,10 +297,12 @@ struct Tile {
 template <int KIND, int BNT>
 __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
     Tile tl;
+    // tile indices and counts are below 2^31: 32-bit division (the 64-bit one is a long sequence)
+    const uint32_t t32 = (uint32_t)t, ntn = (uint32_t)p.n_tiles_n;
     if (!p.group_k) {
-        const int64_t mt = t / p.n_tiles_n, nt = t - mt * p.n_tiles_n;
-        tl.m0 = mt * BM;
-        tl.n0 = nt * BNT;
+        const uint32_t mt = t32 / ntn, nt = t32 - mt * ntn;
+        tl.m0 = (int64_t)mt * BM;
+        tl.n0 = (int64_t)nt * BNT;
         int lo = 0, hi = p.E;  // largest e with offs[e] <= m0
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -316,19 +318,19 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
         // when c + i is even and from the back otherwise: at any time half the CTAs work on long
         // contractions (operand-bound) and half on short ones (master-weight-bound), and each CTA
         // alternates.  For even G this maps slots onto list positions one to one.
-        const int64_t per_e = (int64_t)p.n_tiles_m * p.n_tiles_n;
-        int64_t l = t;
+        const uint32_t per_e = (uint32_t)p.n_tiles_m * ntn;
+        uint32_t l = t32;
         if (p.order != nullptr && (gridDim.x & 1u) == 0) {
-            const int64_t G = gridDim.x, c = t % G, i = t / G;
-            const int64_t fi = i * (G / 2) + c / 2;
-            l = ((c + i) & 1) == 0 ? fi : p.num_tiles - 1 - fi;
+            const uint32_t G = gridDim.x, i = t32 / G, c = t32 - i * G;
+            const uint32_t fi = i * (G / 2) + c / 2;
+            l = ((c + i) & 1) == 0 ? fi : (uint32_t)p.num_tiles - 1 - fi;
         }
-        const int64_t r = l / per_e, rem = l - r * per_e;
-        const int64_t e = p.order != nullptr ? (int64_t)__ldg(p.order + r) : r;
-        const int64_t mt = rem / p.n_tiles_n, nt = rem - mt * p.n_tiles_n;
-        tl.e = (int)e;
-        tl.m0 = mt * BM;
-        tl.n0 = nt * BNT;
+        const uint32_t r = l / per_e, rem = l - r * per_e;
+        const int e = p.order != nullptr ? __ldg(p.order + r) : (int)r;
+        const uint32_t mt = rem / ntn, nt = rem - mt * ntn;
+        tl.e = e;
+        tl.m0 = (int64_t)mt * BM;
+        tl.n0 = (int64_t)nt * BNT;
         tl.b_row = tl.n0;
         const int32_t k0 = __ldg(p.offs + e), k1 = __ldg(p.offs + e + 1);
         tl.k_begin = k0;
@@ -491,6 +493,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
         for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND, BNT>(p, t);
+            // fused SGD: the CTA's next tile (its first master-weight chunks are loaded ahead),
+            // decoded while the accumulator is still being produced
+            const int64_t tn = t + gridDim.x;
+            const bool has_next = tn < p.num_tiles;
+            Tile tn_l{};
+            if (kSgd && has_next) tn_l = decode_tile<KIND, BNT>(p, tn);
             if (!mbar_wait(tmem_full + acc, acc_ph[acc], abort_flag)) break;
             tc_fence_after();
             const bool live = tl.n_stages > 0;
@@ -517,11 +525,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint64_t *eb = epi_bar + SGD_NB * wi;
                 const int y0 = (int)((int64_t)tl.e * p.M + tl.m0 + q * 32);
                 const int x0 = (int)(tl.n0 + half * (BNT / 2));
-                const int64_t tn = t + gridDim.x;
-                const bool has_next = tn < p.num_tiles;
                 int ny0 = 0, nx0 = 0;
                 if (has_next) {
-                    const Tile tn_l = decode_tile<KIND, BNT>(p, tn);
                     ny0 = (int)((int64_t)tn_l.e * p.M + tn_l.m0 + q * 32);
                     nx0 = (int)(tn_l.n0 + half * (BNT / 2));
                 }
