@@ -145,23 +145,25 @@ class LayerStep:
         fwd = 2 * rows * (2 * self.f) * self.d + 2 * rows * self.d * self.f
         return fwd, 2 * fwd
 
-    def run(self, timer=None):
+    def run(self, timer=None, io=None):
+        """One layer step; io = (X, logits, dy, y) device tensors to use instead of the step's own."""
         m, torch = self.m, self.torch
         T, d, f, E, k = self.T, self.d, self.f, self.E, self.k
         FOS, MMA = m.FOUR_OVER_SIX, m.SF_MMA_LAYOUT
         tm = timer if timer is not None else _NullTimer()
+        X, logits, dy, y = io if io is not None else (self.X, self.logits, self.dy, self.y)
         n = 0
         seed = 1000 + self.step_index
         self.step_index += 1
         # ---------------- forward
         with tm("route"):
-            m.moe4_route_topk(self.logits, T, E, k, self.idx, self.w)
+            m.moe4_route_topk(logits, T, E, k, self.idx, self.w)
             m.moe4_permute_plan(self.idx, T, k, E, self.offs, self.row_of, self.src_of, self.rows_cap, self.plan_ws)
         n += 4
         Rp = int(self.offs[E].item())          # host needs the padded row count (one 4-byte read)
         self.Rp = Rp
         with tm("quant_x"):
-            m.nvfp4_quantize(self.X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
+            m.nvfp4_quantize(X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
             m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
         n += 3
         with tm("quant_w"):
@@ -187,11 +189,11 @@ class LayerStep:
             m.hadamard_dequant(self.Yc_c, self.Yc_s, self.Yc_g, Rp, d, self.Yhat[:Rp])
         n += 3
         with tm("combine"):
-            m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, self.y)
+            m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, y)
         n += 1
         # ---------------- backward
         with tm("mxfp8_quant"):
-            m.moe4_combine_backward(self.dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYp[:Rp])
+            m.moe4_combine_backward(dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYp[:Rp])
             m.mxfp8_quantize_rowcol(self.dYp[:Rp], Rp, d, self.dYr_q, self.dYr_e, self.dYc_q, self.dYc_e)
         n += 2
         with tm("requant"):
@@ -734,31 +736,56 @@ def main():
     # ------------------------------------------------ end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
+        # Each step's inputs (X, logits, dy) come from pinned host memory and its output y goes back
+        # to pinned host memory, inside the timed region.  As in a training loop, step i+1's inputs
+        # are copied on a side stream while step i computes (two device input sets), and step i's
+        # y is copied back after it (two device y buffers); the region ends when every copy is done.
         hX = torch.empty(step.X.shape, dtype=step.X.dtype, pin_memory=True)
         hX.copy_(step.X)
         hL = torch.empty(step.logits.shape, dtype=step.logits.dtype, pin_memory=True)
         hL.copy_(step.logits)
         hD = torch.empty(step.dy.shape, dtype=step.dy.dtype, pin_memory=True)
         hD.copy_(step.dy)
-        hY = torch.empty(step.y.shape, dtype=step.y.dtype, pin_memory=True)
+        hY = [torch.empty(step.y.shape, dtype=step.y.dtype, pin_memory=True) for _ in range(2)]
+        io = [(step.X, step.logits, step.dy, step.y),
+              (torch.empty_like(step.X), torch.empty_like(step.logits), torch.empty_like(step.dy),
+               torch.empty_like(step.y))]
+        cs = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+
+        def copy_in(b):
+            with torch.cuda.stream(cs):
+                io[b][0].copy_(hX, non_blocking=True)
+                io[b][1].copy_(hL, non_blocking=True)
+                io[b][2].copy_(hD, non_blocking=True)
+                ev_in[b].record(cs)
+
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            step.X.copy_(hX, non_blocking=True)
-            step.logits.copy_(hL, non_blocking=True)
-            step.dy.copy_(hD, non_blocking=True)
-            step.run()
-            hY.copy_(step.y, non_blocking=True)
-            torch.cuda.synchronize()
+        copy_in(0)
+        for i in range(args.steps):
+            b = i % 2
+            if i + 1 < args.steps:
+                if i >= 1:
+                    cs.wait_event(ev_done[1 - b])  # step i-1 is done with that input set
+                copy_in(1 - b)
+            torch.cuda.current_stream().wait_event(ev_in[b])
+            step.run(io=io[b])
+            ev_done[b].record()
+            cs.wait_event(ev_done[b])
+            with torch.cuda.stream(cs):
+                hY[b].copy_(io[b][3], non_blocking=True)
+        torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
         if dist is not None:
             tt = torch.tensor([e2e_s], dtype=torch.float64)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e2e_s = float(tt.item())
         h2d = hX.numel() * 2 + hL.numel() * 4 + hD.numel() * 2
-        d2h = hY.numel() * 2 + 4
+        d2h = hY[0].numel() * 2 + 4
         e2e = {"value": world * step_flops * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s / args.steps * 1e3}
 
