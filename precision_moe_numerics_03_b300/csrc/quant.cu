@@ -109,8 +109,10 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, con
     } else {
         const float rcp = sv.y;
         float v[16];
+        // packed products: they feed only the E2M1 conversion, never an add, so nothing can fuse
+        const uint64_t r2 = f2_pack(rcp, rcp);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(y[i], rcp);
+        for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(y[2 * i], y[2 * i + 1]), r2), v[2 * i], v[2 * i + 1]);
         w0 = e2m1x8_rn(v);
         w1 = e2m1x8_rn(v + 8);
         uint32_t sfh2 = e4m3x2_to_h2(scode | (scode << 8));
