@@ -115,14 +115,14 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, con
         for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(y[2 * i], y[2 * i + 1]), r2), v[2 * i], v[2 * i + 1]);
         w0 = e2m1x8_rn(v);
         w1 = e2m1x8_rn(v + 8);
-        uint32_t sfh2 = e4m3x2_to_h2(scode | (scode << 8));
-        const __half2 sfh = *reinterpret_cast<const __half2 *>(&sfh2);
+        // d = y - e*sf: e*sf has at most 6 significant bits and is exact in binary32, so the fused
+        // form rounds once, exactly as the subtraction of the exact product does
+        const float nsf = -sfv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint32_t h = e2m1x2_to_h2((i < 4 ? w0 : w1) >> (8 * (i & 3)));
-            const float2 f = __half22float2(__hmul2(*reinterpret_cast<const __half2 *>(&h), sfh));
-            d[2 * i] = __fsub_rn(y[2 * i], f.x);
-            d[2 * i + 1] = __fsub_rn(y[2 * i + 1], f.y);
+            const float2 e = h2_bits_to_f2(e2m1x2_to_h2((i < 4 ? w0 : w1) >> (8 * (i & 3))));
+            d[2 * i] = __fmaf_rn(e.x, nsf, y[2 * i]);
+            d[2 * i + 1] = __fmaf_rn(e.y, nsf, y[2 * i + 1]);
         }
     }
     float s[16];
