@@ -346,6 +346,53 @@ def measure_next_rows(step, reps=3):
     }
 
 
+def compute_probe(kind, reps=5, dev="cuda:0"):
+    """The grouped GEMM on a compute-bound shape (not the layer's): 8 groups of 8192 rows, N = K =
+    8192, bf16 out (about 5.3k FLOP per byte).  kind 0: NVFP4 (Four Over Six operands, tensor-core
+    scale layout); kind 1: MXFP8 (nearest-even operands, rows grouped).  Returns (ms, TFLOP/s)."""
+    import torch
+    from precision_moe_numerics_03_b300 import inputs, moe4 as m
+    E, rows_e, N, K = 8, 8192, 8192, 8192
+    R = E * rows_e
+    g = lambda s: inputs.device_generator(11, s, dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    x = inputs.device_normal((R, K), 1.0, g(0), dev).view(torch.int16)
+    w = inputs.device_normal((E * N, K), 0.02, g(1), dev).view(torch.int16)
+    offs = torch.arange(0, R + 1, rows_e, dtype=torch.int32, device=dev)
+    out = torch.empty((R, N), dtype=torch.int16, device=dev)
+    if kind == 0:
+        MMA = m.SF_MMA_LAYOUT
+        ac, asf = torch.empty((R, K // 2), **u8), torch.empty((R, K // 16), **u8)
+        bc, bsf = torch.empty((E * N, K // 2), **u8), torch.empty((E * N, K // 16), **u8)
+        ag, bg = torch.empty(1, dtype=torch.float32, device=dev), torch.empty(E, dtype=torch.float32, device=dev)
+        qws = m.workspace(m.moe4_workspace_size(m.OP_NVFP4_QUANTIZE, E), dev)
+        m.nvfp4_quantize(x, 1, R, K, K, ac, asf, ag, None, m.FOUR_OVER_SIX | MMA, qws)
+        m.nvfp4_quantize(w, E, N, K, K, bc, bsf, bg, None, m.FOUR_OVER_SIX | MMA, qws)
+        del x, w
+        call = lambda: m.grouped_expert_gemm_nvfp4(ac, asf, ag, bc, bsf, bg, offs, E, R, N, K, out, m.OUT_BF16 | MMA)
+    else:
+        aq, ae = torch.empty((R, K), **u8), torch.empty((R, K // 32), **u8)
+        bq, be = torch.empty((E * N, K), **u8), torch.empty((E * N, K // 32), **u8)
+        m.mxfp8_quantize(x, R, K, aq, ae, 0, 0, m.ROWWISE)
+        m.mxfp8_quantize(w, E * N, K, bq, be, 0, 0, m.ROWWISE)
+        del x, w
+        ws = m.workspace(m.moe4_workspace_size_gemm(1, R, E, N, K), dev)
+        call = lambda: m.grouped_gemm_mxfp8(aq, ae, bq, be, offs, E, R, N, K, out, m.OUT_BF16 | m.GROUP_M, ws)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(reps):
+        call()
+    e0.record()
+    torch.cuda.synchronize()
+    if m.moe4_get_status() != m.OK:
+        raise RuntimeError("a device wait timed out in the compute probe")
+    ms = s0.elapsed_time(e0) / reps
+    return ms, 2.0 * R * N * K / (ms / 1e3) / 1e12
+
+
 class _NullTimer:
     def __call__(self, name):
         return self
@@ -562,6 +609,10 @@ def profile_case(name):
             out = torch.empty((rows, d), dtype=torch.int16, device=dev)
             calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws))
             calls.append(lambda: moe4.hadamard_dequant(c, s_, gd, rows, d, out))
+    elif name in ("gemm_nvfp4_probe", "gemm_mxfp8_probe"):
+        compute_probe(0 if name == "gemm_nvfp4_probe" else 1, reps=3, dev=dev)
+        print("profile case %s done" % name)
+        return 0
     elif name == "gemm_nvfp4":
         rows = 128 * 64
         x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
@@ -629,7 +680,8 @@ def main():
     ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
-                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard"],
+                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "gemm_nvfp4_probe",
+                             "gemm_mxfp8_probe"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
     if args.profile_case:
@@ -797,6 +849,15 @@ def main():
         mf["nvfp4_gemm_speedup"] = round(mf["gemm_ms"] / per["gemm_nvfp4"], 3)
         mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["swiglu_quant_h"], 4)
         nxt["hadamard_mxfp8_codec"]["nvfp4_codec_ms"] = round(per["hadamard"], 4)
+        probe = {"shape": "8 groups x 8192 rows, N = K = 8192, bf16 out (compute-bound; not the layer's shape)"}
+        # timed alone: the burst bf16 figure x the nominal ratios (FP4 6x, FP8 2x)
+        pk = {"nvfp4": peaks["bf16"] * 6.0, "mxfp8": peaks["bf16"] * 2.0}
+        for kind, name in ((0, "nvfp4"), (1, "mxfp8")):
+            pm, pt = compute_probe(kind)
+            probe[name] = {"ms": round(pm, 4), "TFLOP/s": round(pt, 1), "frac_of_derived_peak": round(pt / pk[name], 3)}
+        probe["derived_peaks_TFLOPs"] = {k: round(v, 1) for k, v in pk.items()}
+        probe["peak_source"] = peaks["src"] + " bf16 burst x nominal ratio"
+        nxt["gemm_compute_probe"] = probe
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

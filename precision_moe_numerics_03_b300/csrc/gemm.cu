@@ -70,8 +70,12 @@ constexpr int SGD_LA = 1;                     // load lookahead, chunks
 static_assert(SGD_LA <= SGD_NB - 2, "a refilled buffer's store must be allowed to still be pending");
 constexpr int EPI_WARP_BYTES = SGD_NB * (SGD_W_CHUNK + SGD_B_CHUNK);
 constexpr int EPI_SGD_BYTES = 8 * EPI_WARP_BYTES;
-// TMA-store epilogue: one 32x32 binary32 tile per epilogue warp
-constexpr int EPI_W_TILE = 32 * 32 * 4;
+// TMA-store epilogue: one staged chunk of 32 rows per epilogue warp, TMA_CW columns wide (32 for
+// NVFP4; 16 for MXFP8, whose smaller staging leaves room for a fourth operand stage)
+template <int KIND>
+constexpr int TMA_CW = KIND == 0 ? 32 : 16;
+template <int KIND>
+constexpr int EPI_W_TILE = 32 * TMA_CW<KIND> * 4;
 // Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
 // TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
@@ -81,15 +85,20 @@ enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3 };
 constexpr int HMX_PITCH = 128 * 2 + 16;
 constexpr int HMX_WARP_BYTES = 32 * HMX_PITCH;
 constexpr int EPI_HMX_BYTES = 8 * HMX_WARP_BYTES;
-constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE;
+template <int KIND>
+constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE<KIND>;
 template <int EM>
 struct EpiCfg {
     // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
     // tile's MMAs overlap the previous tile's master-weight traffic
     static constexpr int BNT = EM == EPI_SGD ? 128 : BN;
     static constexpr int NST = EM == EPI_SGD ? 4 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
-    static constexpr int BYTES =
-        EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
+    // operand stages for a given operand kind: the MXFP8 TMA-store mode fits a fourth one
+    template <int KIND>
+    static constexpr int NSTK = (EM == EPI_TMA && KIND == 1) ? 4 : NST;
+    template <int KIND>
+    static constexpr int BYTESK =
+        EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
 };
 
 template <int KIND, int NST, int EPI, int BNT>
@@ -345,9 +354,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWb, const Args p) {
     // tmW: the output D (EPI_TMA) or the master weights (EPI_SGD); tmWb: their bf16 copy (EPI_SGD)
     constexpr bool kSgd = EM == EPI_SGD;
-    constexpr int NST = EpiCfg<EM>::NST;
+    constexpr int NST = EpiCfg<EM>::template NSTK<KIND>;
     constexpr int BNT = EpiCfg<EM>::BNT;
-    using L = Layout<KIND, NST, EpiCfg<EM>::BYTES, BNT>;
+    using L = Layout<KIND, NST, EpiCfg<EM>::template BYTESK<KIND>, BNT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -668,49 +677,55 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();  // the staging rows are rewritten by this warp's next tile
             } else if constexpr (EM == EPI_TMA) {
-                // each 32-column chunk: registers -> swizzled 32x32 staging tile -> TMA bulk store
-                // (binary32 rows of 128 bytes with the 128-byte swizzle, bf16 rows of 64 bytes with
-                // the 64-byte swizzle; piece j of row l sits at j ^ (l & 7) or j ^ ((l >> 1) & 3))
-                uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE;
+                // each CW-column chunk: registers -> swizzled 32 x CW staging tile -> TMA bulk store.
+                // A staged row is CW * 4 (binary32) or CW * 2 (bf16) bytes with the swizzle of that
+                // width: with P 16-byte pieces per row, piece j of row l sits at
+                // j ^ ((l >> (3 - log2 P)) & (P - 1))
+                constexpr int CW = TMA_CW<KIND>;
+                constexpr int PF = CW / 4, PB = CW / 8;            // pieces per binary32 / bf16 row
+                constexpr int SF = PF == 8 ? 0 : (PF == 4 ? 1 : 2);  // 3 - log2(PF)
+                constexpr int SB = PB == 8 ? 0 : (PB == 4 ? 1 : 2);
+                uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE<KIND>;
                 const int y0 = (int)((p.group_k ? (int64_t)tl.e * p.M : 0) + tl.m0 + q * 32);
                 const int x0 = (int)(tl.n0 + half * (BNT / 2));
-                for (int c = 0; c < BNT / 64; ++c) {
-                    uint32_t r[32];
+                for (int c = 0; c < (BNT / 2) / CW; ++c) {
+                    uint32_t r[CW];
                     if (live) {
-                        tc_ld32(tbase + (uint32_t)(c * 32), r);
+                        if constexpr (CW == 32) tc_ld32(tbase + (uint32_t)(c * CW), r);
+                        else tc_ld16(tbase + (uint32_t)(c * CW), r);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = 0;
+                        for (int i = 0; i < CW; ++i) r[i] = 0;
                     }
-                    float v[32];
+                    float v[CW];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < CW; ++i)
                         v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
                     if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile out
                     __syncwarp();
                     if (p.mode == BF16) {
-                        uint8_t *row = stage + lane * 64;
+                        uint8_t *row = stage + lane * (CW * 2);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
+                        for (int j = 0; j < PB; ++j) {
                             uint32_t w[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
                                 w[i] = (uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i]) |
                                        ((uint32_t)f32_to_bf16_bits(v[8 * j + 2 * i + 1]) << 16);
-                            *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> SB) & (PB - 1))) << 4)) =
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     } else {
-                        uint8_t *row = stage + lane * 128;
+                        uint8_t *row = stage + lane * (CW * 4);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<float4 *>(row + ((j ^ (lane & 7)) << 4)) =
+                        for (int j = 0; j < PF; ++j)
+                            *reinterpret_cast<float4 *>(row + ((j ^ ((lane >> SF) & (PF - 1))) << 4)) =
                                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmW, stage, x0 + 32 * c, y0);
+                        tma_store_2d(&tmW, stage, x0 + CW * c, y0);
                         bulk_commit();
                     }
                 }
@@ -827,7 +842,7 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t inner_bytes, int6
 template <int KIND, int EM>
 static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tw, const CUtensorMap &twb,
                   const Args &a, cudaStream_t st) {
-    using L = Layout<KIND, EpiCfg<EM>::NST, EpiCfg<EM>::BYTES, EpiCfg<EM>::BNT>;
+    using L = Layout<KIND, EpiCfg<EM>::template NSTK<KIND>, EpiCfg<EM>::template BYTESK<KIND>, EpiCfg<EM>::BNT>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, EM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -841,11 +856,15 @@ static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMa
     return launch_status();
 }
 
-// The output D as [rows, N] for the TMA-store epilogue: 32x32 boxes, binary32 (128-byte swizzle)
-// or bf16 (64-byte swizzle).
-static bool make_out_map(CUtensorMap *m, void *d, bool bf16, int64_t rows, int64_t N) {
-    return bf16 ? make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, d, N, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
-                : make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+// The output D as [rows, N] for the TMA-store epilogue: cw-column x 32-row boxes (cw 32 or 16) with
+// the swizzle of the staged row's width.
+static CUtensorMapSwizzle swizzle_for(int row_bytes) {
+    return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                            : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+static bool make_out_map(CUtensorMap *m, void *d, bool bf16, int64_t rows, int64_t N, int cw) {
+    return bf16 ? make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, d, N, rows, cw, 32, swizzle_for(cw * 2))
+                : make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, rows, cw, 32, swizzle_for(cw * 4));
 }
 
 }  // namespace gemm
@@ -937,7 +956,7 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     a.sfa_tile_stride = K / 64;
     a.sfb_tile_stride = K / 64;
     CUtensorMap td;
-    if (!make_out_map(&td, d, bf16, rows_total, N)) return MOE4_ERR_CUDA;
+    if (!make_out_map(&td, d, bf16, rows_total, N, TMA_CW<0>)) return MOE4_ERR_CUDA;
     return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
 }
 
@@ -1037,7 +1056,7 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     g.sfb_tile_stride = K / 128;
     if (g.mode == ACC_F32) return launch<1, EPI_REG>(ta, tb, ta, tb, g, st);
     CUtensorMap td;
-    if (!make_out_map(&td, d, bf16, gk ? E * M : M, N)) return MOE4_ERR_CUDA;
+    if (!make_out_map(&td, d, bf16, gk ? E * M : M, N, TMA_CW<1>)) return MOE4_ERR_CUDA;
     return launch<1, EPI_TMA>(ta, tb, td, td, g, st);
 }
 
