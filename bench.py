@@ -119,7 +119,6 @@ class LayerStep:
         self.Yhat = torch.empty((R, d), dtype=torch.int16, device=dev)
         self.y = torch.empty((T, d), dtype=torch.int16, device=dev)
         # backward tensors
-        self.dYp = torch.empty((R, d), dtype=torch.int16, device=dev)
         self.dYr_q, self.dYr_e = torch.empty((R, d), **u8), torch.empty((R, d // 32), **u8)
         self.dYc_q, self.dYc_e = torch.empty(d * R, **u8), torch.empty(d * R // 32, **u8)
         self.WdT_q, self.WdT_e = torch.empty((E, f, d), **u8), torch.empty((E, f, d // 32), **u8)
@@ -192,10 +191,10 @@ class LayerStep:
             m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, y)
         n += 1
         # ---------------- backward
-        with tm("mxfp8_quant"):
-            m.moe4_combine_backward(dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYp[:Rp])
-            m.mxfp8_quantize_rowcol(self.dYp[:Rp], Rp, d, self.dYr_q, self.dYr_e, self.dYc_q, self.dYc_e)
-        n += 2
+        with tm("mxfp8_quant"):  # combine gradient straight into both MXFP8 layouts of dY
+            m.moe4_combine_backward_mxfp8(dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYr_q, self.dYr_e,
+                                          self.dYc_q, self.dYc_e)
+        n += 1
         with tm("requant"):
             m.mxfp8_requant_transpose_sr(self.Wd_c, self.Wd_s, self.Wd_g, E, d, f, self.WdT_q, self.WdT_e, seed, 1,
                                          m.SR | MMA)
@@ -248,8 +247,9 @@ class LayerStep:
         b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
                            rows * f * nv + live * d * f * nv + rows * d * 2)
         b["requant"] = (w_gu + w_d + rows * (f + d)) * (nv + mx)
-        # combine backward (read dy, write dYp) + one read of dYp and dGU for both MXFP8 layouts
-        b["mxfp8_quant"] = rows * d * (2 + 2 + 2 * mx) + T * d * 2 + rows * 2 * f * (2 + 2 * mx)
+        # combine gradient formed from dy (read once) straight into both MXFP8 layouts of dY, and one
+        # read of dGU for its two layouts
+        b["mxfp8_quant"] = rows * d * 2 * mx + T * d * 2 + rows * 2 * f * (2 + 2 * mx)
         b["gemm_mxfp8_dgrad"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +          # down
                                  rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2)   # gate/up
         # wgrad operands + the SGD epilogue: read W32, write W32 and the bf16 copy

@@ -300,6 +300,16 @@ int moe4_combine_backward(const uint16_t *dy, const int32_t *row_of, const float
                           const int32_t *src_of, int64_t T, int64_t k, int64_t d,
                           int64_t rows_total, uint16_t *dyhat, void *stream);
 
+/* moe4_combine_backward_mxfp8: the combine's gradient fused with its MXFP8 quantisation for the
+ * backward GEMMs [LHC backward pass: MXFP8 operands]: the bf16 dyhat of moe4_combine_backward
+ * (same arithmetic, same bits) is never written; its row-wise MXFP8 q_row [rows_total, d],
+ * e8_row [rows_total, d/32] and transposed MXFP8 q_col [d, rows_total], e8_col [d, rows_total/32]
+ * are, byte for byte as mxfp8_quantize_rowcol of that dyhat would give them (nearest-even).
+ * d % 32 == 0, rows_total % 32 == 0; dy, q_row, q_col 16-byte aligned; flags 0. */
+int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *row_of, const float *w, const int32_t *src_of,
+                                int64_t T, int64_t k, int64_t d, int64_t rows_total, uint8_t *q_row,
+                                uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags, void *stream);
+
 /* moe4_combine: y bf16 [T, d], y[t] = sum over slots j in order of w[t,j] * yhat[row_of[t,j]]:
  * one binary32 product and one binary32 add per slot from 0, then nearest-even to bf16.
  * yhat bf16 [rows, d]; d % 8 == 0. */

@@ -22,7 +22,9 @@ constexpr int kTileC = 64;
 // dGU [R, 2f] (gate columns, then up columns) formed from the binary32 GU and dH and rounded to
 // bf16 exactly as moe4_swiglu_backward does; its tiles pair 32 gate columns with the same 32 up
 // columns, so each GU and dH value is read once.
-enum class SrcKind { Nvfp4, Bf16, SwigluBwd };
+// CombineBwd: the combine's gradient dYhat [R, C] formed on the fly, dispatched row r = token t's
+// slot j: bf16(w[t, j] * dy[t]) as moe4_combine_backward computes it (padding rows zero).
+enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 
 // Output of half a warp: 128 values of output row c (input column c) of this tile.  Lane
 // sub = lane % 16 owns values 8*sub .. 8*sub + 7; lanes 4b .. 4b+3 of the half form 32-block b
@@ -86,12 +88,14 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
 constexpr int kPitch16 = kTileR + 8;
 
 template <SrcKind kind, bool kSR, bool kRow = false>
-__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 : 5) requant_transpose_kernel(
+__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd || kind == SrcKind::CombineBwd) ? 4 : 5)
+requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
     uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
     uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr, const float *__restrict__ gu = nullptr,
-    const float *__restrict__ dh = nullptr) {
+    const float *__restrict__ dh = nullptr, const int32_t *__restrict__ src_of = nullptr,
+    const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
     __shared__ __align__(16) uint16_t tile[kTileC][kPitch16];
     const int64_t f = C / 2;  // SwigluBwd: C = 2f
@@ -156,6 +160,31 @@ __global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 :
                         tile[half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(dgv);
                         tile[32 + half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(duv);
                     }
+                }
+            } else if constexpr (kind == SrcKind::CombineBwd) {
+                const int32_t tok = __ldg(src_of + r);
+                float wj = 0.0f;
+                if (tok >= 0)
+                    for (int j = 0; j < topk; ++j)
+                        if (__ldg(row_of + (int64_t)tok * topk + j) == (int32_t)r) wj = __ldg(wts + (int64_t)tok * topk + j);
+                const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (int64_t)(tok < 0 ? 0 : tok) * C + c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = tok >= 0 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        h[4 * q + i] = (uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_lo(ws[i]))) |
+                                       ((uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_hi(ws[i]))) << 16);
+                }
+                if constexpr (kRow) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[2 * i] = bf16_lo(h[i]);
+                        v[2 * i + 1] = bf16_hi(h[i]);
+                    }
+                    emit_rowwise32(v, r, c, C, q_r, e8_r);
                 }
             } else {
                 const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (m * R + r) * C + c);
@@ -356,5 +385,22 @@ extern "C" int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int6
     requant_transpose_kernel<SrcKind::SwigluBwd, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, nullptr, 1, rows, 2 * f, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, gu,
         dh);
+    return launch_status();
+}
+
+extern "C" int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *row_of, const float *w,
+                                           const int32_t *src_of, int64_t T, int64_t k, int64_t d, int64_t rows_total,
+                                           uint8_t *q_row, uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col,
+                                           uint32_t flags, void *stream) {
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 32 == 0 && rows_total >= 0 && rows_total % 32 == 0);
+    MOE4_CHECK_ARG(flags == 0 && src_of && q_row && e8_row && q_col && e8_col);
+    MOE4_CHECK_ARG(T == 0 || (dy && row_of && w && aligned16(dy)));
+    MOE4_CHECK_ARG(aligned16(q_row) && aligned16(q_col));
+    const int64_t tiles = ((rows_total + kTileR - 1) / kTileR) * ((d + kTileC - 1) / kTileC);
+    if (tiles == 0) return MOE4_OK;
+    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
+    requant_transpose_kernel<SrcKind::CombineBwd, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+        nullptr, nullptr, nullptr, dy, 1, rows_total, d, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row,
+        nullptr, nullptr, src_of, row_of, w, (int)k);
     return launch_status();
 }

@@ -68,6 +68,8 @@ _SIGNATURES = {
     "moe4_swiglu_backward": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "moe4_swiglu_backward_mxfp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "moe4_combine_backward": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "moe4_combine_backward_mxfp8": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32,
+                                           _vp]),
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_sgd_update": (_int, [_vp, _vp, _i64, _f32, _vp, _vp]),
@@ -254,6 +256,12 @@ def moe4_combine_backward(dy, row_of, w, src_of, T, k, d, rows_total, dyhat, str
 
 def moe4_swiglu(gu, rows, f, h, stream=None):
     _call("moe4_swiglu", _p(gu), rows, f, _p(h), _s(stream))
+
+
+def moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, rows_total, q_row, e8_row, q_col, e8_col, flags=0,
+                                stream=None):
+    _call("moe4_combine_backward_mxfp8", _p(dy), _p(row_of), _p(w), _p(src_of), T, k, d, rows_total, _p(q_row),
+          _p(e8_row), _p(q_col), _p(e8_col), flags, _s(stream))
 
 
 def moe4_combine(yhat, row_of, w, T, k, d, y, stream=None):

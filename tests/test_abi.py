@@ -70,6 +70,9 @@ MISALIGNED = FAKE + 4
     ("moe4_swiglu_backward_mxfp8", (FAKE, FAKE, 48, 64, FAKE, FAKE, FAKE, FAKE, 0, None)),        # rows % 32
     ("moe4_swiglu_backward_mxfp8", (FAKE, FAKE, 32, 48, FAKE, FAKE, FAKE, FAKE, 0, None)),        # f % 32
     ("moe4_swiglu_backward_mxfp8", (FAKE, MISALIGNED, 32, 64, FAKE, FAKE, FAKE, FAKE, 0, None)),  # dh alignment
+    ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 8, 48, 128, FAKE, FAKE, FAKE, FAKE, 0, None)),  # d % 32
+    ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 40, 64, 128, FAKE, FAKE, FAKE, FAKE, 0, None)),  # k > 32
+    ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 100, FAKE, FAKE, FAKE, FAKE, 0, None)),  # rows % 32
     ("hadamard_quant", (FAKE, 4, 64, FAKE, FAKE, FAKE, 1, FAKE, 4, None)),                   # cols % 128
     ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 200, 256, FAKE,
                                                FAKE, 0, None, 0, None)),                      # N % 256

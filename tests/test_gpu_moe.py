@@ -175,6 +175,33 @@ def test_swiglu_backward_mxfp8_against_oracle():
     assert np.mean(to_np(out[2]) == rq) >= 0.9  # the transposed layout: structure (same blocks)
 
 
+@pytest.mark.parametrize("T,E,k,d", [(300, 16, 4, 96), (4096, 8, 2, 2048), (16384, 384, 8, 4096)])
+def test_combine_backward_mxfp8_equals_unfused(T, E, k, d):
+    """Fused combine gradient + MXFP8 (both layouts) equals moe4_combine_backward followed by
+    mxfp8_quantize_rowcol, byte for byte; the last case is the 384-expert layer's dY."""
+    lg = _logits(T, E, E > 8, 11 * T + E)
+    ridx, rw = oracle.route_topk(lg, k)
+    rows_cap = T * k + 127 * E
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    src_of = torch.empty(rows_cap, dtype=torch.int32, device=DEV)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E))
+    moe4.moe4_permute_plan(to_dev(ridx), T, k, E, offs, row_of, src_of, rows_cap, ws)
+    torch.cuda.synchronize()
+    R = int(to_np(offs)[-1])
+    dy = inputs.device_normal((T, d), 1.0, inputs.device_generator(12, T, DEV), DEV).view(torch.int16)
+    w = to_dev(rw)
+    out = [empty_u8(R, d), empty_u8(R, d // 32), empty_u8(d, R), empty_u8(d, R // 32)]
+    moe4.moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, R, *out)
+    dyhat = torch.empty((R, d), dtype=torch.int16, device=DEV)
+    moe4.moe4_combine_backward(dy, row_of, w, src_of, T, k, d, R, dyhat)
+    ref = [empty_u8(R, d), empty_u8(R, d // 32), empty_u8(d, R), empty_u8(d, R // 32)]
+    moe4.mxfp8_quantize_rowcol(dyhat, R, d, *ref)
+    torch.cuda.synchronize()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (300, 16, 4)])
 def test_combine_backward_bit_exact(T, E, k):
     lg = _logits(T, E, True, 3 * T + E)
