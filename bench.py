@@ -541,14 +541,25 @@ def cpu_cores_used():
 
 
 # ---------------------------------------------------------------------------------------------
+def max_over_ranks(x, dist):
+    """The largest of a float over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
+    dims = dict(d=SMALL["d"], f=SMALL["f"]) if args.small else {}
     flops, secs = 0, 0.0
     for i in range(args.warmup):
-        oracle_sample_step(seed=i)
+        oracle_sample_step(seed=i, **dims)
     for i in range(args.steps):
-        fl, s = oracle_sample_step(seed=100 + i)
+        fl, s = oracle_sample_step(seed=100 + i, **dims)
         flops += fl
         secs += s
     value = flops / secs / 1e12
@@ -740,10 +751,7 @@ def main():
     elapsed_ms = t_start.elapsed_time(t_end)
     if moe4.moe4_get_status() != moe4.OK:
         raise RuntimeError("a device wait timed out in the timed region")
-    if dist is not None:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist)
     ms = elapsed_ms / args.steps
     fwd_flops, bwd_flops = step.gemm_flops()
     step_flops = fwd_flops + bwd_flops
@@ -832,10 +840,7 @@ def main():
                 hY[b].copy_(io[b][3], non_blocking=True)
         torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
-        if dist is not None:
-            tt = torch.tensor([e2e_s], dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
+        e2e_s = max_over_ranks(e2e_s, dist)
         h2d = hX.numel() * 2 + hL.numel() * 4 + hD.numel() * 2
         d2h = hY[0].numel() * 2 + 4
         e2e = {"value": world * step_flops * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
