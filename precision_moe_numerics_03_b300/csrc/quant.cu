@@ -200,12 +200,11 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
         const uint4 *src = reinterpret_cast<const uint4 *>(srcp);
         const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
         const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // packed products: y feeds the amax, a product and the addend of an FMA, never an add
         float y[16];
+        const uint64_t g2 = f2_pack(g_enc, g_enc);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            y[2 * i] = __fmul_rn(bf16_lo(wv[i]), g_enc);
-            y[2 * i + 1] = __fmul_rn(bf16_hi(wv[i]), g_enc);
-        }
+        for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(bf16_lo(wv[i]), bf16_hi(wv[i])), g2), y[2 * i], y[2 * i + 1]);
         uint32_t w0, w1, scode;
         nvfp4_block(y, four_over_six, tab, w0, w1, scode);
         *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
@@ -328,7 +327,7 @@ __global__ void __launch_bounds__(256) hadamard_quant_kernel(const uint16_t *__r
         }
         fwht128_sub16(u);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], gs.enc);
+        for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(u[2 * i], u[2 * i + 1]), f2_pack(gs.enc, gs.enc)), u[2 * i], u[2 * i + 1]);
         uint32_t w0, w1, scode;
         nvfp4_block(u, four_over_six, tab, w0, w1, scode);
         if (live) {
