@@ -208,7 +208,7 @@ class LayerStep:
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp,
                                            self.W32_d, self.Wb_d, LR, self.amax_d, 0, self.gws)
-        n += 3
+        n += 4  # two scale-layout passes, the expert ranking for the tile schedule, the GEMM
         with tm("swiglu_bwd"):
             m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
         n += 1
@@ -228,7 +228,7 @@ class LayerStep:
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d,
                                            Rp, self.W32_gu, self.Wb_gu, LR, self.amax_gu, 0, self.gws)
-        n += 3
+        n += 4
         self.launches += n
         return n
 
