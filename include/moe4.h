@@ -90,6 +90,13 @@ size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, int64_t b_r
  * bounded wait gives up.  Returns MOE4_OK or MOE4_ERR_TIMEOUT (or MOE4_ERR_CUDA). */
 int moe4_get_status(void *stream);
 
+/* moe4_selftest_wait: runs, on `stream`, one wait that nothing completes, through the same
+ * bounded-wait path as the GEMM kernels: it gives up after limit_cycles SM clock cycles
+ * (1 <= limit_cycles <= 2^32) and records the timeout, so that moe4_get_status then returns
+ * MOE4_ERR_TIMEOUT once and the context stays usable.  A check of the failure path without a
+ * fault; the pages have no counterpart. */
+int moe4_selftest_wait(int64_t limit_cycles, void *stream);
+
 /* ------------------------------------------------------------------ NVFP4 [LHC fewer bits; DEBUT]
  * nvfp4_quantize: x bf16 [nmat, rows, ld] (the first `cols` of each row are used; ld >= cols,
  * ld % 8 == 0).  For each matrix m: amax_m = max|x| (or amax_in[m] with MOE4_AMAX_GIVEN);

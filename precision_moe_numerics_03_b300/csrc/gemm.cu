@@ -181,7 +181,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait: false when the CTA is aborting or the wait ran out (which starts the abort).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+// Waits for the phase of `parity` to complete, at most `limit` SM clock cycles; on expiry it
+// raises the CTA's abort flag and the library status word (reported by moe4_get_status).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          long long limit = kWaitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const long long t0 = clock64();
@@ -190,7 +193,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(a, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(&g_status, 1u);
             return false;
@@ -867,6 +870,20 @@ static bool make_out_map(CUtensorMap *m, void *d, bool bf16, int64_t rows, int64
                 : make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, rows, cw, 32, swizzle_for(cw * 4));
 }
 
+// A wait that nothing completes, through the GEMMs' bounded-wait path: phase 0 of a fresh
+// mbarrier with no arrivals.  It gives up after `limit` cycles and records the timeout.
+__global__ void wait_selftest_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, limit);
+}
+
 }  // namespace gemm
 }  // namespace moe4
 
@@ -881,7 +898,6 @@ extern "C" int moe4_get_status(void *stream) {
     return v ? MOE4_ERR_TIMEOUT : MOE4_OK;
 }
 
-// Canonical scales -> tensor-core layout into ws when the caller did not pass that layout.
 // order[rank] = expert, ranks by decreasing group size (ties: lower expert first).  One CTA.
 __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t *__restrict__ offs, int E,
                                                             int32_t *__restrict__ order) {
@@ -896,6 +912,7 @@ __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t *__res
     }
 }
 
+// Canonical scales -> tensor-core layout into ws when the caller did not pass that layout.
 static int stage_scales(const uint8_t *a_sf, int64_t a_rows, const uint8_t *b_sf, int64_t b_rows, int64_t K, int blk,
                         uint32_t flags, void *ws, size_t ws_bytes, const uint8_t **sfa, const uint8_t **sfb,
                         cudaStream_t st) {
@@ -1119,4 +1136,10 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
         !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return MOE4_ERR_CUDA;
     return launch<1, EPI_SGD>(ta, tb, tw, twb, g, st);
+}
+
+extern "C" int moe4_selftest_wait(int64_t limit_cycles, void *stream) {
+    MOE4_CHECK_ARG(limit_cycles > 0 && limit_cycles <= (int64_t(1) << 32));
+    wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>((long long)limit_cycles);
+    return launch_status();
 }

@@ -46,6 +46,7 @@ _SIGNATURES = {
     "moe4_workspace_size": (_sz, [_int, _i64, _i64, _i64]),
     "moe4_workspace_size_gemm": (_sz, [_int, _i64, _i64, _i64, _i64]),
     "moe4_get_status": (_int, [_vp]),
+    "moe4_selftest_wait": (_int, [_i64, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
@@ -148,6 +149,10 @@ def moe4_workspace_size_gemm(kind: int, a_rows: int, E: int, b_rows: int, K: int
 
 def moe4_get_status(stream=None) -> int:
     return load().moe4_get_status(_s(stream))
+
+
+def moe4_selftest_wait(limit_cycles, stream=None):
+    _call("moe4_selftest_wait", limit_cycles, _s(stream))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
