@@ -146,7 +146,8 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec
  * word < floor(frac * 2^32), frac being its distance above the E4M3 value below, in units of
  * the gap.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
  * rows % 32 == 0, cols % 32 == 0.  Input scales canonical, or in the tensor-core tile layout with
- * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0). */
+ * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0).  nmat and cols / 64 at most 65535 (one
+ * thread block per 128 x 64 tile on a three-dimensional grid); beyond that MOE4_ERR_ARG. */
 int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const float *g_dec,
                                int64_t nmat, int64_t rows, int64_t cols, uint8_t *q_t,
                                uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,

@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(256) convert_kernel(int kind, const float *__r
             reinterpret_cast<uint2 *>(out)[q] = make_uint2(lo, hi);
         } else {
             // the kernels' four-at-a-time rounding (integer fast path, per-element path otherwise)
-            reinterpret_cast<uint32_t *>(out)[q] = e4m3x4_sr(v.x, v.y, v.z, v.w, sr_words4((uint64_t)q, 0u, keys));
+            reinterpret_cast<uint32_t *>(out)[q] =
+                e4m3x4_sr_nw(v.x, v.y, v.z, v.w, sr_words4_not((uint64_t)q, 0u, keys));
         }
     }
 }

@@ -122,10 +122,11 @@ static inline PhiloxKeys philox_keys(uint64_t seed) {
     return k;
 }
 
-__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 const PhiloxKeys K) {
+template <int NR>
+__device__ __forceinline__ void philox_rounds(uint32_t &c0, uint32_t &c1, uint32_t &c2, uint32_t &c3,
+                                              const PhiloxKeys &K) {
 #pragma unroll
-    for (int r = 0; r < 10; ++r) {
+    for (int r = 0; r < NR; ++r) {
         // high and low halves as two multiplies (measured cheaper on this GPU than one 64-bit
         // product: ~96 versus ~122 issue slots per call)
         const uint32_t hi0 = __umulhi(c0, 0xD2511F53u), lo0 = c0 * 0xD2511F53u;
@@ -137,12 +138,35 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
         c0 = n0;
         c2 = n2;
     }
+}
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 const PhiloxKeys K) {
+    philox_rounds<10>(c0, c1, c2, c3, K);
     return {c0, c1, c2, c3};
+}
+
+// The same generator returning the complement of each word.  The last round's XORs absorb the
+// complement, and ~(c * M) = c * (2^32 - M) + (2^32 - 1) is one multiply-add, so the complemented
+// words cost nothing extra; the rounding below works on ~r.
+__device__ __forceinline__ Philox4 philox4x32_10_not(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                     const PhiloxKeys K) {
+    philox_rounds<9>(c0, c1, c2, c3, K);
+    const uint32_t hi0 = __umulhi(c0, 0xD2511F53u), hi1 = __umulhi(c2, 0xCD9E8D57u);
+    return {~(hi1 ^ c1 ^ K.k0[9]), c2 * 0x326172A9u + 0xFFFFFFFFu, ~(hi0 ^ c3 ^ K.k1[9]),
+            c0 * 0x2DAEE0ADu + 0xFFFFFFFFu};
 }
 
 // The four stochastic-rounding words of output indices 4j .. 4j+3.
 __device__ __forceinline__ Philox4 sr_words4(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
     return philox4x32_10((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, K);
+}
+// Their complements; the 32-bit form is for tensors of at most 2^34 values (counter word 1 zero).
+__device__ __forceinline__ Philox4 sr_words4_not(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
+    return philox4x32_10_not((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, K);
+}
+__device__ __forceinline__ Philox4 sr_words4_not32(uint32_t j, uint32_t stream_id, const PhiloxKeys K) {
+    return philox4x32_10_not(j, 0u, stream_id, 0u, K);
 }
 
 // ------------------------------------------------------------------ MXFP8 scale and rounding
@@ -155,6 +179,15 @@ __device__ __forceinline__ int mx_scale_exponent(float a) {
     const int e = p - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
     return e < -127 ? -127 : e;
 }
+
+// The same scale as one biased field fs = e + 135, clamped below at 8 (e >= -127), for finite
+// a >= 0: adding 0x1FFFFF to the bits carries into the exponent exactly when the mantissa field
+// exceeds 0x600000 (a > 1.75 * 2^p, i.e. a > 448 * 2^(p-8)), and zero or subnormal a gives a
+// field below 8.  Scale code e + 127 = fs - 8; 2^-e = (262 - fs) << 23.
+__device__ __forceinline__ uint32_t mx_scale_fs(float a) {
+    return max((__float_as_uint(a) + 0x1FFFFFu) >> 23, 8u);
+}
+__device__ __forceinline__ float mx_inv_scale_fs(uint32_t fs) { return __uint_as_float((262u - fs) << 23); }
 
 // 2^-e as binary32 for e in [-127, 126].
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
@@ -203,6 +236,59 @@ __device__ __forceinline__ uint32_t e4m3x4_sr(float v0, float v1, float v2, floa
     }
     return e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
 }
+// bits + ((~r) >> 12) as one high multiply-add: hi32(~r * 2^20) + bits.
+__device__ __forceinline__ uint32_t sr_carry(uint32_t bits, uint32_t nr) {
+    uint32_t t;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(t) : "r"(nr), "r"(1u << 20), "r"(bits));
+    return t & 0xFFF00000u;
+}
+// The fast-path test of e4m3x4_sr for four values: 2*bits - 2 (mod 2^32) drops the sign and sends
+// +-0 to the top, so the minimum is >= 2*0x3C800000 - 2 iff each value is zero or at least 2^-6 in
+// magnitude.
+constexpr uint32_t kSrFastMin = 0x78FFFFFEu;
+__device__ __forceinline__ uint32_t sr_fast_key4(float v0, float v1, float v2, float v3) {
+    return min(min(__float_as_uint(v0) * 2u - 2u, __float_as_uint(v1) * 2u - 2u),
+               min(__float_as_uint(v2) * 2u - 2u, __float_as_uint(v3) * 2u - 2u));
+}
+// The integer-carry rounding of four values that passed that test, with complemented words ~r.
+__device__ __forceinline__ uint32_t e4m3x4_sr_fast(float v0, float v1, float v2, float v3, const Philox4 nw) {
+    return e4m3x4_rn(__uint_as_float(sr_carry(__float_as_uint(v0), nw.x)),
+                     __uint_as_float(sr_carry(__float_as_uint(v1), nw.y)),
+                     __uint_as_float(sr_carry(__float_as_uint(v2), nw.z)),
+                     __uint_as_float(sr_carry(__float_as_uint(v3), nw.w)));
+}
+// e4m3x4_sr with the complemented words ~r (sr_words4_not).
+__device__ __forceinline__ uint32_t e4m3x4_sr_nw(float v0, float v1, float v2, float v3, const Philox4 nw) {
+    if (sr_fast_key4(v0, v1, v2, v3) >= kSrFastMin) return e4m3x4_sr_fast(v0, v1, v2, v3, nw);
+    return e4m3_sr(v0, ~nw.x) | (e4m3_sr(v1, ~nw.y) << 8) | (e4m3_sr(v2, ~nw.z) << 16) | (e4m3_sr(v3, ~nw.w) << 24);
+}
+
+// max(|a|, |b|) per 16-bit half (f16 or bf16); the sign bit of each half is the XOR of the
+// inputs' signs, so the caller takes the magnitude of the final result.
+template <bool kF16>
+__device__ __forceinline__ uint32_t max_abs16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    if constexpr (kF16)
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Four E2M1 code pairs (a word) -> four f16x2 (exact).
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t h[4]) {
+    asm("{\n"
+        ".reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+        "}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
 // ------------------------------------------------------------------ packed binary32 pairs
 // mul/add/sub.rn.f32x2: two IEEE round-to-nearest operations in one instruction.  The compiler may
 // fuse a packed multiply and a following packed add or subtract into one multiply-add (observed:

@@ -7,10 +7,10 @@
 // with probability given by the distance so that the value is kept on average.
 //
 // Tile: 128 input rows (the output's contiguous dimension) x 64 input columns.  Phase 1: each
-// thread reads one row's 32 codes (16 bytes) and two scale bytes, dequantises them to binary32
-// and stores them transposed in shared memory (row pitch 132 floats: conflict-free both ways).
-// Phase 2: each warp emits one output row segment of 128 values: lane l owns 4 consecutive values
-// (one Philox call gives their 4 words), 8 lanes form one 32-block (amax by 3 shuffles).
+// thread reads one row's 32 values (16 code bytes and two scale bytes, or 64 bytes of bf16) and
+// stores them as 16 column pairs, one 32-bit word each, in the transposed shared tile.  Phase 2:
+// each warp emits two output rows (one column pair) of 128 values: lane l owns 4 consecutive
+// values of each (one Philox call gives their 4 words), 8 lanes form one 32-block.
 #include "common.cuh"
 
 namespace moe4 {
@@ -26,38 +26,82 @@ constexpr int kTileC = 64;
 // slot j: bf16(w[t, j] * dy[t]) as moe4_combine_backward computes it (padding rows zero).
 enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 
-// Output of half a warp: 128 values of output row c (input column c) of this tile.  Lane
-// sub = lane % 16 owns values 8*sub .. 8*sub + 7; lanes 4b .. 4b+3 of the half form 32-block b
-// (amax by two shuffles).  Every lane takes part in the shuffles; `live` only guards the stores.
-template <bool kSR>
-__device__ __forceinline__ void emit8(const float x[8], bool live, int64_t m, int64_t c, int64_t r0, int64_t R,
-                                      int64_t C, uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
-                                      const PhiloxKeys keys, uint32_t stream_id) {
-    const int sub = lane_id() & 15;
-    float a = fmaxf(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))),
-                    fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-    const int e = mx_scale_exponent(a);
-    const float s = pow2_neg(e);
-    const uint64_t s2 = f2_pack(s, s);
-    float v[8];
+// Output of one warp: 128 values of each of the output rows cA and cA + 1 (the input columns of
+// one pair-row of the tile, word p = {column cA, column cA + 1} as 16-bit halves).  Lane l owns
+// input rows 4l .. 4l+3 of both; lanes 8b .. 8b+7 form 32-block b, whose amax is taken on the
+// packed 16-bit pairs (the binary32 values are monotone in them: an NVFP4 source is scaled by
+// g > 0 with one rounding, a bf16 source converts exactly).  Every lane takes part in the
+// shuffles; `live` only guards the stores.
+template <SrcKind kind, bool kSR, bool kJ32>
+__device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int64_t m, int64_t cA, int64_t r0,
+                                          int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
+                                          const PhiloxKeys keys, uint32_t stream_id) {
+    constexpr bool kF16 = kind == SrcKind::Nvfp4;
+    const int lane = lane_id();
+    uint32_t mx = max_abs16x2<kF16>(max_abs16x2<kF16>(p.x, p.y), max_abs16x2<kF16>(p.z, p.w));
+    mx = max_abs16x2<kF16>(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+    mx = max_abs16x2<kF16>(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+    mx = max_abs16x2<kF16>(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+    float xa[4], xb[4], aA, aB;
+    if constexpr (kF16) {
+        const float2 am = h2_bits_to_f2(mx);
+        aA = __fmul_rn(fabsf(am.x), g);
+        aB = __fmul_rn(fabsf(am.y), g);
+        const uint64_t g2 = f2_pack(g, g);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), s2), v[2 * i], v[2 * i + 1]);
-    const int64_t r = r0 + sub * 8;
-    const int64_t idx = (m * C + c) * R + r;
-    uint32_t lo, hi;
-    if constexpr (kSR) {
-        const uint64_t j = (uint64_t)idx >> 2;
-        lo = e4m3x4_sr(v[0], v[1], v[2], v[3], sr_words4(j, stream_id, keys));
-        hi = e4m3x4_sr(v[4], v[5], v[6], v[7], sr_words4(j + 1, stream_id, keys));
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = h2_bits_to_f2(w[k]);
+            f2_unpack(f2_mul(f2_pack(f.x, f.y), g2), xa[k], xb[k]);
+        }
     } else {
-        lo = e4m3x4_rn(v[0], v[1], v[2], v[3]);
-        hi = e4m3x4_rn(v[4], v[5], v[6], v[7]);
+        aA = fabsf(bf16_lo(mx));
+        aB = fabsf(bf16_hi(mx));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            xa[k] = bf16_lo(w[k]);
+            xb[k] = bf16_hi(w[k]);
+        }
     }
-    if (live && r < R) {
-        *reinterpret_cast<uint2 *>(q_t + idx) = make_uint2(lo, hi);
-        if ((sub & 3) == 0) e8_t[(m * C + c) * (R / 32) + (r >> 5)] = (uint8_t)(e + 127);
+    const uint32_t fA = mx_scale_fs(aA), fB = mx_scale_fs(aB);
+    const uint64_t s2 = f2_pack(mx_inv_scale_fs(fA), mx_inv_scale_fs(fB));
+    float va[4], vb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f2_unpack(f2_mul(f2_pack(xa[k], xb[k]), s2), va[k], vb[k]);
+    const int64_t rowA = m * C + cA;  // output row in the [nmat * C, R] view
+    const int64_t idx = rowA * R + r0 + 4 * lane;
+    uint32_t qa, qb;
+    if constexpr (kSR) {
+        Philox4 wa, wb;
+        if constexpr (kJ32) {
+            const uint32_t j = (uint32_t)((uint64_t)idx >> 2);
+            wa = sr_words4_not32(j, stream_id, keys);
+            wb = sr_words4_not32(j + (uint32_t)(R >> 2), stream_id, keys);
+        } else {
+            const uint64_t j = (uint64_t)idx >> 2;
+            wa = sr_words4_not(j, stream_id, keys);
+            wb = sr_words4_not(j + (uint64_t)(R >> 2), stream_id, keys);
+        }
+        // one branch for the eight values (the per-element path is rare)
+        if (min(sr_fast_key4(va[0], va[1], va[2], va[3]), sr_fast_key4(vb[0], vb[1], vb[2], vb[3])) >= kSrFastMin) {
+            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], wa);
+            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], wb);
+        } else {
+            qa = e4m3x4_sr_nw(va[0], va[1], va[2], va[3], wa);
+            qb = e4m3x4_sr_nw(vb[0], vb[1], vb[2], vb[3], wb);
+        }
+    } else {
+        qa = e4m3x4_rn(va[0], va[1], va[2], va[3]);
+        qb = e4m3x4_rn(vb[0], vb[1], vb[2], vb[3]);
+    }
+    if (live && r0 + 4 * lane < R) {
+        *reinterpret_cast<uint32_t *>(q_t + idx) = qa;
+        *reinterpret_cast<uint32_t *>(q_t + idx + R) = qb;
+        if ((lane & 7) == 0) {
+            const int64_t eo = rowA * (R / 32) + (r0 >> 5) + (lane >> 3);
+            e8_t[eo] = (uint8_t)(fA - 8u);
+            e8_t[eo + R / 32] = (uint8_t)(fB - 8u);
+        }
     }
 }
 
@@ -68,8 +112,8 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
-    const int e = mx_scale_exponent(a);
-    const float s = pow2_neg(e);
+    const uint32_t fs = mx_scale_fs(a);
+    const float s = mx_inv_scale_fs(fs);
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -78,16 +122,18 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
     uint4 *dst = reinterpret_cast<uint4 *>(q_r + r * C + c);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    e8_r[r * (C / 32) + c / 32] = (uint8_t)(e + 127);
+    e8_r[r * (C / 32) + c / 32] = (uint8_t)(fs - 8u);
 }
 
-// Shared tile: 64 input columns x 128 input rows of 16-bit values, transposed (row = input
-// column).  An NVFP4 source stores e2m1 * e4m3 as f16 (at most 6 significant bits: exact) and the
-// binary32 product with g_dec is formed when the value is read back, the same single rounding;
-// a bf16 source stores its bits.
-constexpr int kPitch16 = kTileR + 8;
+// Shared tile: 32 pair-rows x 128 input rows of 32-bit words; word [p][r] holds input columns
+// 2p (low half) and 2p + 1 (high half) of input row r as 16-bit values.  An NVFP4 source stores
+// e2m1 * e4m3 as f16 (at most 6 significant bits: exact) and the binary32 product with g_dec is
+// formed when the value is read back, the same single rounding; a bf16 source stores its bits.
+// Phase 1 writes one word per pair (consecutive rows across a warp), phase 2 reads 16 bytes per
+// lane (512 contiguous bytes per warp): both conflict-free.
+constexpr int kPairs = kTileC / 2;
 
-template <SrcKind kind, bool kSR, bool kRow = false>
+template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true>
 __global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd || kind == SrcKind::CombineBwd) ? 4 : 5)
 requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
@@ -97,17 +143,12 @@ requant_transpose_kernel(
     const float *__restrict__ dh = nullptr, const int32_t *__restrict__ src_of = nullptr,
     const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
-    __shared__ __align__(16) uint16_t tile[kTileC][kPitch16];
+    __shared__ __align__(16) uint32_t tile[kPairs][kTileR];
     const int64_t f = C / 2;  // SwigluBwd: C = 2f
-    const int64_t n_rt = (R + kTileR - 1) / kTileR;
-    const int64_t n_ct = kSwb ? f / 32 : (C + kTileC - 1) / kTileC;
-    const int64_t t = blockIdx.x;
-    const int64_t rt = t % n_rt;
-    const int64_t rest = t / n_rt;
-    const int64_t ct = rest % n_ct;
-    const int64_t m = rest / n_ct;
-    const int64_t r0 = rt * kTileR, c0 = ct * (kSwb ? 32 : kTileC);
-    // output column of transposed tile row cl
+    // grid (row tiles, column tiles, matrices): no index division
+    const int64_t m = blockIdx.z;
+    const int64_t r0 = (int64_t)blockIdx.x * kTileR, c0 = (int64_t)blockIdx.y * (kSwb ? 32 : kTileC);
+    // input column (output row) of tile column cl
     auto out_col = [&](int cl) -> int64_t { return kSwb ? (cl < 32 ? c0 + cl : f + c0 + (cl - 32)) : c0 + cl; };
 
     // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
@@ -131,17 +172,19 @@ requant_transpose_kernel(
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const __half2 sfh = *reinterpret_cast<const __half2 *>(q < 2 ? &sfa2 : &sfb2);
+                    uint32_t e2[4];
+                    e2m1x8_to_h2x4(words[q], e2);
 #pragma unroll
                     for (int b2 = 0; b2 < 4; ++b2) {
-                        uint32_t e2 = e2m1x2_to_h2(words[q] >> (8 * b2));
-                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2), sfh);
+                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2[b2]), sfh);
                         h[4 * q + b2] = *reinterpret_cast<const uint32_t *>(&es);
                     }
                 }
             } else if constexpr (kSwb) {
                 // 16 gate/up column pairs per thread (one s per pair): dg = (dh * u) * s * (1 + g *
                 // (1 - s)) and du = dh * (g * s), s = 1 / (1 + exp(-g)), each step one binary32
-                // rounding, then bf16; dg to tile rows half*16 + i, du to rows 32 + half*16 + i
+                // rounding, then bf16; gate column c0 + half*16 + i goes to pair-row half*8 + i/2,
+                // its up partner to pair-row 16 + half*8 + i/2
                 const int64_t j0 = c0 + half * 16;
                 const float4 *gp = reinterpret_cast<const float4 *>(gu + r * 2 * f + j0);
                 const float4 *upp = reinterpret_cast<const float4 *>(gu + r * 2 * f + f + j0);
@@ -151,15 +194,20 @@ requant_transpose_kernel(
                     const float4 g4 = __ldg(gp + k4), u4 = __ldg(upp + k4), d4 = __ldg(dp + k4);
                     const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, us[4] = {u4.x, u4.y, u4.z, u4.w};
                     const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+                    uint32_t dgb[4], dub[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
                         const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
                         const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
                         const float duv = __fmul_rn(ds[i], __fmul_rn(gs[i], sg));
-                        tile[half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(dgv);
-                        tile[32 + half * 16 + 4 * k4 + i][rl] = f32_to_bf16_bits(duv);
+                        dgb[i] = f32_to_bf16_bits(dgv);
+                        dub[i] = f32_to_bf16_bits(duv);
                     }
+                    tile[half * 8 + 2 * k4][rl] = dgb[0] | (dgb[1] << 16);
+                    tile[half * 8 + 2 * k4 + 1][rl] = dgb[2] | (dgb[3] << 16);
+                    tile[16 + half * 8 + 2 * k4][rl] = dub[0] | (dub[1] << 16);
+                    tile[16 + half * 8 + 2 * k4 + 1][rl] = dub[2] | (dub[3] << 16);
                 }
             } else if constexpr (kind == SrcKind::CombineBwd) {
                 const int32_t tok = __ldg(src_of + r);
@@ -211,18 +259,15 @@ requant_transpose_kernel(
             for (int i = 0; i < 16; ++i) h[i] = 0u;
             if constexpr (kSwb) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    tile[half * 16 + i][rl] = 0;
-                    tile[32 + half * 16 + i][rl] = 0;
+                for (int i = 0; i < 8; ++i) {
+                    tile[half * 8 + i][rl] = 0u;
+                    tile[16 + half * 8 + i][rl] = 0u;
                 }
             }
         }
         if constexpr (!kSwb) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                tile[half * 32 + 2 * i][rl] = (uint16_t)(h[i] & 0xFFFFu);
-                tile[half * 32 + 2 * i + 1][rl] = (uint16_t)(h[i] >> 16);
-            }
+            for (int i = 0; i < 16; ++i) tile[half * 16 + i][rl] = h[i];
         }
     }
     __syncthreads();
@@ -235,33 +280,23 @@ requant_transpose_kernel(
         if (r < R) {
             float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)tile[half * 32 + i][rl] << 16);
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t wv = tile[half * 16 + i][rl];
+                v[2 * i] = bf16_lo(wv);
+                v[2 * i + 1] = bf16_hi(wv);
+            }
             emit_rowwise32(v, r, out_col(half * 32), C, q_r, e8_r);
         }
     }
 
-    // phase 2: each warp emits two output rows per iteration (lanes 0-15 and 16-31)
+    // phase 2: each warp emits one pair-row (two output rows) per iteration
     const float g = (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
-    const int lane = lane_id();
-    const int sub = lane & 15;
 #pragma unroll 1
-    for (int i = 0; i < kTileC / 16; ++i) {
-        const int cl = warp_id() + 16 * i + 8 * (lane >> 4);
-        const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cl][sub * 8]);
-        const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
-        float x[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if constexpr (kind == SrcKind::Nvfp4) {
-                const float2 f = h2_bits_to_f2(pw[k]);
-                f2_unpack(f2_mul(f2_pack(f.x, f.y), f2_pack(g, g)), x[2 * k], x[2 * k + 1]);
-            } else {
-                x[2 * k] = bf16_lo(pw[k]);
-                x[2 * k + 1] = bf16_hi(pw[k]);
-            }
-        }
-        const int64_t c = out_col(cl);
-        emit8<kSR>(x, c < C, m, c, r0, R, C, q_t, e8_t, keys, stream_id);
+    for (int i = 0; i < kPairs / 8; ++i) {
+        const int cp = warp_id() + 8 * i;
+        const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cp][4 * lane_id()]);
+        const int64_t cA = out_col(2 * cp);
+        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8_t, keys, stream_id);
     }
 }
 
@@ -285,20 +320,29 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        const int e = mx_scale_exponent(a);
-        const float s = pow2_neg(e);
+        const uint32_t fs = mx_scale_fs(a);
+        const float s = mx_inv_scale_fs(fs);
         const float v0 = __fmul_rn(x4[0], s), v1 = __fmul_rn(x4[1], s);
         const float v2 = __fmul_rn(x4[2], s), v3 = __fmul_rn(x4[3], s);
         uint32_t packed;
         if (sr) {
-            packed = e4m3x4_sr(v0, v1, v2, v3, sr_words4((uint64_t)gidx, stream_id, keys));
+            packed = e4m3x4_sr_nw(v0, v1, v2, v3, sr_words4_not((uint64_t)gidx, stream_id, keys));
         } else {
             packed = e4m3x4_rn(v0, v1, v2, v3);
         }
         if (!live) continue;
         *reinterpret_cast<uint32_t *>(q + gidx * 4) = packed;
-        if ((gidx & 7) == 0) e8[gidx >> 3] = (uint8_t)(e + 127);
+        if ((gidx & 7) == 0) e8[gidx >> 3] = (uint8_t)(fs - 8u);
     }
+}
+
+// Grid of the transposing kernel: x row tiles, y column tiles, z matrices (rejected beyond the
+// launch limits: 2^31 - 1 and 65535).
+static bool requant_grid(int64_t rows, int64_t col_tiles, int64_t nmat, dim3 &grid) {
+    const int64_t rt = (rows + kTileR - 1) / kTileR;
+    if (rt >= (int64_t(1) << 31) || col_tiles > 65535 || nmat > 65535) return false;
+    grid = dim3((unsigned)rt, (unsigned)col_tiles, (unsigned)nmat);
+    return true;
 }
 
 }  // namespace moe4
@@ -315,14 +359,19 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     MOE4_CHECK_ARG((flags & ~(MOE4_SR | MOE4_SF_MMA_LAYOUT)) == 0);
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
     MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
-    const int64_t tiles = nmat * ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
-    if (tiles == 0) return MOE4_OK;
-    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-    if (flags & MOE4_SR)
-        requant_transpose_kernel<SrcKind::Nvfp4, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+    dim3 grid;
+    MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, nmat, grid));
+    if (rows == 0) return MOE4_OK;
+    // output indices below 2^34: the Philox counter's second word is zero throughout
+    const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 34);
+    if ((flags & MOE4_SR) && j32)
+        requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, as_stream(stream)>>>(
+            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
+    else if (flags & MOE4_SR)
+        requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, as_stream(stream)>>>(
             codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
     else
-        requant_transpose_kernel<SrcKind::Nvfp4, false><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+        requant_transpose_kernel<SrcKind::Nvfp4, false><<<grid, 256, 0, as_stream(stream)>>>(
             codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
     return launch_status();
 }
@@ -346,14 +395,17 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         mxfp8_rowwise_kernel<<<(unsigned)grid, 256, 0, st>>>(x, rows, cols, q, e8, philox_keys(seed), stream_id, sr);
     } else {
         MOE4_CHECK_ARG(rows % 32 == 0 && aligned16(x) && aligned16(q));
-        const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
-        if (tiles == 0) return MOE4_OK;
-        MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-        if (sr)
-            requant_transpose_kernel<SrcKind::Bf16, true><<<(unsigned)tiles, 256, 0, st>>>(
+        dim3 grid;
+        MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, 1, grid));
+        if (rows == 0) return MOE4_OK;
+        if (sr && (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 34))
+            requant_transpose_kernel<SrcKind::Bf16, true><<<grid, 256, 0, st>>>(
+                nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
+        else if (sr)
+            requant_transpose_kernel<SrcKind::Bf16, true, false, false><<<grid, 256, 0, st>>>(
                 nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
         else
-            requant_transpose_kernel<SrcKind::Bf16, false><<<(unsigned)tiles, 256, 0, st>>>(
+            requant_transpose_kernel<SrcKind::Bf16, false><<<grid, 256, 0, st>>>(
                 nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
     }
     return launch_status();
@@ -365,10 +417,10 @@ extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t co
     MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 32 == 0 && flags == 0);
     MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || x));
     MOE4_CHECK_ARG(aligned16(x) && aligned16(q_row) && aligned16(q_col));
-    const int64_t tiles = ((rows + kTileR - 1) / kTileR) * ((cols + kTileC - 1) / kTileC);
-    if (tiles == 0) return MOE4_OK;
-    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-    requant_transpose_kernel<SrcKind::Bf16, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+    dim3 grid;
+    MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, 1, grid));
+    if (rows == 0) return MOE4_OK;
+    requant_transpose_kernel<SrcKind::Bf16, false, true><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row);
     return launch_status();
 }
@@ -379,10 +431,10 @@ extern "C" int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int6
     MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && f > 0 && f % 32 == 0 && flags == 0);
     MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || (gu && dh)));
     MOE4_CHECK_ARG(aligned16(gu) && aligned16(dh) && aligned16(q_row) && aligned16(q_col));
-    const int64_t tiles = ((rows + kTileR - 1) / kTileR) * (f / 32);
-    if (tiles == 0) return MOE4_OK;
-    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-    requant_transpose_kernel<SrcKind::SwigluBwd, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+    dim3 grid;
+    MOE4_CHECK_ARG(requant_grid(rows, f / 32, 1, grid));
+    if (rows == 0) return MOE4_OK;
+    requant_transpose_kernel<SrcKind::SwigluBwd, false, true><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, nullptr, 1, rows, 2 * f, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, gu,
         dh);
     return launch_status();
@@ -396,10 +448,10 @@ extern "C" int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *ro
     MOE4_CHECK_ARG(flags == 0 && src_of && q_row && e8_row && q_col && e8_col);
     MOE4_CHECK_ARG(T == 0 || (dy && row_of && w && aligned16(dy)));
     MOE4_CHECK_ARG(aligned16(q_row) && aligned16(q_col));
-    const int64_t tiles = ((rows_total + kTileR - 1) / kTileR) * ((d + kTileC - 1) / kTileC);
-    if (tiles == 0) return MOE4_OK;
-    MOE4_CHECK_ARG(tiles < (int64_t(1) << 31));
-    requant_transpose_kernel<SrcKind::CombineBwd, false, true><<<(unsigned)tiles, 256, 0, as_stream(stream)>>>(
+    dim3 grid;
+    MOE4_CHECK_ARG(requant_grid(rows_total, (d + kTileC - 1) / kTileC, 1, grid));
+    if (rows_total == 0) return MOE4_OK;
+    requant_transpose_kernel<SrcKind::CombineBwd, false, true><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, dy, 1, rows_total, d, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row,
         nullptr, nullptr, src_of, row_of, w, (int)k);
     return launch_status();
