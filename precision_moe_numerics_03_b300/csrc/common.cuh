@@ -340,6 +340,13 @@ __device__ __forceinline__ float2 h2_bits_to_f2(uint32_t h) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
+// fma.rn.f32x2: two single-rounding multiply-adds.
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

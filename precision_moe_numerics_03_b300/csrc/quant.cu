@@ -116,13 +116,16 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, con
         w0 = e2m1x8_rn(v);
         w1 = e2m1x8_rn(v + 8);
         // d = y - e*sf: e*sf has at most 6 significant bits and is exact in binary32, so the fused
-        // form rounds once, exactly as the subtraction of the exact product does
-        const float nsf = -sfv;
+        // form rounds once, exactly as the subtraction of the exact product does (packed pairs:
+        // the multiply-add feeds only the squares)
+        const uint64_t nsf2 = f2_pack(-sfv, -sfv);
+        uint32_t eh[8];
+        e2m1x8_to_h2x4(w0, eh);
+        e2m1x8_to_h2x4(w1, eh + 4);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float2 e = h2_bits_to_f2(e2m1x2_to_h2((i < 4 ? w0 : w1) >> (8 * (i & 3))));
-            d[2 * i] = __fmaf_rn(e.x, nsf, y[2 * i]);
-            d[2 * i + 1] = __fmaf_rn(e.y, nsf, y[2 * i + 1]);
+            const float2 e = h2_bits_to_f2(eh[i]);
+            f2_unpack(f2_fma(f2_pack(e.x, e.y), nsf2, f2_pack(y[2 * i], y[2 * i + 1])), d[2 * i], d[2 * i + 1]);
         }
     }
     float s[16];
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
     const uint16_t *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
-    float *__restrict__ g_dec) {
+    float *__restrict__ g_dec, uint32_t div_m, uint32_t div_s) {
     __shared__ float2 tab[128];
     fill_scale_tab(tab);
     const int64_t nblk = cols / 16;
@@ -192,7 +195,11 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
         }
         const int64_t rem = b - mat_begin;
         int64_t row = 0, blk = 0;
-        if (!contiguous || sf_mma) {
+        if (sf_mma) {
+            // nblk % 4 == 0 here: rem / nblk = (rem / 4) / (nblk / 4) by multiply and shift
+            row = (int64_t)(uint32_t)(((uint64_t)((uint32_t)rem >> 2) * div_m) >> div_s);
+            blk = rem - row * nblk;
+        } else if (!contiguous) {
             row = (int64_t)((uint32_t)rem / (uint32_t)nblk);
             blk = rem - row * nblk;
         }
@@ -428,6 +435,16 @@ __global__ void __launch_bounds__(256) hadamard_dequant_mx_kernel(const uint8_t 
 }
 #undef MOE4_SUB16_LOOP
 
+// Division of n < 2^31 by d >= 1 as (n * m) >> s (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994, theorem 4.2): l = ceil(log2 d), s = 31 + l,
+// m = ceil(2^s / d), which is below 2^32.
+static void div_magic(uint32_t d, uint32_t &m, uint32_t &s) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    s = 31 + l;
+    m = (uint32_t)(((uint64_t(1) << s) + d - 1) / d);
+}
+
 static int grid_for(int64_t work_items, int threads, int per_sm) {
     const int64_t need = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms() * per_sm;
@@ -468,9 +485,11 @@ extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int
     }
     const int64_t total = nmat * rows * (cols / 16);
     const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
+    uint32_t div_m = 0, div_s = 0;
+    if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
     nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, given ? amax_in : nullptr,
                                              amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf,
-                                             g_dec);
+                                             g_dec, div_m, div_s);
     return launch_status();
 }
 
@@ -578,7 +597,10 @@ extern "C" int nvfp4_quantize_noalloc(const uint16_t *x, int64_t nmat, int64_t r
     }
     const int64_t total = nmat * rows * (cols / 16);
     const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
+    uint32_t div_m = 0, div_s = 0;
+    if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
     nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, nullptr, amax_bits,
-                                             (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf, g_dec);
+                                             (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf, g_dec, div_m,
+                                             div_s);
     return launch_status();
 }

@@ -40,6 +40,27 @@ def test_requant_small(shape, sr, seed, sid):
     assert first_mismatch(to_np(q), rq) is None
 
 
+@pytest.mark.parametrize("sr", [True, False])
+def test_requant_extreme_global_scales(sr):
+    """Three matrices with global decode scales far apart: tiny (amax ~1e-36, g_dec below 2^-116),
+    ordinary, and huge (amax ~1e30, g_dec above 2), the last two with all-zero 32-row blocks in
+    some output rows (their block scale is the smallest, 2^-127)."""
+    rows, cols = 160, 192
+    rng = np.random.default_rng(77)
+    base = rng.standard_t(3, (3, rows, cols))
+    base[1:, :32, 5] = 0.0
+    base[1:, 64:96, 70:74] = 0.0
+    x = inputs.to_bf16_bits((base * np.array([1e-36, 1.0, 1e30])[:, None, None]).astype(np.float32))
+    x = x.reshape(3 * rows, cols)
+    c, s, g = nvfp4_quantize(to_dev(x), 3, rows, cols)
+    q, e8 = _requant_gpu(c, s, g, 3, rows, cols, 5, 1, sr)
+    oc, os_, og = oracle.nvfp4_quantize(oracle.bf16_to_f32(x).reshape(3, rows, cols))
+    assert og[0] < 2.0 ** -116 and og[2] > 2.0
+    rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=sr, seed=5, stream_id=1)
+    assert first_mismatch(to_np(e8), re8) is None
+    assert first_mismatch(to_np(q), rq) is None
+
+
 def test_requant_single_expert_operands():
     rng = inputs.host_rng(1, 0)
     x = inputs.to_bf16_bits(inputs.host_outliers(rng, inputs.host_normal(rng, (256, 512))))
