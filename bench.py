@@ -148,7 +148,7 @@ class LayerStep:
         """One layer step; io = (X, logits, dy, y) device tensors to use instead of the step's own."""
         m, torch = self.m, self.torch
         T, d, f, E, k = self.T, self.d, self.f, self.E, self.k
-        FOS, MMA = m.FOUR_OVER_SIX, m.SF_MMA_LAYOUT
+        FOS, MMA, OMMA = m.FOUR_OVER_SIX, m.SF_MMA_LAYOUT, m.SF_OUT_MMA
         tm = timer if timer is not None else _NullTimer()
         X, logits, dy, y = io if io is not None else (self.X, self.logits, self.dy, self.y)
         n = 0
@@ -193,42 +193,42 @@ class LayerStep:
         # ---------------- backward
         with tm("mxfp8_quant"):  # combine gradient straight into both MXFP8 layouts of dY
             m.moe4_combine_backward_mxfp8(dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYr_q, self.dYr_e,
-                                          self.dYc_q, self.dYc_e)
+                                          self.dYc_q, self.dYc_e, OMMA)
         n += 1
         with tm("requant"):
             m.mxfp8_requant_transpose_sr(self.Wd_c, self.Wd_s, self.Wd_g, E, d, f, self.WdT_q, self.WdT_e, seed, 1,
-                                         m.SR | MMA)
+                                         m.SR | MMA | OMMA)
             m.mxfp8_requant_transpose_sr(self.Hq_c, self.Hq_s, self.Hq_g, 1, Rp, f, self.HqT_q, self.HqT_e, seed, 2,
-                                         m.SR | MMA)
+                                         m.SR | MMA | OMMA)
         n += 2
         with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dYr_q, self.dYr_e, self.WdT_q, self.WdT_e, self.offs, E, Rp, f, d, self.dH,
-                                 m.OUT_F32 | m.GROUP_M, self.gws)
-        n += 3
+                                 m.OUT_F32 | m.GROUP_M | MMA, self.gws)
+        n += 1
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp,
-                                           self.W32_d, self.Wb_d, LR, self.amax_d, 0, self.gws)
-        n += 4  # two scale-layout passes, the expert ranking for the tile schedule, the GEMM
+                                           self.W32_d, self.Wb_d, LR, self.amax_d, MMA, self.gws)
+        n += 2  # the expert ranking for the tile schedule, the GEMM
         with tm("swiglu_bwd"):
             m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
         n += 1
         with tm("mxfp8_quant"):
-            m.mxfp8_quantize_rowcol(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, self.dGUc_q, self.dGUc_e)
+            m.mxfp8_quantize_rowcol(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, self.dGUc_q, self.dGUc_e, OMMA)
         n += 1
         with tm("requant"):
             m.mxfp8_requant_transpose_sr(self.Wgu_c, self.Wgu_s, self.Wgu_g, E, 2 * f, d, self.WguT_q, self.WguT_e,
-                                         seed, 3, m.SR | MMA)
+                                         seed, 3, m.SR | MMA | OMMA)
             m.mxfp8_requant_transpose_sr(self.Xp_c, self.Xp_s, self.Xq_g, 1, Rp, d, self.XpT_q, self.XpT_e, seed, 4,
-                                         m.SR | MMA)
+                                         m.SR | MMA | OMMA)
         n += 2
         with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dGUr_q, self.dGUr_e, self.WguT_q, self.WguT_e, self.offs, E, Rp, d, 2 * f,
-                                 self.dXp, m.OUT_BF16 | m.GROUP_M, self.gws)
-        n += 3
+                                 self.dXp, m.OUT_BF16 | m.GROUP_M | MMA, self.gws)
+        n += 1
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d,
-                                           Rp, self.W32_gu, self.Wb_gu, LR, self.amax_gu, 0, self.gws)
-        n += 4
+                                           Rp, self.W32_gu, self.Wb_gu, LR, self.amax_gu, MMA, self.gws)
+        n += 2
         self.launches += n
         return n
 

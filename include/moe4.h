@@ -70,6 +70,7 @@ extern "C" {
 #define MOE4_ACCUMULATE     0x04000u /* grouped GEMM: D += result (binary32 output only) */
 #define MOE4_SF_MMA_LAYOUT  0x10000u /* scale factors are in the tensor-core tile layout */
 #define MOE4_MXFP8          0x20000u /* Hadamard codec: the 8.25-bit MXFP8 variant */
+#define MOE4_SF_OUT_MMA     0x40000u /* MXFP8 producers: output scales in the tensor-core tile layout */
 
 /* ------------------------------------------------------------------ library */
 int moe4_version(void);                      /* e.g. 100 for 0.1.0 */
@@ -146,8 +147,11 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec
  * word < floor(frac * 2^32), frac being its distance above the E4M3 value below, in units of
  * the gap.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
  * rows % 32 == 0, cols % 32 == 0.  Input scales canonical, or in the tensor-core tile layout with
- * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0).  nmat and cols / 64 at most 65535 (one
- * thread block per 128 x 64 tile on a three-dimensional grid); beyond that MOE4_ERR_ARG. */
+ * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0).  With MOE4_SF_OUT_MMA, e8_t is written in
+ * the tensor-core tile layout of moe4_sf_to_mma_layout (as [nmat * cols, rows / 32]; rows % 128
+ * == 0, cols % 128 == 0), ready for the MXFP8 GEMMs' MOE4_SF_MMA_LAYOUT.  nmat and cols / 64 at
+ * most 65535 (one thread block per 128 x 64 tile on a three-dimensional grid); beyond that
+ * MOE4_ERR_ARG. */
 int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const float *g_dec,
                                int64_t nmat, int64_t rows, int64_t cols, uint8_t *q_t,
                                uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,
@@ -165,7 +169,9 @@ int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, ui
  * backward's dY and dGU feed the rows-grouped dgrad row-wise and the contraction-grouped wgrad
  * transposed [DEBUT] confirmed list).  q_row [rows, cols], e8_row [rows, cols/32]; q_col
  * [cols, rows], e8_col [cols, rows/32]; the bytes equal those of the two single-layout calls.
- * rows % 32 == 0, cols % 32 == 0; x, q_row and q_col 16-byte aligned; flags must be 0. */
+ * rows % 32 == 0, cols % 32 == 0; x, q_row and q_col 16-byte aligned.  flags: 0, or
+ * MOE4_SF_OUT_MMA to write both scale outputs in the tensor-core tile layout (rows % 128 == 0,
+ * cols % 128 == 0). */
 int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q_row,
                           uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
                           void *stream);
@@ -296,7 +302,8 @@ int moe4_swiglu_backward(const float *gu, const float *dh, int64_t rows, int64_t
  * bf16 dgu of moe4_swiglu_backward (same arithmetic, same bits) is never written: its row-wise
  * MXFP8 q_row [rows, 2f], e8_row [rows, 2f/32] and its transposed MXFP8 q_col [2f, rows],
  * e8_col [2f, rows/32] are, byte for byte as mxfp8_quantize_rowcol of that dgu would give them
- * (nearest-even).  rows % 32 == 0, f % 32 == 0; gu, dh, q_row, q_col 16-byte aligned; flags 0. */
+ * (nearest-even).  rows % 32 == 0, f % 32 == 0; gu, dh, q_row, q_col 16-byte aligned.  flags: 0,
+ * or MOE4_SF_OUT_MMA (both scale outputs in the tile layout; rows % 128 == 0, f % 64 == 0). */
 int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int64_t rows, int64_t f, uint8_t *q_row,
                                uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags, void *stream);
 
@@ -313,7 +320,8 @@ int moe4_combine_backward(const uint16_t *dy, const int32_t *row_of, const float
  * (same arithmetic, same bits) is never written; its row-wise MXFP8 q_row [rows_total, d],
  * e8_row [rows_total, d/32] and transposed MXFP8 q_col [d, rows_total], e8_col [d, rows_total/32]
  * are, byte for byte as mxfp8_quantize_rowcol of that dyhat would give them (nearest-even).
- * d % 32 == 0, rows_total % 32 == 0; dy, q_row, q_col 16-byte aligned; flags 0. */
+ * d % 32 == 0, rows_total % 32 == 0; dy, q_row, q_col 16-byte aligned.  flags: 0, or
+ * MOE4_SF_OUT_MMA (both scale outputs in the tile layout; rows_total % 128 == 0, d % 128 == 0). */
 int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *row_of, const float *w, const int32_t *src_of,
                                 int64_t T, int64_t k, int64_t d, int64_t rows_total, uint8_t *q_row,
                                 uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags, void *stream);

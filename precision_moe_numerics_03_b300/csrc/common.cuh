@@ -347,6 +347,19 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     return r;
 }
 
+// Offset of the scale byte of (row, blk) in the tensor-core tile layout of a matrix with
+// `rows` rows and `nblk` blocks per row (nblk % 4 == 0): 512 bytes per 128-row tile and group of
+// four blocks, row 32j + i of the tile at 16i + 4j.
+__device__ __forceinline__ int64_t sf_mma_offset(int64_t row, int64_t blk, int64_t nblk) {
+    const int64_t rt = row >> 7, i = row & 31, j = (row >> 5) & 3;
+    const int64_t kg = blk >> 2, kb = blk & 3;
+    return (rt * (nblk >> 2) + kg) * 512 + i * 16 + j * 4 + kb;
+}
+// The same byte in the canonical [rows, nblk] layout or in the tile layout.
+__device__ __forceinline__ int64_t sf_offset(int64_t row, int64_t blk, int64_t nblk, bool mma) {
+    return mma ? sf_mma_offset(row, blk, nblk) : row * nblk + blk;
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

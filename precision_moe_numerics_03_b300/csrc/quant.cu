@@ -155,14 +155,6 @@ __device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_si
     }
 }
 
-// Offset of the scale byte of (row, blk) in the tensor-core tile layout of a matrix with
-// `rows` rows and `nblk` blocks per row.
-__device__ __forceinline__ int64_t sf_mma_offset(int64_t row, int64_t blk, int64_t nblk) {
-    const int64_t rt = row >> 7, i = row & 31, j = (row >> 5) & 3;
-    const int64_t kg = blk >> 2, kb = blk & 3;
-    return (rt * (nblk >> 2) + kg) * 512 + i * 16 + j * 4 + kb;
-}
-
 // One thread per 16-value block.  amax per matrix from amax_in (given) or amax_bits (pass 1).
 // The block index b runs over all matrices; with contiguous rows (ld == cols) the input, code and
 // canonical-scale offsets are b*16, b*8 and b, and the matrix index only moves forward in the

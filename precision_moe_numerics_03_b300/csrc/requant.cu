@@ -31,10 +31,11 @@ enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 // input rows 4l .. 4l+3 of both; lanes 8b .. 8b+7 form 32-block b, whose amax is taken on the
 // packed 16-bit pairs (the binary32 values are monotone in them: an NVFP4 source is scaled by
 // g > 0 with one rounding, a bf16 source converts exactly).  Every lane takes part in the
-// shuffles; `live` only guards the stores.
+// shuffles; `live` only guards the stores.  The scale codes go to e8s[cl], e8s[cl + 1] (the
+// tile's 64 output rows x 4 blocks), written out once per tile.
 template <SrcKind kind, bool kSR, bool kJ32>
 __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int64_t m, int64_t cA, int64_t r0,
-                                          int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t *__restrict__ e8_t,
+                                          int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t (*e8s)[4], int cl,
                                           const PhiloxKeys keys, uint32_t stream_id) {
     constexpr bool kF16 = kind == SrcKind::Nvfp4;
     const int lane = lane_id();
@@ -97,10 +98,9 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
     if (live && r0 + 4 * lane < R) {
         *reinterpret_cast<uint32_t *>(q_t + idx) = qa;
         *reinterpret_cast<uint32_t *>(q_t + idx + R) = qb;
-        if ((lane & 7) == 0) {
-            const int64_t eo = rowA * (R / 32) + (r0 >> 5) + (lane >> 3);
-            e8_t[eo] = (uint8_t)(fA - 8u);
-            e8_t[eo + R / 32] = (uint8_t)(fB - 8u);
+        if ((lane & 7) == 0) {  // the tile's scale codes, stored after the loop
+            e8s[cl][lane >> 3] = (uint8_t)(fA - 8u);
+            e8s[cl + 1][lane >> 3] = (uint8_t)(fB - 8u);
         }
     }
 }
@@ -108,7 +108,7 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
 // The row-wise MXFP8 of the 32 values a thread holds in phase 1 (one block along the row),
 // nearest-even: written to q_r [R, C] and e8_r [R, C/32] when the kernel also emits that layout.
 __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int64_t c, int64_t C,
-                                               uint8_t *__restrict__ q_r, uint8_t *__restrict__ e8_r) {
+                                               uint8_t *__restrict__ q_r, uint8_t *__restrict__ e8_r, bool e8_mma) {
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
@@ -122,7 +122,7 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
     uint4 *dst = reinterpret_cast<uint4 *>(q_r + r * C + c);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    e8_r[r * (C / 32) + c / 32] = (uint8_t)(fs - 8u);
+    e8_r[sf_offset(r, c / 32, C / 32, e8_mma)] = (uint8_t)(fs - 8u);
 }
 
 // Shared tile: 32 pair-rows x 128 input rows of 32-bit words; word [p][r] holds input columns
@@ -134,16 +134,18 @@ __device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int
 constexpr int kPairs = kTileC / 2;
 
 template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true>
-__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd || kind == SrcKind::CombineBwd) ? 4 : 5)
+__global__ void __launch_bounds__(256, (kSR || kRow || kind == SrcKind::SwigluBwd || kind == SrcKind::CombineBwd) ? 4 : 5)
 requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
     uint8_t *__restrict__ e8_t, const PhiloxKeys keys, uint32_t stream_id, bool sf_mma,
     uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr, const float *__restrict__ gu = nullptr,
     const float *__restrict__ dh = nullptr, const int32_t *__restrict__ src_of = nullptr,
-    const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0) {
+    const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0,
+    bool e8_mma = false) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
     __shared__ __align__(16) uint32_t tile[kPairs][kTileR];
+    __shared__ __align__(4) uint8_t e8s[kTileC][4];
     const int64_t f = C / 2;  // SwigluBwd: C = 2f
     // grid (row tiles, column tiles, matrices): no index division
     const int64_t m = blockIdx.z;
@@ -232,7 +234,7 @@ requant_transpose_kernel(
                         v[2 * i] = bf16_lo(h[i]);
                         v[2 * i + 1] = bf16_hi(h[i]);
                     }
-                    emit_rowwise32(v, r, c, C, q_r, e8_r);
+                    emit_rowwise32(v, r, c, C, q_r, e8_r, e8_mma);
                 }
             } else {
                 const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (m * R + r) * C + c);
@@ -251,7 +253,7 @@ requant_transpose_kernel(
                         v[2 * i] = bf16_lo(h[i]);
                         v[2 * i + 1] = bf16_hi(h[i]);
                     }
-                    emit_rowwise32(v, r, c, C, q_r, e8_r);
+                    emit_rowwise32(v, r, c, C, q_r, e8_r, e8_mma);
                 }
             }
         } else {
@@ -285,7 +287,7 @@ requant_transpose_kernel(
                 v[2 * i] = bf16_lo(wv);
                 v[2 * i + 1] = bf16_hi(wv);
             }
-            emit_rowwise32(v, r, out_col(half * 32), C, q_r, e8_r);
+            emit_rowwise32(v, r, out_col(half * 32), C, q_r, e8_r, e8_mma);
         }
     }
 
@@ -296,7 +298,25 @@ requant_transpose_kernel(
         const int cp = warp_id() + 8 * i;
         const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cp][4 * lane_id()]);
         const int64_t cA = out_col(2 * cp);
-        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8_t, keys, stream_id);
+        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8s, 2 * cp, keys, stream_id);
+    }
+    // scale codes: one thread per output row, its (up to) four blocks of this tile; the four are
+    // adjacent bytes in both layouts (a whole word when R % 128 == 0)
+    __syncthreads();
+    if (threadIdx.x < kTileC) {
+        const int cl = threadIdx.x;
+        const int64_t c = out_col(cl);
+        if (c < C) {
+            const int64_t row = m * C + c, nkb = R / 32, kb0 = r0 >> 5;
+            const int64_t off = sf_offset(row, kb0, nkb, e8_mma);
+            const uint32_t word = *reinterpret_cast<const uint32_t *>(e8s[cl]);
+            if ((nkb & 3) == 0 && ((reinterpret_cast<uintptr_t>(e8_t) & 3u) == 0)) {
+                *reinterpret_cast<uint32_t *>(e8_t + off) = word;
+            } else {
+                const int nb = nkb - kb0 < 4 ? (int)(nkb - kb0) : 4;
+                for (int b = 0; b < nb; ++b) e8_t[off + b] = (uint8_t)(word >> (8 * b));
+            }
+        }
     }
 }
 
@@ -356,23 +376,28 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && rows % 32 == 0 && cols % 32 == 0);
     MOE4_CHECK_ARG(codes && sf && g_dec && q_t && e8_t);
     MOE4_CHECK_ARG(aligned16(codes) && aligned16(q_t) && (reinterpret_cast<uintptr_t>(sf) & 1u) == 0);
-    MOE4_CHECK_ARG((flags & ~(MOE4_SR | MOE4_SF_MMA_LAYOUT)) == 0);
+    MOE4_CHECK_ARG((flags & ~(MOE4_SR | MOE4_SF_MMA_LAYOUT | MOE4_SF_OUT_MMA)) == 0);
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
+    const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
     MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
+    MOE4_CHECK_ARG(!e8_mma || (rows % 128 == 0 && cols % 128 == 0));
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, nmat, grid));
     if (rows == 0) return MOE4_OK;
     // output indices below 2^34: the Philox counter's second word is zero throughout
     const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 34);
+    const PhiloxKeys keys = philox_keys(seed);
+    cudaStream_t st = as_stream(stream);
+#define MOE4_REQUANT_ARGS                                                                                        \
+    codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, sf_mma, nullptr, nullptr, nullptr, \
+        nullptr, nullptr, nullptr, nullptr, 0, e8_mma
     if ((flags & MOE4_SR) && j32)
-        requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, as_stream(stream)>>>(
-            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
+        requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_REQUANT_ARGS);
     else if (flags & MOE4_SR)
-        requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, as_stream(stream)>>>(
-            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
+        requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, st>>>(MOE4_REQUANT_ARGS);
     else
-        requant_transpose_kernel<SrcKind::Nvfp4, false><<<grid, 256, 0, as_stream(stream)>>>(
-            codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, philox_keys(seed), stream_id, sf_mma);
+        requant_transpose_kernel<SrcKind::Nvfp4, false><<<grid, 256, 0, st>>>(MOE4_REQUANT_ARGS);
+#undef MOE4_REQUANT_ARGS
     return launch_status();
 }
 
@@ -414,29 +439,34 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
 extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q_row,
                                      uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
                                      void *stream) {
-    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 32 == 0 && flags == 0);
+    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 32 == 0 && (flags & ~MOE4_SF_OUT_MMA) == 0);
     MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || x));
     MOE4_CHECK_ARG(aligned16(x) && aligned16(q_row) && aligned16(q_col));
+    const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
+    MOE4_CHECK_ARG(!e8_mma || (rows % 128 == 0 && cols % 128 == 0));
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, 1, grid));
     if (rows == 0) return MOE4_OK;
     requant_transpose_kernel<SrcKind::Bf16, false, true><<<grid, 256, 0, as_stream(stream)>>>(
-        nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row);
+        nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, nullptr,
+        nullptr, nullptr, nullptr, nullptr, 0, e8_mma);
     return launch_status();
 }
 
 extern "C" int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int64_t rows, int64_t f, uint8_t *q_row,
                                           uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags,
                                           void *stream) {
-    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && f > 0 && f % 32 == 0 && flags == 0);
+    MOE4_CHECK_ARG(rows >= 0 && rows % 32 == 0 && f > 0 && f % 32 == 0 && (flags & ~MOE4_SF_OUT_MMA) == 0);
     MOE4_CHECK_ARG(q_row && e8_row && q_col && e8_col && (rows == 0 || (gu && dh)));
     MOE4_CHECK_ARG(aligned16(gu) && aligned16(dh) && aligned16(q_row) && aligned16(q_col));
+    const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
+    MOE4_CHECK_ARG(!e8_mma || (rows % 128 == 0 && f % 64 == 0));
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows, f / 32, 1, grid));
     if (rows == 0) return MOE4_OK;
     requant_transpose_kernel<SrcKind::SwigluBwd, false, true><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, nullptr, 1, rows, 2 * f, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, gu,
-        dh);
+        dh, nullptr, nullptr, nullptr, 0, e8_mma);
     return launch_status();
 }
 
@@ -445,14 +475,16 @@ extern "C" int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *ro
                                            uint8_t *q_row, uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col,
                                            uint32_t flags, void *stream) {
     MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 32 == 0 && rows_total >= 0 && rows_total % 32 == 0);
-    MOE4_CHECK_ARG(flags == 0 && src_of && q_row && e8_row && q_col && e8_col);
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_OUT_MMA) == 0 && src_of && q_row && e8_row && q_col && e8_col);
     MOE4_CHECK_ARG(T == 0 || (dy && row_of && w && aligned16(dy)));
     MOE4_CHECK_ARG(aligned16(q_row) && aligned16(q_col));
+    const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
+    MOE4_CHECK_ARG(!e8_mma || (rows_total % 128 == 0 && d % 128 == 0));
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows_total, (d + kTileC - 1) / kTileC, 1, grid));
     if (rows_total == 0) return MOE4_OK;
     requant_transpose_kernel<SrcKind::CombineBwd, false, true><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, dy, 1, rows_total, d, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row,
-        nullptr, nullptr, src_of, row_of, w, (int)k);
+        nullptr, nullptr, src_of, row_of, w, (int)k, e8_mma);
     return launch_status();
 }

@@ -27,6 +27,7 @@ GROUP_K = 0x02000
 ACCUMULATE = 0x04000
 SF_MMA_LAYOUT = 0x10000
 MXFP8 = 0x20000
+SF_OUT_MMA = 0x40000
 
 OP_NVFP4_QUANTIZE = 1
 OP_HADAMARD_QUANT = 2

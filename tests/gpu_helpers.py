@@ -50,3 +50,10 @@ def first_mismatch(a: np.ndarray, b: np.ndarray):
         return None
     i = tuple(bad[0])
     return "first mismatch at %s: got %r want %r (%d mismatches of %d)" % (i, a[i], b[i], len(bad), a.size)
+
+
+def mma_layout(e8: torch.Tensor, rows: int, nblk: int) -> torch.Tensor:
+    """Canonical scale bytes [rows, nblk] rearranged by the library's own layout change."""
+    out = torch.empty(rows * nblk, dtype=torch.uint8, device=e8.device)
+    moe4.moe4_sf_to_mma_layout(e8, 1, rows, nblk, out)
+    return out

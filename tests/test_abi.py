@@ -95,6 +95,14 @@ MISALIGNED = FAKE + 4
     ("moe4_sgd_update", (FAKE, FAKE, 6, 0.1, FAKE, None)),                                   # n % 4
     ("moe4_sf_to_mma_layout", (FAKE, 1, 100, 4, FAKE, None)),                                # rows % 128
     ("moe4_convert", (7, FAKE, 4, FAKE, None)),                                              # bad kind
+    # output scales in the tile layout need whole 128-row tiles and groups of four blocks
+    ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 96, 128, FAKE, FAKE, 0, 0, 0x40000, None)),  # rows % 128
+    ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 128, 64, FAKE, FAKE, 0, 0, 0x40000, None)),  # cols % 128
+    ("mxfp8_quantize_rowcol", (FAKE, 96, 128, FAKE, FAKE, FAKE, FAKE, 0x40000, None)),          # rows % 128
+    ("moe4_swiglu_backward_mxfp8", (FAKE, FAKE, 128, 32, FAKE, FAKE, FAKE, FAKE, 0x40000, None)),  # f % 64
+    ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 128, FAKE, FAKE, FAKE, FAKE, 0x40000,
+                                     None)),                                                  # d % 128
+    ("mxfp8_quantize", (FAKE, 128, 128, FAKE, FAKE, 0, 0, 0x10 | 0x40000, None)),             # not offered
 ])
 def test_argument_checks_fail_on_host(lib, case):
     name, args = case
@@ -105,3 +113,11 @@ def test_missing_workspace_is_reported(lib):
     # nvfp4_quantize without AMAX_GIVEN and without ws -> MOE4_ERR_WORKSPACE, before any launch
     assert lib.nvfp4_quantize(FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, None, 0, None) == -5
     assert lib.hadamard_quant(FAKE, 4, 128, FAKE, FAKE, FAKE, 1, None, 0, None) == -5
+
+
+def test_python_flags_match_the_header():
+    from precision_moe_numerics_03_b300 import moe4
+    defs = dict(re.findall(r"^#define MOE4_(\w+)\s+(0x[0-9A-Fa-f]+)u", open(HEADER).read(), flags=re.M))
+    assert len(defs) >= 12
+    for name, value in defs.items():
+        assert getattr(moe4, name) == int(value, 16), name

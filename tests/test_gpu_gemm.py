@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from precision_moe_numerics_03_b300 import inputs, moe4
-from gpu_helpers import DEV, empty_u8, nvfp4_quantize, to_dev, to_np
+from gpu_helpers import DEV, empty_u8, mma_layout, nvfp4_quantize, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -212,3 +212,45 @@ def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd(sizes, M, N):
     assert torch.equal(wb_f, wb_ref)
     want = np.abs(oracle.bf16_to_f32(to_np(wb_ref, np.uint16))).reshape(E, -1).max(axis=1)
     assert np.array_equal(to_np(amax), want.astype(np.float32))
+
+
+def test_mxfp8_gemms_read_tile_layout_scales():
+    """MOE4_SF_MMA_LAYOUT on the MXFP8 GEMMs (operand scales already in the tensor-core tile
+    layout, as the producers write them with MOE4_SF_OUT_MMA): the same bits as from canonical
+    scales, for the rows-grouped dgrad and the contraction-grouped fused SGD."""
+    rng = np.random.default_rng(24)
+    sizes = [256, 0, 128, 384]
+    E, N, K = len(sizes), 512, 640
+    offs = to_dev(_offs(sizes))
+    M = int(sum(sizes))
+    aq, ae = _mxfp8_rowwise(_bf16(rng, (M, K)), M, K)
+    bq, be = _mxfp8_rowwise(_bf16(rng, (E * N, K), 0.02), E * N, K)
+    ae_t, be_t = mma_layout(ae, M, K // 32), mma_layout(be, E * N, K // 32)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, E, N, K))
+    D0 = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    D1 = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8(aq, ae, bq, be, offs, E, M, N, K, D0, moe4.OUT_F32 | moe4.GROUP_M, ws)
+    moe4.grouped_gemm_mxfp8(aq, ae_t, bq, be_t, offs, E, M, N, K, D1, moe4.OUT_F32 | moe4.GROUP_M | moe4.SF_MMA_LAYOUT,
+                            None)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    assert torch.equal(D0, D1)
+    # contraction-grouped with the fused update: A [Mw, Kt], B [Nw, Kt]
+    Mw, Nw, Kt = 256, 512, M
+    xq, xe = _mxfp8_rowwise(_bf16(rng, (Mw, Kt)), Mw, Kt)
+    yq, ye = _mxfp8_rowwise(_bf16(rng, (Nw, Kt)), Nw, Kt)
+    w0 = to_dev((rng.standard_normal((E, Mw, Nw)) * 0.02).astype(np.float32))
+    outs = []
+    for tile in (False, True):
+        w, wb = w0.clone(), torch.zeros((E, Mw, Nw), dtype=torch.int16, device=DEV)
+        amax = torch.empty(E, dtype=torch.float32, device=DEV)
+        a_e = mma_layout(xe, Mw, Kt // 32) if tile else xe
+        b_e = mma_layout(ye, Nw, Kt // 32) if tile else ye
+        gws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, Mw, 1, Nw, Kt))
+        moe4.grouped_gemm_mxfp8_wgrad_sgd(xq, a_e, yq, b_e, offs, E, Mw, Nw, Kt, w, wb, 1e-2, amax,
+                                          moe4.SF_MMA_LAYOUT if tile else 0, gws)
+        torch.cuda.synchronize()
+        assert moe4.moe4_get_status() == moe4.OK
+        outs.append((w, wb, amax))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from precision_moe_numerics_03_b300 import inputs, moe4
-from gpu_helpers import DEV, empty_u8, first_mismatch, nvfp4_quantize, to_dev, to_np
+from gpu_helpers import DEV, empty_u8, first_mismatch, mma_layout, nvfp4_quantize, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -150,6 +150,13 @@ def test_swiglu_backward_mxfp8_equals_unfused(rows, f):
     out, ref = _swiglu_bwd_mxfp8_both(gu, dh, rows, f)
     for a, b in zip(out, ref):
         assert torch.equal(a, b)
+    if rows % 128 == 0 and f % 64 == 0:
+        mma = [empty_u8(rows, 2 * f), empty_u8(rows, 2 * f // 32), empty_u8(2 * f, rows), empty_u8(2 * f, rows // 32)]
+        moe4.moe4_swiglu_backward_mxfp8(gu, dh, rows, f, *mma, flags=moe4.SF_OUT_MMA)
+        torch.cuda.synchronize()
+        assert torch.equal(mma[0], out[0]) and torch.equal(mma[2], out[2])
+        assert torch.equal(mma[1].reshape(-1), mma_layout(out[1], rows, 2 * f // 32))
+        assert torch.equal(mma[3].reshape(-1), mma_layout(out[3], 2 * f, rows // 32))
 
 
 def test_swiglu_backward_mxfp8_against_oracle():
@@ -200,6 +207,14 @@ def test_combine_backward_mxfp8_equals_unfused(T, E, k, d):
     torch.cuda.synchronize()
     for a, b in zip(out, ref):
         assert torch.equal(a, b)
+    if d % 128 == 0:
+        # MOE4_SF_OUT_MMA: the scales as the library's layout change of the canonical ones
+        mma = [empty_u8(R, d), empty_u8(R, d // 32), empty_u8(d, R), empty_u8(d, R // 32)]
+        moe4.moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, R, *mma, flags=moe4.SF_OUT_MMA)
+        torch.cuda.synchronize()
+        assert torch.equal(mma[0], out[0]) and torch.equal(mma[2], out[2])
+        assert torch.equal(mma[1].reshape(-1), mma_layout(out[1], R, d // 32))
+        assert torch.equal(mma[3].reshape(-1), mma_layout(out[3], d, R // 32))
 
 
 @pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (300, 16, 4)])

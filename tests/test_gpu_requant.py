@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from precision_moe_numerics_03_b300 import inputs, moe4
-from gpu_helpers import DEV, empty_u8, first_mismatch, nvfp4_quantize, to_dev, to_np
+from gpu_helpers import DEV, empty_u8, first_mismatch, mma_layout, nvfp4_quantize, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -177,3 +177,34 @@ def test_requant_reads_tensor_core_scale_layout():
     rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=True, seed=5, stream_id=1)
     assert first_mismatch(to_np(q2), rq) is None and first_mismatch(to_np(e2), re8) is None
     assert torch.equal(q1, q2) and torch.equal(e1, e2)
+
+
+@pytest.mark.parametrize("sr", [True, False])
+def test_requant_scales_in_tile_layout(sr):
+    """MOE4_SF_OUT_MMA: the same codes, and the scales as moe4_sf_to_mma_layout of the canonical
+    ones (the canonical output has its own parity tests); two matrices, so tiles of the scale
+    matrix [nmat * cols, rows / 32] follow on across the matrix boundary."""
+    nmat, rows, cols = 2, 384, 256
+    rng = np.random.default_rng(91)
+    x = inputs.to_bf16_bits(rng.standard_t(3, (nmat * rows, cols)).astype(np.float32))
+    c, s, g = nvfp4_quantize(to_dev(x), nmat, rows, cols)
+    base = moe4.SR if sr else 0
+    q0, e0 = _requant_gpu(c, s, g, nmat, rows, cols, 9, 2, sr)
+    q1, e1 = empty_u8(nmat, cols, rows), empty_u8(nmat, cols, rows // 32)
+    moe4.mxfp8_requant_transpose_sr(c, s, g, nmat, rows, cols, q1, e1, 9, 2, base | moe4.SF_OUT_MMA)
+    torch.cuda.synchronize()
+    assert torch.equal(q0, q1)
+    assert torch.equal(e1.reshape(-1), mma_layout(e0, nmat * cols, rows // 32))
+
+
+def test_rowcol_scales_in_tile_layout():
+    rows, cols = 384, 256
+    x = inputs.device_student_t((rows, cols), inputs.device_generator(92, 0, DEV), DEV).view(torch.int16)
+    ref = [empty_u8(rows, cols), empty_u8(rows, cols // 32), empty_u8(cols, rows), empty_u8(cols, rows // 32)]
+    moe4.mxfp8_quantize_rowcol(x, rows, cols, *ref)
+    out = [empty_u8(rows, cols), empty_u8(rows, cols // 32), empty_u8(cols, rows), empty_u8(cols, rows // 32)]
+    moe4.mxfp8_quantize_rowcol(x, rows, cols, *out, flags=moe4.SF_OUT_MMA)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], ref[0]) and torch.equal(out[2], ref[2])
+    assert torch.equal(out[1].reshape(-1), mma_layout(ref[1], rows, cols // 32))
+    assert torch.equal(out[3].reshape(-1), mma_layout(ref[3], cols, rows // 32))
