@@ -360,6 +360,19 @@ __device__ __forceinline__ int64_t sf_offset(int64_t row, int64_t blk, int64_t n
     return mma ? sf_mma_offset(row, blk, nblk) : row * nblk + blk;
 }
 
+// d0 = RN(lo(e2) * nsf + y0), d1 = RN(hi(e2) * nsf + y1): binary32 multiply-adds taking the two
+// f16 halves of e2 and the f16 nsf as exact operands.
+__device__ __forceinline__ void fma2_f16(uint32_t e2, uint16_t nsf, float y0, float y1, float &d0, float &d1) {
+    asm("{\n"
+        ".reg .b16 lo, hi;\n"
+        "mov.b32 {lo, hi}, %2;\n"
+        "fma.rn.f32.f16 %0, lo, %3, %4;\n"
+        "fma.rn.f32.f16 %1, hi, %3, %5;\n"
+        "}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(e2), "h"(nsf), "f"(y0), "f"(y1));
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

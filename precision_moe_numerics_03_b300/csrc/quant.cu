@@ -115,18 +115,15 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, con
         for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(y[2 * i], y[2 * i + 1]), r2), v[2 * i], v[2 * i + 1]);
         w0 = e2m1x8_rn(v);
         w1 = e2m1x8_rn(v + 8);
-        // d = y - e*sf: e*sf has at most 6 significant bits and is exact in binary32, so the fused
-        // form rounds once, exactly as the subtraction of the exact product does (packed pairs:
-        // the multiply-add feeds only the squares)
-        const uint64_t nsf2 = f2_pack(-sfv, -sfv);
+        // d = y - e*sf: e*sf has at most 6 significant bits and is exact, so the fused form rounds
+        // once, exactly as the subtraction of the exact product does.  e (E2M1) and -sf (E4M3)
+        // are exact in f16 and enter the binary32 multiply-add as f16 operands.
+        const uint16_t nsf = __half_as_ushort(__float2half_rn(-sfv));
         uint32_t eh[8];
         e2m1x8_to_h2x4(w0, eh);
         e2m1x8_to_h2x4(w1, eh + 4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float2 e = h2_bits_to_f2(eh[i]);
-            f2_unpack(f2_fma(f2_pack(e.x, e.y), nsf2, f2_pack(y[2 * i], y[2 * i + 1])), d[2 * i], d[2 * i + 1]);
-        }
+        for (int i = 0; i < 8; ++i) fma2_f16(eh[i], nsf, y[2 * i], y[2 * i + 1], d[2 * i], d[2 * i + 1]);
     }
     float s[16];
 #pragma unroll
