@@ -46,7 +46,7 @@ METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
-TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2700.3 / 2753.6}
+TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.6 / 2216.7}
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 4, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
 
 
@@ -167,9 +167,11 @@ class LayerStep:
         n += 3
         with tm("quant_w"):
             GIVEN = m.AMAX_GIVEN
-            m.nvfp4_quantize(self.Wb_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.amax_gu,
-                             FOS | MMA | GIVEN)
-            m.nvfp4_quantize(self.Wb_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, self.amax_d, FOS | MMA | GIVEN)
+            # the FP32 master weights, rounded to bf16 as they are read (no stored bf16 copy)
+            m.nvfp4_quantize_f32(self.W32_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.amax_gu,
+                                 FOS | MMA | GIVEN)
+            m.nvfp4_quantize_f32(self.W32_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, self.amax_d,
+                                 FOS | MMA | GIVEN)
         n += 2
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
@@ -207,7 +209,7 @@ class LayerStep:
         n += 1
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dYc_q, self.dYc_e, self.HqT_q, self.HqT_e, self.offs, E, d, f, Rp,
-                                           self.W32_d, self.Wb_d, LR, self.amax_d, MMA, self.gws)
+                                           self.W32_d, None, LR, self.amax_d, MMA, self.gws)
         n += 2  # the expert ranking for the tile schedule, the GEMM
         with tm("swiglu_bwd"):
             m.moe4_swiglu_backward(self.GU[:Rp], self.dH[:Rp], Rp, f, self.dGU[:Rp])
@@ -227,7 +229,7 @@ class LayerStep:
         n += 1
         with tm("gemm_mxfp8_wgrad_sgd"):
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d,
-                                           Rp, self.W32_gu, self.Wb_gu, LR, self.amax_gu, MMA, self.gws)
+                                           Rp, self.W32_gu, None, LR, self.amax_gu, MMA, self.gws)
         n += 2
         self.launches += n
         return n
@@ -242,7 +244,7 @@ class LayerStep:
         mx = 1.03125      # MXFP8 bytes per value (E4M3 + E8M0 per 32)
         w_gu, w_d = E * 2 * f * d, E * d * f
         b = {}
-        b["quant_w"] = (w_gu + w_d) * (2 + nv)                           # amax comes from the SGD epilogue
+        b["quant_w"] = (w_gu + w_d) * (4 + nv)                           # FP32 read; amax from the SGD epilogue
         b["quant_x"] = T * d * (2 + 2 + nv) + rows * d * nv * 2          # + gather read/write
         b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
                            rows * f * nv + live * d * f * nv + rows * d * 2)
@@ -252,9 +254,9 @@ class LayerStep:
         b["mxfp8_quant"] = rows * d * 2 * mx + T * d * 2 + rows * 2 * f * (2 + 2 * mx)
         b["gemm_mxfp8_dgrad"] = (rows * d * mx + live * f * d * mx + rows * f * 4 +          # down
                                  rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2)   # gate/up
-        # wgrad operands + the SGD epilogue: read W32, write W32 and the bf16 copy
+        # wgrad operands + the SGD epilogue: read W32, write W32 (the bf16 copy is not stored)
         b["gemm_mxfp8_wgrad_sgd"] = (rows * d * mx + rows * f * mx + rows * 2 * f * mx + rows * d * mx +
-                                     (w_gu + w_d) * (4 + 4 + 2))
+                                     (w_gu + w_d) * (4 + 4))
         b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 * 2 + rows * f * (2 + nv)
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
         b["hadamard"] = rows * d * (2 + 2 + nv + nv + 2)
@@ -270,6 +272,9 @@ def measure_next_rows(step, reps=3):
     down with SwiGLU between them), and the 8.25-bit Hadamard + MXFP8 return-path codec."""
     torch, m = step.torch, step.m
     T, d, f, E, k, Rp, dev = step.T, step.d, step.f, step.E, step.k, step.Rp, step.dev
+    # the final layers' forward reads bf16 weights: refresh the copies from the updated FP32 masters
+    m.moe4_convert(2, step.W32_gu, step.W32_gu.numel(), step.Wb_gu)
+    m.moe4_convert(2, step.W32_d, step.W32_d.numel(), step.Wb_d)
     u8 = dict(dtype=torch.uint8, device=dev)
     Xq, Xe = torch.empty((T, d), **u8), torch.empty((T, d // 32), **u8)
     Xpq, Xpe = torch.empty((Rp, d), **u8), torch.empty((Rp, d // 32), **u8)
@@ -596,8 +601,10 @@ def profile_case(name):
         quant = lambda: moe4.nvfp4_quantize(w, E, 2 * f, d, d, c, s_, gd, None,
                                             moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT, ws)
         quant()
-        if name == "quant_w":
-            calls.append(quant)
+        if name == "quant_w":  # as in the layer step: the FP32 master weights
+            w32 = inputs.device_normal((E * 2 * f, d), 0.02, g(8), dev, dtype=torch.float32)
+            calls.append(lambda: moe4.nvfp4_quantize_f32(w32, E, 2 * f, d, d, c, s_, gd, None,
+                                                         moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT, ws))
         elif name == "requant":
             q, e8 = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
             calls.append(lambda: moe4.mxfp8_requant_transpose_sr(c, s_, gd, E, 2 * f, d, q, e8, 1, 3,
@@ -654,10 +661,9 @@ def profile_case(name):
             if name == "gemm_mxfp8_wgrad":
                 calls.append(lambda: moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, M, N, rows, out,
                                                              moe4.OUT_F32 | moe4.GROUP_K, ws))
-            else:
-                wb = out.to(torch.bfloat16).view(torch.int16)
+            else:  # as in the layer step: no stored bf16 copy
                 amax = torch.empty(E, dtype=torch.float32, device=dev)
-                calls.append(lambda: moe4.grouped_gemm_mxfp8_wgrad_sgd(a, ae, b, be, offs, E, M, N, rows, out, wb,
+                calls.append(lambda: moe4.grouped_gemm_mxfp8_wgrad_sgd(a, ae, b, be, offs, E, M, N, rows, out, None,
                                                                        LR, amax, 0, ws))
         else:
             N, K = d, 2 * f

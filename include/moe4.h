@@ -114,6 +114,15 @@ int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, 
                    uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
                    uint32_t flags, void *ws, size_t ws_bytes, void *stream);
 
+/* nvfp4_quantize_f32: the same quantiser reading binary32 x [nmat, rows, ld] (ld % 4 == 0): each
+ * value is rounded to bf16 (nearest-even) as it is read, so the outputs equal those of
+ * nvfp4_quantize on the bf16 copy of x, byte for byte, and amax_m is max |bf16(x)|.  For FP32
+ * master weights whose bf16 copy is never stored (grouped_gemm_mxfp8_wgrad_sgd with
+ * w_bf16 = NULL): 4 bytes read per value instead of 2 written and 2 read. */
+int nvfp4_quantize_f32(const float *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                       uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
+                       uint32_t flags, void *ws, size_t ws_bytes, void *stream);
+
 /* nvfp4_quantize_noalloc: the same quantisation as nvfp4_quantize (amax computed here, flags
  * MOE4_FOUR_OVER_SIX and MOE4_SF_MMA_LAYOUT only), for callers that cannot allocate device
  * memory: a host runtime that plans all of its device memory when it starts and allows no
@@ -247,7 +256,8 @@ int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
  * take MOE4_AMAX_GIVEN).  Bit-identical to grouped_gemm_mxfp8(MOE4_GROUP_K | MOE4_OUT_F32)
  * followed by moe4_sgd_update.  A [M, K], B [N, K], w32 / w_bf16 [E, M, N]; M % 128 == 0,
  * N % 256 == 0, K % 128 == 0; offs as for grouped_gemm_mxfp8 (offs[E] = K).  Experts with no rows
- * keep their weights (and still report their amax).  flags: MOE4_SF_MMA_LAYOUT or 0 (canonical
+ * keep their weights (and still report their amax).  w_bf16 may be NULL: the bf16 copy is then
+ * not written, amax_out is unchanged (for nvfp4_quantize_f32 of w32).  flags: MOE4_SF_MMA_LAYOUT or 0 (canonical
  * scales are converted into ws, moe4_workspace_size_gemm(1, M, 1, N, K) bytes). */
 int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
                                  const uint8_t *b_e8, const int32_t *group_offs, int64_t E,

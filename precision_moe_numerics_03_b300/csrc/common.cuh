@@ -34,6 +34,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
+// bf16(lo) | bf16(hi) << 16, both nearest-even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 
 // ------------------------------------------------------------------ FP4 / FP8 conversions
 // Eight binary32 values -> eight E2M1 codes packed into a 32-bit word (element i in nibble i),

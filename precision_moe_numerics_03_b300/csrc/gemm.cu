@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
                 const float lr = p.lr;
+                const bool with_bf16 = p.w_bf16 != nullptr;  // else only the amax of the bf16 values
                 uint32_t amax2 = 0;
                 bool ok = true;
 #pragma unroll 1
@@ -598,16 +599,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                         amax2 = __vmaxu2(amax2, pk[2 * j] & 0x7FFF7FFFu);
                         amax2 = __vmaxu2(amax2, pk[2 * j + 1] & 0x7FFF7FFFu);
                     }
+                    if (with_bf16) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 2) & 1)) << 4)) =
-                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int j = 0; j < 2; ++j)
+                            *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 2) & 1)) << 4)) =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         if (live) {
                             tma_store_2d(&tmW, wring + buf * SGD_W_CHUNK, x0 + SGD_CW * c, y0);
-                            tma_store_2d(&tmWb, bring + buf * SGD_B_CHUNK, x0 + SGD_CW * c, y0);
+                            if (with_bf16) tma_store_2d(&tmWb, bring + buf * SGD_B_CHUNK, x0 + SGD_CW * c, y0);
                         }
                         bulk_commit();  // one group per chunk, empty or not, so group counts match chunks
                     }
@@ -1083,7 +1086,7 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
                                             float *amax_out, uint32_t flags, void *ws, size_t ws_bytes,
                                             void *stream) {
     MOE4_CHECK_ARG(E >= 1 && M >= 0 && M % BM == 0 && N > 0 && N % BN == 0 && K >= 0 && K % 128 == 0);
-    MOE4_CHECK_ARG(a && a_e8 && b && b_e8 && group_offs && w32 && w_bf16 && amax_out);
+    MOE4_CHECK_ARG(a && a_e8 && b && b_e8 && group_offs && w32 && amax_out);
     MOE4_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(a_e8) && aligned16(b_e8) && aligned16(w32) &&
                    aligned16(w_bf16) && aligned4(amax_out));
     MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
@@ -1132,8 +1135,12 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     g.sfa_tile_stride = K / 128;
     g.sfb_tile_stride = K / 128;
     CUtensorMap tw, twb;  // the master weights and their bf16 copy as [E*M, N], 16-column x 32-row boxes
-    if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_32B))
+    if (!make_map_t(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w32, N, E * M, SGD_CW, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MOE4_ERR_CUDA;
+    if (!w_bf16)
+        twb = tw;  // never used: the bf16 copy is not written
+    else if (!make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, SGD_CW, 32,
+                         CU_TENSOR_MAP_SWIZZLE_32B))
         return MOE4_ERR_CUDA;
     return launch<1, EPI_SGD>(ta, tb, tw, twb, g, st);
 }

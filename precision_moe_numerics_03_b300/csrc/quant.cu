@@ -30,11 +30,24 @@ int num_sms() {
 // ------------------------------------------------------------------ amax pass
 // Per matrix: max |x| over bf16 values, as binary32 bits (non-negative floats order as unsigned
 // integers), folded into amax_bits[m] with one atomicMax per block.
-__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t *__restrict__ x, int64_t rows,
+// Eight consecutive values as four bf16 pairs (element 2i in the low half of word i): bf16 input
+// as stored, binary32 input rounded to bf16 (nearest-even) first.
+template <typename TIn>
+__device__ __forceinline__ uint4 load8_bf16(const TIn *p) {
+    if constexpr (sizeof(TIn) == 2) {
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        return make_uint4(bf16x2_rn(a.x, a.y), bf16x2_rn(a.z, a.w), bf16x2_rn(b.x, b.y), bf16x2_rn(b.z, b.w));
+    }
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const TIn *__restrict__ x, int64_t rows,
                                                         int64_t cols, int64_t ld, int64_t mat_stride,
                                                         unsigned int *__restrict__ amax_bits) {
     const int m = blockIdx.y;
-    const uint16_t *xm = x + (int64_t)m * mat_stride;
+    const TIn *xm = x + (int64_t)m * mat_stride;
     const int64_t vec_per_row = cols / 8;
     const int64_t nvec = rows * vec_per_row;
     uint32_t best = 0;  // two packed bf16 magnitudes
@@ -42,7 +55,7 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t *__restri
          v += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = (ld == cols) ? 0 : v / vec_per_row;
         const int64_t c = (ld == cols) ? v * 8 : (v - r * vec_per_row) * 8;
-        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(xm + r * ld + c));
+        const uint4 q = load8_bf16(xm + r * ld + c);
         best = __vmaxu2(best, q.x & 0x7FFF7FFFu);
         best = __vmaxu2(best, q.y & 0x7FFF7FFFu);
         best = __vmaxu2(best, q.z & 0x7FFF7FFFu);
@@ -156,8 +169,9 @@ __device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_si
 // The block index b runs over all matrices; with contiguous rows (ld == cols) the input, code and
 // canonical-scale offsets are b*16, b*8 and b, and the matrix index only moves forward in the
 // grid-stride loop, so no division is needed on that path.
+template <typename TIn>
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
-    const uint16_t *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+    const TIn *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
     float *__restrict__ g_dec, uint32_t div_m, uint32_t div_s) {
@@ -192,9 +206,8 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
             row = (int64_t)((uint32_t)rem / (uint32_t)nblk);
             blk = rem - row * nblk;
         }
-        const uint16_t *srcp = contiguous ? x + b * 16 : x + m * mat_stride + row * ld + blk * 16;
-        const uint4 *src = reinterpret_cast<const uint4 *>(srcp);
-        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+        const TIn *srcp = contiguous ? x + b * 16 : x + m * mat_stride + row * ld + blk * 16;
+        const uint4 q0 = load8_bf16(srcp), q1 = load8_bf16(srcp + 8);
         const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         // packed products: y feeds the amax, a product and the addend of an FMA, never an add
         float y[16];
@@ -444,10 +457,12 @@ static int grid_for(int64_t work_items, int threads, int per_sm) {
 
 using namespace moe4;
 
-extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
-                              uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
-                              uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
-    MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0 && ld >= cols && ld % 8 == 0);
+template <typename TIn>
+static int nvfp4_quantize_impl(const TIn *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld, uint8_t *codes,
+                               uint8_t *sf, float *g_dec, const float *amax_in, uint32_t flags, void *ws,
+                               size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0 && ld >= cols &&
+                   (ld * (int64_t)sizeof(TIn)) % 16 == 0);
     MOE4_CHECK_ARG(g_dec);
     MOE4_CHECK_ARG(rows == 0 || (x && codes && sf && aligned16(x) && aligned16(codes)));
     MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_AMAX_GIVEN | MOE4_SF_MMA_LAYOUT)) == 0);
@@ -469,17 +484,29 @@ extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int
             const int64_t per_mat_cap = ((int64_t)num_sms() * 8 + nmat - 1) / nmat;
             if (gx > per_mat_cap) gx = (int)per_mat_cap;
             if (gx < 1) gx = 1;
-            amax_bf16_kernel<<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
+            amax_bf16_kernel<TIn><<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
         }
     }
     const int64_t total = nmat * rows * (cols / 16);
     const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
     uint32_t div_m = 0, div_s = 0;
     if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
-    nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, given ? amax_in : nullptr,
-                                             amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf,
-                                             g_dec, div_m, div_s);
+    nvfp4_quant_kernel<TIn><<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, given ? amax_in : nullptr,
+                                                  amax_bits, (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf,
+                                                  g_dec, div_m, div_s);
     return launch_status();
+}
+
+extern "C" int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                              uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
+                              uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    return nvfp4_quantize_impl(x, nmat, rows, cols, ld, codes, sf, g_dec, amax_in, flags, ws, ws_bytes, stream);
+}
+
+extern "C" int nvfp4_quantize_f32(const float *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
+                                  uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
+                                  uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    return nvfp4_quantize_impl(x, nmat, rows, cols, ld, codes, sf, g_dec, amax_in, flags, ws, ws_bytes, stream);
 }
 
 extern "C" int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec, int64_t nmat,
@@ -582,13 +609,13 @@ extern "C" int nvfp4_quantize_noalloc(const uint16_t *x, int64_t nmat, int64_t r
         const int64_t per_mat_cap = ((int64_t)num_sms() * 8 + nmat - 1) / nmat;
         if (gx > per_mat_cap) gx = (int)per_mat_cap;
         if (gx < 1) gx = 1;
-        amax_bf16_kernel<<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
+        amax_bf16_kernel<uint16_t><<<dim3(gx, (unsigned)nmat), 256, 0, st>>>(x, rows, cols, ld, rows * ld, amax_bits);
     }
     const int64_t total = nmat * rows * (cols / 16);
     const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
     uint32_t div_m = 0, div_s = 0;
     if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
-    nvfp4_quant_kernel<<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, nullptr, amax_bits,
+    nvfp4_quant_kernel<uint16_t><<<grid, 256, 0, st>>>(x, nmat, rows, cols, ld, rows * ld, nullptr, amax_bits,
                                              (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, codes, sf, g_dec, div_m,
                                              div_s);
     return launch_status();

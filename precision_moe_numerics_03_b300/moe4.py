@@ -49,6 +49,7 @@ _SIGNATURES = {
     "moe4_get_status": (_int, [_vp]),
     "moe4_selftest_wait": (_int, [_i64, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
+    "nvfp4_quantize_f32": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
     "mxfp8_requant_transpose_sr": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
@@ -165,6 +166,12 @@ def workspace(nbytes: int, device="cuda") -> torch.Tensor:
 def nvfp4_quantize(x, nmat, rows, cols, ld, codes, sf, g_dec, amax_in=None, flags=FOUR_OVER_SIX, ws=None,
                    stream=None):
     _call("nvfp4_quantize", _p(x), nmat, rows, cols, ld, _p(codes), _p(sf), _p(g_dec), _p(amax_in), flags,
+          _p(ws), _ws_bytes(ws), _s(stream))
+
+
+def nvfp4_quantize_f32(x, nmat, rows, cols, ld, codes, sf, g_dec, amax_in=None, flags=FOUR_OVER_SIX, ws=None,
+                       stream=None):
+    _call("nvfp4_quantize_f32", _p(x), nmat, rows, cols, ld, _p(codes), _p(sf), _p(g_dec), _p(amax_in), flags,
           _p(ws), _ws_bytes(ws), _s(stream))
 
 

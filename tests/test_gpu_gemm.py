@@ -212,6 +212,13 @@ def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd(sizes, M, N):
     assert torch.equal(wb_f, wb_ref)
     want = np.abs(oracle.bf16_to_f32(to_np(wb_ref, np.uint16))).reshape(E, -1).max(axis=1)
     assert np.array_equal(to_np(amax), want.astype(np.float32))
+    # without a bf16 copy: the same master weights and amax
+    w_n = to_dev(w0)
+    amax_n = torch.full((E,), -1.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8_wgrad_sgd(aq, ae, bq, be, to_dev(offs), E, M, N, Kt, w_n, None, lr, amax_n, 0, ws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    assert torch.equal(w_n, w_ref) and torch.equal(amax_n, amax)
 
 
 def test_mxfp8_gemms_read_tile_layout_scales():

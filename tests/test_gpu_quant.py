@@ -340,3 +340,38 @@ def test_full_tensor_parity_small_moe_operands():
     b = inputs.to_bf16_bits((rng.standard_normal((8 * 2048, 2048)) * 0.02).astype(np.float32))
     _check_quant(a, 1, 8704, 2048)
     _check_quant(b, 8, 2048, 2048)
+
+
+@pytest.mark.parametrize("given,mma,ld", [(False, False, 256), (True, True, 256), (False, True, 260)])
+def test_quantize_f32_equals_quantize_of_bf16_copy(given, mma, ld):
+    """nvfp4_quantize_f32 rounds each binary32 value to bf16 as it reads it: its outputs equal the
+    oracle's quantisation of the oracle's bf16 rounding of the same values (ties to even included:
+    some values sit exactly halfway between two bf16 numbers), with or without a given amax, in
+    both scale layouts, with padded rows."""
+    nmat, rows, cols = 3, 128, 256
+    rng = np.random.default_rng(61)
+    x = (rng.standard_normal((nmat, rows, cols)) * np.array([0.02, 1.0, 30.0])[:, None, None]).astype(np.float32)
+    bits = x.view(np.uint32)
+    tie = rng.random(x.shape) < 0.05            # force the 16 dropped bits to exactly one half
+    bits[tie] = (bits[tie] & 0xFFFF0000) | 0x8000
+    xb = oracle.f32_to_bf16(x)                    # the bf16 copy, nearest-even
+    amax = np.abs(oracle.bf16_to_f32(xb)).reshape(nmat, -1).max(axis=1).astype(np.float32)
+    xpad = np.zeros((nmat, rows, ld), np.float32)
+    xpad[:, :, :cols] = x
+    c, s = empty_u8(nmat, rows, cols // 2), empty_u8(nmat, rows, cols // 16)
+    g = torch.empty(nmat, dtype=torch.float32, device=DEV)
+    flags = moe4.FOUR_OVER_SIX | (moe4.AMAX_GIVEN if given else 0) | (moe4.SF_MMA_LAYOUT if mma else 0)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, nmat))
+    moe4.nvfp4_quantize_f32(to_dev(xpad), nmat, rows, cols, ld, c, s, g, to_dev(amax) if given else None, flags, ws)
+    torch.cuda.synchronize()
+    rc, rs, rg = oracle.nvfp4_quantize(oracle.bf16_to_f32(xb))
+    assert first_mismatch(to_np(g), rg) is None
+    assert first_mismatch(to_np(c), rc) is None
+    s_np = to_np(s)
+    if mma:
+        s2 = empty_u8(nmat, rows, cols // 16)
+        moe4.moe4_sf_to_mma_layout(to_dev(rs), nmat, rows, cols // 16, s2)
+        torch.cuda.synchronize()
+        assert np.array_equal(s_np, to_np(s2))
+    else:
+        assert first_mismatch(s_np, rs) is None
