@@ -105,20 +105,25 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
     }
 }
 
-// The row-wise MXFP8 of the 32 values a thread holds in phase 1 (one block along the row),
-// nearest-even: written to q_r [R, C] and e8_r [R, C/32] when the kernel also emits that layout.
-__device__ __forceinline__ void emit_rowwise32(const float v[32], int64_t r, int64_t c, int64_t C,
+// The row-wise MXFP8 of the 32 bf16 values a thread holds in phase 1 (one block along the row,
+// h[i] = elements 2i, 2i+1), nearest-even: written to q_r [R, C] and e8_r [R, C/32] (canonical or
+// tile layout) when the kernel also emits that layout.  The amax is taken on the packed pairs.
+__device__ __forceinline__ void emit_rowwise32(const uint32_t h[16], int64_t r, int64_t c, int64_t C,
                                                uint8_t *__restrict__ q_r, uint8_t *__restrict__ e8_r, bool e8_mma) {
-    float a = 0.0f;
+    uint32_t mx = max_abs16x2<false>(h[0], h[1]);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
-    const uint32_t fs = mx_scale_fs(a);
+    for (int i = 2; i < 16; ++i) mx = max_abs16x2<false>(mx, h[i]);
+    const uint32_t fs = mx_scale_fs(fmaxf(fabsf(bf16_lo(mx)), fabsf(bf16_hi(mx))));
     const float s = mx_inv_scale_fs(fs);
+    const uint64_t s2 = f2_pack(s, s);
     uint32_t w[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        w[j] = e4m3x4_rn(__fmul_rn(v[4 * j], s), __fmul_rn(v[4 * j + 1], s), __fmul_rn(v[4 * j + 2], s),
-                         __fmul_rn(v[4 * j + 3], s));
+    for (int j = 0; j < 8; ++j) {
+        float v0, v1, v2, v3;
+        f2_unpack(f2_mul(f2_pack(bf16_lo(h[2 * j]), bf16_hi(h[2 * j])), s2), v0, v1);
+        f2_unpack(f2_mul(f2_pack(bf16_lo(h[2 * j + 1]), bf16_hi(h[2 * j + 1])), s2), v2, v3);
+        w[j] = e4m3x4_rn(v0, v1, v2, v3);
+    }
     uint4 *dst = reinterpret_cast<uint4 *>(q_r + r * C + c);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -214,9 +219,27 @@ requant_transpose_kernel(
             } else if constexpr (kind == SrcKind::CombineBwd) {
                 const int32_t tok = __ldg(src_of + r);
                 float wj = 0.0f;
-                if (tok >= 0)
-                    for (int j = 0; j < topk; ++j)
-                        if (__ldg(row_of + (int64_t)tok * topk + j) == (int32_t)r) wj = __ldg(wts + (int64_t)tok * topk + j);
+                if (tok >= 0) {
+                    // the routing slot of row r: its k row indices and weights are loaded together
+                    // (16-byte loads when k % 4 == 0 and both arrays are 16-byte aligned), so the
+                    // dy loads below wait on src_of only
+                    const int64_t base = (int64_t)tok * topk;
+                    const bool vec = (topk & 3) == 0 &&
+                                     ((reinterpret_cast<uintptr_t>(row_of) | reinterpret_cast<uintptr_t>(wts)) & 15u) == 0;
+                    if (vec) {
+                        for (int j = 0; j < topk; j += 4) {
+                            const int4 ro = __ldg(reinterpret_cast<const int4 *>(row_of + base + j));
+                            const float4 wv = __ldg(reinterpret_cast<const float4 *>(wts + base + j));
+                            wj = ro.x == (int32_t)r ? wv.x : wj;
+                            wj = ro.y == (int32_t)r ? wv.y : wj;
+                            wj = ro.z == (int32_t)r ? wv.z : wj;
+                            wj = ro.w == (int32_t)r ? wv.w : wj;
+                        }
+                    } else {
+                        for (int j = 0; j < topk; ++j)
+                            if (__ldg(row_of + base + j) == (int32_t)r) wj = __ldg(wts + base + j);
+                    }
+                }
                 const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (int64_t)(tok < 0 ? 0 : tok) * C + c);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -227,15 +250,7 @@ requant_transpose_kernel(
                         h[4 * q + i] = (uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_lo(ws[i]))) |
                                        ((uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_hi(ws[i]))) << 16);
                 }
-                if constexpr (kRow) {
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        v[2 * i] = bf16_lo(h[i]);
-                        v[2 * i + 1] = bf16_hi(h[i]);
-                    }
-                    emit_rowwise32(v, r, c, C, q_r, e8_r, e8_mma);
-                }
+                if constexpr (kRow) emit_rowwise32(h, r, c, C, q_r, e8_r, e8_mma);
             } else {
                 const uint4 *src = reinterpret_cast<const uint4 *>(xbf + (m * R + r) * C + c);
 #pragma unroll
@@ -246,15 +261,7 @@ requant_transpose_kernel(
                     h[4 * q + 2] = w.z;
                     h[4 * q + 3] = w.w;
                 }
-                if constexpr (kRow) {
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        v[2 * i] = bf16_lo(h[i]);
-                        v[2 * i + 1] = bf16_hi(h[i]);
-                    }
-                    emit_rowwise32(v, r, c, C, q_r, e8_r, e8_mma);
-                }
+                if constexpr (kRow) emit_rowwise32(h, r, c, C, q_r, e8_r, e8_mma);
             }
         } else {
 #pragma unroll
@@ -280,14 +287,10 @@ requant_transpose_kernel(
         const int half = threadIdx.x >> 7;
         const int64_t r = r0 + rl;
         if (r < R) {
-            float v[32];
+            uint32_t hw[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t wv = tile[half * 16 + i][rl];
-                v[2 * i] = bf16_lo(wv);
-                v[2 * i + 1] = bf16_hi(wv);
-            }
-            emit_rowwise32(v, r, out_col(half * 32), C, q_r, e8_r, e8_mma);
+            for (int i = 0; i < 16; ++i) hw[i] = tile[half * 16 + i][rl];
+            emit_rowwise32(hw, r, out_col(half * 32), C, q_r, e8_r, e8_mma);
         }
     }
 
