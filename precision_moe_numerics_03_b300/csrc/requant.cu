@@ -139,7 +139,7 @@ __device__ __forceinline__ void emit_rowwise32(const uint32_t h[16], int64_t r, 
 constexpr int kPairs = kTileC / 2;
 
 template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true>
-__global__ void __launch_bounds__(256, (kSR || kRow || kind == SrcKind::SwigluBwd || kind == SrcKind::CombineBwd) ? 4 : 5)
+__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 : 5)
 requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
