@@ -36,7 +36,7 @@ enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 template <SrcKind kind, bool kSR, bool kJ32>
 __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int64_t m, int64_t cA, int64_t r0,
                                           int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t (*e8s)[4], int cl,
-                                          const PhiloxKeys keys, uint32_t stream_id) {
+                                          const PhiloxKeys keys, uint32_t stream_id, bool safe) {
     constexpr bool kF16 = kind == SrcKind::Nvfp4;
     const int lane = lane_id();
     uint32_t mx = max_abs16x2<kF16>(max_abs16x2<kF16>(p.x, p.y), max_abs16x2<kF16>(p.z, p.w));
@@ -83,8 +83,11 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
             wa = sr_words4_not(j, stream_id, keys);
             wb = sr_words4_not(j + (uint64_t)(R >> 2), stream_id, keys);
         }
-        // one branch for the eight values (the per-element path is rare)
-        if (min(sr_fast_key4(va[0], va[1], va[2], va[3]), sr_fast_key4(vb[0], vb[1], vb[2], vb[3])) >= kSrFastMin) {
+        if (safe) {  // the tile's scales rule out non-zero values below 2^-6 (see the kernel)
+            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], wa);
+            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], wb);
+        } else if (min(sr_fast_key4(va[0], va[1], va[2], va[3]), sr_fast_key4(vb[0], vb[1], vb[2], vb[3])) >=
+                   kSrFastMin) {  // one test for the eight values (the per-element path is rare)
             qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], wa);
             qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], wb);
         } else {
@@ -158,6 +161,11 @@ requant_transpose_kernel(
     // input column (output row) of tile column cl
     auto out_col = [&](int cl) -> int64_t { return kSwb ? (cl < 32 ? c0 + cl : f + c0 + (cl - 32)) : c0 + cl; };
 
+    // NVFP4 source with stochastic rounding: the smallest non-zero and the largest block scale of
+    // the tile (f16 bits), reduced over the CTA (see `safe` below)
+    constexpr bool kScaleRange = kSR && kind == SrcKind::Nvfp4;
+    __shared__ uint32_t sf_red[2][8];
+    uint32_t sf_lo = 0x7C00u, sf_hi = 0u;
     // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
     {
         const int rl = threadIdx.x & (kTileR - 1);
@@ -175,6 +183,11 @@ requant_transpose_kernel(
                                             : (m * R + r) * nblk + b;
                 const uint32_t sf2 = e4m3x2_to_h2(__ldg(reinterpret_cast<const uint16_t *>(sf + soff)));
                 const uint32_t sfa2 = __byte_perm(sf2, 0, 0x1010), sfb2 = __byte_perm(sf2, 0, 0x3232);
+                if constexpr (kScaleRange) {
+                    const uint32_t sa = sf2 & 0xFFFFu, sb = sf2 >> 16;
+                    sf_lo = min(sa ? sa : 0x7C00u, sb ? sb : 0x7C00u);
+                    sf_hi = max(sa, sb);
+                }
                 const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -278,8 +291,32 @@ requant_transpose_kernel(
 #pragma unroll
             for (int i = 0; i < 16; ++i) tile[half * 16 + i][rl] = h[i];
         }
+        if constexpr (kScaleRange) {
+            sf_lo = __reduce_min_sync(0xFFFFFFFFu, sf_lo);
+            sf_hi = __reduce_max_sync(0xFFFFFFFFu, sf_hi);
+            if (lane_id() == 0) {
+                sf_red[0][warp_id()] = sf_lo;
+                sf_red[1][warp_id()] = sf_hi;
+            }
+        }
     }
     __syncthreads();
+    // safe: every non-zero value of the tile reaches at least 2^-6 after the MXFP8 scaling, so
+    // the stochastic rounding needs no per-value test.  A non-zero value is e*sf with |e| >= 1/2,
+    // and each 32-block's amax is at most 6 * sf_max * g (to within one rounding), so with
+    // 2^-e > 224 / amax a value lands at |v| >= (sf_min / sf_max) * (112 / 6) * (1 - 2^-23), which
+    // is above 2^-6 for sf_max <= 1024 * sf_min; 0.5 * sf_min * g >= 2^-100 keeps every product
+    // normal and the scale exponent unclamped.  An all-zero tile is safe too.
+    bool safe = false;
+    if constexpr (kScaleRange) {
+        const int ln = lane_id();
+        const uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, ln < 8 ? sf_red[0][ln] : 0x7C00u);
+        const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, ln < 8 ? sf_red[1][ln] : 0u);
+        const float lo_f = __half2float(__ushort_as_half((unsigned short)lo));
+        const float hi_f = __half2float(__ushort_as_half((unsigned short)hi));
+        const float gd = __ldg(g_dec + m);
+        safe = lo == 0x7C00u || (hi_f <= lo_f * 1024.0f && 0.5f * lo_f * gd >= 0x1p-100f);
+    }
     if constexpr (kSwb && kRow) {
         // the row-wise MXFP8 block of row r: gate columns (half 0) or up columns (half 1), read
         // back from one column of the transposed tile
@@ -301,7 +338,7 @@ requant_transpose_kernel(
         const int cp = warp_id() + 8 * i;
         const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cp][4 * lane_id()]);
         const int64_t cA = out_col(2 * cp);
-        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8s, 2 * cp, keys, stream_id);
+        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8s, 2 * cp, keys, stream_id, safe);
     }
     // scale codes: one thread per output row, its (up to) four blocks of this tile; the four are
     // adjacent bytes in both layouts (a whole word when R % 128 == 0)

@@ -208,3 +208,24 @@ def test_rowcol_scales_in_tile_layout():
     assert torch.equal(out[0], ref[0]) and torch.equal(out[2], ref[2])
     assert torch.equal(out[1].reshape(-1), mma_layout(ref[1], rows, cols // 32))
     assert torch.equal(out[3].reshape(-1), mma_layout(ref[3], cols, rows // 32))
+
+
+@pytest.mark.parametrize("sr", [True, False])
+def test_requant_rows_of_very_different_scale(sr):
+    """Every seventh input row is 10^-4 times smaller: its NVFP4 block scales sit more than 2^10
+    below the others in the same tile, so after the MXFP8 scaling some of its values fall below
+    2^-6 and round into the E4M3 subnormals (the per-value path of the stochastic rounding);
+    tiles without such rows take the tile-wide fast path."""
+    nmat, rows, cols = 2, 256, 128
+    rng = np.random.default_rng(71)
+    base = rng.standard_t(3, (nmat, rows, cols))
+    base[:, ::7, :] *= 1e-4
+    x = inputs.to_bf16_bits(base.astype(np.float32)).reshape(nmat * rows, cols)
+    c, s, g = nvfp4_quantize(to_dev(x), nmat, rows, cols)
+    q, e8 = _requant_gpu(c, s, g, nmat, rows, cols, 11, 3, sr)
+    oc, os_, og = oracle.nvfp4_quantize(oracle.bf16_to_f32(x).reshape(nmat, rows, cols))
+    rq, re8 = oracle.mxfp8_requant_transpose(oc, os_, og, sr=sr, seed=11, stream_id=3)
+    sub = ((rq & 0x78) == 0) & ((rq & 0x07) != 0)
+    assert sub.sum() > 1000  # the E4M3 subnormal range is exercised
+    assert first_mismatch(to_np(e8), re8) is None
+    assert first_mismatch(to_np(q), rq) is None
