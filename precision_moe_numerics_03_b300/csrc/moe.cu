@@ -200,27 +200,31 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ g
 // h = silu(g) * u:  du = dh * silu(g),  dg = dh * u * s * (1 + g * (1 - s)) with s = 1/(1+exp(-g)).
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const float *__restrict__ gu, const float *__restrict__ dh,
                                                          int64_t rows, int64_t f, uint16_t *__restrict__ dgu) {
-    const int64_t quads = rows * f / 4;
-    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = (q * 4) / f;
-        const int64_t c = q * 4 - r * f;
-        const float4 g = __ldg(reinterpret_cast<const float4 *>(gu + r * 2 * f + c));
-        const float4 u = __ldg(reinterpret_cast<const float4 *>(gu + r * 2 * f + f + c));
-        const float4 d = __ldg(reinterpret_cast<const float4 *>(dh + r * f + c));
-        const float gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w}, ds[4] = {d.x, d.y, d.z, d.w};
-        uint32_t og[2] = {0, 0}, ou[2] = {0, 0};
+    const int64_t fq = f / 4;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *gr = gu + r * 2 * f, *dr = dh + r * f;
+        uint16_t *outr = dgu + r * 2 * f;
+#pragma unroll 2
+        for (int64_t cq = threadIdx.x; cq < fq; cq += blockDim.x) {
+            const int64_t c = cq * 4;
+            const float4 g = __ldg(reinterpret_cast<const float4 *>(gr + c));
+            const float4 u = __ldg(reinterpret_cast<const float4 *>(gr + f + c));
+            const float4 d = __ldg(reinterpret_cast<const float4 *>(dr + c));
+            const float gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w}, ds[4] = {d.x, d.y, d.z, d.w};
+            uint32_t og[2] = {0, 0}, ou[2] = {0, 0};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
-            const float silu = __fmul_rn(gs[i], sg);
-            const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
-            const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
-            const float duv = __fmul_rn(ds[i], silu);
-            og[i >> 1] |= (uint32_t)f32_to_bf16_bits(dgv) << (16 * (i & 1));
-            ou[i >> 1] |= (uint32_t)f32_to_bf16_bits(duv) << (16 * (i & 1));
+            for (int i = 0; i < 4; ++i) {
+                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
+                const float silu = __fmul_rn(gs[i], sg);
+                const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
+                const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
+                const float duv = __fmul_rn(ds[i], silu);
+                og[i >> 1] |= (uint32_t)f32_to_bf16_bits(dgv) << (16 * (i & 1));
+                ou[i >> 1] |= (uint32_t)f32_to_bf16_bits(duv) << (16 * (i & 1));
+            }
+            *reinterpret_cast<uint2 *>(outr + c) = make_uint2(og[0], og[1]);
+            *reinterpret_cast<uint2 *>(outr + f + c) = make_uint2(ou[0], ou[1]);
         }
-        *reinterpret_cast<uint2 *>(dgu + r * 2 * f + c) = make_uint2(og[0], og[1]);
-        *reinterpret_cast<uint2 *>(dgu + r * 2 * f + f + c) = make_uint2(ou[0], ou[1]);
     }
 }
 
@@ -264,12 +268,11 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t *__rest
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ yhat, const int32_t *__restrict__ row_of,
                                                       const float *__restrict__ w, int64_t T, int k, int64_t d,
                                                       uint16_t *__restrict__ y) {
+    // one token per block iteration, eight columns per thread and step: no index division
     const int64_t per_tok = d / 8;
-    const int64_t items = T * per_tok;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = it / per_tok;
-        const int64_t c = (it - t * per_tok) * 8;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x)
+    for (int64_t ci = threadIdx.x; ci < per_tok; ci += blockDim.x) {
+        const int64_t c = ci * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
             const int64_t row = row_of[t * k + j];
@@ -377,7 +380,7 @@ extern "C" int moe4_swiglu_backward(const float *gu, const float *dh, int64_t ro
     MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0 && gu && dh && dgu && aligned16(gu) && aligned16(dh) &&
                    (reinterpret_cast<uintptr_t>(dgu) & 7u) == 0);
     if (rows == 0) return MOE4_OK;
-    swiglu_bwd_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, dh, rows, f, dgu);
+    swiglu_bwd_kernel<<<grid_cap(rows * 256, 256, 8), 256, 0, as_stream(stream)>>>(gu, dh, rows, f, dgu);
     return launch_status();
 }
 
@@ -397,7 +400,7 @@ extern "C" int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const f
     MOE4_CHECK_ARG(T >= 0 && k >= 1 && d > 0 && d % 8 == 0);
     MOE4_CHECK_ARG(T == 0 || (yhat && row_of && w && y && aligned16(yhat) && aligned16(y)));
     if (T == 0) return MOE4_OK;
-    combine_kernel<<<grid_cap(T * d / 8, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
+    combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
     return launch_status();
 }
 
