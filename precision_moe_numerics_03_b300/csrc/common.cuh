@@ -391,25 +391,39 @@ __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 // 16, 32, 64 pair lane l with lane l ^ 1, ^2, ^4, where fma(+-1, own, partner) rounds the exact
 // sum or difference once, as the add or subtract would.
 __device__ __forceinline__ void fwht128_sub16(float u[16]) {
+    // span 1 in scalar form (its inputs may be products, which must not meet a packed add)
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
+    for (int i = 0; i < 16; i += 2) {
+        const float a = u[i], b = u[i + 1];
+        u[i] = __fadd_rn(a, b);
+        u[i + 1] = __fsub_rn(a, b);
+    }
+    // spans 2, 4, 8 two butterflies at a time: elements i, i+1 (i even, bit h clear) against
+    // i+h, i+h+1; every input is a sum or difference, so packed add/sub round as the scalar ones
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+    for (int h = 2; h < 16; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; i += 2)
             if ((i & h) == 0) {
-                const float a = u[i], b = u[i + h];
-                u[i] = __fadd_rn(a, b);
-                u[i + h] = __fsub_rn(a, b);
+                const uint64_t a = f2_pack(u[i], u[i + 1]), b = f2_pack(u[i + h], u[i + h + 1]);
+                f2_unpack(f2_add(a, b), u[i], u[i + 1]);
+                f2_unpack(f2_sub(a, b), u[i + h], u[i + h + 1]);
             }
     const int lane = lane_id();
 #pragma unroll
     for (int lm = 1; lm < 8; lm <<= 1) {
         const float sgn = (lane & lm) ? -1.0f : 1.0f;
+        const uint64_t sg2 = f2_pack(sgn, sgn);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __fmaf_rn(sgn, u[i], __shfl_xor_sync(0xFFFFFFFFu, u[i], lm));
+        for (int i = 0; i < 16; i += 2) {
+            const float p0 = __shfl_xor_sync(0xFFFFFFFFu, u[i], lm), p1 = __shfl_xor_sync(0xFFFFFFFFu, u[i + 1], lm);
+            f2_unpack(f2_fma(sg2, f2_pack(u[i], u[i + 1]), f2_pack(p0, p1)), u[i], u[i + 1]);
+        }
     }
     const float c = __uint_as_float(0x3DB504F3u);  // nearest binary32 to 1/sqrt(128)
+    const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], c);
+    for (int i = 0; i < 16; i += 2) f2_unpack(f2_mul(f2_pack(u[i], u[i + 1]), c2), u[i], u[i + 1]);
 }
 
 
