@@ -58,18 +58,14 @@ struct Cfg<1> {                       // MXFP8
     static constexpr int ELEMS_PER_ATOM = 128;
 };
 
-// Epilogue staging of the fused SGD mode, per epilogue warp: a ring of SGD_NB buffers, each a
-// 32x16 binary32 chunk (64-byte rows, 64-byte swizzle) and a 32x16 bf16 chunk (32-byte rows,
-// 32-byte swizzle), with one mbarrier per buffer.  Master-weight loads run SGD_LA chunks ahead of
-// the chunk being updated, so each warp keeps several loads in flight.
+// Epilogue staging of the fused SGD mode, per epilogue warp: a ring of buffers, each a 32x16
+// binary32 chunk (64-byte rows, 64-byte swizzle) and, when the bf16 copy is written, a 32x16 bf16
+// chunk (32-byte rows, 32-byte swizzle), with one mbarrier per buffer.  Master-weight loads run a
+// fixed number of chunks ahead of the chunk being updated, so each warp keeps several loads in
+// flight; without the bf16 chunks the ring has room to run further ahead (SgdRing below).
 constexpr int SGD_CW = 16;                    // columns per chunk
 constexpr int SGD_W_CHUNK = 32 * SGD_CW * 4;  // 2 KB
 constexpr int SGD_B_CHUNK = 32 * SGD_CW * 2;  // 1 KB
-constexpr int SGD_NB = 3;                     // ring buffers per warp
-constexpr int SGD_LA = 1;                     // load lookahead, chunks
-static_assert(SGD_LA <= SGD_NB - 2, "a refilled buffer's store must be allowed to still be pending");
-constexpr int EPI_WARP_BYTES = SGD_NB * (SGD_W_CHUNK + SGD_B_CHUNK);
-constexpr int EPI_SGD_BYTES = 8 * EPI_WARP_BYTES;
 // TMA-store epilogue: one staged chunk of 32 rows per epilogue warp, TMA_CW columns wide (32 for
 // NVFP4; 16 for MXFP8, whose smaller staging leaves room for a fourth operand stage)
 template <int KIND>
@@ -79,7 +75,20 @@ constexpr int EPI_W_TILE = 32 * TMA_CW<KIND> * 4;
 // Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
 // TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
-enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3 };
+enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4 };
+// EPI_SGD writes the bf16 copy, EPI_SGD32 only the binary32 master weights (and the amax).
+constexpr bool is_sgd(int em) { return em == EPI_SGD || em == EPI_SGD32; }
+template <int EM>
+struct SgdRing {
+    static constexpr bool BF16 = EM == EPI_SGD;
+    static constexpr int NB = BF16 ? 3 : 5;  // ring buffers per warp
+    static constexpr int LA = BF16 ? 1 : 3;  // load lookahead, chunks
+    static constexpr int B_CHUNK = BF16 ? SGD_B_CHUNK : 0;
+    static constexpr int WARP_BYTES = NB * (SGD_W_CHUNK + B_CHUNK);
+    // the store that last read a refilled buffer may still be the one pending group allowed
+    static_assert(LA == NB - 2, "bulk_wait_read_1 before a refill assumes LA = NB - 2");
+};
+constexpr int SGD_NB_MAX = 5;
 // Fused return-path codec (NVFP4 GEMM): each epilogue warp stages its 32 rows x 128 columns of
 // bf16 product (rows padded to 272 bytes: conflict-free 16-byte stores and loads).
 constexpr int HMX_PITCH = 128 * 2 + 16;
@@ -91,14 +100,15 @@ template <int EM>
 struct EpiCfg {
     // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
     // tile's MMAs overlap the previous tile's master-weight traffic
-    static constexpr int BNT = EM == EPI_SGD ? 128 : BN;
-    static constexpr int NST = EM == EPI_SGD ? 4 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
+    static constexpr int BNT = is_sgd(EM) ? 128 : BN;
+    static constexpr int NST = is_sgd(EM) ? 4 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
     // operand stages for a given operand kind: the MXFP8 TMA-store mode fits a fourth one
     template <int KIND>
     static constexpr int NSTK = (EM == EPI_TMA && KIND == 1) ? 4 : NST;
     template <int KIND>
     static constexpr int BYTESK =
-        EM == EPI_SGD ? EPI_SGD_BYTES : (EM == EPI_TMA ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
+        is_sgd(EM) ? 8 * SgdRing<EM>::WARP_BYTES
+                   : (EM == EPI_TMA ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
 };
 
 template <int KIND, int NST, int EPI, int BNT>
@@ -114,7 +124,7 @@ struct Layout {
     static constexpr int OFF_EPI = (OFF_SFB + NST * SFB + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI;
     // full, empty, tmem_full[2], tmem_empty[2], drain, epilogue
-    static constexpr int NBAR = 2 * NST + 5 + 8 * SGD_NB;
+    static constexpr int NBAR = 2 * NST + 5 + 8 * SGD_NB_MAX;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
@@ -356,7 +366,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWb, const Args p) {
     // tmW: the output D (EPI_TMA) or the master weights (EPI_SGD); tmWb: their bf16 copy (EPI_SGD)
-    constexpr bool kSgd = EM == EPI_SGD;
+    constexpr bool kSgd = is_sgd(EM);
+    using Ring = SgdRing<EM>;
     constexpr int NST = EpiCfg<EM>::template NSTK<KIND>;
     constexpr int BNT = EpiCfg<EM>::BNT;
     using L = Layout<KIND, NST, EpiCfg<EM>::template BYTESK<KIND>, BNT>;
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *full = bars, *empty = bars + NST;
     // per accumulator buffer: tmem_full (MMA done) and tmem_empty (epilogue has read it)
     uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 2, *drain = tmem_full + 4;
-    uint64_t *epi_bar = tmem_full + 5;  // fused SGD: SGD_NB per epilogue warp
+    uint64_t *epi_bar = tmem_full + 5;  // fused SGD: Ring::NB per epilogue warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(tmem_empty + i, EPI_THREADS);
         }
         mbar_init(drain, 1);
-        for (int i = 0; i < 8 * SGD_NB; ++i) mbar_init(epi_bar + i, 1);
+        for (int i = 0; i < 8 * Ring::NB; ++i) mbar_init(epi_bar + i, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -523,18 +534,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // W32 <- W32 - lr * dW, bf16 copy, running max |bf16|.  This warp owns rows
                 // 32q..32q+31 and columns half*128 .. +127 of the tile, in NCH 16-column chunks.
                 // Chunks form one stream over this CTA's tiles: chunk u (tile u / NCH of the CTA,
-                // column chunk u % NCH) uses ring buffer u % SGD_NB, whose barrier completes for
-                // the (u / SGD_NB)-th time.  TMA brings the 32x16 binary32 chunk into shared memory
+                // column chunk u % NCH) uses ring buffer u % NB, whose barrier completes for
+                // the (u / NB)-th time.  TMA brings the 32x16 binary32 chunk into shared memory
                 // (64-byte swizzle: lane l's 16-byte piece j sits at piece j ^ ((l >> 1) & 3) of
                 // its 64-byte row), the lane updates its row in place and writes the bf16 row
                 // (32-byte swizzle: piece j at j ^ ((l >> 2) & 1)), and TMA stores both.  The load
-                // of chunk u + SGD_LA is issued before chunk u is processed; it may belong to the
+                // of chunk u + LA is issued before chunk u is processed; it may belong to the
                 // CTA's next tile, whose master weights do not depend on that tile's accumulator.
                 constexpr int NCH = (BNT / 2) / SGD_CW;
                 const int wi = warp - 4;
-                uint8_t *wring = smem + L::OFF_EPI + wi * EPI_WARP_BYTES;
-                uint8_t *bring = wring + SGD_NB * SGD_W_CHUNK;
-                uint64_t *eb = epi_bar + SGD_NB * wi;
+                constexpr int NB = Ring::NB, LA = Ring::LA;
+                uint8_t *wring = smem + L::OFF_EPI + wi * Ring::WARP_BYTES;
+                uint8_t *bring = wring + NB * SGD_W_CHUNK;
+                uint64_t *eb = epi_bar + NB * wi;
                 const int y0 = (int)((int64_t)tl.e * p.M + tl.m0 + q * 32);
                 const int x0 = (int)(tl.n0 + half * (BNT / 2));
                 int ny0 = 0, nx0 = 0;
@@ -548,31 +560,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 auto issue = [&](uint32_t u) {  // lane 0
                     const bool nxt = u >= u0 + NCH;
                     const int c = (int)(u % NCH);
-                    const int buf = (int)(u % SGD_NB);
-                    bulk_wait_read_1();  // the store of chunk u - SGD_NB, from this buffer, has read it
+                    const int buf = (int)(u % NB);
+                    bulk_wait_read_1();  // the store of chunk u - NB, from this buffer, has read it
                     mbar_expect_tx(eb + buf, SGD_W_CHUNK);
                     tma_load_2d(wring + buf * SGD_W_CHUNK, &tmW, eb + buf, (nxt ? nx0 : x0) + SGD_CW * c,
                                 nxt ? ny0 : y0);
                 };
-                while (sgd_issued < u0 + SGD_LA && sgd_issued < u_end) {  // the stream's first chunks
+                while (sgd_issued < u0 + LA && sgd_issued < u_end) {  // the stream's first chunks
                     if (lane == 0) issue(sgd_issued);
                     ++sgd_issued;
                 }
                 __syncwarp();
                 const float lr = p.lr;
-                const bool with_bf16 = p.w_bf16 != nullptr;  // else only the amax of the bf16 values
+                constexpr bool with_bf16 = Ring::BF16;  // else only the amax of the bf16 values
                 uint32_t amax2 = 0;
                 bool ok = true;
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c) {
                     const uint32_t u = u0 + c;
-                    if (sgd_issued == u + SGD_LA && sgd_issued < u_end) {
+                    if (sgd_issued == u + LA && sgd_issued < u_end) {
                         if (lane == 0) issue(sgd_issued);
                         ++sgd_issued;
                     }
                     __syncwarp();
-                    const int buf = (int)(u % SGD_NB);
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(eb + buf, (u / SGD_NB) & 1u, abort_flag));
+                    const int buf = (int)(u % NB);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(eb + buf, (u / NB) & 1u, abort_flag));
                     if (!ok) break;
                     ++sgd_done;
                     uint32_t r[16];
@@ -583,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int i = 0; i < 16; ++i) r[i] = 0;
                     }
                     uint8_t *wrow = wring + buf * SGD_W_CHUNK + lane * 64;
-                    uint8_t *brow = bring + buf * SGD_B_CHUNK + lane * 32;
+                    uint8_t *brow = bring + buf * Ring::B_CHUNK + lane * 32;
                     uint32_t pk[8];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -599,7 +611,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         amax2 = __vmaxu2(amax2, pk[2 * j] & 0x7FFF7FFFu);
                         amax2 = __vmaxu2(amax2, pk[2 * j + 1] & 0x7FFF7FFFu);
                     }
-                    if (with_bf16) {
+                    if constexpr (with_bf16) {
 #pragma unroll
                         for (int j = 0; j < 2; ++j)
                             *reinterpret_cast<uint4 *>(brow + ((j ^ ((lane >> 2) & 1)) << 4)) =
@@ -610,7 +622,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) {
                         if (live) {
                             tma_store_2d(&tmW, wring + buf * SGD_W_CHUNK, x0 + SGD_CW * c, y0);
-                            if (with_bf16) tma_store_2d(&tmWb, bring + buf * SGD_B_CHUNK, x0 + SGD_CW * c, y0);
+                            if constexpr (with_bf16)
+                                tma_store_2d(&tmWb, bring + buf * Ring::B_CHUNK, x0 + SGD_CW * c, y0);
                         }
                         bulk_commit();  // one group per chunk, empty or not, so group counts match chunks
                     }
@@ -789,9 +802,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // master-weight loads the loop did not consume (it stopped early): let them land
             if (lane == 0) {
                 for (uint32_t u = sgd_done; u < sgd_issued; ++u) {
-                    const uint32_t aa = smem_u32(epi_bar + SGD_NB * (warp - 4) + u % SGD_NB);
+                    const uint32_t aa = smem_u32(epi_bar + Ring::NB * (warp - 4) + u % Ring::NB);
                     const long long t0 = clock64();
-                    while (!mbar_try_wait(aa, (u / SGD_NB) & 1u) && clock64() - t0 < kWaitCycles) {
+                    while (!mbar_try_wait(aa, (u / Ring::NB) & 1u) && clock64() - t0 < kWaitCycles) {
                     }
                 }
             }
@@ -1103,6 +1116,7 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
         if (rc != MOE4_OK) return rc;
     }
     constexpr int BNS = EpiCfg<EPI_SGD>::BNT;
+    static_assert(EpiCfg<EPI_SGD32>::BNT == BNS, "both SGD modes use the same tiles");
     if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BNS)) return MOE4_ERR_CUDA;
     // the expert order for the tile schedule, after the staged scales in the workspace (without
     // room for it the tiles run in expert order)
@@ -1142,7 +1156,7 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     else if (!make_map_t(&twb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w_bf16, N, E * M, SGD_CW, 32,
                          CU_TENSOR_MAP_SWIZZLE_32B))
         return MOE4_ERR_CUDA;
-    return launch<1, EPI_SGD>(ta, tb, tw, twb, g, st);
+    return w_bf16 ? launch<1, EPI_SGD>(ta, tb, tw, twb, g, st) : launch<1, EPI_SGD32>(ta, tb, tw, twb, g, st);
 }
 
 extern "C" int moe4_selftest_wait(int64_t limit_cycles, void *stream) {
