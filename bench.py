@@ -46,7 +46,7 @@ METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
-TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.6 / 2216.7}
+TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.6 / 2216.7}  # no-copy SGD mode, deeper ring
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 4, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
 
 
