@@ -52,7 +52,7 @@ extern "C" {
 /* ------------------------------------------------------------------ status codes */
 #define MOE4_OK               0
 #define MOE4_ERR_ARG        (-1) /* null pointer, bad size, misaligned buffer, bad flag */
-#define MOE4_ERR_UNSUPPORTED (-2) /* a valid request this build does not implement */
+#define MOE4_ERR_UNSUPPORTED (-2) /* a valid request the library does not implement */
 #define MOE4_ERR_CUDA       (-3) /* a CUDA call or kernel launch failed */
 #define MOE4_ERR_TIMEOUT    (-4) /* a device-side wait gave up (reported by moe4_get_status) */
 #define MOE4_ERR_WORKSPACE  (-5) /* ws is NULL or smaller than moe4_workspace_size() */
