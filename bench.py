@@ -13,7 +13,8 @@ N(0,1) bias, Student-t(3) activations, N(0, 0.02) expert weights held as FP32 ma
             dequantise -> transpose -> MXFP8 requantisation with Philox stochastic rounding of
             W_down, H, W_gate/up and X; grouped MXFP8 dgrad (row-grouped) and wgrad
             (contraction-grouped) GEMMs for both projections; SwiGLU backward; SGD on the FP32
-            master weights (which writes the bf16 copies the next step quantises).
+            master weights, fused into the weight-gradient GEMMs (the next step quantises the
+            masters, rounded to bf16 as they are read).
 
 `value` is expert-GEMM TFLOP/s of the whole step: the algorithmic FLOPs of the six expert GEMMs
 (routed rows only) divided by the device time of the step.  The JSON line also carries per-kernel
@@ -688,7 +689,8 @@ def profile_case(name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    # ten steps: the copy pipeline of the end-to-end measurement fills once and drains once per run
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="the small 8-expert shapes (a quick check, not a bench line)")
