@@ -91,6 +91,7 @@ class LayerStep:
         self.Wb_d = self.W32_d.to(torch.bfloat16).view(torch.int16)
         # per-expert amax of the bf16 copies: written by the fused wgrad + SGD epilogue of each step
         # and read by the next step's weight quantisation (here seeded for the first step)
+        self.amax_h = torch.zeros(1, dtype=torch.float32, device=dev)
         self.amax_gu = self.Wb_gu.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
         self.amax_d = self.Wb_d.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
         # routing
@@ -178,10 +179,11 @@ class LayerStep:
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
                                         E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
         n += 1
-        with tm("swiglu_quant_h"):
-            m.moe4_swiglu(self.GU[:Rp], Rp, f, self.H[:Rp])
-            m.nvfp4_quantize(self.H[:Rp], 1, Rp, f, f, self.Hq_c, self.Hq_s, self.Hq_g, None, FOS | MMA, self.qws)
-        n += 3
+        with tm("swiglu_quant_h"):  # SwiGLU with the amax of H, so H is quantised in one pass
+            m.moe4_swiglu_amax(self.GU[:Rp], Rp, f, self.H[:Rp], self.amax_h)
+            m.nvfp4_quantize(self.H[:Rp], 1, Rp, f, f, self.Hq_c, self.Hq_s, self.Hq_g, self.amax_h,
+                             FOS | MMA | m.AMAX_GIVEN)
+        n += 2
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s, self.Wd_g, self.offs,
                                         E, Rp, d, f, self.Y, m.OUT_BF16 | MMA)
@@ -258,7 +260,7 @@ class LayerStep:
         # wgrad operands + the SGD epilogue: read W32, write W32 (the bf16 copy is not stored)
         b["gemm_mxfp8_wgrad_sgd"] = (rows * d * mx + rows * f * mx + rows * 2 * f * mx + rows * d * mx +
                                      (w_gu + w_d) * (4 + 4))
-        b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 * 2 + rows * f * (2 + nv)
+        b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 + rows * f * (2 + nv)  # amax fused into SwiGLU
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
         b["hadamard"] = rows * d * (2 + 2 + nv + nv + 2)
         b["combine"] = rows * d * 2 + T * d * 2

@@ -301,6 +301,11 @@ int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64_t T, int64
  * columns and u the last f (binary32, then nearest-even to bf16).  f % 4 == 0. */
 int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h, void *stream);
 
+/* moe4_swiglu_amax: moe4_swiglu, and amax_out[0] = max |h| over the bf16 results (binary32; 0 for
+ * rows == 0), exactly the amax nvfp4_quantize would compute for h, so that call can take
+ * MOE4_AMAX_GIVEN and skip its own pass over h.  amax_out 4-byte aligned; it is cleared first. */
+int moe4_swiglu_amax(const float *gu, int64_t rows, int64_t f, uint16_t *h, float *amax_out, void *stream);
+
 /* moe4_swiglu_backward: gu f32 [rows, 2f] (the forward's gate | up), dh f32 [rows, f] ->
  * dgu bf16 [rows, 2f]: dg = dh * u * s * (1 + g * (1 - s)), du = dh * g * s with
  * s = 1/(1+exp(-g)), binary32 then nearest-even to bf16.  f % 4 == 0. */

@@ -177,9 +177,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t *__rest
 }
 
 // ------------------------------------------------------------------ SwiGLU
+// With amax_bits, also the largest |h| of the bf16 results (as binary32 bits, atomicMax).
 __global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ gu, int64_t rows, int64_t f,
-                                                     uint16_t *__restrict__ h) {
+                                                     uint16_t *__restrict__ h, unsigned int *__restrict__ amax_bits) {
     const int64_t quads = rows * f / 4;
+    uint32_t best = 0;  // two packed bf16 magnitudes
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = (q * 4) / f;
         const int64_t c = q * 4 - r * f;
@@ -193,6 +195,12 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ g
             out[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(silu, us[i])) << (16 * (i & 1));
         }
         *reinterpret_cast<uint2 *>(h + r * f + c) = make_uint2(out[0], out[1]);
+        best = __vmaxu2(best, __vmaxu2(out[0] & 0x7FFF7FFFu, out[1] & 0x7FFF7FFFu));
+    }
+    if (amax_bits) {
+        uint32_t mag = max(best & 0xFFFFu, best >> 16) << 16;
+        mag = __reduce_max_sync(0xFFFFFFFFu, mag);
+        if (lane_id() == 0 && mag) atomicMax(amax_bits, mag);
     }
 }
 
@@ -369,9 +377,22 @@ extern "C" int moe4_permute_nvfp4(const uint8_t *codes, const uint8_t *sf, int64
 }
 
 extern "C" int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h, void *stream) {
-    MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0 && gu && h && aligned16(gu) && (reinterpret_cast<uintptr_t>(h) & 7u) == 0);
+    MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0);
+    MOE4_CHECK_ARG(rows == 0 || (gu && h && aligned16(gu) && (reinterpret_cast<uintptr_t>(h) & 7u) == 0));
     if (rows == 0) return MOE4_OK;
-    swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, rows, f, h);
+    swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, rows, f, h, nullptr);
+    return launch_status();
+}
+
+extern "C" int moe4_swiglu_amax(const float *gu, int64_t rows, int64_t f, uint16_t *h, float *amax_out,
+                                void *stream) {
+    MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0 && amax_out && aligned4(amax_out));
+    MOE4_CHECK_ARG(rows == 0 || (gu && h && aligned16(gu) && (reinterpret_cast<uintptr_t>(h) & 7u) == 0));
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (rows == 0) return MOE4_OK;
+    swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, st>>>(gu, rows, f, h,
+                                                                  reinterpret_cast<unsigned int *>(amax_out));
     return launch_status();
 }
 

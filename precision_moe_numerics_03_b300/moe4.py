@@ -74,6 +74,7 @@ _SIGNATURES = {
     "moe4_combine_backward_mxfp8": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32,
                                            _vp]),
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "moe4_swiglu_amax": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_sgd_update": (_int, [_vp, _vp, _i64, _f32, _vp, _vp]),
     "moe4_convert": (_int, [_int, _vp, _i64, _vp, _vp]),
@@ -269,6 +270,10 @@ def moe4_combine_backward(dy, row_of, w, src_of, T, k, d, rows_total, dyhat, str
 
 def moe4_swiglu(gu, rows, f, h, stream=None):
     _call("moe4_swiglu", _p(gu), rows, f, _p(h), _s(stream))
+
+
+def moe4_swiglu_amax(gu, rows, f, h, amax_out, stream=None):
+    _call("moe4_swiglu_amax", _p(gu), rows, f, _p(h), _p(amax_out), _s(stream))
 
 
 def moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, rows_total, q_row, e8_row, q_col, e8_col, flags=0,

@@ -91,6 +91,8 @@ MISALIGNED = FAKE + 4
     ("moe4_route_topk", (FAKE, 4, 8, 40, FAKE, FAKE, None)),                                 # k > 32
     ("moe4_permute_plan", (FAKE, 4, 2, 8, FAKE, FAKE, FAKE, 10, FAKE, 1 << 20, None)),       # rows_cap too small
     ("moe4_swiglu", (FAKE, 4, 6, FAKE, None)),                                               # f % 4
+    ("moe4_swiglu_amax", (FAKE, 4, 8, FAKE, None, None)),                                    # no amax_out
+    ("moe4_swiglu_amax", (FAKE, 4, 8, FAKE, FAKE + 2, None)),                                # amax alignment
     ("moe4_combine", (FAKE, FAKE, FAKE, 4, 2, 12, FAKE, None)),                              # d % 8
     ("moe4_sgd_update", (FAKE, FAKE, 6, 0.1, FAKE, None)),                                   # n % 4
     ("moe4_sf_to_mma_layout", (FAKE, 1, 100, 4, FAKE, None)),                                # rows % 128

@@ -84,6 +84,23 @@ def test_swiglu_within_one_bf16_ulp():
     assert np.max(np.abs(got - want)) <= 1
 
 
+@pytest.mark.parametrize("rows,f", [(640, 1024), (0, 64), (160512, 2048)])
+def test_swiglu_amax_equals_swiglu_and_max(rows, f):
+    """moe4_swiglu_amax writes the same h as moe4_swiglu and the max |h| of those bf16 values
+    (the last case is the 384-expert layer's H); an empty input gives amax 0."""
+    gen = inputs.device_generator(13, rows, DEV)
+    gu = inputs.device_normal((max(rows, 1), 2 * f), 3.0, gen, DEV, dtype=torch.float32)[:rows].contiguous()
+    h0 = torch.empty((rows, f), dtype=torch.int16, device=DEV)
+    h1 = torch.full((rows, f), -1, dtype=torch.int16, device=DEV)
+    amax = torch.full((1,), -5.0, dtype=torch.float32, device=DEV)
+    moe4.moe4_swiglu(gu, rows, f, h0)
+    moe4.moe4_swiglu_amax(gu, rows, f, h1, amax)
+    torch.cuda.synchronize()
+    assert torch.equal(h0, h1)
+    want = float(np.abs(oracle.bf16_to_f32(to_np(h0, np.uint16))).max()) if rows else 0.0
+    assert float(to_np(amax)[0]) == want
+
+
 def test_combine_bit_exact():
     T, k, d, R = 1000, 8, 512, 9000
     rng = np.random.default_rng(3)
