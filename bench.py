@@ -794,6 +794,23 @@ def main():
         ach = gbytes[dom] / (t_dom / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
                 "traffic": None, "kernel": dom}
+    # the metric against both denominators: measured HBM copy and the derived FP4 peak, and the
+    # nominal 8 TB/s and the pages' 15 PF dense FP4; for the NVFP4 GEMMs also the fraction of the
+    # time bound max(bytes / bandwidth, FLOPs / peak) of their own traffic and work
+    t_g = per["gemm_nvfp4"] / 1e3
+    bound_meas = max(gbytes["gemm_nvfp4"] / (peaks["hbm"] * 1e9), fwd_flops / (fp4_peak * 1e12))
+    bound_nom = max(gbytes["gemm_nvfp4"] / 8000e9, fwd_flops / 15000e12)
+    req_gbs = gbytes["requant"] / (per["requant"] / 1e3) / 1e9
+    metric_detail = {
+        "nvfp4_gemm": {"TFLOP/s": comps["gemm_nvfp4"]["TFLOP/s"],
+                       "frac_fp4_peak_derived": round(comps["gemm_nvfp4"]["TFLOP/s"] / fp4_peak, 4),
+                       "frac_fp4_peak_15PF": round(comps["gemm_nvfp4"]["TFLOP/s"] / 15000.0, 4),
+                       "frac_time_bound_measured": round(bound_meas / t_g, 4),
+                       "frac_time_bound_nominal": round(bound_nom / t_g, 4)},
+        "requant": {"GB/s": round(req_gbs, 1), "frac_hbm_measured": round(req_gbs / peaks["hbm"], 4),
+                    "frac_hbm_nominal_8TBs": round(req_gbs / 8000.0, 4),
+                    "note": "issue-bound (Philox4x32-10): ncu issue-slot figures in profiles/"},
+    }
     nl = GROUP_LAUNCHES.get(dom, 1)
     roof["launches_per_step"] = nl
     if dom in TRAFFIC_RATIO:
@@ -893,6 +910,7 @@ def main():
             "requant_GBps": requant_gbs, "requant_frac_hbm": requant_gbs / peaks["hbm"] if requant_gbs else None,
             "nvfp4_gemm_TFLOPs": comps["gemm_nvfp4"]["TFLOP/s"],
             "nvfp4_gemm_frac_fp4_peak": comps["gemm_nvfp4"]["TFLOP/s"] / fp4_peak,
+            "metric_detail": metric_detail,
             "components": comps,
             "roofline": roof,
             "clocks": clk,
