@@ -77,7 +77,7 @@ constexpr int EPI_W_TILE = 32 * TMA_CW<KIND> * 4;
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
 enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4 };
 // EPI_SGD writes the bf16 copy, EPI_SGD32 only the binary32 master weights (and the amax).
-constexpr bool is_sgd(int em) { return em == EPI_SGD || em == EPI_SGD32; }
+__host__ __device__ constexpr bool is_sgd(int em) { return em == EPI_SGD || em == EPI_SGD32; }
 template <int EM>
 struct SgdRing {
     static constexpr bool BF16 = EM == EPI_SGD;
