@@ -261,3 +261,59 @@ def test_mxfp8_gemms_read_tile_layout_scales():
         outs.append((w, wb, amax))
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_nvfp4_forward_gate_up_full_size_sampled_rows():
+    """The layer step's gate/up GEMM as it runs there: 16384 tokens x d_model 4096 (Student-t(3))
+    quantised to NVFP4 with one per-tensor scale, gathered into expert order by a top-8 plan over
+    384 experts (N(0,1) logits + per-expert bias), tile-layout scales, against 384 experts'
+    gate/up weights [4096, 4096] N(0, 0.02) with per-expert scales; binary32 output.  Checked on
+    sampled rows of three experts (the largest group, the first and the last non-empty one): the
+    oracle quantises those token rows with the tensor's amax and the expert's weights with the
+    expert's amax, and multiplies in float64."""
+    T, d, f, E, k = 16384, 4096, 2048, 384, 8
+    rng = np.random.default_rng(0)
+    lg = (rng.standard_normal((T, E)) + rng.standard_normal(E)).astype(np.float32)
+    idx, _ = oracle.route_topk(lg, k)
+    roffs, rrow = oracle.permute_plan(idx, E)
+    Rp = int(roffs[-1])
+    rows_cap = T * k + 127 * E
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    src_of = torch.empty(rows_cap, dtype=torch.int32, device=DEV)
+    moe4.moe4_permute_plan(to_dev(idx), T, k, E, offs, row_of, src_of, rows_cap,
+                           moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E)))
+    x = inputs.device_student_t((T, d), inputs.device_generator(21, 0, DEV), DEV).view(torch.int16)
+    w = inputs.device_normal((E * 2 * f, d), 0.02, inputs.device_generator(21, 1, DEV), DEV).view(torch.int16)
+    xc, xs, xg = nvfp4_quantize(x, 1, T, d)
+    xpc, xps = empty_u8(Rp, d // 2), empty_u8(Rp, d // 16)
+    moe4.moe4_permute_nvfp4(xc, xs, T, d, src_of, Rp, xpc, xps, moe4.SF_MMA_LAYOUT)
+    del xc, xs
+    wc, ws_, wg = nvfp4_quantize(w, E, 2 * f, d, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    GU = torch.empty((Rp, 2 * f), dtype=torch.float32, device=DEV)
+    gws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, Rp, E, 2 * f, d))
+    moe4.grouped_expert_gemm_nvfp4(xpc, xps, xg, wc, ws_, wg, offs, E, Rp, 2 * f, d, GU,
+                                   moe4.OUT_F32 | moe4.SF_MMA_LAYOUT, gws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    assert np.array_equal(to_np(offs), roffs)
+    del wc, ws_
+
+    x32 = oracle.bf16_to_f32(to_np(x, np.uint16))
+    x_amax = np.abs(x32).max()
+    src = np.full(Rp, -1, np.int64)
+    src[rrow.reshape(-1)] = np.repeat(np.arange(T), k)
+    sizes = np.diff(roffs)
+    live = np.nonzero(sizes)[0]
+    for e in [int(np.argmax(sizes)), int(live[0]), int(live[-1])]:
+        lo, hi = int(roffs[e]), int(roffs[e + 1])
+        rows = np.unique(np.concatenate([np.random.default_rng(e).choice(np.arange(lo, hi), 12), [lo, hi - 1]]))
+        real = src[rows] >= 0
+        xs_ = np.zeros((len(rows), d), np.float32)
+        xs_[real] = x32[src[rows][real]]
+        rxc, rxs, rxg = oracle.nvfp4_quantize(xs_, amax=x_amax)
+        we = oracle.bf16_to_f32(to_np(w[e * 2 * f:(e + 1) * 2 * f], np.uint16))
+        rwc, rws, rwg = oracle.nvfp4_quantize(we)
+        Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rxc, rxs, rxg),
+                                        oracle.nvfp4_dequantize(rwc, rws, rwg)[None], np.array([0, len(rows)]))
+        check_f32(to_np(GU[torch.as_tensor(rows, device=DEV)]), Dref, S, "expert %d" % e)

@@ -229,3 +229,31 @@ def test_requant_rows_of_very_different_scale(sr):
     assert sub.sum() > 1000  # the E4M3 subnormal range is exercised
     assert first_mismatch(to_np(e8), re8) is None
     assert first_mismatch(to_np(q), rq) is None
+
+
+def test_requant_full_size_gate_up_weights_sampled():
+    """The layer step's largest requantisation as it runs there: 384 experts' gate/up weights
+    [384, 4096, 4096] N(0, 0.02), NVFP4 with per-expert scales in the tile layout, to MXFP8
+    [384, 4096, 4096] transposed with stochastic rounding (6.4G values: 32-bit Philox counters).
+    Sampled: experts 0, 191 and 383, three slices of 32 output rows each; the oracle quantises
+    those input columns with the expert's amax and rounds them with the global output index."""
+    E, rows, cols = 384, 4096, 4096
+    w = inputs.device_normal((E * rows, cols), 0.02, inputs.device_generator(22, 0, DEV), DEV).view(torch.int16)
+    c, s, g = nvfp4_quantize(w, E, rows, cols, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    q, e8 = empty_u8(E, cols, rows), empty_u8(E, cols, rows // 32)
+    seed, sid = 7, 3
+    moe4.mxfp8_requant_transpose_sr(c, s, g, E, rows, cols, q, e8, seed, sid, moe4.SR | moe4.SF_MMA_LAYOUT)
+    torch.cuda.synchronize()
+    del c, s
+    for e in [0, 191, 383]:
+        we = oracle.bf16_to_f32(to_np(w[e * rows:(e + 1) * rows], np.uint16))
+        amax = np.abs(we).max()
+        qn, e8n = to_np(q[e]), to_np(e8[e])
+        for c0 in [0, 2048, 4064]:
+            codes, scl, gd = oracle.nvfp4_quantize(np.ascontiguousarray(we[:, c0:c0 + 32]), amax=amax)
+            assert np.asarray(gd).reshape(-1)[0] == to_np(g)[e]
+            xh = oracle.nvfp4_dequantize(codes, scl, gd)
+            rq, re8 = oracle.mxfp8_quantize_rows(np.ascontiguousarray(xh.T), sr=True, seed=seed, stream_id=sid,
+                                                 idx_base=(e * cols + c0) * rows)
+            assert first_mismatch(qn[c0:c0 + 32], rq) is None
+            assert first_mismatch(e8n[c0:c0 + 32], re8) is None
