@@ -317,3 +317,47 @@ def test_nvfp4_forward_gate_up_full_size_sampled_rows():
         Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rxc, rxs, rxg),
                                         oracle.nvfp4_dequantize(rwc, rws, rwg)[None], np.array([0, len(rows)]))
         check_f32(to_np(GU[torch.as_tensor(rows, device=DEV)]), Dref, S, "expert %d" % e)
+
+
+def test_mxfp8_wgrad_fused_sgd_full_size_equals_unfused():
+    """The layer step's down-projection weight update at full size: 384 experts, W32 [384, 4096,
+    2048], the contraction over each expert's rows of a skewed top-8 routing (largest group
+    thousands of rows, many tiny, some empty), MXFP8 operands with tile-layout scales.  The fused
+    kernel without a bf16 copy (size-interleaved tile schedule, five-buffer ring) gives the same
+    FP32 masters as the contraction-grouped GEMM to memory followed by moe4_sgd_update, bit for
+    bit, and the amax of their bf16 rounding."""
+    E, M, N = 384, 4096, 2048
+    rng = np.random.default_rng(1)
+    counts = rng.multinomial(16384 * 8, rng.dirichlet(np.ones(E) * 0.5))
+    offs_np = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int32)
+    Kt = int(offs_np[-1])
+    offs = to_dev(offs_np)
+    gen = inputs.device_generator(23, 0, DEV)
+
+    def codes(n):  # E4M3 codes without the NaN patterns
+        c = torch.randint(0, 0x7F, (n,), generator=gen, device=DEV, dtype=torch.int32)
+        s = torch.randint(0, 2, (n,), generator=gen, device=DEV, dtype=torch.int32) * 0x80
+        return (c | s).to(torch.uint8)
+
+    a, b = codes(M * Kt), codes(N * Kt)
+    ae = torch.randint(118, 124, (M * Kt // 32,), generator=gen, device=DEV, dtype=torch.int32).to(torch.uint8)
+    be = torch.randint(118, 124, (N * Kt // 32,), generator=gen, device=DEV, dtype=torch.int32).to(torch.uint8)
+    ae_t, be_t = mma_layout(ae, M, Kt // 32), mma_layout(be, N, Kt // 32)
+    w0 = inputs.device_normal((E, M, N), 0.02, inputs.device_generator(23, 1, DEV), DEV, dtype=torch.float32)
+    lr = 1e-3
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, Kt))
+    dW = torch.empty((E, M, N), dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8(a, ae, b, be, offs, E, M, N, Kt, dW, moe4.OUT_F32 | moe4.GROUP_K, ws)
+    w_ref = w0.clone()
+    wb_ref = torch.empty((E, M, N), dtype=torch.int16, device=DEV)
+    moe4.moe4_sgd_update(w_ref, dW, w_ref.numel(), lr, wb_ref)
+    del dW
+    w_f = w0.clone()
+    amax = torch.full((E,), -1.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8_wgrad_sgd(a, ae_t, b, be_t, offs, E, M, N, Kt, w_f, None, lr, amax, moe4.SF_MMA_LAYOUT,
+                                      ws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    assert torch.equal(w_f, w_ref)
+    want = wb_ref.view(torch.bfloat16).abs().reshape(E, -1).amax(dim=1).float()
+    assert torch.equal(amax, want)
