@@ -257,3 +257,33 @@ def test_requant_full_size_gate_up_weights_sampled():
                                                  idx_base=(e * cols + c0) * rows)
             assert first_mismatch(qn[c0:c0 + 32], rq) is None
             assert first_mismatch(e8n[c0:c0 + 32], re8) is None
+
+
+def test_mxfp8_colwise_sr_beyond_2_34_values():
+    """More than 2^34 output values (131072 x 131200): the Philox counter's second word becomes
+    non-zero for the last output rows, so the transposing kernel runs its 64-bit counter
+    instance.  Input: bf16 values from a multiplicative hash of the element index (all finite);
+    checked on the first and the last 32 output rows against the oracle with the global index."""
+    rows, cols = 131072, 131200
+    n = rows * cols
+    assert n > (1 << 34)
+    x = torch.empty(n, dtype=torch.int16, device=DEV)
+    step = 1 << 28
+    for s0 in range(0, n, step):
+        i = torch.arange(s0, min(n, s0 + step), device=DEV, dtype=torch.int64)
+        h = (i * 2654435761) & 0xFFFFFFFF
+        bits = 0x3C00 + ((h >> 7) & 0x07FF) + ((h >> 20) & 1) * 0x8000
+        x[s0:s0 + len(i)] = bits.to(torch.int32).to(torch.int16)
+        del i, h, bits
+    q, e8 = empty_u8(cols, rows), empty_u8(cols, rows // 32)
+    seed, sid = 9, 5
+    moe4.mxfp8_quantize(x, rows, cols, q, e8, seed, sid, moe4.COLWISE | moe4.SR)
+    torch.cuda.synchronize()
+    xv = x.view(rows, cols)
+    for c0 in [0, cols - 32]:
+        xs = oracle.bf16_to_f32(to_np(xv[:, c0:c0 + 32].contiguous(), np.uint16))
+        rq, re8 = oracle.mxfp8_quantize_rows(np.ascontiguousarray(xs.T), sr=True, seed=seed, stream_id=sid,
+                                             idx_base=c0 * rows)
+        assert c0 == 0 or (c0 * rows) // 4 >= (1 << 32)  # the last slice: counter word 1 is 1
+        assert first_mismatch(to_np(q[c0:c0 + 32]), rq) is None
+        assert first_mismatch(to_np(e8[c0:c0 + 32]), re8) is None
