@@ -9,6 +9,8 @@
 //
 // HBM-bound kernels: 16-byte vector loads, one thread per 16-value block (two 16-byte loads, one
 // 8-byte code store, one scale byte), grid-stride loops sized to the SM count.
+#include <atomic>
+
 #include "common.cuh"
 
 #include <cfloat>
@@ -16,15 +18,17 @@
 
 namespace moe4 {
 
+// The current device's SM count, looked up once per device.
 int num_sms() {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0, n = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached = n > 0 ? n : 148;
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached;
+    return n;
 }
 
 // ------------------------------------------------------------------ amax pass
