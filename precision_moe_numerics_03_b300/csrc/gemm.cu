@@ -281,6 +281,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The same load without the wait (several loads, then one tc_wait_ld).
+__device__ __forceinline__ void tc_ld32_nw(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -709,19 +723,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE<KIND>;
                 const int y0 = (int)((p.group_k ? (int64_t)tl.e * p.M : 0) + tl.m0 + q * 32);
                 const int x0 = (int)(tl.n0 + half * (BNT / 2));
-                for (int c = 0; c < (BNT / 2) / CW; ++c) {
-                    uint32_t r[CW];
-                    if (live) {
-                        if constexpr (CW == 32) tc_ld32(tbase + (uint32_t)(c * CW), r);
-                        else tc_ld16(tbase + (uint32_t)(c * CW), r);
-                    } else {
+                // the warp's whole slab (32 rows x BNT/2 columns) goes to registers first and the
+                // accumulator is handed back at once, so the next tile's MMAs run while this tile
+                // is converted and stored
+                constexpr int NCOL = BNT / 2;
+                uint32_t accr[NCOL];
+                if (live) {
 #pragma unroll
-                        for (int i = 0; i < CW; ++i) r[i] = 0;
-                    }
+                    for (int c = 0; c < NCOL / 32; ++c) tc_ld32_nw(tbase + (uint32_t)(c * 32), accr + 32 * c);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NCOL; ++i) accr[i] = 0;
+                }
+                tc_fence_before();
+                mbar_arrive(tmem_empty + acc);
+#pragma unroll
+                for (int c = 0; c < NCOL / CW; ++c) {
                     float v[CW];
 #pragma unroll
                     for (int i = 0; i < CW; ++i)
-                        v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(r[i]), alpha) : __uint_as_float(r[i]);
+                        v[i] = KIND == 0 ? __fmul_rn(__uint_as_float(accr[c * CW + i]), alpha)
+                                         : __uint_as_float(accr[c * CW + i]);
                     if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile out
                     __syncwarp();
                     if (p.mode == BF16) {
@@ -793,7 +816,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            if constexpr (EM != EPI_HMX) {
+            if constexpr (EM != EPI_HMX && EM != EPI_TMA) {  // those two hand the accumulator back early
                 tc_fence_before();
                 mbar_arrive(tmem_empty + acc);
             }
