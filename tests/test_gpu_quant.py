@@ -81,9 +81,12 @@ def test_degenerate_tensors():
     assert list(to_np(g)) == [1.0, 1.0]
 
 
-def test_sf_mma_layout_is_a_permutation():
+@pytest.mark.parametrize("rows,cols", [(256, 512), (384, 192), (128, 320), (256, 448)])
+def test_sf_mma_layout_is_a_permutation(rows, cols):
+    """The tile-layout scale offsets divide the block index by cols/64 through a multiply and
+    shift: cols/64 = 8, 3, 5 and 7 here."""
     rng = np.random.default_rng(4)
-    nmat, rows, cols = 2, 256, 512
+    nmat = 2
     x = inputs.to_bf16_bits(rng.standard_normal((nmat * rows, cols)).astype(np.float32))
     xd = to_dev(x)
     c0, s0, g0 = nvfp4_quantize(xd, nmat, rows, cols)
