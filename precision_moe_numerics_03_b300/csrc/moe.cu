@@ -177,9 +177,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t *__rest
 }
 
 // ------------------------------------------------------------------ SwiGLU
-// With amax_bits, also the largest |h| of the bf16 results (as binary32 bits, atomicMax).
-__global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ gu, int64_t rows, int64_t f,
-                                                     uint16_t *__restrict__ h, unsigned int *__restrict__ amax_bits) {
+// With kAmax, also the largest |h| of the bf16 results (as binary32 bits, one atomicMax per
+// block).  Each instance is held to 32 registers so that eight blocks stay resident per SM.
+template <bool kAmax>
+__global__ void __launch_bounds__(256, 8) swiglu_kernel(const float *__restrict__ gu, int64_t rows, int64_t f,
+                                                        uint16_t *__restrict__ h, unsigned int *__restrict__ amax_bits) {
     const int64_t quads = rows * f / 4;
     uint32_t best = 0;  // two packed bf16 magnitudes
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += (int64_t)gridDim.x * blockDim.x) {
@@ -195,12 +197,19 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ g
             out[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(silu, us[i])) << (16 * (i & 1));
         }
         *reinterpret_cast<uint2 *>(h + r * f + c) = make_uint2(out[0], out[1]);
-        best = __vmaxu2(best, __vmaxu2(out[0] & 0x7FFF7FFFu, out[1] & 0x7FFF7FFFu));
+        if (kAmax) best = __vmaxu2(best, __vmaxu2(out[0] & 0x7FFF7FFFu, out[1] & 0x7FFF7FFFu));
     }
-    if (amax_bits) {
+    if (kAmax) {
+        __shared__ uint32_t part[8];
         uint32_t mag = max(best & 0xFFFFu, best >> 16) << 16;
         mag = __reduce_max_sync(0xFFFFFFFFu, mag);
-        if (lane_id() == 0 && mag) atomicMax(amax_bits, mag);
+        if (lane_id() == 0) part[threadIdx.x >> 5] = mag;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t m = part[0];
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, part[w]);
+            if (m) atomicMax(amax_bits, m);
+        }
     }
 }
 
@@ -380,7 +389,7 @@ extern "C" int moe4_swiglu(const float *gu, int64_t rows, int64_t f, uint16_t *h
     MOE4_CHECK_ARG(rows >= 0 && f > 0 && f % 4 == 0);
     MOE4_CHECK_ARG(rows == 0 || (gu && h && aligned16(gu) && (reinterpret_cast<uintptr_t>(h) & 7u) == 0));
     if (rows == 0) return MOE4_OK;
-    swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, rows, f, h, nullptr);
+    swiglu_kernel<false><<<grid_cap(rows * f / 4, 256, 8), 256, 0, as_stream(stream)>>>(gu, rows, f, h, nullptr);
     return launch_status();
 }
 
@@ -391,8 +400,8 @@ extern "C" int moe4_swiglu_amax(const float *gu, int64_t rows, int64_t f, uint16
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
     if (rows == 0) return MOE4_OK;
-    swiglu_kernel<<<grid_cap(rows * f / 4, 256, 8), 256, 0, st>>>(gu, rows, f, h,
-                                                                  reinterpret_cast<unsigned int *>(amax_out));
+    swiglu_kernel<true><<<grid_cap(rows * f / 4, 256, 8), 256, 0, st>>>(gu, rows, f, h,
+                                                                        reinterpret_cast<unsigned int *>(amax_out));
     return launch_status();
 }
 
