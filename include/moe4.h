@@ -282,7 +282,8 @@ int moe4_route_topk(const float *logits, int64_t T, int64_t E, int64_t k, int32_
 /* moe4_permute_plan: from idx [T, k] build offs int32 [E+1] (each expert's rows, stable in
  * (token, slot), zero-padded to a multiple of 128), row_of int32 [T, k] (dispatched row of each
  * (token, slot)) and src_of int32 [rows_cap] (source token of each dispatched row, -1 for
- * padding).  rows_cap >= T*k + 127*E.  ws: moe4_workspace_size(MOE4_OP_PERMUTE_PLAN, T, k, E). */
+ * padding).  rows_cap >= T*k + 127*E, and T*k + 127*E <= 2^31 - 1 (row indices are int32).
+ * ws: moe4_workspace_size(MOE4_OP_PERMUTE_PLAN, T, k, E). */
 int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64_t E, int32_t *offs,
                       int32_t *row_of, int32_t *src_of, int64_t rows_cap, void *ws,
                       size_t ws_bytes, void *stream);
@@ -343,7 +344,7 @@ int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *row_of, const
 
 /* moe4_combine: y bf16 [T, d], y[t] = sum over slots j in order of w[t,j] * yhat[row_of[t,j]]:
  * one binary32 product and one binary32 add per slot from 0, then nearest-even to bf16.
- * yhat bf16 [rows, d]; d % 8 == 0. */
+ * yhat bf16 [rows, d]; 1 <= k <= 32 (as moe4_route_topk); d % 8 == 0. */
 int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const float *w, int64_t T,
                  int64_t k, int64_t d, uint16_t *y, void *stream);
 

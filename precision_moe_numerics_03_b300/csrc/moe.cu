@@ -350,7 +350,10 @@ extern "C" int moe4_route_topk(const float *logits, int64_t T, int64_t E, int64_
 extern "C" int moe4_permute_plan(const int32_t *idx, int64_t T, int64_t k, int64_t E, int32_t *offs,
                                  int32_t *row_of, int32_t *src_of, int64_t rows_cap, void *ws, size_t ws_bytes,
                                  void *stream) {
-    MOE4_CHECK_ARG(T >= 0 && k >= 1 && E >= 1 && E <= 4096 && offs && rows_cap >= T * k + 127 * E);
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && E >= 1 && E <= 4096 && offs);
+    // row indices and offsets are int32: the padded row count must fit
+    MOE4_CHECK_ARG(T <= INT32_MAX && k <= INT32_MAX && T * k + 127 * E <= INT32_MAX);
+    MOE4_CHECK_ARG(rows_cap >= T * k + 127 * E);
     MOE4_CHECK_ARG(T == 0 || (idx && row_of && src_of));
     const int64_t n = T * k;
     const int64_t nchunks = (n + kChunk - 1) / kChunk;
@@ -427,7 +430,7 @@ extern "C" int moe4_combine_backward(const uint16_t *dy, const int32_t *row_of, 
 
 extern "C" int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const float *w, int64_t T, int64_t k,
                             int64_t d, uint16_t *y, void *stream) {
-    MOE4_CHECK_ARG(T >= 0 && k >= 1 && d > 0 && d % 8 == 0);
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 8 == 0);
     MOE4_CHECK_ARG(T == 0 || (yhat && row_of && w && y && aligned16(yhat) && aligned16(y)));
     if (T == 0) return MOE4_OK;
     combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);

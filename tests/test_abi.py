@@ -90,6 +90,8 @@ MISALIGNED = FAKE + 4
                             None, 0, None)),                                                 # bf16 accumulate
     ("moe4_route_topk", (FAKE, 4, 8, 40, FAKE, FAKE, None)),                                 # k > 32
     ("moe4_permute_plan", (FAKE, 4, 2, 8, FAKE, FAKE, FAKE, 10, FAKE, 1 << 20, None)),       # rows_cap too small
+    ("moe4_permute_plan", (FAKE, 1 << 28, 8, 8, FAKE, FAKE, FAKE, 1 << 32, FAKE, 1 << 40, None)),  # rows past int32
+    ("moe4_combine", (FAKE, FAKE, FAKE, 4, 40, 16, FAKE, None)),                             # k > 32
     ("moe4_swiglu", (FAKE, 4, 6, FAKE, None)),                                               # f % 4
     ("moe4_swiglu_amax", (FAKE, 4, 8, FAKE, None, None)),                                    # no amax_out
     ("moe4_swiglu_amax", (FAKE, 4, 8, FAKE, FAKE + 2, None)),                                # amax alignment
