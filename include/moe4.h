@@ -238,8 +238,8 @@ int grouped_expert_gemm_nvfp4_hadamard_mx(const uint8_t *a_codes, const uint8_t 
  * MOE4_GROUP_K (wgrad): A [M, Ktot], B [N, Ktot]; D [E, M, N] with
  *   D[e] = A[:, offs[e]:offs[e+1]] * B[:, offs[e]:offs[e+1]]^T; offs[E] = Ktot = K; an empty
  *   group writes zeros (or leaves D[e] untouched with MOE4_ACCUMULATE).
- * offs entries are multiples of 128; M % 128 == 0, N % 256 == 0, K % 128 == 0.  Output
- * binary32 or bf16; MOE4_ACCUMULATE adds into a binary32 D.  Canonical scale factors are
+ * offs entries are multiples of 128; M % 128 == 0, N % 256 == 0, K % 128 == 0; M, E*N and K
+ * below 2^31 (and E*M with MOE4_GROUP_K).  Output binary32 or bf16; MOE4_ACCUMULATE adds into a binary32 D.  Canonical scale factors are
  * converted into ws (moe4_workspace_size_gemm(1, ...)). */
 int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
                        const uint8_t *b_e8, const int32_t *group_offs, int64_t E, int64_t M,

@@ -1078,6 +1078,7 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     MOE4_CHECK_ARG(gk != ((flags & MOE4_GROUP_M) != 0));
     MOE4_CHECK_ARG(!((flags & MOE4_ACCUMULATE) && bf16));
     MOE4_CHECK_ARG(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    MOE4_CHECK_ARG(!gk || E * M < (int64_t(1) << 31));  // the output's row coordinate e*M + m is an int32
     cudaStream_t st = as_stream(stream);
     Args g{};
     const uint8_t *sfa, *sfb;

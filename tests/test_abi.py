@@ -88,6 +88,8 @@ MISALIGNED = FAKE + 4
                             None, 0, None)),                                                 # both groupings
     ("grouped_gemm_mxfp8", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 128, FAKE, 0x200 | 0x2000 | 0x4000,
                             None, 0, None)),                                                 # bf16 accumulate
+    ("grouped_gemm_mxfp8", (FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 14, 1 << 17, 256, 128, FAKE, 0x100 | 0x2000,
+                            None, 0, None)),                                                 # E*M past int32
     ("moe4_route_topk", (FAKE, 4, 8, 40, FAKE, FAKE, None)),                                 # k > 32
     ("moe4_permute_plan", (FAKE, 4, 2, 8, FAKE, FAKE, FAKE, 10, FAKE, 1 << 20, None)),       # rows_cap too small
     ("moe4_permute_plan", (FAKE, 1 << 28, 8, 8, FAKE, FAKE, FAKE, 1 << 32, FAKE, 1 << 40, None)),  # rows past int32
