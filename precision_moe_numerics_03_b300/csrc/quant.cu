@@ -517,6 +517,7 @@ extern "C" int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const f
                                 int64_t rows, int64_t cols, void *out, uint32_t flags, void *stream) {
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && cols > 0 && cols % 16 == 0);
     MOE4_CHECK_ARG(codes && sf && g_dec && out && aligned16(out) && aligned16(codes));
+    MOE4_CHECK_ARG((flags & ~(MOE4_OUT_BF16 | MOE4_OUT_F32)) == 0);
     const bool bf16 = (flags & MOE4_OUT_BF16) != 0;
     MOE4_CHECK_ARG(bf16 != ((flags & MOE4_OUT_F32) != 0));
     const int64_t total = nmat * rows * (cols / 16);
