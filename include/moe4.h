@@ -357,7 +357,8 @@ int moe4_sgd_update(float *w32, const float *dw, int64_t n, float lr, uint16_t *
  * moe4_convert: the device's own conversions of binary32 in[n]: kind 0 = E2M1 code (one byte
  * per value, nearest-even, saturating, sign kept), 1 = E4M3 code (nearest-even, saturating),
  * 2 = bf16 bits (two bytes per value), 3 = E4M3 code by stochastic rounding with word
- * moe4_sr_word(seed=0, stream_id=0, idx=i) of value i.  n % 4 == 0. */
+ * moe4_sr_word(seed=0, stream_id=0, idx=i) of value i.  n % 4 == 0; in 16-byte aligned, out
+ * 4-byte aligned (8-byte for kind 2). */
 int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream);
 
 /* moe4_sr_words: the stochastic-rounding words of indices idx_base .. idx_base+n-1 (n % 4 == 0,

@@ -96,6 +96,8 @@ extern "C" size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, 
 
 extern "C" int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream) {
     MOE4_CHECK_ARG(kind >= 0 && kind <= 3 && n >= 0 && n % 4 == 0 && in && out && aligned16(in) && aligned4(out));
+    // bf16 output is stored eight bytes (four values) at a time
+    MOE4_CHECK_ARG(kind != 2 || (reinterpret_cast<uintptr_t>(out) & 7u) == 0);
     if (n == 0) return MOE4_OK;
     int64_t grid = (n / 4 + 255) / 256;
     if (grid > (int64_t)num_sms() * 16) grid = (int64_t)num_sms() * 16;

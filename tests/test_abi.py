@@ -103,6 +103,7 @@ MISALIGNED = FAKE + 4
     ("moe4_sgd_update", (FAKE, FAKE, 6, 0.1, FAKE, None)),                                   # n % 4
     ("moe4_sf_to_mma_layout", (FAKE, 1, 100, 4, FAKE, None)),                                # rows % 128
     ("moe4_convert", (7, FAKE, 4, FAKE, None)),                                              # bad kind
+    ("moe4_convert", (2, FAKE, 4, MISALIGNED, None)),                                        # bf16 out align 8
     # output scales in the tile layout need whole 128-row tiles and groups of four blocks
     ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 96, 128, FAKE, FAKE, 0, 0, 0x40000, None)),  # rows % 128
     ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 128, 64, FAKE, FAKE, 0, 0, 0x40000, None)),  # cols % 128
