@@ -1,8 +1,10 @@
 """Pins of the oracle's Philox4x32-10 and stochastic rounding.
 
-Philox: the all-zero known answer of the published generator (6627e8d5 e169c58d bc57ac4c
-9b00dbd8) and agreement with an independent implementation, Triton's `tl.philox`, executed by
-Triton's CPU interpreter in a child process (a library routine; it is never used by the product).
+Philox: the three known answers published with the generator (Salmon, Moraes, Dror and Shaw,
+"Parallel random numbers: as easy as 1, 2, 3", SC'11, and its Random123 release: all-zero
+counter and key, all-ones, and the digits of pi) and agreement with an independent
+implementation, Triton's `tl.philox`, executed by Triton's CPU interpreter in a child process
+(a library routine; it is never used by the product).
 
 Stochastic rounding ("4-bit computation from the start of Inkling 2 Small's pretraining",
 lhc.media, backward-pass paragraphs: chooses the higher or lower representable value by distance
@@ -28,6 +30,20 @@ KAT_ZERO = [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
 def test_philox_known_answer_zero(orc):
     out = orc.philox4x32_10([0, 0, 0, 0], [0, 0])
     assert [int(x) for x in out] == KAT_ZERO
+
+
+# (counter, key, answer): every counter and key word set, then the hexadecimal digits of pi
+KAT_MORE = [
+    ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+    ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+     [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+]
+
+
+@pytest.mark.parametrize("ctr,key,answer", KAT_MORE)
+def test_philox_known_answers_nonzero(orc, ctr, key, answer):
+    # non-zero keys and counters exercise the key schedule and every multiplier's high half
+    assert [int(x) for x in orc.philox4x32_10(ctr, key)] == answer
 
 
 _TRITON_CHILD = r"""
