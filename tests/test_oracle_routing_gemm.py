@@ -1,5 +1,5 @@
-"""Pins of the oracle's support steps (routing, dispatch permutation, SwiGLU, combine, SGD) and of
-its float64 reference GEMMs.
+"""Pins of the oracle's support steps (routing, dispatch permutation, SwiGLU and its gradient,
+combine and its gradient, SGD) and of its float64 reference GEMMs.
 
 Routing follows the Inkling 2 Small model card (each token goes to 8 of 384 experts; "Thinking
 Machines: Nvidia FP4 Up to 6x Faster, Runs Gain 8%", model-card update); dispatch is in NVFP4
@@ -115,3 +115,48 @@ def test_grouped_gemm_k_against_torch(orc):
         lo, hi = offs[e], offs[e + 1]
         ref = torch.from_numpy(A[:, lo:hi]).double() @ torch.from_numpy(B[:, lo:hi]).double().T
         assert np.allclose(D[e], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_swiglu_backward_against_autograd(orc):
+    # torch's autograd differentiates silu(g) * u in float64 on its own (a library routine): a
+    # dropped term, a sign or the gate/up halves swapped in the oracle's closed form fails here
+    rng = np.random.default_rng(11)
+    rows, f = 6, 24
+    gu = (rng.standard_normal((rows, 2 * f)) * 3).astype(np.float32)
+    gu[0, :4] = [0.0, -30.0, 30.0, 1e-3]
+    dh = rng.standard_normal((rows, f)).astype(np.float32)
+    g = torch.from_numpy(gu[:, :f]).double().requires_grad_(True)
+    u = torch.from_numpy(gu[:, f:]).double().requires_grad_(True)
+    (torch.nn.functional.silu(g) * u).backward(torch.from_numpy(dh).double())
+    want = torch.cat([g.grad, u.grad], dim=1).numpy()
+    got = orc.swiglu_backward(gu, dh)
+    assert got.shape == (rows, 2 * f) and got.dtype == np.float32
+    assert np.allclose(got.astype(np.float64), want, rtol=2e-7, atol=1e-30)
+
+
+def test_swiglu_forward_against_torch_silu(orc):
+    rng = np.random.default_rng(12)
+    gu = (rng.standard_normal((5, 32)) * 4).astype(np.float32)
+    g, u = torch.from_numpy(gu[:, :16]).double(), torch.from_numpy(gu[:, 16:]).double()
+    want = (torch.nn.functional.silu(g) * u).numpy()
+    assert np.allclose(orc.swiglu(gu), want, rtol=2e-7, atol=1e-30)
+
+
+def test_combine_backward_is_the_adjoint_of_the_combine(orc):
+    # <combine(yhat), dy> = <yhat, combine_backward(dy)>.  Small integers and power-of-two
+    # weights keep every product, sum and bf16 rounding exact, so the identity holds exactly;
+    # a transposed index (token for row) or a weight taken from the wrong slot breaks it
+    rng = np.random.default_rng(13)
+    T, k, d, R = 40, 4, 32, 200
+    row_of = rng.permutation(R)[:T * k].reshape(T, k).astype(np.int32)
+    w = rng.choice(np.float32([1.0, 0.5, 0.25]), size=(T, k)).astype(np.float32)
+    yh = orc.f32_to_bf16(rng.integers(-4, 5, (R, d)).astype(np.float32))
+    dy = orc.f32_to_bf16(rng.integers(-4, 5, (T, d)).astype(np.float32))
+    y = orc.bf16_to_f32(orc.combine(yh, row_of, w)).astype(np.float64)
+    dyhat = orc.bf16_to_f32(orc.combine_backward(dy, row_of, w, R)).astype(np.float64)
+    lhs = float(np.sum(y * orc.bf16_to_f32(dy)))
+    rhs = float(np.sum(orc.bf16_to_f32(yh).astype(np.float64) * dyhat))
+    assert lhs == rhs and lhs != 0.0
+    # rows no (token, slot) maps to are zero
+    unused = np.setdiff1d(np.arange(R), row_of.reshape(-1))
+    assert unused.size == R - T * k and np.all(dyhat[unused] == 0)
