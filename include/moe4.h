@@ -34,7 +34,8 @@
  *     nibble), sf uint8 E4M3 [R, C/16] ("canonical" layout), and one float per-tensor decode
  *     scale g_dec (per matrix; per expert for weights).
  *   - MXFP8 tensor [R, C]: q uint8 E4M3 [R, C], e8 uint8 E8M0 [R, C/32] (canonical layout).
- *   - Return value: MOE4_OK, or a negative status; on error nothing has been enqueued.
+ *   - Return value: MOE4_OK, or a negative status.  After MOE4_ERR_ARG or MOE4_ERR_WORKSPACE
+ *     nothing has been enqueued; after MOE4_ERR_CUDA part of the call's work may have been.
  *     Argument checks cover null pointers, sizes, divisibility and 16-byte alignment of every
  *     vector-accessed buffer.  NaN and infinite inputs are not checked and give unspecified
  *     codes.

@@ -957,6 +957,13 @@ __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t *__res
     }
 }
 
+// Whether ws holds the tensor-core copies of both operands' scale factors.
+static bool scales_ws_ok(int64_t a_rows, int64_t b_rows, int64_t K, int blk, const void *ws, size_t ws_bytes) {
+    const size_t na = (size_t)(a_rows * (K / blk)), nb = (size_t)(b_rows * (K / blk));
+    const size_t need = (na + 255) / 256 * 256 + (nb + 255) / 256 * 256;
+    return ws && ws_bytes >= need && aligned16(ws);
+}
+
 // Canonical scales -> tensor-core layout into ws when the caller did not pass that layout.
 static int stage_scales(const uint8_t *a_sf, int64_t a_rows, const uint8_t *b_sf, int64_t b_rows, int64_t K, int blk,
                         uint32_t flags, void *ws, size_t ws_bytes, const uint8_t **sfa, const uint8_t **sfb,
@@ -966,9 +973,8 @@ static int stage_scales(const uint8_t *a_sf, int64_t a_rows, const uint8_t *b_sf
         *sfb = b_sf;
         return MOE4_OK;
     }
-    const size_t na = (size_t)(a_rows * (K / blk)), nb = (size_t)(b_rows * (K / blk));
-    const size_t need = (na + 255) / 256 * 256 + (nb + 255) / 256 * 256;
-    if (!ws || ws_bytes < need || !aligned16(ws)) return MOE4_ERR_WORKSPACE;
+    if (!scales_ws_ok(a_rows, b_rows, K, blk, ws, ws_bytes)) return MOE4_ERR_WORKSPACE;
+    const size_t na = (size_t)(a_rows * (K / blk));
     uint8_t *wa = static_cast<uint8_t *>(ws);
     uint8_t *wb = wa + (na + 255) / 256 * 256;
     int rc = moe4_sf_to_mma_layout(a_sf, 1, a_rows, K / blk, wa, st);
@@ -1134,6 +1140,9 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
                    aligned16(w_bf16) && aligned4(amax_out));
     MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
     MOE4_CHECK_ARG(E * M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    // a missing workspace is reported before anything is enqueued
+    if (M > 0 && K > 0 && !(flags & MOE4_SF_MMA_LAYOUT) && !scales_ws_ok(M, N, K, 32, ws, ws_bytes))
+        return MOE4_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(amax_out, 0, (size_t)E * sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
     if (M == 0) return MOE4_OK;

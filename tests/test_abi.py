@@ -122,6 +122,14 @@ def test_missing_workspace_is_reported(lib):
     # nvfp4_quantize without AMAX_GIVEN and without ws -> MOE4_ERR_WORKSPACE, before any launch
     assert lib.nvfp4_quantize(FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, None, 0, None) == -5
     assert lib.hadamard_quant(FAKE, 4, 128, FAKE, FAKE, FAKE, 1, None, 0, None) == -5
+    # the GEMMs with canonical scales need room for their tensor-core copies
+    assert lib.grouped_expert_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE, 0x200,
+                                         None, 0, None) == -5
+    assert lib.grouped_gemm_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 128, FAKE, 0x100 | 0x1000,
+                                  None, 0, None) == -5
+    # the fused SGD reports it before clearing amax_out (nothing is enqueued on an error return)
+    assert lib.grouped_gemm_mxfp8_wgrad_sgd(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 128, 256, 256, FAKE, None, 0.1, FAKE,
+                                            0, FAKE, 64, None) == -5
 
 
 def test_python_flags_match_the_header():
@@ -130,3 +138,21 @@ def test_python_flags_match_the_header():
     assert len(defs) >= 12
     for name, value in defs.items():
         assert getattr(moe4, name) == int(value, 16), name
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """include/moe4.h compiles as strict C99 and a C program linked against libmoe4.so runs the
+    host-side calls (queries and argument checks) without Python or a GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    pkg = os.path.join(ROOT, "precision_moe_numerics_03_b300")
+    exe = str(tmp_path / "c_abi_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_check.c"), "-L", pkg, "-lmoe4", "-Wl,-rpath," + pkg,
+                    "-o", exe], check=True, capture_output=True, text=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "ok"
