@@ -38,7 +38,9 @@
  *     nothing has been enqueued; after MOE4_ERR_CUDA part of the call's work may have been.
  *     Argument checks cover null pointers, sizes, divisibility and 16-byte alignment of every
  *     vector-accessed buffer.  NaN and infinite inputs are not checked and give unspecified
- *     codes.
+ *     codes.  Index arrays that live in device memory (group_offs, row_of, src_of) are read
+ *     only by the kernels and are not checked: entries outside the ranges a call documents give
+ *     undefined results, including reads out of bounds (moe4_permute_plan produces valid ones).
  */
 #ifndef MOE4_H
 #define MOE4_H
