@@ -90,6 +90,13 @@ size_t moe4_workspace_size(int op, int64_t a, int64_t b, int64_t c);
  * the experts by group size); with less, that kernel runs its tiles in expert order. */
 size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, int64_t b_rows, int64_t K);
 
+/* moe4_check_group_offsets: checks, on the host, group offsets the caller holds in HOST memory
+ * (offs_host [E+1]) against the rules the grouped GEMMs assume of their device copy: offs[0] = 0,
+ * non-decreasing, every entry a multiple of `align` (128 for the GEMMs), offs[E] = total.
+ * Returns MOE4_OK or MOE4_ERR_ARG; reads nothing on the device and enqueues nothing.  The GEMMs
+ * themselves do not read their offsets back to check them. */
+int moe4_check_group_offsets(const int32_t *offs_host, int64_t E, int64_t total, int64_t align);
+
 /* Synchronise `stream`, then read and clear the device status word that kernels set when a
  * bounded wait gives up.  Returns MOE4_OK or MOE4_ERR_TIMEOUT (or MOE4_ERR_CUDA). */
 int moe4_get_status(void *stream);

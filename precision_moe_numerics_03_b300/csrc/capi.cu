@@ -94,6 +94,16 @@ extern "C" size_t moe4_workspace_size_gemm(int kind, int64_t a_rows, int64_t E, 
     return ((a + 255) / 256 * 256) + ((b + 255) / 256 * 256) + order;
 }
 
+extern "C" int moe4_check_group_offsets(const int32_t *offs_host, int64_t E, int64_t total, int64_t align) {
+    MOE4_CHECK_ARG(offs_host && E >= 1 && total >= 0 && align >= 1);
+    MOE4_CHECK_ARG(offs_host[0] == 0 && (int64_t)offs_host[E] == total);
+    for (int64_t e = 0; e < E; ++e) {
+        MOE4_CHECK_ARG(offs_host[e + 1] >= offs_host[e]);
+        MOE4_CHECK_ARG((int64_t)offs_host[e + 1] % align == 0);
+    }
+    return MOE4_OK;
+}
+
 extern "C" int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream) {
     MOE4_CHECK_ARG(kind >= 0 && kind <= 3 && n >= 0 && n % 4 == 0 && in && out && aligned16(in) && aligned4(out));
     // bf16 output is stored eight bytes (four values) at a time

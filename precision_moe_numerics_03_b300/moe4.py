@@ -48,6 +48,7 @@ _SIGNATURES = {
     "moe4_workspace_size_gemm": (_sz, [_int, _i64, _i64, _i64, _i64]),
     "moe4_get_status": (_int, [_vp]),
     "moe4_selftest_wait": (_int, [_i64, _vp]),
+    "moe4_check_group_offsets": (_int, [_vp, _i64, _i64, _i64]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_f32": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
@@ -152,6 +153,13 @@ def moe4_workspace_size_gemm(kind: int, a_rows: int, E: int, b_rows: int, K: int
 
 def moe4_get_status(stream=None) -> int:
     return load().moe4_get_status(_s(stream))
+
+
+def moe4_check_group_offsets(offs, total: int, align: int = 128):
+    """Host-side check of group offsets (a host array or CPU tensor of E+1 int32 values)."""
+    import numpy as np
+    a = np.ascontiguousarray(offs.cpu().numpy() if hasattr(offs, "cpu") else offs, dtype=np.int32)
+    _call("moe4_check_group_offsets", a.ctypes.data, a.size - 1, total, align)
 
 
 def moe4_selftest_wait(limit_cycles, stream=None):

@@ -156,3 +156,26 @@ def test_plain_c_caller(lib, tmp_path):
     out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "ok"
+
+
+def test_group_offsets_check_on_host(lib):
+    """moe4_check_group_offsets: the rules the grouped GEMMs assume of their offsets, checked on a
+    host copy (a group offset over the total, a decreasing entry, a ragged one, a non-zero start)."""
+    import numpy as np
+    from precision_moe_numerics_03_b300 import moe4
+
+    def check(offs, total, align=128):
+        a = np.ascontiguousarray(offs, dtype=np.int32)
+        return lib.moe4_check_group_offsets(a.ctypes.data, a.size - 1, total, align)
+
+    assert check([0, 128, 128, 512], 512) == 0            # an empty group is fine
+    assert check([0, 0], 0) == 0
+    assert check([0, 128, 640], 512) == -1                 # last offset over the total
+    assert check([0, 256, 128, 512], 512) == -1            # decreasing
+    assert check([0, 100, 512], 512) == -1                 # not a multiple of 128
+    assert check([0, 100, 200], 200, align=1) == 0
+    assert check([128, 256], 256) == -1                    # does not start at 0
+    assert lib.moe4_check_group_offsets(None, 2, 0, 128) == -1
+    moe4.moe4_check_group_offsets(np.array([0, 128, 256], np.int32), 256)
+    with pytest.raises(moe4.Moe4Error):
+        moe4.moe4_check_group_offsets(np.array([0, 384, 256], np.int32), 256)
