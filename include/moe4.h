@@ -24,7 +24,9 @@
  *
  * Conventions for every call:
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless a comment says
- *     "host".  The library never allocates device memory and never frees what it is given.
+ *     "host".  No call allocates device memory (no cudaMalloc) or frees what it is given; the
+ *     only device memory the library owns is the small static scratch array of
+ *     nvfp4_quantize_noalloc, which exists from the moment the library is loaded.
  *     Calls that need scratch take (ws, ws_bytes); moe4_workspace_size() gives the size.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
  *     only enqueues work on it and returns; nothing is synchronised unless a comment says so.
