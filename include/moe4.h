@@ -25,8 +25,8 @@
  * Conventions for every call:
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless a comment says
  *     "host".  No call allocates device memory (no cudaMalloc) or frees what it is given; the
- *     only device memory the library owns is the small static scratch array of
- *     nvfp4_quantize_noalloc, which exists from the moment the library is loaded.
+ *     library's own device data is static and exists from the moment it is loaded: the status
+ *     word of moe4_get_status and the 16 KiB scratch array of nvfp4_quantize_noalloc.
  *     Calls that need scratch take (ws, ws_bytes); moe4_workspace_size() gives the size.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
  *     only enqueues work on it and returns; nothing is synchronised unless a comment says so.
