@@ -179,3 +179,19 @@ def test_group_offsets_check_on_host(lib):
     moe4.moe4_check_group_offsets(np.array([0, 128, 256], np.int32), 256)
     with pytest.raises(moe4.Moe4Error):
         moe4.moe4_check_group_offsets(np.array([0, 384, 256], np.int32), 256)
+
+
+def test_library_exports_nothing_undeclared(lib):
+    """Every C-named function the library exports is declared in include/moe4.h (the reverse of
+    test_every_declared_symbol_is_exported): no undocumented entry point."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("no nm")
+    from precision_moe_numerics_03_b300 import moe4
+    out = subprocess.run([nm, "-D", "--defined-only", moe4.LIB_PATH], check=True, capture_output=True,
+                         text=True).stdout
+    exported = sorted({f[2] for f in (ln.split() for ln in out.splitlines())
+                       if len(f) == 3 and f[1] == "T" and not f[2].startswith("_")})
+    assert exported == _declared()
