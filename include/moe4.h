@@ -120,7 +120,9 @@ int moe4_selftest_wait(int64_t limit_cycles, void *stream);
  * Outputs: codes [nmat, rows, cols/2], sf [nmat, rows, cols/16] (canonical, or the tensor-core
  * tile layout of moe4_sf_to_mma_layout with MOE4_SF_MMA_LAYOUT, which needs rows % 128 == 0 and
  * cols % 64 == 0), g_dec [nmat].  cols % 16 == 0.
- * ws: moe4_workspace_size(MOE4_OP_NVFP4_QUANTIZE, nmat) bytes unless MOE4_AMAX_GIVEN.
+ * ws: moe4_workspace_size(MOE4_OP_NVFP4_QUANTIZE, nmat) bytes unless MOE4_AMAX_GIVEN.  Without
+ * MOE4_AMAX_GIVEN nmat is at most 65535 (the amax pass runs one grid row per matrix); beyond
+ * that MOE4_ERR_ARG, before anything is enqueued.
  * Bit-exact with the oracle: every binary32 step is one correctly rounded operation. */
 int nvfp4_quantize(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
                    uint8_t *codes, uint8_t *sf, float *g_dec, const float *amax_in,
@@ -144,8 +146,11 @@ int nvfp4_quantize_f32(const float *x, int64_t nmat, int64_t rows, int64_t cols,
  *   - Scratch: the per-matrix amax lives in a fixed array of 4096 uint32 (16 KiB) that every GPU
  *     which loads the library holds until the process exits.  nmat > 4096 returns MOE4_ERR_ARG.
  *   - Allocation: none.  The call makes no cudaMalloc or cudaFree and no allocating library call.
- *   - First call on a device: it looks up the array's device address (cudaGetSymbolAddress) and
- *     caches it per device; make that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress, which allocates nothing), so the call stays correct after the
+ *     context has been torn down and created again (cudaDeviceReset moves the array).  The first
+ *     call in a context also loads the library's device code there; make it before any stream
+ *     capture.
  *   - Every call uses the same array and clears the part it needs first; calls whose work
  *     overlaps on the GPU (on different streams, or on different host threads) race on it. */
 int nvfp4_quantize_noalloc(const uint16_t *x, int64_t nmat, int64_t rows, int64_t cols,

@@ -22,7 +22,6 @@
 // Every mbarrier wait is bounded (about two seconds of SM clock); a wait that gives up sets the
 // library status word, stops the CTA's loops, drains its own copies and MMAs, and frees tensor
 // memory before the CTA exits.
-#include <atomic>
 
 #include "common.cuh"
 
@@ -887,17 +886,12 @@ template <int KIND, int EM>
 static int launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tw, const CUtensorMap &twb,
                   const Args &a, cudaStream_t st) {
     using L = Layout<KIND, EpiCfg<EM>::template NSTK<KIND>, EpiCfg<EM>::template BYTESK<KIND>, EpiCfg<EM>::BNT>;
-    // the dynamic shared-memory limit is a per-device attribute of the kernel: set it once per
-    // device (atomically, so concurrent first calls from several host threads are harmless)
-    static std::atomic<bool> attr_set[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE4_ERR_CUDA;
-    if (!attr_set[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, EM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::SMEM) != cudaSuccess)
-            return MOE4_ERR_CUDA;
-        attr_set[dev].store(true, std::memory_order_release);
-    }
+    // the dynamic shared-memory limit is an attribute of the kernel in the current context: set
+    // on every call (a host-side call), so it also holds after the context has been torn down
+    // and created again (cudaDeviceReset), which forgets it
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, EM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM) != cudaSuccess)
+        return MOE4_ERR_CUDA;
     if (a.num_tiles == 0) return MOE4_OK;
     const int64_t grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
     grouped_gemm_kernel<KIND, EM><<<(unsigned)grid, THREADS, L::SMEM, st>>>(ta, tb, tw, twb, a);

@@ -14,7 +14,6 @@
 #include "common.cuh"
 
 #include <cfloat>
-#include <mutex>
 
 namespace moe4 {
 
@@ -473,6 +472,8 @@ static int nvfp4_quantize_impl(const TIn *x, int64_t nmat, int64_t rows, int64_t
     const bool given = (flags & MOE4_AMAX_GIVEN) != 0;
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
     MOE4_CHECK_ARG(!given || amax_in);
+    // the amax pass runs one grid row per matrix (gridDim.y at most 65535)
+    MOE4_CHECK_ARG(given || nmat <= 65535);
     MOE4_CHECK_ARG(!sf_mma || (rows % 128 == 0 && cols % 64 == 0));
     MOE4_CHECK_ARG(rows * (cols / 16) < (int64_t(1) << 32));
     cudaStream_t st = as_stream(stream);
@@ -571,25 +572,18 @@ extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const f
 // ------------------------------------------------------------------ allocation-free variant
 // nvfp4_quantize needs scratch for the per-matrix amax of its first pass.  This variant keeps
 // that scratch in a fixed array in device memory that belongs to the library, for callers that
-// cannot allocate device memory themselves (see include/moe4.h).  The array's device address is
-// looked up once per device (host code only sees a host-side stand-in for the symbol).
+// cannot allocate device memory themselves (see include/moe4.h).  Host code only sees a
+// host-side stand-in for the symbol, so every call looks up the array's device address in the
+// current context.  The lookup allocates nothing, and a fresh one per call stays right after the
+// context is torn down and created again (cudaDeviceReset), when the array may have moved.
 namespace moe4 {
 constexpr int64_t kNoAllocMaxMats = 4096;
-constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) unsigned int g_noalloc_amax[kNoAllocMaxMats];
 
 static unsigned int *noalloc_amax_address() {
-    static std::mutex mu;
-    static unsigned int *addr[kNoAllocMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<unsigned int *>(p);
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(p);
 }
 }  // namespace moe4
 

@@ -62,6 +62,8 @@ MISALIGNED = FAKE + 4
     ("nvfp4_quantize", (MISALIGNED, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, FAKE, 64, None)),
     ("nvfp4_quantize", (FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 1 << 30, FAKE, 64, None)),  # bad flag
     ("nvfp4_quantize", (FAKE, 1, 16, 16, 16, FAKE, FAKE, FAKE, None, 2, FAKE, 64, None)),   # AMAX_GIVEN, no amax
+    ("nvfp4_quantize", (FAKE, 65536, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, FAKE, 1 << 20, None)),  # amax pass grid
+    ("nvfp4_quantize_f32", (FAKE, 65536, 16, 16, 16, FAKE, FAKE, FAKE, None, 1, FAKE, 1 << 20, None)),
     ("nvfp4_dequantize", (FAKE, FAKE, FAKE, 1, 16, 16, FAKE, 0x200 | 0x10000, None)),          # canonical sf only
     ("nvfp4_dequantize", (FAKE, FAKE, FAKE, 1, 16, 16, FAKE, 0x300, None)),                    # two outputs
     ("mxfp8_requant_transpose_sr", (FAKE, FAKE, FAKE, 1, 48, 64, FAKE, FAKE, 0, 0, 4, None)),  # rows % 32

@@ -361,3 +361,120 @@ def test_mxfp8_wgrad_fused_sgd_full_size_equals_unfused():
     assert torch.equal(w_f, w_ref)
     want = wb_ref.view(torch.bfloat16).abs().reshape(E, -1).amax(dim=1).float()
     assert torch.equal(amax, want)
+
+
+@pytest.mark.parametrize("M,N", [(4096, 2048), (4096, 4096)])
+def test_mxfp8_wgrad_full_contraction_against_oracle(M, N):
+    """The contraction-grouped weight gradient at the layer's contraction lengths, against the
+    oracle: groups of 9728 rows (the size of the largest expert group of the layer step's skewed
+    routing), 1152 rows, one 128-row tile, an empty group and 256 rows, each ending in zero padding
+    rows.  A = the column-wise MXFP8 (nearest-even) of a bf16 gradient [Kt, M] (dY for the down
+    projection, dGU for gate/up); B = the dequantise -> transpose -> MXFP8 stochastic-rounding
+    requantisation of an NVFP4 forward operand [Kt, N] (H, or the gathered X).  Both operands are
+    first checked bit for bit against the oracle's own quantisation, then the binary32 dW is
+    compared element by element on 40 sampled rows of M (every column, the full contraction of
+    each group) with the oracle's float64 product, and the fused SGD update on the same operands
+    against the oracle's sgd_update of that product ("4-bit computation from the start of Inkling 2
+    Small's pretraining", backward-pass paragraphs; precisions paragraph: FP32 master weights)."""
+    sizes = [9728, 1152, 128, 0, 256]
+    pads = [37, 100, 5, 0, 128 - 77]
+    E = len(sizes)
+    offs_np = _offs(sizes)
+    Kt = int(offs_np[-1])
+    rng = np.random.default_rng(40 + N // 1024)
+    live = np.ones(Kt, bool)
+    for lo, sz, pd in zip(offs_np[:-1], sizes, pads):
+        live[lo + sz - pd:lo + sz] = False
+    g_bits = _bf16(rng, (Kt, M))
+    x_bits = _bf16(rng, (Kt, N), t=True)
+    g_bits[~live] = 0
+    x_bits[~live] = 0
+    # device operands
+    aq, ae = empty_u8(M, Kt), empty_u8(M, Kt // 32)
+    moe4.mxfp8_quantize(to_dev(g_bits), Kt, M, aq, ae, 0, 0, moe4.COLWISE)
+    xc, xs, xg = nvfp4_quantize(to_dev(x_bits), 1, Kt, N)
+    bq, be = empty_u8(N, Kt), empty_u8(N, Kt // 32)
+    moe4.mxfp8_requant_transpose_sr(xc, xs, xg, 1, Kt, N, bq, be, 9, 2, moe4.SR)
+    # oracle operands, and the device's equal to them bit for bit
+    raq, rae = oracle.mxfp8_quantize(oracle.bf16_to_f32(g_bits), colwise=True)
+    rxc, rxs, rxg = oracle.nvfp4_quantize(oracle.bf16_to_f32(x_bits))
+    rbq, rbe = oracle.mxfp8_requant_transpose(rxc, rxs, rxg, sr=True, seed=9, stream_id=2)
+    for got, want, name in ((aq, raq, "A codes"), (ae, rae, "A scales"), (bq, rbq, "B codes"), (be, rbe, "B scales")):
+        g_np = to_np(got).reshape(want.shape)
+        assert np.array_equal(g_np, want), "%s differ in %d places" % (name, int(np.sum(g_np != want)))
+    offs = to_dev(offs_np)
+    ae_t, be_t = mma_layout(ae, M, Kt // 32), mma_layout(be, N, Kt // 32)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, 1, N, Kt))
+    D = torch.full((E, M, N), np.nan, dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8(aq, ae_t, bq, be_t, offs, E, M, N, Kt, D, moe4.OUT_F32 | moe4.GROUP_K | moe4.SF_MMA_LAYOUT,
+                            None)
+    w0 = inputs.device_normal((E, M, N), 0.02, inputs.device_generator(40, N, DEV), DEV, dtype=torch.float32)
+    lr = 1e-3
+    w = w0.clone()
+    amax = torch.full((E,), -1.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8_wgrad_sgd(aq, ae_t, bq, be_t, offs, E, M, N, Kt, w, None, lr, amax, moe4.SF_MMA_LAYOUT,
+                                      ws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    rows = np.unique(np.concatenate([np.random.default_rng(N).choice(M, 38, replace=False), [0, M - 1]]))
+    rows_d = torch.as_tensor(rows, device=DEV)
+    ra = oracle.mxfp8_dequantize(raq, rae)[rows]
+    rb = oracle.mxfp8_dequantize(rbq, rbe)
+    Dref, S = oracle.grouped_gemm_k(ra, rb, offs_np)
+    Dg = to_np(D[:, rows_d])
+    for e in range(E):
+        check_f32(Dg[e], Dref[e], S[e], "wgrad expert %d (%d rows)" % (e, sizes[e]))
+    assert np.all(Dg[3] == 0)
+    # the fused update against the oracle's SGD of the oracle's product: the product's error
+    # (2^-16 * S, times lr) plus one rounding of the step and one of the difference
+    w0_np = to_np(w0[:, rows_d])
+    w_ref, _ = oracle.sgd_update(w0_np, Dref.astype(np.float32), lr)
+    got = to_np(w[:, rows_d]).astype(np.float64)
+    tol = lr * ELEM * S + 2.0 ** -23 * (lr * np.abs(Dref) + np.abs(w_ref.astype(np.float64)))
+    bad = np.abs(got - w_ref) > tol
+    assert not bad.any(), "%d of %d updated weights outside the bound" % (int(bad.sum()), bad.size)
+    assert torch.equal(w[3], w0[3])  # the empty group keeps its weights
+    want_amax = torch.stack([w[e].to(torch.bfloat16).abs().max().float() for e in range(E)])
+    assert torch.equal(amax, want_amax)
+
+
+def test_nvfp4_down_bf16_full_size_sampled_rows():
+    """The layer step's down-projection GEMM as it runs there: H [padded rows, 2048] (Student-t(3),
+    zero on the padding rows of a top-8 plan over 384 experts) quantised to NVFP4 with one
+    per-tensor scale, times 384 experts' down weights [4096, 2048] N(0, 0.02) with per-expert
+    scales, tile-layout scales, bf16 output.  Checked on sampled rows of three experts (the largest
+    group, the first and the last non-empty one) against the oracle's float64 product of its own
+    quantisation (H rows with the whole tensor's amax, each expert's weights with its own)."""
+    T, d, f, E, k = 16384, 4096, 2048, 384, 8
+    rng = np.random.default_rng(0)
+    lg = (rng.standard_normal((T, E)) + rng.standard_normal(E)).astype(np.float32)
+    idx, _ = oracle.route_topk(lg, k)
+    roffs, rrow = oracle.permute_plan(idx, E)
+    Rp = int(roffs[-1])
+    real = np.zeros(Rp, bool)
+    real[rrow.reshape(-1)] = True
+    h = inputs.device_student_t((Rp, f), inputs.device_generator(22, 0, DEV), DEV).view(torch.int16)
+    h[torch.as_tensor(~real, device=DEV)] = 0
+    w = inputs.device_normal((E * d, f), 0.02, inputs.device_generator(22, 1, DEV), DEV).view(torch.int16)
+    hc, hs, hg = nvfp4_quantize(h, 1, Rp, f, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    wc, wsf, wg = nvfp4_quantize(w, E, d, f, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    Y = torch.empty((Rp, d), dtype=torch.int16, device=DEV)
+    gws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, Rp, E, d, f))
+    moe4.grouped_expert_gemm_nvfp4(hc, hs, hg, wc, wsf, wg, to_dev(roffs), E, Rp, d, f, Y,
+                                   moe4.OUT_BF16 | moe4.SF_MMA_LAYOUT, gws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    del wc, wsf, hc, hs
+    h32 = oracle.bf16_to_f32(to_np(h, np.uint16))
+    h_amax = np.abs(h32).max()
+    sizes = np.diff(roffs)
+    live = np.nonzero(sizes)[0]
+    for e in [int(np.argmax(sizes)), int(live[0]), int(live[-1])]:
+        lo, hi = int(roffs[e]), int(roffs[e + 1])
+        rows = np.unique(np.concatenate([np.random.default_rng(e).choice(np.arange(lo, hi), 12), [lo, hi - 1]]))
+        rhc, rhs, rhg = oracle.nvfp4_quantize(h32[rows], amax=h_amax)
+        we = oracle.bf16_to_f32(to_np(w[e * d:(e + 1) * d], np.uint16))
+        rwc, rws, rwg = oracle.nvfp4_quantize(we)
+        Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rhc, rhs, rhg),
+                                        oracle.nvfp4_dequantize(rwc, rws, rwg)[None], np.array([0, len(rows)]))
+        check_bf16(to_np(Y[torch.as_tensor(rows, device=DEV)], np.uint16), Dref, S)
