@@ -168,10 +168,12 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *sf, const float *g_dec
  * scale exponent e = smallest integer with blockamax <= 448 * 2^e, clamped to [-127, 127], stored
  * as e + 127; elements v = x_hat * 2^-e rounded to E4M3 stochastically (MOE4_SR) or to
  * nearest-even.  Stochastic rounding of the element with linear index idx in the output
- * [nmat, cols, rows] uses word idx % 4 of Philox4x32-10(counter = (lo(idx/4), hi(idx/4),
- * stream_id, 0), key = (lo(seed), hi(seed))) and rounds the magnitude up iff
- * word < floor(frac * 2^32), frac being its distance above the E4M3 value below, in units of
- * the gap.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
+ * [nmat, cols, rows] draws a 16-bit number r: half idx % 2 (0 = low) of word (idx / 2) % 4 of
+ * Philox4x32-10(counter = (lo(idx/8), hi(idx/8), stream_id, 0), key = (lo(seed), hi(seed))), so one
+ * call serves eight consecutive elements; the magnitude rounds up iff r < floor(frac * 2^16),
+ * frac being its distance above the E4M3 value below, in units of the gap.  The probability of
+ * rounding up is therefore frac less at most 2^-16: the expected result lies within 2^-16 of a
+ * gap of the value, toward zero.  Outputs q_t [nmat, cols, rows], e8_t [nmat, cols, rows/32] (canonical).
  * rows % 32 == 0, cols % 32 == 0.  Input scales canonical, or in the tensor-core tile layout with
  * MOE4_SF_MMA_LAYOUT (rows % 128 == 0, cols % 64 == 0).  With MOE4_SF_OUT_MMA, e8_t is written in
  * the tensor-core tile layout of moe4_sf_to_mma_layout (as [nmat * cols, rows / 32]; rows % 128
@@ -373,14 +375,15 @@ int moe4_sgd_update(float *w32, const float *dw, int64_t n, float lr, uint16_t *
 /* ------------------------------------------------------------------ conversions (for checks)
  * moe4_convert: the device's own conversions of binary32 in[n]: kind 0 = E2M1 code (one byte
  * per value, nearest-even, saturating, sign kept), 1 = E4M3 code (nearest-even, saturating),
- * 2 = bf16 bits (two bytes per value), 3 = E4M3 code by stochastic rounding with word
- * moe4_sr_word(seed=0, stream_id=0, idx=i) of value i.  n % 4 == 0; in 16-byte aligned, out
- * 4-byte aligned (8-byte for kind 2). */
+ * 2 = bf16 bits (two bytes per value), 3 = E4M3 code by stochastic rounding of value i with the
+ * 16-bit number of index i that moe4_sr_words(seed=0, stream_id=0) gives.  n % 4 == 0; in 16-byte
+ * aligned, out 4-byte aligned (8-byte for kind 2). */
 int moe4_convert(int kind, const float *in, int64_t n, void *out, void *stream);
 
-/* moe4_sr_words: the stochastic-rounding words of indices idx_base .. idx_base+n-1 (n % 4 == 0,
- * idx_base % 4 == 0), uint32 out[n]. */
-int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint32_t *out,
+/* moe4_sr_words: the 16-bit stochastic-rounding numbers of output indices idx_base ..
+ * idx_base+n-1 (see mxfp8_requant_transpose_sr), uint16 out[n]; n % 8 == 0, idx_base % 8 == 0,
+ * out 16-byte aligned. */
+int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint16_t *out,
                   void *stream);
 
 #ifdef __cplusplus

@@ -76,8 +76,8 @@ def lib() -> ctypes.CDLL:
             "orc_e2m1_rne_sat_range": (None, [ctypes.c_uint32, _u64, _u8p]),
             "orc_e4m3_rne_sat_range": (None, [ctypes.c_uint32, _u64, _u8p]),
             "orc_bf16_rne_array": (None, [_f32p, _i64, _u16p]),
-            "orc_sr_words": (None, [_u64, ctypes.c_uint32, _u64, _i64, _u32p]),
-            "orc_e4m3_sr_array": (None, [_f32p, _u32p, _i64, _u8p]),
+            "orc_sr_words": (None, [_u64, ctypes.c_uint32, _u64, _i64, _u16p]),
+            "orc_e4m3_sr_array": (None, [_f32p, _u16p, _i64, _u8p]),
             "orc_e4m3_rne_sat_array": (None, [_f32p, _i64, _u8p]),
             "orc_e2m1_rne_sat_array": (None, [_f32p, _i64, _u8p]),
         }
@@ -171,16 +171,18 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 
 def sr_words(seed: int, stream_id: int, idx_base: int, n: int) -> np.ndarray:
-    out = np.empty(n, np.uint32)
-    lib().orc_sr_words(seed, stream_id, idx_base, n, _p(out, _u32p))
+    """The 16-bit stochastic-rounding numbers of output indices idx_base .. idx_base+n-1."""
+    out = np.empty(n, np.uint16)
+    lib().orc_sr_words(seed, stream_id, idx_base, n, _p(out, _u16p))
     return out
 
 
-def e4m3_sr(v, r32) -> np.ndarray:
+def e4m3_sr(v, r16) -> np.ndarray:
+    """Stochastic rounding of binary32 v to E4M3 codes with 16-bit numbers r16 (one per value)."""
     v = np.ascontiguousarray(v, dtype=np.float32)
-    r = np.ascontiguousarray(r32, dtype=np.uint32)
+    r = np.ascontiguousarray(r16, dtype=np.uint16)
     out = np.empty(v.shape, np.uint8)
-    lib().orc_e4m3_sr_array(_p(v, _f32p), _p(r, _u32p), v.size, _p(out, _u8p))
+    lib().orc_e4m3_sr_array(_p(v, _f32p), _p(r, _u16p), v.size, _p(out, _u8p))
     return out
 
 

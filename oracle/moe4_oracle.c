@@ -156,26 +156,31 @@ void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The random word of one element.  The pages ask only that stochastic rounding keep the value on
- * average.  Reading: the word is keyed on (seed, element index): idx is the element's linear
- * index in the OUTPUT array; Philox is run on counter (lo(idx/4), hi(idx/4), stream_id, 0) with
- * key (lo(seed), hi(seed)), and word idx%4 of its output is used. */
+/* The random number of one element.  The pages ask only that stochastic rounding keep the value
+ * on average.  Reading: each element draws a 16-bit number keyed on (seed, element index), idx
+ * being the element's linear index in the OUTPUT array.  Philox runs on counter (lo(idx/8),
+ * hi(idx/8), stream_id, 0) with key (lo(seed), hi(seed)); the element takes word (idx/2) % 4 of
+ * the output, its low 16 bits when idx is even and its high 16 bits when idx is odd.  One Philox
+ * call therefore serves eight consecutive elements. */
 uint32_t orc_sr_word(uint64_t seed, uint32_t stream_id, uint64_t idx)
 {
-    uint64_t j = idx >> 2;
+    uint64_t j = idx >> 3;
     uint32_t ctr[4] = {(uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t out[4];
     orc_philox4x32_10(ctr, key, out);
-    return out[idx & 3];
+    uint32_t word = out[(idx >> 1) & 3];
+    return (idx & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
 /* Stochastic rounding of binary32 v to E4M3 [LHC, backward-pass paragraphs: "probabilistically
  * chooses the higher or lower representable value based on their distance"].  lo is the largest
  * E4M3 magnitude <= |v|, hi the next one; frac = (|v| - lo) / (hi - lo) (exact in double); the
- * magnitude rounds up to hi iff r32 < floor(frac * 2^32).  Magnitudes >= 448 give 448.  The
- * sign is applied afterwards. */
-uint32_t orc_e4m3_sr(float v, uint32_t r32)
+ * magnitude rounds up to hi iff r16 < floor(frac * 2^16), r16 being the element's 16-bit number.
+ * The probability of rounding up is floor(frac * 2^16) / 2^16: frac less at most 2^-16, so the
+ * value is kept on average to within 2^-16 of a gap.  Magnitudes >= 448 give 448.  The sign is
+ * applied afterwards. */
+uint32_t orc_e4m3_sr(float v, uint32_t r16)
 {
     uint32_t sign = (f2u(v) >> 31) << 7;
     double a = fabs((double)v);
@@ -183,8 +188,8 @@ uint32_t orc_e4m3_sr(float v, uint32_t r32)
     int c = grid_floor(a, e4m3_grid, 127);
     double lo = e4m3_grid(c), hi = e4m3_grid(c + 1);
     double frac = (a - lo) / (hi - lo);
-    uint64_t threshold = (uint64_t)floor(frac * 4294967296.0);
-    return sign | (uint32_t)((uint64_t)r32 < threshold ? c + 1 : c);
+    uint32_t threshold = (uint32_t)floor(frac * 65536.0);
+    return sign | (uint32_t)(r16 < threshold ? c + 1 : c);
 }
 
 /* ============================================================================================
@@ -519,14 +524,14 @@ void orc_bf16_rne_array(const float *x, int64_t n, uint16_t *out)
     for (int64_t i = 0; i < n; ++i) out[i] = (uint16_t)orc_bf16_rne(x[i]);
 }
 
-void orc_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint32_t *out)
+void orc_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint16_t *out)
 {
-    for (int64_t i = 0; i < n; ++i) out[i] = orc_sr_word(seed, stream_id, idx_base + (uint64_t)i);
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint16_t)orc_sr_word(seed, stream_id, idx_base + (uint64_t)i);
 }
 
-void orc_e4m3_sr_array(const float *v, const uint32_t *r32, int64_t n, uint8_t *out)
+void orc_e4m3_sr_array(const float *v, const uint16_t *r16, int64_t n, uint8_t *out)
 {
-    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_e4m3_sr(v[i], r32[i]);
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_e4m3_sr(v[i], r16[i]);
 }
 
 void orc_e4m3_rne_sat_array(const float *v, int64_t n, uint8_t *out)

@@ -23,9 +23,11 @@ __global__ void __launch_bounds__(256) convert_kernel(int kind, const float *__r
             const uint32_t hi = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
             reinterpret_cast<uint2 *>(out)[q] = make_uint2(lo, hi);
         } else {
-            // the kernels' four-at-a-time rounding (integer fast path, per-element path otherwise)
+            // the kernels' four-at-a-time rounding (integer fast path, per-element path otherwise);
+            // indices 4q .. 4q+3 are half of Philox call q/2
+            const Philox4 P = sr_words8_not((uint64_t)q >> 1, 0u, keys);
             reinterpret_cast<uint32_t *>(out)[q] =
-                e4m3x4_sr_nw(v.x, v.y, v.z, v.w, sr_words4_not((uint64_t)q, 0u, keys));
+                (q & 1) ? e4m3x4_sr_nw(v.x, v.y, v.z, v.w, P.z, P.w) : e4m3x4_sr_nw(v.x, v.y, v.z, v.w, P.x, P.y);
         }
     }
 }
@@ -33,7 +35,7 @@ __global__ void __launch_bounds__(256) convert_kernel(int kind, const float *__r
 __global__ void __launch_bounds__(256) sr_words_kernel(const PhiloxKeys keys, uint32_t stream_id, uint64_t j0, int64_t nq,
                                                        uint4 *__restrict__ out) {
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nq; q += (int64_t)gridDim.x * blockDim.x) {
-        const Philox4 w = sr_words4(j0 + (uint64_t)q, stream_id, keys);
+        const Philox4 w = sr_words8(j0 + (uint64_t)q, stream_id, keys);  // the numbers of 8 indices
         out[q] = make_uint4(w.x, w.y, w.z, w.w);
     }
 }
@@ -115,13 +117,13 @@ extern "C" int moe4_convert(int kind, const float *in, int64_t n, void *out, voi
     return launch_status();
 }
 
-extern "C" int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint32_t *out,
+extern "C" int moe4_sr_words(uint64_t seed, uint32_t stream_id, uint64_t idx_base, int64_t n, uint16_t *out,
                              void *stream) {
-    MOE4_CHECK_ARG(n >= 0 && n % 4 == 0 && idx_base % 4 == 0 && out && aligned16(out));
+    MOE4_CHECK_ARG(n >= 0 && n % 8 == 0 && idx_base % 8 == 0 && out && aligned16(out));
     if (n == 0) return MOE4_OK;
-    int64_t grid = (n / 4 + 255) / 256;
+    int64_t grid = (n / 8 + 255) / 256;
     if (grid > (int64_t)num_sms() * 16) grid = (int64_t)num_sms() * 16;
-    sr_words_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(philox_keys(seed), stream_id, idx_base / 4, n / 4,
+    sr_words_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(philox_keys(seed), stream_id, idx_base / 8, n / 8,
                                                                    reinterpret_cast<uint4 *>(out));
     return launch_status();
 }

@@ -163,15 +163,20 @@ __device__ __forceinline__ Philox4 philox4x32_10_not(uint32_t c0, uint32_t c1, u
             c0 * 0x2DAEE0ADu + 0xFFFFFFFFu};
 }
 
-// The four stochastic-rounding words of output indices 4j .. 4j+3.
-__device__ __forceinline__ Philox4 sr_words4(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
+// ------------------------------------------------------------------ stochastic-rounding numbers
+// Every element draws a 16-bit number keyed on (seed, its index idx in the output array): the
+// eight output indices 8j .. 8j+7 share Philox4x32-10 call j, on counter (lo(j), hi(j),
+// stream_id, 0) and key (lo(seed), hi(seed)); element 8j + 2i + h takes half h (0 low, 1 high)
+// of output word i.  So the four words of call j, stored in order, are the eight numbers in
+// index order (little-endian 16-bit halves).
+__device__ __forceinline__ Philox4 sr_words8(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
     return philox4x32_10((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, K);
 }
-// Their complements; the 32-bit form is for tensors of at most 2^34 values (counter word 1 zero).
-__device__ __forceinline__ Philox4 sr_words4_not(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
+// Their complements; the 32-bit form is for tensors of at most 2^35 values (counter word 1 zero).
+__device__ __forceinline__ Philox4 sr_words8_not(uint64_t j, uint32_t stream_id, const PhiloxKeys K) {
     return philox4x32_10_not((uint32_t)j, (uint32_t)(j >> 32), stream_id, 0u, K);
 }
-__device__ __forceinline__ Philox4 sr_words4_not32(uint32_t j, uint32_t stream_id, const PhiloxKeys K) {
+__device__ __forceinline__ Philox4 sr_words8_not32(uint32_t j, uint32_t stream_id, const PhiloxKeys K) {
     return philox4x32_10_not(j, 0u, stream_id, 0u, K);
 }
 
@@ -198,20 +203,20 @@ __device__ __forceinline__ float mx_inv_scale_fs(uint32_t fs) { return __uint_as
 // 2^-e as binary32 for e in [-127, 126].
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
 
-// Stochastic rounding of v (|v| <= 448) to an E4M3 code with random word r: the magnitude goes
-// up to the next E4M3 value iff r < floor(frac * 2^32), frac = distance above the value below in
-// units of the gap.  E4M3 normal range (|v| >= 2^-6): the value below keeps v's top 3 mantissa
-// bits, so its code is ((bits >> 20) & 0x7FF) - 960 (exponent rebias 127 -> 7, 3 mantissa
-// bits), the next value is code + 1, and the threshold is v's low 20 mantissa bits moved to the
-// top (bits << 12).  Subnormal range (|v| < 2^-6): the gap is 2^-9 and the code floor(|v|*512).
+// Stochastic rounding of v (|v| <= 448) to an E4M3 code with the element's 16-bit number r: the
+// magnitude goes up to the next E4M3 value iff r < floor(frac * 2^16), frac = distance above the
+// value below in units of the gap.  E4M3 normal range (|v| >= 2^-6): the value below keeps v's
+// top 3 mantissa bits, so its code is ((bits >> 20) & 0x7FF) - 960 (exponent rebias 127 -> 7, 3
+// mantissa bits), the next value is code + 1, and floor(frac * 2^16) is v's low 20 mantissa bits
+// shifted right by 4.  Subnormal range (|v| < 2^-6): the gap is 2^-9 and the code floor(|v|*512).
 __device__ __forceinline__ uint32_t e4m3_sr_normal(uint32_t bits, uint32_t r) {
-    return (((bits >> 20) & 0x7FFu) - 960u + (r < (bits << 12) ? 1u : 0u)) | ((bits >> 24) & 0x80u);
+    return (((bits >> 20) & 0x7FFu) - 960u + (r < ((bits & 0xFFFFFu) >> 4) ? 1u : 0u)) | ((bits >> 24) & 0x80u);
 }
 __device__ __forceinline__ bool e4m3_is_normal(uint32_t bits) { return (bits & 0x7FFFFFFFu) >= 0x3C800000u; }
 __device__ __forceinline__ uint32_t e4m3_sr_small(uint32_t bits, uint32_t r) {
     const float s = __fmul_rn(__uint_as_float(bits & 0x7FFFFFFFu), 512.0f);
     const uint32_t fl = __float2uint_rz(s);
-    const uint32_t thr = __float2uint_rz(__fmul_rn(__fsub_rn(s, __uint2float_rz(fl)), 4294967296.0f));
+    const uint32_t thr = __float2uint_rz(__fmul_rn(__fsub_rn(s, __uint2float_rz(fl)), 65536.0f));
     return (fl + (r < thr ? 1u : 0u)) | ((bits >> 24) & 0x80u);
 }
 // Zero (+-0) needs no arithmetic; the float path for tiny non-zero values is a rarely taken branch.
@@ -221,52 +226,46 @@ __device__ __forceinline__ uint32_t e4m3_sr(float v, uint32_t r) {
     if ((bits & 0x7FFFFFFFu) == 0u) return (bits >> 24) & 0x80u;
     return e4m3_sr_small(bits, r);
 }
-// Four values at once (byte i = element i).  When each is zero or has |v| >= 2^-6 (the usual
-// case) the decision is made by integer addition: adding (~r) >> 12 = 2^20 - 1 - (r >> 12) to the
-// binary32 bits carries into bit 20 exactly when (r >> 12) < low20, i.e. when r < low20 * 2^12,
-// the rule above; masking the low 20 bits then leaves the chosen E4M3 value (|v| <= 448 keeps the
-// carry below the sign bit and the result finite), which the nearest-even conversion returns
-// unchanged.  Any other lane takes the per-element path.
-__device__ __forceinline__ uint32_t e4m3x4_sr(float v0, float v1, float v2, float v3, const Philox4 w) {
-    const uint32_t b0 = __float_as_uint(v0), b1 = __float_as_uint(v1);
-    const uint32_t b2 = __float_as_uint(v2), b3 = __float_as_uint(v3);
-    // 2*bits - 2 (mod 2^32) drops the sign and sends +-0 to the top: >= 2*0x3C800000 - 2 iff the
-    // value is zero or at least 2^-6 in magnitude
-    const uint32_t t = min(min(b0 * 2u - 2u, b1 * 2u - 2u), min(b2 * 2u - 2u, b3 * 2u - 2u));
-    if (t >= 0x78FFFFFEu) {
-        const float m0 = __uint_as_float((b0 + (~w.x >> 12)) & 0xFFF00000u);
-        const float m1 = __uint_as_float((b1 + (~w.y >> 12)) & 0xFFF00000u);
-        const float m2 = __uint_as_float((b2 + (~w.z >> 12)) & 0xFFF00000u);
-        const float m3 = __uint_as_float((b3 + (~w.w >> 12)) & 0xFFF00000u);
-        return e4m3x4_rn(m0, m1, m2, m3);
-    }
-    return e4m3_sr(v0, w.x) | (e4m3_sr(v1, w.y) << 8) | (e4m3_sr(v2, w.z) << 16) | (e4m3_sr(v3, w.w) << 24);
+// The integer-carry form for a value that is zero or at least 2^-6 in magnitude, with nw = ~word
+// (each 16-bit half of nw is 0xFFFF - r of its element).  Adding 16 * (0xFFFF - r) to the binary32
+// bits carries into bit 20 exactly when r < (low20 >> 4), the rule above (the low 4 bits of low20
+// cannot complete a carry on their own); masking the low 20 bits then leaves the chosen E4M3
+// value (|v| <= 448 keeps the carry below the sign bit and the result finite), which the
+// nearest-even conversion returns unchanged.
+//   low half:  16 * (0xFFFF - r) = nw's low 16 bits inserted at bit 4 (one bfi);
+//   high half: nw >> 12 = 16 * (0xFFFF - r) plus a nibble of the low half, added to the bits with
+//              their own low nibble cleared, where that nibble cannot carry (one high multiply-add).
+__device__ __forceinline__ uint32_t sr_carry_lo(uint32_t bits, uint32_t nw) {
+    uint32_t x;
+    asm("bfi.b32 %0, %1, %2, 4, 16;" : "=r"(x) : "r"(nw), "r"(0u));
+    return (bits + x) & 0xFFF00000u;
 }
-// bits + ((~r) >> 12) as one high multiply-add: hi32(~r * 2^20) + bits.
-__device__ __forceinline__ uint32_t sr_carry(uint32_t bits, uint32_t nr) {
+__device__ __forceinline__ uint32_t sr_carry_hi(uint32_t bits, uint32_t nw) {
     uint32_t t;
-    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(t) : "r"(nr), "r"(1u << 20), "r"(bits));
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(t) : "r"(nw), "r"(1u << 20), "r"(bits & 0xFFFFFFF0u));
     return t & 0xFFF00000u;
 }
-// The fast-path test of e4m3x4_sr for four values: 2*bits - 2 (mod 2^32) drops the sign and sends
-// +-0 to the top, so the minimum is >= 2*0x3C800000 - 2 iff each value is zero or at least 2^-6 in
-// magnitude.
+// The fast-path test for four values: 2*bits - 2 (mod 2^32) drops the sign and sends +-0 to the
+// top, so the minimum is >= 2*0x3C800000 - 2 iff each value is zero or at least 2^-6 in magnitude.
 constexpr uint32_t kSrFastMin = 0x78FFFFFEu;
 __device__ __forceinline__ uint32_t sr_fast_key4(float v0, float v1, float v2, float v3) {
     return min(min(__float_as_uint(v0) * 2u - 2u, __float_as_uint(v1) * 2u - 2u),
                min(__float_as_uint(v2) * 2u - 2u, __float_as_uint(v3) * 2u - 2u));
 }
-// The integer-carry rounding of four values that passed that test, with complemented words ~r.
-__device__ __forceinline__ uint32_t e4m3x4_sr_fast(float v0, float v1, float v2, float v3, const Philox4 nw) {
-    return e4m3x4_rn(__uint_as_float(sr_carry(__float_as_uint(v0), nw.x)),
-                     __uint_as_float(sr_carry(__float_as_uint(v1), nw.y)),
-                     __uint_as_float(sr_carry(__float_as_uint(v2), nw.z)),
-                     __uint_as_float(sr_carry(__float_as_uint(v3), nw.w)));
+// Four consecutive elements (byte i = element i) that passed that test, their numbers in the
+// complemented words n01 (elements 0, 1) and n23 (elements 2, 3).
+__device__ __forceinline__ uint32_t e4m3x4_sr_fast(float v0, float v1, float v2, float v3, uint32_t n01,
+                                                   uint32_t n23) {
+    return e4m3x4_rn(__uint_as_float(sr_carry_lo(__float_as_uint(v0), n01)),
+                     __uint_as_float(sr_carry_hi(__float_as_uint(v1), n01)),
+                     __uint_as_float(sr_carry_lo(__float_as_uint(v2), n23)),
+                     __uint_as_float(sr_carry_hi(__float_as_uint(v3), n23)));
 }
-// e4m3x4_sr with the complemented words ~r (sr_words4_not).
-__device__ __forceinline__ uint32_t e4m3x4_sr_nw(float v0, float v1, float v2, float v3, const Philox4 nw) {
-    if (sr_fast_key4(v0, v1, v2, v3) >= kSrFastMin) return e4m3x4_sr_fast(v0, v1, v2, v3, nw);
-    return e4m3_sr(v0, ~nw.x) | (e4m3_sr(v1, ~nw.y) << 8) | (e4m3_sr(v2, ~nw.z) << 16) | (e4m3_sr(v3, ~nw.w) << 24);
+// The same for any four values: the fast path when it applies, else element by element.
+__device__ __forceinline__ uint32_t e4m3x4_sr_nw(float v0, float v1, float v2, float v3, uint32_t n01, uint32_t n23) {
+    if (sr_fast_key4(v0, v1, v2, v3) >= kSrFastMin) return e4m3x4_sr_fast(v0, v1, v2, v3, n01, n23);
+    return e4m3_sr(v0, ~n01 & 0xFFFFu) | (e4m3_sr(v1, ~n01 >> 16) << 8) | (e4m3_sr(v2, ~n23 & 0xFFFFu) << 16) |
+           (e4m3_sr(v3, ~n23 >> 16) << 24);
 }
 
 // max(|a|, |b|) per 16-bit half (f16 or bf16); the sign bit of each half is the XOR of the

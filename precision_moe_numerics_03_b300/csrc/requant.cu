@@ -10,7 +10,8 @@
 // thread reads one row's 32 values (16 code bytes and two scale bytes, or 64 bytes of bf16) and
 // stores them as 16 column pairs, one 32-bit word each, in the transposed shared tile.  Phase 2:
 // each warp emits two output rows (one column pair) of 128 values: lane l owns 4 consecutive
-// values of each (one Philox call gives their 4 words), 8 lanes form one 32-block.
+// values of each (two lanes share the Philox calls that give their 16-bit numbers), 8 lanes form
+// one 32-block.
 #include "common.cuh"
 
 namespace moe4 {
@@ -73,26 +74,31 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
     const int64_t idx = rowA * R + r0 + 4 * lane;
     uint32_t qa, qb;
     if constexpr (kSR) {
-        Philox4 wa, wb;
-        if constexpr (kJ32) {
-            const uint32_t j = (uint32_t)((uint64_t)idx >> 2);
-            wa = sr_words4_not32(j, stream_id, keys);
-            wb = sr_words4_not32(j + (uint32_t)(R >> 2), stream_id, keys);
-        } else {
-            const uint64_t j = (uint64_t)idx >> 2;
-            wa = sr_words4_not(j, stream_id, keys);
-            wb = sr_words4_not(j + (uint64_t)(R >> 2), stream_id, keys);
-        }
+        // the 16-bit numbers of this lane's values: indices idx .. idx+3 (row A) and idx+R ..
+        // idx+R+3 (row B), with idx % 8 = 4 * (lane & 1) (R and r0 are multiples of 32); lanes 2m
+        // and 2m+1 share one Philox call per row, so the even lane runs row A's call, the odd lane
+        // row B's, and each hands its partner the two words of the partner's half
+        const bool odd = (lane & 1) != 0;
+        const int64_t i8 = rowA * R + r0 + 8 * (lane >> 1) + (odd ? R : 0);
+        Philox4 P;
+        if constexpr (kJ32)
+            P = sr_words8_not32((uint32_t)((uint64_t)i8 >> 3), stream_id, keys);
+        else
+            P = sr_words8_not((uint64_t)i8 >> 3, stream_id, keys);
+        const uint32_t g0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? P.x : P.z, 1);
+        const uint32_t g1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? P.y : P.w, 1);
+        const uint32_t a01 = odd ? g0 : P.x, a23 = odd ? g1 : P.y;
+        const uint32_t b01 = odd ? P.z : g0, b23 = odd ? P.w : g1;
         if (safe) {  // the tile's scales rule out non-zero values below 2^-6 (see the kernel)
-            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], wa);
-            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], wb);
+            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], a01, a23);
+            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], b01, b23);
         } else if (min(sr_fast_key4(va[0], va[1], va[2], va[3]), sr_fast_key4(vb[0], vb[1], vb[2], vb[3])) >=
                    kSrFastMin) {  // one test for the eight values (the per-element path is rare)
-            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], wa);
-            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], wb);
+            qa = e4m3x4_sr_fast(va[0], va[1], va[2], va[3], a01, a23);
+            qb = e4m3x4_sr_fast(vb[0], vb[1], vb[2], vb[3], b01, b23);
         } else {
-            qa = e4m3x4_sr_nw(va[0], va[1], va[2], va[3], wa);
-            qb = e4m3x4_sr_nw(vb[0], vb[1], vb[2], vb[3], wb);
+            qa = e4m3x4_sr_nw(va[0], va[1], va[2], va[3], a01, a23);
+            qb = e4m3x4_sr_nw(vb[0], vb[1], vb[2], vb[3], b01, b23);
         }
     } else {
         qa = e4m3x4_rn(va[0], va[1], va[2], va[3]);
@@ -385,8 +391,9 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
         const float v0 = __fmul_rn(x4[0], s), v1 = __fmul_rn(x4[1], s);
         const float v2 = __fmul_rn(x4[2], s), v3 = __fmul_rn(x4[3], s);
         uint32_t packed;
-        if (sr) {
-            packed = e4m3x4_sr_nw(v0, v1, v2, v3, sr_words4_not((uint64_t)gidx, stream_id, keys));
+        if (sr) {  // indices 4*gidx .. 4*gidx+3: half of Philox call gidx/2 (see sr_words8)
+            const Philox4 P = sr_words8_not((uint64_t)gidx >> 1, stream_id, keys);
+            packed = (gidx & 1) ? e4m3x4_sr_nw(v0, v1, v2, v3, P.z, P.w) : e4m3x4_sr_nw(v0, v1, v2, v3, P.x, P.y);
         } else {
             packed = e4m3x4_rn(v0, v1, v2, v3);
         }
@@ -424,8 +431,8 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, nmat, grid));
     if (rows == 0) return MOE4_OK;
-    // output indices below 2^34: the Philox counter's second word is zero throughout
-    const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 34);
+    // output indices below 2^35: the Philox counter's second word is zero throughout
+    const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 35);
     const PhiloxKeys keys = philox_keys(seed);
     cudaStream_t st = as_stream(stream);
 #define MOE4_REQUANT_ARGS                                                                                        \
@@ -463,7 +470,7 @@ extern "C" int mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uin
         dim3 grid;
         MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, 1, grid));
         if (rows == 0) return MOE4_OK;
-        if (sr && (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 34))
+        if (sr && (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 35))
             requant_transpose_kernel<SrcKind::Bf16, true><<<grid, 256, 0, st>>>(
                 nullptr, nullptr, nullptr, x, 1, rows, cols, q, e8, philox_keys(seed), stream_id, false);
         else if (sr)

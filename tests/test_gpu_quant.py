@@ -327,12 +327,12 @@ def test_device_stochastic_rounding_and_words():
     v[1024:1024 + 4 * 64:4] = edges[np.arange(64) % edges.size]
     out = torch.empty(n, dtype=torch.uint8, device=DEV)
     moe4.moe4_convert(3, to_dev(v), n, out)
-    words = torch.empty(n, dtype=torch.int32, device=DEV)
+    words = torch.empty(n, dtype=torch.int16, device=DEV)
     moe4.moe4_sr_words(0x0123456789ABCDEF, 5, 1 << 33, n, words)
     torch.cuda.synchronize()
     ref_words0 = oracle.sr_words(0, 0, 0, n)
     assert first_mismatch(to_np(out), oracle.e4m3_sr(v, ref_words0)) is None
-    assert first_mismatch(to_np(words, np.uint32), oracle.sr_words(0x0123456789ABCDEF, 5, 1 << 33, n)) is None
+    assert first_mismatch(to_np(words, np.uint16), oracle.sr_words(0x0123456789ABCDEF, 5, 1 << 33, n)) is None
 
 
 def test_full_tensor_parity_small_moe_operands():

@@ -259,14 +259,15 @@ def test_requant_full_size_gate_up_weights_sampled():
             assert first_mismatch(e8n[c0:c0 + 32], re8) is None
 
 
-def test_mxfp8_colwise_sr_beyond_2_34_values():
-    """More than 2^34 output values (131072 x 131200): the Philox counter's second word becomes
-    non-zero for the last output rows, so the transposing kernel runs its 64-bit counter
-    instance.  Input: bf16 values from a multiplicative hash of the element index (all finite);
-    checked on the first and the last 32 output rows against the oracle with the global index."""
-    rows, cols = 131072, 131200
+def test_mxfp8_colwise_sr_beyond_2_35_values():
+    """More than 2^35 output values (131072 x 262400): with eight values per Philox call the
+    counter's second word becomes non-zero for the last output rows, so the transposing kernel
+    runs its 64-bit counter instance.  Input: bf16 values from a multiplicative hash of the
+    element index (all finite); checked on the first and the last 32 output rows against the
+    oracle with the global index."""
+    rows, cols = 131072, 262400
     n = rows * cols
-    assert n > (1 << 34)
+    assert n > (1 << 35)
     x = torch.empty(n, dtype=torch.int16, device=DEV)
     step = 1 << 28
     for s0 in range(0, n, step):
@@ -284,6 +285,6 @@ def test_mxfp8_colwise_sr_beyond_2_34_values():
         xs = oracle.bf16_to_f32(to_np(xv[:, c0:c0 + 32].contiguous(), np.uint16))
         rq, re8 = oracle.mxfp8_quantize_rows(np.ascontiguousarray(xs.T), sr=True, seed=seed, stream_id=sid,
                                              idx_base=c0 * rows)
-        assert c0 == 0 or (c0 * rows) // 4 >= (1 << 32)  # the last slice: counter word 1 is 1
+        assert c0 == 0 or (c0 * rows) // 8 >= (1 << 32)  # the last slice: counter word 1 is 1
         assert first_mismatch(to_np(q[c0:c0 + 32]), rq) is None
         assert first_mismatch(to_np(e8[c0:c0 + 32]), re8) is None

@@ -8,7 +8,11 @@ implementation, Triton's `tl.philox`, executed by Triton's CPU interpreter in a 
 
 Stochastic rounding ("4-bit computation from the start of Inkling 2 Small's pretraining",
 lhc.media, backward-pass paragraphs: chooses the higher or lower representable value by distance
-so that the value is preserved on average):
+so that the value is preserved on average), with one 16-bit number per element:
+  - the numbers are the 16-bit halves of the Philox words, eight elements per call;
+  - over all 2^16 numbers, a value rounds up exactly floor(frac * 2^16) times, frac its distance
+    above the lower neighbour in units of the gap computed in exact rationals: the probability of
+    rounding up is frac less at most 2^-16;
   - the result is always one of the two neighbours;
   - exactly representable values never move;
   - at a quarter of the way up, the up-fraction over 2^22 words is 1/4 within 5 sigma, and the
@@ -95,14 +99,49 @@ def test_philox_against_triton_interpreter(orc):
 
 
 def test_sr_word_keying(orc):
+    """Element idx takes half idx % 2 of word (idx / 2) % 4 of the Philox call on counter idx / 8."""
     seed, sid = 0x0123456789ABCDEF, 7
-    idx = np.array([0, 1, 2, 3, 4, 5, (1 << 32) * 4 + 6, (1 << 40) + 3], np.uint64)
+    idx = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 13, (1 << 32) * 8 + 6, (1 << 35) + 3, (1 << 40) + 7], np.uint64)
     for i in idx:
         i = int(i)
-        j = i >> 2
+        j = i >> 3
         words = orc.philox4x32_10([j & 0xFFFFFFFF, j >> 32, sid, 0],
                                   [seed & 0xFFFFFFFF, seed >> 32])
-        assert orc.sr_words(seed, sid, i, 1)[0] == words[i & 3]
+        want = (int(words[(i >> 1) & 3]) >> (16 * (i & 1))) & 0xFFFF
+        assert int(orc.sr_words(seed, sid, i, 1)[0]) == want
+    # eight consecutive numbers are the four words of one call, as little-endian 16-bit halves
+    w = orc.philox4x32_10([5, 0, sid, 0], [seed & 0xFFFFFFFF, seed >> 32])
+    assert np.array_equal(orc.sr_words(seed, sid, 40, 8), np.asarray(w, np.uint32).view(np.uint16))
+
+
+def test_sr_up_count_over_all_numbers_is_floor_frac(orc):
+    """Brute force over every 16-bit number: the count of numbers that round v up equals
+    floor(frac * 2^16), with frac = (|v| - lo) / (hi - lo) in exact rationals (normal and subnormal
+    E4M3 range, both signs)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(17)
+    codes = np.arange(0x7F, dtype=np.uint8)
+    grid = [Fraction(float(g)) for g in orc.e4m3_value(codes)]
+    vals = []
+    for c in [0, 1, 5, 7, 8, 9, 40, 77, 118, 125]:
+        lo, hi = float(grid[c]), float(grid[c + 1])
+        for t in np.concatenate([rng.random(6), [2.0 ** -16, 1 - 2.0 ** -16, 0.5, 1.0 / 3]]):
+            v = np.float32(lo + t * (hi - lo))
+            if lo < float(v) < hi:
+                vals.append(v)
+    r = np.arange(1 << 16, dtype=np.uint16)
+    for v in vals:
+        for sv in (v, -v):
+            got = orc.e4m3_sr(np.full(r.size, sv, np.float32), r)
+            a = Fraction(float(abs(sv)))
+            c = max(i for i in range(127) if grid[i] <= a)
+            frac = (a - grid[c]) / (grid[c + 1] - grid[c])
+            ups = int(np.sum((got & 0x7F) == c + 1))
+            assert ups == int(frac * (1 << 16)), (float(sv), ups)
+            assert np.all(((got & 0x7F) == c) | ((got & 0x7F) == c + 1))
+            assert np.all((got >> 7) == (1 if sv < 0 else 0))
+            # the probability of rounding up is below frac by less than 2^-16
+            assert 0 <= frac - Fraction(ups, 1 << 16) < Fraction(1, 1 << 16)
 
 
 def _e4m3_neighbours(orc, v):
@@ -119,7 +158,7 @@ def test_sr_lands_on_a_neighbour(orc):
     rng = np.random.default_rng(3)
     v = (rng.standard_normal(200000) * np.exp2(rng.integers(-12, 9, 200000))).astype(np.float32)
     v = np.clip(v, -448, 448).astype(np.float32)
-    r = rng.integers(0, 1 << 32, size=v.size, dtype=np.uint64).astype(np.uint32)
+    r = rng.integers(0, 1 << 16, size=v.size, dtype=np.uint64).astype(np.uint16)
     got = orc.e4m3_sr(v, r)
     lo, hi, _ = _e4m3_neighbours(orc, v)
     mag = got & 0x7F
@@ -130,8 +169,8 @@ def test_sr_lands_on_a_neighbour(orc):
 def test_sr_exact_values_never_move(orc):
     vals = orc.e4m3_value(np.arange(0x7F, dtype=np.uint8))
     v = np.concatenate([vals, -vals]).astype(np.float32)
-    for r in [0, 1, 0x7FFFFFFF, 0xFFFFFFFF]:
-        got = orc.e4m3_sr(v, np.full(v.size, r, np.uint32))
+    for r in [0, 1, 0x7FFF, 0xFFFF]:
+        got = orc.e4m3_sr(v, np.full(v.size, r, np.uint16))
         assert np.array_equal(got, orc.e4m3_rne_sat(v))
 
 
@@ -176,7 +215,7 @@ def test_sr_unbiased_on_random_values(orc):
 
 def test_philox_words_uniform(orc):
     w = orc.sr_words(seed=99, stream_id=1, idx_base=0, n=1 << 20)
-    hist = np.bincount(w >> 24, minlength=256).astype(np.float64)
+    hist = np.bincount(w >> 8, minlength=256).astype(np.float64)
     expected = w.size / 256
     chi2 = ((hist - expected) ** 2 / expected).sum()
     # 255 degrees of freedom: mean 255, sd 22.6; 6 sd bound
