@@ -34,6 +34,13 @@ import sys
 import threading
 import time
 
+# The oracle legs (the reference arm and the CPU baseline) run on one host thread: their float64
+# matmuls are held to one BLAS thread, which has to be fixed before numpy loads its BLAS.
+if "--impl=reference" in sys.argv or "--cpu-leg" in sys.argv or (
+        "--impl" in sys.argv and sys.argv[sys.argv.index("--impl") + 1:][:1] == ["reference"]):
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,8 +54,8 @@ METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
-TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.6 / 2216.7}  # no-copy SGD mode, deeper ring
-GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 4, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
+TRAFFIC_RATIO = {}
+GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
 
 
 def load_peaks():
@@ -92,6 +99,7 @@ class LayerStep:
         # per-expert amax of the bf16 copies: written by the fused wgrad + SGD epilogue of each step
         # and read by the next step's weight quantisation (here seeded for the first step)
         self.amax_h = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.amax_y = torch.zeros(1, dtype=torch.float32, device=dev)
         self.amax_gu = self.Wb_gu.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
         self.amax_d = self.Wb_d.view(torch.bfloat16).view(E, -1).abs().amax(dim=1).float().contiguous()
         # routing
@@ -168,12 +176,14 @@ class LayerStep:
             m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
         n += 3
         with tm("quant_w"):
-            GIVEN = m.AMAX_GIVEN
-            # the FP32 master weights, rounded to bf16 as they are read (no stored bf16 copy)
-            m.nvfp4_quantize_f32(self.W32_gu, E, 2 * f, d, d, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.amax_gu,
-                                 FOS | MMA | GIVEN)
-            m.nvfp4_quantize_f32(self.W32_d, E, d, f, f, self.Wd_c, self.Wd_s, self.Wd_g, self.amax_d,
-                                 FOS | MMA | GIVEN)
+            # the FP32 master weights, rounded to bf16 as they are read (no stored bf16 copy), to
+            # NVFP4 for the forward and, in the same pass, requantised to the MXFP8 transposes the
+            # backward's dgrad reads; experts that received no rows are skipped
+            WF = FOS | m.SR | MMA | OMMA
+            m.nvfp4_quantize_f32_requant(self.W32_gu, E, 2 * f, d, self.amax_gu, self.Wgu_c, self.Wgu_s, self.Wgu_g,
+                                         self.WguT_q, self.WguT_e, seed, 3, self.offs, WF)
+            m.nvfp4_quantize_f32_requant(self.W32_d, E, d, f, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g,
+                                         self.WdT_q, self.WdT_e, seed, 1, self.offs, WF)
         n += 2
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
@@ -185,13 +195,14 @@ class LayerStep:
                              FOS | MMA | m.AMAX_GIVEN)
         n += 2
         with tm("gemm_nvfp4"):
-            m.grouped_expert_gemm_nvfp4(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s, self.Wd_g, self.offs,
-                                        E, Rp, d, f, self.Y, m.OUT_BF16 | MMA)
+            # the down projection; its last stage also returns the amax of the Hadamard-rotated rows
+            m.grouped_expert_gemm_nvfp4_hadamard_amax(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s,
+                                                      self.Wd_g, self.offs, E, Rp, d, f, self.Y, self.amax_y, MMA)
         n += 1
-        with tm("hadamard"):
-            m.hadamard_quant(self.Y[:Rp], Rp, d, self.Yc_c, self.Yc_s, self.Yc_g, FOS, self.hws)
+        with tm("hadamard"):  # the NVFP4 return-path codec, its per-tensor amax given by the GEMM
+            m.hadamard_quant(self.Y[:Rp], Rp, d, self.Yc_c, self.Yc_s, self.Yc_g, FOS | m.AMAX_GIVEN, self.amax_y)
             m.hadamard_dequant(self.Yc_c, self.Yc_s, self.Yc_g, Rp, d, self.Yhat[:Rp])
-        n += 3
+        n += 2
         with tm("combine"):
             m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, y)
         n += 1
@@ -201,11 +212,9 @@ class LayerStep:
                                           self.dYc_q, self.dYc_e, OMMA)
         n += 1
         with tm("requant"):
-            m.mxfp8_requant_transpose_sr(self.Wd_c, self.Wd_s, self.Wd_g, E, d, f, self.WdT_q, self.WdT_e, seed, 1,
-                                         m.SR | MMA | OMMA)
             m.mxfp8_requant_transpose_sr(self.Hq_c, self.Hq_s, self.Hq_g, 1, Rp, f, self.HqT_q, self.HqT_e, seed, 2,
                                          m.SR | MMA | OMMA)
-        n += 2
+        n += 1
         with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dYr_q, self.dYr_e, self.WdT_q, self.WdT_e, self.offs, E, Rp, f, d, self.dH,
                                  m.OUT_F32 | m.GROUP_M | MMA, self.gws)
@@ -221,11 +230,9 @@ class LayerStep:
             m.mxfp8_quantize_rowcol(self.dGU[:Rp], Rp, 2 * f, self.dGUr_q, self.dGUr_e, self.dGUc_q, self.dGUc_e, OMMA)
         n += 1
         with tm("requant"):
-            m.mxfp8_requant_transpose_sr(self.Wgu_c, self.Wgu_s, self.Wgu_g, E, 2 * f, d, self.WguT_q, self.WguT_e,
-                                         seed, 3, m.SR | MMA | OMMA)
             m.mxfp8_requant_transpose_sr(self.Xp_c, self.Xp_s, self.Xq_g, 1, Rp, d, self.XpT_q, self.XpT_e, seed, 4,
                                          m.SR | MMA | OMMA)
-        n += 2
+        n += 1
         with tm("gemm_mxfp8_dgrad"):
             m.grouped_gemm_mxfp8(self.dGUr_q, self.dGUr_e, self.WguT_q, self.WguT_e, self.offs, E, Rp, d, 2 * f,
                                  self.dXp, m.OUT_BF16 | m.GROUP_M | MMA, self.gws)
@@ -247,11 +254,13 @@ class LayerStep:
         mx = 1.03125      # MXFP8 bytes per value (E4M3 + E8M0 per 32)
         w_gu, w_d = E * 2 * f * d, E * d * f
         b = {}
-        b["quant_w"] = (w_gu + w_d) * (4 + nv)                           # FP32 read; amax from the SGD epilogue
+        # the weights of experts with rows: FP32 read, NVFP4 and the MXFP8 transpose written (amax from
+        # the SGD epilogue)
+        b["quant_w"] = (w_gu + w_d) * live / E * (4 + nv + mx)
         b["quant_x"] = T * d * (2 + 2 + nv) + rows * d * nv * 2          # + gather read/write
         b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
                            rows * f * nv + live * d * f * nv + rows * d * 2)
-        b["requant"] = (w_gu + w_d + rows * (f + d)) * (nv + mx)
+        b["requant"] = rows * (f + d) * (nv + mx)                        # H and the gathered X
         # combine gradient formed from dy (read once) straight into both MXFP8 layouts of dY, and one
         # read of dGU for its two layouts
         b["mxfp8_quant"] = rows * d * 2 * mx + T * d * 2 + rows * 2 * f * (2 + 2 * mx)
@@ -259,10 +268,10 @@ class LayerStep:
                                  rows * 2 * f * mx + live * d * 2 * f * mx + rows * d * 2)   # gate/up
         # wgrad operands + the SGD epilogue: read W32, write W32 (the bf16 copy is not stored)
         b["gemm_mxfp8_wgrad_sgd"] = (rows * d * mx + rows * f * mx + rows * 2 * f * mx + rows * d * mx +
-                                     (w_gu + w_d) * (4 + 4))
+                                     (w_gu + w_d) * live / E * (4 + 4))   # experts without rows are skipped
         b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 + rows * f * (2 + nv)  # amax fused into SwiGLU
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
-        b["hadamard"] = rows * d * (2 + 2 + nv + nv + 2)
+        b["hadamard"] = rows * d * (2 + nv + nv + 2)   # amax from the down GEMM's last stage
         b["combine"] = rows * d * 2 + T * d * 2
         b["route"] = T * E * 4 + rows * 4 * 4
         return b
@@ -401,6 +410,48 @@ def compute_probe(kind, reps=5, dev="cuda:0"):
     return ms, 2.0 * R * N * K / (ms / 1e3) / 1e12
 
 
+def measure_tensor_peaks(dev="cuda:0", iters=20000, sustain_s=3.0):
+    """The tensor pipe's dense NVFP4 and MXFP8 rates on this GPU, in TFLOP/s, from the library's
+    throughput probe (one CTA per SM, operands resident in shared memory, the GEMMs' own MMA
+    instructions).  burst: five launches after two untimed ones; sustained: launches back to back
+    for `sustain_s` seconds, the rate over the last third (under the power cap, as a kernel inside a
+    long step runs)."""
+    import torch
+    from precision_moe_numerics_03_b300 import moe4 as m
+    n = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(n, dtype=torch.int32, device=dev)
+    out = {"ctas": n, "iters": iters}
+    for kind, name, flop in ((0, "nvfp4", 2.0 ** 24), (1, "mxfp8", 2.0 ** 23)):
+        launch = lambda: m.moe4_tensor_peak_probe(kind, iters, n, sink)
+        work = n * iters * flop
+        for _ in range(2):
+            launch()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(5):
+            launch()
+        e0.record()
+        torch.cuda.synchronize()
+        burst = 5 * work / (s0.elapsed_time(e0) / 1e3) / 1e12
+        chunks = []
+        t_end = time.perf_counter() + sustain_s
+        while time.perf_counter() < t_end:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(10):
+                launch()
+            b.record()
+            b.synchronize()
+            chunks.append(a.elapsed_time(b))
+        tail = chunks[len(chunks) * 2 // 3:]
+        sustained = 10 * len(tail) * work / (sum(tail) / 1e3) / 1e12
+        out[name] = {"burst_TFLOPs": round(burst, 1), "sustained_TFLOPs": round(sustained, 1)}
+    if m.moe4_get_status() != m.OK:
+        raise RuntimeError("a device wait timed out in the tensor peak probe")
+    return out
+
+
 class _NullTimer:
     def __call__(self, name):
         return self
@@ -499,8 +550,38 @@ class ClockSampler:
 # the oracle on a bounded sample (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------------------------
 def oracle_sample_step(d=D_MODEL, f=D_FF, rows=128, seed=0):
-    """One expert, one 128-row tile of routed tokens, every step of the method on the oracle.
-    Returns (expert-GEMM FLOPs, seconds)."""
+    """One expert, one 128-row tile of routed tokens, every step of the method on the oracle.  Run
+    it in a process started with one BLAS thread (the reference arm, or `--cpu-leg`): the oracle's C
+    is single-threaded too.  Returns (expert-GEMM FLOPs, seconds)."""
+    return _oracle_sample_step(d, f, rows, seed)
+
+
+def cpu_leg_in_child():
+    """The CPU baseline in a fresh process with one BLAS thread: the step sample and the requant
+    sample of the oracle.  Returns their JSON record."""
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg"], capture_output=True, text=True,
+                         timeout=600)
+    if out.returncode != 0:
+        raise RuntimeError("CPU baseline leg failed: " + out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def oracle_requant_sample(rows=1024, d=D_MODEL, seed=0):
+    """The oracle's dequantise -> transpose -> MXFP8 stochastic-rounding requantisation of a slice
+    of the backward-requant workload's activations (Student-t(3), d_model 4096), on one thread.
+    Returns (algorithmic bytes at 0.5625 B read + 1.03125 B written per value, seconds)."""
+    import oracle
+    from precision_moe_numerics_03_b300 import inputs
+    rng = inputs.host_rng(4, 200 + seed)
+    x = oracle.bf16_to_f32(inputs.to_bf16_bits(inputs.host_student_t(rng, (rows, d))))
+    q = oracle.nvfp4_quantize(x)
+    t0 = time.perf_counter()
+    oracle.mxfp8_requant_transpose(*q, sr=True, seed=seed, stream_id=4)
+    secs = time.perf_counter() - t0
+    return rows * d * (0.5625 + 1.03125), secs
+
+
+def _oracle_sample_step(d, f, rows, seed):
     import oracle
     from precision_moe_numerics_03_b300 import inputs
     rng = inputs.host_rng(5, 100 + seed)
@@ -544,8 +625,8 @@ def oracle_sample_step(d=D_MODEL, f=D_FF, rows=128, seed=0):
 
 
 def cpu_cores_used():
-    import torch
-    return max(1, torch.get_num_threads())
+    """The oracle legs run on one host thread (single-threaded C, one BLAS thread)."""
+    return 1
 
 
 # ---------------------------------------------------------------------------------------------
@@ -604,10 +685,13 @@ def profile_case(name):
         quant = lambda: moe4.nvfp4_quantize(w, E, 2 * f, d, d, c, s_, gd, None,
                                             moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT, ws)
         quant()
-        if name == "quant_w":  # as in the layer step: the FP32 master weights
+        if name == "quant_w":  # as in the layer step: the FP32 master weights, with their MXFP8 transposes
             w32 = inputs.device_normal((E * 2 * f, d), 0.02, g(8), dev, dtype=torch.float32)
-            calls.append(lambda: moe4.nvfp4_quantize_f32(w32, E, 2 * f, d, d, c, s_, gd, None,
-                                                         moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT, ws))
+            am = w32.to(torch.bfloat16).abs().view(E, -1).amax(dim=1).float().contiguous()
+            q, e8 = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
+            fl = moe4.FOUR_OVER_SIX | moe4.SR | moe4.SF_MMA_LAYOUT | moe4.SF_OUT_MMA
+            calls.append(lambda: moe4.nvfp4_quantize_f32_requant(w32, E, 2 * f, d, am, c, s_, gd, q, e8, 1, 3, None,
+                                                                 fl))
         elif name == "requant":
             q, e8 = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
             calls.append(lambda: moe4.mxfp8_requant_transpose_sr(c, s_, gd, E, 2 * f, d, q, e8, 1, 3,
@@ -698,6 +782,7 @@ def main():
     ap.add_argument("--small", action="store_true", help="the small 8-expert shapes (a quick check, not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
@@ -705,6 +790,11 @@ def main():
                              "gemm_mxfp8_probe"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
+    if args.cpu_leg:  # the CPU baseline's oracle samples, in their own one-thread process
+        fl, secs = oracle_sample_step(seed=0)
+        rb, rsecs = oracle_requant_sample()
+        print(json.dumps({"flops": fl, "seconds": secs, "requant_bytes": rb, "requant_seconds": rsecs}))
+        return 0
     if args.profile_case:
         return profile_case(args.profile_case)
 
@@ -780,8 +870,11 @@ def main():
     comps["gemm_nvfp4"]["TFLOP/s"] = round(fwd_flops / (per["gemm_nvfp4"] / 1e3) / 1e12, 1)
     comps["gemm_mxfp8_dgrad"]["TFLOP/s"] = round(fwd_flops / (per["gemm_mxfp8_dgrad"] / 1e3) / 1e12, 1)
     comps["gemm_mxfp8_wgrad_sgd"]["TFLOP/s"] = round(fwd_flops / (per["gemm_mxfp8_wgrad_sgd"] / 1e3) / 1e12, 1)
-    fp4_peak = peaks["bf16_sus"] * 6.0     # nominal FP4 / BF16 ratio (13.5 / 2.25)
-    fp8_peak = peaks["bf16_sus"] * 2.0
+    # dense FP4 / FP8 peaks of this GPU, measured by the tensor-pipe probe (sustained: the GEMMs
+    # are timed inside a long step), after the timed region
+    tpk = measure_tensor_peaks(dev)
+    fp4_peak = tpk["nvfp4"]["sustained_TFLOPs"]
+    fp8_peak = tpk["mxfp8"]["sustained_TFLOPs"]
     dom = max(per, key=per.get)
     t_dom = per[dom]
     flops_dom = {"gemm_nvfp4": (fwd_flops, fp4_peak), "gemm_mxfp8_dgrad": (fwd_flops, fp8_peak),
@@ -803,13 +896,16 @@ def main():
     req_gbs = gbytes["requant"] / (per["requant"] / 1e3) / 1e9
     metric_detail = {
         "nvfp4_gemm": {"TFLOP/s": comps["gemm_nvfp4"]["TFLOP/s"],
-                       "frac_fp4_peak_derived": round(comps["gemm_nvfp4"]["TFLOP/s"] / fp4_peak, 4),
+                       "frac_fp4_peak_measured": round(comps["gemm_nvfp4"]["TFLOP/s"] / fp4_peak, 4),
                        "frac_fp4_peak_15PF": round(comps["gemm_nvfp4"]["TFLOP/s"] / 15000.0, 4),
                        "frac_time_bound_measured": round(bound_meas / t_g, 4),
                        "frac_time_bound_nominal": round(bound_nom / t_g, 4)},
         "requant": {"GB/s": round(req_gbs, 1), "frac_hbm_measured": round(req_gbs / peaks["hbm"], 4),
                     "frac_hbm_nominal_8TBs": round(req_gbs / 8000.0, 4),
                     "note": "issue-bound (Philox4x32-10): ncu issue-slot figures in profiles/"},
+        "tensor_peaks": tpk,
+        "peaks_note": "FP4/FP8 denominators: the sustained rate of moe4_tensor_peak_probe on this GPU; HBM: "
+                      "MEASURED_PEAKS.json copy bandwidth",
     }
     nl = GROUP_LAUNCHES.get(dom, 1)
     roof["launches_per_step"] = nl
@@ -882,21 +978,26 @@ def main():
         mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["swiglu_quant_h"], 4)
         nxt["hadamard_mxfp8_codec"]["nvfp4_codec_ms"] = round(per["hadamard"], 4)
         probe = {"shape": "8 groups x 8192 rows, N = K = 8192, bf16 out (compute-bound; not the layer's shape)"}
-        # timed alone: the burst bf16 figure x the nominal ratios (FP4 6x, FP8 2x)
-        pk = {"nvfp4": peaks["bf16"] * 6.0, "mxfp8": peaks["bf16"] * 2.0}
+        # timed alone: the burst rates of the tensor-pipe probe
+        pk = {"nvfp4": tpk["nvfp4"]["burst_TFLOPs"], "mxfp8": tpk["mxfp8"]["burst_TFLOPs"]}
         for kind, name in ((0, "nvfp4"), (1, "mxfp8")):
             pm, pt = compute_probe(kind)
-            probe[name] = {"ms": round(pm, 4), "TFLOP/s": round(pt, 1), "frac_of_derived_peak": round(pt / pk[name], 3)}
-        probe["derived_peaks_TFLOPs"] = {k: round(v, 1) for k, v in pk.items()}
-        probe["peak_source"] = peaks["src"] + " bf16 burst x nominal ratio"
+            probe[name] = {"ms": round(pm, 4), "TFLOP/s": round(pt, 1), "frac_of_measured_peak": round(pt / pk[name], 3)}
+        probe["peaks_TFLOPs"] = {k: round(v, 1) for k, v in pk.items()}
+        probe["peak_source"] = "moe4_tensor_peak_probe burst rate on this GPU"
         nxt["gemm_compute_probe"] = probe
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        fl, secs = oracle_sample_step(seed=0)
+        leg = cpu_leg_in_child()
+        fl, secs, rb, rsecs = leg["flops"], leg["seconds"], leg["requant_bytes"], leg["requant_seconds"]
         cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
                "sample": "one expert (gate/up 4096x4096, down 4096x2048 weights) and one 128-row tile of routed "
-                         "tokens through every step", "seconds": round(secs, 2)}
+                         "tokens through every step", "seconds": round(secs, 2),
+               "requant_GBps": round(rb / rsecs / 1e9, 4),
+               "requant_sample": "1024 x 4096 Student-t(3) activations: NVFP4 -> dequantise -> transpose -> MXFP8 "
+                                 "stochastic rounding, %.2f s" % rsecs,
+               "host_cores_available": os.cpu_count()}
 
     if rank == 0:
         line = {

@@ -110,6 +110,17 @@ int moe4_get_status(void *stream);
  * fault; the pages have no counterpart. */
 int moe4_selftest_wait(int64_t limit_cycles, void *stream);
 
+/* moe4_tensor_peak_probe: the throughput ceiling of the tensor pipe for the GEMMs' instruction
+ * mix.  Each of `ctas` CTAs (one per SM) keeps one operand stage in shared memory and issues
+ * `iters` rounds of the grouped GEMMs' four block-scaled MMAs into one tensor-memory accumulator:
+ * kind 0 = NVFP4 (mxf4nvf4, 128 x 256 x 256 per round, 2^24 FLOP), kind 1 = MXFP8 (mxf8f6f4,
+ * 128 x 256 x 128 per round, 2^23 FLOP); kinds 2 and 3 are the same with each round's scale
+ * factors copied into tensor memory again first (tcgen05.cp), as the GEMMs do per operand stage.
+ * No operand traffic, so FLOPs / time is the pipe's own rate; time it with events on `stream`.  1 <= iters <= 2^20, 1 <= ctas <= 4096; sink [ctas]
+ * uint32 (never written in practice; it keeps the result live).  A measurement aid; the pages
+ * quote only datasheet peaks. */
+int moe4_tensor_peak_probe(int kind, int64_t iters, int64_t ctas, uint32_t *sink, void *stream);
+
 /* ------------------------------------------------------------------ NVFP4 [LHC fewer bits; DEBUT]
  * nvfp4_quantize: x bf16 [nmat, rows, ld] (the first `cols` of each row are used; ld >= cols,
  * ld % 8 == 0).  For each matrix m: amax_m = max|x| (or amax_in[m] with MOE4_AMAX_GIVEN);
@@ -185,6 +196,23 @@ int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const fl
                                uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,
                                void *stream);
 
+/* nvfp4_quantize_f32_requant: the weight path of one training step in one pass over the binary32
+ * master weights x [nmat, rows, cols] (contiguous rows): nvfp4_quantize_f32 with MOE4_AMAX_GIVEN
+ * (amax_in [nmat]; Four Over Six with MOE4_FOUR_OVER_SIX) writes codes [nmat, rows, cols/2], sf
+ * (canonical, or the tile layout with MOE4_SF_MMA_LAYOUT) and g_dec [nmat] for the forward GEMM,
+ * and mxfp8_requant_transpose_sr of that result (seed, stream_id, MOE4_SR, MOE4_SF_OUT_MMA as
+ * there) writes q_t [nmat, cols, rows] and e8_t for the backward GEMM [LHC backward pass:
+ * dequantise, transpose at higher precision, requantise to MXFP8 with stochastic rounding].  Every
+ * output byte equals that of the two calls in sequence.  group_offs: device int32 [nmat + 1] or
+ * NULL; a matrix m with group_offs[m + 1] == group_offs[m] (an expert that received no rows) is
+ * skipped and its outputs are left as they are.  rows % 32 == 0 (% 128 with either tile-layout
+ * flag), cols % 64 == 0 (% 128 with MOE4_SF_OUT_MMA); x, codes and q_t 16-byte aligned; nmat, and
+ * cols / 64, at most 65535. */
+int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t rows, int64_t cols,
+                               const float *amax_in, uint8_t *codes, uint8_t *sf, float *g_dec,
+                               uint8_t *q_t, uint8_t *e8_t, uint64_t seed, uint32_t stream_id,
+                               const int32_t *group_offs, uint32_t flags, void *stream);
+
 /* mxfp8_quantize: bf16 x [rows, cols] to MXFP8 with the same scale and rounding rules.
  * MOE4_ROWWISE: q [rows, cols], e8 [rows, cols/32] (cols % 32 == 0); random index = the
  * element's index in q.  MOE4_COLWISE: q [cols, rows], e8 [cols, rows/32] (rows % 32 == 0,
@@ -208,7 +236,9 @@ int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t cols, uint8_t
  * hadamard_quant: x bf16 [rows, cols], cols % 128 == 0.  Each contiguous 128-chunk of a row is
  * rotated by the Sylvester-ordered Hadamard matrix (butterflies of span 1, 2, ..., 64, then
  * times RN(1/sqrt(128))) in binary32, and the rotated tensor is NVFP4-quantised as above (its
- * own amax; Four Over Six per flags).  ws: moe4_workspace_size(MOE4_OP_HADAMARD_QUANT).
+ * own amax; Four Over Six per flags).  ws: moe4_workspace_size(MOE4_OP_HADAMARD_QUANT), 4-byte
+ * aligned; with MOE4_AMAX_GIVEN, ws instead holds that amax already (binary32, as
+ * grouped_expert_gemm_nvfp4_hadamard_amax returns it) and the amax pass over x is skipped.
  * hadamard_dequant: NVFP4 dequantise, the same rotation (it is its own inverse), bf16 out.
  * With MOE4_MXFP8 (the only flag then), the 8.25-bit variant [LHC communication: the return path
  * falls from sixteen to 8.25 bits per value]: after the rotation each 32-block is quantised to
@@ -235,6 +265,21 @@ int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const
                               const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t N,
                               int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
                               void *stream);
+
+/* grouped_expert_gemm_nvfp4_hadamard_amax: grouped_expert_gemm_nvfp4 with bf16 output d, which
+ * also returns in amax_out[0] the largest magnitude of the Hadamard(128)-rotated d (each 128-column
+ * chunk of a row rotated as hadamard_quant does it), computed in the GEMM's last stage from the
+ * bf16 values it stores [LHC kernels paragraph: the transform and quantisation fused into the
+ * final stage of the matrix multiplication].  It is exactly the amax hadamard_quant would compute
+ * for d, so the return-path encoder can take it with MOE4_AMAX_GIVEN and read d once: the NVFP4
+ * codec needs its per-tensor scale before the first block is quantised, so the quantisation
+ * itself is a second pass.  d as for MOE4_OUT_BF16; amax_out 4-byte aligned, cleared first; flags
+ * MOE4_SF_MMA_LAYOUT or 0; other rules as grouped_expert_gemm_nvfp4. */
+int grouped_expert_gemm_nvfp4_hadamard_amax(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                                            const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                                            const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t N,
+                                            int64_t K, uint16_t *d, float *amax_out, uint32_t flags, void *ws,
+                                            size_t ws_bytes, void *stream);
 
 /* grouped_expert_gemm_nvfp4_hadamard_mx: the expert GEMM above with the return-path codec fused
  * into its last stage [LHC kernels paragraph: the transform and the quantisation run in the final
@@ -275,9 +320,13 @@ int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
  * take MOE4_AMAX_GIVEN).  Bit-identical to grouped_gemm_mxfp8(MOE4_GROUP_K | MOE4_OUT_F32)
  * followed by moe4_sgd_update.  A [M, K], B [N, K], w32 / w_bf16 [E, M, N]; M % 128 == 0,
  * N % 256 == 0, K % 128 == 0; offs as for grouped_gemm_mxfp8 (offs[E] = K).  Experts with no rows
- * keep their weights (and still report their amax).  w_bf16 may be NULL: the bf16 copy is then
- * not written, amax_out is unchanged (for nvfp4_quantize_f32 of w32).  flags: MOE4_SF_MMA_LAYOUT or 0 (canonical
- * scales are converted into ws, moe4_workspace_size_gemm(1, M, 1, N, K) bytes). */
+ * are skipped: under plain SGD their weights do not change, so their w32, w_bf16 and amax_out
+ * entries are left as they are (amax_out[e] keeps the value an earlier call wrote).  w_bf16 may be
+ * NULL: the bf16 copy is then not written and amax_out still gets max |bf16(w32[e])| (for
+ * nvfp4_quantize_f32 of w32 with MOE4_AMAX_GIVEN).  flags: MOE4_SF_MMA_LAYOUT or 0 (canonical
+ * scales are converted into ws, moe4_workspace_size_gemm(1, M, 1, N, K) bytes); with room in ws
+ * after the staged scales for E + 1 int32 (E < 4096), the tiles run in a size-interleaved order
+ * of the experts that have rows. */
 int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
                                  const uint8_t *b_e8, const int32_t *group_offs, int64_t E,
                                  int64_t M, int64_t N, int64_t K, float *w32, uint16_t *w_bf16,

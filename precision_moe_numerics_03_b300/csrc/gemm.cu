@@ -157,6 +157,7 @@ struct Args {
     float lr;               // Out::Sgd
     unsigned int *amax;     // Out::Sgd: per-expert max |bf16 copy| as binary32 bits
     uint8_t *e8;            // fused codec: E8M0 scales [M, N/32] (d holds the E4M3 codes [M, N])
+    unsigned int *had_amax; // bf16 output: max |Hadamard(128)-rotated rows| (binary32 bits), or null
     const int32_t *order;   // contraction-grouped: experts by decreasing group size, or null
     int64_t num_tiles;
     int n_tiles_n, n_tiles_m;
@@ -332,7 +333,7 @@ struct Tile {
 };
 
 template <int KIND, int BNT>
-__device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
+__device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t, int64_t ntiles) {
     Tile tl;
     // tile indices and counts are below 2^31: 32-bit division (the 64-bit one is a long sequence)
     const uint32_t t32 = (uint32_t)t, ntn = (uint32_t)p.n_tiles_n;
@@ -354,13 +355,14 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
         // slot t = c + G*i (CTA c of G, its i-th tile) takes the list's next entry from the front
         // when c + i is even and from the back otherwise: at any time half the CTAs work on long
         // contractions (operand-bound) and half on short ones (master-weight-bound), and each CTA
-        // alternates.  For even G this maps slots onto list positions one to one.
+        // alternates.  For even G this maps slots onto the ntiles list positions one to one (the
+        // fused SGD lists only the experts that have rows).
         const uint32_t per_e = (uint32_t)p.n_tiles_m * ntn;
         uint32_t l = t32;
         if (p.order != nullptr && (gridDim.x & 1u) == 0) {
             const uint32_t G = gridDim.x, i = t32 / G, c = t32 - i * G;
             const uint32_t fi = i * (G / 2) + c / 2;
-            l = ((c + i) & 1) == 0 ? fi : (uint32_t)p.num_tiles - 1 - fi;
+            l = ((c + i) & 1) == 0 ? fi : (uint32_t)ntiles - 1 - fi;
         }
         const uint32_t r = l / per_e, rem = l - r * per_e;
         const int e = p.order != nullptr ? __ldg(p.order + r) : (int)r;
@@ -374,6 +376,27 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t) {
         tl.n_stages = (k1 - k0) / Cfg<KIND>::ELEMS;
     }
     return tl;
+}
+
+// The largest magnitude of RN(H_128 u / sqrt(128)) over one 128-value row chunk held by one
+// thread: butterflies of span 1, 2, ..., 64, (u[i], u[i+h]) <- (u[i] + u[i+h], u[i] - u[i+h]) for i
+// with bit h clear, each one binary32 rounding (the order of the return-path codec's transform);
+// then, as RN(x * c) is monotone in |x| for c > 0, the largest |u| times c = RN(1/sqrt(128)) is the
+// largest rotated magnitude.  u is overwritten.
+__device__ __forceinline__ float fwht128_amax(float (&u)[128]) {
+#pragma unroll
+    for (int h = 1; h < 128; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+            if ((i & h) == 0) {
+                const float a = u[i], b = u[i + h];
+                u[i] = __fadd_rn(a, b);
+                u[i + h] = __fsub_rn(a, b);
+            }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) m = fmaxf(m, fabsf(u[i]));
+    return __fmul_rn(m, __uint_as_float(0x3DB504F3u));
 }
 
 template <int KIND, int EM>
@@ -397,6 +420,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
     const int warp = warp_id(), lane = lane_id();
+    // Tiles to run.  The fused SGD skips experts without rows (their weights do not change): with
+    // an expert order the list holds only the experts that have rows, order[E] of them.
+    const int64_t ntiles = (kSgd && p.order != nullptr)
+                               ? (int64_t)__ldg(p.order + p.E) * p.n_tiles_m * p.n_tiles_n
+                               : p.num_tiles;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(full + s, 1);
@@ -429,8 +457,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t issued_parity[NST];
         bool issued[NST];
         for (int s = 0; s < NST; ++s) issued[s] = false, issued_parity[s] = 0;
-        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND, BNT>(p, t);
+        for (int64_t t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND, BNT>(p, t, ntiles);
             for (int ks = 0; ks < tl.n_stages; ++ks) {
                 if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag)) break;
                 uint64_t *fb = full + stage;
@@ -468,8 +496,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;  // accumulator buffer of this tile
         const uint32_t a_base = smem_u32(smem + L::OFF_A), b_base = smem_u32(smem + L::OFF_B);
         const uint32_t sfa_base = smem_u32(smem + L::OFF_SFA), sfb_base = smem_u32(smem + L::OFF_SFB);
-        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND, BNT>(p, t);
+        for (int64_t t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND, BNT>(p, t, ntiles);
+            if (kSgd && tl.n_stages == 0) continue;  // an expert without rows: skipped by every role
             if (!mbar_wait(tmem_empty + acc, acc_ph[acc] ^ 1u, abort_flag)) break;
             tc_fence_after();
             const uint32_t tmem_d = tmem + (uint32_t)(acc * BNT);
@@ -529,14 +558,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_ph[2] = {0u, 0u};
         int acc = 0;
         uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
-        for (int64_t t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile tl = decode_tile<KIND, BNT>(p, t);
-            // fused SGD: the CTA's next tile (its first master-weight chunks are loaded ahead),
-            // decoded while the accumulator is still being produced
-            const int64_t tn = t + gridDim.x;
-            const bool has_next = tn < p.num_tiles;
+        for (int64_t t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+            const Tile tl = decode_tile<KIND, BNT>(p, t, ntiles);
+            if (kSgd && tl.n_stages == 0) continue;  // an expert without rows: skipped by every role
+            // fused SGD: the CTA's next tile that has rows (its first master-weight chunks are
+            // loaded ahead), decoded while the accumulator is still being produced
+            int64_t tn = t + gridDim.x;
             Tile tn_l{};
-            if (kSgd && has_next) tn_l = decode_tile<KIND, BNT>(p, tn);
+            if constexpr (kSgd) {
+                for (; tn < ntiles; tn += gridDim.x) {
+                    tn_l = decode_tile<KIND, BNT>(p, tn, ntiles);
+                    if (tn_l.n_stages > 0) break;
+                }
+            }
+            const bool has_next = tn < ntiles;
             if (!mbar_wait(tmem_full + acc, acc_ph[acc], abort_flag)) break;
             tc_fence_after();
             const bool live = tl.n_stages > 0;
@@ -772,6 +807,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                         bulk_commit();
                     }
                 }
+                if constexpr (KIND == 0 && NCOL == 128) {
+                    // the return path's amax: this lane's row chunk (columns x0 .. x0+127, one whole
+                    // Hadamard chunk) as the bf16 values just stored, rotated in registers
+                    if (p.had_amax != nullptr) {
+                        float u[128];
+#pragma unroll
+                        for (int i = 0; i < 128; ++i)
+                            u[i] = __uint_as_float((uint32_t)f32_to_bf16_bits(
+                                                       __fmul_rn(__uint_as_float(accr[i]), alpha)) << 16);
+                        uint32_t m = __float_as_uint(fwht128_amax(u));
+                        m = __reduce_max_sync(0xFFFFFFFFu, m);
+                        if (lane == 0 && m) atomicMax(p.had_amax, m);
+                    }
+                }
             } else {
                 for (int c = 0; c < BNT / 64; ++c) {
                     uint32_t r[32];
@@ -923,6 +972,94 @@ __global__ void wait_selftest_kernel(long long limit) {
     if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, limit);
 }
 
+// Throughput of the tensor pipe on one CTA per SM: one stage of operands stays in shared memory
+// (128 x 128-byte A, 256 x 128-byte B with their scale factors), the scale factors are copied into
+// tensor memory once, and the issuing thread runs `iters` rounds of the GEMM's four block-scaled
+// MMAs (128 x 256 x 256 FP4 or 128 x 256 x 128 FP8 per round) into one binary32 accumulator,
+// then commits once and waits (bounded).  No operand traffic: the rate is the pipe's own.  With
+// kCopySf every round first copies its scale factors into tensor memory again, into one of four
+// column sets in turn, as the GEMM does for each operand stage.
+template <int KIND, bool kCopySf>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int64_t iters, uint32_t *sink) {
+    constexpr int SFA = Cfg<KIND>::ATOMS * 512, SFB = 2 * SFA;
+    constexpr int OFF_B = A_TILE, OFF_SFA = OFF_B + BN * BKB, OFF_SFB = OFF_SFA + SFA, OFF_BAR = OFF_SFB + SFB;
+    constexpr int SF_COLS_A = Cfg<KIND>::ATOMS * 4;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *done = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 8);
+    int *abort_flag = reinterpret_cast<int *>(smem + OFF_BAR + 12);
+    // operands: a hash pattern of valid FP4 / E4M3 codes (no NaN), scales 1.0
+    for (int i = threadIdx.x; i < OFF_SFA / 4; i += blockDim.x) {
+        uint32_t h = (uint32_t)i * 2654435761u;
+        h ^= h >> 15;
+        reinterpret_cast<uint32_t *>(smem)[i] = KIND == 0 ? h : (h & 0x77777777u);
+    }
+    const uint8_t one = KIND == 0 ? 0x38 : 127;  // E4M3 1.0, E8M0 2^0
+    for (int i = threadIdx.x; i < SFA + SFB; i += blockDim.x) smem[OFF_SFA + i] = one;
+    if (threadIdx.x == 0) {
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    fence_async_smem();
+    if (warp_id() == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    if (threadIdx.x == 0) {
+        constexpr uint32_t SF_SET = 3 * SF_COLS_A;  // A and two row tiles of B
+        const uint32_t sfa_base = smem_u32(smem + OFF_SFA), sfb_base = smem_u32(smem + OFF_SFB);
+        auto copy_sf = [&](uint32_t sf_col) {
+#pragma unroll
+            for (int i = 0; i < Cfg<KIND>::ATOMS; ++i) {
+                tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_base + i * 512, 0, 128, 0));
+#pragma unroll
+                for (int rt = 0; rt < 2; ++rt)
+                    tc_cp_sf(sf_col + SF_COLS_A + 8 * i + 4 * rt, smem_desc(sfb_base + rt * SFA + i * 512, 0, 128, 0));
+            }
+        };
+        copy_sf(tmem + BN);
+        const uint32_t a_addr = smem_u32(smem), b_addr = smem_u32(smem + OFF_B);
+#pragma unroll 1
+        for (int64_t it = 0; it < iters; ++it) {
+            uint32_t sf_col = tmem + BN;
+            if constexpr (kCopySf) {
+                sf_col += (uint32_t)(it & 3) * SF_SET;
+                copy_sf(sf_col);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024, 2);
+                const uint64_t bd = smem_desc(b_addr + 32 * k, 16, 1024, 2);
+                if constexpr (KIND == 0)
+                    tc_mma<0>(tmem, ad, bd, make_idesc<0, BN>(0), sf_col + 4 * k, sf_col + SF_COLS_A + 8 * k,
+                              (it > 0 || k > 0) ? 1u : 0u);
+                else
+                    tc_mma<1>(tmem, ad, bd, make_idesc<1, BN>((uint32_t)k), sf_col, sf_col + SF_COLS_A,
+                              (it > 0 || k > 0) ? 1u : 0u);
+            }
+        }
+        tc_commit(done);
+        mbar_wait(done, 0u, abort_flag);
+    }
+    __syncthreads();
+    tc_fence_after();
+    uint32_t r[32];
+    tc_ld32(tmem + ((uint32_t)(warp_id() * 32) << 16), r);  // keeps the accumulator live
+    if (lane_id() == 0 && r[0] == 0x7FC00001u) sink[blockIdx.x] = r[1];
+    tc_fence_before();
+    __syncthreads();
+    if (warp_id() == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
 }  // namespace gemm
 }  // namespace moe4
 
@@ -937,18 +1074,33 @@ extern "C" int moe4_get_status(void *stream) {
     return v ? MOE4_ERR_TIMEOUT : MOE4_OK;
 }
 
-// order[rank] = expert, ranks by decreasing group size (ties: lower expert first).  One CTA.
-__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t *__restrict__ offs, int E,
-                                                            int32_t *__restrict__ order) {
+// Before the fused SGD: amax_out[e] = 0 for every expert that has rows (the others are skipped
+// and keep theirs), and, when `order` is given (E < 4096), the experts that have rows by
+// decreasing group size (ties by index) in order[0 .. L) with L = order[E].
+__global__ void __launch_bounds__(1024) sgd_prep_kernel(const int32_t *__restrict__ offs, int E,
+                                                        int32_t *__restrict__ order, unsigned int *__restrict__ amax) {
     __shared__ int32_t sz[4096];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sz[e] = __ldg(offs + e + 1) - __ldg(offs + e);
+    __shared__ int live;
+    if (threadIdx.x == 0) live = 0;
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t n = __ldg(offs + e + 1) - __ldg(offs + e);
+        if (n > 0) {
+            amax[e] = 0u;
+            atomicAdd(&live, 1);
+        }
+        if (order != nullptr) sz[e] = n;
+    }
+    __syncthreads();
+    if (order == nullptr) return;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int ke = sz[e];
+        if (ke == 0) continue;
         int rank = 0;
         for (int j = 0; j < E; ++j) rank += (sz[j] > ke) || (sz[j] == ke && j < e);
         order[rank] = e;
     }
+    if (threadIdx.x == 0) order[E] = live;
 }
 
 // Whether ws holds the tensor-core copies of both operands' scale factors.
@@ -1019,6 +1171,55 @@ extern "C" int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *
     a.sfb_tile_stride = K / 64;
     CUtensorMap td;
     if (!make_out_map(&td, d, bf16, rows_total, N, TMA_CW<0>)) return MOE4_ERR_CUDA;
+    return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
+}
+
+extern "C" int grouped_expert_gemm_nvfp4_hadamard_amax(const uint8_t *a_codes, const uint8_t *a_sf,
+                                                       const float *a_g_dec, const uint8_t *b_codes,
+                                                       const uint8_t *b_sf, const float *b_g_dec,
+                                                       const int32_t *group_offs, int64_t E, int64_t rows_total,
+                                                       int64_t N, int64_t K, uint16_t *d, float *amax_out,
+                                                       uint32_t flags, void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && rows_total >= 0 && rows_total % BM == 0 && N > 0 && N % BN == 0 && K > 0 &&
+                   K % 256 == 0);
+    MOE4_CHECK_ARG(a_codes && a_sf && a_g_dec && b_codes && b_sf && b_g_dec && group_offs && d && amax_out);
+    MOE4_CHECK_ARG(aligned16(a_codes) && aligned16(b_codes) && aligned16(a_sf) && aligned16(b_sf) && aligned16(d) &&
+                   aligned4(amax_out));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    MOE4_CHECK_ARG(rows_total < (int64_t(1) << 31) && E * N < (int64_t(1) << 31));
+    // a missing workspace is reported before anything is enqueued
+    if (rows_total > 0 && !(flags & MOE4_SF_MMA_LAYOUT) && !scales_ws_ok(rows_total, E * N, K, 16, ws, ws_bytes))
+        return MOE4_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (rows_total == 0) return MOE4_OK;
+    const uint8_t *sfa, *sfb;
+    int rc = stage_scales(a_sf, rows_total, b_sf, E * N, K, 16, flags, ws, ws_bytes, &sfa, &sfb, st);
+    if (rc != MOE4_OK) return rc;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, a_codes, K / 2, rows_total, BM) || !make_map(&tb, b_codes, K / 2, E * N, BN))
+        return MOE4_ERR_CUDA;
+    Args a{};
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.a_g_dec = a_g_dec;
+    a.b_g_dec = b_g_dec;
+    a.offs = group_offs;
+    a.E = (int)E;
+    a.group_k = 0;
+    a.M = rows_total;
+    a.N = N;
+    a.K = K;
+    a.d = d;
+    a.mode = BF16;
+    a.had_amax = reinterpret_cast<unsigned int *>(amax_out);
+    a.n_tiles_n = (int)(N / BN);
+    a.n_tiles_m = (int)(rows_total / BM);
+    a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
+    a.sfa_tile_stride = K / 64;
+    a.sfb_tile_stride = K / 64;
+    CUtensorMap td;
+    if (!make_out_map(&td, d, true, rows_total, N, TMA_CW<0>)) return MOE4_ERR_CUDA;
     return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
 }
 
@@ -1138,12 +1339,14 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     if (M > 0 && K > 0 && !(flags & MOE4_SF_MMA_LAYOUT) && !scales_ws_ok(M, N, K, 32, ws, ws_bytes))
         return MOE4_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
-    if (cudaMemsetAsync(amax_out, 0, (size_t)E * sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
-    if (M == 0) return MOE4_OK;
+    if (M == 0) {  // empty weight matrices: the amax of every expert that has rows is 0
+        sgd_prep_kernel<<<1, 1024, 0, st>>>(group_offs, (int)E, nullptr, reinterpret_cast<unsigned int *>(amax_out));
+        return launch_status();
+    }
     Args g{};
     const uint8_t *sfa = a_e8, *sfb = b_e8;
     CUtensorMap ta, tb;
-    const int64_t Kmap = K > 0 ? K : 128;  // an empty contraction still runs the epilogue (dW = 0)
+    const int64_t Kmap = K > 0 ? K : 128;  // K = 0: every expert is skipped, the maps are never read
     if (K > 0) {
         int rc = stage_scales(a_e8, M, b_e8, N, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
         if (rc != MOE4_OK) return rc;
@@ -1152,17 +1355,18 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
     static_assert(EpiCfg<EPI_SGD32>::BNT == BNS, "both SGD modes use the same tiles");
     if (!make_map(&ta, a, Kmap, M, BM) || !make_map(&tb, b, Kmap, N, BNS)) return MOE4_ERR_CUDA;
     // the expert order for the tile schedule, after the staged scales in the workspace (without
-    // room for it the tiles run in expert order)
+    // room for it the tiles run in expert order); the same one-CTA kernel clears the amax of the
+    // experts that have rows
     size_t used = 0;
     if (K > 0 && !(flags & MOE4_SF_MMA_LAYOUT)) {
         const size_t na = (size_t)(M * (K / 32)), nb = (size_t)(N * (K / 32));
         used = (na + 255) / 256 * 256 + (nb + 255) / 256 * 256;
     }
-    if (E <= 4096 && ws && aligned16(ws) && ws_bytes >= used + (size_t)E * sizeof(int32_t)) {
-        int32_t *order = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + used);
-        expert_order_kernel<<<1, 1024, 0, st>>>(group_offs, (int)E, order);
-        g.order = order;
-    }
+    int32_t *order = nullptr;
+    if (E < 4096 && ws && aligned16(ws) && ws_bytes >= used + (size_t)(E + 1) * sizeof(int32_t))
+        order = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + used);
+    sgd_prep_kernel<<<1, 1024, 0, st>>>(group_offs, (int)E, order, reinterpret_cast<unsigned int *>(amax_out));
+    g.order = order;
     g.sfa = sfa;
     g.sfb = sfb;
     g.offs = group_offs;
@@ -1190,6 +1394,28 @@ extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e
                          CU_TENSOR_MAP_SWIZZLE_32B))
         return MOE4_ERR_CUDA;
     return w_bf16 ? launch<1, EPI_SGD>(ta, tb, tw, twb, g, st) : launch<1, EPI_SGD32>(ta, tb, tw, twb, g, st);
+}
+
+template <int KIND, bool kCopySf>
+static int launch_peak(int64_t iters, int64_t ctas, uint32_t *sink, cudaStream_t st) {
+    constexpr int SMEM = A_TILE + BN * BKB + 3 * 4 * 512 + 64 + 1024;
+    if (cudaFuncSetAttribute(mma_peak_kernel<KIND, kCopySf>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+        cudaSuccess)
+        return MOE4_ERR_CUDA;
+    mma_peak_kernel<KIND, kCopySf><<<(unsigned)ctas, 128, SMEM, st>>>(iters, sink);
+    return launch_status();
+}
+
+extern "C" int moe4_tensor_peak_probe(int kind, int64_t iters, int64_t ctas, uint32_t *sink, void *stream) {
+    MOE4_CHECK_ARG(kind >= 0 && kind <= 3 && iters >= 1 && iters <= (int64_t(1) << 20) && ctas >= 1 && ctas <= 4096);
+    MOE4_CHECK_ARG(sink && aligned4(sink));
+    cudaStream_t st = as_stream(stream);
+    switch (kind) {
+        case 0: return launch_peak<0, false>(iters, ctas, sink, st);
+        case 1: return launch_peak<1, false>(iters, ctas, sink, st);
+        case 2: return launch_peak<0, true>(iters, ctas, sink, st);
+        default: return launch_peak<1, true>(iters, ctas, sink, st);
+    }
 }
 
 extern "C" int moe4_selftest_wait(int64_t limit_cycles, void *stream) {

@@ -48,18 +48,23 @@ _SIGNATURES = {
     "moe4_workspace_size_gemm": (_sz, [_int, _i64, _i64, _i64, _i64]),
     "moe4_get_status": (_int, [_vp]),
     "moe4_selftest_wait": (_int, [_i64, _vp]),
+    "moe4_tensor_peak_probe": (_int, [_int, _i64, _i64, _vp, _vp]),
     "moe4_check_group_offsets": (_int, [_vp, _i64, _i64, _i64]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_f32": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
     "mxfp8_requant_transpose_sr": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
+    "nvfp4_quantize_f32_requant": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _vp,
+                                          _u32, _vp]),
     "mxfp8_quantize": (_int, [_vp, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
     "mxfp8_quantize_rowcol": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "hadamard_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "hadamard_dequant": (_int, [_vp, _vp, _vp, _i64, _i64, _vp, _u32, _vp]),
     "grouped_expert_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32,
                                          _vp, _sz, _vp]),
+    "grouped_expert_gemm_nvfp4_hadamard_amax": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                        _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_expert_gemm_nvfp4_hadamard_mx": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                       _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32, _vp, _sz, _vp]),
@@ -166,6 +171,10 @@ def moe4_selftest_wait(limit_cycles, stream=None):
     _call("moe4_selftest_wait", limit_cycles, _s(stream))
 
 
+def moe4_tensor_peak_probe(kind, iters, ctas, sink, stream=None):
+    _call("moe4_tensor_peak_probe", kind, iters, ctas, _p(sink), _s(stream))
+
+
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     """A 256-byte aligned scratch buffer of at least nbytes (torch's allocator aligns to 512)."""
     return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
@@ -200,6 +209,12 @@ def mxfp8_requant_transpose_sr(codes, sf, g_dec, nmat, rows, cols, q_t, e8_t, se
           seed, stream_id, flags, _s(stream))
 
 
+def nvfp4_quantize_f32_requant(x, nmat, rows, cols, amax_in, codes, sf, g_dec, q_t, e8_t, seed=0, stream_id=0,
+                               group_offs=None, flags=FOUR_OVER_SIX | SR, stream=None):
+    _call("nvfp4_quantize_f32_requant", _p(x), nmat, rows, cols, _p(amax_in), _p(codes), _p(sf), _p(g_dec), _p(q_t),
+          _p(e8_t), seed, stream_id, _p(group_offs), flags, _s(stream))
+
+
 def mxfp8_quantize(x, rows, cols, q, e8, seed=0, stream_id=0, flags=ROWWISE, stream=None):
     _call("mxfp8_quantize", _p(x), rows, cols, _p(q), _p(e8), seed, stream_id, flags, _s(stream))
 
@@ -223,6 +238,13 @@ def grouped_expert_gemm_nvfp4(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, gr
                               flags=OUT_F32, ws=None, stream=None):
     _call("grouped_expert_gemm_nvfp4", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf), _p(b_g_dec),
           _p(group_offs), E, rows_total, N, K, _p(d), flags, _p(ws), _ws_bytes(ws), _s(stream))
+
+
+def grouped_expert_gemm_nvfp4_hadamard_amax(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, group_offs, E,
+                                            rows_total, N, K, d, amax_out, flags=0, ws=None, stream=None):
+    _call("grouped_expert_gemm_nvfp4_hadamard_amax", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf),
+          _p(b_g_dec), _p(group_offs), E, rows_total, N, K, _p(d), _p(amax_out), flags, _p(ws), _ws_bytes(ws),
+          _s(stream))
 
 
 def grouped_expert_gemm_nvfp4_hadamard_mx(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, group_offs, E, rows_total,

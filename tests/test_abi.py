@@ -78,6 +78,11 @@ MISALIGNED = FAKE + 4
     ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 40, 64, 128, FAKE, FAKE, FAKE, FAKE, 0, None)),  # k > 32
     ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 100, FAKE, FAKE, FAKE, FAKE, 0, None)),  # rows % 32
     ("hadamard_quant", (FAKE, 4, 64, FAKE, FAKE, FAKE, 1, FAKE, 4, None)),                   # cols % 128
+    ("hadamard_quant", (FAKE, 4, 128, FAKE, FAKE, FAKE, 1 | 0x10000, FAKE, 4, None)),         # bad flag
+    ("grouped_expert_gemm_nvfp4_hadamard_amax", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE,
+                                                 None, 0, None, 0, None)),                    # no amax_out
+    ("grouped_expert_gemm_nvfp4_hadamard_amax", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE,
+                                                 FAKE, 0x200, None, 0, None)),                # output flag
     ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 200, 256, FAKE,
                                                FAKE, 0, None, 0, None)),                      # N % 256
     ("grouped_expert_gemm_nvfp4_hadamard_mx", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256,
@@ -114,6 +119,16 @@ MISALIGNED = FAKE + 4
     ("moe4_combine_backward_mxfp8", (FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 128, FAKE, FAKE, FAKE, FAKE, 0x40000,
                                      None)),                                                  # d % 128
     ("mxfp8_quantize", (FAKE, 128, 128, FAKE, FAKE, 0, 0, 0x10 | 0x40000, None)),             # not offered
+    # the fused weight path: cols % 64, rows % 32, no amax, tile layouts on 128-row tiles
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 96, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 48, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 96, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x10005,
+                                    None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x40005,
+                                    None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x100,
+                                    None)),                                                   # bad flag
 ])
 def test_argument_checks_fail_on_host(lib, case):
     name, args = case

@@ -105,3 +105,68 @@ def test_fused_against_oracle_end_to_end():
     err = np.linalg.norm(chunks(got - ref), axis=2)
     assert np.all(err <= bound), "worst chunk err/bound %.3f" % float(np.max(err / bound))
     assert np.mean(to_np(q) == rq) >= 0.9 and np.mean(to_np(e8) == re8) >= 0.9
+
+
+def _nvfp4_codec_case(h, w, offs, E, N, K):
+    """The down projection with the rotated amax from its last stage, then the NVFP4 return-path
+    encoder taking that amax; beside it the plain bf16 GEMM and the encoder's own amax pass."""
+    R = int(offs[-1])
+    ac, asf, ag = nvfp4_quantize(h, 1, R, K)
+    bc, bsf, bg = nvfp4_quantize(w, E, N, K)
+    offs_d = to_dev(offs)
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, R, E, N, K))
+    y1 = torch.empty((R, N), dtype=torch.int16, device=DEV)
+    amax = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_expert_gemm_nvfp4_hadamard_amax(ac, asf, ag, bc, bsf, bg, offs_d, E, R, N, K, y1, amax, 0, ws)
+    c1, s1, g1 = empty_u8(R, N // 2), empty_u8(R, N // 16), torch.empty(1, dtype=torch.float32, device=DEV)
+    moe4.hadamard_quant(y1, R, N, c1, s1, g1, moe4.FOUR_OVER_SIX | moe4.AMAX_GIVEN, amax)
+    y2 = torch.empty((R, N), dtype=torch.int16, device=DEV)
+    moe4.grouped_expert_gemm_nvfp4(ac, asf, ag, bc, bsf, bg, offs_d, E, R, N, K, y2, moe4.OUT_BF16, ws)
+    c2, s2, g2 = empty_u8(R, N // 2), empty_u8(R, N // 16), torch.empty(1, dtype=torch.float32, device=DEV)
+    hws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT))
+    moe4.hadamard_quant(y2, R, N, c2, s2, g2, moe4.FOUR_OVER_SIX, hws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    assert torch.equal(y1, y2)
+    assert torch.equal(amax.view(torch.int32), hws[:4].view(torch.int32))
+    assert torch.equal(c1, c2) and torch.equal(s1, s2) and torch.equal(g1, g2)
+    return y1, amax, c1, s1, g1
+
+
+def test_nvfp4_codec_amax_from_gemm_small_groups():
+    """The NVFP4 return path with its amax taken in the GEMM's last stage equals the bf16 GEMM
+    followed by the two-pass encoder, byte for byte, and both equal the oracle's encoder of the
+    same bf16 product."""
+    rng = np.random.default_rng(44)
+    sizes = [256, 128, 0, 384, 128]
+    E, N, K = len(sizes), 512, 512
+    offs = _offs(sizes)
+    h = inputs.to_bf16_bits((rng.standard_t(3, (int(offs[-1]), K)) / np.sqrt(3)).astype(np.float32))
+    w = inputs.to_bf16_bits((rng.standard_normal((E * N, K)) * 0.02).astype(np.float32))
+    y, amax, c, s, g = _nvfp4_codec_case(to_dev(h), to_dev(w), offs, E, N, K)
+    rc, rs, rg = oracle.hadamard_quant(oracle.bf16_to_f32(to_np(y, np.uint16)))
+    assert np.array_equal(to_np(c), rc) and np.array_equal(to_np(s), rs) and float(to_np(g)[0]) == float(rg)
+
+
+def test_nvfp4_codec_amax_from_gemm_layer_shape():
+    """At the layer step's down-projection shape (384 experts, 160512 padded rows, d_model 4096,
+    width 2048): the same byte-for-byte equality, and sampled rows against the oracle: its
+    rotation of the whole bf16 product gives the amax, then its NVFP4 quantiser encodes the
+    sampled rotated rows with that amax ("4-bit computation from the start of Inkling 2 Small's
+    pretraining", communication and kernels paragraphs)."""
+    rng = np.random.default_rng(0)
+    counts = rng.multinomial(16384 * 8, rng.dirichlet(np.ones(384) * 0.5))
+    offs = _offs((counts + 127) // 128 * 128)
+    E, N, K = 384, 4096, 2048
+    R = int(offs[-1])
+    h = inputs.device_student_t((R, K), inputs.device_generator(9, 0, DEV), DEV).view(torch.int16)
+    w = inputs.device_normal((E * N, K), 0.02, inputs.device_generator(9, 1, DEV), DEV).view(torch.int16)
+    y, amax, c, s, g = _nvfp4_codec_case(h, w, offs, E, N, K)
+    del h, w
+    rot = oracle.hadamard_rotate(oracle.bf16_to_f32(to_np(y, np.uint16)))
+    ref_amax = np.float32(np.abs(rot).max())
+    assert float(to_np(amax)[0]) == float(ref_amax)
+    rows = np.unique(np.random.default_rng(3).choice(R, 64, replace=False))
+    rc, rs, rg = oracle.nvfp4_quantize(rot[rows], amax=ref_amax)
+    assert float(to_np(g)[0]) == float(rg)
+    assert np.array_equal(to_np(c)[rows], rc) and np.array_equal(to_np(s)[rows], rs)
