@@ -196,8 +196,8 @@ int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const fl
                                uint8_t *e8_t, uint64_t seed, uint32_t stream_id, uint32_t flags,
                                void *stream);
 
-/* nvfp4_quantize_f32_requant: the weight path of one training step in one pass over the binary32
- * master weights x [nmat, rows, cols] (contiguous rows): nvfp4_quantize_f32 with MOE4_AMAX_GIVEN
+/* nvfp4_quantize_f32_requant: the weight path of one training step over the binary32 master
+ * weights x [nmat, rows, cols] (contiguous rows), in one call: nvfp4_quantize_f32 with MOE4_AMAX_GIVEN
  * (amax_in [nmat]; Four Over Six with MOE4_FOUR_OVER_SIX) writes codes [nmat, rows, cols/2], sf
  * (canonical, or the tile layout with MOE4_SF_MMA_LAYOUT) and g_dec [nmat] for the forward GEMM,
  * and mxfp8_requant_transpose_sr of that result (seed, stream_id, MOE4_SR, MOE4_SF_OUT_MMA as

@@ -13,7 +13,6 @@
 // values of each (two lanes share the Philox calls that give their 16-bit numbers), 8 lanes form
 // one 32-block.
 #include "common.cuh"
-#include "nvfp4.cuh"
 
 namespace moe4 {
 
@@ -26,20 +25,7 @@ constexpr int kTileC = 64;
 // columns, so each GU and dH value is read once.
 // CombineBwd: the combine's gradient dYhat [R, C] formed on the fly, dispatched row r = token t's
 // slot j: bf16(w[t, j] * dy[t]) as moe4_combine_backward computes it (padding rows zero).
-// F32Nvfp4: binary32 master weights, NVFP4-quantised here (written out for the forward GEMM, as
-// nvfp4_quantize_f32 with a given amax writes them) and then requantised from those codes, as
-// the Nvfp4 source would be: the fused weight path.
-enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd, F32Nvfp4 };
-
-// The F32Nvfp4 source's extra arguments: its NVFP4 outputs and the rule that skips matrices.
-struct Nvfp4Out {
-    const float *amax;     // [nmat] per-matrix amax (of the bf16 rounding of the values)
-    uint8_t *codes;        // [nmat, R, C/2]
-    uint8_t *sf;           // [nmat, R, C/16], canonical or tile layout (sf_mma)
-    float *g_dec;          // [nmat]
-    const int32_t *offs;   // [nmat + 1] or null: matrix m is skipped when offs[m + 1] == offs[m]
-    bool four_over_six, sf_mma;
-};
+enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 
 // Output of one warp: 128 values of each of the output rows cA and cA + 1 (the input columns of
 // one pair-row of the tile, word p = {column cA, column cA + 1} as 16-bit halves).  Lane l owns
@@ -52,7 +38,7 @@ template <SrcKind kind, bool kSR, bool kJ32>
 __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int64_t m, int64_t cA, int64_t r0,
                                           int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t (*e8s)[4], int cl,
                                           const PhiloxKeys keys, uint32_t stream_id, bool safe) {
-    constexpr bool kF16 = kind == SrcKind::Nvfp4 || kind == SrcKind::F32Nvfp4;
+    constexpr bool kF16 = kind == SrcKind::Nvfp4;
     const int lane = lane_id();
     uint32_t mx = max_abs16x2<kF16>(max_abs16x2<kF16>(p.x, p.y), max_abs16x2<kF16>(p.z, p.w));
     mx = max_abs16x2<kF16>(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -162,7 +148,7 @@ __device__ __forceinline__ void emit_rowwise32(const uint32_t h[16], int64_t r, 
 constexpr int kPairs = kTileC / 2;
 
 template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true>
-__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd || kind == SrcKind::F32Nvfp4) ? 4 : 5)
+__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 : 5)
 requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
@@ -170,18 +156,13 @@ requant_transpose_kernel(
     uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr, const float *__restrict__ gu = nullptr,
     const float *__restrict__ dh = nullptr, const int32_t *__restrict__ src_of = nullptr,
     const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0,
-    bool e8_mma = false, const float *__restrict__ x32 = nullptr, const Nvfp4Out qo = {}) {
+    bool e8_mma = false, const int32_t *__restrict__ skip_offs = nullptr) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
-    constexpr bool kQuant = kind == SrcKind::F32Nvfp4;
+    // expert weights: a matrix whose group has no rows (skip_offs[m + 1] == skip_offs[m]) is
+    // skipped whole, its outputs left as they are
+    if (skip_offs != nullptr && __ldg(skip_offs + blockIdx.z + 1) == __ldg(skip_offs + blockIdx.z)) return;
     __shared__ __align__(16) uint32_t tile[kPairs][kTileR];
     __shared__ __align__(4) uint8_t e8s[kTileC][4];
-    // the fused weight path: a matrix whose group has no rows is skipped whole (its outputs are
-    // left as they are); the scale table of the block quantiser
-    __shared__ float2 qtab[kQuant ? 128 : 1];
-    if constexpr (kQuant) {
-        if (qo.offs != nullptr && __ldg(qo.offs + blockIdx.z + 1) == __ldg(qo.offs + blockIdx.z)) return;
-        fill_scale_tab(qtab);
-    }
     const int64_t f = C / 2;  // SwigluBwd: C = 2f
     // grid (row tiles, column tiles, matrices): no index division
     const int64_t m = blockIdx.z;
@@ -191,7 +172,7 @@ requant_transpose_kernel(
 
     // NVFP4 source with stochastic rounding: the smallest non-zero and the largest block scale of
     // the tile (f16 bits), reduced over the CTA (see `safe` below)
-    constexpr bool kScaleRange = kSR && (kind == SrcKind::Nvfp4 || kQuant);
+    constexpr bool kScaleRange = kSR && kind == SrcKind::Nvfp4;
     __shared__ uint32_t sf_red[2][8];
     uint32_t sf_lo = 0x7C00u, sf_hi = 0u;
     // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
@@ -202,54 +183,7 @@ requant_transpose_kernel(
         const int64_t c = out_col(half * 32);
         uint32_t h[16];  // 32 16-bit values, element 2i in the low half of h[i]
         if (r < R && c < C) {
-            if constexpr (kQuant) {
-                // 32 binary32 values -> bf16 (nearest-even) -> y = RN(x * g_enc) -> two NVFP4 blocks
-                // with Four Over Six, exactly as nvfp4_quantize_f32 with the given amax; codes and
-                // scales go out for the forward GEMM, the exact f16 products e2m1 * e4m3 into the tile
-                const GlobalScale gs = global_scale(__ldg(qo.amax + m));
-                const uint64_t g2 = f2_pack(gs.enc, gs.enc);
-                const int64_t nblk = C / 16, b = c / 16;
-                const float4 *src = reinterpret_cast<const float4 *>(x32 + (m * R + r) * C + c);
-                uint32_t sc[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    uint32_t wv[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float4 f = __ldg(src + 4 * k + i);
-                        wv[2 * i] = bf16x2_rn(f.x, f.y);
-                        wv[2 * i + 1] = bf16x2_rn(f.z, f.w);
-                    }
-                    float y[16];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        f2_unpack(f2_mul(f2_pack(bf16_lo(wv[i]), bf16_hi(wv[i])), g2), y[2 * i], y[2 * i + 1]);
-                    uint32_t w0, w1, scode;
-                    nvfp4_block(y, qo.four_over_six, qtab, w0, w1, scode);
-                    *reinterpret_cast<uint2 *>(qo.codes + ((m * R + r) * C + c) / 2 + 8 * k) = make_uint2(w0, w1);
-                    sc[k] = scode;
-                    const uint32_t sfh = e4m3x2_to_h2(scode | (scode << 8));  // the scale as f16, twice
-                    uint32_t e2[8];
-                    e2m1x8_to_h2x4(w0, e2);
-                    e2m1x8_to_h2x4(w1, e2 + 4);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2[i]),
-                                                   *reinterpret_cast<const __half2 *>(&sfh));
-                        h[8 * k + i] = *reinterpret_cast<const uint32_t *>(&es);
-                    }
-                }
-                // the two scale codes are adjacent bytes in both layouts (b even)
-                const int64_t soff = m * R * nblk + sf_offset(r, b, nblk, qo.sf_mma);
-                *reinterpret_cast<uint16_t *>(qo.sf + soff) = (uint16_t)(sc[0] | (sc[1] << 8));
-                if constexpr (kScaleRange) {
-                    const uint32_t sf2 = e4m3x2_to_h2(sc[0] | (sc[1] << 8));
-                    const uint32_t sa = sf2 & 0xFFFFu, sb = sf2 >> 16;
-                    sf_lo = min(sa ? sa : 0x7C00u, sb ? sb : 0x7C00u);
-                    sf_hi = max(sa, sb);
-                }
-                if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) qo.g_dec[m] = gs.dec;
-            } else if constexpr (kind == SrcKind::Nvfp4) {
+            if constexpr (kind == SrcKind::Nvfp4) {
                 const uint4 w = __ldg(reinterpret_cast<const uint4 *>(codes + ((m * R + r) * C + c) / 2));
                 // the scales of blocks c/16 and c/16 + 1 (c/16 even): adjacent bytes in both layouts
                 const int64_t nblk = C / 16, b = c / 16;
@@ -389,7 +323,7 @@ requant_transpose_kernel(
         const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, ln < 8 ? sf_red[1][ln] : 0u);
         const float lo_f = __half2float(__ushort_as_half((unsigned short)lo));
         const float hi_f = __half2float(__ushort_as_half((unsigned short)hi));
-        const float gd = kQuant ? global_scale(__ldg(qo.amax + m)).dec : __ldg(g_dec + m);
+        const float gd = __ldg(g_dec + m);
         safe = lo == 0x7C00u || (hi_f <= lo_f * 1024.0f && 0.5f * lo_f * gd >= 0x1p-100f);
     }
     if constexpr (kSwb && kRow) {
@@ -407,7 +341,7 @@ requant_transpose_kernel(
     }
 
     // phase 2: each warp emits one pair-row (two output rows) per iteration
-    const float g = kQuant ? global_scale(__ldg(qo.amax + m)).dec : (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
+    const float g = (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
 #pragma unroll 1
     for (int i = 0; i < kPairs / 8; ++i) {
         const int cp = warp_id() + 8 * i;
@@ -533,20 +467,25 @@ extern "C" int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t 
     dim3 grid;
     MOE4_CHECK_ARG(requant_grid(rows, cols / kTileC, nmat, grid));
     if (rows == 0) return MOE4_OK;
+    cudaStream_t st = as_stream(stream);
+    // two passes over the experts that have rows: the HBM-bound quantiser of the binary32
+    // masters, then the issue-bound requantiser of its codes (one fused pass measured slower:
+    // its block quantiser and the requantiser share a CTA's issue slots and its barrier)
+    int rc = quantize_f32_given(x, nmat, rows, cols, amax_in, codes, sf, g_dec, group_offs,
+                                (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, st);
+    if (rc != MOE4_OK) return rc;
     const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 35);
     const PhiloxKeys keys = philox_keys(seed);
-    const Nvfp4Out qo{amax_in, codes, sf, g_dec, group_offs, (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma};
-    cudaStream_t st = as_stream(stream);
-#define MOE4_FUSED_ARGS                                                                                         \
-    nullptr, nullptr, nullptr, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, false, nullptr, nullptr, \
-        nullptr, nullptr, nullptr, nullptr, nullptr, 0, e8_mma, x, qo
+#define MOE4_WEIGHT_ARGS                                                                                          \
+    codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, sf_mma, nullptr, nullptr, nullptr, \
+        nullptr, nullptr, nullptr, nullptr, 0, e8_mma, group_offs
     if ((flags & MOE4_SR) && j32)
-        requant_transpose_kernel<SrcKind::F32Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_FUSED_ARGS);
+        requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
     else if (flags & MOE4_SR)
-        requant_transpose_kernel<SrcKind::F32Nvfp4, true, false, false><<<grid, 256, 0, st>>>(MOE4_FUSED_ARGS);
+        requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
     else
-        requant_transpose_kernel<SrcKind::F32Nvfp4, false><<<grid, 256, 0, st>>>(MOE4_FUSED_ARGS);
-#undef MOE4_FUSED_ARGS
+        requant_transpose_kernel<SrcKind::Nvfp4, false><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
+#undef MOE4_WEIGHT_ARGS
     return launch_status();
 }
 
