@@ -14,7 +14,8 @@ N(0,1) bias, Student-t(3) activations, N(0, 0.02) expert weights held as FP32 ma
             W_down, H, W_gate/up and X; grouped MXFP8 dgrad (row-grouped) and wgrad
             (contraction-grouped) GEMMs for both projections; SwiGLU backward; SGD on the FP32
             master weights, fused into the weight-gradient GEMMs (the next step quantises the
-            masters, rounded to bf16 as they are read).
+            masters, rounded to bf16 as they are read); the dispatch's gradient (each token's k
+            rows of dX summed back into token order).
 
 `value` is expert-GEMM TFLOP/s of the whole step: the algorithmic FLOPs of the six expert GEMMs
 (routed rows only) divided by the device time of the step.  The JSON line also carries per-kernel
@@ -140,6 +141,7 @@ class LayerStep:
         self.WguT_q, self.WguT_e = torch.empty((E, d, 2 * f), **u8), torch.empty((E, d, 2 * f // 32), **u8)
         self.XpT_q, self.XpT_e = torch.empty(d * R, **u8), torch.empty(d * R // 32, **u8)
         self.dXp = torch.empty((R, d), dtype=torch.int16, device=dev)
+        self.dX = torch.empty((T, d), dtype=torch.int16, device=dev)
         # scratch for the GEMMs' scale-layout change (largest call)
         wsz = max(moe4.moe4_workspace_size_gemm(1, R, E, f, d), moe4.moe4_workspace_size_gemm(1, R, E, d, 2 * f),
                   moe4.moe4_workspace_size_gemm(1, d, 1, f, R), moe4.moe4_workspace_size_gemm(1, 2 * f, 1, d, R))
@@ -241,6 +243,9 @@ class LayerStep:
             m.grouped_gemm_mxfp8_wgrad_sgd(self.dGUc_q, self.dGUc_e, self.XpT_q, self.XpT_e, self.offs, E, 2 * f, d,
                                            Rp, self.W32_gu, None, LR, self.amax_gu, MMA, self.gws)
         n += 2
+        with tm("dispatch_bwd"):  # each token's k dispatched rows of dX summed back into token order
+            m.moe4_dispatch_backward(self.dXp, self.row_of, T, k, d, self.dX)
+        n += 1
         self.launches += n
         return n
 
@@ -273,6 +278,7 @@ class LayerStep:
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
         b["hadamard"] = rows * d * (2 + nv + nv + 2)   # amax from the down GEMM's last stage
         b["combine"] = rows * d * 2 + T * d * 2
+        b["dispatch_bwd"] = rows * d * 2 + T * d * 2
         b["route"] = T * E * 4 + rows * 4 * 4
         return b
 

@@ -416,6 +416,14 @@ int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *row_of, const
 int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const float *w, int64_t T,
                  int64_t k, int64_t d, uint16_t *y, void *stream);
 
+/* moe4_dispatch_backward: the gradient of the dispatch (the NVFP4 row gather is passed straight
+ * through): dx[t] = sum over slots j in order of dxp[row_of[t,j]], one binary32 add per slot from
+ * 0, then nearest-even to bf16 [LHC communication paragraph: tokens are sent to the processors of
+ * their experts and the results combined; this is that send's adjoint].  dxp bf16 [rows, d], dx
+ * bf16 [T, d]; 1 <= k <= 32; d % 8 == 0; dxp and dx 16-byte aligned. */
+int moe4_dispatch_backward(const uint16_t *dxp, const int32_t *row_of, int64_t T, int64_t k, int64_t d,
+                           uint16_t *dx, void *stream);
+
 /* moe4_sgd_update: FP32 master weights [LHC: master weights in FP32] w32 <- w32 - lr * dw (one
  * product, one difference) and w_bf16 <- bf16(w32) (nearest-even); n % 4 == 0. */
 int moe4_sgd_update(float *w32, const float *dw, int64_t n, float lr, uint16_t *w_bf16,

@@ -469,6 +469,21 @@ def combine(yhat_bf16: np.ndarray, row_of: np.ndarray, w: np.ndarray) -> np.ndar
     return f32_to_bf16(acc)
 
 
+def dispatch_backward(dxp_bf16: np.ndarray, row_of: np.ndarray) -> np.ndarray:
+    """The gradient of the dispatch (row t of the tokens was sent to rows row_of[t, j]; the
+    quantisation of the sent rows passes the gradient straight through): dx[t] = sum over slots j
+    in order of dxp[row_of[t, j]], one binary32 add per slot from 0; returned as bf16."""
+    g = bf16_to_f32(dxp_bf16)
+    T, k = row_of.shape
+    out = np.empty((T, g.shape[1]), np.uint16)
+    for t in range(T):
+        acc = np.zeros(g.shape[1], np.float32)
+        for j in range(k):
+            acc = (acc + g[row_of[t, j]]).astype(np.float32)
+        out[t] = f32_to_bf16(acc)
+    return out
+
+
 def sgd_update(w32: np.ndarray, dw: np.ndarray, lr: float):
     """Plain SGD on the binary32 master weights (the pages keep master weights in FP32 but name
     no optimiser): w <- w - (lr * dw), one product and one difference; plus the bf16 copy that the

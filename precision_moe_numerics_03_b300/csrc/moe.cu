@@ -293,7 +293,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
             const int64_t row = row_of[t * k + j];
-            const float wj = w[t * k + j];
+            // without weights (the dispatch's gradient) each slot's value is added as it is: the
+            // product by 1 is exact
+            const float wj = w != nullptr ? w[t * k + j] : 1.0f;
             const uint4 q = __ldg(reinterpret_cast<const uint4 *>(yhat + row * d + c));
             const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -434,6 +436,15 @@ extern "C" int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const f
     MOE4_CHECK_ARG(T == 0 || (yhat && row_of && w && y && aligned16(yhat) && aligned16(y)));
     if (T == 0) return MOE4_OK;
     combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
+    return launch_status();
+}
+
+extern "C" int moe4_dispatch_backward(const uint16_t *dxp, const int32_t *row_of, int64_t T, int64_t k, int64_t d,
+                                      uint16_t *dx, void *stream) {
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 8 == 0);
+    MOE4_CHECK_ARG(T == 0 || (dxp && row_of && dx && aligned16(dxp) && aligned16(dx)));
+    if (T == 0) return MOE4_OK;
+    combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(dxp, row_of, nullptr, T, (int)k, d, dx);
     return launch_status();
 }
 

@@ -82,6 +82,7 @@ _SIGNATURES = {
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "moe4_swiglu_amax": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    "moe4_dispatch_backward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_sgd_update": (_int, [_vp, _vp, _i64, _f32, _vp, _vp]),
     "moe4_convert": (_int, [_int, _vp, _i64, _vp, _vp]),
     "moe4_sr_words": (_int, [_u64, _u32, _u64, _i64, _vp, _vp]),
@@ -314,6 +315,10 @@ def moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, rows_total, q_ro
 
 def moe4_combine(yhat, row_of, w, T, k, d, y, stream=None):
     _call("moe4_combine", _p(yhat), _p(row_of), _p(w), T, k, d, _p(y), _s(stream))
+
+
+def moe4_dispatch_backward(dxp, row_of, T, k, d, dx, stream=None):
+    _call("moe4_dispatch_backward", _p(dxp), _p(row_of), T, k, d, _p(dx), _s(stream))
 
 
 def moe4_sgd_update(w32, dw, n, lr, w_bf16, stream=None):

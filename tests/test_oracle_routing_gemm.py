@@ -160,3 +160,22 @@ def test_combine_backward_is_the_adjoint_of_the_combine(orc):
     # rows no (token, slot) maps to are zero
     unused = np.setdiff1d(np.arange(R), row_of.reshape(-1))
     assert unused.size == R - T * k and np.all(dyhat[unused] == 0)
+
+
+def test_dispatch_backward_is_the_adjoint_of_the_gather(orc):
+    # <gather(x), g> = <x, dispatch_backward(g)> with gather(x)[row_of[t, j]] = x[t]: small integers
+    # keep every sum and bf16 rounding exact, so the identity holds exactly; a transposed index or
+    # a dropped slot breaks it
+    rng = np.random.default_rng(14)
+    T, k, d, R = 30, 8, 16, 400
+    row_of = rng.permutation(R)[:T * k].reshape(T, k).astype(np.int32)
+    x = rng.integers(-4, 5, (T, d)).astype(np.float32)
+    g = orc.f32_to_bf16(rng.integers(-4, 5, (R, d)).astype(np.float32))
+    xp = orc.permute_rows(x, row_of, R).astype(np.float64)
+    dx = orc.bf16_to_f32(orc.dispatch_backward(g, row_of)).astype(np.float64)
+    lhs = float(np.sum(xp * orc.bf16_to_f32(g)))
+    rhs = float(np.sum(x.astype(np.float64) * dx))
+    assert lhs == rhs and lhs != 0.0
+    # one slot: the gradient row itself; slot order matters only through rounding
+    one = orc.dispatch_backward(g, row_of[:, :1])
+    assert np.array_equal(one, g[row_of[:, 0]])
