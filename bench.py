@@ -55,8 +55,9 @@ METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
-TRAFFIC_RATIO = {}
-GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 2}
+TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.9 / 2216.7}  # profiles/gemm_mxfp8_wgrad_sgd_16experts.md
+MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "swiglu_quant_h", "hadamard", "mxfp8_quant"}
+GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 4}
 
 
 def load_peaks():
@@ -186,7 +187,7 @@ class LayerStep:
                                          self.WguT_q, self.WguT_e, seed, 3, self.offs, WF)
             m.nvfp4_quantize_f32_requant(self.W32_d, E, d, f, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g,
                                          self.WdT_q, self.WdT_e, seed, 1, self.offs, WF)
-        n += 2
+        n += 4  # each call: the quantiser, then the requantiser
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
                                         E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
@@ -720,11 +721,31 @@ def profile_case(name):
             out = torch.empty((rows, d), dtype=torch.int16, device=dev)
             calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws))
             calls.append(lambda: moe4.hadamard_dequant(c, s_, gd, rows, d, out))
+    elif name == "tensor_peaks":  # the four kinds of the tensor-pipe probe, as TFLOP/s
+        n = torch.cuda.get_device_properties(dev).multi_processor_count
+        sink = torch.zeros(n, dtype=torch.int32, device=dev)
+        res = {}
+        for kind, flop in ((0, 2.0 ** 24), (1, 2.0 ** 23), (2, 2.0 ** 24), (3, 2.0 ** 23)):
+            for iters in (5000, 20000):
+                for _ in range(2):
+                    moe4.moe4_tensor_peak_probe(kind, iters, n, sink)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(5):
+                    moe4.moe4_tensor_peak_probe(kind, iters, n, sink)
+                b.record()
+                torch.cuda.synchronize()
+                res["kind%d_iters%d" % (kind, iters)] = round(n * iters * flop / (a.elapsed_time(b) / 5 / 1e3) / 1e12, 1)
+        if moe4.moe4_get_status() != moe4.OK:
+            raise RuntimeError("a device wait timed out")
+        print(json.dumps(res))
+        return 0
     elif name in ("gemm_nvfp4_probe", "gemm_mxfp8_probe"):
         compute_probe(0 if name == "gemm_nvfp4_probe" else 1, reps=3, dev=dev)
         print("profile case %s done" % name)
         return 0
-    elif name == "gemm_nvfp4":
+    elif name in ("gemm_nvfp4", "gemm_nvfp4_down_amax"):
         rows = 128 * 64
         x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
         w = inputs.device_normal((E * 2 * f, d), 0.02, g(0), dev).view(torch.int16)
@@ -737,9 +758,21 @@ def profile_case(name):
         moe4.nvfp4_quantize(x, 1, rows, d, d, ac, as_, ag, None, flags, ws)
         moe4.nvfp4_quantize(w, E, 2 * f, d, d, bc, bs, bg, None, flags, ws)
         offs = torch.arange(0, rows + 1, rows // E, dtype=torch.int32, device=dev)
-        out = torch.empty((rows, 2 * f), dtype=torch.float32, device=dev)
-        calls.append(lambda: moe4.grouped_expert_gemm_nvfp4(ac, as_, ag, bc, bs, bg, offs, E, rows, 2 * f, d, out,
-                                                            moe4.OUT_F32 | moe4.SF_MMA_LAYOUT))
+        if name == "gemm_nvfp4":  # the gate/up projection: binary32 out
+            out = torch.empty((rows, 2 * f), dtype=torch.float32, device=dev)
+            calls.append(lambda: moe4.grouped_expert_gemm_nvfp4(ac, as_, ag, bc, bs, bg, offs, E, rows, 2 * f, d, out,
+                                                                moe4.OUT_F32 | moe4.SF_MMA_LAYOUT))
+        else:  # the down projection as the step runs it: bf16 out and the rotated amax for the codec
+            hc, hs = torch.empty((rows, f // 2), **u8), torch.empty((rows, f // 16), **u8)
+            h = inputs.device_student_t((rows, f), g(9), dev).view(torch.int16)
+            moe4.nvfp4_quantize(h, 1, rows, f, f, hc, hs, ag, None, flags, ws)
+            wd = inputs.device_normal((E * d, f), 0.02, g(10), dev).view(torch.int16)
+            dc, ds_ = torch.empty((E, d, f // 2), **u8), torch.empty((E, d, f // 16), **u8)
+            moe4.nvfp4_quantize(wd, E, d, f, f, dc, ds_, bg, None, flags, ws)
+            y = torch.empty((rows, d), dtype=torch.int16, device=dev)
+            am = torch.empty(1, dtype=torch.float32, device=dev)
+            calls.append(lambda: moe4.grouped_expert_gemm_nvfp4_hadamard_amax(hc, hs, ag, dc, ds_, bg, offs, E, rows, d,
+                                                                              f, y, am, moe4.SF_MMA_LAYOUT))
     else:
         rows = 128 * 64
         offs = torch.arange(0, rows + 1, rows // E, dtype=torch.int32, device=dev)
@@ -791,8 +824,9 @@ def main():
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
-                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_mxfp8_wgrad", "gemm_mxfp8_wgrad_sgd",
-                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "gemm_nvfp4_probe",
+                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_nvfp4_down_amax", "gemm_mxfp8_wgrad",
+                             "gemm_mxfp8_wgrad_sgd",
+                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "gemm_nvfp4_probe", "tensor_peaks",
                              "gemm_mxfp8_probe"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
@@ -881,7 +915,9 @@ def main():
     tpk = measure_tensor_peaks(dev)
     fp4_peak = tpk["nvfp4"]["sustained_TFLOPs"]
     fp8_peak = tpk["mxfp8"]["sustained_TFLOPs"]
-    dom = max(per, key=per.get)
+    # the dominant kernel: the group with the most time among those that run one kernel ("quant_w"
+    # runs two, the FP32-master quantiser and the requantiser, each below the fused SGD GEMM)
+    dom = max((k for k in per if k not in MULTI_KERNEL_GROUPS), key=per.get)
     t_dom = per[dom]
     flops_dom = {"gemm_nvfp4": (fwd_flops, fp4_peak), "gemm_mxfp8_dgrad": (fwd_flops, fp8_peak),
                  "gemm_mxfp8_wgrad_sgd": (fwd_flops, fp8_peak)}.get(dom)
