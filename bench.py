@@ -8,7 +8,8 @@ N(0,1) bias, Student-t(3) activations, N(0, 0.02) expert weights held as FP32 ma
   forward   top-k routing and dispatch plan; NVFP4 (Four Over Six) quantisation of X, of every
             expert's gate/up and down weights (per-expert scales) and of H; NVFP4 row gather;
             grouped NVFP4 GEMMs (gate/up, then down) with SwiGLU between them; Hadamard(128) NVFP4
-            return-path encode + decode; weighted combine;
+            return-path encode (its amax from the down GEMM), then decode and weighted combine in
+            one pass;
   backward  combine gradient; MXFP8 quantisation of dY and dGU (row-wise and transposed);
             dequantise -> transpose -> MXFP8 requantisation with Philox stochastic rounding of
             W_down, H, W_gate/up and X; grouped MXFP8 dgrad (row-grouped) and wgrad
@@ -202,12 +203,11 @@ class LayerStep:
             m.grouped_expert_gemm_nvfp4_hadamard_amax(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s,
                                                       self.Wd_g, self.offs, E, Rp, d, f, self.Y, self.amax_y, MMA)
         n += 1
-        with tm("hadamard"):  # the NVFP4 return-path codec, its per-tensor amax given by the GEMM
+        with tm("hadamard"):  # the NVFP4 return-path encoder, its per-tensor amax given by the GEMM
             m.hadamard_quant(self.Y[:Rp], Rp, d, self.Yc_c, self.Yc_s, self.Yc_g, FOS | m.AMAX_GIVEN, self.amax_y)
-            m.hadamard_dequant(self.Yc_c, self.Yc_s, self.Yc_g, Rp, d, self.Yhat[:Rp])
-        n += 2
-        with tm("combine"):
-            m.moe4_combine(self.Yhat, self.row_of, self.w, T, k, d, y)
+        n += 1
+        with tm("combine"):  # decode of the returned rows (rotation back, bf16) and the weighted combine
+            m.moe4_combine_hadamard(self.Yc_c, self.Yc_s, self.Yc_g, self.row_of, self.w, T, k, d, y)
         n += 1
         # ---------------- backward
         with tm("mxfp8_quant"):  # combine gradient straight into both MXFP8 layouts of dY
@@ -277,8 +277,8 @@ class LayerStep:
                                      (w_gu + w_d) * live / E * (4 + 4))   # experts without rows are skipped
         b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 + rows * f * (2 + nv)  # amax fused into SwiGLU
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
-        b["hadamard"] = rows * d * (2 + nv + nv + 2)   # amax from the down GEMM's last stage
-        b["combine"] = rows * d * 2 + T * d * 2
+        b["hadamard"] = rows * d * (2 + nv)            # amax from the down GEMM's last stage
+        b["combine"] = rows * d * nv + T * d * 2       # decoded from the NVFP4 rows as it combines
         b["dispatch_bwd"] = rows * d * 2 + T * d * 2
         b["route"] = T * E * 4 + rows * 4 * 4
         return b
@@ -721,6 +721,17 @@ def profile_case(name):
             out = torch.empty((rows, d), dtype=torch.int16, device=dev)
             calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws))
             calls.append(lambda: moe4.hadamard_dequant(c, s_, gd, rows, d, out))
+    elif name in ("swiglu_bwd", "swiglu_bwd_mxfp8"):
+        rows = 32768                     # a fifth of the layer's padded rows, SwiGLU width 2048
+        gu = torch.randn((rows, 2 * f), generator=g(11), device=dev)
+        dh = torch.randn((rows, f), generator=g(12), device=dev)
+        if name == "swiglu_bwd":
+            dgu = torch.empty((rows, 2 * f), dtype=torch.int16, device=dev)
+            calls.append(lambda: moe4.moe4_swiglu_backward(gu, dh, rows, f, dgu))
+        else:
+            qr, er = torch.empty((rows, 2 * f), **u8), torch.empty((rows, 2 * f // 32), **u8)
+            qc, ec = torch.empty((2 * f, rows), **u8), torch.empty((2 * f, rows // 32), **u8)
+            calls.append(lambda: moe4.moe4_swiglu_backward_mxfp8(gu, dh, rows, f, qr, er, qc, ec, moe4.SF_OUT_MMA))
     elif name == "tensor_peaks":  # the four kinds of the tensor-pipe probe, as TFLOP/s
         n = torch.cuda.get_device_properties(dev).multi_processor_count
         sink = torch.zeros(n, dtype=torch.int32, device=dev)
@@ -827,6 +838,7 @@ def main():
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_nvfp4_down_amax", "gemm_mxfp8_wgrad",
                              "gemm_mxfp8_wgrad_sgd",
                              "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "gemm_nvfp4_probe", "tensor_peaks",
+                             "swiglu_bwd", "swiglu_bwd_mxfp8",
                              "gemm_mxfp8_probe"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")
     args = ap.parse_args()
@@ -1018,7 +1030,7 @@ def main():
         mf["nvfp4_gemm_ms"] = round(per["gemm_nvfp4"], 4)
         mf["nvfp4_gemm_speedup"] = round(mf["gemm_ms"] / per["gemm_nvfp4"], 3)
         mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["swiglu_quant_h"], 4)
-        nxt["hadamard_mxfp8_codec"]["nvfp4_codec_ms"] = round(per["hadamard"], 4)
+        nxt["hadamard_mxfp8_codec"]["nvfp4_encode_and_decode_combine_ms"] = round(per["hadamard"] + per["combine"], 4)
         probe = {"shape": "8 groups x 8192 rows, N = K = 8192, bf16 out (compute-bound; not the layer's shape)"}
         # timed alone: the burst rates of the tensor-pipe probe
         pk = {"nvfp4": tpk["nvfp4"]["burst_TFLOPs"], "mxfp8": tpk["mxfp8"]["burst_TFLOPs"]}

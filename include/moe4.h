@@ -391,6 +391,16 @@ int moe4_swiglu_backward(const float *gu, const float *dh, int64_t rows, int64_t
 int moe4_swiglu_backward_mxfp8(const float *gu, const float *dh, int64_t rows, int64_t f, uint8_t *q_row,
                                uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, uint32_t flags, void *stream);
 
+/* moe4_combine_hadamard: the combine straight from the NVFP4-encoded return path [LHC
+ * communication paragraph: the expert outputs come back Hadamard-rotated and quantised, and are
+ * combined]: y[t] = sum over slots j in order of w[t,j] * yhat[row_of[t,j]], where yhat is what
+ * hadamard_dequant decodes from (codes [rows, d/2], sf [rows, d/16] canonical, g_dec[0]) — the
+ * bytes of hadamard_dequant followed by moe4_combine, without the decoded rows in memory (only the
+ * rows a token maps to are decoded).  y bf16 [T, d]; 1 <= k <= 32; d % 128 == 0; T * d / 16 below
+ * 2^32; codes and y 16-byte aligned. */
+int moe4_combine_hadamard(const uint8_t *codes, const uint8_t *sf, const float *g_dec, const int32_t *row_of,
+                          const float *w, int64_t T, int64_t k, int64_t d, uint16_t *y, void *stream);
+
 /* moe4_combine_backward: the gradient of the combine with respect to the returned rows:
  * dyhat[row_of[t,j]] = bf16(w[t,j] * dy[t]) (one binary32 product per value), and zero rows for
  * padding (src_of < 0).  dy bf16 [T, d], dyhat bf16 [rows_total, d]; d % 8 == 0, k <= 32.  The

@@ -384,6 +384,58 @@ __global__ void __launch_bounds__(256) hadamard_dequant_kernel(const uint8_t *__
     }
 }
 
+// The combine straight from the NVFP4-encoded return path (hadamard_dequant then moe4_combine,
+// without the decoded rows in memory).  Lane l of a group of eight holds 16 columns of one
+// token's 128-column chunk; in slot order each slot's dispatched row is decoded exactly as
+// hadamard_dequant_kernel does it (dequantise, rotate, round to bf16) and added, times its routing
+// weight, to a binary32 accumulator exactly as combine_kernel does it; then bf16.  Every lane
+// takes part in the shuffles of the rotation; lanes past the end compute on zeros.
+__global__ void __launch_bounds__(256) combine_hadamard_kernel(const uint8_t *__restrict__ codes,
+                                                               const uint8_t *__restrict__ sf,
+                                                               const float *__restrict__ g_dec,
+                                                               const int32_t *__restrict__ row_of,
+                                                               const float *__restrict__ w, int64_t T, int k,
+                                                               int64_t d, uint16_t *__restrict__ y) {
+    const float gd = *g_dec;
+    const uint32_t per_row = (uint32_t)(d / 16);  // 16-value sub-blocks per row
+    const int64_t nsub = T * per_row;
+    MOE4_SUB16_LOOP(nsub) {
+        const int64_t b = b0 + lane_id();
+        const bool live = b < nsub;
+        const uint32_t t = live ? (uint32_t)b / per_row : 0u;  // nsub < 2^32 (checked on the host)
+        const uint32_t sb = live ? (uint32_t)b - t * per_row : 0u;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            float u[16];
+            float wj = 0.0f;
+            if (live) {
+                const int64_t row = __ldg(row_of + (int64_t)t * k + j);
+                wj = __ldg(w + (int64_t)t * k + j);
+                const int64_t sub = row * per_row + sb;
+                const uint2 cw = __ldg(reinterpret_cast<const uint2 *>(codes + sub * 8));
+                const float sfv = e4m3_to_f32(__ldg(sf + sub));
+                float e[16];
+                e2m1x8_to_f32(cw.x, e);
+                e2m1x8_to_f32(cw.y, e + 8);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(__fmul_rn(e[i], sfv), gd);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = 0.0f;
+            }
+            fwht128_sub16(u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float yh = __uint_as_float((uint32_t)f32_to_bf16_bits(u[i]) << 16);
+                acc[i] = __fadd_rn(acc[i], __fmul_rn(wj, yh));
+            }
+        }
+        if (live) store16_bf16(y + (int64_t)t * d + (int64_t)sb * 16, acc);
+    }
+}
+
 // The 8.25-bit return-path codec: Hadamard(128), then MXFP8 (E4M3 elements, one E8M0 scale per 32
 // by the ceiling rule, nearest-even).  One pass: the scales are per 32-block, which is the
 // sub-block pair of lanes 2k and 2k+1 (block amax by one shuffle).
@@ -591,6 +643,19 @@ extern "C" int hadamard_dequant(const uint8_t *codes, const uint8_t *sf, const f
     const int64_t nsub = rows * (cols / 16);
     if (nsub == 0) return MOE4_OK;
     hadamard_dequant_kernel<<<grid_for(nsub, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, nsub, out_bf16);
+    return launch_status();
+}
+
+extern "C" int moe4_combine_hadamard(const uint8_t *codes, const uint8_t *sf, const float *g_dec,
+                                     const int32_t *row_of, const float *w, int64_t T, int64_t k, int64_t d,
+                                     uint16_t *y, void *stream) {
+    MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 128 == 0);
+    MOE4_CHECK_ARG(T * (d / 16) < (int64_t(1) << 32));
+    MOE4_CHECK_ARG(T == 0 || (codes && sf && g_dec && row_of && w && y && aligned16(codes) && aligned16(y)));
+    const int64_t nsub = T * (d / 16);
+    if (nsub == 0) return MOE4_OK;
+    combine_hadamard_kernel<<<grid_for(nsub, 256, 8), 256, 0, as_stream(stream)>>>(codes, sf, g_dec, row_of, w, T,
+                                                                                    (int)k, d, y);
     return launch_status();
 }
 

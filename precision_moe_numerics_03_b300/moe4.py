@@ -82,6 +82,7 @@ _SIGNATURES = {
     "moe4_swiglu": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "moe4_swiglu_amax": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "moe4_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    "moe4_combine_hadamard": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_dispatch_backward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe4_sgd_update": (_int, [_vp, _vp, _i64, _f32, _vp, _vp]),
     "moe4_convert": (_int, [_int, _vp, _i64, _vp, _vp]),
@@ -315,6 +316,10 @@ def moe4_combine_backward_mxfp8(dy, row_of, w, src_of, T, k, d, rows_total, q_ro
 
 def moe4_combine(yhat, row_of, w, T, k, d, y, stream=None):
     _call("moe4_combine", _p(yhat), _p(row_of), _p(w), T, k, d, _p(y), _s(stream))
+
+
+def moe4_combine_hadamard(codes, sf, g_dec, row_of, w, T, k, d, y, stream=None):
+    _call("moe4_combine_hadamard", _p(codes), _p(sf), _p(g_dec), _p(row_of), _p(w), T, k, d, _p(y), _s(stream))
 
 
 def moe4_dispatch_backward(dxp, row_of, T, k, d, dx, stream=None):

@@ -108,6 +108,8 @@ MISALIGNED = FAKE + 4
     ("moe4_swiglu_amax", (FAKE, 4, 8, FAKE, FAKE + 2, None)),                                # amax alignment
     ("moe4_combine", (FAKE, FAKE, FAKE, 4, 2, 12, FAKE, None)),                              # d % 8
     ("moe4_dispatch_backward", (FAKE, FAKE, 4, 40, 16, FAKE, None)),                         # k > 32
+    ("moe4_combine_hadamard", (FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 64, FAKE, None)),          # d % 128
+    ("moe4_combine_hadamard", (FAKE, FAKE, FAKE, FAKE, FAKE, 4, 33, 128, FAKE, None)),        # k > 32
     ("moe4_dispatch_backward", (FAKE, FAKE, 4, 2, 16, MISALIGNED, None)),                    # dx alignment
     ("moe4_sgd_update", (FAKE, FAKE, 6, 0.1, FAKE, None)),                                   # n % 4
     ("moe4_sf_to_mma_layout", (FAKE, 1, 100, 4, FAKE, None)),                                # rows % 128

@@ -170,3 +170,35 @@ def test_nvfp4_codec_amax_from_gemm_layer_shape():
     rc, rs, rg = oracle.nvfp4_quantize(rot[rows], amax=ref_amax)
     assert float(to_np(g)[0]) == float(rg)
     assert np.array_equal(to_np(c)[rows], rc) and np.array_equal(to_np(s)[rows], rs)
+
+
+def _plan(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    lg = (rng.standard_normal((T, E)) + rng.standard_normal(E)).astype(np.float32)
+    idx, w = oracle.route_topk(lg, k)
+    offs, row_of = oracle.permute_plan(idx, E)
+    return offs, row_of, w
+
+
+@pytest.mark.parametrize("T,E,k,d", [(300, 16, 4, 256), (16384, 384, 8, 4096)])
+def test_combine_from_encoded_return_path(T, E, k, d):
+    """moe4_combine_hadamard (decode + combine in one pass) equals hadamard_dequant followed by
+    moe4_combine byte for byte; the small case also equals the oracle's decode and combine."""
+    offs, row_of, w = _plan(T, E, k, 50 + T)
+    R = int(offs[-1])
+    yb = inputs.device_student_t((R, d), inputs.device_generator(50, T, DEV), DEV).view(torch.int16)
+    c, s = empty_u8(R, d // 2), empty_u8(R, d // 16)
+    g = torch.empty(1, dtype=torch.float32, device=DEV)
+    moe4.hadamard_quant(yb, R, d, c, s, g, moe4.FOUR_OVER_SIX, moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT)))
+    row_d, w_d = to_dev(row_of), to_dev(w)
+    y = torch.empty((T, d), dtype=torch.int16, device=DEV)
+    moe4.moe4_combine_hadamard(c, s, g, row_d, w_d, T, k, d, y)
+    yhat = torch.empty((R, d), dtype=torch.int16, device=DEV)
+    moe4.hadamard_dequant(c, s, g, R, d, yhat)
+    y2 = torch.empty((T, d), dtype=torch.int16, device=DEV)
+    moe4.moe4_combine(yhat, row_d, w_d, T, k, d, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    if T <= 1024:
+        rh = oracle.hadamard_dequant(to_np(c), to_np(s), to_np(g)[0])
+        assert np.array_equal(to_np(y, np.uint16), oracle.combine(rh, row_of, w))
