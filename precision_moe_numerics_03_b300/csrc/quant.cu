@@ -407,15 +407,31 @@ __global__ void __launch_bounds__(256) combine_hadamard_kernel(const uint8_t *__
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            float u[16];
-            float wj = 0.0f;
-            if (live) {
+        // slot j's codes and scale are loaded while slot j-1 is decoded (one slot ahead)
+        auto load_slot = [&](int j, uint2 &cw, uint32_t &sfc, float &wj) {
+            cw = make_uint2(0u, 0u);
+            sfc = 0u;
+            wj = 0.0f;
+            if (live && j < k) {
                 const int64_t row = __ldg(row_of + (int64_t)t * k + j);
                 wj = __ldg(w + (int64_t)t * k + j);
                 const int64_t sub = row * per_row + sb;
-                const uint2 cw = __ldg(reinterpret_cast<const uint2 *>(codes + sub * 8));
-                const float sfv = e4m3_to_f32(__ldg(sf + sub));
+                cw = __ldg(reinterpret_cast<const uint2 *>(codes + sub * 8));
+                sfc = __ldg(sf + sub);
+            }
+        };
+        uint2 cw;
+        uint32_t sfc;
+        float wj;
+        load_slot(0, cw, sfc, wj);
+        for (int j = 0; j < k; ++j) {
+            uint2 ncw;
+            uint32_t nsfc;
+            float nwj;
+            load_slot(j + 1, ncw, nsfc, nwj);
+            float u[16];
+            if (live) {
+                const float sfv = e4m3_to_f32(sfc);
                 float e[16];
                 e2m1x8_to_f32(cw.x, e);
                 e2m1x8_to_f32(cw.y, e + 8);
@@ -431,6 +447,9 @@ __global__ void __launch_bounds__(256) combine_hadamard_kernel(const uint8_t *__
                 const float yh = __uint_as_float((uint32_t)f32_to_bf16_bits(u[i]) << 16);
                 acc[i] = __fadd_rn(acc[i], __fmul_rn(wj, yh));
             }
+            cw = ncw;
+            sfc = nsfc;
+            wj = nwj;
         }
         if (live) store16_bf16(y + (int64_t)t * d + (int64_t)sb * 16, acc);
     }
