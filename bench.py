@@ -721,6 +721,28 @@ def profile_case(name):
             out = torch.empty((rows, d), dtype=torch.int16, device=dev)
             calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws))
             calls.append(lambda: moe4.hadamard_dequant(c, s_, gd, rows, d, out))
+    elif name == "hadamard_given":       # as in the layer step: the rotated amax comes from the down GEMM
+        rows = 32768
+        x = inputs.device_student_t((rows, d), g(3), dev)
+        h = torch.ones((1, 1), device=dev)
+        while h.shape[0] < 128:          # Sylvester's construction, normalised below
+            h = torch.cat([torch.cat([h, h], 1), torch.cat([h, -h], 1)], 0)
+        am = ((x.float().view(-1, 128) @ h) / 128 ** 0.5).abs().max().reshape(1).contiguous()
+        x = x.view(torch.int16)
+        c, s_ = torch.empty((rows, d // 2), **u8), torch.empty((rows, d // 16), **u8)
+        gd = torch.empty(1, dtype=torch.float32, device=dev)
+        calls.append(lambda: moe4.hadamard_quant(x, rows, d, c, s_, gd, moe4.FOUR_OVER_SIX | moe4.AMAX_GIVEN, am))
+    elif name == "combine_hadamard":     # 8192 tokens x top-8 returned rows of d_model 4096, decoded as combined
+        T, k = 8192, 8
+        x = inputs.device_student_t((T * k, d), g(3), dev).view(torch.int16)
+        c, s_ = torch.empty((T * k, d // 2), **u8), torch.empty((T * k, d // 16), **u8)
+        gd = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT), dev)
+        moe4.hadamard_quant(x, T * k, d, c, s_, gd, moe4.FOUR_OVER_SIX, ws)
+        row_of = torch.randperm(T * k, generator=g(4), device=dev).to(torch.int32).view(T, k)
+        w = torch.softmax(torch.randn((T, k), generator=g(5), device=dev), dim=1).contiguous()
+        y = torch.empty((T, d), dtype=torch.int16, device=dev)
+        calls.append(lambda: moe4.moe4_combine_hadamard(c, s_, gd, row_of, w, T, k, d, y))
     elif name in ("swiglu_bwd", "swiglu_bwd_mxfp8"):
         rows = 32768                     # a fifth of the layer's padded rows, SwiGLU width 2048
         gu = torch.randn((rows, 2 * f), generator=g(11), device=dev)
@@ -837,7 +859,8 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["requant", "quant_w", "gemm_nvfp4", "gemm_nvfp4_down_amax", "gemm_mxfp8_wgrad",
                              "gemm_mxfp8_wgrad_sgd",
-                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "gemm_nvfp4_probe", "tensor_peaks",
+                             "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "hadamard_given", "combine_hadamard",
+                             "gemm_nvfp4_probe", "tensor_peaks",
                              "swiglu_bwd", "swiglu_bwd_mxfp8",
                              "gemm_mxfp8_probe"],
                     help="run one kernel a few times on a mid-size case (for ncu captures; prints no bench line)")

@@ -288,3 +288,50 @@ def test_mxfp8_colwise_sr_beyond_2_35_values():
         assert c0 == 0 or (c0 * rows) // 8 >= (1 << 32)  # the last slice: counter word 1 is 1
         assert first_mismatch(to_np(q[c0:c0 + 32]), rq) is None
         assert first_mismatch(to_np(e8[c0:c0 + 32]), re8) is None
+
+
+def test_sr_unbiased_over_seeds_backward_requant_shape():
+    """The backward-requant workload's activations, X [32768, 4096] Student-t(3): NVFP4, then the
+    MXFP8 stochastic-rounding transpose with seeds 0..15 ("4-bit computation from the start of
+    Inkling 2 Small's pretraining", backward-pass paragraphs: the value is kept on average).  Over
+    the 134M outputs, the mean of the 16 decoded draws minus the exact NVFP4 value, in units of
+    each value's predicted standard deviation, aggregates to |z| < 5, both plainly and signed by
+    the value.  The signed statistic sees a pull toward zero: with fractions spread evenly over a
+    gap, a deficit of b gaps per value moves it by about b * 4 * pi * sqrt(n), so 8-bit random
+    numbers (b = 2^-9 on average) would give about -285 here and the 16-bit ones (b = 2^-17)
+    about -1.1.  The codes and scales are the oracle's bit for bit in the other tests; this
+    checks the statistics at full size."""
+    rows, cols = 32768, 4096
+    x = inputs.device_student_t((rows, cols), inputs.device_generator(4, 7, DEV), DEV).view(torch.int16)
+    c, s, g = nvfp4_quantize(x, 1, rows, cols)
+    # the exact binary32 values the requantiser rounds, from the oracle's decode, transposed
+    xh = oracle.nvfp4_dequantize(to_np(c)[0], to_np(s)[0], float(to_np(g)[0])).T
+    xh = torch.from_numpy(np.ascontiguousarray(xh)).to(DEV).double()
+    e4 = torch.from_numpy(oracle.e4m3_value(np.arange(256, dtype=np.uint8) & 0x7F).astype(np.float64)).to(DEV)
+    e4 = torch.where(torch.arange(256, device=DEV) >= 128, -e4, e4)
+    acc = torch.zeros_like(xh)
+    e8_first = None
+    for seed in range(16):
+        q, e8 = _requant_gpu(c, s, g, 1, rows, cols, seed, 0, True)
+        q, e8 = q[0], e8[0]
+        if e8_first is None:
+            e8_first = e8.clone()
+        assert torch.equal(e8, e8_first)  # the scales do not depend on the random numbers
+        scale = torch.exp2(e8.double() - 127).repeat_interleave(32, dim=1)
+        acc += e4[q.long()] * scale
+        del q
+    mean = acc / 16
+    scale = torch.exp2(e8_first.double() - 127).repeat_interleave(32, dim=1)
+    grid = torch.from_numpy(oracle.e4m3_value(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)).to(DEV)
+    v = xh.abs() / scale
+    lo = (torch.searchsorted(grid, v.reshape(-1), right=True) - 1).clamp(0, 125).reshape(v.shape)
+    gap = (grid[lo + 1] - grid[lo]) * scale
+    p = ((xh.abs() - grid[lo] * scale) / gap).clamp(0, 1)
+    sd = gap * torch.sqrt(p * (1 - p) / 16)
+    live = sd > 0
+    z = (mean - xh)[live] / sd[live]
+    n = float(live.sum())
+    z_plain = float(z.sum()) / np.sqrt(n)
+    z_signed = float((z * torch.sign(xh[live])).sum()) / np.sqrt(n)
+    assert n > 1e8
+    assert abs(z_plain) < 5 and abs(z_signed) < 5, (z_plain, z_signed)
