@@ -158,27 +158,29 @@ class LayerStep:
         fwd = 2 * rows * (2 * self.f) * self.d + 2 * rows * self.d * self.f
         return fwd, 2 * fwd
 
-    def run(self, timer=None, io=None):
-        """One layer step; io = (X, logits, dy, y) device tensors to use instead of the step's own."""
+    def run(self, timer=None, io=None, ev=None):
+        """One layer step; io = (X, logits, dy, y) device tensors to use instead of the step's own.
+        ev (end to end): events the step's stream waits on right before the first use of each
+        input ("logits", "X", "dy", all recorded after their host-to-device copies), and one it
+        records as soon as y is complete ("y"), so that the copies overlap the step's own work."""
         m, torch = self.m, self.torch
         T, d, f, E, k = self.T, self.d, self.f, self.E, self.k
         FOS, MMA, OMMA = m.FOUR_OVER_SIX, m.SF_MMA_LAYOUT, m.SF_OUT_MMA
         tm = timer if timer is not None else _NullTimer()
         X, logits, dy, y = io if io is not None else (self.X, self.logits, self.dy, self.y)
+        cur = torch.cuda.current_stream()
+        wait = (lambda name: cur.wait_event(ev[name])) if ev is not None else (lambda name: None)
         n = 0
         seed = 1000 + self.step_index
         self.step_index += 1
         # ---------------- forward
+        wait("logits")
         with tm("route"):
             m.moe4_route_topk(logits, T, E, k, self.idx, self.w)
             m.moe4_permute_plan(self.idx, T, k, E, self.offs, self.row_of, self.src_of, self.rows_cap, self.plan_ws)
         n += 4
         Rp = int(self.offs[E].item())          # host needs the padded row count (one 4-byte read)
         self.Rp = Rp
-        with tm("quant_x"):
-            m.nvfp4_quantize(X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
-            m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
-        n += 3
         with tm("quant_w"):
             # the FP32 master weights, rounded to bf16 as they are read (no stored bf16 copy), to
             # NVFP4 for the forward and, in the same pass, requantised to the MXFP8 transposes the
@@ -189,6 +191,11 @@ class LayerStep:
             m.nvfp4_quantize_f32_requant(self.W32_d, E, d, f, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g,
                                          self.WdT_q, self.WdT_e, seed, 1, self.offs, WF)
         n += 4  # each call: the quantiser, then the requantiser
+        wait("X")  # the weight path needs none of the step's inputs: X's copy can run beside it
+        with tm("quant_x"):
+            m.nvfp4_quantize(X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
+            m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
+        n += 3
         with tm("gemm_nvfp4"):
             m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
                                         E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
@@ -209,6 +216,9 @@ class LayerStep:
         with tm("combine"):  # decode of the returned rows (rotation back, bf16) and the weighted combine
             m.moe4_combine_hadamard(self.Yc_c, self.Yc_s, self.Yc_g, self.row_of, self.w, T, k, d, y)
         n += 1
+        if ev is not None:
+            ev["y"].record(cur)
+        wait("dy")
         # ---------------- backward
         with tm("mxfp8_quant"):  # combine gradient straight into both MXFP8 layouts of dY
             m.moe4_combine_backward_mxfp8(dy, self.row_of, self.w, self.src_of, T, k, d, Rp, self.dYr_q, self.dYr_e,
@@ -998,8 +1008,11 @@ def main():
     if not args.no_e2e:
         # Each step's inputs (X, logits, dy) come from pinned host memory and its output y goes back
         # to pinned host memory, inside the timed region.  As in a training loop, step i+1's inputs
-        # are copied on a side stream while step i computes (two device input sets), and step i's
-        # y is copied back after it (two device y buffers); the region ends when every copy is done.
+        # are copied on a side stream while step i computes (two device input sets, logits first,
+        # each input with its own event, so that a step waits for an input only where it first
+        # reads it: the weight path runs while X and dy arrive), and step i's y is copied back as
+        # soon as the combine has written it, beside the backward (two device y buffers; step i+2
+        # writes its y only once that copy is done).  The region ends when every copy is done.
         hX = torch.empty(step.X.shape, dtype=step.X.dtype, pin_memory=True)
         hX.copy_(step.X)
         hL = torch.empty(step.logits.shape, dtype=step.logits.dtype, pin_memory=True)
@@ -1011,15 +1024,15 @@ def main():
               (torch.empty_like(step.X), torch.empty_like(step.logits), torch.empty_like(step.dy),
                torch.empty_like(step.y))]
         cs = torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev = [{name: torch.cuda.Event() for name in ("logits", "X", "dy", "y")} for _ in range(2)]
         ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
         def copy_in(b):
             with torch.cuda.stream(cs):
-                io[b][0].copy_(hX, non_blocking=True)
-                io[b][1].copy_(hL, non_blocking=True)
-                io[b][2].copy_(hD, non_blocking=True)
-                ev_in[b].record(cs)
+                for name, dst, src in (("logits", io[b][1], hL), ("X", io[b][0], hX), ("dy", io[b][2], hD)):
+                    dst.copy_(src, non_blocking=True)
+                    ev[b][name].record(cs)
 
         torch.cuda.synchronize()
         if dist is not None:
@@ -1032,12 +1045,14 @@ def main():
                 if i >= 1:
                     cs.wait_event(ev_done[1 - b])  # step i-1 is done with that input set
                 copy_in(1 - b)
-            torch.cuda.current_stream().wait_event(ev_in[b])
-            step.run(io=io[b])
+            if i >= 2:
+                torch.cuda.current_stream().wait_event(ev_out[b])  # step i-2's y has been read back
+            step.run(io=io[b], ev=ev[b])
             ev_done[b].record()
-            cs.wait_event(ev_done[b])
+            cs.wait_event(ev[b]["y"])
             with torch.cuda.stream(cs):
                 hY[b].copy_(io[b][3], non_blocking=True)
+                ev_out[b].record(cs)
         torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
         e2e_s = max_over_ranks(e2e_s, dist)
