@@ -54,6 +54,7 @@ WORKLOAD = "inkling-moe-layer-step: T=16384 d=4096 f=2048 E=384 top8, NVFP4 fwd 
 SMALL = dict(T=4096, d=2048, f=1024, E=8, k=2)
 METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
+WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
 TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.9 / 2216.7}  # profiles/gemm_mxfp8_wgrad_sgd_16experts.md
@@ -110,6 +111,10 @@ class LayerStep:
         self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
         self.offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
         self.row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+        # the weight path's side stream (higher priority: its quantiser's CTAs are placed first)
+        self.side = torch.cuda.Stream(device=dev, priority=-1)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_q = [torch.cuda.Event() for _ in range(2 * WEIGHT_CHUNKS)]
         self.src_of = torch.empty(R, dtype=torch.int32, device=dev)
         self.plan_ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E), dev)
         self.qws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, E), dev)
@@ -183,14 +188,12 @@ class LayerStep:
         self.Rp = Rp
         with tm("quant_w"):
             # the FP32 master weights, rounded to bf16 as they are read (no stored bf16 copy), to
-            # NVFP4 for the forward and, in the same pass, requantised to the MXFP8 transposes the
-            # backward's dgrad reads; experts that received no rows are skipped
-            WF = FOS | m.SR | MMA | OMMA
-            m.nvfp4_quantize_f32_requant(self.W32_gu, E, 2 * f, d, self.amax_gu, self.Wgu_c, self.Wgu_s, self.Wgu_g,
-                                         self.WguT_q, self.WguT_e, seed, 3, self.offs, WF)
-            m.nvfp4_quantize_f32_requant(self.W32_d, E, d, f, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g,
-                                         self.WdT_q, self.WdT_e, seed, 1, self.offs, WF)
-        n += 4  # each call: the quantiser, then the requantiser
+            # NVFP4 for the forward, then requantised to the MXFP8 transposes the backward's dgrad
+            # reads; experts that received no rows are skipped.  Software-pipelined over expert
+            # chunks: chunk i+1's quantiser (HBM-bound) runs on a side stream on part of each SM
+            # while chunk i's requantiser (issue-bound) takes the rest.
+            self.weight_path(seed, cur)
+        n += 4 * WEIGHT_CHUNKS  # each chunk: the quantiser, then the requantiser
         wait("X")  # the weight path needs none of the step's inputs: X's copy can run beside it
         with tm("quant_x"):
             m.nvfp4_quantize(X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
@@ -259,6 +262,34 @@ class LayerStep:
         n += 1
         self.launches += n
         return n
+
+    def weight_path(self, seed, cur):
+        """Both projections' weight paths, WEIGHT_CHUNKS expert chunks each: the first chunk's
+        quantiser on the whole GPU, then every chunk's requantiser on the step's stream beside the
+        next chunk's quantiser (MOE4_SHARE_SMS) on the side stream."""
+        m, E, d, f = self.m, self.E, self.d, self.f
+        WF = m.FOUR_OVER_SIX | m.SR | m.SF_MMA_LAYOUT | m.SF_OUT_MMA
+        bounds = [E * i // WEIGHT_CHUNKS for i in range(WEIGHT_CHUNKS + 1)]
+        chunks = []
+        for W, am, c, sf, g, qt, et, rows, cols, sid in (
+                (self.W32_gu, self.amax_gu, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.WguT_q, self.WguT_e, 2 * f, d, 3),
+                (self.W32_d, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g, self.WdT_q, self.WdT_e, d, f, 1)):
+            for e0, e1 in zip(bounds[:-1], bounds[1:]):
+                # mat_base = the chunk's first expert: its random numbers are those of one call over
+                # the projection's whole stack
+                chunks.append(((W[e0:e1], e1 - e0, rows, cols, am[e0:e1], c[e0:e1], sf[e0:e1], g[e0:e1], qt[e0:e1],
+                                et[e0:e1], seed, sid, self.offs[e0:e1 + 1]), e0))
+        m.nvfp4_quantize_f32_requant(*chunks[0][0], WF | m.PASS_QUANT, mat_base=chunks[0][1])
+        self.ev_fork.record(cur)
+        self.side.wait_event(self.ev_fork)
+        for i, (args, e0) in enumerate(chunks):
+            if i + 1 < len(chunks):
+                m.nvfp4_quantize_f32_requant(*chunks[i + 1][0], WF | m.PASS_QUANT | m.SHARE_SMS, self.side,
+                                             mat_base=chunks[i + 1][1])
+                self.ev_q[i + 1].record(self.side)
+            if i > 0:
+                cur.wait_event(self.ev_q[i])
+            m.nvfp4_quantize_f32_requant(*args, WF | m.PASS_REQUANT, mat_base=e0)
 
     # algorithmic HBM bytes of the kernel groups (per step), for the roofline
     def group_bytes(self):

@@ -76,6 +76,9 @@ extern "C" {
 #define MOE4_SF_MMA_LAYOUT  0x10000u /* scale factors are in the tensor-core tile layout */
 #define MOE4_MXFP8          0x20000u /* Hadamard codec: the 8.25-bit MXFP8 variant */
 #define MOE4_SF_OUT_MMA     0x40000u /* MXFP8 producers: output scales in the tensor-core tile layout */
+#define MOE4_PASS_QUANT     0x100000u /* weight path: run only its first pass (the NVFP4 quantiser) */
+#define MOE4_PASS_REQUANT   0x200000u /* weight path: run only its second pass (the requantiser) */
+#define MOE4_SHARE_SMS      0x400000u /* weight path: the quantiser keeps to part of each SM */
 
 /* ------------------------------------------------------------------ library */
 int moe4_version(void);                      /* e.g. 100 for 0.1.0 */
@@ -207,11 +210,23 @@ int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const fl
  * NULL; a matrix m with group_offs[m + 1] == group_offs[m] (an expert that received no rows) is
  * skipped and its outputs are left as they are.  rows % 32 == 0 (% 128 with either tile-layout
  * flag), cols % 64 == 0 (% 128 with MOE4_SF_OUT_MMA); x, codes and q_t 16-byte aligned; nmat, and
- * cols / 64, at most 65535. */
+ * cols / 64, at most 65535.
+ * Split passes: MOE4_PASS_QUANT runs only the quantiser (q_t and e8_t are not touched),
+ * MOE4_PASS_REQUANT only the requantiser, which reads the codes, sf and g_dec a MOE4_PASS_QUANT
+ * call with the same arguments wrote (at most one of the two; neither = both passes in order).
+ * mat_base (0 <= mat_base <= 2^40): the call's matrices are matrices mat_base .. mat_base + nmat - 1
+ * of a larger stack, whose other arguments the caller has offset to that slice (x, amax_in, codes,
+ * sf, g_dec, q_t, e8_t, group_offs); the stochastic rounding's random index of an element is its
+ * index in the whole stack's q_t, so calls over slices write the bytes of one call over the stack.
+ * 0 for a call over a whole stack.
+ * MOE4_SHARE_SMS runs the quantiser on a small grid that holds part of each SM only, so that a
+ * requantiser launched beside it on another stream (another matrix set's MOE4_PASS_REQUANT) runs
+ * on the rest of every SM at the same time: the quantiser's memory waits and the requantiser's
+ * arithmetic then overlap.  The outputs do not depend on these flags. */
 int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t rows, int64_t cols,
                                const float *amax_in, uint8_t *codes, uint8_t *sf, float *g_dec,
                                uint8_t *q_t, uint8_t *e8_t, uint64_t seed, uint32_t stream_id,
-                               const int32_t *group_offs, uint32_t flags, void *stream);
+                               int64_t mat_base, const int32_t *group_offs, uint32_t flags, void *stream);
 
 /* mxfp8_quantize: bf16 x [rows, cols] to MXFP8 with the same scale and rounding rules.
  * MOE4_ROWWISE: q [rows, cols], e8 [rows, cols/32] (cols % 32 == 0); random index = the

@@ -538,9 +538,9 @@ static int grid_for(int64_t work_items, int threads, int per_sm) {
 
 int quantize_f32_given(const float *x, int64_t nmat, int64_t rows, int64_t cols, const float *amax_in,
                        uint8_t *codes, uint8_t *sf, float *g_dec, const int32_t *skip_offs, bool four_over_six,
-                       bool sf_mma, cudaStream_t st) {
+                       bool sf_mma, cudaStream_t st, int ctas_per_sm) {
     const int64_t total = nmat * rows * (cols / 16);
-    const int grid = grid_for(total > nmat ? total : nmat, 256, 8);
+    const int grid = grid_for(total > nmat ? total : nmat, 256, ctas_per_sm);
     uint32_t div_m = 0, div_s = 0;
     if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
     nvfp4_quant_kernel<float><<<grid, 256, 0, st>>>(x, nmat, rows, cols, cols, rows * cols, amax_in, nullptr,

@@ -37,7 +37,7 @@ enum class SrcKind { Nvfp4, Bf16, SwigluBwd, CombineBwd };
 template <SrcKind kind, bool kSR, bool kJ32>
 __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int64_t m, int64_t cA, int64_t r0,
                                           int64_t R, int64_t C, uint8_t *__restrict__ q_t, uint8_t (*e8s)[4], int cl,
-                                          const PhiloxKeys keys, uint32_t stream_id, bool safe) {
+                                          const PhiloxKeys keys, uint32_t stream_id, bool safe, int64_t mr) {
     constexpr bool kF16 = kind == SrcKind::Nvfp4;
     const int lane = lane_id();
     uint32_t mx = max_abs16x2<kF16>(max_abs16x2<kF16>(p.x, p.y), max_abs16x2<kF16>(p.z, p.w));
@@ -77,9 +77,11 @@ __device__ __forceinline__ void emit_pair(const uint4 p, float g, bool live, int
         // the 16-bit numbers of this lane's values: indices idx .. idx+3 (row A) and idx+R ..
         // idx+R+3 (row B), with idx % 8 = 4 * (lane & 1) (R and r0 are multiples of 32); lanes 2m
         // and 2m+1 share one Philox call per row, so the even lane runs row A's call, the odd lane
-        // row B's, and each hands its partner the two words of the partner's half
+        // row B's, and each hands its partner the two words of the partner's half.  The random
+        // index counts matrices from mr's origin (mr = m plus the call's matrix base), so a call
+        // over a slice of a weight stack draws the numbers of the whole stack's call.
         const bool odd = (lane & 1) != 0;
-        const int64_t i8 = rowA * R + r0 + 8 * (lane >> 1) + (odd ? R : 0);
+        const int64_t i8 = (mr * C + cA) * R + r0 + 8 * (lane >> 1) + (odd ? R : 0);
         Philox4 P;
         if constexpr (kJ32)
             P = sr_words8_not32((uint32_t)((uint64_t)i8 >> 3), stream_id, keys);
@@ -156,7 +158,7 @@ requant_transpose_kernel(
     uint8_t *__restrict__ q_r = nullptr, uint8_t *__restrict__ e8_r = nullptr, const float *__restrict__ gu = nullptr,
     const float *__restrict__ dh = nullptr, const int32_t *__restrict__ src_of = nullptr,
     const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0,
-    bool e8_mma = false, const int32_t *__restrict__ skip_offs = nullptr) {
+    bool e8_mma = false, const int32_t *__restrict__ skip_offs = nullptr, int64_t m_base = 0) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
     // expert weights: a matrix whose group has no rows (skip_offs[m + 1] == skip_offs[m]) is
     // skipped whole, its outputs left as they are
@@ -347,7 +349,8 @@ requant_transpose_kernel(
         const int cp = warp_id() + 8 * i;
         const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cp][4 * lane_id()]);
         const int64_t cA = out_col(2 * cp);
-        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8s, 2 * cp, keys, stream_id, safe);
+        emit_pair<kind, kSR, kJ32>(p, g, cA < C, m, cA, r0, R, C, q_t, e8s, 2 * cp, keys, stream_id, safe,
+                                   m + m_base);
     }
     // scale codes: one thread per output row, its (up to) four blocks of this tile; the four are
     // adjacent bytes in both layouts (a whole word when R % 128 == 0)
@@ -451,14 +454,21 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     return launch_status();
 }
 
+// MOE4_SHARE_SMS: quantiser CTAs per SM (62 registers x 256 threads each), leaving the rest of the
+// register file to requantiser CTAs (48 x 256) launched beside it
+constexpr int kShareCtasPerSm = 2;
+
 extern "C" int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t rows, int64_t cols,
                                           const float *amax_in, uint8_t *codes, uint8_t *sf, float *g_dec,
                                           uint8_t *q_t, uint8_t *e8_t, uint64_t seed, uint32_t stream_id,
-                                          const int32_t *group_offs, uint32_t flags, void *stream) {
+                                          int64_t mat_base, const int32_t *group_offs, uint32_t flags, void *stream) {
     MOE4_CHECK_ARG(nmat >= 1 && rows >= 0 && rows % 32 == 0 && cols > 0 && cols % 64 == 0);
+    MOE4_CHECK_ARG(mat_base >= 0 && mat_base <= (int64_t(1) << 40));
     MOE4_CHECK_ARG(x && amax_in && codes && sf && g_dec && q_t && e8_t);
     MOE4_CHECK_ARG(aligned16(x) && aligned16(codes) && aligned16(q_t) && (reinterpret_cast<uintptr_t>(sf) & 1u) == 0);
-    MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_SR | MOE4_SF_MMA_LAYOUT | MOE4_SF_OUT_MMA)) == 0);
+    MOE4_CHECK_ARG((flags & ~(MOE4_FOUR_OVER_SIX | MOE4_SR | MOE4_SF_MMA_LAYOUT | MOE4_SF_OUT_MMA | MOE4_PASS_QUANT |
+                              MOE4_PASS_REQUANT | MOE4_SHARE_SMS)) == 0);
+    MOE4_CHECK_ARG((flags & (MOE4_PASS_QUANT | MOE4_PASS_REQUANT)) != (MOE4_PASS_QUANT | MOE4_PASS_REQUANT));
     const bool sf_mma = (flags & MOE4_SF_MMA_LAYOUT) != 0;
     const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
     MOE4_CHECK_ARG(!sf_mma || rows % 128 == 0);
@@ -471,14 +481,18 @@ extern "C" int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t 
     // two passes over the experts that have rows: the HBM-bound quantiser of the binary32
     // masters, then the issue-bound requantiser of its codes (one fused pass measured slower:
     // its block quantiser and the requantiser share a CTA's issue slots and its barrier)
-    int rc = quantize_f32_given(x, nmat, rows, cols, amax_in, codes, sf, g_dec, group_offs,
-                                (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, st);
-    if (rc != MOE4_OK) return rc;
-    const bool j32 = (uint64_t)nmat * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 35);
+    if ((flags & MOE4_PASS_REQUANT) == 0) {
+        const int rc = quantize_f32_given(x, nmat, rows, cols, amax_in, codes, sf, g_dec, group_offs,
+                                          (flags & MOE4_FOUR_OVER_SIX) != 0, sf_mma, st,
+                                          (flags & MOE4_SHARE_SMS) ? kShareCtasPerSm : 8);
+        if (rc != MOE4_OK) return rc;
+        if (flags & MOE4_PASS_QUANT) return MOE4_OK;
+    }
+    const bool j32 = (uint64_t)(mat_base + nmat) * (uint64_t)rows * (uint64_t)cols <= (uint64_t(1) << 35);
     const PhiloxKeys keys = philox_keys(seed);
 #define MOE4_WEIGHT_ARGS                                                                                          \
     codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, sf_mma, nullptr, nullptr, nullptr, \
-        nullptr, nullptr, nullptr, nullptr, 0, e8_mma, group_offs
+        nullptr, nullptr, nullptr, nullptr, 0, e8_mma, group_offs, mat_base
     if ((flags & MOE4_SR) && j32)
         requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
     else if (flags & MOE4_SR)

@@ -28,6 +28,9 @@ ACCUMULATE = 0x04000
 SF_MMA_LAYOUT = 0x10000
 MXFP8 = 0x20000
 SF_OUT_MMA = 0x40000
+PASS_QUANT = 0x100000
+PASS_REQUANT = 0x200000
+SHARE_SMS = 0x400000
 
 OP_NVFP4_QUANTIZE = 1
 OP_HADAMARD_QUANT = 2
@@ -55,8 +58,8 @@ _SIGNATURES = {
     "nvfp4_quantize_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _u32, _vp]),
     "mxfp8_requant_transpose_sr": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
-    "nvfp4_quantize_f32_requant": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _vp,
-                                          _u32, _vp]),
+    "nvfp4_quantize_f32_requant": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _i64,
+                                          _vp, _u32, _vp]),
     "mxfp8_quantize": (_int, [_vp, _i64, _i64, _vp, _vp, _u64, _u32, _u32, _vp]),
     "mxfp8_quantize_rowcol": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "hadamard_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
@@ -212,9 +215,9 @@ def mxfp8_requant_transpose_sr(codes, sf, g_dec, nmat, rows, cols, q_t, e8_t, se
 
 
 def nvfp4_quantize_f32_requant(x, nmat, rows, cols, amax_in, codes, sf, g_dec, q_t, e8_t, seed=0, stream_id=0,
-                               group_offs=None, flags=FOUR_OVER_SIX | SR, stream=None):
+                               group_offs=None, flags=FOUR_OVER_SIX | SR, stream=None, mat_base=0):
     _call("nvfp4_quantize_f32_requant", _p(x), nmat, rows, cols, _p(amax_in), _p(codes), _p(sf), _p(g_dec), _p(q_t),
-          _p(e8_t), seed, stream_id, _p(group_offs), flags, _s(stream))
+          _p(e8_t), seed, stream_id, mat_base, _p(group_offs), flags, _s(stream))
 
 
 def mxfp8_quantize(x, rows, cols, q, e8, seed=0, stream_id=0, flags=ROWWISE, stream=None):

@@ -124,15 +124,19 @@ MISALIGNED = FAKE + 4
                                      None)),                                                  # d % 128
     ("mxfp8_quantize", (FAKE, 128, 128, FAKE, FAKE, 0, 0, 0x10 | 0x40000, None)),             # not offered
     # the fused weight path: cols % 64, rows % 32, no amax, tile layouts on 128-row tiles
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 96, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 48, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 5, None)),
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 96, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x10005,
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 96, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 48, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 5, None)),
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 96, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 0x10005,
                                     None)),
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x40005,
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 0x40005,
                                     None)),
-    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, None, 0x100,
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None, 0x100,
                                     None)),                                                   # bad flag
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, None,
+                                    0x300005, None)),                                         # both passes alone
+    ("nvfp4_quantize_f32_requant", (FAKE, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, -1, None, 5,
+                                    None)),                                                   # mat_base < 0
 ])
 def test_argument_checks_fail_on_host(lib, case):
     name, args = case

@@ -102,3 +102,67 @@ def test_fused_weight_path_layer_shape():
     want = _two_calls(w32, E, rows, cols, amax, 1003, 3, flags)
     for a, b in zip(got, want):
         assert torch.equal(a, b)
+
+
+def test_weight_path_chunked_on_two_streams_equals_one_call():
+    """The layer step's schedule: the stack cut into expert chunks, chunk i+1's quantiser
+    (MOE4_PASS_QUANT | MOE4_SHARE_SMS) on a side stream beside chunk i's requantiser
+    (MOE4_PASS_REQUANT), each call on slices with its mat_base: every output byte equals one call
+    over the whole stack, skipped experts included."""
+    nmat, rows, cols = 10, 256, 512
+    w32 = inputs.device_normal((nmat, rows, cols), 0.02, inputs.device_generator(31, 3, DEV), DEV,
+                               dtype=torch.float32)
+    amax = _amax_of_bf16(w32)
+    offs = to_dev(np.array([0, 128, 128, 384, 512, 512, 640, 768, 768, 896, 1024], np.int32))
+    flags = moe4.FOUR_OVER_SIX | moe4.SR | moe4.SF_MMA_LAYOUT | moe4.SF_OUT_MMA
+    want = _fused(w32, nmat, rows, cols, amax, 9, 3, flags, offs=offs, fill=0x5A)
+    out = [empty_u8(nmat, rows, cols // 2), empty_u8(nmat, rows * cols // 16),
+           torch.empty(nmat, dtype=torch.float32, device=DEV), empty_u8(nmat, cols, rows),
+           empty_u8(nmat, cols * rows // 32)]
+    for t in out:
+        t.view(torch.uint8).fill_(0x5A)
+    bounds = [0, 3, 4, 7, 10]
+    args = [(w32[a:b], b - a, rows, cols, amax[a:b], out[0][a:b], out[1][a:b], out[2][a:b], out[3][a:b],
+             out[4][a:b], 9, 3, offs[a:b + 1]) for a, b in zip(bounds[:-1], bounds[1:])]
+    side = torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    ev = [torch.cuda.Event() for _ in args]
+    moe4.nvfp4_quantize_f32_requant(*args[0], flags | moe4.PASS_QUANT, mat_base=bounds[0])
+    ev[0].record(cur)
+    side.wait_event(ev[0])
+    for i, a in enumerate(args):
+        if i + 1 < len(args):
+            moe4.nvfp4_quantize_f32_requant(*args[i + 1], flags | moe4.PASS_QUANT | moe4.SHARE_SMS, side,
+                                            mat_base=bounds[i + 1])
+            ev[i + 1].record(side)
+        if i > 0:
+            cur.wait_event(ev[i])
+        moe4.nvfp4_quantize_f32_requant(*a, flags | moe4.PASS_REQUANT, mat_base=bounds[i])
+    torch.cuda.synchronize()
+    for a, b in zip(out, want):
+        assert torch.equal(a.view(torch.uint8).reshape(-1), b.view(torch.uint8).reshape(-1))
+
+
+def test_weight_path_slice_far_into_a_stack_against_oracle():
+    """One matrix called as matrix 2^21 + 3 of a stack of [128, 256] matrices: its random indices
+    start past 2^35 (the kernel's 64-bit index path) and equal the oracle's dequantise -> transpose
+    -> MXFP8 rows with that index base."""
+    rows, cols = 128, 256
+    mat_base = (1 << 21) + 3
+    rng = np.random.default_rng(32)
+    w = (rng.standard_normal((1, rows, cols)) * 0.02).astype(np.float32)
+    w32 = to_dev(w)
+    amax = _amax_of_bf16(w32)
+    flags = moe4.FOUR_OVER_SIX | moe4.SR
+    codes, sf, g, q, e8 = [empty_u8(1, rows, cols // 2), empty_u8(1, rows * cols // 16),
+                           torch.empty(1, dtype=torch.float32, device=DEV), empty_u8(1, cols, rows),
+                           empty_u8(1, cols * rows // 32)]
+    moe4.nvfp4_quantize_f32_requant(w32, 1, rows, cols, amax, codes, sf, g, q, e8, 21, 5, None, flags,
+                                    mat_base=mat_base)
+    torch.cuda.synchronize()
+    wb = oracle.bf16_to_f32(oracle.f32_to_bf16(w))
+    rc, rs, rg = oracle.nvfp4_quantize(wb, amax=to_np(amax))
+    xt = np.ascontiguousarray(oracle.nvfp4_dequantize(rc, rs, rg)[0].T)
+    rq, re8 = oracle.mxfp8_quantize_rows(xt, sr=True, seed=21, stream_id=5, idx_base=mat_base * cols * rows)
+    assert first_mismatch(to_np(q).reshape(rq.shape), rq) is None
+    assert first_mismatch(to_np(e8).reshape(re8.shape), re8) is None
