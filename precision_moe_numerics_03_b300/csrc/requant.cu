@@ -149,8 +149,11 @@ __device__ __forceinline__ void emit_rowwise32(const uint32_t h[16], int64_t r, 
 // lane (512 contiguous bytes per warp): both conflict-free.
 constexpr int kPairs = kTileC / 2;
 
-template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true>
-__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd) ? 4 : 5)
+// TC: tile columns, 64, or 128 for the bf16 and combine-gradient sources (each thread then
+// holds two 32-column groups of its row, all eight 16-byte loads issued before any is used:
+// twice the bytes in flight of the 64-column tile, for kernels that wait on their loads).
+template <SrcKind kind, bool kSR, bool kRow = false, bool kJ32 = true, int TC = kTileC>
+__global__ void __launch_bounds__(256, (kSR || kind == SrcKind::SwigluBwd || TC == 128) ? 4 : 5)
 requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf, const float *__restrict__ g_dec,
     const uint16_t *__restrict__ xbf, int64_t nmat, int64_t R, int64_t C, uint8_t *__restrict__ q_t,
@@ -160,15 +163,17 @@ requant_transpose_kernel(
     const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0,
     bool e8_mma = false, const int32_t *__restrict__ skip_offs = nullptr, int64_t m_base = 0) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
+    static_assert(TC == 64 || (TC == 128 && (kind == SrcKind::Bf16 || kind == SrcKind::CombineBwd)),
+                  "128-column tiles: bf16 and combine-gradient sources only");
     // expert weights: a matrix whose group has no rows (skip_offs[m + 1] == skip_offs[m]) is
     // skipped whole, its outputs left as they are
     if (skip_offs != nullptr && __ldg(skip_offs + blockIdx.z + 1) == __ldg(skip_offs + blockIdx.z)) return;
-    __shared__ __align__(16) uint32_t tile[kPairs][kTileR];
-    __shared__ __align__(4) uint8_t e8s[kTileC][4];
+    __shared__ __align__(16) uint32_t tile[TC / 2][kTileR];
+    __shared__ __align__(4) uint8_t e8s[TC][4];
     const int64_t f = C / 2;  // SwigluBwd: C = 2f
     // grid (row tiles, column tiles, matrices): no index division
     const int64_t m = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.x * kTileR, c0 = (int64_t)blockIdx.y * (kSwb ? 32 : kTileC);
+    const int64_t r0 = (int64_t)blockIdx.x * kTileR, c0 = (int64_t)blockIdx.y * (kSwb ? 32 : TC);
     // input column (output row) of tile column cl
     auto out_col = [&](int cl) -> int64_t { return kSwb ? (cl < 32 ? c0 + cl : f + c0 + (cl - 32)) : c0 + cl; };
 
@@ -178,7 +183,75 @@ requant_transpose_kernel(
     __shared__ uint32_t sf_red[2][8];
     uint32_t sf_lo = 0x7C00u, sf_hi = 0u;
     // phase 1: load, (NVFP4: e2m1 * e4m3 in f16), store transposed
-    {
+    if constexpr (TC == 128) {
+        // thread (row rl, half): tile columns 32 * half + 64 * g, g = 0, 1 -> pair-rows
+        // 16 * half + 32 * g + i; the values are those of the 64-column path below
+        const int rl = threadIdx.x & (kTileR - 1);
+        const int half = threadIdx.x >> 7;
+        const int64_t r = r0 + rl;
+        int32_t tok = 0;
+        float wj = 0.0f;
+        if constexpr (kind == SrcKind::CombineBwd) {
+            if (r < R) {
+                tok = __ldg(src_of + r);
+                if (tok >= 0) {
+                    const int64_t base = (int64_t)tok * topk;
+                    const bool vec = (topk & 3) == 0 &&
+                                     ((reinterpret_cast<uintptr_t>(row_of) | reinterpret_cast<uintptr_t>(wts)) & 15u) == 0;
+                    if (vec) {
+                        for (int j = 0; j < topk; j += 4) {
+                            const int4 ro = __ldg(reinterpret_cast<const int4 *>(row_of + base + j));
+                            const float4 wv = __ldg(reinterpret_cast<const float4 *>(wts + base + j));
+                            wj = ro.x == (int32_t)r ? wv.x : wj;
+                            wj = ro.y == (int32_t)r ? wv.y : wj;
+                            wj = ro.z == (int32_t)r ? wv.z : wj;
+                            wj = ro.w == (int32_t)r ? wv.w : wj;
+                        }
+                    } else {
+                        for (int j = 0; j < topk; ++j)
+                            if (__ldg(row_of + base + j) == (int32_t)r) wj = __ldg(wts + base + j);
+                    }
+                }
+            }
+        }
+        uint4 v[2][4];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int64_t c = c0 + 32 * half + 64 * g;
+            const bool ld = r < R && c < C && (kind != SrcKind::CombineBwd || tok >= 0);
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                kind == SrcKind::CombineBwd ? xbf + (int64_t)(tok < 0 ? 0 : tok) * C + c : xbf + (m * R + r) * C + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[g][q] = ld ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int64_t c = c0 + 32 * half + 64 * g;
+            uint32_t h[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t ws[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (kind == SrcKind::CombineBwd)
+                        h[4 * q + i] = (uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_lo(ws[i]))) |
+                                       ((uint32_t)f32_to_bf16_bits(__fmul_rn(wj, bf16_hi(ws[i]))) << 16);
+                    else
+                        h[4 * q + i] = ws[i];
+                }
+            }
+            const bool in = r < R && c < C;
+            if (!in) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[i] = 0u;
+            }
+            if constexpr (kRow) {
+                if (in) emit_rowwise32(h, r, c, C, q_r, e8_r, e8_mma);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tile[16 * half + 32 * g + i][rl] = h[i];
+        }
+    } else {
         const int rl = threadIdx.x & (kTileR - 1);
         const int half = threadIdx.x >> 7;
         const int64_t r = r0 + rl;
@@ -345,7 +418,7 @@ requant_transpose_kernel(
     // phase 2: each warp emits one pair-row (two output rows) per iteration
     const float g = (kind == SrcKind::Nvfp4) ? __ldg(g_dec + m) : 1.0f;
 #pragma unroll 1
-    for (int i = 0; i < kPairs / 8; ++i) {
+    for (int i = 0; i < TC / 16; ++i) {
         const int cp = warp_id() + 8 * i;
         const uint4 p = *reinterpret_cast<const uint4 *>(&tile[cp][4 * lane_id()]);
         const int64_t cA = out_col(2 * cp);
@@ -355,7 +428,7 @@ requant_transpose_kernel(
     // scale codes: one thread per output row, its (up to) four blocks of this tile; the four are
     // adjacent bytes in both layouts (a whole word when R % 128 == 0)
     __syncthreads();
-    if (threadIdx.x < kTileC) {
+    if (threadIdx.x < TC) {
         const int cl = threadIdx.x;
         const int64_t c = out_col(cl);
         if (c < C) {
@@ -411,6 +484,10 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const uint16_t *__re
 
 // Grid of the transposing kernel: x row tiles, y column tiles, z matrices (rejected beyond the
 // launch limits: 2^31 - 1 and 65535).
+// tile columns of the two-layout quantisers of bf16 sources (mxfp8_quantize_rowcol and the combine
+// gradient): the wide tile, whose threads keep twice the loads in flight
+constexpr int kWideTile = 128;
+
 static bool requant_grid(int64_t rows, int64_t col_tiles, int64_t nmat, dim3 &grid) {
     const int64_t rt = (rows + kTileR - 1) / kTileR;
     if (rt >= (int64_t(1) << 31) || col_tiles > 65535 || nmat > 65535) return false;
@@ -547,9 +624,9 @@ extern "C" int mxfp8_quantize_rowcol(const uint16_t *x, int64_t rows, int64_t co
     const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
     MOE4_CHECK_ARG(!e8_mma || (rows % 128 == 0 && cols % 128 == 0));
     dim3 grid;
-    MOE4_CHECK_ARG(requant_grid(rows, (cols + kTileC - 1) / kTileC, 1, grid));
+    MOE4_CHECK_ARG(requant_grid(rows, (cols + kWideTile - 1) / kWideTile, 1, grid));
     if (rows == 0) return MOE4_OK;
-    requant_transpose_kernel<SrcKind::Bf16, false, true><<<grid, 256, 0, as_stream(stream)>>>(
+    requant_transpose_kernel<SrcKind::Bf16, false, true, true, kWideTile><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, x, 1, rows, cols, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row, nullptr,
         nullptr, nullptr, nullptr, nullptr, 0, e8_mma);
     return launch_status();
@@ -583,9 +660,9 @@ extern "C" int moe4_combine_backward_mxfp8(const uint16_t *dy, const int32_t *ro
     const bool e8_mma = (flags & MOE4_SF_OUT_MMA) != 0;
     MOE4_CHECK_ARG(!e8_mma || (rows_total % 128 == 0 && d % 128 == 0));
     dim3 grid;
-    MOE4_CHECK_ARG(requant_grid(rows_total, (d + kTileC - 1) / kTileC, 1, grid));
+    MOE4_CHECK_ARG(requant_grid(rows_total, (d + kWideTile - 1) / kWideTile, 1, grid));
     if (rows_total == 0) return MOE4_OK;
-    requant_transpose_kernel<SrcKind::CombineBwd, false, true><<<grid, 256, 0, as_stream(stream)>>>(
+    requant_transpose_kernel<SrcKind::CombineBwd, false, true, true, kWideTile><<<grid, 256, 0, as_stream(stream)>>>(
         nullptr, nullptr, nullptr, dy, 1, rows_total, d, q_col, e8_col, philox_keys(0), 0u, false, q_row, e8_row,
         nullptr, nullptr, src_of, row_of, w, (int)k, e8_mma);
     return launch_status();
