@@ -6,8 +6,9 @@
 // and requantised into MXFP8 with stochastic rounding, which picks the upper or lower neighbour
 // with probability given by the distance so that the value is kept on average.
 //
-// Tile: 128 input rows (the output's contiguous dimension) x 64 input columns.  Phase 1: each
-// thread reads one row's 32 values (16 code bytes and two scale bytes, or 64 bytes of bf16) and
+// Tile: 128 input rows (the output's contiguous dimension) x 64 input columns (128 for the
+// two-layout quantisers of bf16 sources).  Phase 1: each thread reads one row's 32 values (16 code
+// bytes and two scale bytes, or 64 bytes of bf16; two such groups on a 128-column tile) and
 // stores them as 16 column pairs, one 32-bit word each, in the transposed shared tile.  Phase 2:
 // each warp emits two output rows (one column pair) of 128 values: lane l owns 4 consecutive
 // values of each (two lanes share the Philox calls that give their 16-bit numbers), 8 lanes form
