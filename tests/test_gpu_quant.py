@@ -378,3 +378,39 @@ def test_quantize_f32_equals_quantize_of_bf16_copy(given, mma, ld):
         assert np.array_equal(s_np, to_np(s2))
     else:
         assert first_mismatch(s_np, rs) is None
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_hadamard_codecs_on_subnormal_rows(mx):
+    """Rows at the bottom of the bf16 range: every value subnormal (so the butterflies' sums and
+    differences are subnormal too), subnormal values beside one normal value, and normal values
+    whose differences cancel into the subnormal range; both return-path codecs against the
+    oracle, bit for bit, codes and decoded rows."""
+    rows, cols = 8, 256
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[0:3] *= 1e-39                                  # all subnormal
+    x[3] *= 1e-39
+    x[3, 7] = 1.0                                    # one normal value among subnormals
+    x[4] = np.float32(2.0 ** -125) * np.sign(x[4])   # equal magnitudes at the normal edge: exact cancellations
+    x[5] = (np.float32(2.0 ** -126) * (1 + (rng.integers(0, 4, cols) / 8.0)) * np.sign(x[5])).astype(np.float32)
+    xb = inputs.to_bf16_bits(x)
+    if mx:
+        q, e8, out = _mx_codec(to_dev(xb), rows, cols)
+        rq, re = oracle.hadamard_quant_mx(oracle.bf16_to_f32(xb))
+        assert first_mismatch(to_np(q), rq) is None
+        assert first_mismatch(to_np(e8), re) is None
+        assert first_mismatch(to_np(out, np.uint16), oracle.hadamard_dequant_mx(rq, re)) is None
+    else:
+        codes, sf = empty_u8(rows, cols // 2), empty_u8(rows, cols // 16)
+        gd = torch.empty(1, dtype=torch.float32, device=DEV)
+        ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_HADAMARD_QUANT))
+        moe4.hadamard_quant(to_dev(xb), rows, cols, codes, sf, gd, moe4.FOUR_OVER_SIX, ws)
+        out = torch.empty((rows, cols), dtype=torch.int16, device=DEV)
+        moe4.hadamard_dequant(codes, sf, gd, rows, cols, out)
+        torch.cuda.synchronize()
+        rc, rs, rg = oracle.hadamard_quant(oracle.bf16_to_f32(xb))
+        assert first_mismatch(to_np(codes), rc) is None
+        assert first_mismatch(to_np(sf), rs) is None
+        assert np.array_equal(to_np(gd), np.atleast_1d(rg))
+        assert first_mismatch(to_np(out, np.uint16), oracle.hadamard_dequant(rc, rs, rg)) is None
