@@ -99,7 +99,10 @@ __device__ __forceinline__ GlobalScale global_scale(float amax) {
 __device__ __forceinline__ void fill_scale_tab(float2 *tab) {
     for (int i = threadIdx.x; i < 128; i += blockDim.x) {
         const float v = e4m3_to_f32((uint32_t)i);
-        tab[i] = make_float2(v, v == 0.0f ? 0.0f : __fdiv_rn(1.0f, v));
+        // code 0 has no reciprocal (its blocks take the zero-scale branch); its slot holds -0, the
+        // addend of the squared errors' multiply-adds, read from memory so that the compiler
+        // cannot drop it (see nvfp4_candidate)
+        tab[i] = make_float2(v, v == 0.0f ? -0.0f : __fdiv_rn(1.0f, v));
     }
     __syncthreads();
 }
@@ -141,14 +144,26 @@ __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, con
 #pragma unroll
         for (int i = 0; i < 8; ++i) fma2_f16(eh[i], nsf, y[2 * i], y[2 * i + 1], d[2 * i], d[2 * i + 1]);
     }
-    float s[16];
+    // the squared error: s[i] = RN(d[i]^2), then the fixed tree s[i] += s[i + off] for off = 8, 4,
+    // 2, 1, as pairs (s[2j], s[2j+1]), each pair step the scalar tree's two operations.  A square
+    // is RN(d*d + (-0)), which is RN(d*d): a packed multiply would be fused with the packed add
+    // that consumes it, and -0 as a constant would let the compiler turn the multiply-add back
+    // into that multiply, so the addend comes from the scale table in shared memory
+    const float nz = tab[0].y;
+    const uint64_t nz2 = f2_pack(nz, nz);
+    uint64_t p2[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(d[i], d[i]);
+    for (int j = 0; j < 8; ++j) {
+        const uint64_t dj = f2_pack(d[2 * j], d[2 * j + 1]);
+        p2[j] = f2_fma(dj, dj, nz2);
+    }
 #pragma unroll
-    for (int off = 8; off >= 1; off >>= 1)
+    for (int off = 4; off >= 1; off >>= 1)
 #pragma unroll
-        for (int i = 0; i < off; ++i) s[i] = __fadd_rn(s[i], s[i + off]);
-    return s[0];
+        for (int j = 0; j < off; ++j) p2[j] = f2_add(p2[j], p2[j + off]);
+    float s0, s1;
+    f2_unpack(p2[0], s0, s1);
+    return __fadd_rn(s0, s1);
 }
 
 __device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_six, const float2 *tab, uint32_t &w0,

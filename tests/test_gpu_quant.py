@@ -414,3 +414,19 @@ def test_hadamard_codecs_on_subnormal_rows(mx):
         assert first_mismatch(to_np(sf), rs) is None
         assert np.array_equal(to_np(gd), np.atleast_1d(rg))
         assert first_mismatch(to_np(out, np.uint16), oracle.hadamard_dequant(rc, rs, rg)) is None
+
+
+@pytest.mark.parametrize("fos", [True, False])
+def test_quantize_subnormal_inputs(fos):
+    """NVFP4 of tensors at the bottom of the bf16 range, against the oracle bit for bit: a whole
+    matrix of random subnormal values (the per-tensor scale then lifts them into range), and a
+    normal matrix whose 16-column blocks 3 and 10 hold only subnormal values (their block scale
+    underflows to zero), except one normal value in block 10 of row 5."""
+    rng = np.random.default_rng(43)
+    a = (rng.standard_normal((64, 256)) * 1e-39).astype(np.float32)
+    b = rng.standard_t(3, (64, 256)).astype(np.float32)
+    b[:, 48:64] *= 1e-39
+    b[:, 160:176] *= 1e-39
+    b[5, 160] = 3.0
+    xb = inputs.to_bf16_bits(np.stack([a, b]))
+    _check_quant(xb, 2, 64, 256, fos=fos)
