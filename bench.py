@@ -57,9 +57,13 @@ LR = 1e-3
 WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
 # DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
 # case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
-TRAFFIC_RATIO = {"gemm_mxfp8_wgrad_sgd": 2162.9 / 2216.7}  # profiles/gemm_mxfp8_wgrad_sgd_16experts.md
+# DRAM bytes per step of the kernel groups, read + written, from a one-pass ncu capture of this
+# layer step at full size (dram__bytes_read.sum + dram__bytes_write.sum over the two launches of
+# the second timed step): profiles/layer_step_dram_bytes.md
+DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.205e9}
 MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "swiglu_quant_h", "hadamard", "mxfp8_quant"}
-GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2, "quant_w": 4}
+GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2,
+                  "quant_w": 4 * WEIGHT_CHUNKS}
 
 
 def load_peaks():
@@ -1027,9 +1031,10 @@ def main():
     }
     nl = GROUP_LAUNCHES.get(dom, 1)
     roof["launches_per_step"] = nl
-    if dom in TRAFFIC_RATIO:
-        roof["traffic"] = TRAFFIC_RATIO[dom] * gbytes[dom] / nl
-        roof["traffic_note"] = "DRAM bytes per launch: ncu ratio on a 16-expert capture x algorithmic bytes"
+    if dom in DRAM_PER_STEP:
+        roof["traffic"] = DRAM_PER_STEP[dom] / nl
+        roof["traffic_note"] = ("DRAM bytes per launch (read + write), one-pass ncu capture of this step at full "
+                                "size; algorithmic bytes per launch %.4g" % (gbytes[dom] / nl))
     roof["peak_source"] = peaks["src"]
     req_t = per.get("requant", 0.0)
     requant_gbs = gbytes["requant"] / (req_t / 1e3) / 1e9 if req_t else None
