@@ -63,7 +63,7 @@ WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
 DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.205e9}
 MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "swiglu_quant_h", "hadamard", "mxfp8_quant"}
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2,
-                  "quant_w": 4 * WEIGHT_CHUNKS}
+                  "quant_w": 4 * WEIGHT_CHUNKS}  # two launches per chunk, WEIGHT_CHUNKS chunks per projection
 
 
 def load_peaks():
@@ -79,6 +79,12 @@ def load_peaks():
 # ---------------------------------------------------------------------------------------------
 # the device step
 # ---------------------------------------------------------------------------------------------
+def weight_chunk_bounds(E):
+    """Expert bounds of the weight path's chunks, gate/up then down: WEIGHT_CHUNKS equal chunks."""
+    even = [E * i // WEIGHT_CHUNKS for i in range(WEIGHT_CHUNKS + 1)]
+    return even, even
+
+
 class LayerStep:
     """All device buffers of one layer step and the sequence of library calls."""
 
@@ -118,7 +124,8 @@ class LayerStep:
         # the weight path's side stream (higher priority: its quantiser's CTAs are placed first)
         self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.ev_fork = torch.cuda.Event()
-        self.ev_q = [torch.cuda.Event() for _ in range(2 * WEIGHT_CHUNKS)]
+        self.n_wchunks = sum(len(b) - 1 for b in weight_chunk_bounds(E))
+        self.ev_q = [torch.cuda.Event() for _ in range(self.n_wchunks)]
         self.src_of = torch.empty(R, dtype=torch.int32, device=dev)
         self.plan_ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E), dev)
         self.qws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, E), dev)
@@ -197,7 +204,7 @@ class LayerStep:
             # chunks: chunk i+1's quantiser (HBM-bound) runs on a side stream on part of each SM
             # while chunk i's requantiser (issue-bound) takes the rest.
             self.weight_path(seed, cur)
-        n += 4 * WEIGHT_CHUNKS  # each chunk: the quantiser, then the requantiser
+        n += 2 * self.n_wchunks  # each chunk: the quantiser, then the requantiser
         wait("X")  # the weight path needs none of the step's inputs: X's copy can run beside it
         with tm("quant_x"):
             m.nvfp4_quantize(X, 1, T, d, d, self.Xq_c, self.Xq_s, self.Xq_g, None, FOS, self.qws)
@@ -273,11 +280,11 @@ class LayerStep:
         next chunk's quantiser (MOE4_SHARE_SMS) on the side stream."""
         m, E, d, f = self.m, self.E, self.d, self.f
         WF = m.FOUR_OVER_SIX | m.SR | m.SF_MMA_LAYOUT | m.SF_OUT_MMA
-        bounds = [E * i // WEIGHT_CHUNKS for i in range(WEIGHT_CHUNKS + 1)]
         chunks = []
-        for W, am, c, sf, g, qt, et, rows, cols, sid in (
+        for (W, am, c, sf, g, qt, et, rows, cols, sid), bounds in zip((
                 (self.W32_gu, self.amax_gu, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.WguT_q, self.WguT_e, 2 * f, d, 3),
-                (self.W32_d, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g, self.WdT_q, self.WdT_e, d, f, 1)):
+                (self.W32_d, self.amax_d, self.Wd_c, self.Wd_s, self.Wd_g, self.WdT_q, self.WdT_e, d, f, 1)),
+                weight_chunk_bounds(E)):
             for e0, e1 in zip(bounds[:-1], bounds[1:]):
                 # mat_base = the chunk's first expert: its random numbers are those of one call over
                 # the projection's whole stack
