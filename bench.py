@@ -61,7 +61,7 @@ WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
 # layer step at full size (dram__bytes_read.sum + dram__bytes_write.sum over the two launches of
 # the second timed step): profiles/layer_step_dram_bytes.md
 DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.205e9}
-MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "swiglu_quant_h", "hadamard", "mxfp8_quant"}
+MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "hadamard", "mxfp8_quant"}
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2,
                   "quant_w": 4 * WEIGHT_CHUNKS}  # two launches per chunk, WEIGHT_CHUNKS chunks per projection
 
@@ -211,14 +211,14 @@ class LayerStep:
             m.moe4_permute_nvfp4(self.Xq_c, self.Xq_s, T, d, self.src_of, Rp, self.Xp_c, self.Xp_s, MMA)
         n += 3
         with tm("gemm_nvfp4"):
-            m.grouped_expert_gemm_nvfp4(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g, self.offs,
-                                        E, Rp, 2 * f, d, self.GU, m.OUT_F32 | MMA)
+            # the gate/up projection; its last stage also forms H = SwiGLU(GU) and the amax of H
+            m.grouped_expert_gemm_nvfp4_swiglu(self.Xp_c, self.Xp_s, self.Xq_g, self.Wgu_c, self.Wgu_s, self.Wgu_g,
+                                               self.offs, E, Rp, f, d, self.GU, self.H, self.amax_h, MMA)
         n += 1
-        with tm("swiglu_quant_h"):  # SwiGLU with the amax of H, so H is quantised in one pass
-            m.moe4_swiglu_amax(self.GU[:Rp], Rp, f, self.H[:Rp], self.amax_h)
+        with tm("quant_h"):  # H to NVFP4 in one pass, its amax from the GEMM
             m.nvfp4_quantize(self.H[:Rp], 1, Rp, f, f, self.Hq_c, self.Hq_s, self.Hq_g, self.amax_h,
                              FOS | MMA | m.AMAX_GIVEN)
-        n += 2
+        n += 1
         with tm("gemm_nvfp4"):
             # the down projection; its last stage also returns the amax of the Hadamard-rotated rows
             m.grouped_expert_gemm_nvfp4_hadamard_amax(self.Hq_c, self.Hq_s, self.Hq_g, self.Wd_c, self.Wd_s,
@@ -316,7 +316,7 @@ class LayerStep:
         # the SGD epilogue)
         b["quant_w"] = (w_gu + w_d) * live / E * (4 + nv + mx)
         b["quant_x"] = T * d * (2 + 2 + nv) + rows * d * nv * 2          # + gather read/write
-        b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 +
+        b["gemm_nvfp4"] = (rows * d * nv + live * 2 * f * d * nv + rows * 2 * f * 4 + rows * f * 2 +  # + H
                            rows * f * nv + live * d * f * nv + rows * d * 2)
         b["requant"] = rows * (f + d) * (nv + mx)                        # H and the gathered X
         # combine gradient formed from dy (read once) straight into both MXFP8 layouts of dY, and one
@@ -327,7 +327,7 @@ class LayerStep:
         # wgrad operands + the SGD epilogue: read W32, write W32 (the bf16 copy is not stored)
         b["gemm_mxfp8_wgrad_sgd"] = (rows * d * mx + rows * f * mx + rows * 2 * f * mx + rows * d * mx +
                                      (w_gu + w_d) * live / E * (4 + 4))   # experts without rows are skipped
-        b["swiglu_quant_h"] = rows * 2 * f * 4 + rows * f * 2 + rows * f * (2 + nv)  # amax fused into SwiGLU
+        b["quant_h"] = rows * f * (2 + nv)             # SwiGLU and its amax in the gate/up GEMM
         b["swiglu_bwd"] = rows * (2 * f * 4 + f * 4 + 2 * f * 2)
         b["hadamard"] = rows * d * (2 + nv)            # amax from the down GEMM's last stage
         b["combine"] = rows * d * nv + T * d * 2       # decoded from the NVFP4 rows as it combines
@@ -830,7 +830,7 @@ def profile_case(name):
         compute_probe(0 if name == "gemm_nvfp4_probe" else 1, reps=3, dev=dev)
         print("profile case %s done" % name)
         return 0
-    elif name in ("gemm_nvfp4", "gemm_nvfp4_down_amax"):
+    elif name in ("gemm_nvfp4", "gemm_nvfp4_swiglu", "gemm_nvfp4_down_amax"):
         rows = 128 * 64
         x = inputs.device_student_t((rows, d), g(3), dev).view(torch.int16)
         w = inputs.device_normal((E * 2 * f, d), 0.02, g(0), dev).view(torch.int16)
@@ -847,6 +847,12 @@ def profile_case(name):
             out = torch.empty((rows, 2 * f), dtype=torch.float32, device=dev)
             calls.append(lambda: moe4.grouped_expert_gemm_nvfp4(ac, as_, ag, bc, bs, bg, offs, E, rows, 2 * f, d, out,
                                                                 moe4.OUT_F32 | moe4.SF_MMA_LAYOUT))
+        elif name == "gemm_nvfp4_swiglu":  # the gate/up projection as the step runs it: GU, h and its amax
+            out = torch.empty((rows, 2 * f), dtype=torch.float32, device=dev)
+            hout = torch.empty((rows, f), dtype=torch.int16, device=dev)
+            am = torch.empty(1, dtype=torch.float32, device=dev)
+            calls.append(lambda: moe4.grouped_expert_gemm_nvfp4_swiglu(ac, as_, ag, bc, bs, bg, offs, E, rows, f, d, out,
+                                                                       hout, am, moe4.SF_MMA_LAYOUT))
         else:  # the down projection as the step runs it: bf16 out and the rotated amax for the codec
             hc, hs = torch.empty((rows, f // 2), **u8), torch.empty((rows, f // 16), **u8)
             h = inputs.device_student_t((rows, f), g(9), dev).view(torch.int16)
@@ -909,7 +915,8 @@ def main():
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-next", action="store_true", help="skip the supplementary MXFP8-forward and 8.25-bit codec timings")
     ap.add_argument("--profile-case", default=None,
-                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_nvfp4_down_amax", "gemm_mxfp8_wgrad",
+                    choices=["requant", "quant_w", "gemm_nvfp4", "gemm_nvfp4_swiglu", "gemm_nvfp4_down_amax",
+                             "gemm_mxfp8_wgrad",
                              "gemm_mxfp8_wgrad_sgd",
                              "gemm_mxfp8_dgrad", "sgd", "mxfp8_rowcol", "hadamard", "hadamard_given", "combine_hadamard",
                              "gemm_nvfp4_probe", "tensor_peaks",
@@ -1110,7 +1117,7 @@ def main():
         mf = nxt["mxfp8_forward"]
         mf["nvfp4_gemm_ms"] = round(per["gemm_nvfp4"], 4)
         mf["nvfp4_gemm_speedup"] = round(mf["gemm_ms"] / per["gemm_nvfp4"], 3)
-        mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["swiglu_quant_h"], 4)
+        mf["nvfp4_quant_swiglu_ms"] = round(per["quant_x"] + per["quant_w"] + per["quant_h"], 4)
         nxt["hadamard_mxfp8_codec"]["nvfp4_encode_and_decode_combine_ms"] = round(per["hadamard"] + per["combine"], 4)
         probe = {"shape": "8 groups x 8192 rows, N = K = 8192, bf16 out (compute-bound; not the layer's shape)"}
         # timed alone: the burst rates of the tensor-pipe probe

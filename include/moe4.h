@@ -281,6 +281,21 @@ int grouped_expert_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const
                               int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
                               void *stream);
 
+/* grouped_expert_gemm_nvfp4_swiglu: the gate/up projection with the SwiGLU between the GEMMs in
+ * its last stage.  B = W_gu, E matrices NVFP4 [2f, K] (gate rows 0 .. f-1, then up rows).  Writes
+ * gu [rows_total, 2f] binary32, exactly grouped_expert_gemm_nvfp4's D with MOE4_OUT_F32, and
+ * h [rows_total, f] bf16, h = RN_bf16(silu(g) * u) with g = gu[:, j], u = gu[:, f + j] and
+ * silu(g) = g / (1 + exp(-g)), each step one binary32 rounding, exactly as moe4_swiglu_amax
+ * computes it from gu; amax_out[0] = max |h| as moe4_swiglu_amax returns it.  Each tile of the
+ * GEMM holds 128 gate columns and the same 128 up columns, so gu is not read back.  f % 128 == 0,
+ * K % 256 == 0, rows_total % 128 == 0; gu, h 16-byte aligned; scales and ws as
+ * grouped_expert_gemm_nvfp4 with N = 2f. */
+int grouped_expert_gemm_nvfp4_swiglu(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                                     const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                                     const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t f,
+                                     int64_t K, float *gu, uint16_t *h, float *amax_out, uint32_t flags,
+                                     void *ws, size_t ws_bytes, void *stream);
+
 /* grouped_expert_gemm_nvfp4_hadamard_amax: grouped_expert_gemm_nvfp4 with bf16 output d, which
  * also returns in amax_out[0] the largest magnitude of the Hadamard(128)-rotated d (each 128-column
  * chunk of a row rotated as hadamard_quant does it), computed in the GEMM's last stage from the

@@ -76,7 +76,10 @@ constexpr int EPI_W_TILE = 32 * TMA_CW<KIND> * 4;
 // Epilogue implementations: REG stores from registers (the read-modify-write accumulate mode),
 // TMA stages each warp's 32x32 output tile in shared memory and bulk-stores it, SGD is the fused
 // master-weight update.  Operand stages shrink to make room for the staging buffers.
-enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4 };
+// SWI (the gate/up projection, NVFP4): each tile's 256 B rows are 128 gate rows and the matching
+// 128 up rows, so the epilogue holds gate and up of the same columns and writes GU and the SwiGLU
+// h = silu(g) * u (bf16) with its amax, as TMA does for D.
+enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4, EPI_SWI = 5 };
 // EPI_SGD writes the bf16 copy, EPI_SGD32 only the binary32 master weights (and the amax).
 __host__ __device__ constexpr bool is_sgd(int em) { return em == EPI_SGD || em == EPI_SGD32; }
 template <int EM>
@@ -102,14 +105,14 @@ struct EpiCfg {
     // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
     // tile's MMAs overlap the previous tile's master-weight traffic
     static constexpr int BNT = is_sgd(EM) ? 128 : BN;
-    static constexpr int NST = is_sgd(EM) ? 4 : (EM == EPI_TMA ? 3 : (EM == EPI_HMX ? 2 : STAGES));
+    static constexpr int NST = is_sgd(EM) ? 4 : ((EM == EPI_TMA || EM == EPI_SWI) ? 3 : (EM == EPI_HMX ? 2 : STAGES));
     // operand stages for a given operand kind: the MXFP8 TMA-store mode fits a fourth one
     template <int KIND>
     static constexpr int NSTK = (EM == EPI_TMA && KIND == 1) ? 4 : NST;
     template <int KIND>
     static constexpr int BYTESK =
         is_sgd(EM) ? 8 * SgdRing<EM>::WARP_BYTES
-                   : (EM == EPI_TMA ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
+                   : ((EM == EPI_TMA || EM == EPI_SWI) ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
 };
 
 template <int KIND, int NST, int EPI, int BNT>
@@ -159,6 +162,9 @@ struct Args {
     uint8_t *e8;            // fused codec: E8M0 scales [M, N/32] (d holds the E4M3 codes [M, N])
     unsigned int *had_amax; // bf16 output: max |Hadamard(128)-rotated rows| (binary32 bits), or null
     const int32_t *order;   // contraction-grouped: experts by decreasing group size, or null
+    int64_t swiglu_f;       // EPI_SWI: the SwiGLU width f (B = W_gu [E, 2f, K]; tiles step 128 columns of f)
+    uint16_t *h;            // EPI_SWI: h [M, f] bf16
+    unsigned int *h_amax;   // EPI_SWI: max |h| as binary32 bits
     int64_t num_tiles;
     int n_tiles_n, n_tiles_m;
     int64_t sfa_tile_stride;  // atoms between consecutive 128-row tiles of A's scale layout
@@ -340,7 +346,7 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t, int64_t nt
     if (!p.group_k) {
         const uint32_t mt = t32 / ntn, nt = t32 - mt * ntn;
         tl.m0 = (int64_t)mt * BM;
-        tl.n0 = (int64_t)nt * BNT;
+        tl.n0 = (int64_t)nt * (p.swiglu_f ? 128 : BNT);  // SwiGLU: the tile's gate columns n0 .. n0 + 127
         int lo = 0, hi = p.E;  // largest e with offs[e] <= m0
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -466,12 +472,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t kel = tl.k_begin + (int64_t)ks * Cfg<KIND>::ELEMS;   // contraction element
                 const int xbytes = (int)(KIND == 0 ? kel / 2 : kel);
                 tma_load_2d(smem + L::OFF_A + stage * A_TILE, &tmA, fb, xbytes, (int)tl.m0);
-                tma_load_2d(smem + L::OFF_B + stage * L::B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
+                if constexpr (EM == EPI_SWI) {
+                    // B rows: the gate slice, then the up slice f rows further on (128-row boxes)
+                    tma_load_2d(smem + L::OFF_B + stage * L::B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
+                    tma_load_2d(smem + L::OFF_B + stage * L::B_TILE + 128 * BKB, &tmB, fb, xbytes,
+                                (int)(tl.b_row + p.swiglu_f));
+                } else {
+                    tma_load_2d(smem + L::OFF_B + stage * L::B_TILE, &tmB, fb, xbytes, (int)tl.b_row);
+                }
                 const int64_t atom = kel / Cfg<KIND>::ELEMS_PER_ATOM;
                 const uint8_t *sa = p.sfa + ((tl.m0 / BM) * p.sfa_tile_stride + atom) * 512;
                 bulk_load(smem + L::OFF_SFA + stage * L::SFA, sa, L::SFA, fb);
                 for (int rt = 0; rt < L::RT; ++rt) {
-                    const uint8_t *sb = p.sfb + ((tl.b_row / BM + rt) * p.sfb_tile_stride + atom) * 512;
+                    // the 128-row tile of B's scales that row tile rt of the stage holds
+                    const int64_t brow = (EM == EPI_SWI && rt == 1) ? tl.b_row + p.swiglu_f : tl.b_row + rt * BM;
+                    const uint8_t *sb = p.sfb + ((brow / BM) * p.sfb_tile_stride + atom) * 512;
                     bulk_load(smem + L::OFF_SFB + stage * L::SFB + rt * L::SFA, sb, L::SFA, fb);
                 }
                 issued[stage] = true;
@@ -745,6 +760,83 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if ((sub & 1) == 0) p.e8[grow * (p.N / 32) + col / 32] = (uint8_t)(e + 127);
                 }
                 __syncwarp();  // the staging rows are rewritten by this warp's next tile
+            } else if constexpr (EM == EPI_SWI) {
+                // This warp: rows 32q .. 32q + 31, gate columns 64 * half .. + 63 of the tile
+                // (accumulator columns 64 * half ..) and the same columns of up (accumulator
+                // columns 128 + 64 * half ..).  Both slabs go to registers and the accumulator is
+                // handed back; then six 32-column chunks pass through the staging tile to TMA:
+                // GU [M, 2f] binary32 (gate at column n0 + 64 * half, up f columns further on) and
+                // h = RN_bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)), each step one binary32
+                // rounding, as moe4_swiglu computes it from the same GU values.
+                uint8_t *stage = smem + L::OFF_EPI + (warp - 4) * EPI_W_TILE<KIND>;
+                const int y0 = (int)(tl.m0 + q * 32);
+                const int xg = (int)(tl.n0 + half * 64);
+                const uint32_t tg = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNT + half * 64);
+                uint32_t accr[128];  // gate 0 .. 63, up 64 .. 127
+                if (live) {
+                    tc_ld32_nw(tg, accr);
+                    tc_ld32_nw(tg + 32, accr + 32);
+                    tc_ld32_nw(tg + 128, accr + 64);
+                    tc_ld32_nw(tg + 160, accr + 96);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) accr[i] = 0;
+                }
+                tc_fence_before();
+                mbar_arrive(tmem_empty + acc);
+                uint32_t best = 0;  // two packed bf16 magnitudes of h
+#pragma unroll
+                for (int c = 0; c < 6; ++c) {  // gate 0, gate 1, up 0, up 1, h 0, h 1
+                    if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile out
+                    __syncwarp();
+                    if (c < 4) {
+                        const int off = (c < 2 ? 0 : 64) + (c & 1) * 32;
+                        uint8_t *row = stage + lane * 128;  // 32 binary32, 128-byte swizzle
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) o[i] = __fmul_rn(__uint_as_float(accr[off + 4 * j + i]), alpha);
+                            *reinterpret_cast<float4 *>(row + ((j ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+                        const int cc = (c - 4) * 32;
+                        uint8_t *row = stage + lane * 64;  // 32 bf16, 64-byte swizzle
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t hb[2];
+#pragma unroll
+                                for (int e2 = 0; e2 < 2; ++e2) {
+                                    const int col = cc + 8 * j + 2 * i + e2;
+                                    const float gv = __fmul_rn(__uint_as_float(accr[col]), alpha);
+                                    const float uv = __fmul_rn(__uint_as_float(accr[64 + col]), alpha);
+                                    const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));
+                                    hb[e2] = (uint32_t)f32_to_bf16_bits(__fmul_rn(silu, uv));
+                                }
+                                w[i] = hb[0] | (hb[1] << 16);
+                                best = __vmaxu2(best, w[i] & 0x7FFF7FFFu);
+                            }
+                            *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (c < 4)
+                            tma_store_2d(&tmW, stage, (c < 2 ? xg : (int)(p.swiglu_f + xg)) + (c & 1) * 32, y0);
+                        else
+                            tma_store_2d(&tmWb, stage, xg + (c - 4) * 32, y0);
+                        bulk_commit();
+                    }
+                }
+                uint32_t mag = max(best & 0xFFFFu, best >> 16) << 16;
+                mag = __reduce_max_sync(0xFFFFFFFFu, mag);
+                if (lane == 0 && mag) atomicMax(p.h_amax, mag);
             } else if constexpr (EM == EPI_TMA) {
                 // each CW-column chunk: registers -> swizzled 32 x CW staging tile -> TMA bulk store.
                 // A staged row is CW * 4 (binary32) or CW * 2 (bf16) bytes with the swizzle of that
@@ -864,7 +956,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            if constexpr (EM != EPI_HMX && EM != EPI_TMA) {  // those two hand the accumulator back early
+            if constexpr (EM != EPI_HMX && EM != EPI_TMA && EM != EPI_SWI) {  // those hand it back early
                 tc_fence_before();
                 mbar_arrive(tmem_empty + acc);
             }
@@ -1221,6 +1313,58 @@ extern "C" int grouped_expert_gemm_nvfp4_hadamard_amax(const uint8_t *a_codes, c
     CUtensorMap td;
     if (!make_out_map(&td, d, true, rows_total, N, TMA_CW<0>)) return MOE4_ERR_CUDA;
     return launch<0, EPI_TMA>(ta, tb, td, td, a, st);
+}
+
+extern "C" int grouped_expert_gemm_nvfp4_swiglu(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_g_dec,
+                                                const uint8_t *b_codes, const uint8_t *b_sf, const float *b_g_dec,
+                                                const int32_t *group_offs, int64_t E, int64_t rows_total, int64_t f,
+                                                int64_t K, float *gu, uint16_t *h, float *amax_out, uint32_t flags,
+                                                void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && rows_total >= 0 && rows_total % BM == 0 && f > 0 && f % 128 == 0 && K > 0 &&
+                   K % 256 == 0);
+    MOE4_CHECK_ARG(a_codes && a_sf && a_g_dec && b_codes && b_sf && b_g_dec && group_offs && gu && h && amax_out);
+    MOE4_CHECK_ARG(aligned16(a_codes) && aligned16(b_codes) && aligned16(a_sf) && aligned16(b_sf) && aligned16(gu) &&
+                   aligned16(h) && aligned4(amax_out));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    const int64_t N = 2 * f;
+    MOE4_CHECK_ARG(rows_total < (int64_t(1) << 31) && E * N < (int64_t(1) << 31));
+    if (rows_total > 0 && !(flags & MOE4_SF_MMA_LAYOUT) && !scales_ws_ok(rows_total, E * N, K, 16, ws, ws_bytes))
+        return MOE4_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MOE4_ERR_CUDA;
+    if (rows_total == 0) return MOE4_OK;
+    const uint8_t *sfa, *sfb;
+    int rc = stage_scales(a_sf, rows_total, b_sf, E * N, K, 16, flags, ws, ws_bytes, &sfa, &sfb, st);
+    if (rc != MOE4_OK) return rc;
+    CUtensorMap ta, tb;
+    // B in 128-row boxes: each tile loads 128 gate rows and the 128 up rows f further on
+    if (!make_map(&ta, a_codes, K / 2, rows_total, BM) || !make_map(&tb, b_codes, K / 2, E * N, 128))
+        return MOE4_ERR_CUDA;
+    Args a{};
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.a_g_dec = a_g_dec;
+    a.b_g_dec = b_g_dec;
+    a.offs = group_offs;
+    a.E = (int)E;
+    a.group_k = 0;
+    a.M = rows_total;
+    a.N = N;
+    a.K = K;
+    a.d = gu;
+    a.mode = F32;
+    a.swiglu_f = f;
+    a.h = h;
+    a.h_amax = reinterpret_cast<unsigned int *>(amax_out);
+    a.n_tiles_n = (int)(f / 128);
+    a.n_tiles_m = (int)(rows_total / BM);
+    a.num_tiles = (int64_t)a.n_tiles_m * a.n_tiles_n;
+    a.sfa_tile_stride = K / 64;
+    a.sfb_tile_stride = K / 64;
+    CUtensorMap tgu, th;
+    if (!make_out_map(&tgu, gu, false, rows_total, N, 32) || !make_out_map(&th, h, true, rows_total, f, 32))
+        return MOE4_ERR_CUDA;
+    return launch<0, EPI_SWI>(ta, tb, tgu, th, a, st);
 }
 
 extern "C" int grouped_expert_gemm_nvfp4_hadamard_mx(const uint8_t *a_codes, const uint8_t *a_sf,

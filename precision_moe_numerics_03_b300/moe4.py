@@ -68,6 +68,8 @@ _SIGNATURES = {
                                          _vp, _sz, _vp]),
     "grouped_expert_gemm_nvfp4_hadamard_amax": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                         _vp, _vp, _u32, _vp, _sz, _vp]),
+    "grouped_expert_gemm_nvfp4_swiglu": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                _vp, _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_expert_gemm_nvfp4_hadamard_mx": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                       _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32, _vp, _sz, _vp]),
@@ -249,6 +251,13 @@ def grouped_expert_gemm_nvfp4_hadamard_amax(a_codes, a_sf, a_g_dec, b_codes, b_s
                                             rows_total, N, K, d, amax_out, flags=0, ws=None, stream=None):
     _call("grouped_expert_gemm_nvfp4_hadamard_amax", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf),
           _p(b_g_dec), _p(group_offs), E, rows_total, N, K, _p(d), _p(amax_out), flags, _p(ws), _ws_bytes(ws),
+          _s(stream))
+
+
+def grouped_expert_gemm_nvfp4_swiglu(a_codes, a_sf, a_g_dec, b_codes, b_sf, b_g_dec, group_offs, E, rows_total, f, K,
+                                     gu, h, amax_out, flags=0, ws=None, stream=None):
+    _call("grouped_expert_gemm_nvfp4_swiglu", _p(a_codes), _p(a_sf), _p(a_g_dec), _p(b_codes), _p(b_sf),
+          _p(b_g_dec), _p(group_offs), E, rows_total, f, K, _p(gu), _p(h), _p(amax_out), flags, _p(ws), _ws_bytes(ws),
           _s(stream))
 
 

@@ -481,3 +481,78 @@ def test_nvfp4_down_bf16_full_size_sampled_rows():
         Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rhc, rhs, rhg),
                                         oracle.nvfp4_dequantize(rwc, rws, rwg)[None], np.array([0, len(rows)]))
         check_bf16(to_np(Y[torch.as_tensor(rows, device=DEV)], np.uint16), Dref, S)
+
+
+def _swiglu_pair(xpc, xps, xg, wc, wsf, wg, offs, E, R, f, K, flags):
+    """The fused gate/up GEMM + SwiGLU and, for comparison, the GEMM followed by moe4_swiglu_amax."""
+    gws = moe4.workspace(moe4.moe4_workspace_size_gemm(0, R, E, 2 * f, K))
+    gu_ref = torch.empty((R, 2 * f), dtype=torch.float32, device=DEV)
+    moe4.grouped_expert_gemm_nvfp4(xpc, xps, xg, wc, wsf, wg, offs, E, R, 2 * f, K, gu_ref, moe4.OUT_F32 | flags, gws)
+    h_ref = torch.empty((R, f), dtype=torch.int16, device=DEV)
+    am_ref = torch.empty(1, dtype=torch.float32, device=DEV)
+    moe4.moe4_swiglu_amax(gu_ref, R, f, h_ref, am_ref)
+    gu = torch.full((R, 2 * f), float("nan"), dtype=torch.float32, device=DEV)
+    h = torch.full((R, f), -1, dtype=torch.int16, device=DEV)
+    am = torch.full((1,), 123.0, dtype=torch.float32, device=DEV)
+    moe4.grouped_expert_gemm_nvfp4_swiglu(xpc, xps, xg, wc, wsf, wg, offs, E, R, f, K, gu, h, am, flags, gws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    return (gu, h, am), (gu_ref, h_ref, am_ref)
+
+
+@pytest.mark.parametrize("sf_mma", [False, True])
+def test_nvfp4_gate_up_with_swiglu_equals_gemm_then_swiglu(sf_mma):
+    """grouped_expert_gemm_nvfp4_swiglu against the gate/up GEMM followed by moe4_swiglu_amax, bit
+    for bit (GU, h and the amax of h): four experts (one empty), f = 256 (two tiles of 128 gate and
+    128 up columns), both scale layouts."""
+    sizes, f, K = [128, 256, 0, 384], 256, 512
+    rng = np.random.default_rng(61)
+    E, offs = len(sizes), _offs(sizes)
+    R = int(offs[-1])
+    a_bits = _bf16(rng, (R, K), t=True)
+    b_bits = _bf16(rng, (E * 2 * f, K), 0.05)
+    ac, asf, ag = nvfp4_quantize(to_dev(a_bits), 1, R, K)
+    bc, bsf, bg = nvfp4_quantize(to_dev(b_bits), E, 2 * f, K)
+    flags = 0
+    if sf_mma:
+        asf2, bsf2 = torch.empty_like(asf), torch.empty_like(bsf)
+        moe4.moe4_sf_to_mma_layout(asf, 1, R, K // 16, asf2)
+        moe4.moe4_sf_to_mma_layout(bsf, E, 2 * f, K // 16, bsf2)
+        asf, bsf, flags = asf2, bsf2, moe4.SF_MMA_LAYOUT
+    got, want = _swiglu_pair(ac, asf, ag, bc, bsf, bg, to_dev(offs), E, R, f, K, flags)
+    for a, b, name in zip(got, want, ("GU", "h", "amax")):
+        assert torch.equal(a, b), name
+    # and the GEMM part against the oracle's float64 product
+    rac, ras, rag = oracle.nvfp4_quantize(oracle.bf16_to_f32(a_bits))
+    rbc, rbs, rbg = oracle.nvfp4_quantize(oracle.bf16_to_f32(b_bits).reshape(E, 2 * f, K))
+    Dref, S = oracle.grouped_gemm_m(oracle.nvfp4_dequantize(rac, ras, rag), oracle.nvfp4_dequantize(rbc, rbs, rbg), offs)
+    check_f32(to_np(got[0]), Dref, S, "fused GU")
+
+
+def test_nvfp4_gate_up_with_swiglu_layer_shape():
+    """The layer step's gate/up projection (16384 tokens x top-8 over 384 experts, 160k padded rows,
+    d_model 4096, f = 2048, tile-layout scales): the fused GEMM + SwiGLU equals the GEMM followed
+    by moe4_swiglu_amax, bit for bit, over the whole output."""
+    T, d, f, E, k = 16384, 4096, 2048, 384, 8
+    rng = np.random.default_rng(1)
+    lg = (rng.standard_normal((T, E)) + rng.standard_normal(E)).astype(np.float32)
+    idx, _ = oracle.route_topk(lg, k)
+    rows_cap = T * k + 127 * E
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    src_of = torch.empty(rows_cap, dtype=torch.int32, device=DEV)
+    moe4.moe4_permute_plan(to_dev(idx), T, k, E, offs, row_of, src_of, rows_cap,
+                           moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E)))
+    torch.cuda.synchronize()
+    Rp = int(to_np(offs)[-1])
+    x = inputs.device_student_t((T, d), inputs.device_generator(22, 0, DEV), DEV).view(torch.int16)
+    w = inputs.device_normal((E * 2 * f, d), 0.02, inputs.device_generator(22, 1, DEV), DEV).view(torch.int16)
+    xc, xs, xg = nvfp4_quantize(x, 1, T, d)
+    xpc, xps = empty_u8(Rp, d // 2), empty_u8(Rp, d // 16)
+    moe4.moe4_permute_nvfp4(xc, xs, T, d, src_of, Rp, xpc, xps, moe4.SF_MMA_LAYOUT)
+    del xc, xs, x
+    wc, ws_, wg = nvfp4_quantize(w, E, 2 * f, d, moe4.FOUR_OVER_SIX | moe4.SF_MMA_LAYOUT)
+    del w
+    got, want = _swiglu_pair(xpc, xps, xg, wc, ws_, wg, offs, E, Rp, f, d, moe4.SF_MMA_LAYOUT)
+    for a, b, name in zip(got, want, ("GU", "h", "amax")):
+        assert torch.equal(a, b), name
