@@ -340,6 +340,20 @@ int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
                        int64_t N, int64_t K, void *d, uint32_t flags, void *ws, size_t ws_bytes,
                        void *stream);
 
+/* grouped_gemm_mxfp8_swiglu_backward: the down projection's dgrad with the SwiGLU backward in its
+ * last stage.  dH = grouped_gemm_mxfp8's rows-grouped product of A [M, K] and the experts' B [f, K]
+ * (MOE4_GROUP_M, binary32), never written; instead dgu [M, 2f] bf16 receives
+ * moe4_swiglu_backward(gu, dH): dg = (dh * u) * (s * (1 + g * (1 - s))), du = dh * (g * s),
+ * s = 1 / (1 + exp(-g)), with g = gu[:, j], u = gu[:, f + j], each step one binary32 rounding,
+ * exactly as that call computes them [LHC kernels paragraph: element-wise work fused into the
+ * matrix multiplication's final stage].  gu [M, 2f] binary32 is read once.  f % 256 == 0,
+ * K % 128 == 0 and > 0, M % 128 == 0; gu, dgu 16-byte aligned; scales and ws as
+ * grouped_gemm_mxfp8 with N = f; flags: MOE4_SF_MMA_LAYOUT or 0. */
+int grouped_gemm_mxfp8_swiglu_backward(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
+                                       const uint8_t *b_e8, const int32_t *group_offs, int64_t E, int64_t M,
+                                       int64_t f, int64_t K, const float *gu, uint16_t *dgu, uint32_t flags,
+                                       void *ws, size_t ws_bytes, void *stream);
+
 /* grouped_gemm_mxfp8_wgrad_sgd: the contraction-grouped MXFP8 weight-gradient GEMM fused with
  * the FP32 master-weight update [LHC precisions: master weights in FP32; kernels paragraph:
  * fusing work into the final stage of the matrix multiplication].  For each expert e:

@@ -79,7 +79,14 @@ constexpr int EPI_W_TILE = 32 * TMA_CW<KIND> * 4;
 // SWI (the gate/up projection, NVFP4): each tile's 256 B rows are 128 gate rows and the matching
 // 128 up rows, so the epilogue holds gate and up of the same columns and writes GU and the SwiGLU
 // h = silu(g) * u (bf16) with its amax, as TMA does for D.
-enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4, EPI_SWI = 5 };
+// SWB (the down projection's dgrad, MXFP8): the epilogue applies the SwiGLU backward to the product
+// dH, reading GU through a two-chunk ring per warp and writing dGU (bf16); dH is not stored.
+enum EpiImpl : int { EPI_REG = 0, EPI_TMA = 1, EPI_SGD = 2, EPI_HMX = 3, EPI_SGD32 = 4, EPI_SWI = 5, EPI_SWB = 6 };
+// EPI_SWB ring, per epilogue warp: two buffers, each the gate and the up 32x16 binary32 chunk of
+// GU (64-byte rows, 64-byte swizzle); dg and du (32x16 bf16, 32-byte rows) are written over the
+// gate chunk and stored from there.
+constexpr int SWB_BUF = 4096;
+constexpr int SWB_WARP_BYTES = 2 * SWB_BUF;
 // EPI_SGD writes the bf16 copy, EPI_SGD32 only the binary32 master weights (and the amax).
 __host__ __device__ constexpr bool is_sgd(int em) { return em == EPI_SGD || em == EPI_SGD32; }
 template <int EM>
@@ -105,14 +112,17 @@ struct EpiCfg {
     // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
     // tile's MMAs overlap the previous tile's master-weight traffic
     static constexpr int BNT = is_sgd(EM) ? 128 : BN;
-    static constexpr int NST = is_sgd(EM) ? 4 : ((EM == EPI_TMA || EM == EPI_SWI) ? 3 : (EM == EPI_HMX ? 2 : STAGES));
+    static constexpr int NST =
+        is_sgd(EM) ? 4 : ((EM == EPI_TMA || EM == EPI_SWI || EM == EPI_SWB) ? 3 : (EM == EPI_HMX ? 2 : STAGES));
     // operand stages for a given operand kind: the MXFP8 TMA-store mode fits a fourth one
     template <int KIND>
     static constexpr int NSTK = (EM == EPI_TMA && KIND == 1) ? 4 : NST;
     template <int KIND>
     static constexpr int BYTESK =
         is_sgd(EM) ? 8 * SgdRing<EM>::WARP_BYTES
-                   : ((EM == EPI_TMA || EM == EPI_SWI) ? EPI_TMA_BYTES<KIND> : (EM == EPI_HMX ? EPI_HMX_BYTES : 0));
+                   : ((EM == EPI_TMA || EM == EPI_SWI) ? EPI_TMA_BYTES<KIND>
+                                                       : (EM == EPI_HMX ? EPI_HMX_BYTES
+                                                                        : (EM == EPI_SWB ? 8 * SWB_WARP_BYTES : 0)));
 };
 
 template <int KIND, int NST, int EPI, int BNT>
@@ -163,6 +173,7 @@ struct Args {
     unsigned int *had_amax; // bf16 output: max |Hadamard(128)-rotated rows| (binary32 bits), or null
     const int32_t *order;   // contraction-grouped: experts by decreasing group size, or null
     int64_t swiglu_f;       // EPI_SWI: the SwiGLU width f (B = W_gu [E, 2f, K]; tiles step 128 columns of f)
+    int64_t swb_f;          // EPI_SWB: f (GU and dGU are [M, 2f]; the up half starts at column f)
     uint16_t *h;            // EPI_SWI: h [M, f] bf16
     unsigned int *h_amax;   // EPI_SWI: max |h| as binary32 bits
     int64_t num_tiles;
@@ -573,6 +584,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_ph[2] = {0u, 0u};
         int acc = 0;
         uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
+        uint32_t swb_tile = 0, swb_issued = 0, swb_done = 0;  // SwiGLU backward: the same for its GU chunks
+        // SwiGLU backward (lane 0): chunk u of this warp's stream (tile u / 8 of the CTA, columns
+        // 16 * (u % 8) of the warp's 128) into buffer u % 2: the gate and the up pieces of GU.  The
+        // stores that read that buffer last (chunk u - 2's dg and du) must have read it out first.
+        auto swb_issue = [&](uint32_t u, const Tile &tt) {
+            const int b = (int)(u & 1u);
+            uint8_t *buf = smem + L::OFF_EPI + (warp - 4) * SWB_WARP_BYTES + b * SWB_BUF;
+            uint64_t *bar = epi_bar + 2 * (warp - 4) + b;
+            bulk_wait_read_all();
+            mbar_expect_tx(bar, SWB_BUF);
+            const int yy = (int)(tt.m0 + q * 32);
+            const int xx = (int)(tt.n0 + half * (BNT / 2) + 16 * (int)(u & 7u));
+            tma_load_2d(buf, &tmW, bar, xx, yy);
+            tma_load_2d(buf + SWB_BUF / 2, &tmW, bar, (int)(p.swb_f + xx), yy);
+        };
         for (int64_t t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
             const Tile tl = decode_tile<KIND, BNT>(p, t, ntiles);
             if (kSgd && tl.n_stages == 0) continue;  // an expert without rows: skipped by every role
@@ -580,7 +606,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // loaded ahead), decoded while the accumulator is still being produced
             int64_t tn = t + gridDim.x;
             Tile tn_l{};
-            if constexpr (kSgd) {
+            if constexpr (kSgd || EM == EPI_SWB) {
                 for (; tn < ntiles; tn += gridDim.x) {
                     tn_l = decode_tile<KIND, BNT>(p, tn, ntiles);
                     if (tn_l.n_stages > 0) break;
@@ -760,6 +786,93 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if ((sub & 1) == 0) p.e8[grow * (p.N / 32) + col / 32] = (uint8_t)(e + 127);
                 }
                 __syncwarp();  // the staging rows are rewritten by this warp's next tile
+            } else if constexpr (EM == EPI_SWB) {
+                // dGU = SwiGLU'(GU, dH) for this warp's rows 32q .. 32q + 31 and dH columns
+                // x0 .. x0 + 127 (gate columns of GU; the up columns are f further on), 16 columns a
+                // chunk: dg = (dh * u) * (s * (1 + g * (1 - s))), du = dh * (g * s), s = 1 / (1 +
+                // exp(-g)), each step one binary32 rounding, then bf16, as moe4_swiglu_backward
+                // computes them from dH.  The slab of dH goes to registers and the accumulator is
+                // handed back first; chunk u + 1's GU pieces load while chunk u is processed (the
+                // last chunk's successor is the next tile's first).
+                const int wi = warp - 4;
+                uint8_t *ringw = smem + L::OFF_EPI + wi * SWB_WARP_BYTES;
+                const int y0 = (int)(tl.m0 + q * 32);
+                const int x0 = (int)(tl.n0 + half * (BNT / 2));
+                const uint32_t u0 = swb_tile * 8;
+                if (swb_issued == u0) {  // not loaded ahead (the CTA's first tile)
+                    if (lane == 0) swb_issue(u0, tl);
+                    ++swb_issued;
+                }
+                uint32_t accr[128];
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tc_ld32_nw(tbase + (uint32_t)(c * 32), accr + 32 * c);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) accr[i] = 0;
+                }
+                tc_fence_before();
+                mbar_arrive(tmem_empty + acc);
+                bool ok = true;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t u = u0 + c;
+                    if (c + 1 < 8) {
+                        if (lane == 0) swb_issue(u + 1, tl);
+                        ++swb_issued;
+                    } else if (has_next) {
+                        if (lane == 0) swb_issue(u + 1, tn_l);
+                        ++swb_issued;
+                    }
+                    __syncwarp();
+                    const int b = (int)(u & 1u);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(epi_bar + 2 * wi + b, (u >> 1) & 1u, abort_flag));
+                    if (!ok) break;
+                    ++swb_done;
+                    uint8_t *gbuf = ringw + b * SWB_BUF;
+                    uint8_t *ubuf = gbuf + SWB_BUF / 2;
+                    float gv[16], uv[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int piece = (j ^ ((lane >> 1) & 3)) << 4;
+                        const float4 a4 = *reinterpret_cast<const float4 *>(gbuf + lane * 64 + piece);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(ubuf + lane * 64 + piece);
+                        gv[4 * j] = a4.x, gv[4 * j + 1] = a4.y, gv[4 * j + 2] = a4.z, gv[4 * j + 3] = a4.w;
+                        uv[4 * j] = b4.x, uv[4 * j + 1] = b4.y, uv[4 * j + 2] = b4.z, uv[4 * j + 3] = b4.w;
+                    }
+                    __syncwarp();  // every lane holds its gate row before dg is written over the chunk
+                    uint32_t og[8], ou[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) og[i] = ou[i] = 0u;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float dh = __uint_as_float(accr[16 * c + i]);
+                        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gv[i])));
+                        const float silu = __fmul_rn(gv[i], sg);
+                        const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gv[i], __fsub_rn(1.0f, sg))));
+                        og[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(__fmul_rn(dh, uv[i]), dsilu)) << (16 * (i & 1));
+                        ou[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(dh, silu)) << (16 * (i & 1));
+                    }
+                    // 32-byte bf16 rows, 32-byte swizzle: piece j of row l at j ^ ((l >> 2) & 1)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int piece = (j ^ ((lane >> 2) & 1)) << 4;
+                        *reinterpret_cast<uint4 *>(gbuf + lane * 32 + piece) =
+                            make_uint4(og[4 * j], og[4 * j + 1], og[4 * j + 2], og[4 * j + 3]);
+                        *reinterpret_cast<uint4 *>(gbuf + 1024 + lane * 32 + piece) =
+                            make_uint4(ou[4 * j], ou[4 * j + 1], ou[4 * j + 2], ou[4 * j + 3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmWb, gbuf, x0 + 16 * c, y0);
+                        tma_store_2d(&tmWb, gbuf + 1024, (int)(p.swb_f + x0 + 16 * c), y0);
+                        bulk_commit();
+                    }
+                }
+                ++swb_tile;
+                if (!ok) break;
             } else if constexpr (EM == EPI_SWI) {
                 // This warp: rows 32q .. 32q + 31, gate columns 64 * half .. + 63 of the tile
                 // (accumulator columns 64 * half ..) and the same columns of up (accumulator
@@ -956,12 +1069,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            if constexpr (EM != EPI_HMX && EM != EPI_TMA && EM != EPI_SWI) {  // those hand it back early
+            if constexpr (EM != EPI_HMX && EM != EPI_TMA && EM != EPI_SWI && EM != EPI_SWB) {  // those hand it back early
                 tc_fence_before();
                 mbar_arrive(tmem_empty + acc);
             }
             acc_ph[acc] ^= 1u;
             if (L::NACC == 2) acc ^= 1;
+        }
+        if constexpr (EM == EPI_SWB) {
+            // GU chunk loads the loop did not consume (it stopped early): let them land
+            if (lane == 0) {
+                for (uint32_t u = swb_done; u < swb_issued; ++u) {
+                    const uint32_t aa = smem_u32(epi_bar + 2 * (warp - 4) + (u & 1u));
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(aa, (u >> 1) & 1u) && clock64() - t0 < kWaitCycles) {
+                    }
+                }
+            }
         }
         if constexpr (kSgd) {
             // master-weight loads the loop did not consume (it stopped early): let them land
@@ -1466,6 +1590,50 @@ extern "C" int grouped_gemm_mxfp8(const uint8_t *a, const uint8_t *a_e8, const u
     CUtensorMap td;
     if (!make_out_map(&td, d, bf16, gk ? E * M : M, N, TMA_CW<1>)) return MOE4_ERR_CUDA;
     return launch<1, EPI_TMA>(ta, tb, td, td, g, st);
+}
+
+extern "C" int grouped_gemm_mxfp8_swiglu_backward(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,
+                                                  const uint8_t *b_e8, const int32_t *group_offs, int64_t E, int64_t M,
+                                                  int64_t f, int64_t K, const float *gu, uint16_t *dgu, uint32_t flags,
+                                                  void *ws, size_t ws_bytes, void *stream) {
+    MOE4_CHECK_ARG(E >= 1 && M >= 0 && M % BM == 0 && f > 0 && f % BN == 0 && K >= 0 && K % 128 == 0);
+    MOE4_CHECK_ARG(a && a_e8 && b && b_e8 && group_offs && gu && dgu);
+    MOE4_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(a_e8) && aligned16(b_e8) && aligned16(gu) &&
+                   aligned16(dgu));
+    MOE4_CHECK_ARG((flags & ~MOE4_SF_MMA_LAYOUT) == 0);
+    MOE4_CHECK_ARG(M < (int64_t(1) << 31) && E * f < (int64_t(1) << 31) && K < (int64_t(1) << 31));
+    if (M == 0) return MOE4_OK;
+    if (M > 0 && K > 0 && !(flags & MOE4_SF_MMA_LAYOUT) && !scales_ws_ok(M, E * f, K, 32, ws, ws_bytes))
+        return MOE4_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    if (K == 0) return MOE4_ERR_UNSUPPORTED;  // an empty contraction: dH = 0, not this kernel's case
+    const uint8_t *sfa, *sfb;
+    int rc = stage_scales(a_e8, M, b_e8, E * f, K, 32, flags, ws, ws_bytes, &sfa, &sfb, st);
+    if (rc != MOE4_OK) return rc;
+    CUtensorMap ta, tb, tgu, tdgu;
+    if (!make_map(&ta, a, K, M, BM) || !make_map(&tb, b, K, E * f, BN)) return MOE4_ERR_CUDA;
+    // GU read and dGU written in 32-row x 16-column chunks
+    if (!make_out_map(&tgu, const_cast<float *>(gu), false, M, 2 * f, 16) ||
+        !make_out_map(&tdgu, dgu, true, M, 2 * f, 16))
+        return MOE4_ERR_CUDA;
+    Args g{};
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.offs = group_offs;
+    g.E = (int)E;
+    g.group_k = 0;
+    g.M = M;
+    g.N = f;
+    g.K = K;
+    g.d = dgu;
+    g.mode = BF16;
+    g.swb_f = f;
+    g.n_tiles_m = (int)(M / BM);
+    g.n_tiles_n = (int)(f / BN);
+    g.num_tiles = (int64_t)g.n_tiles_m * g.n_tiles_n;
+    g.sfa_tile_stride = K / 128;
+    g.sfb_tile_stride = K / 128;
+    return launch<1, EPI_SWB>(ta, tb, tgu, tdgu, g, st);
 }
 
 extern "C" int grouped_gemm_mxfp8_wgrad_sgd(const uint8_t *a, const uint8_t *a_e8, const uint8_t *b,

@@ -73,6 +73,8 @@ _SIGNATURES = {
     "grouped_expert_gemm_nvfp4_hadamard_mx": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                       _vp, _vp, _u32, _vp, _sz, _vp]),
     "grouped_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _u32, _vp, _sz, _vp]),
+    "grouped_gemm_mxfp8_swiglu_backward": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _u32,
+                                                  _vp, _sz, _vp]),
     "grouped_gemm_mxfp8_wgrad_sgd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _f32, _vp,
                                             _u32, _vp, _sz, _vp]),
     "moe4_sf_to_mma_layout": (_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
@@ -271,6 +273,12 @@ def grouped_gemm_mxfp8(a, a_e8, b, b_e8, group_offs, E, M, N, K, d, flags=OUT_F3
                        stream=None):
     _call("grouped_gemm_mxfp8", _p(a), _p(a_e8), _p(b), _p(b_e8), _p(group_offs), E, M, N, K, _p(d), flags,
           _p(ws), _ws_bytes(ws), _s(stream))
+
+
+def grouped_gemm_mxfp8_swiglu_backward(a, a_e8, b, b_e8, group_offs, E, M, f, K, gu, dgu, flags=0, ws=None,
+                                       stream=None):
+    _call("grouped_gemm_mxfp8_swiglu_backward", _p(a), _p(a_e8), _p(b), _p(b_e8), _p(group_offs), E, M, f, K, _p(gu),
+          _p(dgu), flags, _p(ws), _ws_bytes(ws), _s(stream))
 
 
 def grouped_gemm_mxfp8_wgrad_sgd(a, a_e8, b, b_e8, group_offs, E, M, N, K, w32, w_bf16, lr, amax_out, flags=0,

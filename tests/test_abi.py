@@ -83,6 +83,14 @@ MISALIGNED = FAKE + 4
                                                  None, 0, None, 0, None)),                    # no amax_out
     ("grouped_expert_gemm_nvfp4_hadamard_amax", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE,
                                                  FAKE, 0x200, None, 0, None)),                # output flag
+    ("grouped_gemm_mxfp8_swiglu_backward", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, 256, FAKE, FAKE, 0, None, 0,
+                                            None)),                                           # f % 256
+    ("grouped_gemm_mxfp8_swiglu_backward", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, None, FAKE, 0, None, 0,
+                                            None)),                                           # no gu
+    ("grouped_gemm_mxfp8_swiglu_backward", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE, MISALIGNED, 0,
+                                            None, 0, None)),                                  # dgu alignment
+    ("grouped_gemm_mxfp8_swiglu_backward", (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 256, FAKE, FAKE, 0x1000,
+                                            None, 0, None)),                                  # bad flag
     ("grouped_expert_gemm_nvfp4_swiglu", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 192, 256, FAKE, FAKE,
                                           FAKE, 0, None, 0, None)),                           # f % 128
     ("grouped_expert_gemm_nvfp4_swiglu", (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, 256, FAKE, None,

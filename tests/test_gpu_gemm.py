@@ -556,3 +556,68 @@ def test_nvfp4_gate_up_with_swiglu_layer_shape():
     got, want = _swiglu_pair(xpc, xps, xg, wc, ws_, wg, offs, E, Rp, f, d, moe4.SF_MMA_LAYOUT)
     for a, b, name in zip(got, want, ("GU", "h", "amax")):
         assert torch.equal(a, b), name
+
+
+def _swb_pair(aq, ae, bq, be, offs, E, M, f, K, gu, flags):
+    """The fused dgrad + SwiGLU backward and the dgrad (binary32 dH) followed by moe4_swiglu_backward."""
+    ws = moe4.workspace(moe4.moe4_workspace_size_gemm(1, M, E, f, K))
+    dh = torch.empty((M, f), dtype=torch.float32, device=DEV)
+    moe4.grouped_gemm_mxfp8(aq, ae, bq, be, offs, E, M, f, K, dh, moe4.OUT_F32 | moe4.GROUP_M | flags, ws)
+    want = torch.empty((M, 2 * f), dtype=torch.int16, device=DEV)
+    moe4.moe4_swiglu_backward(gu, dh, M, f, want)
+    got = torch.full((M, 2 * f), -1, dtype=torch.int16, device=DEV)
+    moe4.grouped_gemm_mxfp8_swiglu_backward(aq, ae, bq, be, offs, E, M, f, K, gu, got, flags, ws)
+    torch.cuda.synchronize()
+    assert moe4.moe4_get_status() == moe4.OK
+    return got, want
+
+
+@pytest.mark.parametrize("sf_mma", [False, True])
+def test_mxfp8_dgrad_with_swiglu_backward_equals_unfused(sf_mma):
+    """grouped_gemm_mxfp8_swiglu_backward against the rows-grouped dgrad (binary32 dH) followed by
+    moe4_swiglu_backward, bit for bit: four experts (one empty), f = 512 (two 256-column tiles),
+    K = 640, GU with values across the sigmoid's range."""
+    rng = np.random.default_rng(71)
+    sizes, f, K = [256, 0, 128, 384], 512, 640
+    E, offs = len(sizes), _offs(sizes)
+    M = int(offs[-1])
+    a_bits = _bf16(rng, (M, K))
+    b_bits = _bf16(rng, (E * f, K), 0.02)
+    aq, ae = _mxfp8_rowwise(a_bits, M, K)
+    bq, be = _mxfp8_rowwise(b_bits, E * f, K)
+    flags = 0
+    if sf_mma:
+        ae2, be2 = torch.empty_like(ae), torch.empty_like(be)
+        moe4.moe4_sf_to_mma_layout(ae, 1, M, K // 32, ae2)
+        moe4.moe4_sf_to_mma_layout(be, 1, E * f, K // 32, be2)
+        ae, be, flags = ae2, be2, moe4.SF_MMA_LAYOUT
+    gu = to_dev((rng.standard_normal((M, 2 * f)) * 3).astype(np.float32))
+    got, want = _swb_pair(aq, ae, bq, be, to_dev(offs), E, M, f, K, gu, flags)
+    assert torch.equal(got, want), int((got != want).sum())
+
+
+def test_mxfp8_dgrad_with_swiglu_backward_layer_shape():
+    """The layer step's down-projection dgrad (160k padded rows over 384 experts of a top-8 plan,
+    f = 2048, d_model 4096) with the SwiGLU backward: equal to the unfused pair over the whole dGU."""
+    T, d, f, E, k = 16384, 4096, 2048, 384, 8
+    rng = np.random.default_rng(2)
+    lg = (rng.standard_normal((T, E)) + rng.standard_normal(E)).astype(np.float32)
+    idx, _ = oracle.route_topk(lg, k)
+    rows_cap = T * k + 127 * E
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    src_of = torch.empty(rows_cap, dtype=torch.int32, device=DEV)
+    moe4.moe4_permute_plan(to_dev(idx), T, k, E, offs, row_of, src_of, rows_cap,
+                           moe4.workspace(moe4.moe4_workspace_size(moe4.OP_PERMUTE_PLAN, T, k, E)))
+    torch.cuda.synchronize()
+    M = int(to_np(offs)[-1])
+    dy = inputs.device_normal((M, d), 1.0, inputs.device_generator(23, 0, DEV), DEV).view(torch.int16)
+    w = inputs.device_normal((E * f, d), 0.02, inputs.device_generator(23, 1, DEV), DEV).view(torch.int16)
+    aq, ae = empty_u8(M, d), empty_u8(M, d // 32)
+    moe4.mxfp8_quantize(dy, M, d, aq, ae, 0, 0, moe4.ROWWISE)
+    bq, be = empty_u8(E * f, d), empty_u8(E * f, d // 32)
+    moe4.mxfp8_quantize(w, E * f, d, bq, be, 0, 0, moe4.ROWWISE)
+    del dy, w
+    gu = inputs.device_normal((M, 2 * f), 2.0, inputs.device_generator(23, 2, DEV), DEV, dtype=torch.float32)
+    got, want = _swb_pair(aq, ae, bq, be, offs, E, M, f, d, gu, 0)
+    assert torch.equal(got, want), int((got != want).sum())
