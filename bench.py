@@ -60,7 +60,7 @@ WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
 # DRAM bytes per step of the kernel groups, read + written, from a one-pass ncu capture of this
 # layer step at full size (dram__bytes_read.sum + dram__bytes_write.sum over the two launches of
 # the second timed step): profiles/layer_step_dram_bytes.md
-DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.205e9}
+DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.215e9}
 MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "hadamard", "mxfp8_quant"}
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2,
                   "quant_w": 4 * WEIGHT_CHUNKS}  # two launches per chunk, WEIGHT_CHUNKS chunks per projection
