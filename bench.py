@@ -6,8 +6,9 @@ tokens, d_model 4096, SwiGLU width 2048, 384 experts, top-8 of N(0,1) logits plu
 N(0,1) bias, Student-t(3) activations, N(0, 0.02) expert weights held as FP32 masters):
 
   forward   top-k routing and dispatch plan; NVFP4 (Four Over Six) quantisation of X, of every
-            expert's gate/up and down weights (per-expert scales) and of H; NVFP4 row gather;
-            grouped NVFP4 GEMMs (gate/up, then down) with SwiGLU between them; Hadamard(128) NVFP4
+            expert's gate/up and down weights (per-expert scales; the weight path pipelined over
+            expert chunks on two streams) and of H; NVFP4 row gather; grouped NVFP4 GEMMs (gate/up
+            with the SwiGLU and the amax of H in its last stage, then down); Hadamard(128) NVFP4
             return-path encode (its amax from the down GEMM), then decode and weighted combine in
             one pass;
   backward  combine gradient; MXFP8 quantisation of dY and dGU (row-wise and transposed);
