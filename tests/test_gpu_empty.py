@@ -56,6 +56,15 @@ def test_quantisers_and_codecs_on_zero_rows():
     moe4.hadamard_quant(x, 0, 128, codes, sf, None, moe4.MXFP8)
     moe4.hadamard_dequant(codes, sf, None, 0, 128, out, moe4.MXFP8)
     assert untouched(codes, sf, out)
+    # the weight path on matrices of no rows, whole and as its split, shared-SM passes on a slice
+    q, e8, gw = buf(), buf(), buf(16)
+    wf = moe4.FOUR_OVER_SIX | moe4.SR
+    moe4.nvfp4_quantize_f32_requant(x, 2, 0, 64, f32(2, 1.0), codes, sf, gw, q, e8, 1, 3, None, wf)
+    moe4.nvfp4_quantize_f32_requant(x, 2, 0, 64, f32(2, 1.0), codes, sf, gw, q, e8, 1, 3, None,
+                                    wf | moe4.PASS_QUANT | moe4.SHARE_SMS, mat_base=5)
+    moe4.nvfp4_quantize_f32_requant(x, 2, 0, 64, f32(2, 1.0), codes, sf, gw, q, e8, 1, 3, None,
+                                    wf | moe4.PASS_REQUANT, mat_base=5)
+    assert untouched(codes, sf, gw, q, e8)
 
 
 def test_moe_steps_on_zero_tokens_and_rows():
@@ -93,6 +102,14 @@ def test_gemms_with_no_rows_or_no_contraction():
                                    moe4.OUT_F32, ws)
     moe4.grouped_gemm_mxfp8(buf(), buf(), buf(), buf(), offs0, E, 0, N, K, d, moe4.OUT_F32 | moe4.GROUP_M, ws)
     assert untouched(d)
+    # the gate/up GEMM with the SwiGLU and the down dgrad with its backward, on no rows: nothing
+    # written but the amax of the empty h, 0
+    h, dgu = buf(1 << 16), buf(1 << 16)
+    hmax = f32(1, -1.0)
+    moe4.grouped_expert_gemm_nvfp4_swiglu(buf(), buf(), f32(1, 1.0), buf(), buf(), f32(E, 1.0), offs0, E, 0, 128, K,
+                                          d, h, hmax, 0, ws)
+    moe4.grouped_gemm_mxfp8_swiglu_backward(buf(), buf(), buf(), buf(), offs0, E, 0, N, K, buf(), dgu, 0, ws)
+    assert untouched(d, h, dgu) and float(to_np(hmax)[0]) == 0.0
     # every group empty along the contraction: D = 0
     M = 128
     dk = torch.full((E, M, N), 5.0, dtype=torch.float32, device=DEV)
