@@ -222,7 +222,8 @@ int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *sf, const fl
  * MOE4_SHARE_SMS runs the quantiser on a small grid that holds part of each SM only, so that a
  * requantiser launched beside it on another stream (another matrix set's MOE4_PASS_REQUANT) runs
  * on the rest of every SM at the same time: the quantiser's memory waits and the requantiser's
- * arithmetic then overlap.  The outputs do not depend on these flags. */
+ * arithmetic then overlap.  The outputs do not depend on these flags.  With rows == 0 the call
+ * writes nothing (g_dec included) and returns MOE4_OK. */
 int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t rows, int64_t cols,
                                const float *amax_in, uint8_t *codes, uint8_t *sf, float *g_dec,
                                uint8_t *q_t, uint8_t *e8_t, uint64_t seed, uint32_t stream_id,
