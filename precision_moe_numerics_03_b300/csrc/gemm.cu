@@ -109,8 +109,8 @@ template <int KIND>
 constexpr int EPI_TMA_BYTES = 8 * EPI_W_TILE<KIND>;
 template <int EM>
 struct EpiCfg {
-    // fused SGD: 128-column tiles, so two binary32 accumulators fit in tensor memory and a
-    // tile's MMAs overlap the previous tile's master-weight traffic
+    // fused SGD: 128-column tiles, so three binary32 accumulators fit in tensor memory and a
+    // tile's MMAs overlap the two previous tiles' master-weight traffic
     static constexpr int BNT = is_sgd(EM) ? 128 : BN;
     static constexpr int NST =
         is_sgd(EM) ? 4 : ((EM == EPI_TMA || EM == EPI_SWI || EM == EPI_SWB) ? 3 : (EM == EPI_HMX ? 2 : STAGES));
@@ -137,8 +137,8 @@ struct Layout {
     static constexpr int OFF_SFB = OFF_SFA + NST * SFA;
     static constexpr int OFF_EPI = (OFF_SFB + NST * SFB + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI;
-    // full, empty, tmem_full[2], tmem_empty[2], drain, epilogue
-    static constexpr int NBAR = 2 * NST + 5 + 8 * SGD_NB_MAX;
+    // full, empty, tmem_full[3], tmem_empty[3], drain, epilogue
+    static constexpr int NBAR = 2 * NST + 7 + 8 * SGD_NB_MAX;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;    // room to align the base to 1024
@@ -147,7 +147,11 @@ struct Layout {
     static constexpr int SF_COLS_A = Cfg<KIND>::ATOMS * 4;
     static constexpr int SF_COLS_B = Cfg<KIND>::ATOMS * 4 * RT;
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr int NACC = 2 * BNT + NST * SF_COLS <= TMEM_COLS ? 2 : 1;
+    // three accumulators where they fit (the fused SGD's 128-column tiles): the MMAs of a long
+    // contraction can then start while the epilogue still streams two earlier tiles' weights
+    static constexpr int NACC = (BNT == 128 && 3 * BNT + NST * SF_COLS <= TMEM_COLS)
+                                    ? 3
+                                    : (2 * BNT + NST * SF_COLS <= TMEM_COLS ? 2 : 1);
     static constexpr int SF_BASE = NACC * BNT;
     static_assert(SF_BASE + NST * SF_COLS <= TMEM_COLS, "tensor memory overflow");
     static_assert(SMEM <= 232448, "shared memory overflow");
@@ -431,8 +435,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars, *empty = bars + NST;
     // per accumulator buffer: tmem_full (MMA done) and tmem_empty (epilogue has read it)
-    uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 2, *drain = tmem_full + 4;
-    uint64_t *epi_bar = tmem_full + 5;  // fused SGD: Ring::NB per epilogue warp
+    uint64_t *tmem_full = bars + 2 * NST, *tmem_empty = tmem_full + 3, *drain = tmem_full + 6;
+    uint64_t *epi_bar = tmem_full + 7;  // fused SGD: Ring::NB per epilogue warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -447,7 +451,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(tmem_full + i, 1);
             mbar_init(tmem_empty + i, EPI_THREADS);
         }
@@ -518,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------------------- MMA issuer
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t acc_ph[2] = {0u, 0u};
+        uint32_t acc_ph[3] = {0u, 0u, 0u};
         int acc = 0;  // accumulator buffer of this tile
         const uint32_t a_base = smem_u32(smem + L::OFF_A), b_base = smem_u32(smem + L::OFF_B);
         const uint32_t sfa_base = smem_u32(smem + L::OFF_SFA), sfb_base = smem_u32(smem + L::OFF_SFB);
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_commit(tmem_full + acc);
             }
             acc_ph[acc] ^= 1u;
-            if (L::NACC == 2) acc ^= 1;
+            if (++acc == L::NACC) acc = 0;
         }
         // all of this thread's MMAs and copies complete before tensor memory is freed
         tc_commit(drain);
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // warp w reads TMEM lanes 32*(w%4).. (its rows) and half (w-4)/4 of the tile's columns
         const int q = warp & 3;
         const int half = (warp - 4) >> 2;
-        uint32_t acc_ph[2] = {0u, 0u};
+        uint32_t acc_ph[3] = {0u, 0u, 0u};
         int acc = 0;
         uint32_t sgd_tile = 0, sgd_issued = 0, sgd_done = 0;  // fused SGD: tiles, chunk loads issued / consumed
         uint32_t swb_tile = 0, swb_issued = 0, swb_done = 0;  // SwiGLU backward: the same for its GU chunks
@@ -1074,7 +1078,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive(tmem_empty + acc);
             }
             acc_ph[acc] ^= 1u;
-            if (L::NACC == 2) acc ^= 1;
+            if (++acc == L::NACC) acc = 0;
         }
         if constexpr (EM == EPI_SWB) {
             // GU chunk loads the loop did not consume (it stopped early): let them land
