@@ -372,15 +372,20 @@ __device__ __forceinline__ Tile decode_tile(const Args &p, int64_t t, int64_t nt
         tl.k_begin = 0;
         tl.n_stages = (int)(p.K / Cfg<KIND>::ELEMS);
     } else {
-        // With an expert order, tiles are listed expert by expert in decreasing group size and
+        // With an expert order, tiles are listed expert by expert in decreasing group size, and
         // slot t = c + G*i (CTA c of G, its i-th tile) takes the list's next entry from the front
-        // when c + i is even and from the back otherwise: at any time half the CTAs work on long
-        // contractions (operand-bound) and half on short ones (master-weight-bound), and each CTA
-        // alternates.  For even G this maps slots onto the ntiles list positions one to one (the
-        // fused SGD lists only the experts that have rows).
+        // when t is a multiple of 3 and from the back otherwise: front slot t is list position
+        // t / 3, back slot t position ntiles - 1 - (t - ceil(t / 3)), one to one for any ntiles.
+        // With G not a multiple of 3 each CTA then runs one tile of a long contraction
+        // (operand-bound) between two of short ones (master-weight-bound), and at any time a third
+        // of the CTAs work on the front.  Otherwise, for even G, slot t takes the front when c + i
+        // is even (each CTA alternates; position i * G/2 + c/2 from its end).  The fused SGD lists
+        // only the experts that have rows.
         const uint32_t per_e = (uint32_t)p.n_tiles_m * ntn;
         uint32_t l = t32;
-        if (p.order != nullptr && (gridDim.x & 1u) == 0) {
+        if (p.order != nullptr && gridDim.x % 3u != 0) {
+            l = t32 % 3u == 0 ? t32 / 3u : (uint32_t)ntiles - 1 - (t32 - (t32 + 2u) / 3u);
+        } else if (p.order != nullptr && (gridDim.x & 1u) == 0) {
             const uint32_t G = gridDim.x, i = t32 / G, c = t32 - i * G;
             const uint32_t fi = i * (G / 2) + c / 2;
             l = ((c + i) & 1) == 0 ? fi : (uint32_t)ntiles - 1 - fi;
