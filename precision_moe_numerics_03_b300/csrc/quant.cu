@@ -110,8 +110,21 @@ __device__ __forceinline__ void fill_scale_tab(float2 *tab) {
 template <int M>  // the candidate's target for the block amax: 6 or 4
 __device__ __forceinline__ float nvfp4_candidate(const float y[16], float a, const float2 *tab, uint32_t &w0,
                                                  uint32_t &w1, uint32_t &scode) {
-    // a/4 is a power-of-two scaling: the product by 0.25 rounds the same real number
-    const float t = M == 4 ? __fmul_rn(a, 0.25f) : __fdiv_rn(a, (float)M);
+    // a/4 is a power-of-two scaling: the product by 0.25 rounds the same real number.  a/6 is
+    // formed by Markstein's correction step (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with
+    // y = RN(1/6), q0 = RN(a*y), r = RN(a - 6*q0) in one fma, t = RN(q0 + r*y).  t is not always
+    // RN(a/6) (it differs in the last place for about 0.03% of normal a), but its E4M3 code, the
+    // only use of t, is that of RN(a/6) for every binary32 a >= 0 (checked exhaustively against
+    // the division); a is clamped to FLT_MAX so that +inf keeps the saturated code of inf / 6.
+    float t;
+    if constexpr (M == 4) {
+        t = __fmul_rn(a, 0.25f);
+    } else {
+        static_assert(M == 6, "candidates 4 and 6");
+        const float am = fminf(a, FLT_MAX), y = __uint_as_float(0x3E2AAAABu);
+        const float q0 = __fmul_rn(am, y);
+        t = __fmaf_rn(__fmaf_rn(-q0, 6.0f, am), y, q0);
+    }
     scode = e4m3_rn(t);  // t >= 0 (or NaN): codes 0..0x7F
     const float2 sv = tab[scode];
     const float sfv = sv.x;
