@@ -56,12 +56,11 @@ SMALL = dict(T=4096, d=2048, f=1024, E=8, k=2)
 METRIC = "expert NVFP4 GEMM TFLOPS + requant GB/s, as % of B300 roofline"
 LR = 1e-3
 WEIGHT_CHUNKS = 4  # expert chunks per projection in the weight path's pipeline
-# DRAM bytes / algorithmic bytes of a kernel, from one ncu capture of that kernel on a 16-expert
-# case (profiles/<kernel>_16experts.md); a kernel changed since its capture has no entry.
 # DRAM bytes per step of the kernel groups, read + written, from a one-pass ncu capture of this
-# layer step at full size (dram__bytes_read.sum + dram__bytes_write.sum over the two launches of
-# the second timed step): profiles/layer_step_dram_bytes.md
-DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 71.215e9}
+# layer step at full size (dram__bytes_read.sum + dram__bytes_write.sum of the group's launches,
+# averaged over the two timed steps): profiles/layer_step_dram_bytes.md.  A kernel changed since
+# its capture has no entry.
+DRAM_PER_STEP = {"gemm_mxfp8_wgrad_sgd": 72.216e9}
 MULTI_KERNEL_GROUPS = {"quant_w", "route", "quant_x", "hadamard", "mxfp8_quant"}
 GROUP_LAUNCHES = {"gemm_mxfp8_wgrad_sgd": 2, "requant": 2, "gemm_nvfp4": 2, "gemm_mxfp8_dgrad": 2,
                   "quant_w": 4 * WEIGHT_CHUNKS}  # two launches per chunk, WEIGHT_CHUNKS chunks per projection
