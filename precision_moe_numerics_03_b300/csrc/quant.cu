@@ -197,12 +197,54 @@ __device__ __forceinline__ void nvfp4_block(const float y[16], bool four_over_si
 }
 
 
-// One thread per 16-value block.  amax per matrix from amax_in (given) or amax_bits (pass 1).
-// The block index b runs over all matrices; with contiguous rows (ld == cols) the input, code and
-// canonical-scale offsets are b*16, b*8 and b, and the matrix index only moves forward in the
-// grid-stride loop, so no division is needed on that path.
+// A block's 16 inputs as loaded (binary32: four float4; bf16: two uint4), kept apart from their
+// conversion to bf16 pairs so that two blocks' loads can be issued before either is used.
 template <typename TIn>
-__global__ void __launch_bounds__(256) nvfp4_quant_kernel(
+struct RawBlock;
+template <>
+struct RawBlock<float> {
+    float4 v[4];
+};
+template <>
+struct RawBlock<uint16_t> {
+    uint4 v[2];
+};
+template <typename TIn>
+__device__ __forceinline__ void raw_load(RawBlock<TIn> &r, const TIn *p, bool ok) {
+    if constexpr (sizeof(TIn) == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            r.v[i] = ok ? __ldg(reinterpret_cast<const float4 *>(p) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) r.v[i] = ok ? __ldg(reinterpret_cast<const uint4 *>(p) + i) : make_uint4(0, 0, 0, 0);
+    }
+}
+// Eight bf16 pairs (element 2i in the low half of word i): bf16 input as stored, binary32 input
+// rounded to bf16 (nearest-even), as load8_bf16 forms them.
+template <typename TIn>
+__device__ __forceinline__ void raw_words(const RawBlock<TIn> &r, uint32_t w[8]) {
+    if constexpr (sizeof(TIn) == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[2 * i] = bf16x2_rn(r.v[i].x, r.v[i].y);
+            w[2 * i + 1] = bf16x2_rn(r.v[i].z, r.v[i].w);
+        }
+    } else {
+        const uint32_t a[8] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = a[i];
+    }
+}
+
+// One thread per 16-value block, two blocks (b and b + stride of the grid-stride loop) per
+// iteration: both blocks' loads are issued first, so each warp has twice the bytes in flight.
+// amax per matrix from amax_in (given) or amax_bits (pass 1).  The block index b runs over all
+// matrices; with contiguous rows (ld == cols) the input, code and canonical-scale offsets are
+// b*16, b*8 and b, and the matrix index only moves forward in the loop, so no division is needed
+// on that path.  At most 80 registers: two CTAs of it and two of the requantiser share an SM.
+template <typename TIn>
+__global__ void __maxnreg__(80) nvfp4_quant_kernel(
     const TIn *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
@@ -223,21 +265,28 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
         g_dec[gtid] = global_scale(am).dec;
     }
     const bool contiguous = (ld == cols);
-    int64_t m = -1, mat_begin = 0, mat_end = 0;
-    float g_enc = 1.0f;
-    bool skip = false;
-    for (int64_t b = gtid; b < total; b += (int64_t)gridDim.x * blockDim.x) {
-        if (b >= mat_end) {
-            m = b / per_mat;
-            mat_begin = m * per_mat;
-            mat_end = mat_begin + per_mat;
-            const float am = amax_in ? amax_in[m] : __uint_as_float(amax_bits[m]);
-            g_enc = global_scale(am).enc;
-            skip = skipped(m);
+    // the matrix of a block: index, first block, end, encode scale, skipped
+    struct Mat {
+        int64_t m, begin, end;
+        float g_enc;
+        bool skip;
+    };
+    auto enter = [&](Mat &s, int64_t bb) {
+        if (bb >= s.end) {
+            s.m = bb / per_mat;
+            s.begin = s.m * per_mat;
+            s.end = s.begin + per_mat;
+            const float am = amax_in ? amax_in[s.m] : __uint_as_float(amax_bits[s.m]);
+            s.g_enc = global_scale(am).enc;
+            s.skip = skipped(s.m);
         }
-        if (skip) continue;
-        const int64_t rem = b - mat_begin;
-        int64_t row = 0, blk = 0;
+    };
+    // row and block of bb within its matrix (the tile-layout scale offset and, with strided rows,
+    // the input address need them)
+    auto locate = [&](const Mat &s, int64_t bb, int64_t &row, int64_t &blk) {
+        const int64_t rem = bb - s.begin;
+        row = 0;
+        blk = 0;
         if (sf_mma) {
             // nblk % 4 == 0 here: rem / nblk = (rem / 4) / (nblk / 4) by multiply and shift
             row = (int64_t)(uint32_t)(((uint64_t)((uint32_t)rem >> 2) * div_m) >> div_s);
@@ -246,21 +295,45 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(
             row = (int64_t)((uint32_t)rem / (uint32_t)nblk);
             blk = rem - row * nblk;
         }
-        const TIn *srcp = contiguous ? x + b * 16 : x + m * mat_stride + row * ld + blk * 16;
-        const uint4 q0 = load8_bf16(srcp), q1 = load8_bf16(srcp + 8);
-        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    };
+    auto source = [&](const Mat &s, int64_t bb, int64_t row, int64_t blk) -> const TIn * {
+        return contiguous ? x + bb * 16 : x + s.m * mat_stride + row * ld + blk * 16;
+    };
+    auto quantise = [&](const Mat &s, int64_t bb, int64_t row, int64_t blk, const uint32_t wv[8]) {
         // packed products: y feeds the amax, a product and the addend of an FMA, never an add
         float y[16];
-        const uint64_t g2 = f2_pack(g_enc, g_enc);
+        const uint64_t g2 = f2_pack(s.g_enc, s.g_enc);
 #pragma unroll
         for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(f2_pack(bf16_lo(wv[i]), bf16_hi(wv[i])), g2), y[2 * i], y[2 * i + 1]);
         uint32_t w0, w1, scode;
         nvfp4_block(y, four_over_six, tab, w0, w1, scode);
-        *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(w0, w1);
+        *reinterpret_cast<uint2 *>(codes + bb * 8) = make_uint2(w0, w1);
         if (sf_mma)
-            sf[mat_begin + sf_mma_offset(row, blk, nblk)] = (uint8_t)scode;
+            sf[s.begin + sf_mma_offset(row, blk, nblk)] = (uint8_t)scode;
         else
-            sf[b] = (uint8_t)scode;
+            sf[bb] = (uint8_t)scode;
+    };
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    Mat s{-1, 0, 0, 1.0f, false};
+    for (int64_t b = gtid; b < total; b += 2 * stride) {
+        const int64_t b2 = b + stride;
+        enter(s, b);
+        Mat s2 = s;
+        const bool two = b2 < total;
+        if (two) enter(s2, b2);
+        const bool l1 = !s.skip, l2 = two && !s2.skip;
+        int64_t r1, k1, r2, k2;
+        locate(s, b, r1, k1);
+        locate(s2, b2, r2, k2);
+        RawBlock<TIn> ra, rb;
+        raw_load(ra, source(s, b, r1, k1), l1);
+        raw_load(rb, source(s2, b2, r2, k2), l2);
+        uint32_t wa[8], wb[8];
+        raw_words(ra, wa);
+        raw_words(rb, wb);
+        if (l1) quantise(s, b, r1, k1, wa);
+        if (l2) quantise(s2, b2, r2, k2, wb);
+        s = s2;  // the next b lies past b2: its matrix is found from b2's
     }
 }
 
