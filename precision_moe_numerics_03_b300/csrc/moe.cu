@@ -231,7 +231,9 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const float *__restrict
             uint32_t og[2] = {0, 0}, ou[2] = {0, 0};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
+                // RN(1 / x) by the reciprocal intrinsic: the same correctly rounded value as the
+                // division of 1 by x
+                const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-gs[i])));
                 const float silu = __fmul_rn(gs[i], sg);
                 const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
                 const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);

@@ -430,3 +430,34 @@ def test_quantize_subnormal_inputs(fos):
     b[5, 160] = 3.0
     xb = inputs.to_bf16_bits(np.stack([a, b]))
     _check_quant(xb, 2, 64, 256, fos=fos)
+
+
+@pytest.mark.parametrize("f32,mma", [(False, False), (False, True), (True, False), (True, True)])
+def test_quantize_strided_rows_several_blocks_per_thread(f32, mma):
+    """Padded rows (ld > cols) on a stack large enough that every thread of the quantiser's grid
+    takes several blocks, two per loop iteration, pairs crossing matrix boundaries: codes, scales
+    (canonical or tile layout) and g_dec against the oracle, bit for bit."""
+    nmat, rows, cols, ld = 5, 2048, 2048, 2080
+    rng = np.random.default_rng(71 + 2 * f32 + mma)
+    x = rng.standard_t(3, (nmat, rows, cols)).astype(np.float32)
+    x *= np.exp2(rng.integers(-6, 6, (nmat, 1, 1))).astype(np.float32)
+    xb = oracle.f32_to_bf16(x)
+    pad = np.zeros((nmat, rows, ld), np.float32 if f32 else np.uint16)
+    pad[:, :, :cols] = x if f32 else xb
+    c, s = empty_u8(nmat, rows, cols // 2), empty_u8(nmat, rows, cols // 16)
+    g = torch.empty(nmat, dtype=torch.float32, device=DEV)
+    flags = moe4.FOUR_OVER_SIX | (moe4.SF_MMA_LAYOUT if mma else 0)
+    ws = moe4.workspace(moe4.moe4_workspace_size(moe4.OP_NVFP4_QUANTIZE, nmat))
+    quant = moe4.nvfp4_quantize_f32 if f32 else moe4.nvfp4_quantize
+    quant(to_dev(pad), nmat, rows, cols, ld, c, s, g, None, flags, ws)
+    torch.cuda.synchronize()
+    rc, rs, rg = oracle.nvfp4_quantize(oracle.bf16_to_f32(xb))
+    assert first_mismatch(to_np(g), rg) is None
+    assert first_mismatch(to_np(c), rc) is None
+    if mma:
+        s2 = empty_u8(nmat, rows, cols // 16)
+        moe4.moe4_sf_to_mma_layout(to_dev(rs), nmat, rows, cols // 16, s2)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(s), to_np(s2))
+    else:
+        assert first_mismatch(to_np(s), rs) is None
