@@ -857,7 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float dh = __uint_as_float(accr[16 * c + i]);
-                        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gv[i])));
+                        const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-gv[i])));
                         const float silu = __fmul_rn(gv[i], sg);
                         const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gv[i], __fsub_rn(1.0f, sg))));
                         og[i >> 1] |= (uint32_t)f32_to_bf16_bits(__fmul_rn(__fmul_rn(dh, uv[i]), dsilu)) << (16 * (i & 1));

@@ -302,7 +302,7 @@ requant_transpose_kernel(
                     uint32_t dgb[4], dub[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gs[i])));
+                        const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-gs[i])));
                         const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gs[i], __fsub_rn(1.0f, sg))));
                         const float dgv = __fmul_rn(__fmul_rn(ds[i], us[i]), dsilu);
                         const float duv = __fmul_rn(ds[i], __fmul_rn(gs[i], sg));
