@@ -181,11 +181,17 @@ def test_mxfp8_wgrad_group_k(accumulate):
 
 
 @pytest.mark.parametrize("sizes,M,N", [([128, 256, 0, 384], 256, 512),
-                                         ([128, 128, 0, 512, 256, 128, 384, 128], 1024, 2048)])
+                                         ([128, 128, 0, 512, 256, 128, 384, 128], 1024, 2048),
+                                         ([128, 0, 256], 256, 512),
+                                         ([256, 128, 0], 128, 512)])
 def test_mxfp8_wgrad_fused_sgd_equals_gemm_then_sgd(sizes, M, N):
     """The fused weight-gradient + SGD epilogue is bit-identical to the unfused pair, and its
-    per-expert amax equals max |bf16 copy|.  The second case has 512 output tiles, several per
-    CTA, so each CTA's epilogue also prefetches the master weights of its next tile."""
+    per-expert amax equals max |bf16 copy|.  The second case has 1024 output tiles, several per
+    CTA, so each CTA's epilogue also prefetches the master weights of its next tile.  The grid is
+    one CTA per tile up to one per SM, so the tile schedule takes both forms an even grid can
+    take: every third slot on the front of the size-sorted list (grids of 32 and 148 CTAs) and
+    alternating (24 and 12 CTAs, multiples of 3).  Tile counts are even (N is a multiple of 256),
+    so the list-in-order form, for odd multiples of 3, needs an odd SM count."""
     rng = np.random.default_rng(23)
     E = len(sizes)
     offs = _offs(sizes)
