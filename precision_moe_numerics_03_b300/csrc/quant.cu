@@ -242,9 +242,10 @@ __device__ __forceinline__ void raw_words(const RawBlock<TIn> &r, uint32_t w[8])
 // amax per matrix from amax_in (given) or amax_bits (pass 1).  The block index b runs over all
 // matrices; with contiguous rows (ld == cols) the input, code and canonical-scale offsets are
 // b*16, b*8 and b, and the matrix index only moves forward in the loop, so no division is needed
-// on that path.  At most 80 registers: two CTAs of it and two of the requantiser share an SM.
+// on that path.  At most 72 registers: two CTAs of it (72 x 256 registers each) and two of the
+// requantiser on 128-column tiles (56 x 256) fill an SM's register file in the weight path.
 template <typename TIn>
-__global__ void __maxnreg__(80) nvfp4_quant_kernel(
+__global__ void __maxnreg__(72) nvfp4_quant_kernel(
     const TIn *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,

@@ -7,7 +7,9 @@
 // with probability given by the distance so that the value is kept on average.
 //
 // Tile: 128 input rows (the output's contiguous dimension) x 64 input columns (128 for the
-// two-layout quantisers of bf16 sources).  Phase 1: each thread reads one row's 32 values (16 code
+// two-layout quantisers of bf16 sources, and for the stochastic rounding of NVFP4 sources whose
+// column count is a multiple of 128: twice the work per barrier and per scale-range reduction).
+// Phase 1: each thread reads one row's 32 values (16 code
 // bytes and two scale bytes, or 64 bytes of bf16; two such groups on a 128-column tile) and
 // stores them as 16 column pairs, one 32-bit word each, in the transposed shared tile.  Phase 2:
 // each warp emits two output rows (one column pair) of 128 values: lane l owns 4 consecutive
@@ -164,8 +166,8 @@ requant_transpose_kernel(
     const int32_t *__restrict__ row_of = nullptr, const float *__restrict__ wts = nullptr, int topk = 0,
     bool e8_mma = false, const int32_t *__restrict__ skip_offs = nullptr, int64_t m_base = 0) {
     constexpr bool kSwb = kind == SrcKind::SwigluBwd;
-    static_assert(TC == 64 || (TC == 128 && (kind == SrcKind::Bf16 || kind == SrcKind::CombineBwd)),
-                  "128-column tiles: bf16 and combine-gradient sources only");
+    static_assert(TC == 64 || (TC == 128 && kind != SrcKind::SwigluBwd),
+                  "128-column tiles: NVFP4, bf16 and combine-gradient sources");
     // expert weights: a matrix whose group has no rows (skip_offs[m + 1] == skip_offs[m]) is
     // skipped whole, its outputs left as they are
     if (skip_offs != nullptr && __ldg(skip_offs + blockIdx.z + 1) == __ldg(skip_offs + blockIdx.z)) return;
@@ -190,6 +192,54 @@ requant_transpose_kernel(
         const int rl = threadIdx.x & (kTileR - 1);
         const int half = threadIdx.x >> 7;
         const int64_t r = r0 + rl;
+        if constexpr (kind == SrcKind::Nvfp4) {
+            // both groups' code words and scale pairs are loaded before either is used
+            const int64_t nblk = C / 16;
+            uint4 wq[2];
+            uint16_t sq[2];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int64_t c = c0 + 32 * half + 64 * g, b = c / 16;
+                const bool ld = r < R && c < C;
+                const int64_t soff = sf_mma ? m * R * nblk + ((r >> 7) * (nblk >> 2) + (b >> 2)) * 512 +
+                                                  (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3)
+                                            : (m * R + r) * nblk + b;
+                wq[g] = ld ? __ldg(reinterpret_cast<const uint4 *>(codes + ((m * R + r) * C + c) / 2))
+                           : make_uint4(0, 0, 0, 0);
+                sq[g] = ld ? __ldg(reinterpret_cast<const uint16_t *>(sf + soff)) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int64_t c = c0 + 32 * half + 64 * g;
+                uint32_t h[16];
+                if (r < R && c < C) {
+                    const uint32_t sf2 = e4m3x2_to_h2(sq[g]);
+                    const uint32_t sfa2 = __byte_perm(sf2, 0, 0x1010), sfb2 = __byte_perm(sf2, 0, 0x3232);
+                    if constexpr (kScaleRange) {
+                        const uint32_t sa = sf2 & 0xFFFFu, sb = sf2 >> 16;
+                        sf_lo = min(sf_lo, min(sa ? sa : 0x7C00u, sb ? sb : 0x7C00u));
+                        sf_hi = max(sf_hi, max(sa, sb));
+                    }
+                    const uint32_t words[4] = {wq[g].x, wq[g].y, wq[g].z, wq[g].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __half2 sfh = *reinterpret_cast<const __half2 *>(q < 2 ? &sfa2 : &sfb2);
+                        uint32_t e2[4];
+                        e2m1x8_to_h2x4(words[q], e2);
+#pragma unroll
+                        for (int b2 = 0; b2 < 4; ++b2) {
+                            const __half2 es = __hmul2(*reinterpret_cast<const __half2 *>(&e2[b2]), sfh);
+                            h[4 * q + b2] = *reinterpret_cast<const uint32_t *>(&es);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) h[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tile[16 * half + 32 * g + i][rl] = h[i];
+            }
+        } else {
         int32_t tok = 0;
         float wj = 0.0f;
         if constexpr (kind == SrcKind::CombineBwd) {
@@ -251,6 +301,7 @@ requant_transpose_kernel(
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) tile[16 * half + 32 * g + i][rl] = h[i];
+        }
         }
     } else {
         const int rl = threadIdx.x & (kTileR - 1);
@@ -376,13 +427,13 @@ requant_transpose_kernel(
 #pragma unroll
             for (int i = 0; i < 16; ++i) tile[half * 16 + i][rl] = h[i];
         }
-        if constexpr (kScaleRange) {
-            sf_lo = __reduce_min_sync(0xFFFFFFFFu, sf_lo);
-            sf_hi = __reduce_max_sync(0xFFFFFFFFu, sf_hi);
-            if (lane_id() == 0) {
-                sf_red[0][warp_id()] = sf_lo;
-                sf_red[1][warp_id()] = sf_hi;
-            }
+    }
+    if constexpr (kScaleRange) {
+        sf_lo = __reduce_min_sync(0xFFFFFFFFu, sf_lo);
+        sf_hi = __reduce_max_sync(0xFFFFFFFFu, sf_hi);
+        if (lane_id() == 0) {
+            sf_red[0][warp_id()] = sf_lo;
+            sf_red[1][warp_id()] = sf_hi;
         }
     }
     __syncthreads();
@@ -522,7 +573,11 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
 #define MOE4_REQUANT_ARGS                                                                                        \
     codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, sf_mma, nullptr, nullptr, nullptr, \
         nullptr, nullptr, nullptr, nullptr, 0, e8_mma
-    if ((flags & MOE4_SR) && j32)
+    if ((flags & MOE4_SR) && j32 && cols % 128 == 0) {
+        dim3 g128 = grid;  // 128-column tiles: half the column tiles
+        g128.y = (unsigned)(cols / 128);
+        requant_transpose_kernel<SrcKind::Nvfp4, true, false, true, 128><<<g128, 256, 0, st>>>(MOE4_REQUANT_ARGS);
+    } else if ((flags & MOE4_SR) && j32)
         requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_REQUANT_ARGS);
     else if (flags & MOE4_SR)
         requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, st>>>(MOE4_REQUANT_ARGS);
@@ -532,8 +587,8 @@ extern "C" int mxfp8_requant_transpose_sr(const uint8_t *codes, const uint8_t *s
     return launch_status();
 }
 
-// MOE4_SHARE_SMS: quantiser CTAs per SM (62 registers x 256 threads each), leaving the rest of the
-// register file to requantiser CTAs (48 x 256) launched beside it
+// MOE4_SHARE_SMS: quantiser CTAs per SM (72 registers x 256 threads each), leaving the rest of the
+// register file to two requantiser CTAs (56 x 256 on 128-column tiles) launched beside it
 constexpr int kShareCtasPerSm = 2;
 
 extern "C" int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t rows, int64_t cols,
@@ -571,7 +626,11 @@ extern "C" int nvfp4_quantize_f32_requant(const float *x, int64_t nmat, int64_t 
 #define MOE4_WEIGHT_ARGS                                                                                          \
     codes, sf, g_dec, nullptr, nmat, rows, cols, q_t, e8_t, keys, stream_id, sf_mma, nullptr, nullptr, nullptr, \
         nullptr, nullptr, nullptr, nullptr, 0, e8_mma, group_offs, mat_base
-    if ((flags & MOE4_SR) && j32)
+    if ((flags & MOE4_SR) && j32 && cols % 128 == 0) {
+        dim3 g128 = grid;  // 128-column tiles: half the column tiles
+        g128.y = (unsigned)(cols / 128);
+        requant_transpose_kernel<SrcKind::Nvfp4, true, false, true, 128><<<g128, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
+    } else if ((flags & MOE4_SR) && j32)
         requant_transpose_kernel<SrcKind::Nvfp4, true><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
     else if (flags & MOE4_SR)
         requant_transpose_kernel<SrcKind::Nvfp4, true, false, false><<<grid, 256, 0, st>>>(MOE4_WEIGHT_ARGS);
