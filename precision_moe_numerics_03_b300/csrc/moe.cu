@@ -284,6 +284,9 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t *__rest
 
 // ------------------------------------------------------------------ combine
 // One thread per 8 output columns of one token; slots in order, one RN product and one RN add.
+// KC > 0: k == KC, known when compiled, so every slot's row is loaded before the first is added
+// (the sum runs in slot order either way); KC == 0: any k.
+template <int KC>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ yhat, const int32_t *__restrict__ row_of,
                                                       const float *__restrict__ w, int64_t T, int k, int64_t d,
                                                       uint16_t *__restrict__ y) {
@@ -293,7 +296,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     for (int64_t ci = threadIdx.x; ci < per_tok; ci += blockDim.x) {
         const int64_t c = ci * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
+        if constexpr (KC > 0) {
+            uint4 q[KC];
+            float wk[KC];
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                const int64_t row = row_of[t * KC + j];
+                wk[j] = w != nullptr ? w[t * KC + j] : 1.0f;
+                q[j] = __ldg(reinterpret_cast<const uint4 *>(yhat + row * d + c));
+            }
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                const uint32_t ws[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wk[j], bf16_lo(ws[i])));
+                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wk[j], bf16_hi(ws[i])));
+                }
+            }
+        }
+        for (int j = 0; KC == 0 && j < k; ++j) {
             const int64_t row = row_of[t * k + j];
             // without weights (the dispatch's gradient) each slot's value is added as it is: the
             // product by 1 is exact
@@ -437,7 +459,10 @@ extern "C" int moe4_combine(const uint16_t *yhat, const int32_t *row_of, const f
     MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 8 == 0);
     MOE4_CHECK_ARG(T == 0 || (yhat && row_of && w && y && aligned16(yhat) && aligned16(y)));
     if (T == 0) return MOE4_OK;
-    combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
+    if (k == 8)
+        combine_kernel<8><<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
+    else
+        combine_kernel<0><<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(yhat, row_of, w, T, (int)k, d, y);
     return launch_status();
 }
 
@@ -446,7 +471,10 @@ extern "C" int moe4_dispatch_backward(const uint16_t *dxp, const int32_t *row_of
     MOE4_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && d > 0 && d % 8 == 0);
     MOE4_CHECK_ARG(T == 0 || (dxp && row_of && dx && aligned16(dxp) && aligned16(dx)));
     if (T == 0) return MOE4_OK;
-    combine_kernel<<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(dxp, row_of, nullptr, T, (int)k, d, dx);
+    if (k == 8)
+        combine_kernel<8><<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(dxp, row_of, nullptr, T, (int)k, d, dx);
+    else
+        combine_kernel<0><<<grid_cap(T * 256, 256, 8), 256, 0, as_stream(stream)>>>(dxp, row_of, nullptr, T, (int)k, d, dx);
     return launch_status();
 }
 
