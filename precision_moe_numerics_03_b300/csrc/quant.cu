@@ -237,19 +237,17 @@ __device__ __forceinline__ void raw_words(const RawBlock<TIn> &r, uint32_t w[8])
     }
 }
 
-// One thread per 16-value block, two blocks (b and b + stride of the grid-stride loop) per
-// iteration: both blocks' loads are issued first, so each warp has twice the bytes in flight.
-// amax per matrix from amax_in (given) or amax_bits (pass 1).  The block index b runs over all
-// matrices; with contiguous rows (ld == cols) the input, code and canonical-scale offsets are
-// b*16, b*8 and b, and the matrix index only moves forward in the loop, so no division is needed
-// on that path.  At most 72 registers: two CTAs of it (72 x 256 registers each) and two of the
-// requantiser on 128-column tiles (56 x 256) fill an SM's register file in the weight path.
-template <typename TIn>
-__global__ void __maxnreg__(72) nvfp4_quant_kernel(
+// One thread per 16-value block.  amax per matrix from amax_in (given) or amax_bits (pass 1).  The
+// block index b runs over all matrices; with contiguous rows (ld == cols) the input, code and
+// canonical-scale offsets are b*16, b*8 and b, and the matrix index only moves forward in the
+// grid-stride loop, so no division is needed on that path.  kTwo: two blocks (b and b + stride)
+// per iteration, both blocks' loads issued first, so each warp has twice the bytes in flight.
+template <typename TIn, bool kTwo>
+__device__ __forceinline__ void nvfp4_quant_blocks(
     const TIn *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld,
     int64_t mat_stride, const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits,
     bool four_over_six, bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
-    float *__restrict__ g_dec, uint32_t div_m, uint32_t div_s, const int32_t *__restrict__ skip_offs = nullptr) {
+    float *__restrict__ g_dec, uint32_t div_m, uint32_t div_s, const int32_t *__restrict__ skip_offs) {
     __shared__ float2 tab[128];
     fill_scale_tab(tab);
     const int64_t nblk = cols / 16;
@@ -316,6 +314,20 @@ __global__ void __maxnreg__(72) nvfp4_quant_kernel(
     };
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     Mat s{-1, 0, 0, 1.0f, false};
+    if constexpr (!kTwo) {
+        for (int64_t b = gtid; b < total; b += stride) {
+            enter(s, b);
+            if (s.skip) continue;
+            int64_t r1, k1;
+            locate(s, b, r1, k1);
+            RawBlock<TIn> ra;
+            raw_load(ra, source(s, b, r1, k1), true);
+            uint32_t wa[8];
+            raw_words(ra, wa);
+            quantise(s, b, r1, k1, wa);
+        }
+        return;
+    }
     for (int64_t b = gtid; b < total; b += 2 * stride) {
         const int64_t b2 = b + stride;
         enter(s, b);
@@ -337,6 +349,28 @@ __global__ void __maxnreg__(72) nvfp4_quant_kernel(
         s = s2;  // the next b lies past b2: its matrix is found from b2's
     }
 }
+
+#define MOE4_QUANT_PARAMS                                                                                         \
+    const TIn *__restrict__ x, int64_t nmat, int64_t rows, int64_t cols, int64_t ld, int64_t mat_stride,          \
+        const float *__restrict__ amax_in, const unsigned int *__restrict__ amax_bits, bool four_over_six,       \
+        bool sf_mma, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf, float *__restrict__ g_dec,           \
+        uint32_t div_m, uint32_t div_s, const int32_t *__restrict__ skip_offs = nullptr
+#define MOE4_QUANT_ARGS \
+    x, nmat, rows, cols, ld, mat_stride, amax_in, amax_bits, four_over_six, sf_mma, codes, sf, g_dec, div_m, div_s, skip_offs
+// One block per iteration, at up to four CTAs per SM: the quantiser running alone on the GPU.
+template <typename TIn>
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(MOE4_QUANT_PARAMS) {
+    nvfp4_quant_blocks<TIn, false>(MOE4_QUANT_ARGS);
+}
+// Two blocks per iteration and at most 72 registers: two CTAs of it (72 x 256 registers each) and
+// two of the requantiser on 128-column tiles (56 x 256) fill an SM's register file, as the weight
+// path runs them side by side.
+template <typename TIn>
+__global__ void __maxnreg__(72) nvfp4_quant_pair_kernel(MOE4_QUANT_PARAMS) {
+    nvfp4_quant_blocks<TIn, true>(MOE4_QUANT_ARGS);
+}
+#undef MOE4_QUANT_PARAMS
+#undef MOE4_QUANT_ARGS
 
 // ------------------------------------------------------------------ dequantise
 __global__ void __launch_bounds__(256) nvfp4_dequant_kernel(
@@ -645,8 +679,14 @@ int quantize_f32_given(const float *x, int64_t nmat, int64_t rows, int64_t cols,
     const int grid = grid_for(total > nmat ? total : nmat, 256, ctas_per_sm);
     uint32_t div_m = 0, div_s = 0;
     if (sf_mma) div_magic((uint32_t)(cols / 64), div_m, div_s);
-    nvfp4_quant_kernel<float><<<grid, 256, 0, st>>>(x, nmat, rows, cols, cols, rows * cols, amax_in, nullptr,
-                                                    four_over_six, sf_mma, codes, sf, g_dec, div_m, div_s, skip_offs);
+    // fewer than eight CTAs per SM: the SMs are shared with the requantiser (MOE4_SHARE_SMS)
+    if (ctas_per_sm < 8)
+        nvfp4_quant_pair_kernel<float><<<grid, 256, 0, st>>>(x, nmat, rows, cols, cols, rows * cols, amax_in, nullptr,
+                                                             four_over_six, sf_mma, codes, sf, g_dec, div_m, div_s,
+                                                             skip_offs);
+    else
+        nvfp4_quant_kernel<float><<<grid, 256, 0, st>>>(x, nmat, rows, cols, cols, rows * cols, amax_in, nullptr,
+                                                        four_over_six, sf_mma, codes, sf, g_dec, div_m, div_s, skip_offs);
     return launch_status();
 }
 
