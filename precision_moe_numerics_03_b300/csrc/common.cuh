@@ -30,7 +30,8 @@ int num_sms();
 // The NVFP4 quantiser of binary32 matrices with a given per-matrix amax (quant.cu), skipping the
 // matrices m with skip_offs[m + 1] == skip_offs[m] when skip_offs is not null.  Arguments checked
 // by the caller.  ctas_per_sm bounds its grid-stride grid (8 fills the GPU; fewer leaves room on
-// every SM for a kernel running beside it on another stream).
+// every SM for a kernel running beside it on another stream, and then selects the quantiser form
+// that takes two blocks per iteration within 72 registers).
 int quantize_f32_given(const float *x, int64_t nmat, int64_t rows, int64_t cols, const float *amax_in,
                        uint8_t *codes, uint8_t *sf, float *g_dec, const int32_t *skip_offs, bool four_over_six,
                        bool sf_mma, cudaStream_t st, int ctas_per_sm = 8);
